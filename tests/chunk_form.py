@@ -1,0 +1,69 @@
+"""Float64 NumPy statement of the gated chunk form, used only to check its derivation.
+
+The CUDA prefill kernels compute the recurrence chunk by chunk. The pages print
+the chunk algorithm only without decay ("Attention as Matrix Algebra: From
+Softmax to the Delta Rule", section 8 "Training the delta rule in chunks":
+(I + L) U = diag(beta) (V - K S), O = Q S + (Q K^T . L_C) U, S <- S + K^T U) and
+derive the chunk update for two tokens ("From KV Cache to a State Matrix",
+section "Chunkwise training for DeltaNet"). With the decay gate the same
+substitution gives, per chunk of C tokens entering with state S,
+
+    g_t = sum_{i<=t} log alpha_i (inside the chunk),  gamma_t = exp(g_t),
+    Gamma_ti = exp(g_t - g_i) for i <= t,
+    L_ti = beta_t Gamma_ti k_t^T k_i  (i < t),  T = (I + L)^{-1} diag(beta),
+    U = T V - T diag(gamma) K S,
+    O = diag(gamma) Q S + (Q K^T . Gamma . [i <= t]) U,
+    S <- gamma_C S + Ktilde^T U,  Ktilde_i = exp(g_C - g_i) k_i,
+
+and the product of the chunk's transitions alpha_t (I - beta_t k_t k_t^T) is
+gamma_C I - Ktilde^T T diag(gamma) K.
+
+Tests compare this module with the token-by-token oracle; that pins the
+derivation the kernels rely on. Nothing here is used by the CUDA path, and the
+oracle does not use this module either.
+"""
+import numpy as np
+from scipy.linalg import solve_triangular
+
+
+def chunk_step(S, q, k, v, log_alpha, beta):
+    """One chunk for one head. q, k [C, dk]; v [C, dv]; log_alpha, beta [C]; S [dk, dv]."""
+    C = len(k)
+    g = np.cumsum(log_alpha)
+    gamma = np.exp(g)
+    diff = g[:, None] - g[None, :]
+    lower_incl = np.tril(np.ones((C, C), dtype=bool))
+    Gamma = np.where(lower_incl, np.exp(np.where(lower_incl, diff, 0.0)), 0.0)
+    L = np.tril(beta[:, None] * Gamma * (k @ k.T), -1)
+    T = solve_triangular(np.eye(C) + L, np.diag(beta), lower=True)
+    U = T @ v - T @ (gamma[:, None] * k) @ S
+    O = gamma[:, None] * (q @ S) + ((q @ k.T) * Gamma) @ U
+    k_tilde = np.exp(g[-1] - g)[:, None] * k
+    S_next = gamma[-1] * S + k_tilde.T @ U
+    return O, S_next
+
+
+def chunked_forward(q, k, v, log_alpha, beta, C, S0=None):
+    """Whole sequence for one head, chunk by chunk. Returns (O [T, dv], S [dk, dv])."""
+    T_len, dk = k.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    out = np.empty((T_len, dv))
+    for c in range(0, T_len, C):
+        sl = slice(c, c + C)
+        out[sl], S = chunk_step(S, q[sl], k[sl], v[sl], log_alpha[sl], beta[sl])
+    return out, S
+
+
+def chunk_transition(k, log_alpha, beta):
+    """gamma_C I - Ktilde^T T diag(gamma) K for one chunk (the WY form of its transitions)."""
+    C, dk = k.shape
+    g = np.cumsum(log_alpha)
+    gamma = np.exp(g)
+    diff = g[:, None] - g[None, :]
+    lower = np.tril(np.ones((C, C), dtype=bool), -1)
+    Gamma = np.where(lower, np.exp(np.where(lower, diff, 0.0)), 0.0)
+    L = beta[:, None] * Gamma * (k @ k.T)
+    T = solve_triangular(np.eye(C) + L, np.diag(beta), lower=True)
+    k_tilde = np.exp(g[-1] - g)[:, None] * k
+    return gamma[-1] * np.eye(dk) - k_tilde.T @ T @ (gamma[:, None] * k)
