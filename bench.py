@@ -1,0 +1,414 @@
+"""Benchmark of the gated delta rule hot path on GB300.
+
+One step is one gdr_chunk_fwd call (chunked prefill) over the B=4, H=16,
+T=4096, d_k=d_v=128 bf16 workload, with inputs resident in HBM. The decode row
+of the hot path (gdr_decode_step over 256 sequences x 32 heads, fp32 state of
+537 MB) is timed in the same run and reported under "decode".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdr|reference]
+
+Prints ONE JSON line on rank 0. Under torchrun (N > 1) every rank runs an
+independent replica of the workload (the path needs no collective); the time
+is the max over ranks and `value` counts the tokens of all ranks.
+`--impl reference` times the float64 CPU oracle (the reference arm) instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from gated_delta_rule_03_gb300 import inputs  # noqa: E402
+
+METRIC = "GDN prefill tokens/s (H=16,d=128,bf16); decode state GB/s vs HBM peak"
+PREFILL_WORKLOAD = "prefill_bf16"
+DECODE_WORKLOAD = "decode_bf16"
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def prefill_bytes(inp):
+    """Algorithmic HBM bytes of one prefill call: read q, k, v and the gates, write o,
+    write S_final (and read S0 when given)."""
+    esz = 2 if inp.dtype == "bf16" else 4
+    per_token_head = (2 * inp.dk + 2 * inp.dv) * esz + 8
+    state = inp.num_seqs * inp.H * inp.dk * inp.dv * 4
+    return inp.total_tokens * inp.H * per_token_head + state * (2 if inp.S0 is not None else 1)
+
+
+def decode_bytes(N, H, dk, dv, esz=2):
+    """Algorithmic HBM bytes of one decode step: the fp32 state read and written once,
+    plus q, k, v, o and the two gates."""
+    return N * H * (2 * dk * dv * 4 + (2 * dk + 2 * dv) * esz + 8)
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from an ncu capture summarised in profiles/traffic.txt, valid
+    only while the kernel's CUDA sources are unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src_sha = sources_sha()
+    with open(path) as f:
+        for line in f:
+            fields = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+            if (fields.get("kernel") == kernel and fields.get("workload") == workload
+                    and fields.get("source_sha") == src_sha):
+                return float(fields["dram_bytes_per_launch"])
+    return None
+
+
+def sources_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_delta_rule_03_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples taken while the GPU works."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        self.index = vis.split(",")[local_rank] if vis else str(local_rank)
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", self.index, "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        sm, reasons, smax = [], set(), None
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_calls(fn, steps, stream, world, device, per_call=True):
+    """Run fn() `steps` times on `stream` between a barrier and a synchronize on both
+    sides; return (total ms max over ranks, mean per-call ms from per-call events)."""
+    barrier(world)
+    torch.cuda.synchronize(device)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(steps)] if per_call else []
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            if per_call:
+                pairs[i][0].record(stream)
+            fn()
+            if per_call:
+                pairs[i][1].record(stream)
+        end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    total = max_over_ranks(start.elapsed_time(end), world, device)
+    mean_call = (sum(a.elapsed_time(b) for a, b in pairs) / steps) if per_call else None
+    return total, mean_call
+
+
+# ----------------------------------------------------------------------------- arms
+
+def oracle_prefill_sample(inp):
+    """Float64 views of the workload for the oracle, prepared outside any timing."""
+    f = lambda t: t.to(torch.float64).numpy()
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy().astype(np.int64)
+    return dict(q=f(inp.q), k=f(inp.k), v=f(inp.v), log_alpha=f(inp.log_alpha),
+                beta=f(inp.beta), S0=None if inp.S0 is None else f(inp.S0), cu_seqlens=cu,
+                num_seqs=inp.num_seqs)
+
+
+def cpu_baseline(inp, seconds):
+    """The oracle, as it stands, on this host's cores: repeat the full workload until
+    `seconds` have passed (at least once)."""
+    import oracle
+    args = oracle_prefill_sample(inp)
+    threads = oracle.default_threads()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.forward(**args, threads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 1000:
+            break
+    tokens = inp.total_tokens * reps
+    return {"value": tokens / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"full {PREFILL_WORKLOAD} workload ({inp.num_seqs}x{inp.seq_lens[0]} "
+                      f"tokens, H={inp.H}, d_k={inp.dk}, d_v={inp.dv}) x {reps} repetitions, "
+                      f"{el:.1f} s, float64 token loop"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    inp = inputs.workload_prefill(PREFILL_WORKLOAD)
+    sample = oracle_prefill_sample(inp)
+    threads = oracle.default_threads()
+    for _ in range(args.warmup):
+        oracle.forward(**sample, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward(**sample, threads=threads)
+    el = time.perf_counter() - t0
+    value = inp.total_tokens * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(inp),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: the full {PREFILL_WORKLOAD} workload, "
+                                   f"float64 token loop on {threads} host threads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(inp):
+    return {"workload": f"{PREFILL_WORKLOAD}: B={inp.num_seqs} H={inp.H} T={inp.seq_lens[0]} "
+                        f"d_k={inp.dk} d_v={inp.dv} chunk={inp.chunk} bf16 q/k/v/o, fp32 "
+                        f"gates and state, S0=0",
+            "global_batch": inp.num_seqs, "seq_len": inp.seq_lens[0], "heads": inp.H,
+            "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"}
+
+
+def run_gdr(args):
+    from gated_delta_rule_03_gb300 import chunk_fwd, chunk_fwd_workspace_size, decode_step, ops
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    peaks = load_peaks()
+
+    inp = inputs.workload_prefill(PREFILL_WORKLOAD)
+    d = lambda t: None if t is None else t.to(device)
+    q, k, v, la, b = d(inp.q), d(inp.k), d(inp.v), d(inp.log_alpha), d(inp.beta)
+    S0, cu = d(inp.S0), d(inp.cu_seqlens)
+    o = torch.empty((inp.total_tokens, inp.H, inp.dv), dtype=q.dtype, device=device)
+    S = torch.empty((inp.num_seqs, inp.H, inp.dk, inp.dv), dtype=torch.float32, device=device)
+    ws = torch.empty(chunk_fwd_workspace_size(inp.num_seqs, inp.total_tokens, inp.H, inp.dk,
+                                              inp.dv, inp.chunk, q.dtype),
+                     dtype=torch.uint8, device=device)
+
+    def step():
+        chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, num_seqs=inp.num_seqs, chunk=inp.chunk,
+                  o=o, S_final=S, workspace=ws, stream=stream)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    total_ms, call_ms = timed_calls(step, args.steps, stream, world, device)
+    clock_info = clocks.stop()
+
+    tokens = inp.total_tokens
+    value = world * tokens * args.steps / (total_ms / 1e3)
+    kernel_launches = ops.chunk_fwd_kernel_launches(inp.dk, inp.dv, q.dtype)
+    main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype)
+    bytes_call = prefill_bytes(inp)
+    achieved = bytes_call / (call_ms / 1e3) / 1e9
+    traffic = recorded_traffic(main_kernel, PREFILL_WORKLOAD)
+
+    # end to end through the public API: pinned host inputs in, results back out
+    pin = lambda t: None if t is None else t.pin_memory()
+    qh, kh, vh, lah, bh = pin(inp.q), pin(inp.k), pin(inp.v), pin(inp.log_alpha), pin(inp.beta)
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    Sh = torch.empty(S.shape, dtype=S.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, lah, bh))
+    d2h = oh.numel() * oh.element_size() + Sh.numel() * Sh.element_size()
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        la.copy_(lah, non_blocking=True)
+        b.copy_(bh, non_blocking=True)
+        step()
+        oh.copy_(o, non_blocking=True)
+        Sh.copy_(S, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(min(args.warmup, 3)):
+            e2e_step()
+    e2e_ms, _ = timed_calls(e2e_step, args.steps, stream, world, device, per_call=False)
+    e2e_value = world * tokens * args.steps / (e2e_ms / 1e3)
+
+    decode = None
+    if not args.no_decode:
+        decode = run_decode(args, decode_step, device, stream, world, peaks)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": ops.chunk_fwd_compute_dtype(inp.dk, inp.dv, q.dtype), "data": "synthetic",
+        "config": workload_config(inp),
+        "roofline": {"kernel": main_kernel, "bound": "hbm", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": bytes_call,
+                     "launch_ms": call_ms, "peak_source": peaks["source"],
+                     "timing": "CUDA events around each gdr_chunk_fwd call on its stream"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": kernel_launches * args.steps,
+        "clocks": clock_info,
+        "decode": decode,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_decode(args, decode_step, device, stream, world, peaks):
+    w = inputs.WORKLOADS[DECODE_WORKLOAD]
+    dec = inputs.workload_decode(DECODE_WORKLOAD)
+    S = dec.S.to(device)
+    qs, ks, vs = dec.q.to(device), dec.k.to(device), dec.v.to(device)
+    las, bs = dec.log_alpha.to(device), dec.beta.to(device)
+    o = torch.empty((dec.N, dec.H, dec.dv), dtype=qs.dtype, device=device)
+    it = [0]
+
+    def step():
+        s = it[0] % dec.steps
+        decode_step(qs[s], ks[s], vs[s], las[s], bs[s], S, o=o, stream=stream)
+        it[0] += 1
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    calls = max(dec.steps, args.steps)
+    total_ms, call_ms = timed_calls(step, calls, stream, world, device)
+    nbytes = decode_bytes(dec.N, dec.H, dec.dk, dec.dv)
+    state_bytes = 2 * dec.N * dec.H * dec.dk * dec.dv * 4
+    achieved = nbytes / (call_ms / 1e3) / 1e9
+    return {"workload": f"{DECODE_WORKLOAD}: N={w['N']} H={w['H']} d_k={w['dk']} d_v={w['dv']}, "
+                        f"{dec.steps} distinct steps cycled, fp32 state "
+                        f"{state_bytes // 2 / 1e6:.0f} MB",
+            "calls": calls, "ms_per_step": total_ms / calls,
+            "state_gbs": world * state_bytes * calls / (total_ms / 1e3) / 1e9,
+            "roofline": {"kernel": "decode_step_kernel", "bound": "hbm", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("decode_step_kernel", DECODE_WORKLOAD),
+                         "algorithmic_bytes_per_launch": nbytes, "launch_ms": call_ms},
+            "gpu_launches": calls}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gdr", "reference"], default="gdr")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gdr(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,172 @@
+// gdr_api.cu -- the C ABI of libgdr: argument validation, workspace layout, dispatch.
+//
+// Every check that can be made without touching the device is made here, before
+// anything is enqueued; a rejected call writes nothing. Checks that need device
+// memory (cu_seqlens) are made by the kernels, which report through the status
+// word at the start of the workspace.
+#include <string.h>
+
+#include "internal.h"
+
+namespace gdr {
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool use_tensor_path(int dk, int dv, int dtype) {
+    (void)dk; (void)dv; (void)dtype;
+    return false;
+}
+
+WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype) {
+    WsLayout L;
+    memset(&L, 0, sizeof(L));
+    L.tensor_path = use_tensor_path(dk, dv, dtype);
+    L.max_chunks = total_tokens / kChunk + num_seqs;
+    size_t off = 0;
+    L.ctl = off;
+    off += 256;
+    L.plan = off;
+    off = align_up(off + sizeof(int4) * (size_t)L.max_chunks, 256);
+    L.seq_chunk = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)(num_seqs + 1), 256);
+    if (!L.tensor_path) {
+        const size_t per = (size_t)L.max_chunks * (size_t)H * kChunk;
+        L.W = off;
+        off = align_up(off + sizeof(float) * per * dk, 256);
+        L.U = off;
+        off = align_up(off + sizeof(float) * per * dv, 256);
+        L.A = off;
+        off = align_up(off + sizeof(float) * per * kChunk, 256);
+        L.g = off;
+        off = align_up(off + sizeof(float) * per, 256);
+    }
+    L.total = off;
+    return L;
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+static bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
+
+static int check_prefill_sizes(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv,
+                               int chunk, int dtype) {
+    if (num_seqs < 1 || total_tokens < 0 || H < 1) return GDR_ERR_INVALID_ARG;
+    if (total_tokens > INT32_MAX || num_seqs > INT32_MAX / 2) return GDR_ERR_INVALID_ARG;
+    if (dtype != GDR_F32 && dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
+    if (dk != 64 && dk != 128) return GDR_ERR_UNSUPPORTED;
+    if (dv < 32 || dv > 256 || dv % 32 != 0) return GDR_ERR_UNSUPPORTED;
+    if (chunk != kChunk) return GDR_ERR_UNSUPPORTED;
+    // grid limits: (num_seqs * H) blocks in x
+    if ((int64_t)H * num_seqs > INT32_MAX / 4) return GDR_ERR_INVALID_ARG;
+    if ((int64_t)H * (total_tokens / kChunk + num_seqs) > INT32_MAX / 4) return GDR_ERR_INVALID_ARG;
+    return GDR_OK;
+}
+
+static bool overlaps(const void *a, size_t an, const void *b, size_t bn) {
+    const char *pa = (const char *)a, *pb = (const char *)b;
+    return pa < pb + bn && pb < pa + an;
+}
+
+}  // namespace gdr
+
+using namespace gdr;
+
+extern "C" {
+
+const char *gdr_status_string(int status) {
+    switch (status) {
+        case GDR_OK: return "GDR_OK";
+        case GDR_ERR_INVALID_ARG: return "GDR_ERR_INVALID_ARG: null pointer or invalid size";
+        case GDR_ERR_UNSUPPORTED: return "GDR_ERR_UNSUPPORTED: dtype, d_k, d_v or chunk not supported";
+        case GDR_ERR_ALIGNMENT: return "GDR_ERR_ALIGNMENT: pointer not aligned as required";
+        case GDR_ERR_WORKSPACE: return "GDR_ERR_WORKSPACE: workspace missing or too small";
+        case GDR_ERR_CUDA: return "GDR_ERR_CUDA: CUDA call or kernel launch failed";
+        case GDR_ERR_DEVICE_TIMEOUT: return "GDR_ERR_DEVICE_TIMEOUT: a device-side wait gave up";
+        case GDR_ERR_BAD_SEQLENS: return "GDR_ERR_BAD_SEQLENS: cu_seqlens not 0..total_tokens non-decreasing";
+        default: return "GDR_ERR_UNKNOWN";
+    }
+}
+
+size_t gdr_chunk_fwd_workspace_size(int64_t num_seqs, int64_t total_tokens, int H, int d_k,
+                                    int d_v, int chunk, int dtype) {
+    if (check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype) != GDR_OK) return 0;
+    return ws_layout(num_seqs, total_tokens, H, d_k, d_v, dtype).total;
+}
+
+int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  const float *beta, const float *S0, const int32_t *cu_seqlens,
+                  int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v, int chunk,
+                  int dtype, void *o, float *S_final, void *workspace, size_t workspace_bytes,
+                  gdr_stream_t stream) {
+    int st = check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype);
+    if (st != GDR_OK) return st;
+    if (!cu_seqlens && total_tokens % num_seqs != 0) return GDR_ERR_INVALID_ARG;
+    if (!S_final || !workspace) return workspace ? GDR_ERR_INVALID_ARG : GDR_ERR_WORKSPACE;
+    if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !o))
+        return GDR_ERR_INVALID_ARG;
+    const void *ptrs16[] = {q, k, v, S0, o, S_final, workspace};
+    for (const void *p : ptrs16)
+        if (p && !aligned16(p)) return GDR_ERR_ALIGNMENT;
+    const void *ptrs4[] = {log_alpha, beta, cu_seqlens};
+    for (const void *p : ptrs4)
+        if (p && !aligned4(p)) return GDR_ERR_ALIGNMENT;
+    const WsLayout L = ws_layout(num_seqs, total_tokens, H, d_k, d_v, dtype);
+    if (workspace_bytes < L.total) return GDR_ERR_WORKSPACE;
+    const size_t esz = dtype == GDR_F32 ? 4 : 2;
+    const size_t o_bytes = (size_t)total_tokens * H * d_v * esz;
+    const size_t s_bytes = (size_t)num_seqs * H * d_k * d_v * sizeof(float);
+    if (S0 && S0 != S_final && overlaps(S0, s_bytes, S_final, s_bytes)) return GDR_ERR_INVALID_ARG;
+    if (o && overlaps(o, o_bytes, S_final, s_bytes)) return GDR_ERR_INVALID_ARG;
+    if (overlaps(workspace, L.total, S_final, s_bytes)) return GDR_ERR_INVALID_ARG;
+    if (o && overlaps(workspace, L.total, o, o_bytes)) return GDR_ERR_INVALID_ARG;
+
+    PrefillArgs a;
+    a.q = q; a.k = k; a.v = v;
+    a.log_alpha = log_alpha; a.beta = beta; a.S0 = S0;
+    a.cu_seqlens = cu_seqlens;
+    a.num_seqs = num_seqs; a.total_tokens = total_tokens;
+    a.H = H; a.dk = d_k; a.dv = d_v; a.chunk = chunk; a.dtype = dtype;
+    a.o = o; a.S_final = S_final;
+    a.ws = (char *)workspace;
+    a.stream = (cudaStream_t)stream;
+    st = launch_plan(a, L);
+    if (st != GDR_OK) return st;
+    return launch_prefill_exact(a, L);
+}
+
+int gdr_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
+                    const float *beta, float *S, void *o, int64_t N, int H, int d_k, int d_v,
+                    int dtype, gdr_stream_t stream) {
+    if (N < 0 || H < 1 || N > INT32_MAX || (int64_t)N * H > INT32_MAX) return GDR_ERR_INVALID_ARG;
+    if (dtype != GDR_F32 && dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
+    if ((d_k != 64 && d_k != 128) || (d_v != 64 && d_v != 128 && d_v != 256))
+        return GDR_ERR_UNSUPPORTED;
+    if (N == 0) return GDR_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !S || !o) return GDR_ERR_INVALID_ARG;
+    const void *ptrs16[] = {q, k, v, S, o};
+    for (const void *p : ptrs16)
+        if (!aligned16(p)) return GDR_ERR_ALIGNMENT;
+    if (!aligned4(log_alpha) || !aligned4(beta)) return GDR_ERR_ALIGNMENT;
+    const size_t esz = dtype == GDR_F32 ? 4 : 2;
+    if (overlaps(o, (size_t)N * H * d_v * esz, S, (size_t)N * H * d_k * d_v * sizeof(float)))
+        return GDR_ERR_INVALID_ARG;
+    return launch_decode(q, k, v, log_alpha, beta, S, o, N, H, d_k, d_v, dtype,
+                         (cudaStream_t)stream);
+}
+
+int gdr_chunk_fwd_path(int d_k, int d_v, int dtype) {
+    const int st = check_prefill_sizes(1, 0, 1, d_k, d_v, kChunk, dtype);
+    if (st != GDR_OK) return st;
+    return use_tensor_path(d_k, d_v, dtype) ? GDR_PATH_TENSOR : GDR_PATH_EXACT;
+}
+
+int gdr_read_device_status(const void *workspace, int *status, gdr_stream_t stream) {
+    if (!workspace || !status) return GDR_ERR_INVALID_ARG;
+    int32_t word = 0;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return GDR_ERR_CUDA;
+    *status = word;
+    return GDR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// internal.h -- declarations shared by the translation units of libgdr (not installed).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gdr.h"
+
+namespace gdr {
+
+constexpr int kChunk = 64;  // tokens per chunk (the only chunk size the kernels support)
+
+// Everything gdr_chunk_fwd receives, after host validation.
+struct PrefillArgs {
+    const void *q, *k, *v;
+    const float *log_alpha, *beta, *S0;
+    const int32_t *cu_seqlens;
+    int64_t num_seqs, total_tokens;
+    int H, dk, dv, chunk, dtype;
+    void *o;
+    float *S_final;
+    char *ws;
+    cudaStream_t stream;
+};
+
+// Byte offsets of the workspace regions. The control words come first:
+//   int32 ctl[0] = device status (GDR_OK / GDR_ERR_*), ctl[1] = number of chunks.
+struct WsLayout {
+    int64_t max_chunks;   // upper bound on sum over sequences of ceil(len / chunk)
+    size_t ctl;           // int32[64]
+    size_t plan;          // int4[max_chunks]: (sequence, first token, tokens, chunk index)
+    size_t seq_chunk;     // int32[num_seqs + 1]: first chunk of each sequence
+    size_t W, U, A, g;    // fp32 per-chunk intermediates of the exact path
+    size_t total;
+    bool tensor_path;     // bf16 tensor-core kernel (true) or exact fp32-arithmetic kernels
+};
+
+bool use_tensor_path(int dk, int dv, int dtype);
+WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype);
+
+// Launchers (return GDR_OK or GDR_ERR_CUDA).
+int launch_plan(const PrefillArgs &a, const WsLayout &L);
+int launch_prefill_exact(const PrefillArgs &a, const WsLayout &L);
+int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
+                  const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
+                  int dtype, cudaStream_t stream);
+
+// Type helpers for kernels.
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
+
+}  // namespace gdr

@@ -1,0 +1,424 @@
+// prefill_exact.cu -- chunked prefill in plain fp32 arithmetic (no tensor cores).
+//
+// This is the path for fp32 inputs, whose accuracy target (1e-4 relative) bf16
+// or tf32 tensor-core products cannot meet, and for shapes the tensor-core
+// kernel does not cover. It computes the chunk form of the gated delta rule:
+// the ungated chunk algorithm of "Attention as Matrix Algebra: From Softmax to
+// the Delta Rule", section 8 ("Training the delta rule in chunks"), with the
+// decay gate carried through the same substitution. Per chunk of C tokens,
+// entering with state S:
+//   g_t = sum_{i<=t} log alpha_i,  gamma_t = exp(g_t),  Gamma_ti = exp(g_t - g_i)
+//   L_ti = beta_t Gamma_ti k_t.k_i (i < t),  T = (I + L)^{-1} diag(beta)
+//   W = T diag(gamma) K,  Utilde = T V                  (prep kernel, all chunks at once)
+//   U = Utilde - W S
+//   O = diag(gamma) Q S + (Q K^T . Gamma . [i <= t]) U
+//   S <- gamma_C S + Ktilde^T U,  Ktilde_i = exp(g_C - g_i) k_i   (chain kernel, in order)
+// Only exponents g_t - g_i with i <= t are formed, so every exponent is <= 0.
+// Padding rows of a partial chunk get beta = 0 and log alpha = 0: they change
+// nothing and their outputs are not stored.
+//
+// Kernels, in stream order:
+//   plan   -- validates cu_seqlens, lists the chunks (sequence, first token,
+//             length) and each sequence's first chunk; writes the status word.
+//   prep   -- one CTA per (chunk, head): W, Utilde, the masked A = QK^T . Gamma, g.
+//   chain  -- one CTA per (sequence, head, 32 value columns): walks the chunks
+//             of its sequence in order, carrying its 32 columns of S (the
+//             columns of S evolve independently) in shared memory.
+#include "internal.h"
+
+namespace gdr {
+
+// ----------------------------------------------------------------------------- plan
+
+__global__ void __launch_bounds__(1024)
+plan_kernel(const int32_t *__restrict__ cu, int64_t num_seqs, int64_t total_tokens,
+            int64_t max_chunks, int4 *__restrict__ plan, int32_t *__restrict__ seq_chunk,
+            int32_t *__restrict__ ctl) {
+    __shared__ int s_scan[1024];
+    __shared__ int s_bad;
+    __shared__ int s_carry;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        s_bad = 0;
+        s_carry = 0;
+    }
+    __syncthreads();
+    const int64_t seq_len = cu ? 0 : total_tokens / num_seqs;
+    for (int64_t base = 0; base < num_seqs; base += blockDim.x) {
+        const int64_t n = base + tid;
+        int cnt = 0;
+        int64_t t0 = 0, len = 0;
+        if (n < num_seqs) {
+            if (cu) {
+                t0 = cu[n];
+                const int64_t t1 = cu[n + 1];
+                len = t1 - t0;
+                if (len < 0 || t0 < 0 || t1 > total_tokens) {
+                    s_bad = 1;
+                    len = 0;
+                }
+            } else {
+                t0 = n * seq_len;
+                len = seq_len;
+            }
+            cnt = (int)((len + kChunk - 1) / kChunk);
+        }
+        s_scan[tid] = cnt;
+        __syncthreads();
+        for (int off = 1; off < (int)blockDim.x; off <<= 1) {
+            const int add = tid >= off ? s_scan[tid - off] : 0;
+            __syncthreads();
+            s_scan[tid] += add;
+            __syncthreads();
+        }
+        const int first = s_carry + s_scan[tid] - cnt;
+        if (n < num_seqs) {
+            seq_chunk[n] = first;
+            for (int j = 0; j < cnt; ++j) {
+                if (first + j >= max_chunks) {
+                    s_bad = 1;
+                    break;
+                }
+                const int64_t rem = len - (int64_t)j * kChunk;
+                plan[first + j] = make_int4((int)n, (int)(t0 + (int64_t)j * kChunk),
+                                            (int)(rem < kChunk ? rem : kChunk), j);
+            }
+        }
+        __syncthreads();
+        if (tid == (int)blockDim.x - 1) s_carry += s_scan[tid];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        if (cu && (cu[0] != 0 || cu[num_seqs] != total_tokens)) s_bad = 1;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        seq_chunk[num_seqs] = s_carry;
+        ctl[0] = s_bad ? GDR_ERR_BAD_SEQLENS : GDR_OK;
+        ctl[1] = s_bad ? 0 : s_carry;
+    }
+}
+
+int launch_plan(const PrefillArgs &a, const WsLayout &L) {
+    plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.num_seqs, a.total_tokens, L.max_chunks,
+                                          (int4 *)(a.ws + L.plan), (int32_t *)(a.ws + L.seq_chunk),
+                                          (int32_t *)(a.ws + L.ctl));
+    return cuda_status(cudaGetLastError());
+}
+
+// ----------------------------------------------------------------------------- prep
+
+template <int DK> struct PrepSmem {
+    static constexpr int KP = DK + 1;  // padded row pitch (floats)
+    static constexpr int CP = kChunk + 1;
+    static constexpr size_t floats = 2 * kChunk * KP + 3 * kChunk * CP + 3 * kChunk;
+    static constexpr size_t bytes = floats * sizeof(float);
+};
+
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(256)
+exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
+                  const float *__restrict__ log_alpha, const float *__restrict__ beta, int H,
+                  int dv, const int4 *__restrict__ plan, const int32_t *__restrict__ ctl,
+                  float *__restrict__ Wws, float *__restrict__ Uws, float *__restrict__ Aws,
+                  float *__restrict__ gws) {
+    using SM = PrepSmem<DK>;
+    constexpr int KP = SM::KP, CP = SM::CP, C = kChunk;
+    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    if (ctl[0] != GDR_OK || c >= ctl[1]) return;
+    const int4 p = plan[c];
+    const int64_t t0 = p.y;
+    const int len = p.z;
+
+    extern __shared__ float smem[];
+    float *ks = smem;                 // [C][KP]
+    float *qs = ks + C * KP;          // [C][KP]
+    float *Lm = qs + C * KP;          // [C][CP] strictly lower: beta_t Gamma_ti k_t.k_i
+    float *Am = Lm + C * CP;          // [C][CP] lower incl. diagonal: Gamma_ti q_t.k_i
+    float *Tm = Am + C * CP;          // [C][CP] T = (I + L)^{-1} diag(beta)
+    float *gs = Tm + C * CP;          // [C] cumulative log decay
+    float *bs = gs + C;               // [C] beta (0 on padding rows)
+    float *gam = bs + C;              // [C] exp(g)
+
+    for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+        const int t = idx / DK, d = idx % DK;
+        float kv = 0.f, qv = 0.f;
+        if (t < len) {
+            const size_t off = ((size_t)(t0 + t) * H + h) * DK + d;
+            kv = to_f32(k[off]);
+            qv = to_f32(q[off]);
+        }
+        ks[t * KP + d] = kv;
+        qs[t * KP + d] = qv;
+    }
+    if (tid < C) {
+        float b = 0.f, l = 0.f;
+        if (tid < len) {
+            const size_t off = (size_t)(t0 + tid) * H + h;
+            b = beta[off];
+            l = log_alpha[off];
+        }
+        bs[tid] = b;
+        gs[tid] = l;
+    }
+    __syncthreads();
+    if (tid < 32) {  // inclusive prefix sum of log alpha, two tokens per lane
+        const float a0 = gs[2 * tid], a1 = gs[2 * tid + 1];
+        float s = a0 + a1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, s, off);
+            if (tid >= off) s += n;
+        }
+        const float excl = s - (a0 + a1);
+        gs[2 * tid] = excl + a0;
+        gs[2 * tid + 1] = excl + a0 + a1;
+        gam[2 * tid] = expf(excl + a0);
+        gam[2 * tid + 1] = expf(excl + a0 + a1);
+    }
+    __syncthreads();
+
+    for (int idx = tid; idx < C * C; idx += blockDim.x) {
+        const int t = idx / C, i = idx % C;
+        float kk = 0.f, qk = 0.f, dec = 0.f;
+        if (i <= t) {
+            for (int d = 0; d < DK; ++d) {
+                const float ki = ks[i * KP + d];
+                kk = fmaf(ks[t * KP + d], ki, kk);
+                qk = fmaf(qs[t * KP + d], ki, qk);
+            }
+            dec = expf(gs[t] - gs[i]);
+        }
+        Lm[t * CP + i] = (i < t) ? bs[t] * dec * kk : 0.f;
+        Am[t * CP + i] = dec * qk;
+    }
+    __syncthreads();
+
+    // Forward substitution, one column of T per thread: (I + L) x = beta_j e_j.
+    if (tid < C) {
+        const int j = tid;
+        for (int t = 0; t < C; ++t) {
+            float x = 0.f;
+            if (t == j) {
+                x = bs[j];
+            } else if (t > j) {
+                float s = 0.f;
+                for (int i = j; i < t; ++i) s = fmaf(Lm[t * CP + i], Tm[i * CP + j], s);
+                x = -s;
+            }
+            Tm[t * CP + j] = x;
+        }
+    }
+    __syncthreads();
+
+    const size_t cb = (size_t)c * H + h;
+    float *Wout = Wws + cb * C * DK;
+    for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+        const int t = idx / DK, d = idx % DK;
+        float s = 0.f;
+        for (int i = 0; i <= t; ++i) s = fmaf(Tm[t * CP + i] * gam[i], ks[i * KP + d], s);
+        Wout[idx] = s;
+    }
+    float *Uout = Uws + cb * C * dv;
+    for (int idx = tid; idx < C * dv; idx += blockDim.x) {
+        const int t = idx / dv, j = idx % dv;
+        float s = 0.f;
+        const int last = t < len ? t : len - 1;
+        for (int i = 0; i <= last; ++i)
+            s = fmaf(Tm[t * CP + i], to_f32(v[((size_t)(t0 + i) * H + h) * dv + j]), s);
+        Uout[idx] = s;
+    }
+    float *Aout = Aws + cb * C * C;
+    for (int idx = tid; idx < C * C; idx += blockDim.x) Aout[idx] = Am[(idx / C) * CP + idx % C];
+    if (tid < C) gws[cb * C + tid] = gs[tid];
+}
+
+// ----------------------------------------------------------------------------- chain
+
+constexpr int kChainCols = 32;  // value columns per chain CTA
+
+template <int DK> struct ChainSmem {
+    static constexpr int KP = DK + 1;
+    static constexpr int SP = kChainCols + 1;
+    static constexpr size_t floats = DK * SP + 3 * kChunk * KP + kChunk * (kChunk + 1) +
+                                     kChunk * SP + 3 * kChunk;
+    static constexpr size_t bytes = floats * sizeof(float);
+};
+
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(256)
+exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                   const float *__restrict__ S0, const int32_t *__restrict__ cu,
+                   int64_t num_seqs, int64_t total_tokens, int H, int dv,
+                   const int32_t *__restrict__ seq_chunk, const int32_t *__restrict__ ctl,
+                   const float *__restrict__ Wws, const float *__restrict__ Uws,
+                   const float *__restrict__ Aws, const float *__restrict__ gws,
+                   Tin *__restrict__ o, float *__restrict__ S_final) {
+    using SM = ChainSmem<DK>;
+    constexpr int KP = SM::KP, SP = SM::SP, C = kChunk, NC = kChainCols, CP = C + 1;
+    if (ctl[0] != GDR_OK) return;
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const int j0 = blockIdx.y * NC;
+    const int tid = threadIdx.x;
+    int64_t t_begin, t_end;
+    if (cu) {
+        t_begin = cu[n];
+        t_end = cu[n + 1];
+    } else {
+        const int64_t sl = total_tokens / num_seqs;
+        t_begin = (int64_t)n * sl;
+        t_end = t_begin + sl;
+    }
+    const int c_first = seq_chunk[n];
+    const int n_chunks = seq_chunk[n + 1] - c_first;
+
+    extern __shared__ float smem[];
+    float *Ss = smem;            // [DK][SP]  the state's columns j0 .. j0+31
+    float *Wc = Ss + DK * SP;    // [C][KP]
+    float *qs = Wc + C * KP;     // [C][KP]
+    float *ks = qs + C * KP;     // [C][KP]
+    float *Ac = ks + C * KP;     // [C][CP]
+    float *Uc = Ac + C * CP;     // [C][SP]  Utilde, then U
+    float *gs = Uc + C * SP;     // [C]
+    float *gam = gs + C;         // [C] exp(g_t)
+    float *kdec = gam + C;       // [C] exp(g_last - g_i)
+
+    const size_t s_base = ((size_t)n * H + h) * DK * dv;
+    for (int idx = tid; idx < DK * NC; idx += blockDim.x) {
+        const int d = idx / NC, j = idx % NC;
+        Ss[d * SP + j] = S0 ? S0[s_base + (size_t)d * dv + j0 + j] : 0.f;
+    }
+    __syncthreads();
+
+    for (int cc = 0; cc < n_chunks; ++cc) {
+        const size_t cb = (size_t)(c_first + cc) * H + h;
+        const int64_t tc0 = t_begin + (int64_t)cc * C;
+        const int len = (int)((t_end - tc0) < C ? (t_end - tc0) : C);
+        for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+            const int t = idx / DK, d = idx % DK;
+            Wc[t * KP + d] = Wws[cb * C * DK + idx];
+            float kv = 0.f, qv = 0.f;
+            if (t < len) {
+                const size_t off = ((size_t)(tc0 + t) * H + h) * DK + d;
+                kv = to_f32(k[off]);
+                qv = to_f32(q[off]);
+            }
+            ks[t * KP + d] = kv;
+            qs[t * KP + d] = qv;
+        }
+        for (int idx = tid; idx < C * C; idx += blockDim.x)
+            Ac[(idx / C) * CP + idx % C] = Aws[cb * C * C + idx];
+        for (int idx = tid; idx < C * NC; idx += blockDim.x) {
+            const int t = idx / NC, j = idx % NC;
+            Uc[t * SP + j] = Uws[cb * C * dv + (size_t)t * dv + j0 + j];
+        }
+        if (tid < C) {
+            gs[tid] = gws[cb * C + tid];
+            gam[tid] = expf(gs[tid]);
+        }
+        __syncthreads();
+        if (tid < C) kdec[tid] = expf(gs[C - 1] - gs[tid]);
+
+        // U = Utilde - W S  and  QS, one token row and 8 columns per thread.
+        const int t = tid >> 2, jg = (tid & 3) * 8;
+        float u[8], qsv[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            u[x] = 0.f;
+            qsv[x] = 0.f;
+        }
+        for (int d = 0; d < DK; ++d) {
+            const float w = Wc[t * KP + d], qq = qs[t * KP + d];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                const float sv = Ss[d * SP + jg + x];
+                u[x] = fmaf(w, sv, u[x]);
+                qsv[x] = fmaf(qq, sv, qsv[x]);
+            }
+        }
+        __syncthreads();  // every thread has read S and Utilde is still intact
+#pragma unroll
+        for (int x = 0; x < 8; ++x) Uc[t * SP + jg + x] -= u[x];
+        __syncthreads();
+        // O = gamma_t QS + A U
+        if (t < len) {
+            float outv[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) outv[x] = gam[t] * qsv[x];
+            for (int i = 0; i <= t; ++i) {
+                const float aw = Ac[t * CP + i];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) outv[x] = fmaf(aw, Uc[i * SP + jg + x], outv[x]);
+            }
+            Tin *op = o + ((size_t)(tc0 + t) * H + h) * dv + j0 + jg;
+#pragma unroll
+            for (int x = 0; x < 8; ++x) op[x] = from_f32<Tin>(outv[x]);
+        }
+        // S <- gamma_C S + Ktilde^T U
+        {
+            constexpr int TPR = 256 / DK;          // threads per state row
+            constexpr int CPT = NC / TPR;          // columns per thread
+            const int d = tid / TPR, jb = (tid % TPR) * CPT;
+            const float gC = gam[C - 1];
+            float acc[CPT];
+#pragma unroll
+            for (int x = 0; x < CPT; ++x) acc[x] = gC * Ss[d * SP + jb + x];
+            for (int i = 0; i < C; ++i) {
+                const float kt = kdec[i] * ks[i * KP + d];
+#pragma unroll
+                for (int x = 0; x < CPT; ++x) acc[x] = fmaf(kt, Uc[i * SP + jb + x], acc[x]);
+            }
+            __syncthreads();  // all reads of the old S (QS above) are done
+#pragma unroll
+            for (int x = 0; x < CPT; ++x) Ss[d * SP + jb + x] = acc[x];
+        }
+        __syncthreads();
+    }
+
+    for (int idx = tid; idx < DK * NC; idx += blockDim.x) {
+        const int d = idx / NC, j = idx % NC;
+        S_final[s_base + (size_t)d * dv + j0 + j] = Ss[d * SP + j];
+    }
+}
+
+// ----------------------------------------------------------------------------- launch
+
+template <typename Tin, int DK>
+static int launch_exact_t(const PrefillArgs &a, const WsLayout &L) {
+    const int32_t *ctl = (const int32_t *)(a.ws + L.ctl);
+    float *W = (float *)(a.ws + L.W), *U = (float *)(a.ws + L.U);
+    float *A = (float *)(a.ws + L.A), *g = (float *)(a.ws + L.g);
+    cudaError_t e;
+    e = cudaFuncSetAttribute(exact_prep_kernel<Tin, DK>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)PrepSmem<DK>::bytes);
+    if (e != cudaSuccess) return GDR_ERR_CUDA;
+    e = cudaFuncSetAttribute(exact_chain_kernel<Tin, DK>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ChainSmem<DK>::bytes);
+    if (e != cudaSuccess) return GDR_ERR_CUDA;
+    if (L.max_chunks > 0) {
+        dim3 grid((unsigned)L.max_chunks, (unsigned)a.H);
+        exact_prep_kernel<Tin, DK><<<grid, 256, PrepSmem<DK>::bytes, a.stream>>>(
+            (const Tin *)a.q, (const Tin *)a.k, (const Tin *)a.v, a.log_alpha, a.beta, a.H, a.dv,
+            (const int4 *)(a.ws + L.plan), ctl, W, U, A, g);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return GDR_ERR_CUDA;
+    }
+    dim3 grid2((unsigned)(a.num_seqs * a.H), (unsigned)(a.dv / kChainCols));
+    exact_chain_kernel<Tin, DK><<<grid2, 256, ChainSmem<DK>::bytes, a.stream>>>(
+        (const Tin *)a.q, (const Tin *)a.k, a.S0, a.cu_seqlens, a.num_seqs, a.total_tokens, a.H,
+        a.dv, (const int32_t *)(a.ws + L.seq_chunk), ctl, W, U, A, g, (Tin *)a.o, a.S_final);
+    return cuda_status(cudaGetLastError());
+}
+
+int launch_prefill_exact(const PrefillArgs &a, const WsLayout &L) {
+    if (a.dtype == GDR_BF16) {
+        if (a.dk == 64) return launch_exact_t<__nv_bfloat16, 64>(a, L);
+        return launch_exact_t<__nv_bfloat16, 128>(a, L);
+    }
+    if (a.dk == 64) return launch_exact_t<float, 64>(a, L);
+    return launch_exact_t<float, 128>(a, L);
+}
+
+}  // namespace gdr

@@ -1,0 +1,201 @@
+"""Thin ctypes binding over libgdr.so (include/gdr.h).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels. PyTorch provides device memory and the current stream. If the
+library is missing the first call raises GdrError; nothing falls back to the CPU.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libgdr.so")
+_lib = None
+
+GDR_F32, GDR_BF16 = 0, 1
+_DTYPES = {torch.float32: GDR_F32, torch.bfloat16: GDR_BF16}
+
+
+class GdrError(RuntimeError):
+    """A libgdr call returned a negative status."""
+
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise GdrError(-5, f"libgdr.so not found at {_LIB_PATH}; build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, fp, i64, c_int = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.gdr_status_string.argtypes = [c_int]
+    lib.gdr_status_string.restype = ctypes.c_char_p
+    lib.gdr_chunk_fwd_workspace_size.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int]
+    lib.gdr_chunk_fwd_workspace_size.restype = ctypes.c_size_t
+    lib.gdr_chunk_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, i64, i64, c_int, c_int, c_int,
+                                  c_int, c_int, vp, fp, vp, ctypes.c_size_t, vp]
+    lib.gdr_chunk_fwd.restype = c_int
+    lib.gdr_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i64, c_int, c_int, c_int, c_int,
+                                    vp]
+    lib.gdr_decode_step.restype = c_int
+    lib.gdr_chunk_fwd_path.argtypes = [c_int, c_int, c_int]
+    lib.gdr_chunk_fwd_path.restype = c_int
+    lib.gdr_read_device_status.argtypes = [vp, ctypes.POINTER(c_int), vp]
+    lib.gdr_read_device_status.restype = c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status):
+    return _load().gdr_status_string(int(status)).decode()
+
+
+def _check(status, what):
+    if status != 0:
+        raise GdrError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def chunk_fwd_workspace_size(num_seqs, total_tokens, H, dk, dv, chunk=64, dtype=torch.bfloat16):
+    """Workspace bytes gdr_chunk_fwd needs (0 if the sizes are unsupported)."""
+    return int(_load().gdr_chunk_fwd_workspace_size(int(num_seqs), int(total_tokens), int(H),
+                                                    int(dk), int(dv), int(chunk),
+                                                    _DTYPES[dtype]))
+
+
+def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None, chunk=64,
+              o=None, S_final=None, workspace=None, stream=None):
+    """Chunked prefill (gdr_chunk_fwd).
+
+    q, k [T, H, dk]; v [T, H, dv] (fp32 or bf16); log_alpha, beta [T, H] fp32;
+    S0 [num_seqs, H, dk, dv] fp32 or None; cu_seqlens [num_seqs+1] int32 or None
+    (then `num_seqs` equal sequences, default 1). Optional preallocated o,
+    S_final and workspace (uint8) tensors are used as given. Returns (o, S_final).
+    """
+    lib = _load()
+    _need(q, "q")
+    dev, dt = q.device, q.dtype
+    if dt not in _DTYPES:
+        raise TypeError(f"unsupported dtype {dt}")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    _need(k, "k", dt, dev)
+    _need(v, "v", dt, dev)
+    _need(log_alpha, "log_alpha", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        n = cu_seqlens.numel() - 1
+    else:
+        n = 1 if num_seqs is None else int(num_seqs)
+    if S0 is not None:
+        _need(S0, "S0", torch.float32, dev)
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=dt, device=dev)
+    if S_final is None:
+        S_final = torch.empty((n, H, dk, dv), dtype=torch.float32, device=dev)
+    _need(o, "o", dt, dev)
+    _need(S_final, "S_final", torch.float32, dev)
+    ws_bytes = chunk_fwd_workspace_size(n, T, H, dk, dv, chunk, dt)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", device=dev)
+    st = lib.gdr_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                           _ptr(cu_seqlens), n, T, H, dk, dv, int(chunk), _DTYPES[dt], _ptr(o),
+                           _ptr(S_final), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(),
+                           _stream_handle(stream, dev))
+    _check(st, "gdr_chunk_fwd")
+    return o, S_final
+
+
+def read_device_status(workspace, stream=None):
+    """Status word the last gdr_chunk_fwd left in `workspace` (synchronises the stream)."""
+    out = ctypes.c_int(0)
+    st = _load().gdr_read_device_status(_ptr(workspace), ctypes.byref(out),
+                                        _stream_handle(stream, workspace.device))
+    _check(st, "gdr_read_device_status")
+    return out.value
+
+
+def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None):
+    """One decode step (gdr_decode_step): q, k [N, H, dk]; v [N, H, dv];
+    log_alpha, beta [N, H] fp32; S [N, H, dk, dv] fp32 updated in place.
+    Returns o [N, H, dv]."""
+    lib = _load()
+    _need(q, "q")
+    dev, dt = q.device, q.dtype
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    _need(k, "k", dt, dev)
+    _need(v, "v", dt, dev)
+    _need(log_alpha, "log_alpha", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(S, "S", torch.float32, dev)
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=dt, device=dev)
+    _need(o, "o", dt, dev)
+    st = lib.gdr_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S),
+                             _ptr(o), N, H, dk, dv, _DTYPES[dt], _stream_handle(stream, dev))
+    _check(st, "gdr_decode_step")
+    return o
+
+
+# What one gdr_chunk_fwd call enqueues on each kernel path (see gdr_chunk_fwd_path in gdr.h).
+_PATHS = {
+    0: dict(launches=3, main_kernel="exact_chain_kernel", compute_dtype="f32"),
+    1: dict(launches=2, main_kernel="tc_prefill_kernel", compute_dtype="bf16"),
+}
+
+
+def chunk_fwd_path(dk, dv, dtype):
+    st = _load().gdr_chunk_fwd_path(int(dk), int(dv), _DTYPES[dtype])
+    if st < 0:
+        raise GdrError(st, "gdr_chunk_fwd_path")
+    return st
+
+
+def chunk_fwd_kernel_launches(dk, dv, dtype):
+    """Kernels one gdr_chunk_fwd call launches for these sizes."""
+    return _PATHS[chunk_fwd_path(dk, dv, dtype)]["launches"]
+
+
+def chunk_fwd_main_kernel(dk, dv, dtype):
+    """Name of the kernel that dominates a gdr_chunk_fwd call for these sizes."""
+    return _PATHS[chunk_fwd_path(dk, dv, dtype)]["main_kernel"]
+
+
+def chunk_fwd_compute_dtype(dk, dv, dtype):
+    """Arithmetic type of the products on the path taken (f32 SIMT or bf16 tensor cores)."""
+    return _PATHS[chunk_fwd_path(dk, dv, dtype)]["compute_dtype"]

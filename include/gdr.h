@@ -1,0 +1,169 @@
+/*
+ * gdr.h -- C ABI of libgdr, the GB300 (sm_103a) gated delta rule library.
+ *
+ * The gated delta rule (Gated DeltaNet recurrence) keeps, per sequence and
+ * head, a d_k x d_v state S and for every token t computes
+ *     S'_t = alpha_t S_{t-1},  vhat_t = S'_t^T k_t,
+ *     S_t  = S'_t + beta_t k_t (v_t - vhat_t)^T,  o_t = S_t^T q_t
+ * ("Linear attention" (arsalanzafar.ai), section "How it works", Eqs. (1)-(4),
+ * keys x values layout; the state is updated before it is read, "How linear
+ * attention works: a small memory matrix and the gated delta rule", section
+ * "Writing a key-value association"). alpha_t = exp(log_alpha_t).
+ * No score scale and no normalisation of q or k are applied: the caller
+ * passes the vectors to use.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise, to
+ *     memory owned by the caller. The library never allocates device memory,
+ *     never frees caller memory and keeps no state between calls.
+ *   - Tensors are dense and row-major. q, k, v, o, S0, S, S_final and the
+ *     workspace start on a 16-byte boundary; log_alpha, beta and cu_seqlens
+ *     on a 4-byte boundary (so per-token slices of the gates are accepted).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and is asynchronous: outputs are valid once the stream has
+ *     reached the call. Only gdr_read_device_status() synchronises.
+ *   - Argument errors are detected on the host before anything is enqueued and
+ *     returned as a negative status; nothing is written in that case.
+ *   - gdr_dtype selects the storage type of q, k, v and o. Gates and states
+ *     are always fp32.
+ *   - Gate preconditions (not checked on the device): log_alpha finite and
+ *     <= 0 (alpha = 0 is expressed as a large negative value, never -inf),
+ *     beta finite. Accuracy is specified for beta in [0, 1].
+ */
+#ifndef GDR_H
+#define GDR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *gdr_stream_t; /* the same handle as cudaStream_t */
+
+typedef enum {
+    GDR_F32 = 0,  /* q, k, v, o in fp32 (exact fp32 arithmetic path) */
+    GDR_BF16 = 1  /* q, k, v, o in bf16 (tensor-core path, fp32 accumulation) */
+} gdr_dtype;
+
+enum {
+    GDR_OK = 0,
+    GDR_ERR_INVALID_ARG = -1,    /* null pointer, negative or inconsistent size */
+    GDR_ERR_UNSUPPORTED = -2,    /* dtype, d_k, d_v or chunk outside the supported set */
+    GDR_ERR_ALIGNMENT = -3,      /* a pointer is not aligned as required */
+    GDR_ERR_WORKSPACE = -4,      /* workspace missing or smaller than required */
+    GDR_ERR_CUDA = -5,           /* a CUDA runtime call or kernel launch failed */
+    GDR_ERR_DEVICE_TIMEOUT = -6, /* a device-side wait gave up (read via gdr_read_device_status) */
+    GDR_ERR_BAD_SEQLENS = -7     /* cu_seqlens not 0 ... total_tokens non-decreasing (device-checked) */
+};
+
+/*
+ * Human-readable name of a status code. The returned string is static.
+ */
+const char *gdr_status_string(int status);
+
+/*
+ * Bytes of device workspace gdr_chunk_fwd needs for these sizes (a host-only
+ * computation; no CUDA call). Returns 0 when the sizes are unsupported or
+ * invalid, in which case gdr_chunk_fwd rejects them too.
+ */
+size_t gdr_chunk_fwd_workspace_size(int64_t num_seqs, int64_t total_tokens, int H, int d_k,
+                                    int d_v, int chunk, int dtype);
+
+/*
+ * Chunked prefill over packed sequences.
+ *
+ * What it computes: for every sequence n and head h, the recurrence above run
+ * over the sequence's tokens from the initial state S0[n, h] (zero if S0 is
+ * NULL); o receives every o_t and S_final[n, h] the state after the last
+ * token. The result is the token recurrence's, computed chunk by chunk
+ * ("Attention as Matrix Algebra: From Softmax to the Delta Rule", section 8
+ * "Training the delta rule in chunks": a unit lower-triangular solve turns
+ * values into pseudo-values, then chunked linear attention carries the state
+ * across chunks), extended with the decay gate: inside a chunk
+ * g_t = sum of log_alpha up to t, (I + L) with L_ti = beta_t exp(g_t - g_i)
+ * k_t.k_i (i < t), and the state between chunks decays by exp(g_last).
+ * Chunks never straddle sequences; a sequence's last chunk may be partial.
+ *
+ * Arguments
+ *   q, k          [total_tokens, H, d_k]  dtype
+ *   v             [total_tokens, H, d_v]  dtype
+ *   log_alpha     [total_tokens, H]       fp32, log of the decay gate (<= 0)
+ *   beta          [total_tokens, H]       fp32, write strength
+ *   S0            [num_seqs, H, d_k, d_v] fp32 (d_v contiguous), or NULL for zero
+ *   cu_seqlens    [num_seqs + 1] int32 token offsets, cu_seqlens[0] = 0,
+ *                 non-decreasing, cu_seqlens[num_seqs] = total_tokens; or NULL for
+ *                 num_seqs sequences of total_tokens / num_seqs tokens each
+ *                 (then num_seqs must divide total_tokens). A sequence of zero
+ *                 tokens is allowed: its S_final equals its S0. cu_seqlens lives in
+ *                 device memory, so it is validated on the device: a violation sets
+ *                 GDR_ERR_BAD_SEQLENS in the workspace status word (see
+ *                 gdr_read_device_status) and the contents of o and S_final are then
+ *                 unspecified; no access leaves the buffers described here.
+ *   num_seqs, total_tokens, H   sizes (num_seqs >= 1, total_tokens >= 0, H >= 1)
+ *   d_k           64 or 128
+ *   d_v           a multiple of 32 in [32, 256] (bf16 tensor-core path: 128 or 256
+ *                 with d_k = 128; other shapes use the exact fp32-arithmetic path)
+ *   chunk         64
+ *   dtype         gdr_dtype of q, k, v and o
+ *   o             [total_tokens, H, d_v]  dtype (written)
+ *   S_final       [num_seqs, H, d_k, d_v] fp32 (written). It may be the same buffer
+ *                 as S0 (in-place update); any other overlap is not allowed.
+ *   workspace     device scratch of at least gdr_chunk_fwd_workspace_size() bytes,
+ *                 16-byte aligned; its first bytes hold the device status word.
+ *                 Calls that share a workspace must be ordered on one stream.
+ *   stream        stream to enqueue on
+ * Returns GDR_OK or a negative status from the list above.
+ */
+int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  const float *beta, const float *S0, const int32_t *cu_seqlens,
+                  int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v, int chunk,
+                  int dtype, void *o, float *S_final, void *workspace, size_t workspace_bytes,
+                  gdr_stream_t stream);
+
+/*
+ * One decode step: one new token for each of N sequences, the state updated in
+ * place. Per (n, h) it reads S once and writes it once, fusing the decay, the
+ * read vhat = alpha S^T k, the delta write S <- alpha S + k u^T with
+ * u = beta (v - vhat), and the output o = S_new^T q
+ * ("Attention as Matrix Algebra", section 9: a generation step reads about
+ * d_k d_v numbers; "Linear attention" (arsalanzafar.ai), Eqs. (1)-(4)).
+ *
+ * Arguments
+ *   q, k        [N, H, d_k]  dtype
+ *   v           [N, H, d_v]  dtype
+ *   log_alpha   [N, H] fp32;  beta [N, H] fp32
+ *   S           [N, H, d_k, d_v] fp32, read and overwritten with the new state
+ *   o           [N, H, d_v]  dtype (written); must not overlap S
+ *   N >= 0, H >= 1, d_k in {64, 128}, d_v in {64, 128, 256}
+ * Returns GDR_OK or a negative status. N = 0 enqueues nothing.
+ */
+int gdr_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
+                    const float *beta, float *S, void *o, int64_t N, int H, int d_k, int d_v,
+                    int dtype, gdr_stream_t stream);
+
+/*
+ * Which kernel path gdr_chunk_fwd takes for these sizes, for diagnostics and
+ * benchmarks (host-only, no CUDA call): GDR_PATH_EXACT (plain fp32 arithmetic:
+ * a planning kernel, a per-chunk kernel and a per-sequence chain kernel) or
+ * GDR_PATH_TENSOR (bf16 tensor cores: a planning kernel and one fused kernel).
+ * Returns a negative status for unsupported sizes.
+ */
+enum { GDR_PATH_EXACT = 0, GDR_PATH_TENSOR = 1 };
+int gdr_chunk_fwd_path(int d_k, int d_v, int dtype);
+
+/*
+ * Reads the device status word that the last gdr_chunk_fwd call on this
+ * workspace left (GDR_OK, GDR_ERR_BAD_SEQLENS or GDR_ERR_DEVICE_TIMEOUT) into
+ * *status (a HOST pointer). It synchronises `stream` first, so it must not be
+ * called inside stream capture. Returns GDR_OK if the status was read.
+ */
+int gdr_read_device_status(const void *workspace, int *status, gdr_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H */
