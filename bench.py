@@ -73,27 +73,32 @@ def decode_bytes(N, H, dk, dv, esz=2):
 
 
 def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch from an ncu capture summarised in profiles/traffic.txt, valid
-    only while the kernel's CUDA sources are unchanged since the capture (else None)."""
+    """DRAM bytes per launch from an ncu capture summarised in profiles/traffic.txt. A
+    record holds while the kernel's source file (and the shared internal header) is
+    unchanged since the capture; otherwise the traffic is unknown (None)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    src_sha = sources_sha()
     with open(path) as f:
         for line in f:
             fields = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-            if (fields.get("kernel") == kernel and fields.get("workload") == workload
-                    and fields.get("source_sha") == src_sha):
+            if fields.get("kernel") != kernel or fields.get("workload") != workload:
+                continue
+            if fields.get("source_sha") == source_sha(fields.get("source", "")):
                 return float(fields["dram_bytes_per_launch"])
     return None
 
 
-def sources_sha():
-    h = hashlib.sha256()
+def source_sha(name):
+    """Hash of one CUDA source file plus the internal header every kernel includes."""
     csrc = os.path.join(ROOT, "gated_delta_rule_03_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    h = hashlib.sha256()
+    for fn in (name, "internal.h"):
+        path = os.path.join(csrc, fn)
+        if not fn or not os.path.exists(path):
+            return None
+        with open(path, "rb") as f:
+            h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -402,12 +407,29 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=["all", "decode"], default="all",
+                    help="'decode' runs only the decode timing (for profiling that kernel)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.only == "decode":
+        return run_decode_only(args)
     return run_gdr(args)
+
+
+def run_decode_only(args):
+    """Only the decode timing, printed as its own JSON object (a profiling aid; the
+    benchmark line proper comes from the default mode)."""
+    from gated_delta_rule_03_gb300 import decode_step
+    world, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    out = run_decode(args, decode_step, device, stream, 1, load_peaks())
+    print(json.dumps({"decode": out}), flush=True)
+    return 0
 
 
 if __name__ == "__main__":
