@@ -145,6 +145,38 @@ int gdr_decode_step(const void *q, const void *k, const void *v, const float *lo
                     int dtype, gdr_stream_t stream);
 
 /*
+ * gdr_chunk_fwd for callers that cannot allocate device memory.
+ *
+ * (The pages have no counterpart: this is a deployment convenience, not part
+ * of the method.) Some callers cannot hand gdr_chunk_fwd a workspace: a
+ * plugin loaded into a runtime that owns the device allocator and offers its
+ * plugins no way to allocate, or a serving loop whose memory policy forbids
+ * device allocations after start-up. This entry point takes the same
+ * arguments as gdr_chunk_fwd minus the workspace and computes the same
+ * result, using as scratch a static array inside the library of
+ * GDR_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library
+ * holds until the process exits. It allocates nothing.
+ *
+ *   - Sizes whose workspace (gdr_chunk_fwd_workspace_size) exceeds
+ *     GDR_NOALLOC_SCRATCH_BYTES are rejected with GDR_ERR_WORKSPACE before
+ *     anything is enqueued; other argument errors are those of gdr_chunk_fwd.
+ *   - The device current on the calling thread must be the one the pointers
+ *     and the stream belong to. The first call on a device looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (nothing needs clearing: each call writes all the scratch it reads).
+ *     Calls that overlap on the GPU race on it: order them on one stream.
+ *   - The status word of the last call sits at the start of the array; it is
+ *     not reachable through gdr_read_device_status.
+ */
+#define GDR_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+int gdr_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_alpha,
+                          const float *beta, const float *S0, const int32_t *cu_seqlens,
+                          int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v,
+                          int chunk, int dtype, void *o, float *S_final, gdr_stream_t stream);
+
+/*
  * Which kernel path gdr_chunk_fwd takes for these sizes, for diagnostics and
  * benchmarks (host-only, no CUDA call): GDR_PATH_EXACT (plain fp32 arithmetic:
  * a planning kernel, a per-chunk kernel and a per-sequence chain kernel) or
