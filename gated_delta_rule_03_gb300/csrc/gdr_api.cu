@@ -13,8 +13,7 @@ namespace gdr {
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool use_tensor_path(int dk, int dv, int dtype) {
-    (void)dk; (void)dv; (void)dtype;
-    return false;
+    return dtype == GDR_BF16 && dk == 128 && (dv == 128 || dv == 256);
 }
 
 WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype) {
@@ -130,7 +129,7 @@ int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
     a.stream = (cudaStream_t)stream;
     st = launch_plan(a, L);
     if (st != GDR_OK) return st;
-    return launch_prefill_exact(a, L);
+    return L.tensor_path ? launch_prefill_tc(a, L) : launch_prefill_exact(a, L);
 }
 
 int gdr_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,

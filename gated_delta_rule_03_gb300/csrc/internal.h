@@ -43,6 +43,7 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
 // Launchers (return GDR_OK or GDR_ERR_CUDA).
 int launch_plan(const PrefillArgs &a, const WsLayout &L);
 int launch_prefill_exact(const PrefillArgs &a, const WsLayout &L);
+int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L);
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
                   int dtype, cudaStream_t stream);
