@@ -36,8 +36,8 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
         off = align_up(off + sizeof(float) * per * dv, 256);
         L.A = off;
         off = align_up(off + sizeof(float) * per * kChunk, 256);
-        L.g = off;
-        off = align_up(off + sizeof(float) * per, 256);
+        L.g = off;  // gamma and kdec per chunk
+        off = align_up(off + sizeof(float) * per * 2, 256);
     }
     L.total = off;
     return L;

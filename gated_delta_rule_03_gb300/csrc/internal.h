@@ -32,7 +32,7 @@ struct WsLayout {
     size_t ctl;           // int32[64]
     size_t plan;          // int4[max_chunks]: (sequence, first token, tokens, chunk index)
     size_t seq_chunk;     // int32[num_seqs + 1]: first chunk of each sequence
-    size_t W, U, A, g;    // fp32 per-chunk intermediates of the exact path
+    size_t W, U, A, g;    // fp32 per-chunk intermediates of the exact path (g: gamma, kdec)
     size_t total;
     bool tensor_path;     // bf16 tensor-core kernel (true) or exact fp32-arithmetic kernels
 };

@@ -7,20 +7,24 @@
 // the Delta Rule", section 8 ("Training the delta rule in chunks"), with the
 // decay gate carried through the same substitution. Per chunk of C tokens,
 // entering with state S:
-//   g_t = sum_{i<=t} log alpha_i,  gamma_t = exp(g_t),  Gamma_ti = exp(g_t - g_i)
+//   gamma_t = prod_{j<=t} alpha_j,  Gamma_ti = prod_{i<j<=t} alpha_j  (= exp(g_t - g_i))
 //   L_ti = beta_t Gamma_ti k_t.k_i (i < t),  T = (I + L)^{-1} diag(beta)
 //   W = T diag(gamma) K,  Utilde = T V                  (prep kernel, all chunks at once)
 //   U = Utilde - W S
 //   O = diag(gamma) Q S + (Q K^T . Gamma . [i <= t]) U
 //   S <- gamma_C S + Ktilde^T U,  Ktilde_i = exp(g_C - g_i) k_i   (chain kernel, in order)
-// Only exponents g_t - g_i with i <= t are formed, so every exponent is <= 0.
-// Padding rows of a partial chunk get beta = 0 and log alpha = 0: they change
-// nothing and their outputs are not stored.
+// The decay factors are products of the per-token alpha_j = exp(log alpha_j), never
+// differences of cumulative log-decays: a cumulative sum that has passed a huge
+// negative log alpha (alpha = 0 written as -1e4) keeps no digits for the small
+// differences after it, whereas the products stay exact to a few ulp (and exactly 0
+// across such a token). Padding rows of a partial chunk get beta = 0 and alpha = 1:
+// they change nothing and their outputs are not stored.
 //
 // Kernels, in stream order:
 //   plan   -- validates cu_seqlens, lists the chunks (sequence, first token,
 //             length) and each sequence's first chunk; writes the status word.
-//   prep   -- one CTA per (chunk, head): W, Utilde, the masked A = QK^T . Gamma, g.
+//   prep   -- one CTA per (chunk, head): W, Utilde, the masked A = QK^T . Gamma,
+//             gamma and kdec_i = Gamma_{C-1,i}.
 //   chain  -- one CTA per (sequence, head, 32 value columns): walks the chunks
 //             of its sequence in order, carrying its 32 columns of S (the
 //             columns of S evolve independently) in shared memory.
@@ -111,7 +115,7 @@ int launch_plan(const PrefillArgs &a, const WsLayout &L) {
 template <int DK> struct PrepSmem {
     static constexpr int KP = DK + 1;  // padded row pitch (floats)
     static constexpr int CP = kChunk + 1;
-    static constexpr size_t floats = 2 * kChunk * KP + 3 * kChunk * CP + 3 * kChunk;
+    static constexpr size_t floats = 2 * kChunk * KP + 4 * kChunk * CP + 3 * kChunk;
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
@@ -122,6 +126,7 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
                   int dv, const int4 *__restrict__ plan, const int32_t *__restrict__ ctl,
                   float *__restrict__ Wws, float *__restrict__ Uws, float *__restrict__ Aws,
                   float *__restrict__ gws) {
+    // gws receives, per chunk, gamma[C] followed by kdec[C].
     using SM = PrepSmem<DK>;
     constexpr int KP = SM::KP, CP = SM::CP, C = kChunk;
     const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -136,9 +141,10 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     float *Lm = qs + C * KP;          // [C][CP] strictly lower: beta_t Gamma_ti k_t.k_i
     float *Am = Lm + C * CP;          // [C][CP] lower incl. diagonal: Gamma_ti q_t.k_i
     float *Tm = Am + C * CP;          // [C][CP] T = (I + L)^{-1} diag(beta)
-    float *gs = Tm + C * CP;          // [C] cumulative log decay
-    float *bs = gs + C;               // [C] beta (0 on padding rows)
-    float *gam = bs + C;              // [C] exp(g)
+    float *Gm = Tm + C * CP;          // [C][CP] Gamma_ti (i <= t)
+    float *al = Gm + C * CP;          // [C] alpha (1 on padding rows)
+    float *bs = al + C;               // [C] beta (0 on padding rows)
+    float *gam = bs + C;              // [C] gamma
 
     for (int idx = tid; idx < C * DK; idx += blockDim.x) {
         const int t = idx / DK, d = idx % DK;
@@ -152,29 +158,24 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
         qs[t * KP + d] = qv;
     }
     if (tid < C) {
-        float b = 0.f, l = 0.f;
+        float b = 0.f, a = 1.f;
         if (tid < len) {
             const size_t off = (size_t)(t0 + tid) * H + h;
             b = beta[off];
-            l = log_alpha[off];
+            a = expf(log_alpha[off]);
         }
         bs[tid] = b;
-        gs[tid] = l;
+        al[tid] = a;
     }
     __syncthreads();
-    if (tid < 32) {  // inclusive prefix sum of log alpha, two tokens per lane
-        const float a0 = gs[2 * tid], a1 = gs[2 * tid + 1];
-        float s = a0 + a1;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float n = __shfl_up_sync(0xffffffffu, s, off);
-            if (tid >= off) s += n;
+    if (tid < C) {  // row t of Gamma by a running product from the diagonal down; then gamma_t
+        const int t = tid;
+        float prod = 1.f;
+        for (int i = t; i >= 0; --i) {
+            Gm[t * CP + i] = prod;      // prod_{i<j<=t} alpha_j
+            prod *= al[i];
         }
-        const float excl = s - (a0 + a1);
-        gs[2 * tid] = excl + a0;
-        gs[2 * tid + 1] = excl + a0 + a1;
-        gam[2 * tid] = expf(excl + a0);
-        gam[2 * tid + 1] = expf(excl + a0 + a1);
+        gam[t] = prod;                  // prod_{j<=t} alpha_j
     }
     __syncthreads();
 
@@ -187,7 +188,7 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
                 kk = fmaf(ks[t * KP + d], ki, kk);
                 qk = fmaf(qs[t * KP + d], ki, qk);
             }
-            dec = expf(gs[t] - gs[i]);
+            dec = Gm[t * CP + i];
         }
         Lm[t * CP + i] = (i < t) ? bs[t] * dec * kk : 0.f;
         Am[t * CP + i] = dec * qk;
@@ -230,7 +231,10 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     }
     float *Aout = Aws + cb * C * C;
     for (int idx = tid; idx < C * C; idx += blockDim.x) Aout[idx] = Am[(idx / C) * CP + idx % C];
-    if (tid < C) gws[cb * C + tid] = gs[tid];
+    if (tid < C) {
+        gws[cb * 2 * C + tid] = gam[tid];
+        gws[cb * 2 * C + C + tid] = Gm[(C - 1) * CP + tid];  // kdec_i = Gamma_{C-1,i}
+    }
 }
 
 // ----------------------------------------------------------------------------- chain
@@ -279,9 +283,8 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     float *ks = qs + C * KP;     // [C][KP]
     float *Ac = ks + C * KP;     // [C][CP]
     float *Uc = Ac + C * CP;     // [C][SP]  Utilde, then U
-    float *gs = Uc + C * SP;     // [C]
-    float *gam = gs + C;         // [C] exp(g_t)
-    float *kdec = gam + C;       // [C] exp(g_last - g_i)
+    float *gam = Uc + C * SP;    // [C] gamma_t
+    float *kdec = gam + C;       // [C] Gamma_{C-1,i}
 
     const size_t s_base = ((size_t)n * H + h) * DK * dv;
     for (int idx = tid; idx < DK * NC; idx += blockDim.x) {
@@ -313,11 +316,10 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             Uc[t * SP + j] = Uws[cb * C * dv + (size_t)t * dv + j0 + j];
         }
         if (tid < C) {
-            gs[tid] = gws[cb * C + tid];
-            gam[tid] = expf(gs[tid]);
+            gam[tid] = gws[cb * 2 * C + tid];
+            kdec[tid] = gws[cb * 2 * C + C + tid];
         }
         __syncthreads();
-        if (tid < C) kdec[tid] = expf(gs[C - 1] - gs[tid]);
 
         // U = Utilde - W S  and  QS, one token row and 8 columns per thread.
         const int t = tid >> 2, jg = (tid & 3) * 8;

@@ -18,8 +18,9 @@ Recipe (one numpy PCG64 generator per workload, `numpy.random.default_rng(seed)`
   * S0 ~ N(0, std^2) in fp32 when a workload asks for an initial state;
   * storage rounding: float64 -> float32 -> bf16 (round to nearest even, by torch).
 Gate variants used by stress cases: "slow" gives log alpha = -softplus(a - 6)
-(alpha about 0.9975) and "none" gives log alpha = 0 (alpha = 1, the ungated
-delta rule).
+(alpha about 0.9975), "none" gives log alpha = 0 (alpha = 1, the ungated
+delta rule) and "strong" gives log alpha = -softplus(a + 1.5) (a chunk of 64
+tokens decays by about e^-110).
 """
 from dataclasses import dataclass
 from typing import Optional
@@ -99,6 +100,8 @@ def _gates(rng, shape, gate):
         log_alpha = -np.logaddexp(0.0, a - 6.0)
     elif gate == "none":
         log_alpha = np.zeros(shape)
+    elif gate == "strong":
+        log_alpha = -np.logaddexp(0.0, a + 1.5)
     else:
         raise ValueError(f"unknown gate variant {gate!r}")
     beta = 1.0 / (1.0 + np.exp(-b))

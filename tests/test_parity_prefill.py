@@ -40,7 +40,7 @@ def test_tiny_fp32_workload():
     check(inputs.workload_prefill("tiny_fp32"))
 
 
-@pytest.mark.parametrize("gate", ["default", "slow", "none"])
+@pytest.mark.parametrize("gate", ["default", "slow", "none", "strong"])
 def test_prefill_bf16_workload(gate):
     check(inputs.workload_prefill("prefill_bf16", gate=gate))
 
@@ -56,7 +56,7 @@ def test_long_bf16_workload_heads_0_1():
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (128, 256), (64, 32), (128, 96)])
-@pytest.mark.parametrize("gate", ["default", "slow", "none"])
+@pytest.mark.parametrize("gate", ["default", "slow", "none", "strong"])
 def test_ragged_multi_chunk(dtype, dk, dv, gate):
     # several chunks plus a ragged tail, nonzero initial state
     inp = inputs.prefill_inputs([200, 64, 1, 130], H=3, dk=dk, dv=dv, dtype=dtype,
@@ -166,3 +166,17 @@ def test_unit_key_beta_one_reads_back_value():
     o, S = gpu_prefill(inp)
     readback = np.einsum("hdv,hd->hv", f64(S)[0], k[-1])
     np.testing.assert_allclose(readback, f64(inp.v)[-1], rtol=0, atol=2e-4)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_near_zero_decay_tokens(dtype):
+    # alpha = 0 written as log alpha = -1e4 on a few tokens (the state is wiped there),
+    # mixed with slow decay elsewhere, so chunks of both decay regimes follow each other
+    inp = inputs.prefill_inputs([333, 200], H=2, dk=128, dv=128, dtype=dtype, seed=14,
+                                s0_std=0.5, gate="slow")
+    rng = np.random.default_rng(15)
+    idx = rng.choice(inp.total_tokens, size=12, replace=False)
+    la = inp.log_alpha.clone()
+    la[idx, :] = -1.0e4
+    inp.log_alpha.copy_(la)
+    check(inp, per_sequence=True)
