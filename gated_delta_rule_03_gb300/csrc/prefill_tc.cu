@@ -73,7 +73,6 @@ constexpr int kPrepWarp0 = 4, kPrepThreads = 128;
 constexpr int kStateWarp0 = 8, kStateThreads = 256;
 constexpr int kBarPrep = 1, kBarState = 2;  // named barrier ids
 constexpr int LP = C + 1;                   // fp32 pitch of the solve matrices
-constexpr int PP = 17;                      // fp32 pitch of the solve scratch blocks
 
 // Shared memory map (bytes from a 1024-aligned base). A stage holds one chunk's inputs.
 constexpr uint32_t STAGE_BYTES = 51200;
@@ -91,8 +90,7 @@ constexpr uint32_t OFF_UT = OFF_WT + 16384;      // U^T bf16 [d_v 128][t 64]; ou
 constexpr uint32_t OFF_AM = OFF_UT + 16384;      // A bf16 [t][i], two 8 KB buffers
 constexpr uint32_t OFF_LF = OFF_AM + 16384;      // L fp32 [64][LP]; then T | T diag(gamma)
 constexpr uint32_t OFF_NF = OFF_LF + C * LP * 4; // (I + L)^{-1} fp32 [64][LP]
-constexpr uint32_t OFF_PF = OFF_NF + C * LP * 4; // solve scratch: 4 x [16][PP] fp32
-constexpr uint32_t OFF_SG = OFF_PF + 4 * 16 * PP * 4;  // state's copy of gamma[64], kdec[64]
+constexpr uint32_t OFF_SG = OFF_NF + C * LP * 4;  // state's copy of gamma[64], kdec[64]
 constexpr uint32_t OFF_BAR = OFF_SG + 2 * C * 4;
 constexpr uint32_t SMEM_USED = OFF_BAR + 128;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for the 1024-byte alignment
@@ -208,12 +206,11 @@ __device__ __forceinline__ void store_row32_sw128(unsigned char *block, int row,
 
 // Nf = (I + L)^{-1} for the strictly lower-triangular 64x64 L in Lf (fp32, pitch LP),
 // by the 128 prep threads. 16x16 diagonal blocks by forward substitution in fp32 (one
-// column per thread), then the off-diagonal blocks by distance from the diagonal with
-// warp-level TF32 products. Only the lower triangle (with its unit diagonal) of Nf is
-// written, and only the strictly lower triangle of Lf is read.
-__device__ __forceinline__ void unit_lower_inverse(const float *__restrict__ Lf,
-                                                   float *__restrict__ Nf, float *__restrict__ Pf,
-                                                   int ptid) {
+// column per thread), then the off-diagonal blocks with warp-level TF32 products. Only
+// the lower triangle (with its unit diagonal) of Nf is written; Lf's strictly lower
+// off-diagonal blocks are overwritten on the way.
+__device__ __forceinline__ void unit_lower_inverse(float *__restrict__ Lf,
+                                                   float *__restrict__ Nf, int ptid) {
     if (ptid < C) {
         const int base = 16 * (ptid >> 4), c = ptid & 15;
         float x[16];
@@ -228,22 +225,35 @@ __device__ __forceinline__ void unit_lower_inverse(const float *__restrict__ Lf,
         for (int r = 0; r < 16; ++r) Nf[(base + r) * LP + base + c] = x[r];
     }
     named_sync(kBarPrep, kPrepThreads);
-    // Off-diagonal blocks by distance d from the diagonal, N_ij = -N_ii sum_{k=j}^{i-1} L_ik N_kj:
-    // one warp per block; the sum goes through the warp's scratch block Pw.
+    // Off-diagonal blocks. With M_ik = N_ii L_ik (i > k), N_ij = -sum_{k=j}^{i-1} M_ik N_kj:
+    // first all six M blocks in one round (written over the L blocks, which are not read
+    // again), then the blocks by distance from the diagonal, each by one warp as a
+    // single chain of accumulated products.
     const int w = ptid >> 5, lane = ptid & 31;
-    float *Pw = Pf + w * 16 * PP;
+    float *__restrict__ Mf = Lf;
+    {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int b = w + 4 * r;  // blocks (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
+            if (b < 6) {
+                const int i = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+                const int k = b < 3 ? b : (b < 5 ? b - 3 : 0);
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                warp_gemm16(Nf + 16 * i * LP + 16 * i, LP, Lf + 16 * i * LP + 16 * k, LP, acc, lane);
+                __syncwarp();
+                warp_store16(Mf + 16 * i * LP + 16 * k, LP, acc, lane, 1.f);
+            }
+        }
+    }
+    named_sync(kBarPrep, kPrepThreads);
 #pragma unroll
     for (int d = 1; d < 4; ++d) {
         if (w < 4 - d) {
             const int i = d + w, j = w;
             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             for (int k = j; k < i; ++k)
-                warp_gemm16(Lf + 16 * i * LP + 16 * k, LP, Nf + 16 * k * LP + 16 * j, LP, acc, lane);
-            warp_store16(Pw, PP, acc, lane, 1.f);
-            __syncwarp();
-            float res[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            warp_gemm16(Nf + 16 * i * LP + 16 * i, LP, Pw, PP, res, lane);
-            warp_store16(Nf + 16 * i * LP + 16 * j, LP, res, lane, -1.f);
+                warp_gemm16(Mf + 16 * i * LP + 16 * k, LP, Nf + 16 * k * LP + 16 * j, LP, acc, lane);
+            warp_store16(Nf + 16 * i * LP + 16 * j, LP, acc, lane, -1.f);
         }
         named_sync(kBarPrep, kPrepThreads);
     }
@@ -440,7 +450,6 @@ tc_prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         float *__restrict__ Lf = reinterpret_cast<float *>(sm + OFF_LF);
         float *__restrict__ Nf = reinterpret_cast<float *>(sm + OFF_NF);
-        float *__restrict__ Pf = reinterpret_cast<float *>(sm + OFF_PF);
         auto check = [&](bool ok) -> bool {  // role-wide agreement after a wait
             if (!ok) { *fail = 1; flags[2] = 1; }
             named_sync(kBarPrep, kPrepThreads);
@@ -518,7 +527,7 @@ tc_prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             named_sync(kBarPrep, kPrepThreads);
 
             // ---- T = (I + L)^{-1} diag(beta) and T diag(gamma), bf16, over L's space
-            unit_lower_inverse(Lf, Nf, Pf, ptid);
+            unit_lower_inverse(Lf, Nf, ptid);
             {
                 const int t = ptid >> 1, hh = ptid & 1;
                 float tv[32], tg[32];
