@@ -38,6 +38,11 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
         off = align_up(off + sizeof(float) * per * kChunk, 256);
         L.g = off;  // gamma and kdec per chunk
         off = align_up(off + sizeof(float) * per * 2, 256);
+    } else {
+        L.T = off;  // two 64x64 bf16 matrices per (chunk, head)
+        off = align_up(off + (size_t)L.max_chunks * (size_t)H * 2 * kChunk * kChunk * 2, 256);
+        L.G = off;  // 256 floats per (chunk, head)
+        off = align_up(off + (size_t)L.max_chunks * (size_t)H * 256 * sizeof(float), 256);
     }
     L.total = off;
     return L;

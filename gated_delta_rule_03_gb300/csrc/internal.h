@@ -33,6 +33,8 @@ struct WsLayout {
     size_t plan;          // int4[max_chunks]: (sequence, first token, tokens, chunk index)
     size_t seq_chunk;     // int32[num_seqs + 1]: first chunk of each sequence
     size_t W, U, A, g;    // fp32 per-chunk intermediates of the exact path (g: gamma, kdec)
+    size_t T;             // tensor-core path: bf16 [max_chunks * H][2][64][64] T' and A^T per unit
+    size_t G;             // tensor-core path: fp32 [max_chunks * H][256] decay factors per unit
     size_t total;
     bool tensor_path;     // bf16 tensor-core kernel (true) or exact fp32-arithmetic kernels
 };

@@ -1,5 +1,7 @@
 // prefill_tc.cu -- chunked prefill of the gated delta rule on the 5th-generation tensor
-// cores (tcgen05), for bf16 q/k/v with d_k = 128 and d_v a multiple of 128.
+// cores (tcgen05), for bf16 q/k/v with d_k = 128 and d_v a multiple of 128: the
+// sequential chain over the chunks of each (sequence, head), and the host launcher of
+// the whole tensor-core path.
 //
 // What it computes is the chunk form of the recurrence: the chunk algorithm of
 // "Attention as Matrix Algebra: From Softmax to the Delta Rule", section 8
@@ -10,258 +12,127 @@
 //   Utilde = T V,  W = T diag(gamma) K,  U = Utilde - W S
 //   O = diag(gamma) Q S + (Q K^T . Gamma . [i <= t]) U
 //   S <- gamma_C S + Ktilde^T U,  Ktilde_i = exp(g_C - g_i) k_i
-//
-// Work mapping. One CTA per (sequence, head, 128-column slice of d_v); the value
-// columns of S evolve independently. Every dense product is a tcgen05.mma chain with
-// bf16 operands in 128-byte-swizzled shared memory and fp32 accumulators in TMEM,
-// in the transposed orientation so that M is always 128:
-//   G      = [K; Q] K^T                       (M=128: 64 keys then 64 queries; N=64)
-//   U~^T   = V^T T^T,  W^T = K^T (T diag gamma)^T                       (N=64, K=64)
-//   (WS)^T = S^T W^T,  O^T = S^T (diag(gamma) Q)^T                      (N=64, K=128)
-//   S_upd^T = U^T Ktilde,  O^T += U^T A^T                         (N=128|64, K=64)
-// q, k and v arrive by TMA as 64x64 bf16 boxes; the same tiles serve as K-major
-// operands (Gram) and as MN-major operands (products over tokens).
-//
-// Warp roles (16 warps; an SM sub-partition holds one warp of each warpgroup), one
-// pipeline:
-//   warp 0      producer: TMA loads of q, k, v and the gates of chunk c into one of
-//               two stages; cumulative log-decay by a warp scan. (Warps 1-3 idle.)
-//   warps 4-7   "prep" (everything that does not depend on S): G, the masked L and A,
-//               the unit lower-triangular solve (fp32, CUDA cores), T and
-//               T diag(gamma), U~ and W, W^T to shared memory, and the in-place
-//               scaling of the stage's Q rows by gamma and K rows by exp(g_C - g).
-//               Its own elected thread issues G and U~/W.
-//   warps 8-15  "state" (the sequential chain): WS, U = U~ - WS, S_upd, the bf16 copy
-//               of S^T that feeds the next chunk, and the outputs. The fp32 master S^T
-//               lives in TMEM: while WS runs it is scaled by gamma_C in place, and
-//               S_upd accumulates U^T Ktilde onto it. Its own elected thread issues
-//               WS, QS, S_upd and AU.
-// Prep runs up to one chunk ahead of state, so the state chain -- WS, U, S_upd, the
-// state update -- is the critical path per chunk.
+// The chunk-parallel part -- L and the triangular solve, giving T -- runs first, for all
+// chunks at once (solve_tc.cu). This file holds everything that follows it.
 //
 // Two equivalent forms of the decay factors, chosen per chunk:
 //  * ratio form, when the chunk's cumulative log-decay g_C (its minimum) stays above
-//    -80 so that gamma and 1/gamma are finite normal floats: Gamma_ti = gamma_t / gamma_i
-//    needs no per-entry exponential, and the decay moves off Q and K entirely --
-//      A U = (1/gamma_C) (Q K^T . [i <= t]) (diag(kdec) U),  S_upd = K^T (diag(kdec) U),
-//      O_t = gamma_t ((S^T q_t) + ((A U)_t)/gamma_t) computed as gamma_t times the
-//      accumulator of Q S + (1/gamma_C)(masked Q K^T)(diag(kdec) U),
-//    with kdec_t = exp(g_C - g_t); q, k stay as loaded.
-//  * exponential form otherwise: Gamma_ti = exp(g_t - g_i) per entry (exponents <= 0),
+//    -80 so that gamma and 1/gamma are finite normal floats. With kdec_t = exp(g_C - g_t)
+//    and U' = diag(kdec) U the decay moves off Q and K:
+//      T' = diag(kdec) T,  U' = T' V - T' diag(gamma) K S,  S_upd = K^T U',
+//      O_t = gamma_t [ (S^T q_t) + (1/gamma_C) ((Q K^T . [i <= t]) U')_t ].
+//  * exponential form otherwise: T' = T, U' = U, Gamma_ti = exp(g_t - g_i) per entry,
 //    and the stage's Q rows are scaled by gamma and K rows by kdec in place.
 // Both compute the same products; only the placement of the decay factors differs.
-// Padding rows of a partial last chunk get beta = 0 and log alpha = 0: their rows of
-// T, W, U~ and U are zero, they change nothing and they are not stored.
+//
+// Work mapping. One CTA per (sequence, head, 128-column slice of d_v); the value columns
+// of S evolve independently. Every dense product is a tcgen05.mma chain with fp32
+// accumulators in TMEM and bf16 operands either in 128-byte-swizzled shared memory or,
+// for the two operands the chain itself produces (S^T and U'^T), in TMEM. A tcgen05.mma
+// instruction costs about as much to issue whatever its N, so products that share an
+// operand are issued as one wide chain:
+//   U'~^T       = V^T T'^T,  W'^T = K^T (T' diag gamma)^T           (N = 64, K = 64)
+//   [O^T | X^T] = S^T [Q; -W']^T               (A = S^T from TMEM;  N = 128, K = d_k)
+//   [S^T | O^T] += U'^T [K | A^T]              (A = U'^T from TMEM; N = 192, K = 64)
+// with U' = U'~ + X, all with M = d_v = 128. A^T (the causal, decay-weighted key-query
+// products), T' and the chunk's decay factors (g, gamma, kdec and the form) come from
+// the solve. Two tiles change orientation on the way (-W'^T into -W' rows next to Q,
+// and O^T into o rows): both are read from TMEM in the m16n8 fragment layout and
+// written transposed with stmatrix; o leaves by TMA store.
+//
+// Loads. Each input goes into a ring of its own, freed as soon as its last reader is
+// done, so that the next chunks load while this one is worked on:
+//   V, T'            2 slots, freed when U'~ and W' are done;
+//   K, A^T, factors  3 slots, freed when the chunk is done;
+//   Q (and -W')      2 slots, freed when [QS | WS] is done.
+//
+// Warp roles (17 warps; TMEM lane quarter = warp % 4):
+//   warps 0-3   epilogue: O^T of chunk c from TMEM (times gamma_t in the ratio form),
+//               transposed into a staging tile, stored by TMA.
+//   warps 4-7   prep: T' diag(gamma), U'~ and W' (its elected thread issues them), -W'
+//               into the Q slot, the in-place scaling of Q and K (exponential form).
+//   warps 8-15  state, the sequential chain: the bf16 S^T and U'^T operands in TMEM,
+//               [S_upd | AU], the decay of the fp32 master S^T (in TMEM); its elected
+//               thread issues both state chains.
+//   warp 16     producer: the TMA and bulk loads of the three rings, in chunk order, each
+//               as soon as its slot is free.
+// The critical path per chunk is: S^T copy -> [QS | WS] -> U'^T copy -> [S_upd | AU].
+// The decay of the master by the next chunk's gamma_C runs while [QS | WS] does.
+// Padding rows of a partial last chunk get log alpha = 0 and beta = 0: their rows of
+// T', W', U' are zero, they change nothing and they are not stored.
 // Every wait is bounded; a role that gives up marks the call GDR_ERR_DEVICE_TIMEOUT in
 // the status word, and the others give up in turn, drain and free TMEM.
 #include <mutex>
 
-#include "internal.h"
-#include "sm100.cuh"
+#include "tc_common.cuh"
 
 namespace gdr {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
 constexpr int C = kChunk;   // 64 tokens per chunk
 constexpr int DK = 128;     // key dimension
 constexpr int NV = 128;     // value columns per CTA
-constexpr int kWarps = 16;
+constexpr int kWarps = 17;
 constexpr int kThreads = kWarps * 32;
-constexpr int kPrepWarp0 = 4, kPrepThreads = 128;
-constexpr int kStateWarp0 = 8, kStateThreads = 256;
-constexpr int kBarPrep = 1, kBarState = 2;  // named barrier ids
-constexpr int LP = C + 1;                   // fp32 pitch of the solve matrices
+constexpr int kEpiThreads = 128;                      // warps 0-3
+constexpr int kPrepWarp0 = 4, kPrepThreads = 128;     // warps 4-7
+constexpr int kStateWarp0 = 8, kStateThreads = 256;   // warps 8-15
+constexpr int kProducerWarp = 16;
+constexpr int kBarPrep = 1, kBarState = 2, kBarEpi = 3;  // named barrier ids
 
-// Shared memory map (bytes from a 1024-aligned base). A stage holds one chunk's inputs.
-constexpr uint32_t STAGE_BYTES = 51200;
-constexpr uint32_t ST_KQ = 0;        // K_b0 | Q_b0 | K_b1 | Q_b1, 8 KB each (b = d_k half)
-constexpr uint32_t ST_V = 32768;     // V_b0 | V_b1 (b = half of this CTA's d_v slice)
-constexpr uint32_t ST_GATE = 49152;  // fp32 g, gamma, beta, kdec = exp(g_C - g), 1/gamma [64 each]
-constexpr int G_G = 0, G_GAM = 64, G_BETA = 128, G_KDEC = 192, G_GINV = 256;  // float offsets
-// Gamma_ti = gamma_t / gamma_i exactly when no gamma underflows: the chunk's cumulative
-// decay g_C (its minimum, since log alpha <= 0) stays above this bound. Otherwise each
-// Gamma_ti is its own exponential of g_t - g_i <= 0.
-constexpr float kRatioSafeLogDecay = -80.f;
-constexpr uint32_t OFF_ST = 2 * STAGE_BYTES;     // S^T bf16 [d_v 128][d_k 128], two K-blocks
-constexpr uint32_t OFF_WT = OFF_ST + 32768;      // W^T bf16 [d_k 128][t 64]
-constexpr uint32_t OFF_UT = OFF_WT + 16384;      // U^T bf16 [d_v 128][t 64]; output staging
-constexpr uint32_t OFF_AM = OFF_UT + 16384;      // A bf16 [t][i], two 8 KB buffers
-constexpr uint32_t OFF_LF = OFF_AM + 16384;      // L fp32 [64][LP]; then T | T diag(gamma)
-constexpr uint32_t OFF_NF = OFF_LF + C * LP * 4; // (I + L)^{-1} fp32 [64][LP]
-constexpr uint32_t OFF_SG = OFF_NF + C * LP * 4;  // state's copy of gamma[64], kdec[64]
-constexpr uint32_t OFF_BAR = OFF_SG + 2 * C * 4;
-constexpr uint32_t SMEM_USED = OFF_BAR + 128;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for the 1024-byte alignment
-static_assert(OFF_LF % 1024 == 0 && OFF_ST % 1024 == 0 && STAGE_BYTES % 1024 == 0, "alignment");
-static_assert(SMEM_BYTES <= 232448, "shared memory");
+// Shared memory map (bytes from a 1024-aligned base).
+constexpr uint32_t RQ = 0, RQ_SLOT = 32768;        // per d_k half b (16 KB): Q_b then -W'_b
+constexpr uint32_t RK = 65536, RK_SLOT = 25600;    // K_b0 | K_b1 | A^T (8 KB each) | factors
+constexpr uint32_t RK_A = 16384, RK_G = 24576;     // offsets of A^T and the factors in a K slot
+constexpr uint32_t RV = RK + 3 * RK_SLOT, RV_SLOT = 24576;  // V_b0 | V_b1 | T'
+constexpr uint32_t RV_T = 16384;
+constexpr int G_GAM = 64, G_KDEC = 128, G_FORM = 192;  // float offsets in the factors (g at 0)
+constexpr uint32_t OFF_TG = RV + 2 * RV_SLOT;   // T' diag(gamma) bf16 [t][i]
+constexpr uint32_t OFF_OST = OFF_TG + 8192;     // output staging [t][128]: two 8 KB tiles
+constexpr uint32_t OFF_EG = OFF_OST + 16384;    // epilogue gates: gamma[4][64], form flag[4]
+constexpr uint32_t OFF_BAR = OFF_EG + 2048;
+static_assert(RK % 1024 == 0 && RK_SLOT % 1024 == 0 && RV % 1024 == 0 && OFF_TG % 1024 == 0 &&
+                  OFF_OST % 1024 == 0,
+              "alignment");
 
 // mbarrier slots at OFF_BAR (8 bytes each), then the TMEM slot and role flags.
 enum {
-    B_FULL0 = 0, B_FULL1,    // producer -> prep/state: stage loaded (tx bytes + gates)
-    B_EMPTY0, B_EMPTY1,      // state -> producer: stage free again
-    B_G,                     // G done                        (prep issuer commit)
-    B_UW0, B_UW1,            // U~ (buffer c%2) and W done     (prep issuer commit)
-    B_WQ,                    // W^T stored, Q/K scaled         (128 prep arrivals)
-    B_WS,                    // WS done                        (state issuer commit)
-    B_S,                     // S_upd done                     (state issuer commit)
-    B_O,                     // QS + AU done                   (state issuer commit)
+    B_QF0 = 0, B_QF1,        // Q slot loaded                              (tx bytes)
+    B_QE0, B_QE1,            // Q slot free: [QS | WS] done                (state issuer commit)
+    B_KF0, B_KF1, B_KF2,     // K slot loaded                              (tx bytes)
+    B_KE0, B_KE1, B_KE2,     // K slot free: chunk done (prep 128 arrivals + state commit)
+    B_VF0, B_VF1,            // V slot loaded                              (tx bytes)
+    B_VE0, B_VE1,            // V slot free: U'~ and W' done               (prep issuer commit)
+    B_UW0, B_UW1,            // U'~ (buffer c%2) and W' of chunk c done   (prep issuer commit)
+    B_WQ0, B_WQ1,            // -W' of chunk c stored, Q/K scaled          (128 prep arrivals)
+    B_WS,                    // [QS | WS] done                             (state issuer commit)
+    B_SO,                    // [S_upd | AU] done                          (state issuer commit)
+    B_OFREE,                 // O read by the epilogue                     (128 arrivals)
+    B_UFREE0, B_UFREE1,      // U'~ buffer read by the state               (state issuer)
+    B_EG0, B_EG1, B_EG2, B_EG3,  // epilogue gates of chunk c in slot c%4  (128 prep arrivals)
     B_DRAIN0, B_DRAIN1,      // drain after an abort
     B_COUNT
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * B_COUNT;
-constexpr uint32_t OFF_FLAGS = OFF_TMEM_SLOT + 4;  // int: prep_fail, state_fail, any_fail
+constexpr uint32_t OFF_FLAGS = OFF_TMEM_SLOT + 4;  // int: prep, state, epilogue, any failure
+constexpr uint32_t SMEM_USED = OFF_FLAGS + 16;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for the 1024-byte alignment
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
-// TMEM columns (fp32 over 128 lanes; TM_S holds the master state S^T).
-constexpr uint32_t TM_G = 0, TM_U = 64 /* two buffers */, TM_W = 192, TM_WS = 256, TM_O = 320,
-                   TM_S = 384, TM_COLS = 512;
+// TMEM columns (fp32 over 128 lanes unless noted). [S | O] and [O | X] are each one
+// MMA's D; U'^T (bf16 pairs) is written over X once X has been read.
+constexpr uint32_t TM_S = 0, TM_O = 128, TM_X = 192, TM_U = 256 /* two buffers */, TM_W = 384,
+                   TM_SA = 448 /* S^T as bf16 pairs */, TM_COLS = 512;
 
-constexpr uint32_t TMA_BYTES = 6 * 64 * 64 * 2;  // K, Q, V: two 64x64 bf16 boxes each
-
-__device__ __forceinline__ void named_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// exp(x) through the hardware base-2 exponential (flushes subnormal results to zero).
-__device__ __forceinline__ float fast_exp(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
-    return y;
-}
-
-// ---------------------------------------------------------------- warp-level 16x16 products
-// The unit lower-triangular solve combines 16x16 blocks. These products are far below
-// the tensor-core MMA's minimum tile (M = 64) and sit on a short dependency chain, so
-// they use the warp-synchronous m16n8k8 TF32 MMA with fp32 accumulation (operands
-// rounded to TF32, 2^-11 relative; the solve's result is rounded to bf16 afterwards).
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4],
-                                                const uint32_t (&b)[2]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// d (+)= A * B for 16x16 row-major blocks A (pitch pa) and B (pitch pb); d holds the
-// result's two 16x8 halves in the m16n8 accumulator layout.
-__device__ __forceinline__ void warp_gemm16(const float *__restrict__ A, int pa,
-                                            const float *__restrict__ B, int pb, float (&d)[2][4],
-                                            int lane) {
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-        const uint32_t a[4] = {to_tf32(A[g * pa + 8 * ks + q]), to_tf32(A[(g + 8) * pa + 8 * ks + q]),
-                               to_tf32(A[g * pa + 8 * ks + q + 4]),
-                               to_tf32(A[(g + 8) * pa + 8 * ks + q + 4])};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t b[2] = {to_tf32(B[(8 * ks + q) * pb + 8 * nt + g]),
-                                   to_tf32(B[(8 * ks + q + 4) * pb + 8 * nt + g])};
-            mma_tf32_16x8x8(d[nt], a, b);
-        }
-    }
-}
-
-// M = scale * d for a 16x16 row-major block M (pitch pm).
-__device__ __forceinline__ void warp_store16(float *__restrict__ M, int pm, const float (&d)[2][4],
-                                             int lane, float scale) {
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        M[g * pm + 8 * nt + 2 * q] = scale * d[nt][0];
-        M[g * pm + 8 * nt + 2 * q + 1] = scale * d[nt][1];
-        M[(g + 8) * pm + 8 * nt + 2 * q] = scale * d[nt][2];
-        M[(g + 8) * pm + 8 * nt + 2 * q + 1] = scale * d[nt][3];
-    }
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// Writes 32 fp32 values as bf16 into columns [32*half, 32*half + 32) of row `row` of a
-// 128-byte-swizzled block of 64-wide rows.
-__device__ __forceinline__ void store_row32_sw128(unsigned char *block, int row, int half,
-                                                  const float (&v)[32]) {
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-        const int chunk = 4 * half + jj;
-        uint4 w;
-        w.x = pack_bf16x2(v[8 * jj + 0], v[8 * jj + 1]);
-        w.y = pack_bf16x2(v[8 * jj + 2], v[8 * jj + 3]);
-        w.z = pack_bf16x2(v[8 * jj + 4], v[8 * jj + 5]);
-        w.w = pack_bf16x2(v[8 * jj + 6], v[8 * jj + 7]);
-        *reinterpret_cast<uint4 *>(block + row * 128 + (((chunk ^ row) & 7) << 4)) = w;
-    }
-}
-
-// Nf = (I + L)^{-1} for the strictly lower-triangular 64x64 L in Lf (fp32, pitch LP),
-// by the 128 prep threads. 16x16 diagonal blocks by forward substitution in fp32 (one
-// column per thread), then the off-diagonal blocks with warp-level TF32 products. Only
-// the lower triangle (with its unit diagonal) of Nf is written; Lf's strictly lower
-// off-diagonal blocks are overwritten on the way.
-__device__ __forceinline__ void unit_lower_inverse(float *__restrict__ Lf,
-                                                   float *__restrict__ Nf, int ptid) {
-    if (ptid < C) {
-        const int base = 16 * (ptid >> 4), c = ptid & 15;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float s = (r == c) ? 1.f : 0.f;
-#pragma unroll
-            for (int k = 0; k < r; ++k) s = fmaf(-Lf[(base + r) * LP + base + k], x[k], s);
-            x[r] = s;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Nf[(base + r) * LP + base + c] = x[r];
-    }
-    named_sync(kBarPrep, kPrepThreads);
-    // Off-diagonal blocks. With M_ik = N_ii L_ik (i > k), N_ij = -sum_{k=j}^{i-1} M_ik N_kj:
-    // first all six M blocks in one round (written over the L blocks, which are not read
-    // again), then the blocks by distance from the diagonal, each by one warp as a
-    // single chain of accumulated products.
-    const int w = ptid >> 5, lane = ptid & 31;
-    float *__restrict__ Mf = Lf;
-    {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int b = w + 4 * r;  // blocks (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
-            if (b < 6) {
-                const int i = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
-                const int k = b < 3 ? b : (b < 5 ? b - 3 : 0);
-                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                warp_gemm16(Nf + 16 * i * LP + 16 * i, LP, Lf + 16 * i * LP + 16 * k, LP, acc, lane);
-                __syncwarp();
-                warp_store16(Mf + 16 * i * LP + 16 * k, LP, acc, lane, 1.f);
-            }
-        }
-    }
-    named_sync(kBarPrep, kPrepThreads);
-#pragma unroll
-    for (int d = 1; d < 4; ++d) {
-        if (w < 4 - d) {
-            const int i = d + w, j = w;
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            for (int k = j; k < i; ++k)
-                warp_gemm16(Mf + 16 * i * LP + 16 * k, LP, Nf + 16 * k * LP + 16 * j, LP, acc, lane);
-            warp_store16(Nf + 16 * i * LP + 16 * j, LP, acc, lane, -1.f);
-        }
-        named_sync(kBarPrep, kPrepThreads);
-    }
-}
 
 struct TcParams {
-    const float *log_alpha, *beta, *S0;
+    const float *S0;
+    const float *factors;      // per solve unit: g, gamma, kdec, form (256 floats)
     const int32_t *cu_seqlens;
+    const int32_t *seq_chunk;  // first chunk of each sequence (planning kernel)
     int64_t num_seqs, total_tokens;
     int H, dv, n_slices;
     __nv_bfloat16 *o;
@@ -269,63 +140,47 @@ struct TcParams {
     int32_t *ctl;
 };
 
-// MMA issue helpers (one thread). Descriptors per the layouts described above.
-__device__ __forceinline__ void issue_gram(uint32_t tmem, uint32_t kq) {
+// Shared address of the 16-byte row segment (row r, 8 columns from c8*8) of a
+// 128-byte-swizzled block of 64-wide bf16 rows.
+__device__ __forceinline__ uint32_t sw128_seg(uint32_t block, int r, int c8) {
+    return block + (uint32_t)(r * 128 + (((c8 ^ r) & 7) << 4));
+}
+
+// Writes a 16-lane x 64-column fp32 TMEM tile (fragment registers of
+// tmem_load_16x256b_x8, times `scale`) transposed: the element at (lane l, column t) goes
+// to row t, column l of 128-byte-swizzled bf16 rows. row_block(l8) gives the block that
+// holds the 8-column segment starting at lane l8 and its segment index within the row.
+template <typename RowBlock>
+__device__ __forceinline__ void transpose_store16(const uint32_t (&r)[32], float scale_sign,
+                                                  const float *col_scale, int lane, int l0,
+                                                  RowBlock row_block) {
+    const int i = lane >> 3, rr = lane & 7;  // this thread addresses row rr of matrix i
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = kq + (kk >> 2) * 16384 + (kk & 3) * 32;
-        mma_bf16(tmem + TM_G, sw128_desc(off, 16, 1024), sw128_desc(off, 16, 1024),
-                 idesc_bf16(128, 64, 0, 0), kk > 0);
+    for (int jj = 0; jj < 4; ++jj) {
+        uint32_t p[4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int j = 2 * jj + m;  // column block
+            const int t0 = 8 * j + 2 * (lane & 3);
+            const float s0 = col_scale ? col_scale[t0] * scale_sign : scale_sign;
+            const float s1 = col_scale ? col_scale[t0 + 1] * scale_sign : scale_sign;
+            p[2 * m] = pack_bf16x2(__uint_as_float(r[4 * j]) * s0, __uint_as_float(r[4 * j + 1]) * s1);
+            p[2 * m + 1] = pack_bf16x2(__uint_as_float(r[4 * j + 2]) * s0, __uint_as_float(r[4 * j + 3]) * s1);
+        }
+        // matrix i: lanes l0 + 8(i & 1) .. +7, columns 8(2jj + (i >> 1)) .. +7
+        const int row = 8 * (2 * jj + (i >> 1)) + rr;
+        uint32_t block;
+        int c8;
+        row_block(l0 + 8 * (i & 1), block, c8);
+        stmatrix_x4_trans(sw128_seg(block, row, c8), p[0], p[1], p[2], p[3]);
     }
 }
 
-__device__ __forceinline__ void issue_uw(uint32_t tmem, uint32_t kq, uint32_t v, uint32_t tm,
-                                         uint32_t tg, uint32_t ubuf) {
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(tmem + TM_U + 64 * ubuf, sw128_desc(v + kk * 2048, 8192, 1024),
-                 sw128_desc(tm + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(tmem + TM_W, sw128_desc(kq + kk * 2048, 16384, 1024),
-                 sw128_desc(tg + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
-}
-
-__device__ __forceinline__ void issue_ws(uint32_t tmem, uint32_t st, uint32_t wt) {
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tmem + TM_WS, sw128_desc(st + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sw128_desc(wt + kk * 2048, 8192, 1024), idesc_bf16(128, 64, 0, 1), kk > 0);
-}
-
-__device__ __forceinline__ void issue_qs(uint32_t tmem, uint32_t st, uint32_t kq) {
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tmem + TM_O, sw128_desc(st + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sw128_desc(kq + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32, 16, 1024),
-                 idesc_bf16(128, 64, 0, 0), kk > 0);
-}
-
-__device__ __forceinline__ void issue_supd_au(uint32_t tmem, uint32_t ut, uint32_t kq,
-                                              uint32_t am, uint32_t bar_s, uint32_t bar_empty,
-                                              uint32_t bar_o) {
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(tmem + TM_S, sw128_desc(ut + kk * 32, 16, 1024),
-                 sw128_desc(kq + kk * 2048, 16384, 1024), idesc_bf16(128, 128, 0, 1), 1);
-    mma_commit(bar_s);
-    mma_commit(bar_empty);  // S_upd and the earlier QS were the stage's last readers
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(tmem + TM_O, sw128_desc(ut + kk * 32, 16, 1024), sw128_desc(am + kk * 32, 16, 1024),
-                 idesc_bf16(128, 64, 0, 0), 1);
-    mma_commit(bar_o);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
-tc_prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v, const TcParams p) {
-    if (p.ctl[0] != GDR_OK) return;  // cu_seqlens rejected by the planning kernel
+tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_t,
+                const __grid_constant__ CUtensorMap map_o, const TcParams p) {
+    if (p.ctl[0] != GDR_OK) return;  // cu_seqlens rejected, or the solve gave up
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte aligned base, derived from the shared array itself so that every access
     // through it stays a shared-memory access the compiler can schedule freely
@@ -334,7 +189,8 @@ tc_prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TMEM_SLOT);
-    volatile int *flags = reinterpret_cast<volatile int *>(sm + OFF_FLAGS);  // prep, state, any
+    volatile int *flags = reinterpret_cast<volatile int *>(sm + OFF_FLAGS);
+    auto note_fail = [&](int role) { flags[role] = 1; flags[3] = 1; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -352,26 +208,41 @@ tc_prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     }
     const int n_chunks = (int)((seq_end - seq_begin + C - 1) / C);
     const int col0 = slice * NV;  // first value column of this CTA
+    auto chunk_len = [&](int c) {
+        const int64_t rem = seq_end - (seq_begin + (int64_t)c * C);
+        return (int)(rem < C ? rem : C);
+    };
+    // ring slots of chunk c
+    auto qslot = [&](int c) { return (uint32_t)(RQ + (c & 1) * RQ_SLOT); };
+    auto kslot = [&](int c) { return (uint32_t)(RK + (c % 3) * RK_SLOT); };
+    auto vslot = [&](int c) { return (uint32_t)(RV + (c & 1) * RV_SLOT); };
 
     if (tid == 0) {
-        mbar_init(bar(B_FULL0), 2);
-        mbar_init(bar(B_FULL1), 2);
-        mbar_init(bar(B_EMPTY0), 2);
-        mbar_init(bar(B_EMPTY1), 2);
-        mbar_init(bar(B_G), 1);
-        mbar_init(bar(B_UW0), 1);
-        mbar_init(bar(B_UW1), 1);
-        mbar_init(bar(B_WQ), kPrepThreads);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_QF0 + i), 1);
+            mbar_init(bar(B_QE0 + i), 1);
+            mbar_init(bar(B_VF0 + i), 1);
+            mbar_init(bar(B_VE0 + i), 1);
+            mbar_init(bar(B_UW0 + i), 1);
+            mbar_init(bar(B_WQ0 + i), kPrepThreads);
+            mbar_init(bar(B_UFREE0 + i), 1);
+            mbar_init(bar(B_DRAIN0 + i), 1);
+        }
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(bar(B_KF0 + i), 1);
+            mbar_init(bar(B_KE0 + i), kPrepThreads + 1);
+        }
+        for (int i = 0; i < 4; ++i) mbar_init(bar(B_EG0 + i), kPrepThreads);
         mbar_init(bar(B_WS), 1);
-        mbar_init(bar(B_S), 1);
-        mbar_init(bar(B_O), 1);
-        mbar_init(bar(B_DRAIN0), 1);
-        mbar_init(bar(B_DRAIN1), 1);
+        mbar_init(bar(B_SO), 1);
+        mbar_init(bar(B_OFREE), kEpiThreads);
         fence_mbar_init();
-        flags[0] = flags[1] = flags[2] = 0;
+        flags[0] = flags[1] = flags[2] = flags[3] = 0;
         prefetch_tensormap(&map_q);
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_v);
+        prefetch_tensormap(&map_t);
+        prefetch_tensormap(&map_o);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), TM_COLS);
@@ -381,237 +252,210 @@ tc_prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    float *__restrict__ eg = reinterpret_cast<float *>(sm + OFF_EG);  // gamma[4][64], flag[4]
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ============================================================ producer
-        for (int c = 0; c < n_chunks; ++c) {
-            const int s = c & 1, u = c >> 1;
-            const uint32_t stage = sbase + s * STAGE_BYTES;
-            bool ok = true;
-            if (c >= 2 && lane == 0) ok = mbar_wait(bar(B_EMPTY0 + s), (u - 1) & 1);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) {
-                flags[2] = 1;
-                break;
+        if (lane == 0) {
+            const int unit0 = p.seq_chunk[n] * p.H + h;  // chunk c is solve unit unit0 + c * H
+            for (int c = 0; c < n_chunks; ++c) {
+                const int tt = (int)(seq_begin + (int64_t)c * C), unit = unit0 + c * p.H;
+                // V, T' (slot free once U'~ and W' of chunk c - 2 are done)
+                if (c >= 2 && !mbar_wait(bar(B_VE0 + (c & 1)), ((c >> 1) - 1) & 1)) { note_fail(3); break; }
+                const uint32_t vs = sbase + vslot(c), vf = bar(B_VF0 + (c & 1));
+                mbar_arrive_expect_tx(vf, 3 * 8192);
+                tma_load_3d(vs, &map_v, vf, col0, h, tt);
+                tma_load_3d(vs + 8192, &map_v, vf, col0 + 64, h, tt);
+                tma_load_3d(vs + RV_T, &map_t, vf, 0, 0, 2 * unit);
+                // K, A^T, factors (slot free once chunk c - 3 is done)
+                if (c >= 3 && !mbar_wait(bar(B_KE0 + c % 3), (c / 3 - 1) & 1)) { note_fail(3); break; }
+                const uint32_t ks = sbase + kslot(c), kf = bar(B_KF0 + c % 3);
+                mbar_arrive_expect_tx(kf, 3 * 8192 + 1024);
+                tma_load_3d(ks, &map_k, kf, 0, h, tt);
+                tma_load_3d(ks + 8192, &map_k, kf, 64, h, tt);
+                tma_load_3d(ks + RK_A, &map_t, kf, 0, 0, 2 * unit + 1);
+                bulk_load(ks + RK_G, p.factors + (size_t)unit * 256, 1024, kf);
+                // Q (slot free once [QS | WS] of chunk c - 2 is done)
+                if (c >= 2 && !mbar_wait(bar(B_QE0 + (c & 1)), ((c >> 1) - 1) & 1)) { note_fail(3); break; }
+                const uint32_t qs = sbase + qslot(c), qf = bar(B_QF0 + (c & 1));
+                mbar_arrive_expect_tx(qf, 2 * 8192);
+                tma_load_3d(qs, &map_q, qf, 0, h, tt);
+                tma_load_3d(qs + 16384, &map_q, qf, 64, h, tt);
             }
-            const int64_t t0 = seq_begin + (int64_t)c * C;
-            const int len = (int)((seq_end - t0) < C ? (seq_end - t0) : C);
-            if (lane == 0) {
-                const uint32_t fb = bar(B_FULL0 + s);
-                mbar_arrive_expect_tx(fb, TMA_BYTES);
-                const int tt = (int)t0;
-                tma_load_3d(stage + ST_KQ + 0, &map_k, fb, 0, h, tt);
-                tma_load_3d(stage + ST_KQ + 16384, &map_k, fb, 64, h, tt);
-                tma_load_3d(stage + ST_KQ + 8192, &map_q, fb, 0, h, tt);
-                tma_load_3d(stage + ST_KQ + 24576, &map_q, fb, 64, h, tt);
-                tma_load_3d(stage + ST_V + 0, &map_v, fb, col0, h, tt);
-                tma_load_3d(stage + ST_V + 8192, &map_v, fb, col0 + 64, h, tt);
-            }
-            // gates of tokens 2*lane and 2*lane + 1, cumulative log-decay by a warp scan
-            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-            if (2 * lane < len) {
-                const size_t off = (size_t)(t0 + 2 * lane) * p.H + h;
-                a0 = p.log_alpha[off];
-                b0 = p.beta[off];
-            }
-            if (2 * lane + 1 < len) {
-                const size_t off = (size_t)(t0 + 2 * lane + 1) * p.H + h;
-                a1 = p.log_alpha[off];
-                b1 = p.beta[off];
-            }
-            float sum = a0 + a1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float up = __shfl_up_sync(0xffffffffu, sum, off);
-                if (lane >= off) sum += up;
-            }
-            const float g0 = sum - a1, g1 = sum;
-            const float g_last = __shfl_sync(0xffffffffu, sum, 31);
-            float *gate = reinterpret_cast<float *>(sm + s * STAGE_BYTES + ST_GATE);
-            gate[G_G + 2 * lane] = g0;
-            gate[G_G + 2 * lane + 1] = g1;
-            gate[G_GAM + 2 * lane] = fast_exp(g0);
-            gate[G_GAM + 2 * lane + 1] = fast_exp(g1);
-            gate[G_BETA + 2 * lane] = b0;
-            gate[G_BETA + 2 * lane + 1] = b1;
-            gate[G_KDEC + 2 * lane] = fast_exp(g_last - g0);
-            gate[G_KDEC + 2 * lane + 1] = fast_exp(g_last - g1);
-            gate[G_GINV + 2 * lane] = fast_exp(-g0);
-            gate[G_GINV + 2 * lane + 1] = fast_exp(-g1);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_FULL0 + s));
         }
-    } else if (warp >= kPrepWarp0 && warp < kStateWarp0) {
+    } else if (warp < kPrepWarp0) {
+        // ============================================================ epilogue
+        const int etid = tid;
+        volatile int *fail = &flags[2];
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+        for (int c = 0; c < n_chunks; ++c) {
+            // Slot c%4 moves on to chunk c + 4 only after this role has read O of chunk
+            // c + 1, so the parity below is unambiguous.
+            const bool ok = mbar_wait(bar(B_EG0 + (c & 3)), (c >> 2) & 1) && mbar_wait(bar(B_SO), c & 1);
+            if (!ok) note_fail(2);
+            named_sync(kBarEpi, kEpiThreads);
+            if (*fail) break;
+            tc_fence_after();
+            uint32_t r0[32], r1[32];
+            tmem_load_16x256b_x8(lane_base + TM_O, r0);
+            tmem_load_16x256b_x8(lane_base + (16u << 16) + TM_O, r1);
+            tc_fence_before();
+            mbar_arrive(bar(B_OFREE));
+            // the staging tile: the TMA store of chunk c - 1 must have read it
+            if (etid == 0) bulk_wait_group_read<0>();
+            named_sync(kBarEpi, kEpiThreads);
+            const uint32_t stg = sbase + OFF_OST;
+            const bool ratio = eg[256 + (c & 3)] != 0.f;
+            const float *gam = ratio ? eg + 64 * (c & 3) : nullptr;
+            auto row_block = [&](int l8, uint32_t &block, int &c8) {
+                const int dv = 32 * warp + l8;  // value column within the slice
+                block = stg + (dv >> 6) * 8192;
+                c8 = (dv & 63) >> 3;
+            };
+            transpose_store16(r0, 1.f, gam, lane, 0, row_block);
+            transpose_store16(r1, 1.f, gam, lane, 16, row_block);
+            fence_async_smem();
+            named_sync(kBarEpi, kEpiThreads);
+            const int64_t t0 = seq_begin + (int64_t)c * C;
+            const int len = chunk_len(c);
+            if (len == C) {
+                if (etid == 0) {
+                    tma_store_3d(&map_o, stg, col0, h, (int)t0);
+                    tma_store_3d(&map_o, stg + 8192, col0 + 64, h, (int)t0);
+                    bulk_commit_group();
+                }
+            } else {  // a partial last chunk: only its own rows, by plain stores
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int idx = etid + k * kEpiThreads;  // 64 rows x 16 segments of 16 bytes
+                    const int row = idx >> 4, seg = idx & 15;
+                    if (row < len) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(
+                            sm + OFF_OST + (seg >> 3) * 8192 + row * 128 + ((((seg & 7) ^ row) & 7) << 4));
+                        *reinterpret_cast<uint4 *>(p.o + ((size_t)(t0 + row) * p.H + h) * p.dv + col0 +
+                                                   seg * 8) = v;
+                    }
+                }
+            }
+        }
+        if (etid == 0) bulk_wait_group_all();  // the stores have completed before exit
+    } else if (warp < kStateWarp0) {
         // ============================================================ prep
         const int ptid = tid - 32 * kPrepWarp0;
-        const int row = 32 * (warp & 3) + lane;  // this thread's TMEM lane
         const bool issuer = ptid == 0;
+        const int q = warp & 3;  // TMEM lane quarter
         volatile int *fail = &flags[0];
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        float *__restrict__ Lf = reinterpret_cast<float *>(sm + OFF_LF);
-        float *__restrict__ Nf = reinterpret_cast<float *>(sm + OFF_NF);
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         auto check = [&](bool ok) -> bool {  // role-wide agreement after a wait
-            if (!ok) { *fail = 1; flags[2] = 1; }
+            if (!ok) note_fail(0);
             named_sync(kBarPrep, kPrepThreads);
             return *fail == 0;
         };
-        if (issuer && n_chunks > 0) {
-            if (mbar_wait(bar(B_FULL0), 0)) {
-                tc_fence_after();
-                issue_gram(tmem, sbase + ST_KQ);
-                mma_commit(bar(B_G));
-            } else {
-                *fail = 1;
-                flags[2] = 1;
-            }
-        }
-        __syncwarp();
-        bool next_g_issued = true;  // (issuer) G of chunk c already issued
         for (int c = 0; c < n_chunks; ++c) {
-            const int s = c & 1, u = c >> 1;
-            const uint32_t stage = sbase + s * STAGE_BYTES;
-            const float *gate = reinterpret_cast<const float *>(sm + s * STAGE_BYTES + ST_GATE);
-            if (issuer && !next_g_issued) {
-                if (mbar_wait(bar(B_FULL0 + s), u & 1)) {
-                    tc_fence_after();
-                    issue_gram(tmem, stage + ST_KQ);
-                    mma_commit(bar(B_G));
-                } else {
-                    *fail = 1;
-                    flags[2] = 1;
-                }
-            }
-            __syncwarp();
-            bool ok = mbar_wait(bar(B_G), c & 1) && mbar_wait(bar(B_FULL0 + s), u & 1);
-            if (!check(ok)) break;
-            tc_fence_after();
-
-            // ---- L (fp32, strictly lower) from K K^T, masked A (bf16) from Q K^T
+            const int u = c >> 1;
+            const uint32_t vs = sbase + vslot(c), ks = sbase + kslot(c), qs = sbase + qslot(c);
+            unsigned char *vs_p = sm + vslot(c), *ks_p = sm + kslot(c), *qs_p = sm + qslot(c);
+            const float *gate = reinterpret_cast<const float *>(ks_p + RK_G);
+            if (!check(mbar_wait(bar(B_VF0 + (c & 1)), u & 1) && mbar_wait(bar(B_KF0 + c % 3), (c / 3) & 1)))
+                break;
+            const bool ratio = gate[G_FORM] != 0.f;
             {
-                const int t = row < C ? row : row - C;
-                // Gamma_ti as gamma_t / gamma_i when that is exact, else exp(g_t - g_i)
-                const bool ratio = gate[G_G + C - 1] > kRatioSafeLogDecay;
-                const float gt = ratio ? gate[G_GAM + t] : gate[G_G + t];
-                const float bt = gate[G_BETA + t];
+                // ---- T' diag(gamma) (bf16), same swizzled layout as T'; epilogue gates
+                const int t = ptid >> 1;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float v[32], gi[32];
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = 4 * (ptid & 1) + jj;  // 16-byte segment: columns 8j..8j+7
+                    const uint32_t off = (uint32_t)(t * 128 + (((j ^ t) & 7) << 4));
+                    uint4 w = *reinterpret_cast<const uint4 *>(vs_p + RV_T + off);
+                    uint32_t *uw = &w.x;
 #pragma unroll
-                    for (int ii = 0; ii < 32; ++ii) gi[ii] = gate[(ratio ? G_GINV : G_G) + 32 * hh + ii];
-                    tmem_load32(lane_base + TM_G + 32 * hh, v);
-                    if (ratio && row >= C) {  // A in ratio form: (1/gamma_C) q_t.k_i
-                        const float ginv_c = gate[G_GINV + C - 1];
-#pragma unroll
-                        for (int ii = 0; ii < 32; ++ii) v[ii] *= ginv_c;
-                    } else {
-#pragma unroll
-                        for (int ii = 0; ii < 32; ++ii) {
-                            const float dec = ratio ? gt * gi[ii] : fast_exp(gt - gi[ii]);
-                            v[ii] *= dec;
-                        }
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&uw[e]));
+                        uw[e] = pack_bf16x2(f.x * gate[G_GAM + 8 * j + 2 * e],
+                                            f.y * gate[G_GAM + 8 * j + 2 * e + 1]);
                     }
-                    if (row < C) {  // L: strictly lower entries only (the solve reads no others)
-#pragma unroll
-                        for (int ii = 0; ii < 32; ++ii)
-                            if (32 * hh + ii < t) Lf[t * LP + 32 * hh + ii] = bt * v[ii];
-                    } else {        // A: causal mask i <= t, zeros above
-#pragma unroll
-                        for (int ii = 0; ii < 32; ++ii)
-                            if (32 * hh + ii > t) v[ii] = 0.f;
-                        store_row32_sw128(sm + OFF_AM + (c & 1) * 8192, t, hh, v);
-                    }
+                    *reinterpret_cast<uint4 *>(sm + OFF_TG + off) = w;
                 }
+                if (ptid < C) eg[64 * (c & 3) + ptid] = gate[G_GAM + ptid];
+                if (ptid == 0) eg[256 + (c & 3)] = ratio ? 1.f : 0.f;
+                mbar_arrive(bar(B_EG0 + (c & 3)));
             }
             fence_async_smem();
             tc_fence_before();
             named_sync(kBarPrep, kPrepThreads);
 
-            // ---- T = (I + L)^{-1} diag(beta) and T diag(gamma), bf16, over L's space
-            unit_lower_inverse(Lf, Nf, ptid);
-            {
-                const int t = ptid >> 1, hh = ptid & 1;
-                float tv[32], tg[32];
-#pragma unroll
-                for (int ii = 0; ii < 32; ++ii) {
-                    tv[ii] = Nf[t * LP + 32 * hh + ii];
-                    tg[ii] = gate[G_GAM + 32 * hh + ii];
-                }
-#pragma unroll
-                for (int ii = 0; ii < 32; ++ii) {
-                    const int i = 32 * hh + ii;
-                    const float x = (i <= t) ? tv[ii] * gate[G_BETA + i] : 0.f;
-                    tv[ii] = x;
-                    tg[ii] *= x;
-                }
-                store_row32_sw128(sm + OFF_LF, t, hh, tv);
-                store_row32_sw128(sm + OFF_LF + 8192, t, hh, tg);
-            }
-            fence_async_smem();
-            named_sync(kBarPrep, kPrepThreads);
-
-            // ---- U~ and W; then, if its stage has landed, G of the next chunk
+            // ---- U'~ and W'
             if (issuer) {
-                tc_fence_after();
-                issue_uw(tmem, stage + ST_KQ, stage + ST_V, sbase + OFF_LF, sbase + OFF_LF + 8192,
-                         c & 1);
-                mma_commit(bar(B_UW0 + (c & 1)));
-                next_g_issued = false;
-                if (c + 1 < n_chunks) {
-                    const int s1 = (c + 1) & 1;
-                    if (mbar_try_wait(bar(B_FULL0 + s1), ((c + 1) >> 1) & 1)) {
-                        tc_fence_after();
-                        issue_gram(tmem, sbase + s1 * STAGE_BYTES + ST_KQ);
-                        mma_commit(bar(B_G));
-                        next_g_issued = true;
-                    }
+                const bool ok = c < 2 || mbar_wait(bar(B_UFREE0 + (c & 1)), ((c >> 1) - 1) & 1);
+                if (ok) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + TM_U + 64 * (c & 1), sw128_desc(vs + kk * 2048, 8192, 1024),
+                                 sw128_desc(vs + RV_T + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + TM_W, sw128_desc(ks + kk * 2048, 8192, 1024),
+                                 sw128_desc(sbase + OFF_TG + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0),
+                                 kk > 0);
+                    mma_commit(bar(B_UW0 + (c & 1)));
+                    mma_commit(bar(B_VE0 + (c & 1)));  // V and T' are read
+                } else {
+                    note_fail(0);
                 }
             }
             __syncwarp();
-            ok = mbar_wait(bar(B_UW0 + (c & 1)), u & 1);
-            if (c > 0) ok = ok && mbar_wait(bar(B_WS), (c - 1) & 1);  // W^T buffer free
+            // U'~, W' done; the Q slot's -W' half free once [QS | WS] of chunk c - 2 is done
+            bool ok = mbar_wait(bar(B_UW0 + (c & 1)), u & 1);
+            if (ok && c >= 2) ok = mbar_wait(bar(B_QE0 + (c & 1)), (u - 1) & 1);
             if (!check(ok)) break;
             tc_fence_after();
 
-            // ---- W^T to shared memory; scale the stage's Q rows by gamma, K rows by kdec
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float v[32];
-                tmem_load32(lane_base + TM_W + 32 * hh, v);
-                store_row32_sw128(sm + OFF_WT, row, hh, v);
+            // ---- -W' (rows t) into the Q slot
+            {
+                uint32_t r[32];
+                auto row_block = [&](int l8, uint32_t &block, int &c8) {
+                    const int dk = 32 * q + l8;
+                    block = qs + (dk >> 6) * 16384 + 8192;
+                    c8 = (dk & 63) >> 3;
+                };
+                tmem_load_16x256b_x8(lane_base + TM_W, r);
+                transpose_store16(r, -1.f, nullptr, lane, 0, row_block);
+                tmem_load_16x256b_x8(lane_base + (16u << 16) + TM_W, r);
+                transpose_store16(r, -1.f, nullptr, lane, 16, row_block);
             }
-            if (!(gate[G_G + C - 1] > kRatioSafeLogDecay))  // exponential form only
-#pragma unroll 2
-            for (int base = 0; base < 2048; base += 8 * kPrepThreads) {
-                uint4 w[8];
-                float f[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t o = (base + k * kPrepThreads + ptid) * 16;
-                    const int r = (o % 16384) / 128;  // rows 0..63 keys, 64..127 queries
-                    f[k] = r < C ? gate[G_KDEC + r] : gate[G_GAM + r - C];
-                    w[k] = *reinterpret_cast<const uint4 *>(sm + s * STAGE_BYTES + ST_KQ + o);
-                }
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    uint32_t *uw = &w[k].x;
+            // Q has landed ([QS | WS] follows B_WQ, and the exponential form scales it here)
+            if (!check(mbar_wait(bar(B_QF0 + (c & 1)), u & 1))) break;
+            if (!ratio) {
+                // exponential form: 16-byte segments of Q (gamma) and K (kdec), in place
+#pragma unroll 4
+                for (int k = 0; k < 16; ++k) {
+                    const int idx = ptid + k * kPrepThreads;  // 0..2047
+                    const bool isq = idx < 1024;
+                    unsigned char *ptr = isq ? qs_p + (idx >> 9) * 16384 + (idx & 511) * 16
+                                             : ks_p + (idx - 1024) * 16;
+                    const int r = ((isq ? (idx & 511) : (idx - 1024)) * 16 % 8192) / 128;  // token row
+                    const float f = isq ? gate[G_GAM + r] : gate[G_KDEC + r];
+                    uint4 w = *reinterpret_cast<const uint4 *>(ptr);
+                    uint32_t *uw = &w.x;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 fl = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&uw[e]));
-                        uw[e] = pack_bf16x2(fl.x * f[k], fl.y * f[k]);
+                        uw[e] = pack_bf16x2(fl.x * f, fl.y * f);
                     }
-                    const uint32_t o = (base + k * kPrepThreads + ptid) * 16;
-                    *reinterpret_cast<uint4 *>(sm + s * STAGE_BYTES + ST_KQ + o) = w[k];
+                    *reinterpret_cast<uint4 *>(ptr) = w;
                 }
             }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(bar(B_WQ));
+            mbar_arrive(bar(B_WQ0 + (c & 1)));
+            mbar_arrive(bar(B_KE0 + c % 3));  // this thread reads the K slot no more
         }
         if (*fail && issuer) {  // let issued MMAs land before TMEM and shared memory go away
             mma_commit(bar(B_DRAIN0));
             mbar_wait(bar(B_DRAIN0), 0);
         }
-    } else if (warp >= kStateWarp0) {
+    } else {
         // ============================================================ state
         const int stid = tid - 32 * kStateWarp0;
         const int half = (warp - kStateWarp0) >> 2;  // which 64 of the d_k entries / 32 of the tokens
@@ -619,165 +463,119 @@ tc_prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const bool issuer = stid == 0;
         volatile int *fail = &flags[1];
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        float *__restrict__ sgate = reinterpret_cast<float *>(sm + OFF_SG);  // gamma | kdec
         auto check = [&](bool ok) -> bool {
-            if (!ok) { *fail = 1; flags[2] = 1; }
+            if (!ok) note_fail(1);
             named_sync(kBarState, kStateThreads);
             return *fail == 0;
         };
-        // master state S^T: lane col0 + row, columns TM_S + d for d in [64*half, 64*half + 64)
+        // this thread's 64 entries of S^T: lane col0 + row, d_k columns [64*half, 64*half + 64);
+        // they live in the fp32 master in TMEM and are read back 32 at a time
         const size_t s_off = ((size_t)n * p.H + h) * DK * p.dv + col0 + row;
+        const uint32_t s_tm = lane_base + TM_S + 64 * half;
+        {  // S0 (or zero) into the master
+            const float *src = p.S0 ? p.S0 + s_off + (size_t)(64 * half) * p.dv : nullptr;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float v[32];
+            for (int hh = 0; hh < 2; ++hh) {
+                float x[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                v[i] = p.S0 ? p.S0[s_off + (size_t)(64 * half + 32 * hh + i) * p.dv] : 0.f;
-            tmem_store32(lane_base + TM_S + 64 * half + 32 * hh, v);
-            store_row32_sw128(sm + OFF_ST + half * 16384, row, hh, v);
+                for (int i = 0; i < 32; ++i) x[i] = src ? src[(size_t)(32 * hh + i) * p.dv] : 0.f;
+                tmem_store32(s_tm + 32 * hh, x);
+            }
+            tc_fence_before();
         }
-        tc_fence_before();
-        fence_async_smem();
-        named_sync(kBarState, kStateThreads);
-        if (issuer && n_chunks > 0) {
-            if (mbar_wait(bar(B_WQ), 0)) {
+        // Step c finishes chunk c - 1 (when c > 0), then starts chunk c (when c < n_chunks).
+        for (int c = 0; c <= n_chunks; ++c) {
+            if (c > 0) {
+                const int cp = c - 1, s = cp & 1;
+                // ---- U'^T = U'~^T + X^T, as bf16 pairs over this thread's read part of X
+                if (!check(mbar_wait(bar(B_WS), cp & 1))) break;
                 tc_fence_after();
-                issue_ws(tmem, sbase + OFF_ST, sbase + OFF_WT);
-                mma_commit(bar(B_WS));
-                issue_qs(tmem, sbase + OFF_ST, sbase + ST_KQ);
-            } else {
-                *fail = 1;
-                flags[2] = 1;
-            }
-        }
-        __syncwarp();
-        for (int c = 0; c < n_chunks; ++c) {
-            const int s = c & 1, u = c >> 1;
-            const uint32_t stage = sbase + s * STAGE_BYTES;
-            const float *gate = reinterpret_cast<const float *>(sm + s * STAGE_BYTES + ST_GATE);
-            const int64_t t0 = seq_begin + (int64_t)c * C;
-            const int len = (int)((seq_end - t0) < C ? (seq_end - t0) : C);
+                {
+                    float a[32], b[32];
+                    tmem_load32(lane_base + TM_U + 64 * s + 32 * half, a);
+                    tmem_load32(lane_base + TM_X + 32 * half, b);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(a[2 * i] + b[2 * i], a[2 * i + 1] + b[2 * i + 1]);
+                    tmem_store16(lane_base + TM_X + 32 * half, w);
+                }
+                tc_fence_before();
+                named_sync(kBarState, kStateThreads);
+                if (issuer) {
+                    tc_fence_after();
+                    mbar_arrive(bar(B_UFREE0 + s));
+                    const uint32_t ks = sbase + kslot(cp);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)  // tokens 16kk..16kk+15: columns X + 32(kk/2) + 8(kk%2)
+                        mma_bf16_ta(tmem + TM_S, tmem + TM_X + 32 * (kk >> 1) + 8 * (kk & 1),
+                                    sw128_desc(ks + kk * 2048, 8192, 1024), idesc_bf16(128, 192, 0, 1), 1);
+                    mma_commit(bar(B_SO));
+                    mma_commit(bar(B_KE0 + cp % 3));  // the state's last reads of the K slot
+                }
+                __syncwarp();
 
-            // ---- while WS runs: copy this chunk's gates, decay the master state in place
-            bool ok = mbar_wait(bar(B_FULL0 + s), u & 1);  // this stage's gates are visible
-            if (!check(ok)) break;
-            tc_fence_after();
-            const bool ratio = gate[G_G + C - 1] > kRatioSafeLogDecay;
-            if (stid < C) {
-                sgate[stid] = gate[G_GAM + stid];
-                sgate[C + stid] = gate[G_KDEC + stid];
+                // ---- the new state (gamma_C S + U'^T K, accumulated in TMEM)
+                if (!check(mbar_wait(bar(B_SO), cp & 1))) break;
+                tc_fence_after();
             }
-            {
-                const float gC = gate[G_GAM + C - 1];
+            if (c == n_chunks) {  // the final state (an empty sequence keeps its initial one)
+                float *dst = p.S_final + s_off + (size_t)(64 * half) * p.dv;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    float v[32];
-                    tmem_load32(lane_base + TM_S + 64 * half + 32 * hh, v);
+                    float x[32];
+                    tmem_load32(s_tm + 32 * hh, x);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= gC;
-                    tmem_store32(lane_base + TM_S + 64 * half + 32 * hh, v);
+                    for (int i = 0; i < 32; ++i) dst[(size_t)(32 * hh + i) * p.dv] = x[i];
                 }
+                break;
             }
-
-            // ---- U^T = U~^T - (WS)^T
-            ok = mbar_wait(bar(B_WS), c & 1) && mbar_wait(bar(B_UW0 + (c & 1)), u & 1);
-            if (!check(ok)) break;
-            tc_fence_after();
-            if (issuer) mbar_arrive(bar(B_EMPTY0 + s));  // the stage's gates are no longer read
-            {
-                float a[32], b[32];
-                tmem_load32(lane_base + TM_U + 64 * (c & 1) + 32 * half, a);
-                tmem_load32(lane_base + TM_WS + 32 * half, b);
-                if (ratio) {  // U' = diag(kdec) U
+            // ---- bf16 S^T into TMEM for [QS | WS] of chunk c, the issue of that chain
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) a[i] = (a[i] - b[i]) * sgate[C + 32 * half + i];
+            for (int hh = 0; hh < 2; ++hh) {
+                float x[32];
+                tmem_load32(s_tm + 32 * hh, x);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+                tmem_store16(lane_base + TM_SA + 32 * half + 16 * hh, w);
+            }
+            tc_fence_before();
+            named_sync(kBarState, kStateThreads);
+            if (issuer) {
+                bool ok = mbar_wait(bar(B_WQ0 + (c & 1)), (c >> 1) & 1);
+                if (ok && c > 0) ok = mbar_wait(bar(B_OFREE), (c - 1) & 1);  // O of chunk c-1 read
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t qw = sbase + qslot(c);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16_ta(tmem + TM_O, tmem + TM_SA + 8 * kk,
+                                    sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                                    idesc_bf16(128, 128, 0, 0), kk > 0);
+                    mma_commit(bar(B_WS));
+                    mma_commit(bar(B_QE0 + (c & 1)));  // Q and -W' are read
                 } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) a[i] -= b[i];
-                }
-                store_row32_sw128(sm + OFF_UT, row, half, a);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            named_sync(kBarState, kStateThreads);
-            if (issuer) {
-                tc_fence_after();
-                issue_supd_au(tmem, sbase + OFF_UT, stage + ST_KQ, sbase + OFF_AM + (c & 1) * 8192,
-                              bar(B_S), bar(B_EMPTY0 + s), bar(B_O));
-            }
-            __syncwarp();
-
-            // ---- the new state (gamma_C S + U^T Ktilde, accumulated in TMEM): its bf16 copy
-            ok = mbar_wait(bar(B_S), c & 1);
-            if (!check(ok)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float v[32];
-                tmem_load32(lane_base + TM_S + 64 * half + 32 * hh, v);
-                store_row32_sw128(sm + OFF_ST + half * 16384, row, hh, v);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            named_sync(kBarState, kStateThreads);
-            if (issuer) {
-                if (c + 1 < n_chunks) {
-                    if (mbar_wait(bar(B_WQ), (c + 1) & 1)) {
-                        tc_fence_after();
-                        issue_ws(tmem, sbase + OFF_ST, sbase + OFF_WT);
-                        mma_commit(bar(B_WS));
-                    } else {
-                        *fail = 1;
-                        flags[2] = 1;
-                    }
+                    note_fail(1);
                 }
             }
             __syncwarp();
-
-            // ---- outputs: O^T from TMEM -> staging tile [t][128] -> coalesced stores
-            ok = mbar_wait(bar(B_O), c & 1);
-            if (!check(ok)) break;
-            tc_fence_after();
-            {
-                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_UT);
-                float v[32];
-                tmem_load32(lane_base + TM_O + 32 * half, v);
-                if (ratio) {  // O_t = gamma_t x accumulator
+            // ---- the master decayed by gamma_C of chunk c, while [QS | WS] runs
+            if (!mbar_wait(bar(B_KF0 + c % 3), (c / 3) & 1)) {
+                note_fail(1);
+            } else {
+                const float gC = reinterpret_cast<const float *>(sm + kslot(c) + RK_G)[G_GAM + C - 1];
 #pragma unroll
-                    for (int ii = 0; ii < 32; ++ii) v[ii] *= sgate[32 * half + ii];
+                for (int hh = 0; hh < 2; ++hh) {
+                    float x[32];
+                    tmem_load32(s_tm + 32 * hh, x);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] *= gC;
+                    tmem_store32(s_tm + 32 * hh, x);
                 }
-#pragma unroll
-                for (int ii = 0; ii < 32; ++ii) stg[(32 * half + ii) * NV + row] = __float2bfloat16_rn(v[ii]);
             }
             tc_fence_before();
-            named_sync(kBarState, kStateThreads);
-            if (issuer && c + 1 < n_chunks) {  // O accumulator free again
-                tc_fence_after();
-                issue_qs(tmem, sbase + OFF_ST, sbase + ((c + 1) & 1) * STAGE_BYTES + ST_KQ);
-            }
-            {
-                const uint4 *stg = reinterpret_cast<const uint4 *>(sm + OFF_UT);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int idx = stid + k * kStateThreads;  // 64 rows x 16 chunks of 16 bytes
-                    const int t = idx >> 4, ch = idx & 15;
-                    if (t < len)
-                        *reinterpret_cast<uint4 *>(p.o + ((size_t)(t0 + t) * p.H + h) * p.dv + col0 +
-                                                   ch * 8) = stg[idx];
-                }
-            }
-            named_sync(kBarState, kStateThreads);  // staging consumed before U^T reuses it
         }
-        if (*fail == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float v[32];
-                tmem_load32(lane_base + TM_S + 64 * half + 32 * hh, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) p.S_final[s_off + (size_t)(64 * half + 32 * hh + i) * p.dv] = v[i];
-            }
-        } else if (issuer) {
+        if (*fail && issuer) {
             mma_commit(bar(B_DRAIN1));
             mbar_wait(bar(B_DRAIN1), 0);
         }
@@ -785,12 +583,16 @@ tc_prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
     tc_fence_before();
     __syncthreads();
-    if (flags[2] != 0 && tid == 0) {
+    if (flags[3] != 0 && tid == 0) {
         atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
-        // loads still in flight land before the shared memory is released
-        for (int s = 0; s < 2 && s < n_chunks; ++s) {
-            const int last_c = ((n_chunks - 1 - s) / 2) * 2 + s;  // last chunk that used stage s
-            mbar_wait(bar(B_FULL0 + s), (last_c >> 1) & 1);
+        // loads still in flight land before the shared memory is released: the last
+        // chunk loaded into each slot (a wait on a phase that never completes gives up)
+        for (int c = n_chunks - 1; c >= 0 && c >= n_chunks - 3; --c) {
+            if (c >= n_chunks - 2) {
+                mbar_wait(bar(B_QF0 + (c & 1)), (c >> 1) & 1);
+                mbar_wait(bar(B_VF0 + (c & 1)), (c >> 1) & 1);
+            }
+            mbar_wait(bar(B_KF0 + c % 3), (c / 3) & 1);
         }
     }
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
@@ -817,13 +619,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tensor map over a packed [T, H, d] bf16 tensor, 64 (features) x 1 (head) x 64 (tokens) boxes.
-bool make_map(CUtensorMap *map, const void *base, int d, int H, int64_t T) {
+bool encode_3d(CUtensorMap *map, const void *base, const cuuint64_t (&dims)[3],
+               const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3]) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T};
-    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * H * 2};
-    const cuuint32_t box[3] = {64, 1, 64};
     const cuuint32_t elem[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
               elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -831,6 +630,24 @@ bool make_map(CUtensorMap *map, const void *base, int d, int H, int64_t T) {
 }
 
 }  // namespace
+
+namespace tc {
+
+bool make_map_thd(CUtensorMap *map, const void *base, int d, int H, int64_t T) {
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * H * 2};
+    const cuuint32_t box[3] = {64, 1, 64};
+    return encode_3d(map, base, dims, strides, box);
+}
+
+bool make_map_units(CUtensorMap *map, const void *base, int64_t units) {
+    const cuuint64_t dims[3] = {64, 64, (cuuint64_t)units};
+    const cuuint64_t strides[2] = {64 * 2, 64 * 64 * 2};
+    const cuuint32_t box[3] = {64, 64, 1};
+    return encode_3d(map, base, dims, strides, box);
+}
+
+}  // namespace tc
 
 int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L) {
     const size_t s_bytes = (size_t)a.num_seqs * a.H * a.dk * a.dv * sizeof(float);
@@ -841,15 +658,20 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L) {
             e = cudaMemcpyAsync(a.S_final, a.S0, s_bytes, cudaMemcpyDeviceToDevice, a.stream);
         return cuda_status(e);
     }
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.q, a.dk, a.H, a.total_tokens) || !make_map(&mk, a.k, a.dk, a.H, a.total_tokens) ||
-        !make_map(&mv, a.v, a.dv, a.H, a.total_tokens))
+    CUtensorMap mq, mk, mv, mt, mo;
+    if (!tc::make_map_thd(&mq, a.q, a.dk, a.H, a.total_tokens) ||
+        !tc::make_map_thd(&mk, a.k, a.dk, a.H, a.total_tokens) ||
+        !tc::make_map_thd(&mv, a.v, a.dv, a.H, a.total_tokens) ||
+        !tc::make_map_thd(&mo, a.o, a.dv, a.H, a.total_tokens) ||
+        !tc::make_map_units(&mt, a.ws + L.T, 2 * L.max_chunks * a.H))
         return GDR_ERR_CUDA;
+    const int st = tc::launch_solve_tc(a, L, mq, mk);
+    if (st != GDR_OK) return st;
     TcParams p;
-    p.log_alpha = a.log_alpha;
-    p.beta = a.beta;
     p.S0 = a.S0;
+    p.factors = reinterpret_cast<const float *>(a.ws + L.G);
     p.cu_seqlens = a.cu_seqlens;
+    p.seq_chunk = reinterpret_cast<const int32_t *>(a.ws + L.seq_chunk);
     p.num_seqs = a.num_seqs;
     p.total_tokens = a.total_tokens;
     p.H = a.H;
@@ -858,11 +680,11 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L) {
     p.o = (__nv_bfloat16 *)a.o;
     p.S_final = a.S_final;
     p.ctl = (int32_t *)(a.ws + L.ctl);
-    if (cudaFuncSetAttribute(tc_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
         return GDR_ERR_CUDA;
     const unsigned grid = (unsigned)(a.num_seqs * a.H * p.n_slices);
-    tc_prefill_kernel<<<grid, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, p);
+    tc_chain_kernel<<<grid, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mt, mo, p);
     return cuda_status(cudaGetLastError());
 }
 

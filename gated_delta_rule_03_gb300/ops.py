@@ -175,7 +175,7 @@ def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None):
 # What one gdr_chunk_fwd call enqueues on each kernel path (see gdr_chunk_fwd_path in gdr.h).
 _PATHS = {
     0: dict(launches=3, main_kernel="exact_chain_kernel", compute_dtype="f32"),
-    1: dict(launches=2, main_kernel="tc_prefill_kernel", compute_dtype="bf16"),
+    1: dict(launches=3, main_kernel="tc_chain_kernel", compute_dtype="bf16"),
 }
 
 
