@@ -20,13 +20,15 @@
 // they differ only in where the decay factors are applied, and both kernels choose
 // the same form for a chunk.)
 //
-// Mapping. A CTA of 4 warps takes units two at a time. One tcgen05.mma chain forms
-// [K_a; K_b] [K_a; K_b; Q_a; Q_b]^T (M = 128, N = 256, K = d_k = 128) in TMEM from
-// TMA-loaded bf16 tiles: its diagonal 64x64 blocks are the units' Gram matrices K K^T
-// and K Q^T. Warps 0-1 read unit a's rows (TMEM lanes 0-63), warps 2-3 unit b's (lanes
-// 64-127). The solve is fp32 on the CUDA cores: 16x16 diagonal blocks by forward
-// substitution, the off-diagonal blocks with warp-level TF32 products. While a pair is
-// solved, the next pair's keys and queries are already loading. Two CTAs share an SM.
+// Mapping. A CTA of 8 warps takes units two at a time; two CTAs share an SM. One
+// tcgen05.mma chain forms [K_a; K_b] [K_a; K_b; Q_a; Q_b]^T (M = 128, N = 256, K = d_k =
+// 128) in TMEM from TMA-loaded bf16 tiles: its diagonal 64x64 blocks are the units' K K^T
+// and K Q^T. All 8 warps read them out at once (warps 0-1: L of unit a from TMEM lanes
+// 0-63; 2-3: L of unit b, lanes 64-127; 4-5 and 6-7: A^T of a and b), then warps 0-3
+// solve unit a while warps 4-7 solve unit b. The solve is fp32 on the CUDA cores in
+// 16x16 blocks: the diagonal blocks by forward substitution, the others with warp-level
+// TF32 products. While a pair is solved, the next pair's keys and queries are loading
+// and its decay gates are in flight to registers.
 #include "tc_common.cuh"
 
 namespace gdr {
@@ -36,21 +38,26 @@ using namespace sm100;
 using namespace tc;
 
 constexpr int C = kChunk;
-constexpr int kThreads = 128;
-constexpr int kBarSolve = 1;  // named barrier of the whole CTA
-constexpr int LP = C + 1;     // fp32 pitch of the solve matrices
+constexpr int kThreads = 256;
+constexpr int kGroupThreads = 128;  // one unit's solve
+constexpr int BP = 17;              // fp32 pitch of a 16x16 block
+constexpr int BF = 16 * BP;         // floats per block
+// Lower-triangular 4x4 arrangement of 16x16 blocks: block (i, k), k <= i, at index
+// i(i+1)/2 + k. A unit has ten blocks of L (then of M = N_ii L_ik, and the diagonal
+// slots as scratch once the substitution has read them) and ten of N = (I + L)^{-1}.
+__host__ __device__ constexpr int blk(int i, int k) { return (i * (i + 1) / 2 + k) * BF; }
+constexpr int UNIT_FLOATS = 20 * BF;
 
 // per d_k half b (32 KB): K_a | K_b | Q_a | Q_b, 8 KB each; rows 0-127 are the MMA's A
 // operand, rows 0-255 its B operand
 constexpr uint32_t OFF_K = 0;
-constexpr uint32_t OFF_LF = 65536;                // L fp32 [64][LP] (then the M blocks)
-constexpr uint32_t OFF_NF = OFF_LF + C * LP * 4;  // (I + L)^{-1} fp32 [64][LP]
-constexpr uint32_t OFF_GATE = OFF_NF + C * LP * 4;
+constexpr uint32_t OFF_LN = 65536;                             // two units' L, N blocks
+constexpr uint32_t OFF_GATE = OFF_LN + 2 * UNIT_FLOATS * 4;
 constexpr int G_G = 0, G_GAM = 64, G_GINV = 128, G_BETA = 192, G_KDEC = 256, G_UNIT = 320;
 constexpr uint32_t OFF_BAR = OFF_GATE + 2 * G_UNIT * 4;  // per unit: g, gamma, 1/gamma, beta, kdec
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
-static_assert(SMEM_BYTES * 2 <= 227 * 1024, "two CTAs per SM");
+static_assert((SMEM_BYTES + 1024) * 2 <= 228 * 1024, "two CTAs per SM");
 enum { B_FULL = 0, B_MMA, B_DRAIN, B_COUNT };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * B_COUNT;
 constexpr uint32_t OFF_FAIL = OFF_TMEM_SLOT + 4;
@@ -76,88 +83,143 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// d (+)= A * B for 16x16 row-major blocks A (pitch pa) and B (pitch pb); d holds the
-// result's two 16x8 halves in the m16n8 accumulator layout.
-__device__ __forceinline__ void warp_gemm16(const float *__restrict__ A, int pa,
-                                            const float *__restrict__ B, int pb, float (&d)[2][4],
-                                            int lane) {
+// d (+)= A * B for 16x16 blocks A and B (pitch BP); d holds the result's two 16x8 halves
+// in the m16n8 accumulator layout.
+__device__ __forceinline__ void warp_gemm16(const float *__restrict__ A, const float *__restrict__ B,
+                                            float (&d)[2][4], int lane) {
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        const uint32_t a[4] = {to_tf32(A[g * pa + 8 * ks + q]), to_tf32(A[(g + 8) * pa + 8 * ks + q]),
-                               to_tf32(A[g * pa + 8 * ks + q + 4]),
-                               to_tf32(A[(g + 8) * pa + 8 * ks + q + 4])};
+        const uint32_t a[4] = {to_tf32(A[g * BP + 8 * ks + q]), to_tf32(A[(g + 8) * BP + 8 * ks + q]),
+                               to_tf32(A[g * BP + 8 * ks + q + 4]),
+                               to_tf32(A[(g + 8) * BP + 8 * ks + q + 4])};
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t b[2] = {to_tf32(B[(8 * ks + q) * pb + 8 * nt + g]),
-                                   to_tf32(B[(8 * ks + q + 4) * pb + 8 * nt + g])};
+            const uint32_t b[2] = {to_tf32(B[(8 * ks + q) * BP + 8 * nt + g]),
+                                   to_tf32(B[(8 * ks + q + 4) * BP + 8 * nt + g])};
             mma_tf32_16x8x8(d[nt], a, b);
         }
     }
 }
 
-// M = scale * d for a 16x16 row-major block M (pitch pm).
-__device__ __forceinline__ void warp_store16(float *__restrict__ M, int pm, const float (&d)[2][4],
-                                             int lane, float scale) {
+// d = scale * M (load) or M = scale * d (store) for a 16x16 block M in the accumulator layout.
+__device__ __forceinline__ void warp_load16(const float *__restrict__ M, float (&d)[2][4], int lane,
+                                            float scale) {
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-        M[g * pm + 8 * nt + 2 * q] = scale * d[nt][0];
-        M[g * pm + 8 * nt + 2 * q + 1] = scale * d[nt][1];
-        M[(g + 8) * pm + 8 * nt + 2 * q] = scale * d[nt][2];
-        M[(g + 8) * pm + 8 * nt + 2 * q + 1] = scale * d[nt][3];
+        d[nt][0] = scale * M[g * BP + 8 * nt + 2 * q];
+        d[nt][1] = scale * M[g * BP + 8 * nt + 2 * q + 1];
+        d[nt][2] = scale * M[(g + 8) * BP + 8 * nt + 2 * q];
+        d[nt][3] = scale * M[(g + 8) * BP + 8 * nt + 2 * q + 1];
     }
 }
 
-// Nf = (I + L)^{-1} for the strictly lower-triangular 64x64 L in Lf (fp32, pitch LP),
-// by the CTA's 128 threads. 16x16 diagonal blocks by forward substitution (one column
-// per thread), then the off-diagonal blocks: with M_ik = N_ii L_ik (i > k),
-// N_ij = -sum_{k=j}^{i-1} M_ik N_kj. All six M blocks are formed in one round (written
-// over the L blocks, which are not read again), then the N blocks by distance from the
-// diagonal, each by one warp as a single chain of accumulated products. Only the lower
-// triangle (with its unit diagonal) of Nf is written.
-__device__ __forceinline__ void unit_lower_inverse(float *__restrict__ Lf, float *__restrict__ Nf,
-                                                   int tid) {
-    if (tid < C) {
-        const int base = 16 * (tid >> 4), c = tid & 15;
+__device__ __forceinline__ void warp_store16(float *__restrict__ M, const float (&d)[2][4], int lane,
+                                             float scale) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        M[g * BP + 8 * nt + 2 * q] = scale * d[nt][0];
+        M[g * BP + 8 * nt + 2 * q + 1] = scale * d[nt][1];
+        M[(g + 8) * BP + 8 * nt + 2 * q] = scale * d[nt][2];
+        M[(g + 8) * BP + 8 * nt + 2 * q + 1] = scale * d[nt][3];
+    }
+}
+
+// N = (I + L)^{-1} for the strictly lower-triangular 64x64 L held as blocks in Lb, by a
+// group of 128 threads (4 warps, named barrier `bar_id`); N's ten lower blocks go to Nb.
+//   1. N_ii by forward substitution, one column of one diagonal block per thread.
+//   2. With M_ik = N_ii L_ik (i > k): N_ij = -sum_{k=j}^{i-1} M_ik N_kj, scheduled in four
+//      rounds so that every round holds at most two dependent block products:
+//        R1  M_10, M_21, M_32, M_20
+//        R2  N_10, N_21, N_32, M_31
+//        R3  N_20, N_31 (two products each); M_30 and P = M_30 N_00; Q = M_31 N_10
+//        R4  N_30 = -(P + Q + M_32 N_20)
+//      M blocks overwrite the L blocks they come from; P and Q go into the diagonal L
+//      slots of blocks 0 and 1, which the substitution no longer needs.
+__device__ __forceinline__ void unit_lower_inverse(float *__restrict__ Lb, float *__restrict__ Nb,
+                                                   int gtid, int bar_id) {
+    if (gtid < C) {
+        const int b = gtid >> 4, c = gtid & 15;
+        const float *Ld = Lb + blk(b, b);
         float x[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float s = (r == c) ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int k = 0; k < r; ++k) s = fmaf(-Lf[(base + r) * LP + base + k], x[k], s);
-            x[r] = s;
+        for (int k = 0; k < 15; ++k) {
+            const float xk = x[k];
+#pragma unroll
+            for (int r = k + 1; r < 16; ++r) x[r] = fmaf(-Ld[r * BP + k], xk, x[r]);
         }
+        float *Nd = Nb + blk(b, b);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Nf[(base + r) * LP + base + c] = x[r];
+        for (int r = 0; r < 16; ++r) Nd[r * BP + c] = x[r];
     }
-    named_sync(kBarSolve, kThreads);
-    const int w = tid >> 5, lane = tid & 31;
-    float *__restrict__ Mf = Lf;
+    named_sync(bar_id, kGroupThreads);
+    const int w = gtid >> 5, lane = gtid & 31;
+    float acc[2][4];
+    auto zero = [&]() {
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int b = w + 4 * r;  // blocks (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
-        if (b < 6) {
-            const int i = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
-            const int k = b < 3 ? b : (b < 5 ? b - 3 : 0);
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            warp_gemm16(Nf + 16 * i * LP + 16 * i, LP, Lf + 16 * i * LP + 16 * k, LP, acc, lane);
-            __syncwarp();
-            warp_store16(Mf + 16 * i * LP + 16 * k, LP, acc, lane, 1.f);
-        }
-    }
-    named_sync(kBarSolve, kThreads);
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int d = 1; d < 4; ++d) {
-        if (w < 4 - d) {
-            const int i = d + w, j = w;
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            for (int k = j; k < i; ++k)
-                warp_gemm16(Mf + 16 * i * LP + 16 * k, LP, Nf + 16 * k * LP + 16 * j, LP, acc, lane);
-            warp_store16(Nf + 16 * i * LP + 16 * j, LP, acc, lane, -1.f);
-        }
-        named_sync(kBarSolve, kThreads);
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+    };
+    // R1: M_10, M_21, M_32, M_20 = N_ii L_ik
+    {
+        const int i = w == 3 ? 2 : w + 1, k = w == 3 ? 0 : w;
+        zero();
+        warp_gemm16(Nb + blk(i, i), Lb + blk(i, k), acc, lane);
+        __syncwarp();
+        warp_store16(Lb + blk(i, k), acc, lane, 1.f);
     }
+    named_sync(bar_id, kGroupThreads);
+    // R2: N_10, N_21, N_32 = -M_{j+1,j} N_jj; M_31 = N_33 L_31
+    zero();
+    if (w < 3) {
+        warp_gemm16(Lb + blk(w + 1, w), Nb + blk(w, w), acc, lane);
+        warp_store16(Nb + blk(w + 1, w), acc, lane, -1.f);
+    } else {
+        warp_gemm16(Nb + blk(3, 3), Lb + blk(3, 1), acc, lane);
+        __syncwarp();
+        warp_store16(Lb + blk(3, 1), acc, lane, 1.f);
+    }
+    named_sync(bar_id, kGroupThreads);
+    // R3
+    zero();
+    if (w == 0) {  // N_20 = -(M_20 N_00 + M_21 N_10)
+        warp_gemm16(Lb + blk(2, 0), Nb + blk(0, 0), acc, lane);
+        warp_gemm16(Lb + blk(2, 1), Nb + blk(1, 0), acc, lane);
+        warp_store16(Nb + blk(2, 0), acc, lane, -1.f);
+    } else if (w == 1) {  // N_31 = -(M_31 N_11 + M_32 N_21)
+        warp_gemm16(Lb + blk(3, 1), Nb + blk(1, 1), acc, lane);
+        warp_gemm16(Lb + blk(3, 2), Nb + blk(2, 1), acc, lane);
+        warp_store16(Nb + blk(3, 1), acc, lane, -1.f);
+    } else if (w == 2) {  // M_30 = N_33 L_30, then P = M_30 N_00 into the L_00 slot
+        warp_gemm16(Nb + blk(3, 3), Lb + blk(3, 0), acc, lane);
+        warp_store16(Lb + blk(3, 0), acc, lane, 1.f);
+        __syncwarp();
+        zero();
+        warp_gemm16(Lb + blk(3, 0), Nb + blk(0, 0), acc, lane);
+        warp_store16(Lb + blk(0, 0), acc, lane, 1.f);
+    } else {  // Q = M_31 N_10 into the L_11 slot
+        warp_gemm16(Lb + blk(3, 1), Nb + blk(1, 0), acc, lane);
+        warp_store16(Lb + blk(1, 1), acc, lane, 1.f);
+    }
+    named_sync(bar_id, kGroupThreads);
+    // R4: N_30 = -(P + Q + M_32 N_20)
+    if (w == 0) {
+        float q2[2][4];
+        warp_load16(Lb + blk(0, 0), acc, lane, 1.f);
+        warp_load16(Lb + blk(1, 1), q2, lane, 1.f);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] += q2[nt][e];
+        warp_gemm16(Lb + blk(3, 2), Nb + blk(2, 0), acc, lane);
+        warp_store16(Nb + blk(3, 0), acc, lane, -1.f);
+    }
+    named_sync(bar_id, kGroupThreads);
 }
 
 struct SolveParams {
@@ -184,18 +246,19 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TMEM_SLOT);
     volatile int *fail = reinterpret_cast<volatile int *>(sm + OFF_FAIL);
-    float *__restrict__ Lf = reinterpret_cast<float *>(sm + OFF_LF);
-    float *__restrict__ Nf = reinterpret_cast<float *>(sm + OFF_NF);
     float *__restrict__ gates = reinterpret_cast<float *>(sm + OFF_GATE);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int group = warp >> 2, gtid = tid & 127;  // solve group: unit a (0) or b (1)
 
     // unit u -> (chunk, head); the second unit of an odd last pair repeats the first
     auto unit_of = [&](int pair, int which) {
         const int u = 2 * pair + which;
         return u < n_units ? u : 2 * pair;
     };
+    int loads_issued = 0, loads_landed = 0;  // (thread 0) for the drain after an abort
     auto load_pair = [&](int pair) {  // one thread
+        ++loads_issued;
         mbar_arrive_expect_tx(bar(B_FULL), 8 * 8192);
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
@@ -204,9 +267,29 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const int h = u % p.H;
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
-                const uint32_t blk = sbase + OFF_K + b * 32768 + which * 8192;
-                tma_load_3d(blk, &map_k, bar(B_FULL), 64 * b, h, pl.y);
-                tma_load_3d(blk + 16384, &map_q, bar(B_FULL), 64 * b, h, pl.y);
+                const uint32_t blkaddr = sbase + OFF_K + b * 32768 + which * 8192;
+                tma_load_3d(blkaddr, &map_k, bar(B_FULL), 64 * b, h, pl.y);
+                tma_load_3d(blkaddr + 16384, &map_q, bar(B_FULL), 64 * b, h, pl.y);
+            }
+        }
+    };
+    // decay gates of one unit of `pair` (warp 0: unit a, warp 1: unit b), into registers
+    float ga0 = 0.f, ga1 = 0.f, gb0 = 0.f, gb1 = 0.f;
+    auto fetch_gates = [&](int pair) {
+        ga0 = ga1 = gb0 = gb1 = 0.f;
+        const int u = 2 * pair + warp;
+        if (u < n_units) {
+            const int4 pl = p.plan[u / p.H];
+            const int h = u % p.H, len = pl.z;
+            if (2 * lane < len) {
+                const size_t off = (size_t)(pl.y + 2 * lane) * p.H + h;
+                ga0 = p.log_alpha[off];
+                gb0 = p.beta[off];
+            }
+            if (2 * lane + 1 < len) {
+                const size_t off = (size_t)(pl.y + 2 * lane + 1) * p.H + h;
+                ga1 = p.log_alpha[off];
+                gb1 = p.beta[off];
             }
         }
     };
@@ -228,135 +311,173 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
 
-    if (tid == 0) load_pair(blockIdx.x);
+    // the Gram chain of `pair` (thread 0), once its keys and queries have landed
+    auto issue_gram = [&](int it_) -> bool {
+        if (!mbar_wait(bar(B_FULL), it_ & 1)) return false;
+        ++loads_landed;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = sbase + OFF_K + (kk >> 2) * 32768 + (kk & 3) * 32;
+            mma_bf16(tmem, sw128_desc(off, 16, 1024), sw128_desc(off, 16, 1024), idesc_bf16(128, 256, 0, 0),
+                     kk > 0);
+        }
+        mma_commit(bar(B_MMA));
+        return true;
+    };
+    if (tid == 0) {
+        load_pair(blockIdx.x);
+        if (!issue_gram(0)) *fail = 1;
+    }
+    if (warp < 2) fetch_gates(blockIdx.x);
     int it = 0;
     for (int pair = blockIdx.x; pair < n_pairs; pair += gridDim.x, ++it) {
-        // ---- gates of both units (warp 0: unit a, warp 1: unit b), by the shared scan
+        const int next = pair + (int)gridDim.x;
+        // ---- gates of both units (warp 0: unit a, warp 1: unit b) by the shared scan;
+        // then the next pair's gates are fetched
         if (warp < 2) {
-            const int u = 2 * pair + warp;
             float *g = gates + warp * G_UNIT;
-            if (u < n_units) {
-                const int4 pl = p.plan[u / p.H];
-                const int h = u % p.H, len = pl.z;
-                float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-                if (2 * lane < len) {
-                    const size_t off = (size_t)(pl.y + 2 * lane) * p.H + h;
-                    a0 = p.log_alpha[off];
-                    b0 = p.beta[off];
-                }
-                if (2 * lane + 1 < len) {
-                    const size_t off = (size_t)(pl.y + 2 * lane + 1) * p.H + h;
-                    a1 = p.log_alpha[off];
-                    b1 = p.beta[off];
-                }
-                const ChunkScan sc = chunk_scan(a0, a1, lane);
-                g[G_G + 2 * lane] = sc.g0;
-                g[G_G + 2 * lane + 1] = sc.g1;
-                g[G_GAM + 2 * lane] = fast_exp(sc.g0);
-                g[G_GAM + 2 * lane + 1] = fast_exp(sc.g1);
-                g[G_GINV + 2 * lane] = fast_exp(-sc.g0);
-                g[G_GINV + 2 * lane + 1] = fast_exp(-sc.g1);
-                g[G_BETA + 2 * lane] = b0;
-                g[G_BETA + 2 * lane + 1] = b1;
-                g[G_KDEC + 2 * lane] = fast_exp(sc.g_last - sc.g0);
-                g[G_KDEC + 2 * lane + 1] = fast_exp(sc.g_last - sc.g1);
-            }
+            const ChunkScan sc = chunk_scan(ga0, ga1, lane);
+            g[G_G + 2 * lane] = sc.g0;
+            g[G_G + 2 * lane + 1] = sc.g1;
+            g[G_GAM + 2 * lane] = fast_exp(sc.g0);
+            g[G_GAM + 2 * lane + 1] = fast_exp(sc.g1);
+            g[G_GINV + 2 * lane] = fast_exp(-sc.g0);
+            g[G_GINV + 2 * lane + 1] = fast_exp(-sc.g1);
+            g[G_BETA + 2 * lane] = gb0;
+            g[G_BETA + 2 * lane + 1] = gb1;
+            g[G_KDEC + 2 * lane] = fast_exp(sc.g_last - sc.g0);
+            g[G_KDEC + 2 * lane + 1] = fast_exp(sc.g_last - sc.g1);
+            if (next < n_pairs) fetch_gates(next);
         }
-        // ---- the pair's keys and queries have landed: one MMA chain for both units
+        // ---- the pair's Gram chain (issued before) has completed: its stage takes the next pair
         if (tid == 0) {
-            bool ok = mbar_wait(bar(B_FULL), it & 1);
-            if (ok) {
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = sbase + OFF_K + (kk >> 2) * 32768 + (kk & 3) * 32;
-                    mma_bf16(tmem, sw128_desc(off, 16, 1024), sw128_desc(off, 16, 1024),
-                             idesc_bf16(128, 256, 0, 0), kk > 0);
-                }
-                mma_commit(bar(B_MMA));
-                ok = mbar_wait(bar(B_MMA), it & 1);
+            if (*fail == 0 && mbar_wait(bar(B_MMA), it & 1)) {
+                if (next < n_pairs) load_pair(next);
+            } else {
+                *fail = 1;
             }
-            if (ok && pair + (int)gridDim.x < n_pairs) load_pair(pair + gridDim.x);  // stage free
-            if (!ok) *fail = 1;
         }
         __syncthreads();
         if (*fail) break;
         tc_fence_after();
 
-#pragma unroll 1
-        for (int which = 0; which < 2; ++which) {
+        // ---- read-out: L blocks of both units (warps 0-3), A^T and the factors (warps 4-7)
+        {
+            const int which = (warp >> 1) & 1;  // unit of this warp's TMEM lanes
             const int u = 2 * pair + which;
-            if (u >= n_units) break;  // uniform over the CTA
             const float *g = gates + which * G_UNIT;
             const bool ratio = g[G_G + C - 1] > kRatioSafeLogDecay;
-            {
-                float *go = p.Gout + (size_t)u * 256;
-                if (tid < C) {
-                    go[tid] = g[G_G + tid];
-                    go[64 + tid] = g[G_GAM + tid];
-                    go[128 + tid] = g[G_KDEC + tid];
-                } else {
-                    go[192 + tid - C] = (tid == C) ? (ratio ? 1.f : 0.f) : 0.f;
-                }
-            }
-            // ---- L (fp32, strictly lower) from this unit's K K^T block, and its A^T
-            if ((warp >> 1) == which) {
-                const int t = 32 * (warp & 1) + lane;
-                const float gt = ratio ? g[G_GAM + t] : g[G_G + t];
-                const float bt = g[G_BETA + t];
+            const int t = 32 * (warp & 1) + lane;  // token row (TMEM lane 64 which + t)
+            if (u < n_units) {
+                if (warp < 4) {
+                    // L_ti = beta_t Gamma_ti k_t.k_i (i < t) into the unit's blocks
+                    float *Lb = reinterpret_cast<float *>(sm + OFF_LN) + which * UNIT_FLOATS;
+                    const float gt = ratio ? g[G_GAM + t] : g[G_G + t];
+                    const float bt = g[G_BETA + t];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (hh > (warp & 1)) break;  // columns >= 32 are above the diagonal of rows < 32
-                    float v[32];
-                    tmem_load32(lane_base + 64 * which + 32 * hh, v);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (hh > (warp & 1)) break;  // columns >= 32 lie above rows < 32
+                        float v[32], f[32];
+                        tmem_load32(lane_base + 64 * which + 32 * hh, v);
+                        const float4 *gv = reinterpret_cast<const float4 *>(g + (ratio ? G_GINV : G_G) + 32 * hh);
 #pragma unroll
-                    for (int ii = 0; ii < 32; ++ii) {
-                        const int i = 32 * hh + ii;
-                        const float dec = ratio ? gt * g[G_GINV + i] : fast_exp(gt - g[G_G + i]);
-                        if (i < t) Lf[t * LP + i] = bt * dec * v[ii];
-                    }
-                }
-                // row i = t of A^T: key i against queries tq >= i
-                const float gi = g[G_G + t];
-                const float ginv_c = g[G_GINV + C - 1];
-                uint4 *dst = reinterpret_cast<uint4 *>(p.Tout + ((size_t)(2 * u + 1) * C + t) * C);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float v[32];
-                    if (hh < (warp & 1)) {  // rows i >= 32: queries tq < 32 are all masked
-#pragma unroll
-                        for (int ii = 0; ii < 32; ++ii) v[ii] = 0.f;
-                    } else {
-                        tmem_load32(lane_base + 128 + 64 * which + 32 * hh, v);
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 x = gv[j];
+                            f[4 * j] = x.x; f[4 * j + 1] = x.y; f[4 * j + 2] = x.z; f[4 * j + 3] = x.w;
+                        }
 #pragma unroll
                         for (int ii = 0; ii < 32; ++ii) {
-                            const int tq = 32 * hh + ii;
-                            const float dec = ratio ? ginv_c : fast_exp(g[G_G + tq] - gi);
-                            v[ii] = (tq >= t) ? v[ii] * dec : 0.f;
+                            const int i = 32 * hh + ii;
+                            const float dec = ratio ? gt * f[ii] : fast_exp(gt - f[ii]);
+                            v[ii] = (i < t) ? bt * dec * v[ii] : 0.f;
+                        }
+                        // whole 16-wide rows of the blocks left of and on the diagonal (the
+                        // zeros on and above the diagonal are never read)
+#pragma unroll
+                        for (int m = 0; m < 2; ++m) {
+                            const int ib = 2 * hh + m;
+                            if (ib <= (t >> 4)) {
+                                float *row = Lb + blk(t >> 4, ib) + (t & 15) * BP;
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) row[e] = v[16 * m + e];
+                            }
                         }
                     }
+                } else {
+                    // row i = t of A^T: key i against queries tq >= i
+                    const float gi = g[G_G + t];
+                    const float ginv_c = g[G_GINV + C - 1];
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.Tout + ((size_t)(2 * u + 1) * C + t) * C);
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        dst[4 * hh + jj] = make_uint4(pack_bf16x2(v[8 * jj], v[8 * jj + 1]),
-                                                      pack_bf16x2(v[8 * jj + 2], v[8 * jj + 3]),
-                                                      pack_bf16x2(v[8 * jj + 4], v[8 * jj + 5]),
-                                                      pack_bf16x2(v[8 * jj + 6], v[8 * jj + 7]));
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float v[32];
+                        if (hh < (warp & 1)) {  // rows i >= 32: queries tq < 32 are all masked
+#pragma unroll
+                            for (int ii = 0; ii < 32; ++ii) v[ii] = 0.f;
+                        } else {
+                            tmem_load32(lane_base + 128 + 64 * which + 32 * hh, v);
+#pragma unroll
+                            for (int ii = 0; ii < 32; ++ii) {
+                                const int tq = 32 * hh + ii;
+                                const float dec = ratio ? ginv_c : fast_exp(g[G_G + tq] - gi);
+                                v[ii] = (tq >= t) ? v[ii] * dec : 0.f;
+                            }
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            dst[4 * hh + jj] = make_uint4(pack_bf16x2(v[8 * jj], v[8 * jj + 1]),
+                                                          pack_bf16x2(v[8 * jj + 2], v[8 * jj + 3]),
+                                                          pack_bf16x2(v[8 * jj + 4], v[8 * jj + 5]),
+                                                          pack_bf16x2(v[8 * jj + 6], v[8 * jj + 7]));
+                    }
+                    // the unit's decay factors for the chain kernel: g and gamma (threads
+                    // t < 32), kdec and the form flag (t >= 32), two tokens each
+                    float *go = p.Gout + (size_t)u * 256;
+                    if (t < 32) {
+                        go[2 * t] = g[G_G + 2 * t];
+                        go[2 * t + 1] = g[G_G + 2 * t + 1];
+                        go[64 + 2 * t] = g[G_GAM + 2 * t];
+                        go[64 + 2 * t + 1] = g[G_GAM + 2 * t + 1];
+                    } else {
+                        const int t2 = t - 32;
+                        go[128 + 2 * t2] = g[G_KDEC + 2 * t2];
+                        go[128 + 2 * t2 + 1] = g[G_KDEC + 2 * t2 + 1];
+                        go[192 + 2 * t2] = (t2 == 0) ? (ratio ? 1.f : 0.f) : 0.f;
+                        go[192 + 2 * t2 + 1] = 0.f;
+                    }
                 }
             }
-            tc_fence_before();  // the TMEM reads are done before the next pair's MMA is issued
-            named_sync(kBarSolve, kThreads);
-            unit_lower_inverse(Lf, Nf, tid);
-            // ---- T' = diag(kdec) (I + L)^{-1} diag(beta) (ratio form; no kdec otherwise), bf16
-            {
-                const int t = tid >> 1, hh = tid & 1;
+        }
+        tc_fence_before();  // the TMEM reads are done before the next pair's MMA is issued
+        __syncthreads();
+        if (tid == 0 && next < n_pairs && !issue_gram(it + 1)) *fail = 1;
+
+        // ---- each group solves its unit: T' = diag(kdec) (I + L)^{-1} diag(beta) (ratio
+        // form; no kdec otherwise), bf16
+        {
+            const int u = 2 * pair + group;
+            if (u < n_units) {
+                float *Lb = reinterpret_cast<float *>(sm + OFF_LN) + group * UNIT_FLOATS;
+                float *Nb = Lb + 10 * BF;
+                const float *g = gates + group * G_UNIT;
+                const bool ratio = g[G_G + C - 1] > kRatioSafeLogDecay;
+                unit_lower_inverse(Lb, Nb, gtid, 1 + group);
+                const int t = gtid >> 1, hh = gtid & 1;
                 const float kd = ratio ? g[G_KDEC + t] : 1.f;
-                float x[32];
+                float x[32], bv[32];
+                const float4 *bp = reinterpret_cast<const float4 *>(g + G_BETA + 32 * hh);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 b4 = bp[j];
+                    bv[4 * j] = b4.x; bv[4 * j + 1] = b4.y; bv[4 * j + 2] = b4.z; bv[4 * j + 3] = b4.w;
+                }
 #pragma unroll
                 for (int ii = 0; ii < 32; ++ii) {
                     const int i = 32 * hh + ii;
-                    x[ii] = (i <= t) ? Nf[t * LP + i] * g[G_BETA + i] * kd : 0.f;
+                    x[ii] = (i <= t) ? Nb[blk(t >> 4, i >> 4) + (t & 15) * BP + (i & 15)] * bv[ii] * kd : 0.f;
                 }
                 uint4 *dst = reinterpret_cast<uint4 *>(p.Tout + ((size_t)(2 * u) * C + t) * C + 32 * hh);
 #pragma unroll
@@ -366,8 +487,8 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                                          pack_bf16x2(x[8 * jj + 4], x[8 * jj + 5]),
                                          pack_bf16x2(x[8 * jj + 6], x[8 * jj + 7]));
             }
-            named_sync(kBarSolve, kThreads);  // Nf and Lf free for the next unit
         }
+        __syncthreads();  // blocks and gates free for the next pair
     }
 
     __syncthreads();
@@ -375,7 +496,7 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
         mma_commit(bar(B_DRAIN));  // issued MMAs and loads land before TMEM and smem go away
         mbar_wait(bar(B_DRAIN), 0);
-        mbar_wait(bar(B_FULL), it & 1);
+        if (loads_issued > loads_landed) mbar_wait(bar(B_FULL), loads_landed & 1);
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
@@ -403,7 +524,7 @@ int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return GDR_ERR_CUDA;
     const int64_t pairs = (L.max_chunks * a.H + 1) / 2;  // upper bound; the kernel reads the count
-    const int64_t grid = pairs < 2 * (int64_t)sms ? pairs : 2 * (int64_t)sms;
+    const int64_t grid = pairs < 2 * (int64_t)sms ? pairs : 2 * (int64_t)sms;  // two CTAs per SM
     tc_solve_kernel<<<(unsigned)grid, kThreads, SMEM_BYTES, a.stream>>>(map_q, map_k, p);
     return cuda_status(cudaGetLastError());
 }
