@@ -16,19 +16,19 @@
 // both stored as bf16 [64][64] row-major: matrix 2u is T' and 2u + 1 is A^T of unit u,
 // units ordered chunk-major, head-minor. Each unit's decay factors go out with them
 // (fp32 [256]: g[64], gamma[64], kdec[64], then 1 for the ratio form and 0 otherwise),
-// so that the chain kernel uses the same values and the same form. (The two forms are described in prefill_tc.cu;
-// they differ only in where the decay factors are applied, and both kernels choose
-// the same form for a chunk.)
+// so that the chain kernel uses the same values and the same form. (The two forms are
+// described in prefill_tc.cu; they differ only in where the decay factors are applied.)
 //
 // Mapping. A CTA of 8 warps takes units two at a time; two CTAs share an SM. One
 // tcgen05.mma chain forms [K_a; K_b] [K_a; K_b; Q_a; Q_b]^T (M = 128, N = 256, K = d_k =
 // 128) in TMEM from TMA-loaded bf16 tiles: its diagonal 64x64 blocks are the units' K K^T
 // and K Q^T. All 8 warps read them out at once (warps 0-1: L of unit a from TMEM lanes
-// 0-63; 2-3: L of unit b, lanes 64-127; 4-5 and 6-7: A^T of a and b), then warps 0-3
-// solve unit a while warps 4-7 solve unit b. The solve is fp32 on the CUDA cores in
-// 16x16 blocks: the diagonal blocks by forward substitution, the others with warp-level
-// TF32 products. While a pair is solved, the next pair's keys and queries are loading
-// and its decay gates are in flight to registers.
+// 0-63; 2-3: L of unit b, lanes 64-127; 4-5 and 6-7: A^T of a and b), then warp 0
+// inverts unit a while warp 4 inverts unit b, and all 8 warps write T'. The inverse is
+// fp32 on the CUDA cores in 16x16 blocks, by one warp and without barriers: the diagonal
+// blocks by forward substitution, the others with warp-level TF32 products. While a
+// pair is solved, the next pair's keys and queries are loading and its decay gates are
+// in flight to registers.
 #include "tc_common.cuh"
 
 namespace gdr {
@@ -39,14 +39,25 @@ using namespace tc;
 
 constexpr int C = kChunk;
 constexpr int kThreads = 256;
-constexpr int kGroupThreads = 128;  // one unit's solve
-constexpr int BP = 17;              // fp32 pitch of a 16x16 block
-constexpr int BF = 16 * BP;         // floats per block
+// A 16x16 fp32 block is stored row-major with its columns permuted per row: element
+// (r, c) at r*16 + (c ^ sw(r)), sw(r) = 8*bit1(r) + 4*bit2(r). The permutation moves
+// groups of four columns, so row segments of 2 and 4 stay contiguous, and it makes both
+// fragment reads of the m16n8k8 TF32 MMA -- rows g, columns q (A) and rows q, columns g
+// (B), g < 8, q < 4 -- fall on 32 different banks.
+__host__ __device__ constexpr int sw(int r) { return (((r >> 1) & 1) << 3) | (((r >> 2) & 1) << 2); }
+__host__ __device__ constexpr int el(int r, int c) { return r * 16 + (c ^ sw(r)); }
+constexpr int BF = 256;             // floats per block
 // Lower-triangular 4x4 arrangement of 16x16 blocks: block (i, k), k <= i, at index
-// i(i+1)/2 + k. A unit has ten blocks of L (then of M = N_ii L_ik, and the diagonal
-// slots as scratch once the substitution has read them) and ten of N = (I + L)^{-1}.
-__host__ __device__ constexpr int blk(int i, int k) { return (i * (i + 1) / 2 + k) * BF; }
-constexpr int UNIT_FLOATS = 20 * BF;
+// i(i+1)/2 + k. A unit has sixteen block slots: the ten of L, where M_ik = N_ii L_ik
+// replaces L_ik (i > k) and N_ii replaces L_ii, then six for N_ik (i > k). Slots are
+// BF + 4 floats apart (16-byte aligned) so that the four diagonal blocks, read at the
+// same element by the forward substitution, start on different banks.
+constexpr int BS = BF + 4;
+__host__ __device__ constexpr int blk(int i, int k) { return (i * (i + 1) / 2 + k) * BS; }
+__host__ __device__ constexpr int nblk(int i, int k) {  // N_ik, i > k
+    return (10 + (i - k == 1 ? k : (i - k == 2 ? 3 + k : 5))) * BS;
+}
+constexpr int UNIT_FLOATS = 16 * BS;
 
 // per d_k half b (32 KB): K_a | K_b | Q_a | Q_b, 8 KB each; rows 0-127 are the MMA's A
 // operand, rows 0-255 its B operand
@@ -76,150 +87,129 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
 
 __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4],
                                                 const uint32_t (&b)[2]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+    // not volatile: independent products may interleave (the outputs keep it alive)
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
         "{%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// d (+)= A * B for 16x16 blocks A and B (pitch BP); d holds the result's two 16x8 halves
-// in the m16n8 accumulator layout.
+// d (+)= A * B for 16x16 blocks A and B (layout el); d holds the result's two 16x8
+// halves in the m16n8 accumulator layout.
 __device__ __forceinline__ void warp_gemm16(const float *__restrict__ A, const float *__restrict__ B,
                                             float (&d)[2][4], int lane) {
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        const uint32_t a[4] = {to_tf32(A[g * BP + 8 * ks + q]), to_tf32(A[(g + 8) * BP + 8 * ks + q]),
-                               to_tf32(A[g * BP + 8 * ks + q + 4]),
-                               to_tf32(A[(g + 8) * BP + 8 * ks + q + 4])};
+        const uint32_t a[4] = {to_tf32(A[el(g, 8 * ks + q)]), to_tf32(A[el(g + 8, 8 * ks + q)]),
+                               to_tf32(A[el(g, 8 * ks + q + 4)]), to_tf32(A[el(g + 8, 8 * ks + q + 4)])};
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t b[2] = {to_tf32(B[(8 * ks + q) * BP + 8 * nt + g]),
-                                   to_tf32(B[(8 * ks + q + 4) * BP + 8 * nt + g])};
+            const uint32_t b[2] = {to_tf32(B[el(8 * ks + q, 8 * nt + g)]),
+                                   to_tf32(B[el(8 * ks + q + 4, 8 * nt + g)])};
             mma_tf32_16x8x8(d[nt], a, b);
         }
     }
 }
 
-// d = scale * M (load) or M = scale * d (store) for a 16x16 block M in the accumulator layout.
-__device__ __forceinline__ void warp_load16(const float *__restrict__ M, float (&d)[2][4], int lane,
-                                            float scale) {
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        d[nt][0] = scale * M[g * BP + 8 * nt + 2 * q];
-        d[nt][1] = scale * M[g * BP + 8 * nt + 2 * q + 1];
-        d[nt][2] = scale * M[(g + 8) * BP + 8 * nt + 2 * q];
-        d[nt][3] = scale * M[(g + 8) * BP + 8 * nt + 2 * q + 1];
-    }
-}
-
+// M = scale * d for a 16x16 block M, d in the accumulator layout.
 __device__ __forceinline__ void warp_store16(float *__restrict__ M, const float (&d)[2][4], int lane,
                                              float scale) {
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-        M[g * BP + 8 * nt + 2 * q] = scale * d[nt][0];
-        M[g * BP + 8 * nt + 2 * q + 1] = scale * d[nt][1];
-        M[(g + 8) * BP + 8 * nt + 2 * q] = scale * d[nt][2];
-        M[(g + 8) * BP + 8 * nt + 2 * q + 1] = scale * d[nt][3];
+        *reinterpret_cast<float2 *>(M + el(g, 8 * nt + 2 * q)) = make_float2(scale * d[nt][0], scale * d[nt][1]);
+        *reinterpret_cast<float2 *>(M + el(g + 8, 8 * nt + 2 * q)) =
+            make_float2(scale * d[nt][2], scale * d[nt][3]);
     }
 }
 
-// N = (I + L)^{-1} for the strictly lower-triangular 64x64 L held as blocks in Lb, by a
-// group of 128 threads (4 warps, named barrier `bar_id`); N's ten lower blocks go to Nb.
-//   1. N_ii by forward substitution, one column of one diagonal block per thread.
-//   2. With M_ik = N_ii L_ik (i > k): N_ij = -sum_{k=j}^{i-1} M_ik N_kj, scheduled in four
-//      rounds so that every round holds at most two dependent block products:
-//        R1  M_10, M_21, M_32, M_20
-//        R2  N_10, N_21, N_32, M_31
-//        R3  N_20, N_31 (two products each); M_30 and P = M_30 N_00; Q = M_31 N_10
-//        R4  N_30 = -(P + Q + M_32 N_20)
-//      M blocks overwrite the L blocks they come from; P and Q go into the diagonal L
-//      slots of blocks 0 and 1, which the substitution no longer needs.
-__device__ __forceinline__ void unit_lower_inverse(float *__restrict__ Lb, float *__restrict__ Nb,
-                                                   int gtid, int bar_id) {
-    if (gtid < C) {
-        const int b = gtid >> 4, c = gtid & 15;
-        const float *Ld = Lb + blk(b, b);
-        float x[16];
+// N = (I + L)^{-1} for the strictly lower-triangular 64x64 L held as blocks in U (see
+// blk, nblk), by one warp:
+//   1. N_ii by forward substitution: lane l takes columns 2(l%8), 2(l%8)+1 of block l/8.
+//   2. M_ik = N_ii L_ik for the six blocks below the diagonal (over L_ik).
+//   3. N_ij = -sum_{k=j}^{i-1} M_ik N_kj by distance from the diagonal, with the partial
+//      sums that do not need the previous level formed one level early, so that the
+//      dependent chain is four block products long.
+__device__ __forceinline__ void warp_lower_inverse(float *__restrict__ U, int lane) {
+    {
+        const int b = lane >> 3, c0 = 2 * (lane & 7);
+        float *D = U + blk(b, b);
+        float x0[16], x1[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) {
+            x0[r] = (r == c0) ? 1.f : 0.f;
+            x1[r] = (r == c0 + 1) ? 1.f : 0.f;
+        }
 #pragma unroll
         for (int k = 0; k < 15; ++k) {
-            const float xk = x[k];
+            const float a0 = x0[k], a1 = x1[k];
 #pragma unroll
-            for (int r = k + 1; r < 16; ++r) x[r] = fmaf(-Ld[r * BP + k], xk, x[r]);
+            for (int r = k + 1; r < 16; ++r) {
+                const float l = D[el(r, k)];
+                x0[r] = fmaf(-l, a0, x0[r]);
+                x1[r] = fmaf(-l, a1, x1[r]);
+            }
         }
-        float *Nd = Nb + blk(b, b);
+        __syncwarp();
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Nd[r * BP + c] = x[r];
+        for (int r = 0; r < 16; ++r) *reinterpret_cast<float2 *>(D + el(r, c0)) = make_float2(x0[r], x1[r]);
+        __syncwarp();
     }
-    named_sync(bar_id, kGroupThreads);
-    const int w = gtid >> 5, lane = gtid & 31;
-    float acc[2][4];
-    auto zero = [&]() {
+    typedef float Acc[2][4];
+    auto zero = [](Acc &a) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+            for (int e = 0; e < 4; ++e) a[nt][e] = 0.f;
     };
-    // R1: M_10, M_21, M_32, M_20 = N_ii L_ik
-    {
-        const int i = w == 3 ? 2 : w + 1, k = w == 3 ? 0 : w;
-        zero();
-        warp_gemm16(Nb + blk(i, i), Lb + blk(i, k), acc, lane);
-        __syncwarp();
-        warp_store16(Lb + blk(i, k), acc, lane, 1.f);
-    }
-    named_sync(bar_id, kGroupThreads);
-    // R2: N_10, N_21, N_32 = -M_{j+1,j} N_jj; M_31 = N_33 L_31
-    zero();
-    if (w < 3) {
-        warp_gemm16(Lb + blk(w + 1, w), Nb + blk(w, w), acc, lane);
-        warp_store16(Nb + blk(w + 1, w), acc, lane, -1.f);
-    } else {
-        warp_gemm16(Nb + blk(3, 3), Lb + blk(3, 1), acc, lane);
-        __syncwarp();
-        warp_store16(Lb + blk(3, 1), acc, lane, 1.f);
-    }
-    named_sync(bar_id, kGroupThreads);
-    // R3
-    zero();
-    if (w == 0) {  // N_20 = -(M_20 N_00 + M_21 N_10)
-        warp_gemm16(Lb + blk(2, 0), Nb + blk(0, 0), acc, lane);
-        warp_gemm16(Lb + blk(2, 1), Nb + blk(1, 0), acc, lane);
-        warp_store16(Nb + blk(2, 0), acc, lane, -1.f);
-    } else if (w == 1) {  // N_31 = -(M_31 N_11 + M_32 N_21)
-        warp_gemm16(Lb + blk(3, 1), Nb + blk(1, 1), acc, lane);
-        warp_gemm16(Lb + blk(3, 2), Nb + blk(2, 1), acc, lane);
-        warp_store16(Nb + blk(3, 1), acc, lane, -1.f);
-    } else if (w == 2) {  // M_30 = N_33 L_30, then P = M_30 N_00 into the L_00 slot
-        warp_gemm16(Nb + blk(3, 3), Lb + blk(3, 0), acc, lane);
-        warp_store16(Lb + blk(3, 0), acc, lane, 1.f);
-        __syncwarp();
-        zero();
-        warp_gemm16(Lb + blk(3, 0), Nb + blk(0, 0), acc, lane);
-        warp_store16(Lb + blk(0, 0), acc, lane, 1.f);
-    } else {  // Q = M_31 N_10 into the L_11 slot
-        warp_gemm16(Lb + blk(3, 1), Nb + blk(1, 0), acc, lane);
-        warp_store16(Lb + blk(1, 1), acc, lane, 1.f);
-    }
-    named_sync(bar_id, kGroupThreads);
-    // R4: N_30 = -(P + Q + M_32 N_20)
-    if (w == 0) {
-        float q2[2][4];
-        warp_load16(Lb + blk(0, 0), acc, lane, 1.f);
-        warp_load16(Lb + blk(1, 1), q2, lane, 1.f);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] += q2[nt][e];
-        warp_gemm16(Lb + blk(3, 2), Nb + blk(2, 0), acc, lane);
-        warp_store16(Nb + blk(3, 0), acc, lane, -1.f);
-    }
-    named_sync(bar_id, kGroupThreads);
+    Acc a0, a1, a2, a3, a4, a5;
+    // M_10, M_21, M_32, M_20, M_31, M_30
+    zero(a0); zero(a1); zero(a2); zero(a3); zero(a4); zero(a5);
+    warp_gemm16(U + blk(1, 1), U + blk(1, 0), a0, lane);
+    warp_gemm16(U + blk(2, 2), U + blk(2, 1), a1, lane);
+    warp_gemm16(U + blk(3, 3), U + blk(3, 2), a2, lane);
+    warp_gemm16(U + blk(2, 2), U + blk(2, 0), a3, lane);
+    warp_gemm16(U + blk(3, 3), U + blk(3, 1), a4, lane);
+    warp_gemm16(U + blk(3, 3), U + blk(3, 0), a5, lane);
+    __syncwarp();
+    warp_store16(U + blk(1, 0), a0, lane, 1.f);
+    warp_store16(U + blk(2, 1), a1, lane, 1.f);
+    warp_store16(U + blk(3, 2), a2, lane, 1.f);
+    warp_store16(U + blk(2, 0), a3, lane, 1.f);
+    warp_store16(U + blk(3, 1), a4, lane, 1.f);
+    warp_store16(U + blk(3, 0), a5, lane, 1.f);
+    __syncwarp();
+    // level 1: N_10, N_21, N_32; partial sums P20 = M_20 N_00, P31 = M_31 N_11, P30 = M_30 N_00
+    zero(a0); zero(a1); zero(a2); zero(a3); zero(a4); zero(a5);
+    warp_gemm16(U + blk(1, 0), U + blk(0, 0), a0, lane);
+    warp_gemm16(U + blk(2, 1), U + blk(1, 1), a1, lane);
+    warp_gemm16(U + blk(3, 2), U + blk(2, 2), a2, lane);
+    warp_gemm16(U + blk(2, 0), U + blk(0, 0), a3, lane);
+    warp_gemm16(U + blk(3, 1), U + blk(1, 1), a4, lane);
+    warp_gemm16(U + blk(3, 0), U + blk(0, 0), a5, lane);
+    warp_store16(U + nblk(1, 0), a0, lane, -1.f);
+    warp_store16(U + nblk(2, 1), a1, lane, -1.f);
+    warp_store16(U + nblk(3, 2), a2, lane, -1.f);
+    __syncwarp();
+    // level 2: N_20 = -(P20 + M_21 N_10), N_31 = -(P31 + M_32 N_21); P30 += M_31 N_10
+    warp_gemm16(U + blk(2, 1), U + nblk(1, 0), a3, lane);
+    warp_gemm16(U + blk(3, 2), U + nblk(2, 1), a4, lane);
+    warp_gemm16(U + blk(3, 1), U + nblk(1, 0), a5, lane);
+    warp_store16(U + nblk(2, 0), a3, lane, -1.f);
+    warp_store16(U + nblk(3, 1), a4, lane, -1.f);
+    __syncwarp();
+    // level 3: N_30 = -(P30 + M_32 N_20)
+    warp_gemm16(U + blk(3, 2), U + nblk(2, 0), a5, lane);
+    warp_store16(U + nblk(3, 0), a5, lane, -1.f);
+    __syncwarp();
+}
+
+// Element (t, i), i <= t, of N = (I + L)^{-1} in the unit's block slots.
+__device__ __forceinline__ float n_entry(const float *__restrict__ U, int t, int i) {
+    const int bt = t >> 4, bi = i >> 4;
+    const int base = bt == bi ? blk(bt, bt) : nblk(bt, bi);
+    return U[base + el(t & 15, i & 15)];
 }
 
 struct SolveParams {
@@ -249,7 +239,6 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     float *__restrict__ gates = reinterpret_cast<float *>(sm + OFF_GATE);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int group = warp >> 2, gtid = tid & 127;  // solve group: unit a (0) or b (1)
 
     // unit u -> (chunk, head); the second unit of an odd last pair repeats the first
     auto unit_of = [&](int pair, int which) {
@@ -400,9 +389,12 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                         for (int m = 0; m < 2; ++m) {
                             const int ib = 2 * hh + m;
                             if (ib <= (t >> 4)) {
-                                float *row = Lb + blk(t >> 4, ib) + (t & 15) * BP;
+                                float *blockp = Lb + blk(t >> 4, ib);
 #pragma unroll
-                                for (int e = 0; e < 16; ++e) row[e] = v[16 * m + e];
+                                for (int e4 = 0; e4 < 4; ++e4)
+                                    *reinterpret_cast<float4 *>(blockp + el(t & 15, 4 * e4)) =
+                                        make_float4(v[16 * m + 4 * e4], v[16 * m + 4 * e4 + 1],
+                                                    v[16 * m + 4 * e4 + 2], v[16 * m + 4 * e4 + 3]);
                             }
                         }
                     }
@@ -455,17 +447,19 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         __syncthreads();
         if (tid == 0 && next < n_pairs && !issue_gram(it + 1)) *fail = 1;
 
-        // ---- each group solves its unit: T' = diag(kdec) (I + L)^{-1} diag(beta) (ratio
-        // form; no kdec otherwise), bf16
+        // ---- warp 0 inverts unit a, warp 4 unit b
+        if ((warp & 3) == 0 && 2 * pair + (warp >> 2) < n_units)
+            warp_lower_inverse(reinterpret_cast<float *>(sm + OFF_LN) + (warp >> 2) * UNIT_FLOATS, lane);
+        __syncthreads();
+        // ---- T' = diag(kdec) (I + L)^{-1} diag(beta) (ratio form; no kdec otherwise), bf16:
+        // warps 0-3 unit a, warps 4-7 unit b, one half row per thread
         {
-            const int u = 2 * pair + group;
+            const int which = warp >> 2, u = 2 * pair + which;
             if (u < n_units) {
-                float *Lb = reinterpret_cast<float *>(sm + OFF_LN) + group * UNIT_FLOATS;
-                float *Nb = Lb + 10 * BF;
-                const float *g = gates + group * G_UNIT;
+                const float *U = reinterpret_cast<const float *>(sm + OFF_LN) + which * UNIT_FLOATS;
+                const float *g = gates + which * G_UNIT;
                 const bool ratio = g[G_G + C - 1] > kRatioSafeLogDecay;
-                unit_lower_inverse(Lb, Nb, gtid, 1 + group);
-                const int t = gtid >> 1, hh = gtid & 1;
+                const int gtid = tid & 127, t = gtid >> 1, hh = gtid & 1;
                 const float kd = ratio ? g[G_KDEC + t] : 1.f;
                 float x[32], bv[32];
                 const float4 *bp = reinterpret_cast<const float4 *>(g + G_BETA + 32 * hh);
@@ -477,7 +471,7 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
                 for (int ii = 0; ii < 32; ++ii) {
                     const int i = 32 * hh + ii;
-                    x[ii] = (i <= t) ? Nb[blk(t >> 4, i >> 4) + (t & 15) * BP + (i & 15)] * bv[ii] * kd : 0.f;
+                    x[ii] = (i <= t) ? n_entry(U, t, i) * bv[ii] * kd : 0.f;
                 }
                 uint4 *dst = reinterpret_cast<uint4 *>(p.Tout + ((size_t)(2 * u) * C + t) * C + 32 * hh);
 #pragma unroll
