@@ -665,7 +665,7 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L) {
         !tc::make_map_thd(&mo, a.o, a.dv, a.H, a.total_tokens) ||
         !tc::make_map_units(&mt, a.ws + L.T, 2 * L.max_chunks * a.H))
         return GDR_ERR_CUDA;
-    const int st = tc::launch_solve_tc(a, L, mq, mk);
+    const int st = tc::launch_solve_tc(a, L, mq, mk, mt);
     if (st != GDR_OK) return st;
     TcParams p;
     p.S0 = a.S0;

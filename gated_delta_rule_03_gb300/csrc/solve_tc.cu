@@ -19,16 +19,20 @@
 // so that the chain kernel uses the same values and the same form. (The two forms are
 // described in prefill_tc.cu; they differ only in where the decay factors are applied.)
 //
-// Mapping. A CTA of 8 warps takes units two at a time; two CTAs share an SM. One
-// tcgen05.mma chain forms [K_a; K_b] [K_a; K_b; Q_a; Q_b]^T (M = 128, N = 256, K = d_k =
-// 128) in TMEM from TMA-loaded bf16 tiles: its diagonal 64x64 blocks are the units' K K^T
-// and K Q^T. All 8 warps read them out at once (warps 0-1: L of unit a from TMEM lanes
-// 0-63; 2-3: L of unit b, lanes 64-127; 4-5 and 6-7: A^T of a and b), then warp 0
-// inverts unit a while warp 4 inverts unit b, and all 8 warps write T'. The inverse is
-// fp32 on the CUDA cores in 16x16 blocks, by one warp and without barriers: the diagonal
-// blocks by forward substitution, the others with warp-level TF32 products. While a
-// pair is solved, the next pair's keys and queries are loading and its decay gates are
-// in flight to registers.
+// Mapping. One CTA per SM walks unit pairs as a pipeline of warp roles joined by
+// mbarriers:
+//   warp 4      loads a pair's keys and queries by TMA into one of two stage slots and
+//               issues its Gram chain [K_a; K_b] [K_a; K_b; Q_a; Q_b]^T (tcgen05, M = 128,
+//               N = 256, K = d_k = 128) into one of two TMEM slots; the diagonal 64x64
+//               blocks are each unit's K K^T and K Q^T;
+//   warps 0-3   read a TMEM slot out (warps 0-1: unit a, TMEM lanes 0-63; 2-3: unit b,
+//               lanes 64-127): the unit's decay factors, its decayed L into fp32 16x16
+//               blocks of one of four solver slots, and its masked, decayed A^T straight
+//               to the workspace;
+//   warps 5-8   one solver warp per slot: the inverse of I + L, then T' in bf16.
+// The inverse is fp32 on the CUDA cores in 16x16 blocks, by one warp and without
+// barriers: the diagonal blocks by forward substitution, the others with warp-level TF32
+// products.
 #include "tc_common.cuh"
 
 namespace gdr {
@@ -38,7 +42,8 @@ using namespace sm100;
 using namespace tc;
 
 constexpr int C = kChunk;
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;  // 9 warps
+constexpr int kProducerWarp = 4, kSolverWarp0 = 5, kSolvers = 4;
 // A 16x16 fp32 block is stored row-major with its columns permuted per row: element
 // (r, c) at r*16 + (c ^ sw(r)), sw(r) = 8*bit1(r) + 4*bit2(r). The permutation moves
 // groups of four columns, so row segments of 2 and 4 stay contiguous, and it makes both
@@ -59,20 +64,30 @@ __host__ __device__ constexpr int nblk(int i, int k) {  // N_ik, i > k
 }
 constexpr int UNIT_FLOATS = 16 * BS;
 
-// per d_k half b (32 KB): K_a | K_b | Q_a | Q_b, 8 KB each; rows 0-127 are the MMA's A
-// operand, rows 0-255 its B operand
-constexpr uint32_t OFF_K = 0;
-constexpr uint32_t OFF_LN = 65536;                             // two units' L, N blocks
-constexpr uint32_t OFF_GATE = OFF_LN + 2 * UNIT_FLOATS * 4;
+// Stage slot (64 KB), per d_k half b (32 KB): K_a | K_b | Q_a | Q_b, 8 KB each; rows
+// 0-127 are the Gram chain's A operand, rows 0-255 its B operand.
+constexpr uint32_t STAGE = 65536;
+constexpr uint32_t OFF_LS = 2 * STAGE;  // solver slots: blocks, then the unit's gates
 constexpr int G_G = 0, G_GAM = 64, G_GINV = 128, G_BETA = 192, G_KDEC = 256, G_UNIT = 320;
-constexpr uint32_t OFF_BAR = OFF_GATE + 2 * G_UNIT * 4;  // per unit: g, gamma, 1/gamma, beta, kdec
-constexpr uint32_t SMEM_USED = OFF_BAR + 64;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
-static_assert((SMEM_BYTES + 1024) * 2 <= 228 * 1024, "two CTAs per SM");
-enum { B_FULL = 0, B_MMA, B_DRAIN, B_COUNT };
+constexpr uint32_t LSLOT = 18432;  // blocks, gates; 1024-aligned (its first 8 KB stage T')
+static_assert(UNIT_FLOATS * 4 + G_UNIT * 4 <= LSLOT && UNIT_FLOATS * 4 >= 8192, "solver slot");
+constexpr uint32_t OFF_BAR = OFF_LS + kSolvers * LSLOT;
+enum {
+    B_STF0 = 0, B_STF1,  // stage slot loaded                  (tx bytes)
+    B_STE0, B_STE1,      // stage slot read by the Gram chain   (commit)
+    B_TMF0, B_TMF1,      // TMEM slot holds a pair's Gram       (commit)
+    B_TME0, B_TME1,      // TMEM slot read out                  (128 read-out arrivals)
+    B_LF0, B_LF1, B_LF2, B_LF3,  // solver slot filled          (64 read-out arrivals)
+    B_LE0, B_LE1, B_LE2, B_LE3,  // solver slot free again      (solver lane 0)
+    B_DRAIN,
+    B_COUNT
+};
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * B_COUNT;
 constexpr uint32_t OFF_FAIL = OFF_TMEM_SLOT + 4;
-constexpr uint32_t TM_COLS = 256;
+constexpr uint32_t SMEM_USED = OFF_FAIL + 16;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
+static_assert(SMEM_BYTES <= 232448 && LSLOT % 1024 == 0 && OFF_LS % 1024 == 0, "shared memory");
+constexpr uint32_t TM_COLS = 512;  // two 256-column slots
 
 // ---------------------------------------------------------------- warp-level 16x16 products
 // The unit lower-triangular solve combines 16x16 blocks. These products are far below
@@ -205,11 +220,54 @@ __device__ __forceinline__ void warp_lower_inverse(float *__restrict__ U, int la
     __syncwarp();
 }
 
-// Element (t, i), i <= t, of N = (I + L)^{-1} in the unit's block slots.
-__device__ __forceinline__ float n_entry(const float *__restrict__ U, int t, int i) {
-    const int bt = t >> 4, bi = i >> 4;
-    const int base = bt == bi ? blk(bt, bt) : nblk(bt, bi);
-    return U[base + el(t & 15, i & 15)];
+// T' = diag(kd) N diag(beta) in bf16 (kd = kdec in the ratio form, else 1), by one warp,
+// into a 128-byte-swizzled [64][64] tile at `tile` (the layout a TMA store reads) that
+// overlays the first 8 KB of U: N's ten blocks are read into registers in the m16n8
+// accumulator layout first, the blocks above the diagonal are zero.
+__device__ __forceinline__ void warp_stage_tprime(float *__restrict__ U, const float *__restrict__ g,
+                                                  bool ratio, unsigned char *tile, int lane) {
+    const int gq = lane >> 2, q = lane & 3;
+    float n[10][2][4];
+#pragma unroll
+    for (int bt = 0; bt < 4; ++bt)
+#pragma unroll
+        for (int bi = 0; bi <= bt; ++bi) {
+            const float *B = U + (bt == bi ? blk(bt, bt) : nblk(bt, bi));
+            const int idx = bt * (bt + 1) / 2 + bi;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const float2 lo = *reinterpret_cast<const float2 *>(B + el(gq, 8 * nt + 2 * q));
+                const float2 hi = *reinterpret_cast<const float2 *>(B + el(gq + 8, 8 * nt + 2 * q));
+                n[idx][nt][0] = lo.x; n[idx][nt][1] = lo.y; n[idx][nt][2] = hi.x; n[idx][nt][3] = hi.y;
+            }
+        }
+    __syncwarp();
+#pragma unroll
+    for (int bt = 0; bt < 4; ++bt) {
+        float kd[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) kd[h] = ratio ? g[G_KDEC + 16 * bt + gq + 8 * h] : 1.f;
+#pragma unroll
+        for (int bi = 0; bi < 4; ++bi)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int i0 = 16 * bi + 8 * nt + 2 * q;  // columns i0, i0 + 1
+                const float b0 = g[G_BETA + i0], b1 = g[G_BETA + i0 + 1];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = 16 * bt + gq + 8 * h;
+                    float x0 = 0.f, x1 = 0.f;
+                    if (bi <= bt) {
+                        const int idx = bt * (bt + 1) / 2 + bi;
+                        // within a diagonal block the entries above the diagonal are zero
+                        x0 = (i0 <= t) ? n[idx][nt][2 * h] * b0 * kd[h] : 0.f;
+                        x1 = (i0 + 1 <= t) ? n[idx][nt][2 * h + 1] * b1 * kd[h] : 0.f;
+                    }
+                    *reinterpret_cast<uint32_t *>(tile + t * 128 + ((((i0 >> 3) ^ t) & 7) << 4) + (i0 & 7) * 2) =
+                        pack_bf16x2(x0, x1);
+                }
+            }
+    }
 }
 
 struct SolveParams {
@@ -221,13 +279,16 @@ struct SolveParams {
     float *Gout;          // [chunks * H][256]: g, gamma, kdec, form flag per unit
 };
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                const SolveParams p) {
+                const __grid_constant__ CUtensorMap map_t, const SolveParams p) {
     if (p.ctl[0] != GDR_OK) return;
     const int n_units = p.ctl[1] * p.H;
     const int n_pairs = (n_units + 1) / 2;
     if ((int)blockIdx.x >= n_pairs) return;
+    // this CTA's pairs: blockIdx.x + k * gridDim.x, k < K
+    const int K = (n_pairs - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    auto pair_of = [&](int k) { return (int)blockIdx.x + k * (int)gridDim.x; };
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -236,61 +297,27 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TMEM_SLOT);
     volatile int *fail = reinterpret_cast<volatile int *>(sm + OFF_FAIL);
-    float *__restrict__ gates = reinterpret_cast<float *>(sm + OFF_GATE);
+    auto lslot = [&](int s) { return reinterpret_cast<float *>(sm + OFF_LS + s * LSLOT); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // unit u -> (chunk, head); the second unit of an odd last pair repeats the first
-    auto unit_of = [&](int pair, int which) {
-        const int u = 2 * pair + which;
-        return u < n_units ? u : 2 * pair;
-    };
-    int loads_issued = 0, loads_landed = 0;  // (thread 0) for the drain after an abort
-    auto load_pair = [&](int pair) {  // one thread
-        ++loads_issued;
-        mbar_arrive_expect_tx(bar(B_FULL), 8 * 8192);
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            const int u = unit_of(pair, which);
-            const int4 pl = p.plan[u / p.H];
-            const int h = u % p.H;
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                const uint32_t blkaddr = sbase + OFF_K + b * 32768 + which * 8192;
-                tma_load_3d(blkaddr, &map_k, bar(B_FULL), 64 * b, h, pl.y);
-                tma_load_3d(blkaddr + 16384, &map_q, bar(B_FULL), 64 * b, h, pl.y);
-            }
-        }
-    };
-    // decay gates of one unit of `pair` (warp 0: unit a, warp 1: unit b), into registers
-    float ga0 = 0.f, ga1 = 0.f, gb0 = 0.f, gb1 = 0.f;
-    auto fetch_gates = [&](int pair) {
-        ga0 = ga1 = gb0 = gb1 = 0.f;
-        const int u = 2 * pair + warp;
-        if (u < n_units) {
-            const int4 pl = p.plan[u / p.H];
-            const int h = u % p.H, len = pl.z;
-            if (2 * lane < len) {
-                const size_t off = (size_t)(pl.y + 2 * lane) * p.H + h;
-                ga0 = p.log_alpha[off];
-                gb0 = p.beta[off];
-            }
-            if (2 * lane + 1 < len) {
-                const size_t off = (size_t)(pl.y + 2 * lane + 1) * p.H + h;
-                ga1 = p.log_alpha[off];
-                gb1 = p.beta[off];
-            }
-        }
-    };
-
     if (tid == 0) {
-        mbar_init(bar(B_FULL), 1);
-        mbar_init(bar(B_MMA), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_STF0 + i), 1);
+            mbar_init(bar(B_STE0 + i), 1);
+            mbar_init(bar(B_TMF0 + i), 1);
+            mbar_init(bar(B_TME0 + i), 128);
+        }
+        for (int i = 0; i < kSolvers; ++i) {
+            mbar_init(bar(B_LF0 + i), 64);
+            mbar_init(bar(B_LE0 + i), 1);
+        }
         mbar_init(bar(B_DRAIN), 1);
         fence_mbar_init();
         *fail = 0;
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_q);
+        prefetch_tensormap(&map_t);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), TM_COLS);
@@ -300,82 +327,126 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
 
-    // the Gram chain of `pair` (thread 0), once its keys and queries have landed
-    auto issue_gram = [&](int it_) -> bool {
-        if (!mbar_wait(bar(B_FULL), it_ & 1)) return false;
-        ++loads_landed;
-        tc_fence_after();
+    if (warp == kProducerWarp) {
+        // ============================================================ loads and Gram chains
+        if (lane == 0) {
+            int loads = 0, landed = 0;
+            for (int k = 0; k <= K && !*fail; ++k) {
+                if (k < K) {  // load pair k into stage slot k % 2 (free once Gram k - 2 has read it)
+                    const int sl = k & 1;
+                    if (k >= 2 && !mbar_wait(bar(B_STE0 + sl), ((k >> 1) - 1) & 1)) { *fail = 1; break; }
+                    mbar_arrive_expect_tx(bar(B_STF0 + sl), 8 * 8192);
+                    ++loads;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = sbase + OFF_K + (kk >> 2) * 32768 + (kk & 3) * 32;
-            mma_bf16(tmem, sw128_desc(off, 16, 1024), sw128_desc(off, 16, 1024), idesc_bf16(128, 256, 0, 0),
-                     kk > 0);
-        }
-        mma_commit(bar(B_MMA));
-        return true;
-    };
-    if (tid == 0) {
-        load_pair(blockIdx.x);
-        if (!issue_gram(0)) *fail = 1;
-    }
-    if (warp < 2) fetch_gates(blockIdx.x);
-    int it = 0;
-    for (int pair = blockIdx.x; pair < n_pairs; pair += gridDim.x, ++it) {
-        const int next = pair + (int)gridDim.x;
-        // ---- gates of both units (warp 0: unit a, warp 1: unit b) by the shared scan;
-        // then the next pair's gates are fetched
-        if (warp < 2) {
-            float *g = gates + warp * G_UNIT;
-            const ChunkScan sc = chunk_scan(ga0, ga1, lane);
-            g[G_G + 2 * lane] = sc.g0;
-            g[G_G + 2 * lane + 1] = sc.g1;
-            g[G_GAM + 2 * lane] = fast_exp(sc.g0);
-            g[G_GAM + 2 * lane + 1] = fast_exp(sc.g1);
-            g[G_GINV + 2 * lane] = fast_exp(-sc.g0);
-            g[G_GINV + 2 * lane + 1] = fast_exp(-sc.g1);
-            g[G_BETA + 2 * lane] = gb0;
-            g[G_BETA + 2 * lane + 1] = gb1;
-            g[G_KDEC + 2 * lane] = fast_exp(sc.g_last - sc.g0);
-            g[G_KDEC + 2 * lane + 1] = fast_exp(sc.g_last - sc.g1);
-            if (next < n_pairs) fetch_gates(next);
-        }
-        // ---- the pair's Gram chain (issued before) has completed: its stage takes the next pair
-        if (tid == 0) {
-            if (*fail == 0 && mbar_wait(bar(B_MMA), it & 1)) {
-                if (next < n_pairs) load_pair(next);
-            } else {
-                *fail = 1;
+                    for (int which = 0; which < 2; ++which) {
+                        int u = 2 * pair_of(k) + which;
+                        if (u >= n_units) u = 2 * pair_of(k);  // a missing unit b repeats a
+                        const int4 pl = p.plan[u / p.H];
+                        const int h = u % p.H;
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const uint32_t dst = sbase + sl * STAGE + b * 32768 + which * 8192;
+                            tma_load_3d(dst, &map_k, bar(B_STF0 + sl), 64 * b, h, pl.y);
+                            tma_load_3d(dst + 16384, &map_q, bar(B_STF0 + sl), 64 * b, h, pl.y);
+                        }
+                    }
+                }
+                if (k >= 1) {  // Gram of pair j = k - 1 into TMEM slot j % 2 (free once read out)
+                    const int j = k - 1, sl = j & 1;
+                    if (!mbar_wait(bar(B_STF0 + sl), (j >> 1) & 1)) { *fail = 1; break; }
+                    ++landed;
+                    if (j >= 2 && !mbar_wait(bar(B_TME0 + sl), ((j >> 1) - 1) & 1)) { *fail = 1; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = sbase + sl * STAGE + (kk >> 2) * 32768 + (kk & 3) * 32;
+                        mma_bf16(tmem + 256 * sl, sw128_desc(off, 16, 1024), sw128_desc(off, 16, 1024),
+                                 idesc_bf16(128, 256, 0, 0), kk > 0);
+                    }
+                    mma_commit(bar(B_STE0 + sl));
+                    mma_commit(bar(B_TMF0 + sl));
+                }
+            }
+            if (*fail) {  // issued MMAs and loads land before TMEM and shared memory go away
+                mma_commit(bar(B_DRAIN));
+                mbar_wait(bar(B_DRAIN), 0);
+                for (int j = landed; j < loads; ++j) mbar_wait(bar(B_STF0 + (j & 1)), (j >> 1) & 1);
             }
         }
-        __syncthreads();
-        if (*fail) break;
-        tc_fence_after();
-
-        // ---- read-out: L blocks of both units (warps 0-3), A^T and the factors (warps 4-7)
-        {
-            const int which = (warp >> 1) & 1;  // unit of this warp's TMEM lanes
-            const int u = 2 * pair + which;
-            const float *g = gates + which * G_UNIT;
-            const bool ratio = g[G_G + C - 1] > kRatioSafeLogDecay;
-            const int t = 32 * (warp & 1) + lane;  // token row (TMEM lane 64 which + t)
-            if (u < n_units) {
-                if (warp < 4) {
-                    // L_ti = beta_t Gamma_ti k_t.k_i (i < t) into the unit's blocks
-                    float *Lb = reinterpret_cast<float *>(sm + OFF_LN) + which * UNIT_FLOATS;
+    } else if (warp < 4) {
+        // ============================================================ read-out
+        const int which = warp >> 1;          // unit a (0) or b (1) of each pair
+        const int t = 32 * (warp & 1) + lane; // token row = TMEM lane 64 which + t
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+        // decay gates of this warp pair's unit of pair k, into registers (warp 2 which)
+        float ga0 = 0.f, ga1 = 0.f, gb0 = 0.f, gb1 = 0.f;
+        auto fetch_gates = [&](int k) {
+            ga0 = ga1 = gb0 = gb1 = 0.f;
+            const int u = 2 * pair_of(k) + which;
+            if (k < K && u < n_units) {
+                const int4 pl = p.plan[u / p.H];
+                const int h = u % p.H, len = pl.z;
+                if (2 * lane < len) {
+                    const size_t off = (size_t)(pl.y + 2 * lane) * p.H + h;
+                    ga0 = p.log_alpha[off];
+                    gb0 = p.beta[off];
+                }
+                if (2 * lane + 1 < len) {
+                    const size_t off = (size_t)(pl.y + 2 * lane + 1) * p.H + h;
+                    ga1 = p.log_alpha[off];
+                    gb1 = p.beta[off];
+                }
+            }
+        };
+        if ((warp & 1) == 0) fetch_gates(0);
+        for (int k = 0; k < K; ++k) {
+            const int sl = k & 1;
+            const int lu = 2 * k + which, ls = lu % kSolvers;  // local unit and its solver slot
+            const int u = 2 * pair_of(k) + which;
+            const bool exists = u < n_units;
+            float *U = lslot(ls);
+            float *g = U + UNIT_FLOATS;
+            bool ok = true;
+            if (exists && lu >= kSolvers) ok = mbar_wait(bar(B_LE0 + ls), ((lu / kSolvers) - 1) & 1);
+            if (!ok) *fail = 1;
+            if ((warp & 1) == 0) {  // the unit's gates, by the shared scan; then the next pair's
+                const ChunkScan sc = chunk_scan(ga0, ga1, lane);
+                if (exists && ok) {
+                    g[G_G + 2 * lane] = sc.g0;
+                    g[G_G + 2 * lane + 1] = sc.g1;
+                    g[G_GAM + 2 * lane] = fast_exp(sc.g0);
+                    g[G_GAM + 2 * lane + 1] = fast_exp(sc.g1);
+                    g[G_GINV + 2 * lane] = fast_exp(-sc.g0);
+                    g[G_GINV + 2 * lane + 1] = fast_exp(-sc.g1);
+                    g[G_BETA + 2 * lane] = gb0;
+                    g[G_BETA + 2 * lane + 1] = gb1;
+                    g[G_KDEC + 2 * lane] = fast_exp(sc.g_last - sc.g0);
+                    g[G_KDEC + 2 * lane + 1] = fast_exp(sc.g_last - sc.g1);
+                }
+                fetch_gates(k + 1);
+            }
+            named_sync(1 + which, 64);  // the gates are visible to both warps of the unit
+            ok = mbar_wait(bar(B_TMF0 + sl), (k >> 1) & 1);
+            if (!ok) *fail = 1;
+            tc_fence_after();
+            if (exists && ok && !*fail) {
+                const bool ratio = g[G_G + C - 1] > kRatioSafeLogDecay;
+                const uint32_t col = 256 * sl + 64 * which;
+                // L_ti = beta_t Gamma_ti k_t.k_i (i < t), whole 16-wide block rows
+                {
                     const float gt = ratio ? g[G_GAM + t] : g[G_G + t];
                     const float bt = g[G_BETA + t];
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         if (hh > (warp & 1)) break;  // columns >= 32 lie above rows < 32
                         float v[32], f[32];
-                        tmem_load32(lane_base + 64 * which + 32 * hh, v);
+                        tmem_load32(lane_base + col + 32 * hh, v);
                         const float4 *gv = reinterpret_cast<const float4 *>(g + (ratio ? G_GINV : G_G) + 32 * hh);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 x = gv[j];
-                            f[4 * j] = x.x; f[4 * j + 1] = x.y; f[4 * j + 2] = x.z; f[4 * j + 3] = x.w;
+                        for (int jv = 0; jv < 8; ++jv) {
+                            const float4 x = gv[jv];
+                            f[4 * jv] = x.x; f[4 * jv + 1] = x.y; f[4 * jv + 2] = x.z; f[4 * jv + 3] = x.w;
                         }
 #pragma unroll
                         for (int ii = 0; ii < 32; ++ii) {
@@ -383,13 +454,11 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                             const float dec = ratio ? gt * f[ii] : fast_exp(gt - f[ii]);
                             v[ii] = (i < t) ? bt * dec * v[ii] : 0.f;
                         }
-                        // whole 16-wide rows of the blocks left of and on the diagonal (the
-                        // zeros on and above the diagonal are never read)
 #pragma unroll
                         for (int m = 0; m < 2; ++m) {
                             const int ib = 2 * hh + m;
                             if (ib <= (t >> 4)) {
-                                float *blockp = Lb + blk(t >> 4, ib);
+                                float *blockp = U + blk(t >> 4, ib);
 #pragma unroll
                                 for (int e4 = 0; e4 < 4; ++e4)
                                     *reinterpret_cast<float4 *>(blockp + el(t & 15, 4 * e4)) =
@@ -398,8 +467,9 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                             }
                         }
                     }
-                } else {
-                    // row i = t of A^T: key i against queries tq >= i
+                }
+                // row i = t of A^T: key i against queries tq >= i, straight to the workspace
+                {
                     const float gi = g[G_G + t];
                     const float ginv_c = g[G_GINV + C - 1];
                     uint4 *dst = reinterpret_cast<uint4 *>(p.Tout + ((size_t)(2 * u + 1) * C + t) * C);
@@ -410,7 +480,7 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
                             for (int ii = 0; ii < 32; ++ii) v[ii] = 0.f;
                         } else {
-                            tmem_load32(lane_base + 128 + 64 * which + 32 * hh, v);
+                            tmem_load32(lane_base + col + 128 + 32 * hh, v);
 #pragma unroll
                             for (int ii = 0; ii < 32; ++ii) {
                                 const int tq = 32 * hh + ii;
@@ -425,74 +495,56 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                                                           pack_bf16x2(v[8 * jj + 4], v[8 * jj + 5]),
                                                           pack_bf16x2(v[8 * jj + 6], v[8 * jj + 7]));
                     }
-                    // the unit's decay factors for the chain kernel: g and gamma (threads
-                    // t < 32), kdec and the form flag (t >= 32), two tokens each
-                    float *go = p.Gout + (size_t)u * 256;
-                    if (t < 32) {
-                        go[2 * t] = g[G_G + 2 * t];
-                        go[2 * t + 1] = g[G_G + 2 * t + 1];
-                        go[64 + 2 * t] = g[G_GAM + 2 * t];
-                        go[64 + 2 * t + 1] = g[G_GAM + 2 * t + 1];
-                    } else {
-                        const int t2 = t - 32;
-                        go[128 + 2 * t2] = g[G_KDEC + 2 * t2];
-                        go[128 + 2 * t2 + 1] = g[G_KDEC + 2 * t2 + 1];
-                        go[192 + 2 * t2] = (t2 == 0) ? (ratio ? 1.f : 0.f) : 0.f;
-                        go[192 + 2 * t2 + 1] = 0.f;
-                    }
+                }
+                // the unit's decay factors for the chain kernel: g and gamma (warp 2 which),
+                // kdec and the form flag (warp 2 which + 1), two tokens per lane
+                float *go = p.Gout + (size_t)u * 256;
+                if ((warp & 1) == 0) {
+                    *reinterpret_cast<float2 *>(go + 2 * lane) = make_float2(g[G_G + 2 * lane], g[G_G + 2 * lane + 1]);
+                    *reinterpret_cast<float2 *>(go + 64 + 2 * lane) =
+                        make_float2(g[G_GAM + 2 * lane], g[G_GAM + 2 * lane + 1]);
+                } else {
+                    *reinterpret_cast<float2 *>(go + 128 + 2 * lane) =
+                        make_float2(g[G_KDEC + 2 * lane], g[G_KDEC + 2 * lane + 1]);
+                    *reinterpret_cast<float2 *>(go + 192 + 2 * lane) =
+                        make_float2(lane == 0 ? (ratio ? 1.f : 0.f) : 0.f, 0.f);
                 }
             }
+            tc_fence_before();
+            mbar_arrive(bar(B_TME0 + sl));              // the TMEM slot is read
+            if (exists) mbar_arrive(bar(B_LF0 + ls));   // the solver slot is filled
         }
-        tc_fence_before();  // the TMEM reads are done before the next pair's MMA is issued
-        __syncthreads();
-        if (tid == 0 && next < n_pairs && !issue_gram(it + 1)) *fail = 1;
-
-        // ---- warp 0 inverts unit a, warp 4 unit b
-        if ((warp & 3) == 0 && 2 * pair + (warp >> 2) < n_units)
-            warp_lower_inverse(reinterpret_cast<float *>(sm + OFF_LN) + (warp >> 2) * UNIT_FLOATS, lane);
-        __syncthreads();
-        // ---- T' = diag(kdec) (I + L)^{-1} diag(beta) (ratio form; no kdec otherwise), bf16:
-        // warps 0-3 unit a, warps 4-7 unit b, one half row per thread
-        {
-            const int which = warp >> 2, u = 2 * pair + which;
-            if (u < n_units) {
-                const float *U = reinterpret_cast<const float *>(sm + OFF_LN) + which * UNIT_FLOATS;
-                const float *g = gates + which * G_UNIT;
-                const bool ratio = g[G_G + C - 1] > kRatioSafeLogDecay;
-                const int gtid = tid & 127, t = gtid >> 1, hh = gtid & 1;
-                const float kd = ratio ? g[G_KDEC + t] : 1.f;
-                float x[32], bv[32];
-                const float4 *bp = reinterpret_cast<const float4 *>(g + G_BETA + 32 * hh);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 b4 = bp[j];
-                    bv[4 * j] = b4.x; bv[4 * j + 1] = b4.y; bv[4 * j + 2] = b4.z; bv[4 * j + 3] = b4.w;
-                }
-#pragma unroll
-                for (int ii = 0; ii < 32; ++ii) {
-                    const int i = 32 * hh + ii;
-                    x[ii] = (i <= t) ? n_entry(U, t, i) * bv[ii] * kd : 0.f;
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(p.Tout + ((size_t)(2 * u) * C + t) * C + 32 * hh);
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                    dst[jj] = make_uint4(pack_bf16x2(x[8 * jj], x[8 * jj + 1]),
-                                         pack_bf16x2(x[8 * jj + 2], x[8 * jj + 3]),
-                                         pack_bf16x2(x[8 * jj + 4], x[8 * jj + 5]),
-                                         pack_bf16x2(x[8 * jj + 6], x[8 * jj + 7]));
+    } else if (warp >= kSolverWarp0) {
+        // ============================================================ solvers
+        const int sv = warp - kSolverWarp0;
+        for (int lu = sv; lu < 2 * K; lu += kSolvers) {
+            const int k = lu >> 1, which = lu & 1;
+            const int u = 2 * pair_of(k) + which;
+            if (u >= n_units) continue;  // the missing half of an odd last pair
+            if (!mbar_wait(bar(B_LF0 + sv), (lu / kSolvers) & 1)) { *fail = 1; break; }
+            float *U = lslot(sv);
+            const float *g = U + UNIT_FLOATS;
+            warp_lower_inverse(U, lane);
+            // T' = diag(kdec) (I + L)^{-1} diag(beta) (ratio form; no kdec otherwise), bf16,
+            // staged over the slot and stored by TMA
+            const bool ratio = g[G_G + C - 1] > kRatioSafeLogDecay;
+            unsigned char *tile = reinterpret_cast<unsigned char *>(U);
+            warp_stage_tprime(U, g, ratio, tile, lane);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(&map_t, smem_u32(tile), 0, 0, 2 * u);
+                bulk_commit_group();
+                bulk_wait_group_read<0>();  // the slot may be refilled once the store has read it
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_LE0 + sv));
         }
-        __syncthreads();  // blocks and gates free for the next pair
+        if (lane == 0) bulk_wait_group_all();  // the T' stores have completed
     }
 
     __syncthreads();
-    if (*fail && tid == 0) {
-        atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
-        mma_commit(bar(B_DRAIN));  // issued MMAs and loads land before TMEM and smem go away
-        mbar_wait(bar(B_DRAIN), 0);
-        if (loads_issued > loads_landed) mbar_wait(bar(B_FULL), loads_landed & 1);
-    }
-    __syncthreads();
+    if (*fail && tid == 0) atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
@@ -501,7 +553,7 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 namespace tc {
 
 int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &map_q,
-                    const CUtensorMap &map_k) {
+                    const CUtensorMap &map_k, const CUtensorMap &map_t) {
     SolveParams p;
     p.log_alpha = a.log_alpha;
     p.beta = a.beta;
@@ -518,8 +570,8 @@ int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return GDR_ERR_CUDA;
     const int64_t pairs = (L.max_chunks * a.H + 1) / 2;  // upper bound; the kernel reads the count
-    const int64_t grid = pairs < 2 * (int64_t)sms ? pairs : 2 * (int64_t)sms;  // two CTAs per SM
-    tc_solve_kernel<<<(unsigned)grid, kThreads, SMEM_BYTES, a.stream>>>(map_q, map_k, p);
+    const int64_t grid = pairs < (int64_t)sms ? pairs : (int64_t)sms;  // one CTA per SM
+    tc_solve_kernel<<<(unsigned)grid, kThreads, SMEM_BYTES, a.stream>>>(map_q, map_k, map_t, p);
     return cuda_status(cudaGetLastError());
 }
 

@@ -83,7 +83,7 @@ bool make_map_units(CUtensorMap *map, const void *base, int64_t units);
 
 // The chunk-parallel solve: T' and A^T for every (chunk, head) into the workspace.
 int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &map_q,
-                    const CUtensorMap &map_k);
+                    const CUtensorMap &map_k, const CUtensorMap &map_t);
 
 }  // namespace tc
 }  // namespace gdr
