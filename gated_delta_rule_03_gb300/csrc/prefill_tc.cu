@@ -46,14 +46,15 @@
 //   K, A^T, factors  3 slots, freed when the chunk is done;
 //   Q (and -W')      2 slots, freed when [QS | WS] is done.
 //
-// Warp roles (17 warps; TMEM lane quarter = warp % 4):
+// Warp roles (18 warps; TMEM lane quarter = warp % 4):
 //   warps 0-3   epilogue: O^T of chunk c from TMEM (times gamma_t in the ratio form),
 //               transposed into a staging tile, stored by TMA.
 //   warps 4-7   prep: T' diag(gamma), U'~ and W' (its elected thread issues them), -W'
 //               into the Q slot, the in-place scaling of Q and K (exponential form).
 //   warps 8-15  state, the sequential chain: the bf16 S^T and U'^T operands in TMEM,
-//               [S_upd | AU], the decay of the fp32 master S^T (in TMEM); its elected
-//               thread issues both state chains.
+//               and the decay of the fp32 master S^T (in TMEM);
+//   warp 17     the state's MMA issuer: [QS | WS] once S^T is in place, [S_upd | AU] once
+//               U'^T is.
 //   warp 16     producer: the TMA and bulk loads of the three rings, in chunk order, each
 //               as soon as its slot is free.
 // The critical path per chunk is: S^T copy -> [QS | WS] -> U'^T copy -> [S_upd | AU].
@@ -75,13 +76,14 @@ using namespace tc;
 constexpr int C = kChunk;   // 64 tokens per chunk
 constexpr int DK = 128;     // key dimension
 constexpr int NV = 128;     // value columns per CTA
-constexpr int kWarps = 17;
+constexpr int kWarps = 18;
 constexpr int kThreads = kWarps * 32;
 constexpr int kEpiThreads = 128;                      // warps 0-3
 constexpr int kPrepWarp0 = 4, kPrepThreads = 128;     // warps 4-7
-constexpr int kStateWarp0 = 8, kStateThreads = 256;   // warps 8-15
-constexpr int kProducerWarp = 16;
-constexpr int kBarPrep = 1, kBarState = 2, kBarEpi = 3;  // named barrier ids
+constexpr int kStateWarp0 = 8;   // warps 8-15
+constexpr int kProducerWarp = 16, kMmaWarp = 17;
+constexpr int kStateWarps = 8;
+constexpr int kBarPrep = 1, kBarEpi = 3;  // named barrier ids
 
 // Shared memory map (bytes from a 1024-aligned base).
 constexpr uint32_t RQ = 0, RQ_SLOT = 32768;        // per d_k half b (16 KB): Q_b then -W'_b
@@ -101,17 +103,18 @@ static_assert(RK % 1024 == 0 && RK_SLOT % 1024 == 0 && RV % 1024 == 0 && OFF_TG 
 // mbarrier slots at OFF_BAR (8 bytes each), then the TMEM slot and role flags.
 enum {
     B_QF0 = 0, B_QF1,        // Q slot loaded                              (tx bytes)
-    B_QE0, B_QE1,            // Q slot free: [QS | WS] done                (state issuer commit)
+    B_QE0, B_QE1,            // Q slot free: [QS | WS] done                (MMA warp commit)   
     B_KF0, B_KF1, B_KF2,     // K slot loaded                              (tx bytes)
     B_KE0, B_KE1, B_KE2,     // K slot free: chunk done (prep 128 arrivals + state commit)
     B_VF0, B_VF1,            // V slot loaded                              (tx bytes)
     B_VE0, B_VE1,            // V slot free: U'~ and W' done               (prep issuer commit)
     B_UW0, B_UW1,            // U'~ (buffer c%2) and W' of chunk c done   (prep issuer commit)
     B_WQ0, B_WQ1,            // -W' of chunk c stored, Q/K scaled          (128 prep arrivals)
-    B_WS,                    // [QS | WS] done                             (state issuer commit)
-    B_SO,                    // [S_upd | AU] done                          (state issuer commit)
+    B_WS,                    // [QS | WS] done                             (MMA warp commit)   
+    B_SO,                    // [S_upd | AU] done                          (MMA warp commit)   
     B_OFREE,                 // O read by the epilogue                     (128 arrivals)
-    B_UFREE0, B_UFREE1,      // U'~ buffer read by the state               (state issuer)
+    B_UFREE0, B_UFREE1,      // U'~ buffer read by the state               (MMA warp)
+    B_SREADY, B_UREADY,      // S^T / U'^T operands written to TMEM        (8 state warps)
     B_EG0, B_EG1, B_EG2, B_EG3,  // epilogue gates of chunk c in slot c%4  (128 prep arrivals)
     B_DRAIN0, B_DRAIN1,      // drain after an abort
     B_COUNT
@@ -236,6 +239,8 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mbar_init(bar(B_WS), 1);
         mbar_init(bar(B_SO), 1);
         mbar_init(bar(B_OFREE), kEpiThreads);
+        mbar_init(bar(B_SREADY), kStateWarps);
+        mbar_init(bar(B_UREADY), kStateWarps);
         fence_mbar_init();
         flags[0] = flags[1] = flags[2] = flags[3] = 0;
         prefetch_tensormap(&map_q);
@@ -455,21 +460,54 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mma_commit(bar(B_DRAIN0));
             mbar_wait(bar(B_DRAIN0), 0);
         }
-    } else {
+    } else if (warp == kMmaWarp) {
+        // ============================================================ state MMA issuer
+        if (lane == 0) {
+            for (int c = 0; c < n_chunks; ++c) {
+                // [O^T | X^T] = S^T [Q; -W']^T once S^T, -W' and (for the O buffer) the
+                // epilogue of chunk c - 1 are ready
+                bool ok = mbar_wait(bar(B_SREADY), c & 1) && mbar_wait(bar(B_WQ0 + (c & 1)), (c >> 1) & 1);
+                if (ok && c > 0) ok = mbar_wait(bar(B_OFREE), (c - 1) & 1);
+                if (!ok) { note_fail(1); break; }
+                tc_fence_after();
+                const uint32_t qw = sbase + qslot(c);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ta(tmem + TM_O, tmem + TM_SA + 8 * kk,
+                                sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                                idesc_bf16(128, 128, 0, 0), kk > 0);
+                mma_commit(bar(B_WS));
+                mma_commit(bar(B_QE0 + (c & 1)));  // Q and -W' are read
+                // [S^T | O^T] += U'^T [K | A^T] once U'^T (and the decayed master) is in place
+                if (!mbar_wait(bar(B_UREADY), c & 1)) { note_fail(1); break; }
+                tc_fence_after();
+                mbar_arrive(bar(B_UFREE0 + (c & 1)));
+                const uint32_t ks = sbase + kslot(c);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // tokens 16kk..16kk+15: columns X + 32(kk/2) + 8(kk%2)
+                    mma_bf16_ta(tmem + TM_S, tmem + TM_X + 32 * (kk >> 1) + 8 * (kk & 1),
+                                sw128_desc(ks + kk * 2048, 8192, 1024), idesc_bf16(128, 192, 0, 1), 1);
+                mma_commit(bar(B_SO));
+                mma_commit(bar(B_KE0 + c % 3));  // the state's last reads of the K slot
+            }
+            if (flags[3]) {  // let issued MMAs land before TMEM and shared memory go away
+                mma_commit(bar(B_DRAIN1));
+                mbar_wait(bar(B_DRAIN1), 0);
+            }
+        }
+    } else if (warp >= kStateWarp0 && warp < kStateWarp0 + kStateWarps) {
         // ============================================================ state
-        const int stid = tid - 32 * kStateWarp0;
         const int half = (warp - kStateWarp0) >> 2;  // which 64 of the d_k entries / 32 of the tokens
         const int row = 32 * (warp & 3) + lane;      // TMEM lane = value column col0 + row
-        const bool issuer = stid == 0;
-        volatile int *fail = &flags[1];
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        auto check = [&](bool ok) -> bool {
-            if (!ok) note_fail(1);
-            named_sync(kBarState, kStateThreads);
-            return *fail == 0;
+        // each state warp's arrival on B_SREADY / B_UREADY after its TMEM stores
+        auto warp_arrive = [&](int b) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(b));
         };
         // this thread's 64 entries of S^T: lane col0 + row, d_k columns [64*half, 64*half + 64);
-        // they live in the fp32 master in TMEM and are read back 32 at a time
+        // they live in the fp32 master in TMEM
         const size_t s_off = ((size_t)n * p.H + h) * DK * p.dv + col0 + row;
         const uint32_t s_tm = lane_base + TM_S + 64 * half;
         {  // S0 (or zero) into the master
@@ -481,41 +519,26 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 for (int i = 0; i < 32; ++i) x[i] = src ? src[(size_t)(32 * hh + i) * p.dv] : 0.f;
                 tmem_store32(s_tm + 32 * hh, x);
             }
-            tc_fence_before();
         }
         // Step c finishes chunk c - 1 (when c > 0), then starts chunk c (when c < n_chunks).
         for (int c = 0; c <= n_chunks; ++c) {
             if (c > 0) {
-                const int cp = c - 1, s = cp & 1;
+                const int cp = c - 1;
                 // ---- U'^T = U'~^T + X^T, as bf16 pairs over this thread's read part of X
-                if (!check(mbar_wait(bar(B_WS), cp & 1))) break;
+                if (!mbar_wait(bar(B_WS), cp & 1)) { note_fail(1); break; }
                 tc_fence_after();
                 {
                     float a[32], b[32];
-                    tmem_load32(lane_base + TM_U + 64 * s + 32 * half, a);
+                    tmem_load32(lane_base + TM_U + 64 * (cp & 1) + 32 * half, a);
                     tmem_load32(lane_base + TM_X + 32 * half, b);
                     uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(a[2 * i] + b[2 * i], a[2 * i + 1] + b[2 * i + 1]);
                     tmem_store16(lane_base + TM_X + 32 * half, w);
                 }
-                tc_fence_before();
-                named_sync(kBarState, kStateThreads);
-                if (issuer) {
-                    tc_fence_after();
-                    mbar_arrive(bar(B_UFREE0 + s));
-                    const uint32_t ks = sbase + kslot(cp);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)  // tokens 16kk..16kk+15: columns X + 32(kk/2) + 8(kk%2)
-                        mma_bf16_ta(tmem + TM_S, tmem + TM_X + 32 * (kk >> 1) + 8 * (kk & 1),
-                                    sw128_desc(ks + kk * 2048, 8192, 1024), idesc_bf16(128, 192, 0, 1), 1);
-                    mma_commit(bar(B_SO));
-                    mma_commit(bar(B_KE0 + cp % 3));  // the state's last reads of the K slot
-                }
-                __syncwarp();
-
+                warp_arrive(B_UREADY);
                 // ---- the new state (gamma_C S + U'^T K, accumulated in TMEM)
-                if (!check(mbar_wait(bar(B_SO), cp & 1))) break;
+                if (!mbar_wait(bar(B_SO), cp & 1)) { note_fail(1); break; }
                 tc_fence_after();
             }
             if (c == n_chunks) {  // the final state (an empty sequence keeps its initial one)
@@ -529,55 +552,26 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 }
                 break;
             }
-            // ---- bf16 S^T into TMEM for [QS | WS] of chunk c, the issue of that chain
+            // ---- bf16 S^T into TMEM for [QS | WS] of chunk c; then the master decayed by
+            // gamma_C of chunk c while [QS | WS] runs
+            float x[2][32];
+            tmem_load64(s_tm, x);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                float x[32];
-                tmem_load32(s_tm + 32 * hh, x);
                 uint32_t w[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+                for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(x[hh][2 * i], x[hh][2 * i + 1]);
                 tmem_store16(lane_base + TM_SA + 32 * half + 16 * hh, w);
             }
-            tc_fence_before();
-            named_sync(kBarState, kStateThreads);
-            if (issuer) {
-                bool ok = mbar_wait(bar(B_WQ0 + (c & 1)), (c >> 1) & 1);
-                if (ok && c > 0) ok = mbar_wait(bar(B_OFREE), (c - 1) & 1);  // O of chunk c-1 read
-                if (ok) {
-                    tc_fence_after();
-                    const uint32_t qw = sbase + qslot(c);
+            warp_arrive(B_SREADY);
+            if (!mbar_wait(bar(B_KF0 + c % 3), (c / 3) & 1)) { note_fail(1); break; }
+            const float gC = reinterpret_cast<const float *>(sm + kslot(c) + RK_G)[G_GAM + C - 1];
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16_ta(tmem + TM_O, tmem + TM_SA + 8 * kk,
-                                    sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                                    idesc_bf16(128, 128, 0, 0), kk > 0);
-                    mma_commit(bar(B_WS));
-                    mma_commit(bar(B_QE0 + (c & 1)));  // Q and -W' are read
-                } else {
-                    note_fail(1);
-                }
+            for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[hh][i] *= gC;
+                tmem_store32(s_tm + 32 * hh, x[hh]);
             }
-            __syncwarp();
-            // ---- the master decayed by gamma_C of chunk c, while [QS | WS] runs
-            if (!mbar_wait(bar(B_KF0 + c % 3), (c / 3) & 1)) {
-                note_fail(1);
-            } else {
-                const float gC = reinterpret_cast<const float *>(sm + kslot(c) + RK_G)[G_GAM + C - 1];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float x[32];
-                    tmem_load32(s_tm + 32 * hh, x);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] *= gC;
-                    tmem_store32(s_tm + 32 * hh, x);
-                }
-            }
-            tc_fence_before();
-        }
-        if (*fail && issuer) {
-            mma_commit(bar(B_DRAIN1));
-            mbar_wait(bar(B_DRAIN1), 0);
         }
     }
 

@@ -181,6 +181,40 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Loads 64 consecutive fp32 columns (two 32-column loads, one wait) of this thread's lane.
+// The wait names every register, so that no use can be scheduled before it.
+__device__ __forceinline__ void tmem_load64(uint32_t taddr, float (&v)[2][32]) {
+    uint32_t r[64];
+#define GDR_LD32(base, off)                                                                          \
+    asm volatile(                                                                                    \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "                                                   \
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "                    \
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"     \
+        : "=r"(r[base + 0]), "=r"(r[base + 1]), "=r"(r[base + 2]), "=r"(r[base + 3]),               \
+          "=r"(r[base + 4]), "=r"(r[base + 5]), "=r"(r[base + 6]), "=r"(r[base + 7]),               \
+          "=r"(r[base + 8]), "=r"(r[base + 9]), "=r"(r[base + 10]), "=r"(r[base + 11]),             \
+          "=r"(r[base + 12]), "=r"(r[base + 13]), "=r"(r[base + 14]), "=r"(r[base + 15]),           \
+          "=r"(r[base + 16]), "=r"(r[base + 17]), "=r"(r[base + 18]), "=r"(r[base + 19]),           \
+          "=r"(r[base + 20]), "=r"(r[base + 21]), "=r"(r[base + 22]), "=r"(r[base + 23]),           \
+          "=r"(r[base + 24]), "=r"(r[base + 25]), "=r"(r[base + 26]), "=r"(r[base + 27]),           \
+          "=r"(r[base + 28]), "=r"(r[base + 29]), "=r"(r[base + 30]), "=r"(r[base + 31])            \
+        : "r"(taddr + off)                                                                           \
+        : "memory")
+    GDR_LD32(0, 0u);
+    GDR_LD32(32, 32u);
+#undef GDR_LD32
+#pragma unroll
+    for (int i = 0; i < 64; i += 8)
+        asm volatile("tcgen05.wait::ld.sync.aligned;"
+                     : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]),
+                       "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])::"memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        v[0][i] = __uint_as_float(r[i]);
+        v[1][i] = __uint_as_float(r[32 + i]);
+    }
+}
+
 // Stores 32 consecutive fp32 columns of this thread's TMEM lane and waits for the store.
 __device__ __forceinline__ void tmem_store32(uint32_t taddr, const float (&v)[32]) {
     asm volatile(
