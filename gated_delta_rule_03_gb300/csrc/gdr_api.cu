@@ -27,7 +27,7 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
     L.plan = off;
     off = align_up(off + sizeof(int4) * (size_t)L.max_chunks, 256);
     L.seq_chunk = off;
-    off = align_up(off + sizeof(int32_t) * (size_t)(num_seqs + 1), 256);
+    off = align_up(off + sizeof(int32_t) * (size_t)kMaxPhases * (size_t)(num_seqs + 1), 256);
     if (!L.tensor_path) {
         const size_t per = (size_t)L.max_chunks * (size_t)H * kChunk;
         L.W = off;
@@ -43,6 +43,8 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
         off = align_up(off + (size_t)L.max_chunks * (size_t)H * 2 * kChunk * kChunk * 2, 256);
         L.G = off;  // 256 floats per (chunk, head)
         off = align_up(off + (size_t)L.max_chunks * (size_t)H * 256 * sizeof(float), 256);
+        L.S = off;  // the state handed from one phase to the next
+        off = align_up(off + (size_t)num_seqs * (size_t)H * dk * dv * sizeof(float), 256);
     }
     L.total = off;
     return L;
@@ -132,9 +134,10 @@ int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
     a.o = o; a.S_final = S_final;
     a.ws = (char *)workspace;
     a.stream = (cudaStream_t)stream;
-    st = launch_plan(a, L);
+    const int phases = L.tensor_path ? tc_phases(a) : 1;
+    st = launch_plan(a, L, phases);
     if (st != GDR_OK) return st;
-    return L.tensor_path ? launch_prefill_tc(a, L) : launch_prefill_exact(a, L);
+    return L.tensor_path ? launch_prefill_tc(a, L, phases) : launch_prefill_exact(a, L);
 }
 
 int gdr_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -161,6 +164,19 @@ int gdr_chunk_fwd_path(int d_k, int d_v, int dtype) {
     const int st = check_prefill_sizes(1, 0, 1, d_k, d_v, kChunk, dtype);
     if (st != GDR_OK) return st;
     return use_tensor_path(d_k, d_v, dtype) ? GDR_PATH_TENSOR : GDR_PATH_EXACT;
+}
+
+int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H, int d_k,
+                                  int d_v, int chunk, int dtype) {
+    const int st = check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype);
+    if (st != GDR_OK) return st;
+    if (!use_tensor_path(d_k, d_v, dtype)) return 3;  // plan, per-chunk prep, chain
+    if (total_tokens == 0) return 1;  // the plan; the state copy is not a kernel of ours
+    int dev = -1, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    return 1 + 2 * tc_phases_for(num_seqs, total_tokens, H, d_v, sms);
 }
 
 int gdr_read_device_status(const void *workspace, int *status, gdr_stream_t stream) {

@@ -11,6 +11,7 @@
 namespace gdr {
 
 constexpr int kChunk = 64;  // tokens per chunk (the only chunk size the kernels support)
+constexpr int kMaxPhases = 8;  // most phases a tensor-core prefill is split into
 
 // Everything gdr_chunk_fwd receives, after host validation.
 struct PrefillArgs {
@@ -26,15 +27,19 @@ struct PrefillArgs {
 };
 
 // Byte offsets of the workspace regions. The control words come first:
-//   int32 ctl[0] = device status (GDR_OK / GDR_ERR_*), ctl[1] = number of chunks.
+//   int32 ctl[0] = device status (GDR_OK / GDR_ERR_*), ctl[1] = number of chunks,
+//   ctl[2 + f] = first chunk of phase f (f = 0 .. phases).
+// Chunks are numbered phase-major (see plan_kernel); a single phase is the plain
+// sequence-by-sequence order.
 struct WsLayout {
     int64_t max_chunks;   // upper bound on sum over sequences of ceil(len / chunk)
     size_t ctl;           // int32[64]
     size_t plan;          // int4[max_chunks]: (sequence, first token, tokens, chunk index)
-    size_t seq_chunk;     // int32[num_seqs + 1]: first chunk of each sequence
+    size_t seq_chunk;     // int32[kMaxPhases][num_seqs + 1]: first chunk of each sequence per phase
     size_t W, U, A, g;    // fp32 per-chunk intermediates of the exact path (g: gamma, kdec)
     size_t T;             // tensor-core path: bf16 [max_chunks * H][2][64][64] T' and A^T per unit
     size_t G;             // tensor-core path: fp32 [max_chunks * H][256] decay factors per unit
+    size_t S;             // tensor-core path: fp32 [num_seqs][H][dk][dv] state between phases
     size_t total;
     bool tensor_path;     // bf16 tensor-core kernel (true) or exact fp32-arithmetic kernels
 };
@@ -43,9 +48,15 @@ bool use_tensor_path(int dk, int dv, int dtype);
 WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype);
 
 // Launchers (return GDR_OK or GDR_ERR_CUDA).
-int launch_plan(const PrefillArgs &a, const WsLayout &L);
+int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases);
 int launch_prefill_exact(const PrefillArgs &a, const WsLayout &L);
-int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L);
+int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases);
+
+// Phases of a tensor-core prefill of these sizes on a GPU with `sms` SMs (1 .. kMaxPhases).
+int tc_phases_for(int64_t num_seqs, int64_t total_tokens, int H, int dv, int sms);
+// The phases a call with these arguments runs: tc_phases_for on the current device, or 1
+// when the second stream it needs cannot be had (see launch_prefill_tc).
+int tc_phases(const PrefillArgs &a);
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
                   int dtype, cudaStream_t stream);

@@ -34,78 +34,150 @@ namespace gdr {
 
 // ----------------------------------------------------------------------------- plan
 
+// Exclusive prefix sum of one int per thread over a block of 1024 threads; *total gets
+// the block's sum. Every thread of the block must call it.
+__device__ __forceinline__ int block_exclusive_scan(int x, int *warp_sums, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int up = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += up;
+    }
+    if (lane == 31) warp_sums[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int up = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += up;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int ex = inc - x + (warp ? warp_sums[warp - 1] : 0);
+    *total = warp_sums[31];
+    __syncthreads();  // warp_sums may be reused
+    return ex;
+}
+
+// The chunk plan, phase-major. Sequence n, of m_n chunks, gives its chunks
+// [floor(f m_n / P), floor((f + 1) m_n / P)) to phase f. Chunks are numbered phase by
+// phase and, within a phase, sequence by sequence, so that the chunks of one phase are
+// contiguous and so are the chunks of one sequence within a phase. Outputs:
+//   plan[chunk]                       (sequence, first token, tokens, index in the sequence)
+//   seq_chunk[f * (num_seqs + 1) + n] first chunk of sequence n in phase f; the entry at
+//                                     n = num_seqs is the end of phase f
+//   ctl[0] status, ctl[1] number of chunks, ctl[2 + f] first chunk of phase f (f <= P)
+// A single block of 1024 threads: sequences in blocks of 1024 for the prefix sums, then a
+// group of threads per sequence writes its plan entries.
 __global__ void __launch_bounds__(1024)
 plan_kernel(const int32_t *__restrict__ cu, int64_t num_seqs, int64_t total_tokens,
-            int64_t max_chunks, int4 *__restrict__ plan, int32_t *__restrict__ seq_chunk,
-            int32_t *__restrict__ ctl) {
-    __shared__ int s_scan[1024];
+            int64_t max_chunks, int phases, int4 *__restrict__ plan,
+            int32_t *__restrict__ seq_chunk, int32_t *__restrict__ ctl) {
+    __shared__ int s_warp[32];
+    __shared__ int s_off[kMaxPhases + 1];
     __shared__ int s_bad;
-    __shared__ int s_carry;
     const int tid = threadIdx.x;
-    if (tid == 0) {
-        s_bad = 0;
-        s_carry = 0;
-    }
+    const int64_t row = num_seqs + 1;  // seq_chunk entries per phase
+    // the solve kernel after this one may be launched now (programmatic launch): it sets
+    // itself up and waits for this grid to complete before reading the plan
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (tid == 0) s_bad = 0;
     __syncthreads();
     const int64_t seq_len = cu ? 0 : total_tokens / num_seqs;
+    // first token and length of sequence n; false if cu_seqlens is out of range there
+    auto seq_range = [&](int64_t n, int64_t &t0, int64_t &len) {
+        if (!cu) {
+            t0 = n * seq_len;
+            len = seq_len;
+            return true;
+        }
+        t0 = cu[n];
+        const int64_t t1 = cu[n + 1];
+        len = t1 - t0;
+        if (len < 0 || t0 < 0 || t1 > total_tokens) {
+            len = 0;
+            return false;
+        }
+        return true;
+    };
+    // pass 1: each sequence's first chunk in each phase, relative to the phase's start
+    int carry[kMaxPhases];
+#pragma unroll
+    for (int f = 0; f < kMaxPhases; ++f) carry[f] = 0;
     for (int64_t base = 0; base < num_seqs; base += blockDim.x) {
         const int64_t n = base + tid;
-        int cnt = 0;
-        int64_t t0 = 0, len = 0;
+        int64_t m = 0;
         if (n < num_seqs) {
-            if (cu) {
-                t0 = cu[n];
-                const int64_t t1 = cu[n + 1];
-                len = t1 - t0;
-                if (len < 0 || t0 < 0 || t1 > total_tokens) {
-                    s_bad = 1;
-                    len = 0;
-                }
-            } else {
-                t0 = n * seq_len;
-                len = seq_len;
-            }
-            cnt = (int)((len + kChunk - 1) / kChunk);
+            int64_t t0, len;
+            if (!seq_range(n, t0, len)) s_bad = 1;
+            m = (len + kChunk - 1) / kChunk;
         }
-        s_scan[tid] = cnt;
-        __syncthreads();
-        for (int off = 1; off < (int)blockDim.x; off <<= 1) {
-            const int add = tid >= off ? s_scan[tid - off] : 0;
-            __syncthreads();
-            s_scan[tid] += add;
-            __syncthreads();
+#pragma unroll
+        for (int f = 0; f < kMaxPhases; ++f) {
+            if (f >= phases) break;
+            const int cnt = (int)((f + 1) * m / phases - f * m / phases);
+            int tot;
+            const int ex = block_exclusive_scan(cnt, s_warp, &tot);
+            if (n < num_seqs) seq_chunk[f * row + n] = carry[f] + ex;
+            carry[f] += tot;
         }
-        const int first = s_carry + s_scan[tid] - cnt;
-        if (n < num_seqs) {
-            seq_chunk[n] = first;
-            for (int j = 0; j < cnt; ++j) {
-                if (first + j >= max_chunks) {
-                    s_bad = 1;
-                    break;
-                }
-                const int64_t rem = len - (int64_t)j * kChunk;
-                plan[first + j] = make_int4((int)n, (int)(t0 + (int64_t)j * kChunk),
-                                            (int)(rem < kChunk ? rem : kChunk), j);
-            }
-        }
-        __syncthreads();
-        if (tid == (int)blockDim.x - 1) s_carry += s_scan[tid];
-        __syncthreads();
     }
     if (tid == 0) {
+        int acc = 0;
+#pragma unroll
+        for (int f = 0; f < kMaxPhases; ++f) {
+            if (f >= phases) break;
+            s_off[f] = acc;
+            acc += carry[f];
+        }
+        s_off[phases] = acc;
         if (cu && (cu[0] != 0 || cu[num_seqs] != total_tokens)) s_bad = 1;
+        if (acc > max_chunks) s_bad = 1;
     }
     __syncthreads();
+    const bool bad = s_bad != 0;
+    if (!bad) {
+        // pass 2: absolute chunk numbers (each thread revisits its own entries)
+        for (int64_t base = 0; base < num_seqs; base += blockDim.x) {
+            const int64_t n = base + tid;
+            if (n < num_seqs)
+                for (int f = 0; f < phases; ++f) seq_chunk[f * row + n] += s_off[f];
+        }
+        if (tid < phases) seq_chunk[tid * row + num_seqs] = s_off[tid + 1];
+        __syncthreads();
+        // pass 3: the plan entries; G groups of 1024 / G threads, a group per sequence
+        int G = 1;
+        while (G < 32 && 2 * G <= num_seqs) G *= 2;
+        const int gsize = (int)blockDim.x / G, g = tid / gsize, gt = tid % gsize;
+        for (int64_t n = g; n < num_seqs; n += G) {
+            int64_t t0, len;
+            seq_range(n, t0, len);
+            const int64_t m = (len + kChunk - 1) / kChunk;
+            for (int f = 0; f < phases; ++f) {
+                const int64_t cb = f * m / phases, ce = (f + 1) * m / phases;
+                const int64_t first = seq_chunk[f * row + n];
+                for (int64_t j = cb + gt; j < ce; j += gsize) {
+                    const int64_t rem = len - j * kChunk;
+                    plan[first + (j - cb)] = make_int4((int)n, (int)(t0 + j * kChunk),
+                                                       (int)(rem < kChunk ? rem : kChunk), (int)j);
+                }
+            }
+        }
+    }
     if (tid == 0) {
-        seq_chunk[num_seqs] = s_carry;
-        ctl[0] = s_bad ? GDR_ERR_BAD_SEQLENS : GDR_OK;
-        ctl[1] = s_bad ? 0 : s_carry;
+        ctl[0] = bad ? GDR_ERR_BAD_SEQLENS : GDR_OK;
+        ctl[1] = bad ? 0 : s_off[phases];
+        for (int f = 0; f <= phases; ++f) ctl[2 + f] = bad ? 0 : s_off[f];
     }
 }
 
-int launch_plan(const PrefillArgs &a, const WsLayout &L) {
+int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases) {
     plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.num_seqs, a.total_tokens, L.max_chunks,
-                                          (int4 *)(a.ws + L.plan), (int32_t *)(a.ws + L.seq_chunk),
+                                          phases, (int4 *)(a.ws + L.plan),
+                                          (int32_t *)(a.ws + L.seq_chunk),
                                           (int32_t *)(a.ws + L.ctl));
     return cuda_status(cudaGetLastError());
 }

@@ -63,6 +63,8 @@
 // T', W', U' are zero, they change nothing and they are not stored.
 // Every wait is bounded; a role that gives up marks the call GDR_ERR_DEVICE_TIMEOUT in
 // the status word, and the others give up in turn, drain and free TMEM.
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "tc_common.cuh"
@@ -132,14 +134,15 @@ constexpr uint32_t TM_S = 0, TM_O = 128, TM_X = 192, TM_U = 256 /* two buffers *
 
 
 struct TcParams {
-    const float *S0;
+    const float *S_in;         // state before this phase's chunks (null: zero)
     const float *factors;      // per solve unit: g, gamma, kdec, form (256 floats)
     const int32_t *cu_seqlens;
-    const int32_t *seq_chunk;  // first chunk of each sequence (planning kernel)
+    const int32_t *seq_chunk;  // first chunk of each sequence in this phase (planning kernel)
     int64_t num_seqs, total_tokens;
     int H, dv, n_slices;
+    int phase, phases;         // this launch runs chunks [floor(f m / P), floor((f+1) m / P))
     __nv_bfloat16 *o;
-    float *S_final;
+    float *S_out;              // state after this phase's chunks (may alias S_in)
     int32_t *ctl;
 };
 
@@ -183,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_t,
                 const __grid_constant__ CUtensorMap map_o, const TcParams p) {
-    if (p.ctl[0] != GDR_OK) return;  // cu_seqlens rejected, or the solve gave up
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte aligned base, derived from the shared array itself so that every access
     // through it stays a shared-memory access the compiler can schedule freely
@@ -209,7 +211,11 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         seq_begin = (int64_t)n * len;
         seq_end = seq_begin + len;
     }
-    const int n_chunks = (int)((seq_end - seq_begin + C - 1) / C);
+    // this phase's chunks of the sequence: local chunk c is the sequence's chunk cb + c
+    const int64_t m = (seq_end - seq_begin + C - 1) / C;
+    const int64_t cb = (int64_t)p.phase * m / p.phases;
+    const int n_chunks = (int)((int64_t)(p.phase + 1) * m / p.phases - cb);
+    seq_begin += cb * C;
     const int col0 = slice * NV;  // first value column of this CTA
     auto chunk_len = [&](int c) {
         const int64_t rem = seq_end - (seq_begin + (int64_t)c * C);
@@ -259,7 +265,16 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t tmem = *tmem_slot;
     float *__restrict__ eg = reinterpret_cast<float *>(sm + OFF_EG);  // gamma[4][64], flag[4]
 
-    if (warp == kProducerWarp) {
+    // Everything above overlaps the tail of the kernel ahead in the stream (programmatic
+    // launch); what that kernel writes (status, plan, solve results, the state of the
+    // previous phase) is read only after it has completed.
+    griddep_wait();
+    griddep_launch_dependents();
+    const bool live = p.ctl[0] == GDR_OK;  // cu_seqlens rejected, or a solve gave up
+
+    if (!live) {
+        // nothing is read or written
+    } else if (warp == kProducerWarp) {
         // ============================================================ producer
         if (lane == 0) {
             const int unit0 = p.seq_chunk[n] * p.H + h;  // chunk c is solve unit unit0 + c * H
@@ -510,8 +525,9 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         // they live in the fp32 master in TMEM
         const size_t s_off = ((size_t)n * p.H + h) * DK * p.dv + col0 + row;
         const uint32_t s_tm = lane_base + TM_S + 64 * half;
-        {  // S0 (or zero) into the master
-            const float *src = p.S0 ? p.S0 + s_off + (size_t)(64 * half) * p.dv : nullptr;
+        {  // the incoming state (or zero) into the master; the same thread later writes
+           // the same entries of S_out, so S_out may be S_in
+            const float *src = p.S_in ? p.S_in + s_off + (size_t)(64 * half) * p.dv : nullptr;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 float x[32];
@@ -541,8 +557,8 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 if (!mbar_wait(bar(B_SO), cp & 1)) { note_fail(1); break; }
                 tc_fence_after();
             }
-            if (c == n_chunks) {  // the final state (an empty sequence keeps its initial one)
-                float *dst = p.S_final + s_off + (size_t)(64 * half) * p.dv;
+            if (c == n_chunks) {  // the outgoing state (no chunks: the incoming one)
+                float *dst = p.S_out + s_off + (size_t)(64 * half) * p.dv;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     float x[32];
@@ -643,7 +659,96 @@ bool make_map_units(CUtensorMap *map, const void *base, int64_t units) {
 
 }  // namespace tc
 
-int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L) {
+// ---------------------------------------------------------------- phases
+
+// The solve of every chunk must finish before the chain reaches it, but nothing else
+// orders the two kernels. A call is therefore split into phases, each taking a fixed
+// share of every sequence's chunks: the chain of phase f runs on the caller's stream
+// while the solve of phase f + 1 runs on a second stream, on the SMs the chain leaves
+// free (one chain CTA per SM). Events order solve f before chain f; the second stream
+// forks from and joins back into the caller's stream, so the call stays one
+// stream-ordered operation and can be captured into a CUDA graph. No kernel waits on
+// another kernel.
+
+namespace {
+
+constexpr int kMaxDevices = 256;
+
+// The second stream and the events of the current host thread on one device. Kept per
+// thread so that calls from several threads never share a stream that one of them may
+// be capturing. Created on first use; never destroyed (they go with the context).
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t ev[kMaxPhases] = {};
+    bool ready = false, failed = false;
+};
+thread_local SideStream t_side[kMaxDevices];
+
+int device_sms(int dev) {
+    static int sms[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    if (!sms[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        sms[dev] = v;
+    }
+    return sms[dev];
+}
+
+// The current thread's side stream on the current device, or null. Resources are not
+// created while `caller` is being captured; such a call runs as one phase.
+SideStream *side_stream(cudaStream_t caller) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    SideStream &sd = t_side[dev];
+    if (sd.ready) return &sd;
+    if (sd.failed) return nullptr;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+        return nullptr;
+    bool ok = cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; ok && i < kMaxPhases; ++i)
+        ok = cudaEventCreateWithFlags(&sd.ev[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        sd.failed = true;  // run single-phase from now on; nothing half-made is used
+        return nullptr;
+    }
+    sd.ready = true;
+    return &sd;
+}
+
+}  // namespace
+
+// The solve keeps pace with the chain when the free SMs solve one chunk of every
+// (sequence, head) no slower than a chain CTA takes one step: about 2.2 us of one SM per
+// solve unit against about 1.8 us per chain step, so 1.25 units per chunk step per free
+// SM. Every phase restarts the chain's pipeline (pipeline fill and drain, about 7 us,
+// and a launch behind an event, about 5 us), so a phase keeps at least 32 chunks of the
+// average sequence. GDR_PREFILL_PHASES=1..8 in the
+// environment overrides the choice (a tuning and testing knob; the result does not
+// depend on the phase count).
+int tc_phases_for(int64_t num_seqs, int64_t total_tokens, int H, int dv, int sms) {
+    if (const char *env = getenv("GDR_PREFILL_PHASES")) {
+        const int v = atoi(env);
+        if (v >= 1 && v <= kMaxPhases) return v;
+    }
+    const int64_t units_per_step = num_seqs * H;
+    const int64_t chain_ctas = units_per_step * (dv / NV);
+    const int64_t free_sms = sms - chain_ctas;
+    if (free_sms < 8 || 5 * units_per_step > 4 * free_sms) return 1;
+    const int64_t avg_chunks = total_tokens / num_seqs / kChunk;
+    const int64_t P = avg_chunks / 32;
+    return P < 1 ? 1 : (P > kMaxPhases ? kMaxPhases : (int)P);
+}
+
+int tc_phases(const PrefillArgs &a) {
+    int dev = -1;
+    if (a.total_tokens == 0 || cudaGetDevice(&dev) != cudaSuccess) return 1;
+    const int P = tc_phases_for(a.num_seqs, a.total_tokens, a.H, a.dv, device_sms(dev));
+    return P > 1 && side_stream(a.stream) ? P : 1;
+}
+
+int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
     const size_t s_bytes = (size_t)a.num_seqs * a.H * a.dk * a.dv * sizeof(float);
     if (a.total_tokens == 0) {  // nothing to compute: S_final = S0 (or zero)
         cudaError_t e = cudaSuccess;
@@ -659,27 +764,68 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L) {
         !tc::make_map_thd(&mo, a.o, a.dv, a.H, a.total_tokens) ||
         !tc::make_map_units(&mt, a.ws + L.T, 2 * L.max_chunks * a.H))
         return GDR_ERR_CUDA;
-    const int st = tc::launch_solve_tc(a, L, mq, mk, mt);
+    if (cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    const int n_slices = a.dv / NV;
+    const int64_t chain_ctas = a.num_seqs * a.H * n_slices;
+    SideStream *sd = nullptr;
+    if (phases > 1) {
+        sd = side_stream(a.stream);
+        if (!sd) return GDR_ERR_CUDA;  // tc_phases made it; it cannot have gone
+    }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GDR_ERR_CUDA;
+    const int free_sms = (int)(device_sms(dev) - chain_ctas);
+
+    // solve of phase 0 on the caller's stream, with the whole GPU
+    int st = tc::launch_solve_tc(a, L, mq, mk, mt, 0, 0, a.stream, true);
     if (st != GDR_OK) return st;
+    if (phases > 1) {  // solves of phases 1 .. P-1 on the side stream, after the solve of
+                       // phase 0 (which has had every SM) and beside the chains
+        cudaError_t e = cudaEventRecord(sd->ev[0], a.stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(sd->stream, sd->ev[0], 0);
+        if (e != cudaSuccess) return GDR_ERR_CUDA;
+        for (int f = 1; f < phases; ++f) {
+            st = tc::launch_solve_tc(a, L, mq, mk, mt, f, free_sms, sd->stream, false);
+            if (st != GDR_OK) return st;
+            if (cudaEventRecord(sd->ev[f], sd->stream) != cudaSuccess) return GDR_ERR_CUDA;
+        }
+    }
     TcParams p;
-    p.S0 = a.S0;
     p.factors = reinterpret_cast<const float *>(a.ws + L.G);
     p.cu_seqlens = a.cu_seqlens;
-    p.seq_chunk = reinterpret_cast<const int32_t *>(a.ws + L.seq_chunk);
     p.num_seqs = a.num_seqs;
     p.total_tokens = a.total_tokens;
     p.H = a.H;
     p.dv = a.dv;
-    p.n_slices = a.dv / NV;
+    p.n_slices = n_slices;
+    p.phases = phases;
     p.o = (__nv_bfloat16 *)a.o;
-    p.S_final = a.S_final;
     p.ctl = (int32_t *)(a.ws + L.ctl);
-    if (cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
-        return GDR_ERR_CUDA;
-    const unsigned grid = (unsigned)(a.num_seqs * a.H * p.n_slices);
-    tc_chain_kernel<<<grid, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mt, mo, p);
-    return cuda_status(cudaGetLastError());
+    float *S_mid = reinterpret_cast<float *>(a.ws + L.S);
+    for (int f = 0; f < phases; ++f) {
+        if (f > 0 && cudaStreamWaitEvent(a.stream, sd->ev[f], 0) != cudaSuccess) return GDR_ERR_CUDA;
+        p.phase = f;
+        p.seq_chunk = reinterpret_cast<const int32_t *>(a.ws + L.seq_chunk) + (size_t)f * (a.num_seqs + 1);
+        p.S_in = f == 0 ? a.S0 : S_mid;
+        p.S_out = f == phases - 1 ? a.S_final : S_mid;
+        // a programmatic dependent of the kernel ahead of it (the solve of phase 0, or the
+        // chain of the previous phase); it waits for that kernel before reading its results
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)chain_ctas);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cfg.stream = a.stream;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, tc_chain_kernel, mq, mk, mv, mt, mo, p) != cudaSuccess)
+            return GDR_ERR_CUDA;
+    }
+    return GDR_OK;
 }
 
 }  // namespace gdr

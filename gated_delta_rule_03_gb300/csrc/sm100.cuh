@@ -94,6 +94,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start before the kernel ahead of it in the stream has finished;
+// griddep_wait blocks until that kernel has completed and its memory writes are
+// visible (a no-op for a kernel launched without the attribute). griddep_launch_dependents
+// lets the next kernel in the stream be launched early (every CTA of this grid must
+// issue it, or exit, before that happens).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

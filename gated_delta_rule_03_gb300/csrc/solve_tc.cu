@@ -273,8 +273,9 @@ __device__ __forceinline__ void warp_stage_tprime(float *__restrict__ U, const f
 struct SolveParams {
     const float *log_alpha, *beta;
     const int4 *plan;  // per chunk: sequence, first token, tokens, index within the sequence
-    int32_t *ctl;      // [0] status, [1] number of chunks
+    int32_t *ctl;      // [0] status, [1] number of chunks, [2 + f] first chunk of phase f
     int H;
+    int phase;            // the units of this phase's chunks are solved
     __nv_bfloat16 *Tout;  // [chunks * H][2][64][64]: T' then A^T per unit
     float *Gout;          // [chunks * H][256]: g, gamma, kdec, form flag per unit
 };
@@ -282,14 +283,6 @@ struct SolveParams {
 __global__ void __launch_bounds__(kThreads, 1)
 tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_t, const SolveParams p) {
-    if (p.ctl[0] != GDR_OK) return;
-    const int n_units = p.ctl[1] * p.H;
-    const int n_pairs = (n_units + 1) / 2;
-    if ((int)blockIdx.x >= n_pairs) return;
-    // this CTA's pairs: blockIdx.x + k * gridDim.x, k < K
-    const int K = (n_pairs - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-    auto pair_of = [&](int k) { return (int)blockIdx.x + k * (int)gridDim.x; };
-
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
@@ -328,6 +321,20 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Everything above overlaps the tail of the planning kernel (programmatic launch);
+    // the plan and the status word are read only after it has completed.
+    griddep_wait();
+    griddep_launch_dependents();
+    // this phase's units are u0 + [0, n_units); local indices below, u0 added for addressing
+    const int u0 = p.ctl[2 + p.phase] * p.H;
+    const int n_units = p.ctl[0] == GDR_OK ? p.ctl[3 + p.phase] * p.H - u0 : 0;
+    const int n_pairs = (n_units + 1) / 2;
+    // this CTA's pairs: blockIdx.x + k * gridDim.x, k < K (none: every role falls through)
+    const int K = (int)blockIdx.x < n_pairs
+                      ? (n_pairs - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                      : 0;
+    auto pair_of = [&](int k) { return (int)blockIdx.x + k * (int)gridDim.x; };
+
     if (warp == kProducerWarp) {
         // ============================================================ loads and Gram chains
         if (lane == 0) {
@@ -342,6 +349,7 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     for (int which = 0; which < 2; ++which) {
                         int u = 2 * pair_of(k) + which;
                         if (u >= n_units) u = 2 * pair_of(k);  // a missing unit b repeats a
+                        u += u0;
                         const int4 pl = p.plan[u / p.H];
                         const int h = u % p.H;
 #pragma unroll
@@ -385,8 +393,8 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             ga0 = ga1 = gb0 = gb1 = 0.f;
             const int u = 2 * pair_of(k) + which;
             if (k < K && u < n_units) {
-                const int4 pl = p.plan[u / p.H];
-                const int h = u % p.H, len = pl.z;
+                const int4 pl = p.plan[(u0 + u) / p.H];
+                const int h = (u0 + u) % p.H, len = pl.z;
                 if (2 * lane < len) {
                     const size_t off = (size_t)(pl.y + 2 * lane) * p.H + h;
                     ga0 = p.log_alpha[off];
@@ -403,8 +411,8 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         for (int k = 0; k < K; ++k) {
             const int sl = k & 1;
             const int lu = 2 * k + which, ls = lu % kSolvers;  // local unit and its solver slot
-            const int u = 2 * pair_of(k) + which;
-            const bool exists = u < n_units;
+            const bool exists = 2 * pair_of(k) + which < n_units;
+            const int u = u0 + 2 * pair_of(k) + which;
             float *U = lslot(ls);
             float *g = U + UNIT_FLOATS;
             bool ok = true;
@@ -519,8 +527,8 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const int sv = warp - kSolverWarp0;
         for (int lu = sv; lu < 2 * K; lu += kSolvers) {
             const int k = lu >> 1, which = lu & 1;
-            const int u = 2 * pair_of(k) + which;
-            if (u >= n_units) continue;  // the missing half of an odd last pair
+            if (2 * pair_of(k) + which >= n_units) continue;  // the missing half of an odd last pair
+            const int u = u0 + 2 * pair_of(k) + which;
             if (!mbar_wait(bar(B_LF0 + sv), (lu / kSolvers) & 1)) { *fail = 1; break; }
             float *U = lslot(sv);
             const float *g = U + UNIT_FLOATS;
@@ -553,7 +561,8 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 namespace tc {
 
 int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &map_q,
-                    const CUtensorMap &map_k, const CUtensorMap &map_t) {
+                    const CUtensorMap &map_k, const CUtensorMap &map_t, int phase, int max_ctas,
+                    cudaStream_t stream, bool programmatic) {
     SolveParams p;
     p.log_alpha = a.log_alpha;
     p.beta = a.beta;
@@ -562,6 +571,7 @@ int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &
     p.H = a.H;
     p.Tout = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.T);
     p.Gout = reinterpret_cast<float *>(a.ws + L.G);
+    p.phase = phase;
     if (cudaFuncSetAttribute(tc_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
         return GDR_ERR_CUDA;
@@ -570,9 +580,19 @@ int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return GDR_ERR_CUDA;
     const int64_t pairs = (L.max_chunks * a.H + 1) / 2;  // upper bound; the kernel reads the count
-    const int64_t grid = pairs < (int64_t)sms ? pairs : (int64_t)sms;  // one CTA per SM
-    tc_solve_kernel<<<(unsigned)grid, kThreads, SMEM_BYTES, a.stream>>>(map_q, map_k, map_t, p);
-    return cuda_status(cudaGetLastError());
+    int64_t grid = pairs < (int64_t)sms ? pairs : (int64_t)sms;  // at most one CTA per SM
+    if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
+    return cuda_status(cudaLaunchKernelEx(&cfg, tc_solve_kernel, map_q, map_k, map_t, p));
 }
 
 }  // namespace tc

@@ -81,9 +81,12 @@ bool make_map_thd(CUtensorMap *map, const void *base, int d, int H, int64_t T);
 // Tensor map over [units][64][64] bf16 matrices, one whole matrix per box, 128-byte swizzle.
 bool make_map_units(CUtensorMap *map, const void *base, int64_t units);
 
-// The chunk-parallel solve: T' and A^T for every (chunk, head) into the workspace.
+// The chunk-parallel solve: T' and A^T for every (chunk, head) of one phase into the
+// workspace, on `stream`, with at most max_ctas CTAs (all SMs when max_ctas <= 0);
+// `programmatic` launches it as a programmatic dependent of the kernel ahead of it.
 int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &map_q,
-                    const CUtensorMap &map_k, const CUtensorMap &map_t);
+                    const CUtensorMap &map_k, const CUtensorMap &map_t, int phase, int max_ctas,
+                    cudaStream_t stream, bool programmatic);
 
 }  // namespace tc
 }  // namespace gdr

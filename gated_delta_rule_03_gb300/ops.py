@@ -50,6 +50,8 @@ def _load():
     lib.gdr_decode_step.restype = c_int
     lib.gdr_chunk_fwd_path.argtypes = [c_int, c_int, c_int]
     lib.gdr_chunk_fwd_path.restype = c_int
+    lib.gdr_chunk_fwd_kernel_launches.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int]
+    lib.gdr_chunk_fwd_kernel_launches.restype = c_int
     lib.gdr_read_device_status.argtypes = [vp, ctypes.POINTER(c_int), vp]
     lib.gdr_read_device_status.restype = c_int
     _lib = lib
@@ -172,10 +174,11 @@ def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None):
     return o
 
 
-# What one gdr_chunk_fwd call enqueues on each kernel path (see gdr_chunk_fwd_path in gdr.h).
+# The dominant kernel and the product arithmetic of each kernel path (see
+# gdr_chunk_fwd_path in gdr.h).
 _PATHS = {
-    0: dict(launches=3, main_kernel="exact_chain_kernel", compute_dtype="f32"),
-    1: dict(launches=3, main_kernel="tc_chain_kernel", compute_dtype="bf16"),
+    0: dict(main_kernel="exact_chain_kernel", compute_dtype="f32"),
+    1: dict(main_kernel="tc_chain_kernel", compute_dtype="bf16"),
 }
 
 
@@ -186,9 +189,13 @@ def chunk_fwd_path(dk, dv, dtype):
     return st
 
 
-def chunk_fwd_kernel_launches(dk, dv, dtype):
-    """Kernels one gdr_chunk_fwd call launches for these sizes."""
-    return _PATHS[chunk_fwd_path(dk, dv, dtype)]["launches"]
+def chunk_fwd_kernel_launches(num_seqs, total_tokens, H, dk, dv, dtype):
+    """Kernels one gdr_chunk_fwd call launches for these sizes on the current device."""
+    st = _load().gdr_chunk_fwd_kernel_launches(int(num_seqs), int(total_tokens), int(H), int(dk),
+                                               int(dv), 64, _DTYPES[dtype])
+    if st < 0:
+        raise GdrError(st, "gdr_chunk_fwd_kernel_launches")
+    return st
 
 
 def chunk_fwd_main_kernel(dk, dv, dtype):

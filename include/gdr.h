@@ -116,6 +116,19 @@ size_t gdr_chunk_fwd_workspace_size(int64_t num_seqs, int64_t total_tokens, int 
  *                 Calls that share a workspace must be ordered on one stream.
  *   stream        stream to enqueue on
  * Returns GDR_OK or a negative status from the list above.
+ *
+ * Streams. On the bf16 tensor-core path a call may split its chunks into
+ * phases and run the per-chunk solve of the next phase on a second stream of
+ * the library's own (one per host thread and device, created on first use)
+ * while the sequential chain of the current phase runs on `stream`. That
+ * stream forks from `stream` and joins back into it inside the call, so the
+ * call behaves as one operation on `stream`, including under stream capture.
+ * A call made while `stream` is being captured, before the calling thread has
+ * made an uncaptured call on that device, runs as a single phase on `stream`
+ * alone (same result, no overlap). The phase count is chosen from the sizes
+ * and the SM count; the environment variable GDR_PREFILL_PHASES (1 to 8), read
+ * at each call, overrides it. The results do not depend on it: the state
+ * passes between phases in fp32, exactly as between chunks.
  */
 int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, const float *S0, const int32_t *cu_seqlens,
@@ -180,11 +193,21 @@ int gdr_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
  * Which kernel path gdr_chunk_fwd takes for these sizes, for diagnostics and
  * benchmarks (host-only, no CUDA call): GDR_PATH_EXACT (plain fp32 arithmetic:
  * a planning kernel, a per-chunk kernel and a per-sequence chain kernel) or
- * GDR_PATH_TENSOR (bf16 tensor cores: a planning kernel and one fused kernel).
+ * GDR_PATH_TENSOR (bf16 tensor cores: a planning kernel, then per phase a
+ * chunk-parallel solve kernel and a per-sequence chain kernel).
  * Returns a negative status for unsupported sizes.
  */
 enum { GDR_PATH_EXACT = 0, GDR_PATH_TENSOR = 1 };
 int gdr_chunk_fwd_path(int d_k, int d_v, int dtype);
+
+/*
+ * Number of kernels one uncaptured gdr_chunk_fwd call with these sizes
+ * launches on the current device (the phase count depends on the device's SM
+ * count), for diagnostics and benchmarks. Returns a negative status for
+ * unsupported or invalid sizes, or GDR_ERR_CUDA if the device cannot be read.
+ */
+int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H, int d_k,
+                                  int d_v, int chunk, int dtype);
 
 /*
  * Reads the device status word that the last gdr_chunk_fwd call on this

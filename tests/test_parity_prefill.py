@@ -122,6 +122,72 @@ def test_in_place_state_update():
     assert rel_err(f64(o), o_ref) <= 2e-2
 
 
+@pytest.mark.parametrize("dv", [128, 256])
+@pytest.mark.parametrize("phases", [2, 3, 5, 8])
+def test_phase_split_matches_single_phase(phases, dv, monkeypatch):
+    # The tensor path may split each sequence's chunks into phases (the solve of the next
+    # phase overlapping the chain of this one); the state passes between phases in fp32
+    # as it does between chunks, so every phase count gives the single-phase bits.
+    # Sequences shorter than the phase count leave some phases empty; one is empty.
+    inp = inputs.prefill_inputs([700, 64, 1, 0, 130, 2000], H=3, dk=128, dv=dv, dtype="bf16",
+                                seed=11 + dv, s0_std=0.5, gate="slow")
+    monkeypatch.setenv("GDR_PREFILL_PHASES", "1")
+    o1, S1 = gpu_prefill(inp)
+    monkeypatch.setenv("GDR_PREFILL_PHASES", str(phases))
+    from gated_delta_rule_03_gb300 import ops
+    assert ops.chunk_fwd_kernel_launches(inp.num_seqs, inp.total_tokens, inp.H, 128, dv,
+                                         torch.bfloat16) == 1 + 2 * phases
+    oP, SP = gpu_prefill(inp)
+    assert torch.equal(o1, oP) and torch.equal(S1, SP)
+    check(inp, per_sequence=True)
+
+
+@pytest.mark.parametrize("phases", [1, 4])
+def test_phase_split_in_place_state(phases, monkeypatch):
+    # S_final may be S0: the first phase reads S0 and the last writes S_final
+    from gated_delta_rule_03_gb300 import chunk_fwd
+    monkeypatch.setenv("GDR_PREFILL_PHASES", str(phases))
+    inp = inputs.prefill_inputs([640, 1000, 3], H=2, dk=128, dv=128, dtype="bf16", seed=12,
+                                s0_std=0.5, gate="none")
+    o_ref, S_ref = oracle_prefill(inp)
+    S = inp.S0.cuda()
+    o, _ = chunk_fwd(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), inp.log_alpha.cuda(),
+                     inp.beta.cuda(), S0=S, cu_seqlens=inp.cu_seqlens.cuda(), S_final=S)
+    torch.cuda.synchronize()
+    assert rel_err(f64(S), S_ref) <= 2e-2
+    assert rel_err(f64(o), o_ref) <= 2e-2
+
+
+def test_phase_split_inside_graph_capture(monkeypatch):
+    # the side stream forks from and joins the captured stream; replaying the graph
+    # gives the eager result
+    from gated_delta_rule_03_gb300 import chunk_fwd
+    monkeypatch.setenv("GDR_PREFILL_PHASES", "4")
+    inp = inputs.prefill_inputs([1024, 960], H=4, dk=128, dv=128, dtype="bf16", seed=13,
+                                s0_std=0.2, gate="slow")
+    dev = lambda t: t.cuda()
+    q, k, v, la, b, S0 = map(dev, (inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0))
+    cu = inp.cu_seqlens.cuda()
+    o_eager, S_eager = chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu)
+    o = torch.empty_like(o_eager)
+    S = torch.empty_like(S_eager)
+    from gated_delta_rule_03_gb300 import ops
+    ws = torch.empty(ops.chunk_fwd_workspace_size(inp.num_seqs, inp.total_tokens, inp.H, 128, 128),
+                     dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # an uncaptured call on this thread first
+        chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, o=o, S_final=S, workspace=ws, stream=s)
+    s.synchronize()
+    o.zero_()
+    S.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, o=o, S_final=S, workspace=ws, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_eager) and torch.equal(S, S_eager)
+
+
 def test_bad_cu_seqlens_reported_through_the_status_word():
     from gated_delta_rule_03_gb300 import chunk_fwd, read_device_status
     inp = inputs.prefill_inputs([100, 50], H=2, dk=128, dv=128, dtype="bf16", seed=9)
