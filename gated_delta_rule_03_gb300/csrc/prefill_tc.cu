@@ -49,12 +49,13 @@
 // Warp roles (18 warps; TMEM lane quarter = warp % 4):
 //   warps 0-3   epilogue: O^T of chunk c from TMEM (times gamma_t in the ratio form),
 //               transposed into a staging tile, stored by TMA.
-//   warps 4-7   prep: T' diag(gamma), U'~ and W' (its elected thread issues them), -W'
-//               into the Q slot, the in-place scaling of Q and K (exponential form).
+//   warps 4-7   prep: T' diag(gamma), -W' into the Q slot, the in-place scaling of Q
+//               and K (exponential form).
 //   warps 8-15  state, the sequential chain: the bf16 S^T and U'^T operands in TMEM,
 //               and the decay of the fp32 master S^T (in TMEM);
-//   warp 17     the state's MMA issuer: [QS | WS] once S^T is in place, [S_upd | AU] once
-//               U'^T is.
+//   warp 17     the MMA issuer: [QS | WS] once S^T is in place, [S_upd | AU] once U'^T
+//               is, and U'~, W' of the next chunk in between, where the tensor pipe would
+//               otherwise wait for the state's conversion.
 //   warp 16     producer: the TMA and bulk loads of the three rings, in chunk order, each
 //               as soon as its slot is free.
 // The critical path per chunk is: S^T copy -> [QS | WS] -> U'^T copy -> [S_upd | AU].
@@ -109,16 +110,16 @@ enum {
     B_KF0, B_KF1, B_KF2,     // K slot loaded                              (tx bytes)
     B_KE0, B_KE1, B_KE2,     // K slot free: chunk done (prep 128 arrivals + state commit)
     B_VF0, B_VF1,            // V slot loaded                              (tx bytes)
-    B_VE0, B_VE1,            // V slot free: U'~ and W' done               (prep issuer commit)
-    B_UW0, B_UW1,            // U'~ (buffer c%2) and W' of chunk c done   (prep issuer commit)
+    B_VE0, B_VE1,            // V slot free: U'~ and W' done               (MMA warp commit)
+    B_WD0, B_WD1,            // W' of chunk c done                         (MMA warp commit)
     B_WQ0, B_WQ1,            // -W' of chunk c stored, Q/K scaled          (128 prep arrivals)
     B_WS,                    // [QS | WS] done                             (MMA warp commit)   
     B_SO,                    // [S_upd | AU] done                          (MMA warp commit)   
     B_OFREE,                 // O read by the epilogue                     (128 arrivals)
-    B_UFREE0, B_UFREE1,      // U'~ buffer read by the state               (MMA warp)
+    B_TGR0, B_TGR1,          // T' diag(gamma) of chunk c staged           (128 prep arrivals)
     B_SREADY, B_UREADY,      // S^T / U'^T operands written to TMEM        (8 state warps)
     B_EG0, B_EG1, B_EG2, B_EG3,  // epilogue gates of chunk c in slot c%4  (128 prep arrivals)
-    B_DRAIN0, B_DRAIN1,      // drain after an abort
+    B_DRAIN,                 // drain after an abort
     B_COUNT
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * B_COUNT;
@@ -232,16 +233,16 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mbar_init(bar(B_QE0 + i), 1);
             mbar_init(bar(B_VF0 + i), 1);
             mbar_init(bar(B_VE0 + i), 1);
-            mbar_init(bar(B_UW0 + i), 1);
+            mbar_init(bar(B_WD0 + i), 1);
             mbar_init(bar(B_WQ0 + i), kPrepThreads);
-            mbar_init(bar(B_UFREE0 + i), 1);
-            mbar_init(bar(B_DRAIN0 + i), 1);
+            mbar_init(bar(B_TGR0 + i), kPrepThreads);
         }
         for (int i = 0; i < 3; ++i) {
             mbar_init(bar(B_KF0 + i), 1);
             mbar_init(bar(B_KE0 + i), kPrepThreads + 1);
         }
         for (int i = 0; i < 4; ++i) mbar_init(bar(B_EG0 + i), kPrepThreads);
+        mbar_init(bar(B_DRAIN), 1);
         mbar_init(bar(B_WS), 1);
         mbar_init(bar(B_SO), 1);
         mbar_init(bar(B_OFREE), kEpiThreads);
@@ -362,7 +363,6 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     } else if (warp < kStateWarp0) {
         // ============================================================ prep
         const int ptid = tid - 32 * kPrepWarp0;
-        const bool issuer = ptid == 0;
         const int q = warp & 3;  // TMEM lane quarter
         volatile int *fail = &flags[0];
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
@@ -388,11 +388,13 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     const uint32_t off = (uint32_t)(t * 128 + (((j ^ t) & 7) << 4));
                     uint4 w = *reinterpret_cast<const uint4 *>(vs_p + RV_T + off);
                     uint32_t *uw = &w.x;
+                    const float4 ga = *reinterpret_cast<const float4 *>(gate + G_GAM + 8 * j);
+                    const float4 gb = *reinterpret_cast<const float4 *>(gate + G_GAM + 8 * j + 4);
+                    const float gj[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&uw[e]));
-                        uw[e] = pack_bf16x2(f.x * gate[G_GAM + 8 * j + 2 * e],
-                                            f.y * gate[G_GAM + 8 * j + 2 * e + 1]);
+                        uw[e] = pack_bf16x2(f.x * gj[2 * e], f.y * gj[2 * e + 1]);
                     }
                     *reinterpret_cast<uint4 *>(sm + OFF_TG + off) = w;
                 }
@@ -400,33 +402,12 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 if (ptid == 0) eg[256 + (c & 3)] = ratio ? 1.f : 0.f;
                 mbar_arrive(bar(B_EG0 + (c & 3)));
             }
+            // T' diag(gamma) is staged: the MMA warp issues U'~ and W' when the chain
+            // reaches them (the single TG buffer is reused only after U'~, W' are done)
             fence_async_smem();
-            tc_fence_before();
-            named_sync(kBarPrep, kPrepThreads);
-
-            // ---- U'~ and W'
-            if (issuer) {
-                const bool ok = c < 2 || mbar_wait(bar(B_UFREE0 + (c & 1)), ((c >> 1) - 1) & 1);
-                if (ok) {
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + TM_U + 64 * (c & 1), sw128_desc(vs + kk * 2048, 8192, 1024),
-                                 sw128_desc(vs + RV_T + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + TM_W, sw128_desc(ks + kk * 2048, 8192, 1024),
-                                 sw128_desc(sbase + OFF_TG + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0),
-                                 kk > 0);
-                    mma_commit(bar(B_UW0 + (c & 1)));
-                    mma_commit(bar(B_VE0 + (c & 1)));  // V and T' are read
-                } else {
-                    note_fail(0);
-                }
-            }
-            __syncwarp();
-            // U'~, W' done; the Q slot's -W' half free once [QS | WS] of chunk c - 2 is done
-            bool ok = mbar_wait(bar(B_UW0 + (c & 1)), u & 1);
+            mbar_arrive(bar(B_TGR0 + (c & 1)));
+            // W' done; the Q slot's -W' half free once [QS | WS] of chunk c - 2 is done
+            bool ok = mbar_wait(bar(B_WD0 + (c & 1)), u & 1);
             if (ok && c >= 2) ok = mbar_wait(bar(B_QE0 + (c & 1)), (u - 1) & 1);
             if (!check(ok)) break;
             tc_fence_after();
@@ -471,14 +452,37 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mbar_arrive(bar(B_WQ0 + (c & 1)));
             mbar_arrive(bar(B_KE0 + c % 3));  // this thread reads the K slot no more
         }
-        if (*fail && issuer) {  // let issued MMAs land before TMEM and shared memory go away
-            mma_commit(bar(B_DRAIN0));
-            mbar_wait(bar(B_DRAIN0), 0);
-        }
     } else if (warp == kMmaWarp) {
         // ============================================================ state MMA issuer
         if (lane == 0) {
-            for (int c = 0; c < n_chunks; ++c) {
+            // U'~^T = V^T T'^T into buffer j % 2 and W'^T = K^T (T' diag gamma)^T of chunk j,
+            // once prep has staged T' diag(gamma) (it saw V, T' and K land). They are issued
+            // where the tensor pipe would otherwise idle: after [QS | WS] of chunk j - 1,
+            // while the state converts U'^T, or else after [S_upd | AU] of chunk j - 1.
+            // W' first: prep transposes it while U'~ is computed.
+            auto issue_uw = [&](int j) {
+                const uint32_t vs = sbase + vslot(j), ks = sbase + kslot(j);
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM_W, sw128_desc(ks + kk * 2048, 8192, 1024),
+                             sw128_desc(sbase + OFF_TG + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0),
+                             kk > 0);
+                mma_commit(bar(B_WD0 + (j & 1)));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM_U + 64 * (j & 1), sw128_desc(vs + kk * 2048, 8192, 1024),
+                             sw128_desc(vs + RV_T + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
+                // U'~ needs no barrier of its own: the state reads it after B_WS, which
+                // this thread commits after these MMAs
+                mma_commit(bar(B_VE0 + (j & 1)));  // V and T' are read
+            };
+            auto tg_ready = [&](int j) { return bar(B_TGR0 + (j & 1)); };
+            if (n_chunks > 0) {
+                if (mbar_wait(tg_ready(0), 0)) issue_uw(0);
+                else note_fail(1);
+            }
+            for (int c = 0; c < n_chunks && !flags[3]; ++c) {
                 // [O^T | X^T] = S^T [Q; -W']^T once S^T, -W' and (for the O buffer) the
                 // epilogue of chunk c - 1 are ready
                 bool ok = mbar_wait(bar(B_SREADY), c & 1) && mbar_wait(bar(B_WQ0 + (c & 1)), (c >> 1) & 1);
@@ -493,10 +497,24 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                                 idesc_bf16(128, 128, 0, 0), kk > 0);
                 mma_commit(bar(B_WS));
                 mma_commit(bar(B_QE0 + (c & 1)));  // Q and -W' are read
+                // W', U'~ of the next chunk now, while the state converts U'^T, if prep
+                // stages T' diag(gamma) within a few hundred cycles (TM_U buffer (c+1)%2 was
+                // converted before [S_upd | AU] of chunk c - 1; W' of chunk c was read before
+                // B_WQ); else after [S_upd | AU]
+                bool uw_next = c + 1 >= n_chunks;
+                if (!uw_next) {
+                    const uint32_t tb = tg_ready(c + 1), par = ((c + 1) >> 1) & 1;
+                    const long long t0 = clock64();
+                    bool ready = mbar_test_wait(tb, par);
+                    while (!ready && clock64() - t0 < 400) ready = mbar_test_wait(tb, par);
+                    if (ready) {
+                        issue_uw(c + 1);
+                        uw_next = true;
+                    }
+                }
                 // [S^T | O^T] += U'^T [K | A^T] once U'^T (and the decayed master) is in place
                 if (!mbar_wait(bar(B_UREADY), c & 1)) { note_fail(1); break; }
                 tc_fence_after();
-                mbar_arrive(bar(B_UFREE0 + (c & 1)));
                 const uint32_t ks = sbase + kslot(c);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // tokens 16kk..16kk+15: columns X + 32(kk/2) + 8(kk%2)
@@ -504,10 +522,14 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                                 sw128_desc(ks + kk * 2048, 8192, 1024), idesc_bf16(128, 192, 0, 1), 1);
                 mma_commit(bar(B_SO));
                 mma_commit(bar(B_KE0 + c % 3));  // the state's last reads of the K slot
+                if (!uw_next) {
+                    if (!mbar_wait(tg_ready(c + 1), ((c + 1) >> 1) & 1)) { note_fail(1); break; }
+                    issue_uw(c + 1);
+                }
             }
             if (flags[3]) {  // let issued MMAs land before TMEM and shared memory go away
-                mma_commit(bar(B_DRAIN1));
-                mbar_wait(bar(B_DRAIN1), 0);
+                mma_commit(bar(B_DRAIN));
+                mbar_wait(bar(B_DRAIN), 0);
             }
         }
     } else if (warp >= kStateWarp0 && warp < kStateWarp0 + kStateWarps) {
