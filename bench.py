@@ -300,7 +300,7 @@ def run_gdr(args):
     tokens = inp.total_tokens
     value = world * tokens * args.steps / (total_ms / 1e3)
     kernel_launches = ops.chunk_fwd_kernel_launches(inp.num_seqs, inp.total_tokens, inp.H, inp.dk,
-                                                    inp.dv, q.dtype)
+                                                    inp.dv, q.dtype, varlen=cu is not None)
     main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype)
     bytes_call = prefill_bytes(inp)
     achieved = bytes_call / (call_ms / 1e3) / 1e9

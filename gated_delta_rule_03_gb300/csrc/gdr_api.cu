@@ -45,6 +45,8 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
         off = align_up(off + (size_t)L.max_chunks * (size_t)H * 256 * sizeof(float), 256);
         L.S = off;  // the state handed from one phase to the next
         off = align_up(off + (size_t)num_seqs * (size_t)H * dk * dv * sizeof(float), 256);
+        L.F = off;  // the solve's pair counters, then one flag per (chunk, head) unit
+        off = align_up(off + ((size_t)kCounters + (size_t)L.max_chunks * (size_t)H) * sizeof(int32_t), 256);
     }
     L.total = off;
     return L;
@@ -134,7 +136,7 @@ int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
     a.o = o; a.S_final = S_final;
     a.ws = (char *)workspace;
     a.stream = (cudaStream_t)stream;
-    const int phases = L.tensor_path ? tc_phases(a) : 1;
+    const int phases = L.tensor_path ? tc_schedule(a) : 1;
     st = launch_plan(a, L, phases);
     if (st != GDR_OK) return st;
     return L.tensor_path ? launch_prefill_tc(a, L, phases) : launch_prefill_exact(a, L);
@@ -167,16 +169,13 @@ int gdr_chunk_fwd_path(int d_k, int d_v, int dtype) {
 }
 
 int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H, int d_k,
-                                  int d_v, int chunk, int dtype) {
+                                  int d_v, int chunk, int dtype, int varlen) {
     const int st = check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype);
     if (st != GDR_OK) return st;
     if (!use_tensor_path(d_k, d_v, dtype)) return 3;  // plan, per-chunk prep, chain
     if (total_tokens == 0) return 1;  // the plan; the state copy is not a kernel of ours
-    int dev = -1, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return GDR_ERR_CUDA;
-    return 1 + 2 * tc_phases_for(num_seqs, total_tokens, H, d_v, sms);
+    const int n = tc_schedule_launches(num_seqs, total_tokens, H, d_v, varlen != 0);
+    return n < 0 ? GDR_ERR_CUDA : n;
 }
 
 int gdr_read_device_status(const void *workspace, int *status, gdr_stream_t stream) {

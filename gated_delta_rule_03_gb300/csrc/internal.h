@@ -12,6 +12,7 @@ namespace gdr {
 
 constexpr int kChunk = 64;  // tokens per chunk (the only chunk size the kernels support)
 constexpr int kMaxPhases = 8;  // most phases a tensor-core prefill is split into
+constexpr int kCounters = 64;  // int32 words before the unit flags in the F region
 
 // Everything gdr_chunk_fwd receives, after host validation.
 struct PrefillArgs {
@@ -40,6 +41,8 @@ struct WsLayout {
     size_t T;             // tensor-core path: bf16 [max_chunks * H][2][64][64] T' and A^T per unit
     size_t G;             // tensor-core path: fp32 [max_chunks * H][256] decay factors per unit
     size_t S;             // tensor-core path: fp32 [num_seqs][H][dk][dv] state between phases
+    size_t F;             // tensor-core path: int32 [kCounters] pair counters (one per phase),
+                          // then [max_chunks * H] unit-solved flags (fused schedule)
     size_t total;
     bool tensor_path;     // bf16 tensor-core kernel (true) or exact fp32-arithmetic kernels
 };
@@ -48,15 +51,21 @@ bool use_tensor_path(int dk, int dv, int dtype);
 WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype);
 
 // Launchers (return GDR_OK or GDR_ERR_CUDA).
+// The planning kernel, for `phases` phases (a phase count of 0, the fused schedule, plans
+// one phase and clears the unit flags).
 int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases);
 int launch_prefill_exact(const PrefillArgs &a, const WsLayout &L);
 int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases);
 
-// Phases of a tensor-core prefill of these sizes on a GPU with `sms` SMs (1 .. kMaxPhases).
-int tc_phases_for(int64_t num_seqs, int64_t total_tokens, int H, int dv, int sms);
-// The phases a call with these arguments runs: tc_phases_for on the current device, or 1
-// when the second stream it needs cannot be had (see launch_prefill_tc).
-int tc_phases(const PrefillArgs &a);
+// The schedule of a tensor-core prefill: 0 for the fused cooperative launch, else the
+// number of phases (1 .. kMaxPhases) of the two-kernel schedule.
+int tc_schedule_for(int64_t num_seqs, int64_t total_tokens, int H, int dv, int sms, bool varlen,
+                    bool cooperative);
+// The schedule a call with these arguments runs on the current device (falls back to
+// one phase when the second stream of the phased schedule cannot be had).
+int tc_schedule(const PrefillArgs &a);
+// Kernels one call with these sizes launches on the current device (or -1).
+int tc_schedule_launches(int64_t num_seqs, int64_t total_tokens, int H, int dv, bool varlen);
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
                   int dtype, cudaStream_t stream);

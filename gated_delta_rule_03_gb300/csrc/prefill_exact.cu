@@ -70,12 +70,15 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_sums, int *
 //   seq_chunk[f * (num_seqs + 1) + n] first chunk of sequence n in phase f; the entry at
 //                                     n = num_seqs is the end of phase f
 //   ctl[0] status, ctl[1] number of chunks, ctl[2 + f] first chunk of phase f (f <= P)
+//   zero[0 .. n_zero)                 cleared (the solve's pair counters and, for the fused
+//                                     schedule, the unit-solved flags after them)
 // A single block of 1024 threads: sequences in blocks of 1024 for the prefix sums, then a
 // group of threads per sequence writes its plan entries.
 __global__ void __launch_bounds__(1024)
 plan_kernel(const int32_t *__restrict__ cu, int64_t num_seqs, int64_t total_tokens,
             int64_t max_chunks, int phases, int4 *__restrict__ plan,
-            int32_t *__restrict__ seq_chunk, int32_t *__restrict__ ctl) {
+            int32_t *__restrict__ seq_chunk, int32_t *__restrict__ ctl,
+            int32_t *__restrict__ zero, int64_t n_zero) {
     __shared__ int s_warp[32];
     __shared__ int s_off[kMaxPhases + 1];
     __shared__ int s_bad;
@@ -85,6 +88,7 @@ plan_kernel(const int32_t *__restrict__ cu, int64_t num_seqs, int64_t total_toke
     // itself up and waits for this grid to complete before reading the plan
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) s_bad = 0;
+    for (int64_t i = tid; i < n_zero; i += blockDim.x) zero[i] = 0;
     __syncthreads();
     const int64_t seq_len = cu ? 0 : total_tokens / num_seqs;
     // first token and length of sequence n; false if cu_seqlens is out of range there
@@ -175,10 +179,14 @@ plan_kernel(const int32_t *__restrict__ cu, int64_t num_seqs, int64_t total_toke
 }
 
 int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases) {
+    const bool fused = phases == 0;
     plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.num_seqs, a.total_tokens, L.max_chunks,
-                                          phases, (int4 *)(a.ws + L.plan),
+                                          fused ? 1 : phases, (int4 *)(a.ws + L.plan),
                                           (int32_t *)(a.ws + L.seq_chunk),
-                                          (int32_t *)(a.ws + L.ctl));
+                                          (int32_t *)(a.ws + L.ctl),
+                                          L.tensor_path ? (int32_t *)(a.ws + L.F) : nullptr,
+                                          !L.tensor_path ? 0
+                                          : kCounters + (fused ? L.max_chunks * a.H : 0));
     return cuda_status(cudaGetLastError());
 }
 

@@ -326,6 +326,30 @@ __device__ __forceinline__ void bulk_wait_group_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Waits until at most N bulk groups of this thread have not completed (writes performed).
+template <int N> __device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Orders this thread's global-memory accesses through the generic proxy with its
+// accesses through the async proxy (TMA and bulk copies), both ways.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Cross-CTA handoff within one (cooperative) grid: everything this thread has written,
+// or has seen written through a CTA-scope synchronisation, is visible to a thread that
+// acquires the flag before it sees the flag set.
+__device__ __forceinline__ void release_flag_gpu(int32_t *flag) {
+    asm volatile("fence.acq_rel.gpu;\n\tst.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1)
+                 : "memory");
+}
+__device__ __forceinline__ int32_t acquire_load_gpu(const int32_t *flag) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return v;
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand (the layout TMA
 // writes with CU_TENSOR_MAP_SWIZZLE_128B: rows of 128 bytes, the 16-byte chunks of
 // row r permuted by chunk ^ (r % 8), 1024-byte aligned atoms of 8 rows).

@@ -50,7 +50,8 @@ def _load():
     lib.gdr_decode_step.restype = c_int
     lib.gdr_chunk_fwd_path.argtypes = [c_int, c_int, c_int]
     lib.gdr_chunk_fwd_path.restype = c_int
-    lib.gdr_chunk_fwd_kernel_launches.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int]
+    lib.gdr_chunk_fwd_kernel_launches.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int,
+                                                  c_int]
     lib.gdr_chunk_fwd_kernel_launches.restype = c_int
     lib.gdr_read_device_status.argtypes = [vp, ctypes.POINTER(c_int), vp]
     lib.gdr_read_device_status.restype = c_int
@@ -189,10 +190,11 @@ def chunk_fwd_path(dk, dv, dtype):
     return st
 
 
-def chunk_fwd_kernel_launches(num_seqs, total_tokens, H, dk, dv, dtype):
-    """Kernels one gdr_chunk_fwd call launches for these sizes on the current device."""
+def chunk_fwd_kernel_launches(num_seqs, total_tokens, H, dk, dv, dtype, varlen=False):
+    """Kernels one gdr_chunk_fwd call launches for these sizes on the current device
+    (varlen: the call passes cu_seqlens)."""
     st = _load().gdr_chunk_fwd_kernel_launches(int(num_seqs), int(total_tokens), int(H), int(dk),
-                                               int(dv), 64, _DTYPES[dtype])
+                                               int(dv), 64, _DTYPES[dtype], int(bool(varlen)))
     if st < 0:
         raise GdrError(st, "gdr_chunk_fwd_kernel_launches")
     return st

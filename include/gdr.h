@@ -117,18 +117,24 @@ size_t gdr_chunk_fwd_workspace_size(int64_t num_seqs, int64_t total_tokens, int 
  *   stream        stream to enqueue on
  * Returns GDR_OK or a negative status from the list above.
  *
- * Streams. On the bf16 tensor-core path a call may split its chunks into
- * phases and run the per-chunk solve of the next phase on a second stream of
- * the library's own (one per host thread and device, created on first use)
- * while the sequential chain of the current phase runs on `stream`. That
- * stream forks from `stream` and joins back into it inside the call, so the
- * call behaves as one operation on `stream`, including under stream capture.
- * A call made while `stream` is being captured, before the calling thread has
- * made an uncaptured call on that device, runs as a single phase on `stream`
- * alone (same result, no overlap). The phase count is chosen from the sizes
- * and the SM count; the environment variable GDR_PREFILL_PHASES (1 to 8), read
- * at each call, overrides it. The results do not depend on it: the state
- * passes between phases in fp32, exactly as between chunks.
+ * Schedules. On the bf16 tensor-core path the per-chunk solve and the
+ * sequential chain over the chunks run concurrently in one of two ways, chosen
+ * from the sizes and the device's SM count:
+ *   - fused (sequences of equal length, cu_seqlens NULL, when the chains leave
+ *     enough SMs free): one cooperative kernel launch on `stream` whose CTAs
+ *     share the work; it needs the whole GPU at one CTA per SM.
+ *   - phased: the chunks are split into phases and the solve of the next phase
+ *     runs on a second stream of the library's own (one per host thread and
+ *     device, created on first use) while the chain of the current phase runs
+ *     on `stream`. That stream forks from `stream` and joins back into it inside
+ *     the call, so the call behaves as one operation on `stream`, including
+ *     under stream capture. A call made while `stream` is being captured, before
+ *     the calling thread has made an uncaptured call on that device, runs as a
+ *     single phase on `stream` alone.
+ * The environment variable GDR_PREFILL_PHASES (1 to 8), read at each call,
+ * forces the phased schedule with that many phases. The results do not depend
+ * on the schedule: the state passes between phases in fp32, exactly as between
+ * chunks, and every schedule performs the same arithmetic.
  */
 int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, const float *S0, const int32_t *cu_seqlens,
@@ -202,12 +208,13 @@ int gdr_chunk_fwd_path(int d_k, int d_v, int dtype);
 
 /*
  * Number of kernels one uncaptured gdr_chunk_fwd call with these sizes
- * launches on the current device (the phase count depends on the device's SM
- * count), for diagnostics and benchmarks. Returns a negative status for
- * unsupported or invalid sizes, or GDR_ERR_CUDA if the device cannot be read.
+ * launches on the current device (the schedule depends on the device's SM
+ * count), for diagnostics and benchmarks. varlen: nonzero when the call passes
+ * cu_seqlens. Returns a negative status for unsupported or invalid sizes, or
+ * GDR_ERR_CUDA if the device cannot be read.
  */
 int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H, int d_k,
-                                  int d_v, int chunk, int dtype);
+                                  int d_v, int chunk, int dtype, int varlen);
 
 /*
  * Reads the device status word that the last gdr_chunk_fwd call on this

@@ -136,7 +136,7 @@ def test_phase_split_matches_single_phase(phases, dv, monkeypatch):
     monkeypatch.setenv("GDR_PREFILL_PHASES", str(phases))
     from gated_delta_rule_03_gb300 import ops
     assert ops.chunk_fwd_kernel_launches(inp.num_seqs, inp.total_tokens, inp.H, 128, dv,
-                                         torch.bfloat16) == 1 + 2 * phases
+                                         torch.bfloat16, varlen=True) == 1 + 2 * phases
     oP, SP = gpu_prefill(inp)
     assert torch.equal(o1, oP) and torch.equal(S1, SP)
     check(inp, per_sequence=True)
@@ -186,6 +186,42 @@ def test_phase_split_inside_graph_capture(monkeypatch):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o, o_eager) and torch.equal(S, S_eager)
+
+
+@pytest.mark.parametrize("S,T,H,dv", [(1, 300, 2, 128), (2, 1000, 3, 128), (3, 640, 5, 256),
+                                      (4, 4096, 16, 128)])
+def test_fused_schedule_matches_phased(S, T, H, dv, monkeypatch):
+    # Equal-length batches take the fused cooperative launch (solve and chain CTAs in one
+    # grid, chains waiting on per-unit flags). Forcing the phased two-kernel schedule must
+    # give the same bits; both match the oracle.
+    from gated_delta_rule_03_gb300 import ops
+    inp = inputs.prefill_inputs([T] * S, H=H, dk=128, dv=dv, dtype="bf16", seed=20 + S,
+                                s0_std=0.5, gate="slow")
+    assert inp.cu_seqlens is None
+    monkeypatch.delenv("GDR_PREFILL_PHASES", raising=False)
+    assert ops.chunk_fwd_kernel_launches(S, S * T, H, 128, dv, torch.bfloat16) == 2
+    o_f, S_f = gpu_prefill(inp)
+    monkeypatch.setenv("GDR_PREFILL_PHASES", "1")
+    o_p, S_p = gpu_prefill(inp)
+    assert torch.equal(o_f, o_p) and torch.equal(S_f, S_p)
+    if S * T <= 4000:
+        check(inp)
+
+
+def test_fused_schedule_repeated_calls_share_a_workspace():
+    # the unit flags are cleared by every call's plan: back-to-back calls on one workspace
+    # and stream give identical results
+    from gated_delta_rule_03_gb300 import chunk_fwd, ops
+    inp = inputs.prefill_inputs([512] * 2, H=4, dk=128, dv=128, dtype="bf16", seed=31, s0_std=0.2)
+    dev = lambda t: t.cuda()
+    q, k, v, la, b, S0 = map(dev, (inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0))
+    ws = torch.empty(ops.chunk_fwd_workspace_size(2, 1024, 4, 128, 128), dtype=torch.uint8,
+                     device="cuda")
+    outs = [chunk_fwd(q, k, v, la, b, S0=S0, num_seqs=2, workspace=ws) for _ in range(4)]
+    torch.cuda.synchronize()
+    for o, S in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(S, outs[0][1])
+    assert ops.read_device_status(ws) == 0
 
 
 def test_bad_cu_seqlens_reported_through_the_status_word():
