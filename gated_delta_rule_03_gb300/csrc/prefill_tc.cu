@@ -27,7 +27,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     chain_body<false>(map_q, map_k, map_v, map_t, map_o, p, (int)blockIdx.x);
 }
 
-static_assert(solve::kThreads <= kThreads, "the fused launch runs the solve on the chain's block");
+static_assert(solve::kSolveWarps * 32 <= kThreads, "the fused launch runs the solve on the chain's block");
 constexpr uint32_t FUSED_SMEM_BYTES = SMEM_BYTES > solve::SMEM_BYTES ? SMEM_BYTES : solve::SMEM_BYTES;
 
 // CTAs [0, chain_ctas) run chains, the others the solve.
@@ -39,8 +39,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     if ((int)blockIdx.x < chain_ctas)
         chain_body<true>(map_q, map_k, map_v, map_t, map_o, p, (int)blockIdx.x);
     else
-        solve::solve_body<true>(map_q, map_k, map_t, sp, (int)blockIdx.x - chain_ctas,
-                                (int)gridDim.x - chain_ctas);
+        solve::solve_body<true>(map_q, map_k, sp);
 }
 
 }  // namespace
@@ -160,9 +159,10 @@ SideStream *side_stream(cudaStream_t caller) {
 }  // namespace
 
 // Fused: the chain CTAs plus at least 1.2 solve CTAs per (sequence, head) must fit on
-// the GPU at one CTA per SM. A solve unit takes about 2.2 us of one SM and a chain step
-// about 1.6 us, so with that many solve CTAs the solve stays ahead of the chains. Only
-// for equal-length sequences (the chunk-major unit order is then closed-form).
+// the GPU at one CTA per SM. A solve CTA finishes a unit about every 2 us and a chain
+// step takes about 1.5 us, so with that many solve CTAs the solve about keeps pace with
+// the chains. Only for equal-length sequences (the chunk-major unit order is then
+// closed-form).
 static bool fused_fits(int64_t num_seqs, int H, int dv, int sms) {
     const int64_t units_per_step = num_seqs * H;
     const int64_t free_sms = sms - units_per_step * (dv / chain::NV);
@@ -274,7 +274,7 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     sp.seqs = (int)a.num_seqs;
     sp.seq_chunks = (int)((a.total_tokens / a.num_seqs + kChunk - 1) / kChunk);
     sp.flags = flags;
-    sp.pair_counter = counters;
+    sp.unit_counter = counters;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
@@ -321,7 +321,7 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
     const int free_sms = (int)(device_sms(dev) - chain_ctas);
 
     // solve of phase 0 on the caller's stream, with the whole GPU
-    int st = tc::launch_solve_tc(a, L, mq, mk, mt, 0, 0, a.stream, true);
+    int st = tc::launch_solve_tc(a, L, mq, mk, 0, 0, a.stream, true);
     if (st != GDR_OK) return st;
     if (phases > 1) {  // solves of phases 1 .. P-1 on the side stream, after the solve of
                        // phase 0 (which has had every SM) and beside the chains
@@ -329,7 +329,7 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
         if (e == cudaSuccess) e = cudaStreamWaitEvent(sd->stream, sd->ev[0], 0);
         if (e != cudaSuccess) return GDR_ERR_CUDA;
         for (int f = 1; f < phases; ++f) {
-            st = tc::launch_solve_tc(a, L, mq, mk, mt, f, free_sms, sd->stream, false);
+            st = tc::launch_solve_tc(a, L, mq, mk, f, free_sms, sd->stream, false);
             if (st != GDR_OK) return st;
             if (cudaEventRecord(sd->ev[f], sd->stream) != cudaSuccess) return GDR_ERR_CUDA;
         }

@@ -8,8 +8,8 @@ namespace {
 
 __global__ void __launch_bounds__(kThreads, 1)
 tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                const __grid_constant__ CUtensorMap map_t, const SolveParams p) {
-    solve_body<false>(map_q, map_k, map_t, p, (int)blockIdx.x, (int)gridDim.x);
+                const SolveParams p) {
+    solve_body<false>(map_q, map_k, p);
 }
 
 }  // namespace
@@ -18,7 +18,7 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 namespace tc {
 
 int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &map_q,
-                    const CUtensorMap &map_k, const CUtensorMap &map_t, int phase, int max_ctas,
+                    const CUtensorMap &map_k, int phase, int max_ctas,
                     cudaStream_t stream, bool programmatic) {
     using namespace solve;
     SolveParams p = {};
@@ -30,7 +30,7 @@ int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &
     p.Tout = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.T);
     p.Gout = reinterpret_cast<float *>(a.ws + L.G);
     p.phase = phase;
-    p.pair_counter = reinterpret_cast<int32_t *>(a.ws + L.F) + phase;
+    p.unit_counter = reinterpret_cast<int32_t *>(a.ws + L.F) + phase;
     if (cudaFuncSetAttribute(tc_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
         return GDR_ERR_CUDA;
@@ -38,8 +38,9 @@ int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return GDR_ERR_CUDA;
-    const int64_t pairs = (L.max_chunks * a.H + 1) / 2;  // upper bound; the kernel reads the count
-    int64_t grid = pairs < (int64_t)sms ? pairs : (int64_t)sms;  // at most one CTA per SM
+    // upper bound on the CTAs that find work (the kernel reads the unit count)
+    const int64_t busy = (L.max_chunks * a.H + kGroups - 1) / kGroups;
+    int64_t grid = busy < (int64_t)sms ? busy : (int64_t)sms;  // at most one CTA per SM
     if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
@@ -51,7 +52,7 @@ int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = programmatic ? 1 : 0;
-    return cuda_status(cudaLaunchKernelEx(&cfg, tc_solve_kernel, map_q, map_k, map_t, p));
+    return cuda_status(cudaLaunchKernelEx(&cfg, tc_solve_kernel, map_q, map_k, p));
 }
 
 }  // namespace tc

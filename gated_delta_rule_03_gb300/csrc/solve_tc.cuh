@@ -17,22 +17,26 @@
 // units ordered chunk-major, head-minor. Each unit's decay factors go out with them
 // (fp32 [256]: g[64], gamma[64], kdec[64], then 1 for the ratio form and 0 otherwise),
 // so that the chain kernel uses the same values and the same form. (The two forms are
-// described in prefill_tc.cu; they differ only in where the decay factors are applied.)
+// described in chain_tc.cuh; they differ only in where the decay factors are applied.)
 //
-// Mapping. One CTA per SM walks unit pairs as a pipeline of warp roles joined by
-// mbarriers:
-//   warp 4      loads a pair's keys and queries by TMA into one of two stage slots and
-//               issues its Gram chain [K_a; K_b] [K_a; K_b; Q_a; Q_b]^T (tcgen05, M = 128,
-//               N = 256, K = d_k = 128) into one of two TMEM slots; the diagonal 64x64
-//               blocks are each unit's K K^T and K Q^T;
-//   warps 0-3   read a TMEM slot out (warps 0-1: unit a, TMEM lanes 0-63; 2-3: unit b,
-//               lanes 64-127): the unit's decay factors, its decayed L into fp32 16x16
-//               blocks of one of four solver slots, and its masked, decayed A^T straight
-//               to the workspace;
-//   warps 5-8   one solver warp per slot: the inverse of I + L, then T' in bf16.
-// The inverse is fp32 on the CUDA cores in 16x16 blocks, by one warp and without
-// barriers: the diagonal blocks by forward substitution, the others with warp-level TF32
-// products.
+// Mapping. Each warpgroup of a CTA solves one (chunk, head) unit at a time, on its own:
+// it claims units from the call's counter, and warp w of the group owns the unit's
+// token rows 16w .. 16w + 15 throughout.
+//   * load: the unit's keys and queries by TMA (128-byte-swizzled 64 x 64 bf16 tiles),
+//     issued for the next unit as soon as this one's have been read;
+//   * gates: warp 0 scans the log-decays of the unit (loaded while the previous unit
+//     was worked on) into the decay factors;
+//   * products: warp w forms its 16 rows of K K^T (keys up to its own block, for L) and
+//     of K Q^T (queries from its own block on, for A^T) with warp-level bf16 MMAs,
+//     ten 8-column tiles each, so that the four warps share the work evenly; L goes to
+//     shared memory as fp32 16 x 16 blocks, A^T and the factors to the workspace;
+//   * inverse: the unit lower-triangular (I + L)^{-1} on the CUDA cores in 16 x 16
+//     blocks: warp w inverts diagonal block w by forward substitution, then the blocks
+//     below the diagonal follow level by level (warp w computes block row w, with
+//     warp-level TF32 products), the group meeting at a named barrier between levels;
+//   * T': warp w writes block row w of diag(kdec) (I + L)^{-1} diag(beta) in bf16.
+// Four groups per SM keep four units in flight, so that one unit's latencies (the load,
+// the level barriers) are covered by the others'.
 #pragma once
 
 #include "tc_common.cuh"
@@ -44,10 +48,10 @@ using namespace sm100;
 using namespace tc;
 
 constexpr int C = kChunk;
-constexpr int kThreads = 288;  // 9 warps
-constexpr int kProducerWarp = 4, kSolverWarp0 = 5, kSolvers = 4;
-// fused launch only: one publisher warp per solver slot releases the slot's units
-constexpr int kPublisherWarp0 = kSolverWarp0 + kSolvers;
+constexpr int kGroups = 4;                 // warpgroups per CTA, one unit each at a time
+constexpr int kThreads = kGroups * 128;    // the standalone kernel's block
+constexpr int kSolveWarps = kGroups * 4;   // warps of a fused launch's block that solve
+
 // A 16x16 fp32 block is stored row-major with its columns permuted per row: element
 // (r, c) at r*16 + (c ^ sw(r)), sw(r) = 8*bit1(r) + 4*bit2(r). The permutation moves
 // groups of four columns, so row segments of 2 and 4 stay contiguous, and it makes both
@@ -59,8 +63,8 @@ constexpr int BF = 256;             // floats per block
 // Lower-triangular 4x4 arrangement of 16x16 blocks: block (i, k), k <= i, at index
 // i(i+1)/2 + k. A unit has sixteen block slots: the ten of L, where M_ik = N_ii L_ik
 // replaces L_ik (i > k) and N_ii replaces L_ii, then six for N_ik (i > k). Slots are
-// BF + 4 floats apart (16-byte aligned) so that the four diagonal blocks, read at the
-// same element by the forward substitution, start on different banks.
+// BF + 4 floats apart (16-byte aligned) so that blocks read at the same element by
+// different warps start on different banks.
 constexpr int BS = BF + 4;
 __host__ __device__ constexpr int blk(int i, int k) { return (i * (i + 1) / 2 + k) * BS; }
 __host__ __device__ constexpr int nblk(int i, int k) {  // N_ik, i > k
@@ -68,36 +72,21 @@ __host__ __device__ constexpr int nblk(int i, int k) {  // N_ik, i > k
 }
 constexpr int UNIT_FLOATS = 16 * BS;
 
-// Stage slot (64 KB), per d_k half b (32 KB): K_a | K_b | Q_a | Q_b, 8 KB each; rows
-// 0-127 are the Gram chain's A operand, rows 0-255 its B operand.
-constexpr uint32_t STAGE = 65536;
-constexpr uint32_t OFF_LS = 2 * STAGE;  // solver slots: blocks, then the unit's gates
-constexpr int G_G = 0, G_GAM = 64, G_GINV = 128, G_BETA = 192, G_KDEC = 256, G_UNIT = 320;
-constexpr uint32_t LSLOT = 18432;  // blocks, gates; 1024-aligned (its first 8 KB stage T')
-static_assert(UNIT_FLOATS * 4 + G_UNIT * 4 <= LSLOT && UNIT_FLOATS * 4 >= 8192, "solver slot");
-constexpr uint32_t OFF_BAR = OFF_LS + kSolvers * LSLOT;
-enum {
-    B_STF0 = 0, B_STF1,  // stage slot loaded                  (tx bytes)
-    B_STE0, B_STE1,      // stage slot read by the Gram chain   (commit)
-    B_TMF0, B_TMF1,      // TMEM slot holds a pair's Gram       (commit)
-    B_TME0, B_TME1,      // TMEM slot read out                  (128 read-out arrivals)
-    B_LF0, B_LF1, B_LF2, B_LF3,  // solver slot filled          (64 read-out arrivals)
-    B_LE0, B_LE1, B_LE2, B_LE3,  // solver slot free again      (solver lane 0)
-    B_PUB0, B_PUB1, B_PUB2, B_PUB3,      // fused: slot's unit stored        (32 solver lanes)
-    B_PUBE0, B_PUBE1, B_PUBE2, B_PUBE3,  // fused: slot's unit published     (publisher)
-    B_PID0, B_PID1, B_PID2, B_PID3, B_PID4, B_PID5, B_PID6, B_PID7,  // pair id k in ring[k % 8]
-    B_DRAIN,
-    B_COUNT
-};
-constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * B_COUNT;
-constexpr uint32_t OFF_FAIL = OFF_TMEM_SLOT + 4;
-constexpr uint32_t OFF_RING = OFF_FAIL + 16;  // int[8]: the pairs this CTA claimed
-constexpr uint32_t SMEM_USED = OFF_RING + 32;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
-static_assert(SMEM_BYTES <= 232448 && LSLOT % 1024 == 0 && OFF_LS % 1024 == 0, "shared memory");
-constexpr uint32_t TM_COLS = 512;  // two 256-column slots
+// Shared memory of one group (the CTA holds kGroups of them, 1024-aligned):
+//   keys then queries, each two 64-feature halves of 64 token rows (8 KB, 128-byte
+//   swizzled as TMA writes them); the blocks; the unit's gates; the load barrier, the
+//   next unit's index and the group's failure flag.
+constexpr uint32_t G_K = 0, G_Q = 16384;
+constexpr uint32_t G_BLK = 32768;
+constexpr uint32_t G_GATES = G_BLK + UNIT_FLOATS * 4;
+constexpr int GG_G = 0, GG_GAM = 64, GG_GINV = 128, GG_BETA = 192, GG_KDEC = 256;  // floats
+constexpr uint32_t G_BAR = G_GATES + 5 * 64 * 4;
+constexpr uint32_t G_NEXT = G_BAR + 8;
+constexpr uint32_t GROUP_BYTES = (G_NEXT + 8 + 1023) / 1024 * 1024;
+constexpr uint32_t SMEM_BYTES = kGroups * GROUP_BYTES + 1024;
+static_assert(SMEM_BYTES <= 232448 && G_GATES % 16 == 0 && G_BAR % 8 == 0, "shared memory");
 
-// ---------------------------------------------------------------- warp-level 16x16 products
+// ---------------------------------------------------------------- warp-level products
 // The unit lower-triangular solve combines 16x16 blocks. These products are far below
 // the tensor-core MMA's minimum tile and sit on a short dependency chain, so they use
 // the warp-synchronous m16n8k8 TF32 MMA with fp32 accumulation (operands rounded to
@@ -147,135 +136,35 @@ __device__ __forceinline__ void warp_store16(float *__restrict__ M, const float 
     }
 }
 
-// N = (I + L)^{-1} for the strictly lower-triangular 64x64 L held as blocks in U (see
-// blk, nblk), by one warp:
-//   1. N_ii by forward substitution: lane l takes columns 2(l%8), 2(l%8)+1 of block l/8.
-//   2. M_ik = N_ii L_ik for the six blocks below the diagonal (over L_ik).
-//   3. N_ij = -sum_{k=j}^{i-1} M_ik N_kj by distance from the diagonal, with the partial
-//      sums that do not need the previous level formed one level early, so that the
-//      dependent chain is four block products long.
-__device__ __forceinline__ void warp_lower_inverse(float *__restrict__ U, int lane) {
-    {
-        const int b = lane >> 3, c0 = 2 * (lane & 7);
-        float *D = U + blk(b, b);
-        float x0[16], x1[16];
+typedef float Acc16[2][4];
+__device__ __forceinline__ void zero16(Acc16 &a) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            x0[r] = (r == c0) ? 1.f : 0.f;
-            x1[r] = (r == c0 + 1) ? 1.f : 0.f;
-        }
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int k = 0; k < 15; ++k) {
-            const float a0 = x0[k], a1 = x1[k];
-#pragma unroll
-            for (int r = k + 1; r < 16; ++r) {
-                const float l = D[el(r, k)];
-                x0[r] = fmaf(-l, a0, x0[r]);
-                x1[r] = fmaf(-l, a1, x1[r]);
-            }
-        }
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < 16; ++r) *reinterpret_cast<float2 *>(D + el(r, c0)) = make_float2(x0[r], x1[r]);
-        __syncwarp();
-    }
-    typedef float Acc[2][4];
-    auto zero = [](Acc &a) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) a[nt][e] = 0.f;
-    };
-    Acc a0, a1, a2, a3, a4, a5;
-    // M_10, M_21, M_32, M_20, M_31, M_30
-    zero(a0); zero(a1); zero(a2); zero(a3); zero(a4); zero(a5);
-    warp_gemm16(U + blk(1, 1), U + blk(1, 0), a0, lane);
-    warp_gemm16(U + blk(2, 2), U + blk(2, 1), a1, lane);
-    warp_gemm16(U + blk(3, 3), U + blk(3, 2), a2, lane);
-    warp_gemm16(U + blk(2, 2), U + blk(2, 0), a3, lane);
-    warp_gemm16(U + blk(3, 3), U + blk(3, 1), a4, lane);
-    warp_gemm16(U + blk(3, 3), U + blk(3, 0), a5, lane);
-    __syncwarp();
-    warp_store16(U + blk(1, 0), a0, lane, 1.f);
-    warp_store16(U + blk(2, 1), a1, lane, 1.f);
-    warp_store16(U + blk(3, 2), a2, lane, 1.f);
-    warp_store16(U + blk(2, 0), a3, lane, 1.f);
-    warp_store16(U + blk(3, 1), a4, lane, 1.f);
-    warp_store16(U + blk(3, 0), a5, lane, 1.f);
-    __syncwarp();
-    // level 1: N_10, N_21, N_32; partial sums P20 = M_20 N_00, P31 = M_31 N_11, P30 = M_30 N_00
-    zero(a0); zero(a1); zero(a2); zero(a3); zero(a4); zero(a5);
-    warp_gemm16(U + blk(1, 0), U + blk(0, 0), a0, lane);
-    warp_gemm16(U + blk(2, 1), U + blk(1, 1), a1, lane);
-    warp_gemm16(U + blk(3, 2), U + blk(2, 2), a2, lane);
-    warp_gemm16(U + blk(2, 0), U + blk(0, 0), a3, lane);
-    warp_gemm16(U + blk(3, 1), U + blk(1, 1), a4, lane);
-    warp_gemm16(U + blk(3, 0), U + blk(0, 0), a5, lane);
-    warp_store16(U + nblk(1, 0), a0, lane, -1.f);
-    warp_store16(U + nblk(2, 1), a1, lane, -1.f);
-    warp_store16(U + nblk(3, 2), a2, lane, -1.f);
-    __syncwarp();
-    // level 2: N_20 = -(P20 + M_21 N_10), N_31 = -(P31 + M_32 N_21); P30 += M_31 N_10
-    warp_gemm16(U + blk(2, 1), U + nblk(1, 0), a3, lane);
-    warp_gemm16(U + blk(3, 2), U + nblk(2, 1), a4, lane);
-    warp_gemm16(U + blk(3, 1), U + nblk(1, 0), a5, lane);
-    warp_store16(U + nblk(2, 0), a3, lane, -1.f);
-    warp_store16(U + nblk(3, 1), a4, lane, -1.f);
-    __syncwarp();
-    // level 3: N_30 = -(P30 + M_32 N_20)
-    warp_gemm16(U + blk(3, 2), U + nblk(2, 0), a5, lane);
-    warp_store16(U + nblk(3, 0), a5, lane, -1.f);
-    __syncwarp();
+        for (int e = 0; e < 4; ++e) a[nt][e] = 0.f;
 }
 
-// T' = diag(kd) N diag(beta) in bf16 (kd = kdec in the ratio form, else 1), by one warp,
-// into a 128-byte-swizzled [64][64] tile at `tile` (the layout a TMA store reads) that
-// overlays the first 8 KB of U: N's ten blocks are read into registers in the m16n8
-// accumulator layout first, the blocks above the diagonal are zero.
-__device__ __forceinline__ void warp_stage_tprime(float *__restrict__ U, const float *__restrict__ g,
-                                                  bool ratio, unsigned char *tile, int lane) {
-    const int gq = lane >> 2, q = lane & 3;
-    float n[10][2][4];
-#pragma unroll
-    for (int bt = 0; bt < 4; ++bt)
-#pragma unroll
-        for (int bi = 0; bi <= bt; ++bi) {
-            const float *B = U + (bt == bi ? blk(bt, bt) : nblk(bt, bi));
-            const int idx = bt * (bt + 1) / 2 + bi;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float2 lo = *reinterpret_cast<const float2 *>(B + el(gq, 8 * nt + 2 * q));
-                const float2 hi = *reinterpret_cast<const float2 *>(B + el(gq + 8, 8 * nt + 2 * q));
-                n[idx][nt][0] = lo.x; n[idx][nt][1] = lo.y; n[idx][nt][2] = hi.x; n[idx][nt][3] = hi.y;
-            }
-        }
-    __syncwarp();
-#pragma unroll
-    for (int bt = 0; bt < 4; ++bt) {
-        float kd[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) kd[h] = ratio ? g[G_KDEC + 16 * bt + gq + 8 * h] : 1.f;
-#pragma unroll
-        for (int bi = 0; bi < 4; ++bi)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int i0 = 16 * bi + 8 * nt + 2 * q;  // columns i0, i0 + 1
-                const float b0 = g[G_BETA + i0], b1 = g[G_BETA + i0 + 1];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int t = 16 * bt + gq + 8 * h;
-                    float x0 = 0.f, x1 = 0.f;
-                    if (bi <= bt) {
-                        const int idx = bt * (bt + 1) / 2 + bi;
-                        // within a diagonal block the entries above the diagonal are zero
-                        x0 = (i0 <= t) ? n[idx][nt][2 * h] * b0 * kd[h] : 0.f;
-                        x1 = (i0 + 1 <= t) ? n[idx][nt][2 * h + 1] * b1 * kd[h] : 0.f;
-                    }
-                    *reinterpret_cast<uint32_t *>(tile + t * 128 + ((((i0 >> 3) ^ t) & 7) << 4) + (i0 & 7) * 2) =
-                        pack_bf16x2(x0, x1);
-                }
-            }
-    }
+// ---------------------------------------------------------------- bf16 products of the Gram
+// ldmatrix of four 8x8 bf16 matrices: lane l supplies a row address of matrix l / 8.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// d += A B for a 16x16 bf16 A (row-major) and a 16x8 B (held by column), fp32 accumulators.
+__device__ __forceinline__ void mma_bf16_16x8x16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                 uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Shared address of the 16-byte segment (row r, features 8c .. 8c + 7) of a 64-feature
+// half tile as TMA writes it with the 128-byte swizzle (segment c of row r at c ^ r % 8).
+__device__ __forceinline__ uint32_t sw128_at(uint32_t half, int r, int c) {
+    return half + (uint32_t)(r * 128 + (((c ^ r) & 7) << 4));
 }
 
 struct SolveParams {
@@ -288,362 +177,363 @@ struct SolveParams {
     // `seq_chunks` chunks each, and a ready flag per unit, set once its results are stored
     int seqs, seq_chunks;
     int32_t *flags;
-    int32_t *pair_counter;  // pairs are claimed from it at run time (zeroed by the plan)
+    int32_t *unit_counter;  // units are claimed from it at run time (zeroed by the plan)
     __nv_bfloat16 *Tout;  // [chunks * H][2][64][64]: T' then A^T per unit
     float *Gout;          // [chunks * H][256]: g, gamma, kdec, form flag per unit
 };
 
-// The solve on CTA `cta` of `ncta`. kFused: the CTA shares a cooperative launch with the
-// chain (which may have more warps: warps past the ninth only pass the block barriers),
+// One warp's part of the solve: warp W of a group (block row W of every unit), its loop
+// over the units the group claims. The block row is a template parameter so that every
+// loop bound and mask below is a constant and the loads can be issued early.
+template <bool kFused>
+struct GroupSolver {
+    const SolveParams &p;
+    const CUtensorMap *map_q, *map_k;
+    uint32_t gbase;            // the group's shared memory
+    float *U, *gt;             // its blocks and gates
+    volatile int *next, *gfail;
+    int grp, lane, u0, n_units;
+
+    // the unit at local index x: the phase's units in order, or (fused) chunk j of
+    // sequence n for head h at x = (j * seqs + n) * H + h
+    __device__ __forceinline__ int unit_at(int x) const {
+        if (!kFused) return u0 + x;
+        const int h = x % p.H, r = x / p.H;
+        return ((r % p.seqs) * p.seq_chunks + r / p.seqs) * p.H + h;
+    }
+    __device__ __forceinline__ void gsync() const { named_sync(1 + grp, 128); }
+    __device__ __forceinline__ uint32_t bar_ld() const { return gbase + G_BAR; }
+    // the leader claims a unit (-1 after the last) and fetches its plan entry
+    __device__ __forceinline__ int claim(int4 &pl) const {
+        const int x = n_units > 0 ? atomicAdd(p.unit_counter, 1) : 0;
+        if (x >= n_units) return -1;
+        pl = p.plan[unit_at(x) / p.H];
+        return x;
+    }
+    __device__ __forceinline__ void issue_load(int x, const int4 &pl) const {  // leader
+        const int h = unit_at(x) % p.H;
+        mbar_arrive_expect_tx(bar_ld(), 4 * 8192);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(gbase + G_K + b * 8192, map_k, bar_ld(), 64 * b, h, pl.y);
+            tma_load_3d(gbase + G_Q + b * 8192, map_q, bar_ld(), 64 * b, h, pl.y);
+        }
+    }
+    // log-decays and write strengths of unit x, two tokens per lane of warp 0 (zero past
+    // the end of the sequence), from the leader's plan entry of it
+    __device__ __forceinline__ void fetch_gates(int x, const int4 &pl, float (&gv)[4]) const {
+        const int first = __shfl_sync(0xffffffffu, pl.y, 0), len = __shfl_sync(0xffffffffu, pl.z, 0);
+        gv[0] = gv[1] = gv[2] = gv[3] = 0.f;
+        if (x < 0) return;
+        const int h = unit_at(x) % p.H;
+        if (2 * lane < len) {
+            const size_t off = (size_t)(first + 2 * lane) * p.H + h;
+            gv[0] = p.log_alpha[off];
+            gv[2] = p.beta[off];
+        }
+        if (2 * lane + 1 < len) {
+            const size_t off = (size_t)(first + 2 * lane + 1) * p.H + h;
+            gv[1] = p.log_alpha[off];
+            gv[3] = p.beta[off];
+        }
+    }
+
+    template <int W>
+    __device__ __forceinline__ void run() const {
+        const int gq = lane >> 2, q = lane & 3;  // m16n8 fragment coordinates
+        const bool leader = W == 0 && lane == 0;
+        int loads = 0, landed = 0;
+        int4 pl_next = make_int4(0, 0, 0, 0);
+        // the first unit
+        if (leader) {
+            const int x = claim(pl_next);
+            *next = x;
+            if (x >= 0) {
+                issue_load(x, pl_next);
+                ++loads;
+            }
+        }
+        gsync();
+        int x = *next;
+        float gv[4] = {0.f, 0.f, 0.f, 0.f};  // warp 0: log-decays, write strengths of unit x
+        if (W == 0) fetch_gates(x, pl_next, gv);
+        uint32_t ld_phase = 0;
+        while (x >= 0) {
+            const int u = unit_at(x);
+            int xn = -1;
+            if (leader) xn = claim(pl_next);  // its latency overlaps the work below
+            // ---- gates of unit x: the shared scan of warp 0
+            if (W == 0) {
+                const ChunkScan sc = chunk_scan(gv[0], gv[1], lane);
+                *reinterpret_cast<float2 *>(gt + GG_G + 2 * lane) = make_float2(sc.g0, sc.g1);
+                *reinterpret_cast<float2 *>(gt + GG_GAM + 2 * lane) = make_float2(fast_exp(sc.g0), fast_exp(sc.g1));
+                *reinterpret_cast<float2 *>(gt + GG_GINV + 2 * lane) = make_float2(fast_exp(-sc.g0), fast_exp(-sc.g1));
+                *reinterpret_cast<float2 *>(gt + GG_BETA + 2 * lane) = make_float2(gv[2], gv[3]);
+                *reinterpret_cast<float2 *>(gt + GG_KDEC + 2 * lane) =
+                    make_float2(fast_exp(sc.g_last - sc.g0), fast_exp(sc.g_last - sc.g1));
+            }
+            if (!mbar_wait(bar_ld(), ld_phase)) *gfail = 1;
+            ld_phase ^= 1;
+            gsync();  // the gates are visible; every thread saw the load land (or gave up)
+            if (*gfail) break;
+            if (leader) ++landed;
+            const bool ratio = gt[GG_G + C - 1] > kRatioSafeLogDecay;
+
+            // ---- rows 16W .. 16W + 15 of K K^T (keys i < 16W + 16) and of K Q^T (queries
+            // t >= 16W): ten 8-column tiles; tile pair j2 <= W holds keys 16 j2 .. 16 j2 + 15,
+            // the others queries 16 (j2 - 1) .. 16 (j2 - 1) + 15
+            float acc[10][4];
+#pragma unroll
+            for (int j = 0; j < 10; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int b = ks >> 2, c = 2 * (ks & 3);  // d_k half, 8-feature segment
+                uint32_t a[4];
+                ldsm_x4(sw128_at(gbase + G_K + b * 8192, 16 * W + (lane & 15), c + (lane >> 4)), a);
+#pragma unroll
+                for (int j2 = 0; j2 < 5; ++j2) {
+                    const bool keys = j2 <= W;
+                    const int r0 = keys ? 16 * j2 : 16 * (j2 - 1);
+                    const uint32_t half = gbase + (keys ? G_K : G_Q) + b * 8192;
+                    uint32_t bf[4];
+                    ldsm_x4(sw128_at(half, r0 + (lane & 7) + 8 * (lane >> 4), c + ((lane >> 3) & 1)), bf);
+                    mma_bf16_16x8x16(acc[2 * j2], a, bf[0], bf[1]);
+                    mma_bf16_16x8x16(acc[2 * j2 + 1], a, bf[2], bf[3]);
+                }
+            }
+            // the gates this warp needs: its rows' (t = 16W + gq + 8hh) and the columns' of
+            // its tiles (i0 = 8j + 2q, two each)
+            float rg[2], rb[2], rgi[2], rkd[2], cg[8][2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int t = 16 * W + gq + 8 * hh;
+                rg[hh] = ratio ? gt[GG_GAM + t] : gt[GG_G + t];
+                rgi[hh] = gt[GG_G + t];
+                rb[hh] = gt[GG_BETA + t];
+                rkd[hh] = ratio ? gt[GG_KDEC + t] : 1.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float2 f = *reinterpret_cast<const float2 *>(gt + (ratio && j < 2 * (W + 1) ? GG_GINV : GG_G) + 8 * j + 2 * q);
+                cg[j][0] = f.x;
+                cg[j][1] = f.y;
+            }
+            const float ginv_c = gt[GG_GINV + C - 1];
+            // L_ti = beta_t Gamma_ti k_t.k_i (i < t) into block row W
+#pragma unroll
+            for (int j = 0; j < 2 * (W + 1); ++j) {
+                const int i0 = 8 * j + 2 * q;
+                float *B = U + blk(W, j >> 1);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int t = 16 * W + gq + 8 * hh;
+                    const float d0 = ratio ? rg[hh] * cg[j][0] : fast_exp(rg[hh] - cg[j][0]);
+                    const float d1 = ratio ? rg[hh] * cg[j][1] : fast_exp(rg[hh] - cg[j][1]);
+                    const float v0 = i0 < t ? rb[hh] * d0 * acc[j][2 * hh] : 0.f;
+                    const float v1 = i0 + 1 < t ? rb[hh] * d1 * acc[j][2 * hh + 1] : 0.f;
+                    *reinterpret_cast<float2 *>(B + el(gq + 8 * hh, 8 * (j & 1) + 2 * q)) = make_float2(v0, v1);
+                }
+            }
+            // A^T_it (t >= i) for keys i = 16W + gq + 8hh and queries t from 16W on, bf16 to
+            // the workspace; the queries before 16W are zero
+            __nv_bfloat16 *arow = p.Tout + (size_t)(2 * u + 1) * C * C;
+#pragma unroll
+            for (int j = 2 * (W + 1); j < 10; ++j) {
+                const int t0 = 8 * (j - 2) + 2 * q;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int i = 16 * W + gq + 8 * hh;
+                    const float d0 = ratio ? ginv_c : fast_exp(cg[j - 2][0] - rgi[hh]);
+                    const float d1 = ratio ? ginv_c : fast_exp(cg[j - 2][1] - rgi[hh]);
+                    const float v0 = t0 >= i ? acc[j][2 * hh] * d0 : 0.f;
+                    const float v1 = t0 + 1 >= i ? acc[j][2 * hh + 1] * d1 : 0.f;
+                    *reinterpret_cast<uint32_t *>(arow + i * C + t0) = pack_bf16x2(v0, v1);
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < W; ++s) {  // rows 16W .. 16W + 15, columns 0 .. 16W - 1
+                const int idx = lane + 32 * s, r = 16 * W + (idx & 15), seg = idx >> 4;
+                *reinterpret_cast<uint4 *>(arow + r * C + 8 * seg) = make_uint4(0, 0, 0, 0);
+            }
+            // the unit's decay factors for the chain: g (warp 0), gamma (1), kdec (2), form (3)
+            {
+                float2 v;
+                if (W == 0) v = *reinterpret_cast<const float2 *>(gt + GG_G + 2 * lane);
+                else if (W == 1) v = *reinterpret_cast<const float2 *>(gt + GG_GAM + 2 * lane);
+                else if (W == 2) v = *reinterpret_cast<const float2 *>(gt + GG_KDEC + 2 * lane);
+                else v = make_float2(lane == 0 ? (ratio ? 1.f : 0.f) : 0.f, 0.f);
+                *reinterpret_cast<float2 *>(p.Gout + (size_t)u * 256 + 64 * W + 2 * lane) = v;
+            }
+            if (leader) *next = xn;
+            gsync();  // keys and queries are read; L is complete; the next unit is known
+            x = *next;
+            if (leader && x >= 0) {
+                fence_async_smem();  // the reads above come before the TMA overwrites the tiles
+                issue_load(x, pl_next);
+                ++loads;
+            }
+            if (W == 0) fetch_gates(x, pl_next, gv);
+
+            // ---- (I + L)^{-1}: diagonal block W by forward substitution, lane l on column
+            // l % 16 (the upper half of the warp repeats the lower and stores nothing)
+            {
+                float *D = U + blk(W, W);
+                const int c0 = lane & 15;
+                float xv[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) xv[r] = (r == c0) ? 1.f : 0.f;
+#pragma unroll
+                for (int k = 0; k < 15; ++k) {
+                    const float ak = xv[k];
+#pragma unroll
+                    for (int r = k + 1; r < 16; ++r) xv[r] = fmaf(-D[el(r, k)], ak, xv[r]);
+                }
+                __syncwarp();
+                if (lane < 16) {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) D[el(r, c0)] = xv[r];
+                }
+                __syncwarp();
+            }
+            // M_Wk = N_WW L_Wk over L_Wk (k < W): the warp's own blocks
+            if (W >= 1) {
+                Acc16 m[W > 0 ? W : 1];
+#pragma unroll
+                for (int k = 0; k < W; ++k) {
+                    zero16(m[k]);
+                    warp_gemm16(U + blk(W, W), U + blk(W, k), m[k], lane);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < W; ++k) warp_store16(U + blk(W, k), m[k], lane, 1.f);
+            }
+            gsync();  // every N_kk is in place
+            // level 1: N_{W,W-1} = -M_{W,W-1} N_{W-1,W-1}, and the partial sums that need
+            // only the diagonal: P20 = M_20 N_00 (warp 2), P31 = M_31 N_11, P30 = M_30 N_00 (3)
+            Acc16 pa, pb;
+            zero16(pa);
+            zero16(pb);
+            if (W >= 1) {
+                constexpr int Wm = W > 0 ? W - 1 : 0;
+                Acc16 n1;
+                zero16(n1);
+                warp_gemm16(U + blk(W, Wm), U + blk(Wm, Wm), n1, lane);
+                if (W == 2) warp_gemm16(U + blk(2, 0), U + blk(0, 0), pa, lane);
+                if (W == 3) {
+                    warp_gemm16(U + blk(3, 1), U + blk(1, 1), pa, lane);
+                    warp_gemm16(U + blk(3, 0), U + blk(0, 0), pb, lane);
+                }
+                warp_store16(U + nblk(W > 0 ? W : 1, Wm), n1, lane, -1.f);
+            }
+            gsync();  // N_10, N_21, N_32 are in place
+            // level 2: N_20 = -(P20 + M_21 N_10) (warp 2); N_31 = -(P31 + M_32 N_21) and
+            // P30 += M_31 N_10 (warp 3)
+            if (W == 2) {
+                warp_gemm16(U + blk(2, 1), U + nblk(1, 0), pa, lane);
+                warp_store16(U + nblk(2, 0), pa, lane, -1.f);
+            } else if (W == 3) {
+                warp_gemm16(U + blk(3, 2), U + nblk(2, 1), pa, lane);
+                warp_gemm16(U + blk(3, 1), U + nblk(1, 0), pb, lane);
+                warp_store16(U + nblk(3, 1), pa, lane, -1.f);
+            }
+            gsync();  // N_20 is in place
+            // level 3: N_30 = -(P30 + M_32 N_20) (warp 3)
+            if (W == 3) {
+                warp_gemm16(U + blk(3, 2), U + nblk(2, 0), pb, lane);
+                warp_store16(U + nblk(3, 0), pb, lane, -1.f);
+            }
+            __syncwarp();
+
+            // ---- T' block row W: diag(kd) N diag(beta), bf16 pairs to the workspace (the
+            // blocks right of the diagonal, and the diagonal block's upper part, are zero)
+            {
+                __nv_bfloat16 *trow = p.Tout + (size_t)2 * u * C * C;
+                float cb[4][2][2];  // beta of columns 16 bi + 8 nt + 2q (+1)
+#pragma unroll
+                for (int bi = 0; bi < 4; ++bi)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const float2 bb = *reinterpret_cast<const float2 *>(gt + GG_BETA + 16 * bi + 8 * nt + 2 * q);
+                        cb[bi][nt][0] = bb.x;
+                        cb[bi][nt][1] = bb.y;
+                    }
+#pragma unroll
+                for (int bi = 0; bi < 4; ++bi) {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int i0 = 16 * bi + 8 * nt + 2 * q;
+                        float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+                        if (bi <= W) {
+                            const float *B = U + (bi == W ? blk(W, W) : nblk(W > bi ? W : 1, W > bi ? bi : 0));
+                            lo = *reinterpret_cast<const float2 *>(B + el(gq, 8 * nt + 2 * q));
+                            hi = *reinterpret_cast<const float2 *>(B + el(gq + 8, 8 * nt + 2 * q));
+                        }
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int t = 16 * W + gq + 8 * hh;
+                            const float2 v = hh ? hi : lo;
+                            const float x0 = i0 <= t ? v.x * cb[bi][nt][0] * rkd[hh] : 0.f;
+                            const float x1 = i0 + 1 <= t ? v.y * cb[bi][nt][1] * rkd[hh] : 0.f;
+                            *reinterpret_cast<uint32_t *>(trow + t * C + i0) = pack_bf16x2(x0, x1);
+                        }
+                    }
+                }
+            }
+            gsync();  // unit u is stored; the blocks and gates may be reused
+            if (kFused && leader) release_flag_gpu(p.flags + u);
+        }
+        if (leader) {
+            if (*gfail) atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
+            // a load still in flight lands before the shared memory goes away
+            for (int j = landed; j < loads; ++j) mbar_wait(bar_ld(), j & 1);
+        }
+    }
+};
+
+// The solve on one CTA. Work is claimed at run time, so the CTA's index does not
+// matter. kFused: the CTA shares a cooperative launch with the chain (whose block has
+// more warps: those past the solve's return at once; no block-wide barrier follows),
 // takes the units in chunk-major order so that the chains find their chunks solved in
 // the order they need them, and publishes each unit with a release of its flag.
 template <bool kFused>
 __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUtensorMap &map_k,
-                                           const CUtensorMap &map_t, const SolveParams &p, int cta,
-                                           int ncta) {
+                                           const SolveParams &p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const uint32_t sbase = smem_u32(sm);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-    auto bar = [&](int i) { return smem_u32(&bars[i]); };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TMEM_SLOT);
-    volatile int *fail = reinterpret_cast<volatile int *>(sm + OFF_FAIL);
-    auto lslot = [&](int s) { return reinterpret_cast<float *>(sm + OFF_LS + s * LSLOT); };
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_STF0 + i), 1);
-            mbar_init(bar(B_STE0 + i), 1);
-            mbar_init(bar(B_TMF0 + i), 1);
-            mbar_init(bar(B_TME0 + i), 128);
-        }
-        for (int i = 0; i < kSolvers; ++i) {
-            mbar_init(bar(B_LF0 + i), 64);
-            mbar_init(bar(B_LE0 + i), 1);
-        }
-        for (int i = 0; i < kSolvers; ++i) {
-            mbar_init(bar(B_PUB0 + i), 32);
-            mbar_init(bar(B_PUBE0 + i), 1);
-        }
-        for (int i = 0; i < 8; ++i) mbar_init(bar(B_PID0 + i), 1);
-        mbar_init(bar(B_DRAIN), 1);
+    if (warp >= kSolveWarps) return;
+    const int grp = warp >> 2, w = warp & 3;  // group, and the warp's block row in it
+    unsigned char *gs = sm + grp * GROUP_BYTES;
+    const uint32_t gbase = smem_u32(gs);
+    volatile int *next = reinterpret_cast<volatile int *>(gs + G_NEXT);
+    if (w == 0 && lane == 0) {
+        mbar_init(gbase + G_BAR, 1);
         fence_mbar_init();
-        *fail = 0;
+        next[1] = 0;
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_q);
-        prefetch_tensormap(&map_t);
     }
-    if (warp == 0) {
-        tmem_alloc(smem_u32(tmem_slot), TM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    named_sync(1 + grp, 128);
 
     // Everything above overlaps the tail of the planning kernel (programmatic launch);
     // the plan and the status word are read only after it has completed.
     griddep_wait();
     griddep_launch_dependents();
-    // this phase's units are u0 + [0, n_units); local indices below, u0 added for addressing
+    // this phase's units are u0 + [0, n_units); local indices, u0 added for addressing
     const int u0 = kFused ? 0 : p.ctl[2 + p.phase] * p.H;
     const int n_units =
         p.ctl[0] == GDR_OK ? (kFused ? p.ctl[1] * p.H : p.ctl[3 + p.phase] * p.H - u0) : 0;
-    const int n_pairs = (n_units + 1) / 2;
-    // The CTA's k-th pair, or -1 after its last. The producer claims pairs one at a time
-    // from the call's counter, as its stage slots free up, so that faster CTAs take more
-    // of them, and hands each on through ring[k % 8] and its barrier; -1 marks the end.
-    // (The producer can be at most six pairs ahead of the slowest role, seven with the
-    // second end mark, so a ring slot and its barrier phase are never reused while a
-    // role still needs them.)
-    volatile int *ring = reinterpret_cast<volatile int *>(sm + OFF_RING);
-    auto pair_id = [&](int k) -> int {
-        if (!mbar_wait(bar(B_PID0 + (k & 7)), (k >> 3) & 1)) {
-            *fail = 1;
-            return -1;
-        }
-        return ring[k & 7];
-    };
-    // the unit at local index x: the phase's units in order, or (fused) chunk j of
-    // sequence n for head h at x = (j * seqs + n) * H + h
-    auto unit_at = [&](int x) {
-        if (!kFused) return u0 + x;
-        const int h = x % p.H, r = x / p.H;
-        return ((r % p.seqs) * p.seq_chunks + r / p.seqs) * p.H + h;
-    };
-
-    if (warp == kProducerWarp) {
-        // ============================================================ loads and Gram chains
-        if (lane == 0) {
-            int loads = 0, landed = 0;
-            for (int k = 0; !*fail; ++k) {
-                // claim pair k once stage slot k % 2 is free (Gram k - 2 has read it), hand
-                // it on, and load it
-                const int sl = k & 1;
-                if (k >= 2 && !mbar_wait(bar(B_STE0 + sl), ((k >> 1) - 1) & 1)) { *fail = 1; break; }
-                int pr = n_pairs > 0 ? atomicAdd(p.pair_counter, 1) : n_pairs;
-                if (pr >= n_pairs) pr = -1;
-                ring[k & 7] = pr;
-                mbar_arrive(bar(B_PID0 + (k & 7)));
-                if (pr < 0) {
-                    // the end, for pair k + 1 too: each solver and publisher walks every
-                    // other pair, so half of them next ask for pair k + 1
-                    ring[(k + 1) & 7] = -1;
-                    mbar_arrive(bar(B_PID0 + ((k + 1) & 7)));
-                }
-                if (pr >= 0) {
-                    mbar_arrive_expect_tx(bar(B_STF0 + sl), 8 * 8192);
-                    ++loads;
-#pragma unroll
-                    for (int which = 0; which < 2; ++which) {
-                        int u = 2 * pr + which;
-                        if (u >= n_units) u = 2 * pr;  // a missing unit b repeats a
-                        u = unit_at(u);
-                        const int4 pl = p.plan[u / p.H];
-                        const int h = u % p.H;
-#pragma unroll
-                        for (int b = 0; b < 2; ++b) {
-                            const uint32_t dst = sbase + sl * STAGE + b * 32768 + which * 8192;
-                            tma_load_3d(dst, &map_k, bar(B_STF0 + sl), 64 * b, h, pl.y);
-                            tma_load_3d(dst + 16384, &map_q, bar(B_STF0 + sl), 64 * b, h, pl.y);
-                        }
-                    }
-                }
-                if (k >= 1) {  // Gram of pair j = k - 1 into TMEM slot j % 2 (free once read out)
-                    const int j = k - 1, sl = j & 1;
-                    if (!mbar_wait(bar(B_STF0 + sl), (j >> 1) & 1)) { *fail = 1; break; }
-                    ++landed;
-                    if (j >= 2 && !mbar_wait(bar(B_TME0 + sl), ((j >> 1) - 1) & 1)) { *fail = 1; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = sbase + sl * STAGE + (kk >> 2) * 32768 + (kk & 3) * 32;
-                        mma_bf16(tmem + 256 * sl, sw128_desc(off, 16, 1024), sw128_desc(off, 16, 1024),
-                                 idesc_bf16(128, 256, 0, 0), kk > 0);
-                    }
-                    mma_commit(bar(B_STE0 + sl));
-                    mma_commit(bar(B_TMF0 + sl));
-                }
-                if (pr < 0) break;
-            }
-            if (*fail) {  // issued MMAs and loads land before TMEM and shared memory go away
-                mma_commit(bar(B_DRAIN));
-                mbar_wait(bar(B_DRAIN), 0);
-                for (int j = landed; j < loads; ++j) mbar_wait(bar(B_STF0 + (j & 1)), (j >> 1) & 1);
-            }
-        }
-    } else if (warp < 4) {
-        // ============================================================ read-out
-        const int which = warp >> 1;          // unit a (0) or b (1) of each pair
-        const int t = 32 * (warp & 1) + lane; // token row = TMEM lane 64 which + t
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
-        // decay gates of this warp pair's unit of pair k, into registers (warp 2 which)
-        float ga0 = 0.f, ga1 = 0.f, gb0 = 0.f, gb1 = 0.f;
-        auto fetch_gates = [&](int pr) {
-            ga0 = ga1 = gb0 = gb1 = 0.f;
-            const int u = 2 * pr + which;
-            if (pr >= 0 && u < n_units) {
-                const int ug = unit_at(u);
-                const int4 pl = p.plan[ug / p.H];
-                const int h = ug % p.H, len = pl.z;
-                if (2 * lane < len) {
-                    const size_t off = (size_t)(pl.y + 2 * lane) * p.H + h;
-                    ga0 = p.log_alpha[off];
-                    gb0 = p.beta[off];
-                }
-                if (2 * lane + 1 < len) {
-                    const size_t off = (size_t)(pl.y + 2 * lane + 1) * p.H + h;
-                    ga1 = p.log_alpha[off];
-                    gb1 = p.beta[off];
-                }
-            }
-        };
-        int pr = pair_id(0);
-        if ((warp & 1) == 0) fetch_gates(pr);
-        for (int k = 0; pr >= 0; ++k) {
-            const int sl = k & 1;
-            const int lu = 2 * k + which, ls = lu % kSolvers;  // local unit and its solver slot
-            const bool exists = 2 * pr + which < n_units;
-            const int u = unit_at(2 * pr + which);
-            const int pr_next = pair_id(k + 1);  // handed on before the Gram of pair k
-            float *U = lslot(ls);
-            float *g = U + UNIT_FLOATS;
-            bool ok = true;
-            if (exists && lu >= kSolvers) ok = mbar_wait(bar(B_LE0 + ls), ((lu / kSolvers) - 1) & 1);
-            if (!ok) *fail = 1;
-            if ((warp & 1) == 0) {  // the unit's gates, by the shared scan; then the next pair's
-                const ChunkScan sc = chunk_scan(ga0, ga1, lane);
-                if (exists && ok) {
-                    g[G_G + 2 * lane] = sc.g0;
-                    g[G_G + 2 * lane + 1] = sc.g1;
-                    g[G_GAM + 2 * lane] = fast_exp(sc.g0);
-                    g[G_GAM + 2 * lane + 1] = fast_exp(sc.g1);
-                    g[G_GINV + 2 * lane] = fast_exp(-sc.g0);
-                    g[G_GINV + 2 * lane + 1] = fast_exp(-sc.g1);
-                    g[G_BETA + 2 * lane] = gb0;
-                    g[G_BETA + 2 * lane + 1] = gb1;
-                    g[G_KDEC + 2 * lane] = fast_exp(sc.g_last - sc.g0);
-                    g[G_KDEC + 2 * lane + 1] = fast_exp(sc.g_last - sc.g1);
-                }
-                fetch_gates(pr_next);
-            }
-            named_sync(1 + which, 64);  // the gates are visible to both warps of the unit
-            ok = mbar_wait(bar(B_TMF0 + sl), (k >> 1) & 1);
-            if (!ok) *fail = 1;
-            tc_fence_after();
-            if (exists && ok && !*fail) {
-                const bool ratio = g[G_G + C - 1] > kRatioSafeLogDecay;
-                const uint32_t col = 256 * sl + 64 * which;
-                // L_ti = beta_t Gamma_ti k_t.k_i (i < t), whole 16-wide block rows
-                {
-                    const float gt = ratio ? g[G_GAM + t] : g[G_G + t];
-                    const float bt = g[G_BETA + t];
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (hh > (warp & 1)) break;  // columns >= 32 lie above rows < 32
-                        float v[32], f[32];
-                        tmem_load32(lane_base + col + 32 * hh, v);
-                        const float4 *gv = reinterpret_cast<const float4 *>(g + (ratio ? G_GINV : G_G) + 32 * hh);
-#pragma unroll
-                        for (int jv = 0; jv < 8; ++jv) {
-                            const float4 x = gv[jv];
-                            f[4 * jv] = x.x; f[4 * jv + 1] = x.y; f[4 * jv + 2] = x.z; f[4 * jv + 3] = x.w;
-                        }
-#pragma unroll
-                        for (int ii = 0; ii < 32; ++ii) {
-                            const int i = 32 * hh + ii;
-                            const float dec = ratio ? gt * f[ii] : fast_exp(gt - f[ii]);
-                            v[ii] = (i < t) ? bt * dec * v[ii] : 0.f;
-                        }
-#pragma unroll
-                        for (int m = 0; m < 2; ++m) {
-                            const int ib = 2 * hh + m;
-                            if (ib <= (t >> 4)) {
-                                float *blockp = U + blk(t >> 4, ib);
-#pragma unroll
-                                for (int e4 = 0; e4 < 4; ++e4)
-                                    *reinterpret_cast<float4 *>(blockp + el(t & 15, 4 * e4)) =
-                                        make_float4(v[16 * m + 4 * e4], v[16 * m + 4 * e4 + 1],
-                                                    v[16 * m + 4 * e4 + 2], v[16 * m + 4 * e4 + 3]);
-                            }
-                        }
-                    }
-                }
-                // row i = t of A^T: key i against queries tq >= i, straight to the workspace
-                {
-                    const float gi = g[G_G + t];
-                    const float ginv_c = g[G_GINV + C - 1];
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.Tout + ((size_t)(2 * u + 1) * C + t) * C);
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        float v[32];
-                        if (hh < (warp & 1)) {  // rows i >= 32: queries tq < 32 are all masked
-#pragma unroll
-                            for (int ii = 0; ii < 32; ++ii) v[ii] = 0.f;
-                        } else {
-                            tmem_load32(lane_base + col + 128 + 32 * hh, v);
-#pragma unroll
-                            for (int ii = 0; ii < 32; ++ii) {
-                                const int tq = 32 * hh + ii;
-                                const float dec = ratio ? ginv_c : fast_exp(g[G_G + tq] - gi);
-                                v[ii] = (tq >= t) ? v[ii] * dec : 0.f;
-                            }
-                        }
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj)
-                            dst[4 * hh + jj] = make_uint4(pack_bf16x2(v[8 * jj], v[8 * jj + 1]),
-                                                          pack_bf16x2(v[8 * jj + 2], v[8 * jj + 3]),
-                                                          pack_bf16x2(v[8 * jj + 4], v[8 * jj + 5]),
-                                                          pack_bf16x2(v[8 * jj + 6], v[8 * jj + 7]));
-                    }
-                }
-                // the unit's decay factors for the chain kernel: g and gamma (warp 2 which),
-                // kdec and the form flag (warp 2 which + 1), two tokens per lane
-                float *go = p.Gout + (size_t)u * 256;
-                if ((warp & 1) == 0) {
-                    *reinterpret_cast<float2 *>(go + 2 * lane) = make_float2(g[G_G + 2 * lane], g[G_G + 2 * lane + 1]);
-                    *reinterpret_cast<float2 *>(go + 64 + 2 * lane) =
-                        make_float2(g[G_GAM + 2 * lane], g[G_GAM + 2 * lane + 1]);
-                } else {
-                    *reinterpret_cast<float2 *>(go + 128 + 2 * lane) =
-                        make_float2(g[G_KDEC + 2 * lane], g[G_KDEC + 2 * lane + 1]);
-                    *reinterpret_cast<float2 *>(go + 192 + 2 * lane) =
-                        make_float2(lane == 0 ? (ratio ? 1.f : 0.f) : 0.f, 0.f);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(bar(B_TME0 + sl));              // the TMEM slot is read
-            if (exists) mbar_arrive(bar(B_LF0 + ls));   // the solver slot is filled
-            pr = pr_next;
-        }
-    } else if (warp >= kSolverWarp0 && warp < kSolverWarp0 + kSolvers) {
-        // ============================================================ solvers
-        const int sv = warp - kSolverWarp0;
-        for (int lu = sv;; lu += kSolvers) {
-            const int which = lu & 1, pr = pair_id(lu >> 1);
-            if (pr < 0) break;
-            if (2 * pr + which >= n_units) continue;  // the missing half of an odd last pair
-            const int u = unit_at(2 * pr + which);
-            if (!mbar_wait(bar(B_LF0 + sv), (lu / kSolvers) & 1)) { *fail = 1; break; }
-            float *U = lslot(sv);
-            const float *g = U + UNIT_FLOATS;
-            warp_lower_inverse(U, lane);
-            // T' = diag(kdec) (I + L)^{-1} diag(beta) (ratio form; no kdec otherwise), bf16,
-            // staged over the slot and stored by TMA
-            const bool ratio = g[G_G + C - 1] > kRatioSafeLogDecay;
-            unsigned char *tile = reinterpret_cast<unsigned char *>(U);
-            warp_stage_tprime(U, g, ratio, tile, lane);
-            if (kFused) {
-                // T' to the workspace by plain stores (16-byte segments, row-major), then to
-                // the slot's publisher, whose gpu-scope release of the unit's flag covers
-                // these stores and the read-out's A^T and factors (stored before B_LF)
-                __syncwarp();
-                uint4 *dst = reinterpret_cast<uint4 *>(p.Tout + (size_t)2 * u * C * C);
-#pragma unroll 4
-                for (int sg = lane; sg < C * 8; sg += 32) {
-                    const int r = sg >> 3, c8 = sg & 7;
-                    dst[sg] = *reinterpret_cast<const uint4 *>(tile + r * 128 + (((c8 ^ r) & 7) << 4));
-                }
-                // the publisher has released this slot's previous unit
-                const bool ok = lu < kSolvers || mbar_wait(bar(B_PUBE0 + sv), ((lu / kSolvers) - 1) & 1);
-                if (!ok) *fail = 1;
-                mbar_arrive(bar(B_PUB0 + sv));
-                __syncwarp();
-                if (!ok) break;
-            } else {
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(&map_t, smem_u32(tile), 0, 0, 2 * u);
-                    bulk_commit_group();
-                    bulk_wait_group_read<0>();  // the slot may be refilled once the store has read it
-                }
-                __syncwarp();
-            }
-            if (lane == 0) mbar_arrive(bar(B_LE0 + sv));
-        }
-        if (lane == 0) bulk_wait_group_all();  // the T' stores have completed
-    } else if (kFused && warp >= kPublisherWarp0 && warp < kPublisherWarp0 + kSolvers) {
-        // ============================================================ publishers (fused)
-        const int sv = warp - kPublisherWarp0;
-        if (lane == 0) {
-            for (int lu = sv;; lu += kSolvers) {
-                const int which = lu & 1, pr = pair_id(lu >> 1);
-                if (pr < 0) break;
-                if (2 * pr + which >= n_units) continue;
-                if (!mbar_wait(bar(B_PUB0 + sv), (lu / kSolvers) & 1)) { *fail = 1; break; }
-                release_flag_gpu(p.flags + unit_at(2 * pr + which));
-                mbar_arrive(bar(B_PUBE0 + sv));
-            }
-        }
+    const GroupSolver<kFused> gsv{p, &map_q, &map_k, gbase,
+                                  reinterpret_cast<float *>(gs + G_BLK), reinterpret_cast<float *>(gs + G_GATES),
+                                  next, next + 1, grp, lane, u0, n_units};
+    switch (w) {
+        case 0: gsv.template run<0>(); break;
+        case 1: gsv.template run<1>(); break;
+        case 2: gsv.template run<2>(); break;
+        default: gsv.template run<3>(); break;
     }
-
-    __syncthreads();
-    if (*fail && tid == 0) atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
-    if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
 }  // namespace solve

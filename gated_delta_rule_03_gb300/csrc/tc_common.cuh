@@ -85,7 +85,7 @@ bool make_map_units(CUtensorMap *map, const void *base, int64_t units);
 // workspace, on `stream`, with at most max_ctas CTAs (all SMs when max_ctas <= 0);
 // `programmatic` launches it as a programmatic dependent of the kernel ahead of it.
 int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &map_q,
-                    const CUtensorMap &map_k, const CUtensorMap &map_t, int phase, int max_ctas,
+                    const CUtensorMap &map_k, int phase, int max_ctas,
                     cudaStream_t stream, bool programmatic);
 
 }  // namespace tc
