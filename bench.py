@@ -74,7 +74,7 @@ def decode_bytes(N, H, dk, dv, esz=2):
 
 def recorded_traffic(kernel, workload):
     """DRAM bytes per launch from an ncu capture summarised in profiles/traffic.txt. A
-    record holds while the kernel's source file (and the shared internal header) is
+    record holds while the kernel's source files (and the shared internal header) are
     unchanged since the capture; otherwise the traffic is unknown (None)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
@@ -89,13 +89,14 @@ def recorded_traffic(kernel, workload):
     return None
 
 
-def source_sha(name):
-    """Hash of one CUDA source file plus the internal header every kernel includes."""
+def source_sha(names):
+    """Hash of the CUDA source files a kernel is built from (comma-separated names) plus
+    the internal header every kernel includes."""
     csrc = os.path.join(ROOT, "gated_delta_rule_03_gb300", "csrc")
     h = hashlib.sha256()
-    for fn in (name, "internal.h"):
+    for fn in [n for n in names.split(",") if n] + ["internal.h"]:
         path = os.path.join(csrc, fn)
-        if not fn or not os.path.exists(path):
+        if not os.path.exists(path):
             return None
         with open(path, "rb") as f:
             h.update(fn.encode() + f.read())
@@ -301,7 +302,7 @@ def run_gdr(args):
     value = world * tokens * args.steps / (total_ms / 1e3)
     kernel_launches = ops.chunk_fwd_kernel_launches(inp.num_seqs, inp.total_tokens, inp.H, inp.dk,
                                                     inp.dv, q.dtype, varlen=cu is not None)
-    main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype)
+    main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype, launches=kernel_launches)
     bytes_call = prefill_bytes(inp)
     achieved = bytes_call / (call_ms / 1e3) / 1e9
     traffic = recorded_traffic(main_kernel, PREFILL_WORKLOAD)

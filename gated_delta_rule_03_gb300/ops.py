@@ -200,9 +200,14 @@ def chunk_fwd_kernel_launches(num_seqs, total_tokens, H, dk, dv, dtype, varlen=F
     return st
 
 
-def chunk_fwd_main_kernel(dk, dv, dtype):
-    """Name of the kernel that dominates a gdr_chunk_fwd call for these sizes."""
-    return _PATHS[chunk_fwd_path(dk, dv, dtype)]["main_kernel"]
+def chunk_fwd_main_kernel(dk, dv, dtype, launches=None):
+    """Name of the kernel that dominates a gdr_chunk_fwd call for these sizes. On the
+    tensor-core path a call of two launches (planning, then one cooperative kernel) runs
+    the fused schedule, whose one kernel holds both the solve and the chain."""
+    path = chunk_fwd_path(dk, dv, dtype)
+    if path == 1 and launches == 2:
+        return "tc_fused_kernel"
+    return _PATHS[path]["main_kernel"]
 
 
 def chunk_fwd_compute_dtype(dk, dv, dtype):
