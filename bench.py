@@ -302,7 +302,9 @@ def run_gdr(args):
     value = world * tokens * args.steps / (total_ms / 1e3)
     kernel_launches = ops.chunk_fwd_kernel_launches(inp.num_seqs, inp.total_tokens, inp.H, inp.dk,
                                                     inp.dv, q.dtype, varlen=cu is not None)
-    main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype, launches=kernel_launches)
+    schedule = ops.chunk_fwd_schedule(inp.num_seqs, inp.total_tokens, inp.H, inp.dk, inp.dv,
+                                      q.dtype, varlen=cu is not None)
+    main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype, schedule=schedule)
     bytes_call = prefill_bytes(inp)
     achieved = bytes_call / (call_ms / 1e3) / 1e9
     traffic = recorded_traffic(main_kernel, PREFILL_WORKLOAD)

@@ -178,6 +178,17 @@ int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H,
     return n < 0 ? GDR_ERR_CUDA : n;
 }
 
+int gdr_chunk_fwd_schedule(int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v,
+                           int chunk, int dtype, int varlen) {
+    const int st = check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype);
+    if (st != GDR_OK) return st;
+    if (!use_tensor_path(d_k, d_v, dtype) || total_tokens == 0) return 1;
+    // the fused schedule is two launches (plan, cooperative kernel); P phases are 1 + 2P
+    const int n = tc_schedule_launches(num_seqs, total_tokens, H, d_v, varlen != 0);
+    if (n < 0) return GDR_ERR_CUDA;
+    return n == 2 ? 0 : (n - 1) / 2;
+}
+
 int gdr_read_device_status(const void *workspace, int *status, gdr_stream_t stream) {
     if (!workspace || !status) return GDR_ERR_INVALID_ARG;
     int32_t word = 0;

@@ -53,6 +53,8 @@ def _load():
     lib.gdr_chunk_fwd_kernel_launches.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int,
                                                   c_int]
     lib.gdr_chunk_fwd_kernel_launches.restype = c_int
+    lib.gdr_chunk_fwd_schedule.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int, c_int]
+    lib.gdr_chunk_fwd_schedule.restype = c_int
     lib.gdr_read_device_status.argtypes = [vp, ctypes.POINTER(c_int), vp]
     lib.gdr_read_device_status.restype = c_int
     _lib = lib
@@ -200,12 +202,21 @@ def chunk_fwd_kernel_launches(num_seqs, total_tokens, H, dk, dv, dtype, varlen=F
     return st
 
 
-def chunk_fwd_main_kernel(dk, dv, dtype, launches=None):
-    """Name of the kernel that dominates a gdr_chunk_fwd call for these sizes. On the
-    tensor-core path a call of two launches (planning, then one cooperative kernel) runs
-    the fused schedule, whose one kernel holds both the solve and the chain."""
+def chunk_fwd_schedule(num_seqs, total_tokens, H, dk, dv, dtype, varlen=False):
+    """Schedule of a gdr_chunk_fwd call with these sizes on the current device: 0 for the
+    fused tensor-core schedule, else the number of phases."""
+    st = _load().gdr_chunk_fwd_schedule(int(num_seqs), int(total_tokens), int(H), int(dk),
+                                        int(dv), 64, _DTYPES[dtype], int(bool(varlen)))
+    if st < 0:
+        raise GdrError(st, "gdr_chunk_fwd_schedule")
+    return st
+
+
+def chunk_fwd_main_kernel(dk, dv, dtype, schedule=None):
+    """Name of the kernel that dominates a gdr_chunk_fwd call for these sizes. The fused
+    schedule (0) of the tensor-core path runs the solve and the chains in one kernel."""
     path = chunk_fwd_path(dk, dv, dtype)
-    if path == 1 and launches == 2:
+    if path == 1 and schedule == 0:
         return "tc_fused_kernel"
     return _PATHS[path]["main_kernel"]
 

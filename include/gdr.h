@@ -217,6 +217,18 @@ int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H,
                                   int d_v, int chunk, int dtype, int varlen);
 
 /*
+ * Schedule of an uncaptured gdr_chunk_fwd call with these sizes on the current
+ * device, for diagnostics and benchmarks: 0 for the fused schedule of the
+ * tensor-core path (the planning kernel, then one cooperative kernel that runs
+ * the chains beside the solve), else the number of phases (1 .. 8) of the
+ * phased schedule; the exact path is one phase. varlen as above. Returns a
+ * negative status for unsupported or invalid sizes, or GDR_ERR_CUDA if the
+ * device cannot be read.
+ */
+int gdr_chunk_fwd_schedule(int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v,
+                           int chunk, int dtype, int varlen);
+
+/*
  * Reads the device status word that the last gdr_chunk_fwd call on this
  * workspace left (GDR_OK, GDR_ERR_BAD_SEQLENS or GDR_ERR_DEVICE_TIMEOUT) into
  * *status (a HOST pointer). It synchronises `stream` first, so it must not be

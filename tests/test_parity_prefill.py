@@ -199,6 +199,7 @@ def test_fused_schedule_matches_phased(S, T, H, dv, monkeypatch):
                                 s0_std=0.5, gate="slow")
     assert inp.cu_seqlens is None
     monkeypatch.delenv("GDR_PREFILL_PHASES", raising=False)
+    assert ops.chunk_fwd_schedule(S, S * T, H, 128, dv, torch.bfloat16) == 0
     assert ops.chunk_fwd_kernel_launches(S, S * T, H, 128, dv, torch.bfloat16) == 2
     o_f, S_f = gpu_prefill(inp)
     monkeypatch.setenv("GDR_PREFILL_PHASES", "1")
