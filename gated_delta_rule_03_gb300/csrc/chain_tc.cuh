@@ -144,6 +144,7 @@ struct TcParams {
     float *S_out;              // state after this phase's chunks (may alias S_in)
     int32_t *ctl;
     const int32_t *flags;      // fused launch: per solve unit, set once the unit is solved
+    int additive;              // the additive rule: W' = 0 (the state does not enter U')
 };
 
 // A chain CTA of a fused launch waits here until the solve has published unit u (its
@@ -437,10 +438,11 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                     block = qs + (dk >> 6) * 16384 + 8192;
                     c8 = (dk & 63) >> 3;
                 };
+                const float wsign = p.additive ? 0.f : -1.f;  // W' (finite) times 0 for the additive rule
                 tmem_load_16x256b_x8(lane_base + TM_W, r);
-                transpose_store16(r, -1.f, nullptr, lane, 0, row_block);
+                transpose_store16(r, wsign, nullptr, lane, 0, row_block);
                 tmem_load_16x256b_x8(lane_base + (16u << 16) + TM_W, r);
-                transpose_store16(r, -1.f, nullptr, lane, 16, row_block);
+                transpose_store16(r, wsign, nullptr, lane, 16, row_block);
             }
             // Q has landed ([QS | WS] follows B_WQ, and the exponential form scales it here)
             if (!check(mbar_wait(bar(B_QF0 + (c & 1)), u & 1))) break;

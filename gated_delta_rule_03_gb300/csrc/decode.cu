@@ -7,7 +7,8 @@
 //   S'  = alpha S + k u^T                   (decay and delta write)
 //   o   = S'^T q = alpha b + (k.q) u        (read-out after the update)
 // which is Eqs. (1)-(4) of "Linear attention" (arsalanzafar.ai), "How it works",
-// for a single token. The kernel is HBM-bound: a generation step reads about
+// for a single token. The additive rule (S' = alpha S + beta k v^T) is the same step
+// with u = beta v. The kernel is HBM-bound: a generation step reads about
 // d_k d_v numbers ("Attention as Matrix Algebra", section 9).
 //
 // Layout: one CTA per (n, h); d_k*d_v/64 threads, each holding 16 rows x 4
@@ -41,7 +42,10 @@ template <typename Tin, int DK, int DV>
 __global__ void __launch_bounds__(DK * DV / 64)
 decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const Tin *__restrict__ v, const float *__restrict__ log_alpha,
-                   const float *__restrict__ beta, float *__restrict__ S, Tin *__restrict__ o) {
+                   const float *__restrict__ beta, float *__restrict__ S, Tin *__restrict__ o,
+                   float read) {
+    // read = 1: the delta rule's correction u = beta (v - alpha S^T k); read = 0: the
+    // additive write u = beta v
     constexpr int NT = DK * DV / 64;  // threads
     constexpr int TPR = DV / 4;       // threads per state row (one float4 each)
     constexpr int RG = NT / TPR;      // row groups (= DK / 16)
@@ -69,6 +73,7 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     for (int j = tid; j < DV; j += NT) vs[j] = to_f32(v[nh * DV + j]);
     const float alpha = expf(log_alpha[nh]);
     const float b = beta[nh];
+    const float ra = read * alpha;
     __syncthreads();
 
     if (tid < 32) {
@@ -102,10 +107,10 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const float kq = s_kq;
     const float4 vv = *reinterpret_cast<const float4 *>(&vs[4 * cg]);
     float4 u;
-    u.x = b * (vv.x - alpha * a.x);
-    u.y = b * (vv.y - alpha * a.y);
-    u.z = b * (vv.z - alpha * a.z);
-    u.w = b * (vv.w - alpha * a.w);
+    u.x = b * (vv.x - ra * a.x);
+    u.y = b * (vv.y - ra * a.y);
+    u.z = b * (vv.z - ra * a.z);
+    u.w = b * (vv.w - ra * a.w);
     if (rg == 0) {
         float4 out;
         out.x = fmaf(alpha, bq.x, kq * u.x);
@@ -128,20 +133,20 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 
 template <typename Tin, int DK, int DV>
 static int launch_decode_t(const void *q, const void *k, const void *v, const float *la,
-                           const float *beta, float *S, void *o, int64_t NH,
+                           const float *beta, float *S, void *o, int64_t NH, float read,
                            cudaStream_t stream) {
     decode_step_kernel<Tin, DK, DV><<<(unsigned)NH, DK * DV / 64, 0, stream>>>(
-        (const Tin *)q, (const Tin *)k, (const Tin *)v, la, beta, S, (Tin *)o);
+        (const Tin *)q, (const Tin *)k, (const Tin *)v, la, beta, S, (Tin *)o, read);
     return cuda_status(cudaGetLastError());
 }
 
 template <typename Tin>
 static int launch_decode_dtype(const void *q, const void *k, const void *v, const float *la,
                                const float *beta, float *S, void *o, int64_t NH, int dk, int dv,
-                               cudaStream_t stream) {
+                               float read, cudaStream_t stream) {
 #define GDR_DECODE_CASE(DK_, DV_)                                                         \
     if (dk == DK_ && dv == DV_)                                                           \
-        return launch_decode_t<Tin, DK_, DV_>(q, k, v, la, beta, S, o, NH, stream);
+        return launch_decode_t<Tin, DK_, DV_>(q, k, v, la, beta, S, o, NH, read, stream);
     GDR_DECODE_CASE(64, 64)
     GDR_DECODE_CASE(64, 128)
     GDR_DECODE_CASE(64, 256)
@@ -154,12 +159,13 @@ static int launch_decode_dtype(const void *q, const void *k, const void *v, cons
 
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
-                  int dtype, cudaStream_t stream) {
+                  int dtype, int rule, cudaStream_t stream) {
     const int64_t NH = N * H;
+    const float read = rule == GDR_RULE_ADDITIVE ? 0.f : 1.f;
     if (dtype == GDR_BF16)
         return launch_decode_dtype<__nv_bfloat16>(q, k, v, log_alpha, beta, S, o, NH, dk, dv,
-                                                  stream);
-    return launch_decode_dtype<float>(q, k, v, log_alpha, beta, S, o, NH, dk, dv, stream);
+                                                  read, stream);
+    return launch_decode_dtype<float>(q, k, v, log_alpha, beta, S, o, NH, dk, dv, read, stream);
 }
 
 }  // namespace gdr

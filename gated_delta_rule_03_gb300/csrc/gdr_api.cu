@@ -69,6 +69,17 @@ static int check_prefill_sizes(int64_t num_seqs, int64_t total_tokens, int H, in
     return GDR_OK;
 }
 
+// The rule of an options block (defaults for a null pointer); reserved words must be zero.
+static int check_options(const gdr_options *opt, int *rule) {
+    *rule = GDR_RULE_DELTA;
+    if (!opt) return GDR_OK;
+    for (int r : opt->reserved)
+        if (r != 0) return GDR_ERR_INVALID_ARG;
+    if (opt->rule != GDR_RULE_DELTA && opt->rule != GDR_RULE_ADDITIVE) return GDR_ERR_UNSUPPORTED;
+    *rule = opt->rule;
+    return GDR_OK;
+}
+
 static bool overlaps(const void *a, size_t an, const void *b, size_t bn) {
     const char *pa = (const char *)a, *pb = (const char *)b;
     return pa < pb + bn && pb < pa + an;
@@ -100,12 +111,15 @@ size_t gdr_chunk_fwd_workspace_size(int64_t num_seqs, int64_t total_tokens, int 
     return ws_layout(num_seqs, total_tokens, H, d_k, d_v, dtype).total;
 }
 
-int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
-                  const float *beta, const float *S0, const int32_t *cu_seqlens,
-                  int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v, int chunk,
-                  int dtype, void *o, float *S_final, void *workspace, size_t workspace_bytes,
-                  gdr_stream_t stream) {
-    int st = check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype);
+int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                     const float *beta, const float *S0, const int32_t *cu_seqlens,
+                     int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v, int chunk,
+                     int dtype, void *o, float *S_final, void *workspace, size_t workspace_bytes,
+                     const gdr_options *options, gdr_stream_t stream) {
+    int rule = GDR_RULE_DELTA;
+    int st = check_options(options, &rule);
+    if (st != GDR_OK) return st;
+    st = check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype);
     if (st != GDR_OK) return st;
     if (!cu_seqlens && total_tokens % num_seqs != 0) return GDR_ERR_INVALID_ARG;
     if (!S_final || !workspace) return workspace ? GDR_ERR_INVALID_ARG : GDR_ERR_WORKSPACE;
@@ -133,6 +147,7 @@ int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
     a.cu_seqlens = cu_seqlens;
     a.num_seqs = num_seqs; a.total_tokens = total_tokens;
     a.H = H; a.dk = d_k; a.dv = d_v; a.chunk = chunk; a.dtype = dtype;
+    a.rule = rule;
     a.o = o; a.S_final = S_final;
     a.ws = (char *)workspace;
     a.stream = (cudaStream_t)stream;
@@ -142,9 +157,22 @@ int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
     return L.tensor_path ? launch_prefill_tc(a, L, phases) : launch_prefill_exact(a, L);
 }
 
-int gdr_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
-                    const float *beta, float *S, void *o, int64_t N, int H, int d_k, int d_v,
-                    int dtype, gdr_stream_t stream) {
+int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  const float *beta, const float *S0, const int32_t *cu_seqlens,
+                  int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v, int chunk,
+                  int dtype, void *o, float *S_final, void *workspace, size_t workspace_bytes,
+                  gdr_stream_t stream) {
+    return gdr_chunk_fwd_ex(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H,
+                            d_k, d_v, chunk, dtype, o, S_final, workspace, workspace_bytes,
+                            nullptr, stream);
+}
+
+int gdr_decode_step_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                       const float *beta, float *S, void *o, int64_t N, int H, int d_k, int d_v,
+                       int dtype, const gdr_options *options, gdr_stream_t stream) {
+    int rule = GDR_RULE_DELTA;
+    const int st = check_options(options, &rule);
+    if (st != GDR_OK) return st;
     if (N < 0 || H < 1 || N > INT32_MAX || (int64_t)N * H > INT32_MAX) return GDR_ERR_INVALID_ARG;
     if (dtype != GDR_F32 && dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
     if ((d_k != 64 && d_k != 128) || (d_v != 64 && d_v != 128 && d_v != 256))
@@ -158,8 +186,14 @@ int gdr_decode_step(const void *q, const void *k, const void *v, const float *lo
     const size_t esz = dtype == GDR_F32 ? 4 : 2;
     if (overlaps(o, (size_t)N * H * d_v * esz, S, (size_t)N * H * d_k * d_v * sizeof(float)))
         return GDR_ERR_INVALID_ARG;
-    return launch_decode(q, k, v, log_alpha, beta, S, o, N, H, d_k, d_v, dtype,
+    return launch_decode(q, k, v, log_alpha, beta, S, o, N, H, d_k, d_v, dtype, rule,
                          (cudaStream_t)stream);
+}
+
+int gdr_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
+                    const float *beta, float *S, void *o, int64_t N, int H, int d_k, int d_v,
+                    int dtype, gdr_stream_t stream) {
+    return gdr_decode_step_ex(q, k, v, log_alpha, beta, S, o, N, H, d_k, d_v, dtype, nullptr, stream);
 }
 
 int gdr_chunk_fwd_path(int d_k, int d_v, int dtype) {

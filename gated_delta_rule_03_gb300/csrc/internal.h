@@ -21,6 +21,7 @@ struct PrefillArgs {
     const int32_t *cu_seqlens;
     int64_t num_seqs, total_tokens;
     int H, dk, dv, chunk, dtype;
+    int rule;  // GDR_RULE_DELTA or GDR_RULE_ADDITIVE
     void *o;
     float *S_final;
     char *ws;
@@ -68,7 +69,7 @@ int tc_schedule(const PrefillArgs &a);
 int tc_schedule_launches(int64_t num_seqs, int64_t total_tokens, int H, int dv, bool varlen);
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
-                  int dtype, cudaStream_t stream);
+                  int dtype, int rule, cudaStream_t stream);
 
 // Type helpers for kernels.
 template <typename T> __device__ __forceinline__ float to_f32(T x);

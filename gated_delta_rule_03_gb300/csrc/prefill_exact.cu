@@ -205,8 +205,9 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
                   const float *__restrict__ log_alpha, const float *__restrict__ beta, int H,
                   int dv, const int4 *__restrict__ plan, const int32_t *__restrict__ ctl,
                   float *__restrict__ Wws, float *__restrict__ Uws, float *__restrict__ Aws,
-                  float *__restrict__ gws) {
-    // gws receives, per chunk, gamma[C] followed by kdec[C].
+                  float *__restrict__ gws, int additive) {
+    // gws receives, per chunk, gamma[C] followed by kdec[C]. With the additive rule the
+    // write does not read the state: L = 0 (so T = diag(beta)) and W = 0.
     using SM = PrepSmem<DK>;
     constexpr int KP = SM::KP, CP = SM::CP, C = kChunk;
     const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -270,7 +271,7 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
             }
             dec = Gm[t * CP + i];
         }
-        Lm[t * CP + i] = (i < t) ? bs[t] * dec * kk : 0.f;
+        Lm[t * CP + i] = (i < t && !additive) ? bs[t] * dec * kk : 0.f;
         Am[t * CP + i] = dec * qk;
     }
     __syncthreads();
@@ -298,7 +299,7 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
         const int t = idx / DK, d = idx % DK;
         float s = 0.f;
         for (int i = 0; i <= t; ++i) s = fmaf(Tm[t * CP + i] * gam[i], ks[i * KP + d], s);
-        Wout[idx] = s;
+        Wout[idx] = additive ? 0.f : s;
     }
     float *Uout = Uws + cb * C * dv;
     for (int idx = tid; idx < C * dv; idx += blockDim.x) {
@@ -483,7 +484,7 @@ static int launch_exact_t(const PrefillArgs &a, const WsLayout &L) {
         dim3 grid((unsigned)L.max_chunks, (unsigned)a.H);
         exact_prep_kernel<Tin, DK><<<grid, 256, PrepSmem<DK>::bytes, a.stream>>>(
             (const Tin *)a.q, (const Tin *)a.k, (const Tin *)a.v, a.log_alpha, a.beta, a.H, a.dv,
-            (const int4 *)(a.ws + L.plan), ctl, W, U, A, g);
+            (const int4 *)(a.ws + L.plan), ctl, W, U, A, g, a.rule == GDR_RULE_ADDITIVE ? 1 : 0);
         e = cudaGetLastError();
         if (e != cudaSuccess) return GDR_ERR_CUDA;
     }

@@ -262,6 +262,7 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     p.S_out = a.S_final;
     p.ctl = (int32_t *)(a.ws + L.ctl);
     p.flags = flags;
+    p.additive = a.rule == GDR_RULE_ADDITIVE;
     solve::SolveParams sp = {};
     sp.log_alpha = a.log_alpha;
     sp.beta = a.beta;
@@ -275,6 +276,7 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     sp.seq_chunks = (int)((a.total_tokens / a.num_seqs + kChunk - 1) / kChunk);
     sp.flags = flags;
     sp.unit_counter = counters;
+    sp.additive = a.rule == GDR_RULE_ADDITIVE;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
@@ -345,6 +347,7 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
     p.phases = phases;
     p.o = (__nv_bfloat16 *)a.o;
     p.ctl = (int32_t *)(a.ws + L.ctl);
+    p.additive = a.rule == GDR_RULE_ADDITIVE;
     float *S_mid = reinterpret_cast<float *>(a.ws + L.S);
     for (int f = 0; f < phases; ++f) {
         if (f > 0 && cudaStreamWaitEvent(a.stream, sd->ev[f], 0) != cudaSuccess) return GDR_ERR_CUDA;

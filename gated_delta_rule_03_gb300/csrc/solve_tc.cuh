@@ -178,6 +178,7 @@ struct SolveParams {
     int seqs, seq_chunks;
     int32_t *flags;
     int32_t *unit_counter;  // units are claimed from it at run time (zeroed by the plan)
+    int additive;           // the additive rule: L = 0, so T = diag(beta)
     __nv_bfloat16 *Tout;  // [chunks * H][2][64][64]: T' then A^T per unit
     float *Gout;          // [chunks * H][256]: g, gamma, kdec, form flag per unit
 };
@@ -311,7 +312,7 @@ struct GroupSolver {
                 const int t = 16 * W + gq + 8 * hh;
                 rg[hh] = ratio ? gt[GG_GAM + t] : gt[GG_G + t];
                 rgi[hh] = gt[GG_G + t];
-                rb[hh] = gt[GG_BETA + t];
+                rb[hh] = p.additive ? 0.f : gt[GG_BETA + t];  // L = 0 for the additive rule
                 rkd[hh] = ratio ? gt[GG_KDEC + t] : 1.f;
             }
 #pragma unroll

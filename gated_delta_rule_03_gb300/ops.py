@@ -15,6 +15,19 @@ _lib = None
 
 GDR_F32, GDR_BF16 = 0, 1
 _DTYPES = {torch.float32: GDR_F32, torch.bfloat16: GDR_BF16}
+# the recurrence's write rule (gdr_options.rule)
+RULES = {"delta": 0, "additive": 1}
+
+
+class GdrOptions(ctypes.Structure):
+    """struct gdr_options of gdr.h."""
+    _fields_ = [("rule", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+
+
+def _options(rule):
+    if rule not in RULES:
+        raise ValueError(f"unknown rule {rule!r}; expected one of {sorted(RULES)}")
+    return ctypes.byref(GdrOptions(RULES[rule]))
 
 
 class GdrError(RuntimeError):
@@ -45,9 +58,15 @@ def _load():
     lib.gdr_chunk_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, i64, i64, c_int, c_int, c_int,
                                   c_int, c_int, vp, fp, vp, ctypes.c_size_t, vp]
     lib.gdr_chunk_fwd.restype = c_int
+    lib.gdr_chunk_fwd_ex.argtypes = [vp, vp, vp, fp, fp, fp, vp, i64, i64, c_int, c_int, c_int,
+                                     c_int, c_int, vp, fp, vp, ctypes.c_size_t, vp, vp]
+    lib.gdr_chunk_fwd_ex.restype = c_int
     lib.gdr_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i64, c_int, c_int, c_int, c_int,
                                     vp]
     lib.gdr_decode_step.restype = c_int
+    lib.gdr_decode_step_ex.argtypes = [vp, vp, vp, fp, fp, fp, vp, i64, c_int, c_int, c_int, c_int,
+                                       vp, vp]
+    lib.gdr_decode_step_ex.restype = c_int
     lib.gdr_chunk_fwd_path.argtypes = [c_int, c_int, c_int]
     lib.gdr_chunk_fwd_path.restype = c_int
     lib.gdr_chunk_fwd_kernel_launches.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int,
@@ -100,7 +119,7 @@ def chunk_fwd_workspace_size(num_seqs, total_tokens, H, dk, dv, chunk=64, dtype=
 
 
 def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None, chunk=64,
-              o=None, S_final=None, workspace=None, stream=None):
+              o=None, S_final=None, workspace=None, stream=None, rule="delta"):
     """Chunked prefill (gdr_chunk_fwd).
 
     q, k [T, H, dk]; v [T, H, dv] (fp32 or bf16); log_alpha, beta [T, H] fp32;
@@ -136,12 +155,12 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", device=dev)
-    st = lib.gdr_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
-                           _ptr(cu_seqlens), n, T, H, dk, dv, int(chunk), _DTYPES[dt], _ptr(o),
-                           _ptr(S_final), _ptr(workspace),
-                           workspace.numel() * workspace.element_size(),
-                           _stream_handle(stream, dev))
-    _check(st, "gdr_chunk_fwd")
+    st = lib.gdr_chunk_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                              _ptr(cu_seqlens), n, T, H, dk, dv, int(chunk), _DTYPES[dt], _ptr(o),
+                              _ptr(S_final), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _options(rule),
+                              _stream_handle(stream, dev))
+    _check(st, "gdr_chunk_fwd_ex")
     return o, S_final
 
 
@@ -154,10 +173,10 @@ def read_device_status(workspace, stream=None):
     return out.value
 
 
-def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None):
-    """One decode step (gdr_decode_step): q, k [N, H, dk]; v [N, H, dv];
-    log_alpha, beta [N, H] fp32; S [N, H, dk, dv] fp32 updated in place.
-    Returns o [N, H, dv]."""
+def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None, rule="delta"):
+    """One decode step (gdr_decode_step_ex): q, k [N, H, dk]; v [N, H, dv];
+    log_alpha, beta [N, H] fp32; S [N, H, dk, dv] fp32 updated in place; rule "delta"
+    (the gated delta rule) or "additive" (S <- alpha S + beta k v^T). Returns o [N, H, dv]."""
     lib = _load()
     _need(q, "q")
     dev, dt = q.device, q.dtype
@@ -171,9 +190,10 @@ def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None):
     if o is None:
         o = torch.empty((N, H, dv), dtype=dt, device=dev)
     _need(o, "o", dt, dev)
-    st = lib.gdr_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S),
-                             _ptr(o), N, H, dk, dv, _DTYPES[dt], _stream_handle(stream, dev))
-    _check(st, "gdr_decode_step")
+    st = lib.gdr_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S),
+                                _ptr(o), N, H, dk, dv, _DTYPES[dt], _options(rule),
+                                _stream_handle(stream, dev))
+    _check(st, "gdr_decode_step_ex")
     return o
 
 

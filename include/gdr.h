@@ -164,6 +164,57 @@ int gdr_decode_step(const void *q, const void *k, const void *v, const float *lo
                     int dtype, gdr_stream_t stream);
 
 /*
+ * Variants of the recurrence, chosen through gdr_options by the _ex entry
+ * points below.
+ *
+ *   GDR_RULE_DELTA      the gated delta rule above (the default):
+ *                         S_t = alpha_t S_{t-1} + beta_t k_t (v_t - alpha_t S_{t-1}^T k_t)^T.
+ *                       With log_alpha = 0 it is the ungated delta rule.
+ *   GDR_RULE_ADDITIVE   the decayed additive write (gated linear attention with a write
+ *                       strength):  S_t = alpha_t S_{t-1} + beta_t k_t v_t^T.
+ *                       This is the decay-gate form of "From KV Cache to a State
+ *                       Matrix" (section "Why DeltaNet may forget too slowly") together
+ *                       with the gradient step of size beta on the dot-product loss
+ *                       ("From attention weights to a state matrix", "Associating keys
+ *                       and values"). The chunk form then needs no triangular solve:
+ *                       the transform T is diag(beta) and the state does not enter the
+ *                       pseudo-values. With log_alpha = 0 and beta = 1 it is plain
+ *                       linear attention, S_t = S_{t-1} + k_t v_t^T.
+ * In both, o_t = S_t^T q_t, read after the update.
+ */
+enum { GDR_RULE_DELTA = 0, GDR_RULE_ADDITIVE = 1 };
+
+/*
+ * Options of the _ex entry points. A null pointer means all defaults; the
+ * reserved words must be zero (else GDR_ERR_INVALID_ARG).
+ *   rule   GDR_RULE_DELTA or GDR_RULE_ADDITIVE (else GDR_ERR_UNSUPPORTED)
+ */
+typedef struct gdr_options {
+    int rule;
+    int reserved[7];
+} gdr_options;
+
+/*
+ * gdr_chunk_fwd with options: the same arguments, layouts, ownership and
+ * errors, for the rule in *options. gdr_chunk_fwd is this call with a null
+ * options pointer.
+ */
+int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                     const float *beta, const float *S0, const int32_t *cu_seqlens,
+                     int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v, int chunk,
+                     int dtype, void *o, float *S_final, void *workspace, size_t workspace_bytes,
+                     const gdr_options *options, gdr_stream_t stream);
+
+/*
+ * gdr_decode_step with options, as gdr_chunk_fwd_ex. For GDR_RULE_ADDITIVE
+ * the step is S <- alpha S + beta k v^T, o = S_new^T q (one read and one
+ * write of S, as for the delta rule).
+ */
+int gdr_decode_step_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                       const float *beta, float *S, void *o, int64_t N, int H, int d_k, int d_v,
+                       int dtype, const gdr_options *options, gdr_stream_t stream);
+
+/*
  * gdr_chunk_fwd for callers that cannot allocate device memory.
  *
  * (The pages have no counterpart: this is a deployment convenience, not part

@@ -108,3 +108,33 @@ def test_invalid_arguments_rejected_on_the_host(lib):
     assert dcall(S=_fake(A + 4)) == -3
     assert dcall(o=p[5]) == -1        # o overlapping S
     assert dcall(N=0) == 0            # nothing to do, nothing enqueued
+
+
+def test_options_validated_on_the_host(lib):
+    # gdr_options: an unknown rule is unsupported, a nonzero reserved word is invalid; both
+    # are rejected before any other check, so fake pointers are never touched
+    from gated_delta_rule_03_gb300.ops import GdrOptions
+    A = 0x10000
+    p = [_fake(A + i * 0x1000000) for i in range(12)]
+    ws_bytes = lib.gdr_chunk_fwd_workspace_size(1, 128, 2, 64, 64, 64, 0)
+
+    def call(opt):
+        return lib.gdr_chunk_fwd_ex(p[0], p[1], p[2], p[3], p[4], None, None, 1, 128, 2, 64, 64,
+                                    64, 0, p[5], p[6], p[7], ws_bytes, opt, None)
+
+    def dcall(opt):
+        return lib.gdr_decode_step_ex(p[0], p[1], p[2], p[3], p[4], p[5], p[6], 4, 2, 128, 128,
+                                      1, opt, None)
+
+    bad_rule = GdrOptions(2)
+    reserved = GdrOptions(1)
+    reserved.reserved[3] = 1
+    for f in (call, dcall):
+        assert f(ctypes.byref(bad_rule)) == -2
+        assert f(ctypes.byref(reserved)) == -1
+    # a valid options block gets as far as the argument checks of the plain entry points
+    ok = GdrOptions(1)
+    assert lib.gdr_chunk_fwd_ex(None, p[1], p[2], p[3], p[4], None, None, 1, 128, 2, 64, 64, 64,
+                                0, p[5], p[6], p[7], ws_bytes, ctypes.byref(ok), None) == -1
+    assert lib.gdr_decode_step_ex(p[0], p[1], p[2], p[3], p[4], p[5], p[6], 0, 2, 128, 128, 1,
+                                  ctypes.byref(ok), None) == 0
