@@ -145,6 +145,10 @@ struct TcParams {
     int32_t *ctl;
     const int32_t *flags;      // fused launch: per solve unit, set once the unit is solved
     int additive;              // the additive rule: W' = 0 (the state does not enter U')
+    // the layer's output step on o (null out_gate: none; only when d_v = NV, one slice)
+    const __nv_bfloat16 *out_gate;
+    const float *out_norm_weight;
+    float out_norm_eps;
 };
 
 // A chain CTA of a fused launch waits here until the solve has published unit u (its
@@ -353,10 +357,56 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             };
             transpose_store16(r0, 1.f, gam, lane, 0, row_block);
             transpose_store16(r1, 1.f, gam, lane, 16, row_block);
-            fence_async_smem();
-            named_sync(kBarEpi, kEpiThreads);
             const int64_t t0 = seq_begin + (int64_t)c * C;
             const int len = chunk_len(c);
+            if (p.out_gate) {
+                // the layer's output step on the staged rows (the CTA holds all d_v = 128
+                // entries of its tokens): thread 2r + f takes the 64 entries of row r in
+                // staging tile f, the pair sums the row's squares
+                named_sync(kBarEpi, kEpiThreads);
+                const int r = etid >> 1, f = etid & 1;
+                unsigned char *tile = sm + OFF_OST + f * 8192;
+                auto seg_at = [&](int s) {
+                    return reinterpret_cast<uint4 *>(tile + r * 128 + (((s ^ r) & 7) << 4));
+                };
+                float ss = 0.f;
+                if (r < len) {
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const uint4 u = *seg_at(s);
+                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&uw[e]));
+                            ss = fmaf(x.x, x.x, fmaf(x.y, x.y, ss));
+                        }
+                    }
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (r < len) {
+                    const float rs = rsqrtf(ss * (1.f / NV) + p.out_norm_eps);
+                    const __nv_bfloat16 *zr = p.out_gate + ((size_t)(t0 + r) * p.H + h) * p.dv + col0 + 64 * f;
+                    const float *wr = p.out_norm_weight ? p.out_norm_weight + col0 + 64 * f : nullptr;
+#pragma unroll 2
+                    for (int s = 0; s < 8; ++s) {
+                        const uint4 u = *seg_at(s);
+                        const uint4 zu = *reinterpret_cast<const uint4 *>(zr + 8 * s);
+                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w}, zw[4] = {zu.x, zu.y, zu.z, zu.w};
+                        uint32_t ow[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&uw[e]));
+                            const float2 g = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&zw[e]));
+                            const float w0 = wr ? wr[8 * s + 2 * e] : 1.f, w1 = wr ? wr[8 * s + 2 * e + 1] : 1.f;
+                            ow[e] = pack_bf16x2(x.x * rs * w0 * (g.x / (1.f + __expf(-g.x))),
+                                                x.y * rs * w1 * (g.y / (1.f + __expf(-g.y))));
+                        }
+                        *seg_at(s) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                    }
+                }
+            }
+            fence_async_smem();
+            named_sync(kBarEpi, kEpiThreads);
             if (len == C) {
                 if (etid == 0) {
                     tma_store_3d(&map_o, stg, col0, h, (int)t0);

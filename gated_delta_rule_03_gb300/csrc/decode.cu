@@ -8,7 +8,9 @@
 //   o   = S'^T q = alpha b + (k.q) u        (read-out after the update)
 // which is Eqs. (1)-(4) of "Linear attention" (arsalanzafar.ai), "How it works",
 // for a single token. The additive rule (S' = alpha S + beta k v^T) is the same step
-// with u = beta v. The kernel is HBM-bound: a generation step reads about
+// with u = beta v. The layer's output step (o / rms(o) * w * silu(z), over the head's
+// value entries) is applied before o is stored when a gate z is given. The kernel is
+// HBM-bound: a generation step reads about
 // d_k d_v numbers ("Attention as Matrix Algebra", section 9).
 //
 // Layout: one CTA per (n, h); d_k*d_v/64 threads, each holding 16 rows x 4
@@ -26,6 +28,9 @@ template <> struct Vec4<float> {
     static __device__ __forceinline__ void store(float *p, float4 x) {
         *reinterpret_cast<float4 *>(p) = x;
     }
+    static __device__ __forceinline__ float4 load(const float *p) {
+        return *reinterpret_cast<const float4 *>(p);
+    }
 };
 template <> struct Vec4<__nv_bfloat16> {
     static __device__ __forceinline__ void store(__nv_bfloat16 *p, float4 x) {
@@ -36,14 +41,23 @@ template <> struct Vec4<__nv_bfloat16> {
         packed.y = *reinterpret_cast<uint32_t *>(&hi);
         *reinterpret_cast<uint2 *>(p) = packed;
     }
+    static __device__ __forceinline__ float4 load(const __nv_bfloat16 *p) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
 };
+
+// z sigmoid(z)
+__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
 
 template <typename Tin, int DK, int DV>
 __global__ void __launch_bounds__(DK * DV / 64)
 decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const Tin *__restrict__ v, const float *__restrict__ log_alpha,
                    const float *__restrict__ beta, float *__restrict__ S, Tin *__restrict__ o,
-                   float read) {
+                   float read, const Tin *__restrict__ z, const float *__restrict__ w, float eps) {
     // read = 1: the delta rule's correction u = beta (v - alpha S^T k); read = 0: the
     // additive write u = beta v
     constexpr int NT = DK * DV / 64;  // threads
@@ -52,9 +66,9 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     constexpr int RPT = DK / RG;      // rows per thread (= 16)
     static_assert(RPT == 16, "each thread holds 16 rows");
 
-    __shared__ float ks[DK], qs[DK], vs[DV];
+    __shared__ float ks[DK], qs[DK], vs[DV], os[DV];
     __shared__ float4 red_k[RG][TPR], red_q[RG][TPR];
-    __shared__ float s_kq;
+    __shared__ float s_kq, s_rstd;
 
     const int64_t nh = blockIdx.x;
     const int tid = threadIdx.x;
@@ -111,14 +125,33 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     u.y = b * (vv.y - ra * a.y);
     u.z = b * (vv.z - ra * a.z);
     u.w = b * (vv.w - ra * a.w);
-    if (rg == 0) {
-        float4 out;
-        out.x = fmaf(alpha, bq.x, kq * u.x);
-        out.y = fmaf(alpha, bq.y, kq * u.y);
-        out.z = fmaf(alpha, bq.z, kq * u.z);
-        out.w = fmaf(alpha, bq.w, kq * u.w);
-        Vec4<Tin>::store(o + nh * DV + 4 * cg, out);
+    float4 out;
+    out.x = fmaf(alpha, bq.x, kq * u.x);
+    out.y = fmaf(alpha, bq.y, kq * u.y);
+    out.z = fmaf(alpha, bq.z, kq * u.z);
+    out.w = fmaf(alpha, bq.w, kq * u.w);
+    if (z) {  // the output step: o / rms(o) * w * silu(z) over the head's DV entries
+        if (rg == 0) *reinterpret_cast<float4 *>(&os[4 * cg]) = out;
+        __syncthreads();
+        if (tid < 32) {
+            float ss = 0.f;
+            for (int j = tid; j < DV; j += 32) ss = fmaf(os[j], os[j], ss);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if (tid == 0) s_rstd = rsqrtf(ss * (1.f / DV) + eps);
+        }
+        __syncthreads();
+        if (rg == 0) {
+            const float r = s_rstd;
+            const float4 zz = Vec4<Tin>::load(z + nh * DV + 4 * cg);
+            const float4 ww = w ? *reinterpret_cast<const float4 *>(w + 4 * cg) : make_float4(1.f, 1.f, 1.f, 1.f);
+            out.x *= r * ww.x * silu(zz.x);
+            out.y *= r * ww.y * silu(zz.y);
+            out.z *= r * ww.z * silu(zz.z);
+            out.w *= r * ww.w * silu(zz.w);
+        }
     }
+    if (rg == 0) Vec4<Tin>::store(o + nh * DV + 4 * cg, out);
 #pragma unroll
     for (int m = 0; m < RPT; ++m) {
         const float kr = ks[rg + m * RG];
@@ -134,19 +167,21 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 template <typename Tin, int DK, int DV>
 static int launch_decode_t(const void *q, const void *k, const void *v, const float *la,
                            const float *beta, float *S, void *o, int64_t NH, float read,
-                           cudaStream_t stream) {
+                           const void *z, const float *w, float eps, cudaStream_t stream) {
     decode_step_kernel<Tin, DK, DV><<<(unsigned)NH, DK * DV / 64, 0, stream>>>(
-        (const Tin *)q, (const Tin *)k, (const Tin *)v, la, beta, S, (Tin *)o, read);
+        (const Tin *)q, (const Tin *)k, (const Tin *)v, la, beta, S, (Tin *)o, read,
+        (const Tin *)z, w, eps);
     return cuda_status(cudaGetLastError());
 }
 
 template <typename Tin>
 static int launch_decode_dtype(const void *q, const void *k, const void *v, const float *la,
                                const float *beta, float *S, void *o, int64_t NH, int dk, int dv,
-                               float read, cudaStream_t stream) {
+                               float read, const void *z, const float *w, float eps,
+                               cudaStream_t stream) {
 #define GDR_DECODE_CASE(DK_, DV_)                                                         \
     if (dk == DK_ && dv == DV_)                                                           \
-        return launch_decode_t<Tin, DK_, DV_>(q, k, v, la, beta, S, o, NH, read, stream);
+        return launch_decode_t<Tin, DK_, DV_>(q, k, v, la, beta, S, o, NH, read, z, w, eps, stream);
     GDR_DECODE_CASE(64, 64)
     GDR_DECODE_CASE(64, 128)
     GDR_DECODE_CASE(64, 256)
@@ -159,13 +194,16 @@ static int launch_decode_dtype(const void *q, const void *k, const void *v, cons
 
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
-                  int dtype, int rule, cudaStream_t stream) {
+                  int dtype, int rule, const void *out_gate, const float *out_norm_weight,
+                  float out_norm_eps, cudaStream_t stream) {
     const int64_t NH = N * H;
     const float read = rule == GDR_RULE_ADDITIVE ? 0.f : 1.f;
     if (dtype == GDR_BF16)
         return launch_decode_dtype<__nv_bfloat16>(q, k, v, log_alpha, beta, S, o, NH, dk, dv,
-                                                  read, stream);
-    return launch_decode_dtype<float>(q, k, v, log_alpha, beta, S, o, NH, dk, dv, read, stream);
+                                                  read, out_gate, out_norm_weight, out_norm_eps,
+                                                  stream);
+    return launch_decode_dtype<float>(q, k, v, log_alpha, beta, S, o, NH, dk, dv, read, out_gate,
+                                      out_norm_weight, out_norm_eps, stream);
 }
 
 }  // namespace gdr

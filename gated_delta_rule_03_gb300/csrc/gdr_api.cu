@@ -69,14 +69,33 @@ static int check_prefill_sizes(int64_t num_seqs, int64_t total_tokens, int H, in
     return GDR_OK;
 }
 
-// The rule of an options block (defaults for a null pointer); reserved words must be zero.
-static int check_options(const gdr_options *opt, int *rule) {
-    *rule = GDR_RULE_DELTA;
+// The checked contents of an options block (defaults for a null pointer).
+struct Opts {
+    int rule = GDR_RULE_DELTA;
+    const void *out_gate = nullptr;
+    const float *out_norm_weight = nullptr;
+    float out_norm_eps = 0.f;
+};
+
+// Reserved words must be zero; the output-step fields need a gate; pointers 16-byte aligned.
+static int check_options(const gdr_options *opt, Opts *o) {
+    *o = Opts();
     if (!opt) return GDR_OK;
     for (int r : opt->reserved)
         if (r != 0) return GDR_ERR_INVALID_ARG;
     if (opt->rule != GDR_RULE_DELTA && opt->rule != GDR_RULE_ADDITIVE) return GDR_ERR_UNSUPPORTED;
-    *rule = opt->rule;
+    o->rule = opt->rule;
+    if (!opt->out_gate) {
+        if (opt->out_norm_weight || opt->out_norm_eps != 0.f) return GDR_ERR_INVALID_ARG;
+        return GDR_OK;
+    }
+    const float eps = opt->out_norm_eps;
+    if (!(eps >= 0.f && eps < 3.0e38f)) return GDR_ERR_INVALID_ARG;  // also rejects NaN
+    if (((uintptr_t)opt->out_gate & 15u) || ((uintptr_t)opt->out_norm_weight & 15u))
+        return GDR_ERR_ALIGNMENT;
+    o->out_gate = opt->out_gate;
+    o->out_norm_weight = opt->out_norm_weight;
+    o->out_norm_eps = eps == 0.f ? 1e-6f : eps;
     return GDR_OK;
 }
 
@@ -116,8 +135,8 @@ int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
                      int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v, int chunk,
                      int dtype, void *o, float *S_final, void *workspace, size_t workspace_bytes,
                      const gdr_options *options, gdr_stream_t stream) {
-    int rule = GDR_RULE_DELTA;
-    int st = check_options(options, &rule);
+    Opts op;
+    int st = check_options(options, &op);
     if (st != GDR_OK) return st;
     st = check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype);
     if (st != GDR_OK) return st;
@@ -140,6 +159,7 @@ int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     if (o && overlaps(o, o_bytes, S_final, s_bytes)) return GDR_ERR_INVALID_ARG;
     if (overlaps(workspace, L.total, S_final, s_bytes)) return GDR_ERR_INVALID_ARG;
     if (o && overlaps(workspace, L.total, o, o_bytes)) return GDR_ERR_INVALID_ARG;
+    if (op.out_gate && o && overlaps(op.out_gate, o_bytes, o, o_bytes)) return GDR_ERR_INVALID_ARG;
 
     PrefillArgs a;
     a.q = q; a.k = k; a.v = v;
@@ -147,14 +167,23 @@ int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     a.cu_seqlens = cu_seqlens;
     a.num_seqs = num_seqs; a.total_tokens = total_tokens;
     a.H = H; a.dk = d_k; a.dv = d_v; a.chunk = chunk; a.dtype = dtype;
-    a.rule = rule;
+    a.rule = op.rule;
+    a.out_gate = op.out_gate;
+    a.out_norm_weight = op.out_norm_weight;
+    a.out_norm_eps = op.out_norm_eps;
     a.o = o; a.S_final = S_final;
     a.ws = (char *)workspace;
     a.stream = (cudaStream_t)stream;
     const int phases = L.tensor_path ? tc_schedule(a) : 1;
     st = launch_plan(a, L, phases);
     if (st != GDR_OK) return st;
-    return L.tensor_path ? launch_prefill_tc(a, L, phases) : launch_prefill_exact(a, L);
+    st = L.tensor_path ? launch_prefill_tc(a, L, phases) : launch_prefill_exact(a, L);
+    // the output step, where the chain did not fuse it (it does on the tensor-core path
+    // when one chain CTA holds all d_v = 128 entries of a token)
+    if (st == GDR_OK && a.out_gate && !(L.tensor_path && d_v == 128))
+        st = launch_out_norm_gate(o, a.out_gate, a.out_norm_weight, a.out_norm_eps,
+                                  total_tokens * H, d_v, dtype, a.stream);
+    return st;
 }
 
 int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -170,8 +199,8 @@ int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
 int gdr_decode_step_ex(const void *q, const void *k, const void *v, const float *log_alpha,
                        const float *beta, float *S, void *o, int64_t N, int H, int d_k, int d_v,
                        int dtype, const gdr_options *options, gdr_stream_t stream) {
-    int rule = GDR_RULE_DELTA;
-    const int st = check_options(options, &rule);
+    Opts op;
+    const int st = check_options(options, &op);
     if (st != GDR_OK) return st;
     if (N < 0 || H < 1 || N > INT32_MAX || (int64_t)N * H > INT32_MAX) return GDR_ERR_INVALID_ARG;
     if (dtype != GDR_F32 && dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
@@ -186,8 +215,10 @@ int gdr_decode_step_ex(const void *q, const void *k, const void *v, const float 
     const size_t esz = dtype == GDR_F32 ? 4 : 2;
     if (overlaps(o, (size_t)N * H * d_v * esz, S, (size_t)N * H * d_k * d_v * sizeof(float)))
         return GDR_ERR_INVALID_ARG;
-    return launch_decode(q, k, v, log_alpha, beta, S, o, N, H, d_k, d_v, dtype, rule,
-                         (cudaStream_t)stream);
+    if (op.out_gate && overlaps(op.out_gate, (size_t)N * H * d_v * esz, o, (size_t)N * H * d_v * esz))
+        return GDR_ERR_INVALID_ARG;
+    return launch_decode(q, k, v, log_alpha, beta, S, o, N, H, d_k, d_v, dtype, op.rule, op.out_gate,
+                         op.out_norm_weight, op.out_norm_eps, (cudaStream_t)stream);
 }
 
 int gdr_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,

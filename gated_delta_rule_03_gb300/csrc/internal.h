@@ -22,6 +22,10 @@ struct PrefillArgs {
     int64_t num_seqs, total_tokens;
     int H, dk, dv, chunk, dtype;
     int rule;  // GDR_RULE_DELTA or GDR_RULE_ADDITIVE
+    // the output step (null out_gate: none): o <- rmsnorm(o) * w * silu(z)
+    const void *out_gate;
+    const float *out_norm_weight;
+    float out_norm_eps;
     void *o;
     float *S_final;
     char *ws;
@@ -69,7 +73,12 @@ int tc_schedule(const PrefillArgs &a);
 int tc_schedule_launches(int64_t num_seqs, int64_t total_tokens, int H, int dv, bool varlen);
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
-                  int dtype, int rule, cudaStream_t stream);
+                  int dtype, int rule, const void *out_gate, const float *out_norm_weight,
+                  float out_norm_eps, cudaStream_t stream);
+// The output step over `rows` rows of d_v entries of o, in place (prefill paths that do
+// not fuse it).
+int launch_out_norm_gate(void *o, const void *z, const float *w, float eps, int64_t rows, int dv,
+                         int dtype, cudaStream_t stream);
 
 // Type helpers for kernels.
 template <typename T> __device__ __forceinline__ float to_f32(T x);

@@ -263,6 +263,11 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     p.ctl = (int32_t *)(a.ws + L.ctl);
     p.flags = flags;
     p.additive = a.rule == GDR_RULE_ADDITIVE;
+    if (a.dv == NV) {  // the output step fused into the chain's epilogue
+        p.out_gate = (const __nv_bfloat16 *)a.out_gate;
+        p.out_norm_weight = a.out_norm_weight;
+        p.out_norm_eps = a.out_norm_eps;
+    }
     solve::SolveParams sp = {};
     sp.log_alpha = a.log_alpha;
     sp.beta = a.beta;
@@ -348,6 +353,11 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
     p.o = (__nv_bfloat16 *)a.o;
     p.ctl = (int32_t *)(a.ws + L.ctl);
     p.additive = a.rule == GDR_RULE_ADDITIVE;
+    if (a.dv == NV) {  // the output step fused into the chain's epilogue
+        p.out_gate = (const __nv_bfloat16 *)a.out_gate;
+        p.out_norm_weight = a.out_norm_weight;
+        p.out_norm_eps = a.out_norm_eps;
+    }
     float *S_mid = reinterpret_cast<float *>(a.ws + L.S);
     for (int f = 0; f < phases; ++f) {
         if (f > 0 && cudaStreamWaitEvent(a.stream, sd->ev[f], 0) != cudaSuccess) return GDR_ERR_CUDA;

@@ -21,13 +21,32 @@ RULES = {"delta": 0, "additive": 1}
 
 class GdrOptions(ctypes.Structure):
     """struct gdr_options of gdr.h."""
-    _fields_ = [("rule", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+    _fields_ = [("rule", ctypes.c_int), ("out_norm_eps", ctypes.c_float),
+                ("out_gate", ctypes.c_void_p), ("out_norm_weight", ctypes.c_void_p),
+                ("reserved", ctypes.c_int * 4)]
 
 
-def _options(rule):
+def _options(rule, out_gate=None, out_norm_weight=None, out_norm_eps=0.0):
     if rule not in RULES:
         raise ValueError(f"unknown rule {rule!r}; expected one of {sorted(RULES)}")
-    return ctypes.byref(GdrOptions(RULES[rule]))
+    opt = GdrOptions(RULES[rule], float(out_norm_eps) if out_gate is not None else 0.0,
+                     None if out_gate is None else out_gate.data_ptr(),
+                     None if out_norm_weight is None else out_norm_weight.data_ptr())
+    return ctypes.byref(opt)
+
+
+def _check_out_step(out_gate, out_norm_weight, like, dv):
+    if out_gate is None:
+        if out_norm_weight is not None:
+            raise ValueError("out_norm_weight needs out_gate")
+        return
+    _need(out_gate, "out_gate", like.dtype, like.device)
+    if tuple(out_gate.shape) != tuple(like.shape):
+        raise ValueError(f"out_gate must have shape {tuple(like.shape)}")
+    if out_norm_weight is not None:
+        _need(out_norm_weight, "out_norm_weight", torch.float32, like.device)
+        if out_norm_weight.numel() != dv:
+            raise ValueError(f"out_norm_weight must have {dv} entries")
 
 
 class GdrError(RuntimeError):
@@ -119,13 +138,17 @@ def chunk_fwd_workspace_size(num_seqs, total_tokens, H, dk, dv, chunk=64, dtype=
 
 
 def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None, chunk=64,
-              o=None, S_final=None, workspace=None, stream=None, rule="delta"):
+              o=None, S_final=None, workspace=None, stream=None, rule="delta", out_gate=None,
+              out_norm_weight=None, out_norm_eps=1e-6):
     """Chunked prefill (gdr_chunk_fwd).
 
     q, k [T, H, dk]; v [T, H, dv] (fp32 or bf16); log_alpha, beta [T, H] fp32;
     S0 [num_seqs, H, dk, dv] fp32 or None; cu_seqlens [num_seqs+1] int32 or None
     (then `num_seqs` equal sequences, default 1). Optional preallocated o,
-    S_final and workspace (uint8) tensors are used as given. Returns (o, S_final).
+    S_final and workspace (uint8) tensors are used as given. rule: "delta" (the gated
+    delta rule) or "additive" (S <- alpha S + beta k v^T). out_gate [T, H, dv] (o's
+    dtype): apply the layer's output step o <- o / rms(o) * out_norm_weight * silu(out_gate)
+    over each head's dv entries (gdr_options in gdr.h). Returns (o, S_final).
     """
     lib = _load()
     _need(q, "q")
@@ -151,6 +174,7 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
         S_final = torch.empty((n, H, dk, dv), dtype=torch.float32, device=dev)
     _need(o, "o", dt, dev)
     _need(S_final, "S_final", torch.float32, dev)
+    _check_out_step(out_gate, out_norm_weight, o, dv)
     ws_bytes = chunk_fwd_workspace_size(n, T, H, dk, dv, chunk, dt)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
@@ -158,7 +182,8 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
     st = lib.gdr_chunk_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
                               _ptr(cu_seqlens), n, T, H, dk, dv, int(chunk), _DTYPES[dt], _ptr(o),
                               _ptr(S_final), _ptr(workspace),
-                              workspace.numel() * workspace.element_size(), _options(rule),
+                              workspace.numel() * workspace.element_size(),
+                              _options(rule, out_gate, out_norm_weight, out_norm_eps),
                               _stream_handle(stream, dev))
     _check(st, "gdr_chunk_fwd_ex")
     return o, S_final
@@ -173,7 +198,8 @@ def read_device_status(workspace, stream=None):
     return out.value
 
 
-def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None, rule="delta"):
+def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None, rule="delta", out_gate=None,
+                out_norm_weight=None, out_norm_eps=1e-6):
     """One decode step (gdr_decode_step_ex): q, k [N, H, dk]; v [N, H, dv];
     log_alpha, beta [N, H] fp32; S [N, H, dk, dv] fp32 updated in place; rule "delta"
     (the gated delta rule) or "additive" (S <- alpha S + beta k v^T). Returns o [N, H, dv]."""
@@ -190,8 +216,10 @@ def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None, rule="delta"):
     if o is None:
         o = torch.empty((N, H, dv), dtype=dt, device=dev)
     _need(o, "o", dt, dev)
+    _check_out_step(out_gate, out_norm_weight, o, dv)
     st = lib.gdr_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S),
-                                _ptr(o), N, H, dk, dv, _DTYPES[dt], _options(rule),
+                                _ptr(o), N, H, dk, dv, _DTYPES[dt],
+                                _options(rule, out_gate, out_norm_weight, out_norm_eps),
                                 _stream_handle(stream, dev))
     _check(st, "gdr_decode_step_ex")
     return o

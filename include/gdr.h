@@ -187,17 +187,32 @@ enum { GDR_RULE_DELTA = 0, GDR_RULE_ADDITIVE = 1 };
 /*
  * Options of the _ex entry points. A null pointer means all defaults; the
  * reserved words must be zero (else GDR_ERR_INVALID_ARG).
- *   rule   GDR_RULE_DELTA or GDR_RULE_ADDITIVE (else GDR_ERR_UNSUPPORTED)
+ *   rule             GDR_RULE_DELTA or GDR_RULE_ADDITIVE (else GDR_ERR_UNSUPPORTED)
+ *   out_gate         the layer's output step, applied to o before it is stored
+ *                    ("Linear attention" (arsalanzafar.ai), "A naive PyTorch
+ *                    implementation": the output normalised over the head
+ *                    dimension, times SiLU of the input-dependent output gate):
+ *                      o_tj <- o_tj / sqrt(mean_j' o_tj'^2 + eps) * w_j * z_tj * sigmoid(z_tj)
+ *                    per token t and head, j over the head's d_v entries. out_gate
+ *                    holds z, laid out like o ([tokens, H, d_v] for gdr_chunk_fwd_ex,
+ *                    [N, H, d_v] for gdr_decode_step_ex), in o's dtype, 16-byte
+ *                    aligned. Null: no output step (then the two fields below must
+ *                    be null and zero). The state is not affected.
+ *   out_norm_weight  w: [d_v] fp32, 16-byte aligned; null means all ones.
+ *   out_norm_eps     eps >= 0 (finite); 0 means 1e-6.
  */
 typedef struct gdr_options {
     int rule;
-    int reserved[7];
+    float out_norm_eps;
+    const void *out_gate;
+    const float *out_norm_weight;
+    int reserved[4];
 } gdr_options;
 
 /*
  * gdr_chunk_fwd with options: the same arguments, layouts, ownership and
- * errors, for the rule in *options. gdr_chunk_fwd is this call with a null
- * options pointer.
+ * errors, for the rule and output step in *options. gdr_chunk_fwd is this call
+ * with a null options pointer. out_gate must not overlap o (it may not be o).
  */
 int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
                      const float *beta, const float *S0, const int32_t *cu_seqlens,
@@ -208,7 +223,8 @@ int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
 /*
  * gdr_decode_step with options, as gdr_chunk_fwd_ex. For GDR_RULE_ADDITIVE
  * the step is S <- alpha S + beta k v^T, o = S_new^T q (one read and one
- * write of S, as for the delta rule).
+ * write of S, as for the delta rule). The output step, if any, is fused into
+ * the same kernel.
  */
 int gdr_decode_step_ex(const void *q, const void *k, const void *v, const float *log_alpha,
                        const float *beta, float *S, void *o, int64_t N, int H, int d_k, int d_v,

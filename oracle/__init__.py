@@ -107,3 +107,19 @@ def decode(q, k, v, log_alpha, beta, S, threads=None):
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (status {rc})")
     return o, S_new
+
+
+def out_norm_gate(o, gate, weight=None, eps=1e-6):
+    """The layer's output step after the recurrence, in float64 ("Linear attention"
+    (arsalanzafar.ai), "A naive PyTorch implementation": the output is normalised over
+    the head dimension, then multiplied by SiLU of the input-dependent output gate):
+
+        o'_tj = o_tj / sqrt(mean_j' o_tj'^2 + eps) * weight_j * gate_tj * sigmoid(gate_tj)
+
+    per token and head; o and gate [..., d_v], weight [d_v] (None: ones). The mean runs
+    over the last axis (the head's value entries). Written out with numpy, elementwise."""
+    o = _f64(o)
+    g = _f64(gate)
+    w = np.ones(o.shape[-1]) if weight is None else _f64(weight)
+    rms = np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    return o / rms * w * (g / (1.0 + np.exp(-g)))

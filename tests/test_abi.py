@@ -132,6 +132,18 @@ def test_options_validated_on_the_host(lib):
     for f in (call, dcall):
         assert f(ctypes.byref(bad_rule)) == -2
         assert f(ctypes.byref(reserved)) == -1
+    # the output-step fields: a weight or an eps without a gate, a negative eps, an
+    # unaligned gate
+    fake = lambda a: ctypes.c_void_p(a)
+    o1 = GdrOptions(0, 0.0, None, A + 0x9000000)
+    o2 = GdrOptions(0, 1e-5, None, None)
+    o3 = GdrOptions(0, -1.0, A + 0x8000000, None)
+    o4 = GdrOptions(0, 0.0, A + 0x8000008, None)
+    for f in (call, dcall):
+        assert f(ctypes.byref(o1)) == -1
+        assert f(ctypes.byref(o2)) == -1
+        assert f(ctypes.byref(o3)) == -1
+        assert f(ctypes.byref(o4)) == -3
     # a valid options block gets as far as the argument checks of the plain entry points
     ok = GdrOptions(1)
     assert lib.gdr_chunk_fwd_ex(None, p[1], p[2], p[3], p[4], None, None, 1, 128, 2, 64, 64, 64,

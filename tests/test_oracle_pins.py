@@ -396,3 +396,34 @@ def test_gated_wy_form_is_the_product_of_transitions():
     S0 = rng.standard_normal((dk, 3))
     _, S = run(np.zeros((C, dk)), k, np.zeros((C, 3)), log_alpha=la, beta=b, S0=S0)
     np.testing.assert_allclose(S, prod @ S0, rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- output step
+
+def test_out_norm_gate_worked_values():
+    # o = [3, 4]: mean square 12.5, so the row is divided by sqrt(12.5) (not by its L2 norm
+    # 5); a gate of 40 has sigmoid(40) = 1 in float64, so SiLU(40) = 40
+    o = np.array([[3.0, 4.0]])
+    got = oracle.out_norm_gate(o, np.full((1, 2), 40.0), eps=0.0)
+    np.testing.assert_allclose(got, [[3 / np.sqrt(12.5) * 40, 4 / np.sqrt(12.5) * 40]], rtol=1e-15)
+    # SiLU(0) = 0 and SiLU(ln 3) = ln 3 * 3/4 (sigmoid(ln 3) = 3/4)
+    got = oracle.out_norm_gate(o, np.array([[0.0, np.log(3.0)]]), eps=0.0)
+    np.testing.assert_allclose(got, [[0.0, 4 / np.sqrt(12.5) * 0.75 * np.log(3.0)]], rtol=1e-15)
+
+
+def test_out_norm_gate_weight_eps_and_scale():
+    rng = np.random.default_rng(7)
+    o = rng.standard_normal((5, 3, 8))
+    big = np.full(o.shape, 40.0)
+    # with unit weight and SiLU(40) = 40 every row has root-mean-square 40 (eps = 0)
+    got = oracle.out_norm_gate(o, big, eps=0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(got ** 2, axis=-1)), 40.0, rtol=1e-13)
+    # the normalisation is invariant to the row's scale; the weight multiplies per column
+    w = rng.uniform(0.5, 2.0, 8)
+    np.testing.assert_allclose(oracle.out_norm_gate(7.5 * o, big, weight=w, eps=0.0),
+                               oracle.out_norm_gate(o, big, eps=0.0) * w, rtol=1e-13)
+    # eps keeps an all-zero row finite (zero) and shrinks a tiny row: rms = sqrt(1e-8 + eps)
+    z = oracle.out_norm_gate(np.zeros((1, 4)), np.ones((1, 4)), eps=1e-6)
+    np.testing.assert_array_equal(z, 0.0)
+    t = oracle.out_norm_gate(np.full((1, 4), 1e-4), np.full((1, 4), 40.0), eps=1e-6)
+    np.testing.assert_allclose(t, 1e-4 / np.sqrt(1e-8 + 1e-6) * 40.0, rtol=1e-13)
