@@ -88,11 +88,14 @@ constexpr int kBarPrep = 1, kBarEpi = 3;  // named barrier ids
 
 // Shared memory map (bytes from a 1024-aligned base).
 constexpr uint32_t RQ = 0, RQ_SLOT = 32768;        // per d_k half b (16 KB): Q_b then -W'_b
-constexpr uint32_t RK = 65536, RK_SLOT = 25600;    // K_b0 | K_b1 | A^T (8 KB each) | factors
+constexpr uint32_t RK = 65536, RK_SLOT = 26624;    // K_b0 | K_b1 | A^T (8 KB each) | factors
 constexpr uint32_t RK_A = 16384, RK_G = 24576;     // offsets of A^T and the factors in a K slot
 constexpr uint32_t RV = RK + 3 * RK_SLOT, RV_SLOT = 24576;  // V_b0 | V_b1 | T'
 constexpr uint32_t RV_T = 16384;
-constexpr int G_GAM = 64, G_KDEC = 128, G_FORM = 192;  // float offsets in the factors (g at 0)
+// float offsets in a unit's factors (g at 0); 1/|k|, 1/|q| of the layer prologue (else 1)
+constexpr int G_GAM = 64, G_KDEC = 128, G_FORM = 192, G_NK = 256, G_NQ = 320;
+constexpr uint32_t kFactorBytes = 384 * 4;
+static_assert(RK_G + kFactorBytes <= RK_SLOT, "K slot");
 constexpr uint32_t OFF_TG = RV + 2 * RV_SLOT;   // T' diag(gamma) bf16 [t][i]
 constexpr uint32_t OFF_OST = OFF_TG + 8192;     // output staging [t][128]: two 8 KB tiles
 constexpr uint32_t OFF_EG = OFF_OST + 16384;    // epilogue gates: gamma[4][64], form flag[4]
@@ -145,6 +148,7 @@ struct TcParams {
     int32_t *ctl;
     const int32_t *flags;      // fused launch: per solve unit, set once the unit is solved
     int additive;              // the additive rule: W' = 0 (the state does not enter U')
+    int prologue;              // the layer prologue: 1/|k|, 1/|q| from the factors apply
     // the layer's output step on o (null out_gate: none; only when d_v = NV, one slice)
     const __nv_bfloat16 *out_gate;
     const float *out_norm_weight;
@@ -313,11 +317,13 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 // K, A^T, factors (slot free once chunk c - 3 is done)
                 if (c >= 3 && !mbar_wait(bar(B_KE0 + c % 3), (c / 3 - 1) & 1)) { note_fail(3); break; }
                 const uint32_t ks = sbase + kslot(c), kf = bar(B_KF0 + c % 3);
-                mbar_arrive_expect_tx(kf, 3 * 8192 + 1024);
+                // the factors: the decay's 1 KB, plus 1/|k|, 1/|q| with the prologue
+                const uint32_t fbytes = p.prologue ? kFactorBytes : 1024u;
+                mbar_arrive_expect_tx(kf, 3 * 8192 + fbytes);
                 tma_load_3d(ks, &map_k, kf, 0, h, tt);
                 tma_load_3d(ks + 8192, &map_k, kf, 64, h, tt);
                 tma_load_3d(ks + RK_A, &map_t, kf, 0, 0, 2 * unit + 1);
-                bulk_load(ks + RK_G, p.factors + (size_t)unit * 256, 1024, kf);
+                bulk_load(ks + RK_G, p.factors + (size_t)unit * 384, fbytes, kf);
                 // Q (slot free once [QS | WS] of chunk c - 2 is done)
                 if (c >= 2 && !mbar_wait(bar(B_QE0 + (c & 1)), ((c >> 1) - 1) & 1)) { note_fail(3); break; }
                 const uint32_t qs = sbase + qslot(c), qf = bar(B_QF0 + (c & 1));
@@ -348,8 +354,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             if (etid == 0) bulk_wait_group_read<0>();
             named_sync(kBarEpi, kEpiThreads);
             const uint32_t stg = sbase + OFF_OST;
-            const bool ratio = eg[256 + (c & 3)] != 0.f;
-            const float *gam = ratio ? eg + 64 * (c & 3) : nullptr;
+            // the output rows' scales (prep), when there are any
+            const float *gam = eg[256 + (c & 3)] != 0.f ? eg + 64 * (c & 3) : nullptr;
             auto row_block = [&](int l8, uint32_t &block, int &c8) {
                 const int dv = 32 * warp + l8;  // value column within the slice
                 block = stg + (dv >> 6) * 8192;
@@ -456,9 +462,17 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                     const uint32_t off = (uint32_t)(t * 128 + (((j ^ t) & 7) << 4));
                     uint4 w = *reinterpret_cast<const uint4 *>(vs_p + RV_T + off);
                     uint32_t *uw = &w.x;
+                    // gamma_i (times the prologue's 1/|k_i|: the unit-length keys enter W' here)
                     const float4 ga = *reinterpret_cast<const float4 *>(gate + G_GAM + 8 * j);
                     const float4 gb = *reinterpret_cast<const float4 *>(gate + G_GAM + 8 * j + 4);
-                    const float gj[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                    float gj[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                    if (p.prologue) {
+                        const float4 na = *reinterpret_cast<const float4 *>(gate + G_NK + 8 * j);
+                        const float4 nb = *reinterpret_cast<const float4 *>(gate + G_NK + 8 * j + 4);
+                        const float nj[8] = {na.x, na.y, na.z, na.w, nb.x, nb.y, nb.z, nb.w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) gj[e] *= nj[e];
+                    }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&uw[e]));
@@ -466,8 +480,11 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                     }
                     *reinterpret_cast<uint4 *>(sm + OFF_TG + off) = w;
                 }
-                if (ptid < C) eg[64 * (c & 3) + ptid] = gate[G_GAM + ptid];
-                if (ptid == 0) eg[256 + (c & 3)] = ratio ? 1.f : 0.f;
+                // the scale of output row t: gamma_t (ratio form) times the prologue's 1/|q_t|
+                if (ptid < C)
+                    eg[64 * (c & 3) + ptid] = p.prologue ? (ratio ? gate[G_GAM + ptid] : 1.f) * gate[G_NQ + ptid]
+                                                         : gate[G_GAM + ptid];
+                if (ptid == 0) eg[256 + (c & 3)] = (ratio || p.prologue) ? 1.f : 0.f;
                 mbar_arrive(bar(B_EG0 + (c & 3)));
             }
             // T' diag(gamma) is staged: the MMA warp issues U'~ and W' when the chain
@@ -639,8 +656,15 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                     tmem_load32(lane_base + TM_U + 64 * (cp & 1) + 32 * half, a);
                     tmem_load32(lane_base + TM_X + 32 * half, b);
                     uint32_t w[16];
+                    if (p.prologue) {  // U'_i 1/|k_i|: the unit-length keys of the state update
+                        const float *nk = reinterpret_cast<const float *>(sm + kslot(cp) + RK_G) + G_NK + 32 * half;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(a[2 * i] + b[2 * i], a[2 * i + 1] + b[2 * i + 1]);
+                        for (int i = 0; i < 16; ++i)
+                            w[i] = pack_bf16x2((a[2 * i] + b[2 * i]) * nk[2 * i], (a[2 * i + 1] + b[2 * i + 1]) * nk[2 * i + 1]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(a[2 * i] + b[2 * i], a[2 * i + 1] + b[2 * i + 1]);
+                    }
                     tmem_store16(lane_base + TM_X + 32 * half, w);
                 }
                 warp_arrive(B_UREADY);

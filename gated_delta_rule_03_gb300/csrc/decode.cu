@@ -8,7 +8,8 @@
 //   o   = S'^T q = alpha b + (k.q) u        (read-out after the update)
 // which is Eqs. (1)-(4) of "Linear attention" (arsalanzafar.ai), "How it works",
 // for a single token. The additive rule (S' = alpha S + beta k v^T) is the same step
-// with u = beta v. The layer's output step (o / rms(o) * w * silu(z), over the head's
+// with u = beta v. With the layer's prologue, k and q are scaled to unit length in
+// shared memory and the gates come from their pre-activations. The layer's output step (o / rms(o) * w * silu(z), over the head's
 // value entries) is applied before o is stored when a gate z is given. The kernel is
 // HBM-bound: a generation step reads about
 // d_k d_v numbers ("Attention as Matrix Algebra", section 9).
@@ -57,7 +58,8 @@ __global__ void __launch_bounds__(DK * DV / 64)
 decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const Tin *__restrict__ v, const float *__restrict__ log_alpha,
                    const float *__restrict__ beta, float *__restrict__ S, Tin *__restrict__ o,
-                   float read, const Tin *__restrict__ z, const float *__restrict__ w, float eps) {
+                   float read, const Tin *__restrict__ z, const float *__restrict__ w, float eps,
+                   int prologue, const float *__restrict__ gate_A, int H) {
     // read = 1: the delta rule's correction u = beta (v - alpha S^T k); read = 0: the
     // additive write u = beta v
     constexpr int NT = DK * DV / 64;  // threads
@@ -68,7 +70,7 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 
     __shared__ float ks[DK], qs[DK], vs[DV], os[DV];
     __shared__ float4 red_k[RG][TPR], red_q[RG][TPR];
-    __shared__ float s_kq, s_rstd;
+    __shared__ float s_kq, s_rstd, s_nk, s_nq;
 
     const int64_t nh = blockIdx.x;
     const int tid = threadIdx.x;
@@ -85,10 +87,32 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         qs[i] = to_f32(q[nh * DK + i]);
     }
     for (int j = tid; j < DV; j += NT) vs[j] = to_f32(v[nh * DV + j]);
-    const float alpha = expf(log_alpha[nh]);
-    const float b = beta[nh];
+    float alpha, b;
+    if (prologue) {  // the layer's gate activations from the pre-activations a, b
+        alpha = expf(prologue_log_alpha(log_alpha[nh], gate_A ? gate_A[nh % H] : 1.f));
+        b = prologue_beta(beta[nh]);
+    } else {
+        alpha = expf(log_alpha[nh]);
+        b = beta[nh];
+    }
     const float ra = read * alpha;
     __syncthreads();
+    if (prologue) {  // unit-length k and q: warp 0 sums k's squares, warp 1 q's
+        if (tid < 64) {
+            const float *x = tid < 32 ? ks : qs;
+            float ss = 0.f;
+            for (int i = tid & 31; i < DK; i += 32) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if ((tid & 31) == 0) (tid < 32 ? s_nk : s_nq) = prologue_inv_norm(ss);
+        }
+        __syncthreads();
+        for (int i = tid; i < DK; i += NT) {
+            ks[i] *= s_nk;
+            qs[i] *= s_nq;
+        }
+        __syncthreads();
+    }
 
     if (tid < 32) {
         float p = 0.f;
@@ -167,21 +191,23 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 template <typename Tin, int DK, int DV>
 static int launch_decode_t(const void *q, const void *k, const void *v, const float *la,
                            const float *beta, float *S, void *o, int64_t NH, float read,
-                           const void *z, const float *w, float eps, cudaStream_t stream) {
+                           const void *z, const float *w, float eps, int prologue,
+                           const float *gate_A, int H, cudaStream_t stream) {
     decode_step_kernel<Tin, DK, DV><<<(unsigned)NH, DK * DV / 64, 0, stream>>>(
         (const Tin *)q, (const Tin *)k, (const Tin *)v, la, beta, S, (Tin *)o, read,
-        (const Tin *)z, w, eps);
+        (const Tin *)z, w, eps, prologue, gate_A, H);
     return cuda_status(cudaGetLastError());
 }
 
 template <typename Tin>
 static int launch_decode_dtype(const void *q, const void *k, const void *v, const float *la,
                                const float *beta, float *S, void *o, int64_t NH, int dk, int dv,
-                               float read, const void *z, const float *w, float eps,
-                               cudaStream_t stream) {
+                               float read, const void *z, const float *w, float eps, int prologue,
+                               const float *gate_A, int H, cudaStream_t stream) {
 #define GDR_DECODE_CASE(DK_, DV_)                                                         \
     if (dk == DK_ && dv == DV_)                                                           \
-        return launch_decode_t<Tin, DK_, DV_>(q, k, v, la, beta, S, o, NH, read, z, w, eps, stream);
+        return launch_decode_t<Tin, DK_, DV_>(q, k, v, la, beta, S, o, NH, read, z, w, eps, \
+                                              prologue, gate_A, H, stream);
     GDR_DECODE_CASE(64, 64)
     GDR_DECODE_CASE(64, 128)
     GDR_DECODE_CASE(64, 256)
@@ -195,15 +221,15 @@ static int launch_decode_dtype(const void *q, const void *k, const void *v, cons
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
                   int dtype, int rule, const void *out_gate, const float *out_norm_weight,
-                  float out_norm_eps, cudaStream_t stream) {
+                  float out_norm_eps, int prologue, const float *gate_A, cudaStream_t stream) {
     const int64_t NH = N * H;
     const float read = rule == GDR_RULE_ADDITIVE ? 0.f : 1.f;
     if (dtype == GDR_BF16)
         return launch_decode_dtype<__nv_bfloat16>(q, k, v, log_alpha, beta, S, o, NH, dk, dv,
                                                   read, out_gate, out_norm_weight, out_norm_eps,
-                                                  stream);
+                                                  prologue, gate_A, H, stream);
     return launch_decode_dtype<float>(q, k, v, log_alpha, beta, S, o, NH, dk, dv, read, out_gate,
-                                      out_norm_weight, out_norm_eps, stream);
+                                      out_norm_weight, out_norm_eps, prologue, gate_A, H, stream);
 }
 
 }  // namespace gdr

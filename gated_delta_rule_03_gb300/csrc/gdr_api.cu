@@ -36,13 +36,13 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
         off = align_up(off + sizeof(float) * per * dv, 256);
         L.A = off;
         off = align_up(off + sizeof(float) * per * kChunk, 256);
-        L.g = off;  // gamma and kdec per chunk
-        off = align_up(off + sizeof(float) * per * 2, 256);
+        L.g = off;  // gamma, kdec, and the prologue's 1/|q|, 1/|k| per chunk token
+        off = align_up(off + sizeof(float) * per * 4, 256);
     } else {
         L.T = off;  // two 64x64 bf16 matrices per (chunk, head)
         off = align_up(off + (size_t)L.max_chunks * (size_t)H * 2 * kChunk * kChunk * 2, 256);
-        L.G = off;  // 256 floats per (chunk, head)
-        off = align_up(off + (size_t)L.max_chunks * (size_t)H * 256 * sizeof(float), 256);
+        L.G = off;  // 384 floats per (chunk, head): decay factors, the prologue's norms
+        off = align_up(off + (size_t)L.max_chunks * (size_t)H * 384 * sizeof(float), 256);
         L.S = off;  // the state handed from one phase to the next
         off = align_up(off + (size_t)num_seqs * (size_t)H * dk * dv * sizeof(float), 256);
         L.F = off;  // the solve's pair counters, then one flag per (chunk, head) unit
@@ -75,16 +75,23 @@ struct Opts {
     const void *out_gate = nullptr;
     const float *out_norm_weight = nullptr;
     float out_norm_eps = 0.f;
+    int prologue = GDR_PROLOGUE_NONE;
+    const float *gate_A = nullptr;
 };
 
 // Reserved words must be zero; the output-step fields need a gate; pointers 16-byte aligned.
 static int check_options(const gdr_options *opt, Opts *o) {
     *o = Opts();
     if (!opt) return GDR_OK;
-    for (int r : opt->reserved)
-        if (r != 0) return GDR_ERR_INVALID_ARG;
+    if (opt->reserved != 0) return GDR_ERR_INVALID_ARG;
     if (opt->rule != GDR_RULE_DELTA && opt->rule != GDR_RULE_ADDITIVE) return GDR_ERR_UNSUPPORTED;
     o->rule = opt->rule;
+    if (opt->prologue != GDR_PROLOGUE_NONE && opt->prologue != GDR_PROLOGUE_LAYER)
+        return GDR_ERR_UNSUPPORTED;
+    if (opt->gate_A && opt->prologue != GDR_PROLOGUE_LAYER) return GDR_ERR_INVALID_ARG;
+    if ((uintptr_t)opt->gate_A & 3u) return GDR_ERR_ALIGNMENT;
+    o->prologue = opt->prologue;
+    o->gate_A = opt->gate_A;
     if (!opt->out_gate) {
         if (opt->out_norm_weight || opt->out_norm_eps != 0.f) return GDR_ERR_INVALID_ARG;
         return GDR_OK;
@@ -171,6 +178,8 @@ int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     a.out_gate = op.out_gate;
     a.out_norm_weight = op.out_norm_weight;
     a.out_norm_eps = op.out_norm_eps;
+    a.prologue = op.prologue;
+    a.gate_A = op.gate_A;
     a.o = o; a.S_final = S_final;
     a.ws = (char *)workspace;
     a.stream = (cudaStream_t)stream;
@@ -218,7 +227,8 @@ int gdr_decode_step_ex(const void *q, const void *k, const void *v, const float 
     if (op.out_gate && overlaps(op.out_gate, (size_t)N * H * d_v * esz, o, (size_t)N * H * d_v * esz))
         return GDR_ERR_INVALID_ARG;
     return launch_decode(q, k, v, log_alpha, beta, S, o, N, H, d_k, d_v, dtype, op.rule, op.out_gate,
-                         op.out_norm_weight, op.out_norm_eps, (cudaStream_t)stream);
+                         op.out_norm_weight, op.out_norm_eps, op.prologue, op.gate_A,
+                         (cudaStream_t)stream);
 }
 
 int gdr_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,

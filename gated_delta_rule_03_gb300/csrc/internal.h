@@ -26,6 +26,9 @@ struct PrefillArgs {
     const void *out_gate;
     const float *out_norm_weight;
     float out_norm_eps;
+    // the layer's prologue (unit-length q and k, gates from pre-activations)
+    int prologue;
+    const float *gate_A;
     void *o;
     float *S_final;
     char *ws;
@@ -74,11 +77,20 @@ int tc_schedule_launches(int64_t num_seqs, int64_t total_tokens, int H, int dv, 
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
                   int dtype, int rule, const void *out_gate, const float *out_norm_weight,
-                  float out_norm_eps, cudaStream_t stream);
+                  float out_norm_eps, int prologue, const float *gate_A, cudaStream_t stream);
 // The output step over `rows` rows of d_v entries of o, in place (prefill paths that do
 // not fuse it).
 int launch_out_norm_gate(void *o, const void *z, const float *w, float eps, int64_t rows, int dv,
                          int dtype, cudaStream_t stream);
+
+// The layer's gate activations (the prologue): log alpha = -A softplus(a), beta = sigmoid(b).
+__device__ __forceinline__ float prologue_log_alpha(float a, float A) {
+    const float sp = a > 20.f ? a : log1pf(expf(a));  // softplus, exact to fp32 beyond 20
+    return -A * sp;
+}
+__device__ __forceinline__ float prologue_beta(float b) { return 1.f / (1.f + expf(-b)); }
+// 1 / max(|x|, 1e-12) from the sum of squares
+__device__ __forceinline__ float prologue_inv_norm(float ss) { return 1.f / fmaxf(sqrtf(ss), 1e-12f); }
 
 // Type helpers for kernels.
 template <typename T> __device__ __forceinline__ float to_f32(T x);

@@ -195,7 +195,7 @@ int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases) {
 template <int DK> struct PrepSmem {
     static constexpr int KP = DK + 1;  // padded row pitch (floats)
     static constexpr int CP = kChunk + 1;
-    static constexpr size_t floats = 2 * kChunk * KP + 4 * kChunk * CP + 3 * kChunk;
+    static constexpr size_t floats = 2 * kChunk * KP + 4 * kChunk * CP + 5 * kChunk;
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
@@ -205,9 +205,12 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
                   const float *__restrict__ log_alpha, const float *__restrict__ beta, int H,
                   int dv, const int4 *__restrict__ plan, const int32_t *__restrict__ ctl,
                   float *__restrict__ Wws, float *__restrict__ Uws, float *__restrict__ Aws,
-                  float *__restrict__ gws, int additive) {
-    // gws receives, per chunk, gamma[C] followed by kdec[C]. With the additive rule the
-    // write does not read the state: L = 0 (so T = diag(beta)) and W = 0.
+                  float *__restrict__ gws, int additive, int prologue,
+                  const float *__restrict__ gate_A) {
+    // gws receives, per chunk, gamma[C], kdec[C], then 1/|q_t| and 1/|k_t| (ones without
+    // the prologue). With the additive rule the write does not read the state: L = 0 (so
+    // T = diag(beta)) and W = 0. With the layer's prologue the rows of q and k are scaled
+    // to unit length here and the gates come from their pre-activations.
     using SM = PrepSmem<DK>;
     constexpr int KP = SM::KP, CP = SM::CP, C = kChunk;
     const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -226,6 +229,8 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     float *al = Gm + C * CP;          // [C] alpha (1 on padding rows)
     float *bs = al + C;               // [C] beta (0 on padding rows)
     float *gam = bs + C;              // [C] gamma
+    float *nq = gam + C;              // [C] 1/|q_t| (prologue), else 1
+    float *nk = nq + C;               // [C] 1/|k_t|
 
     for (int idx = tid; idx < C * DK; idx += blockDim.x) {
         const int t = idx / DK, d = idx % DK;
@@ -242,11 +247,41 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
         float b = 0.f, a = 1.f;
         if (tid < len) {
             const size_t off = (size_t)(t0 + tid) * H + h;
-            b = beta[off];
-            a = expf(log_alpha[off]);
+            if (prologue) {
+                b = prologue_beta(beta[off]);
+                a = expf(prologue_log_alpha(log_alpha[off], gate_A ? gate_A[h] : 1.f));
+            } else {
+                b = beta[off];
+                a = expf(log_alpha[off]);
+            }
         }
         bs[tid] = b;
         al[tid] = a;
+    }
+    __syncthreads();
+    if (prologue) {  // unit-length rows: four threads per row of k and of q
+        const int t = tid >> 2, part = tid & 3;
+        float sk = 0.f, sq = 0.f;
+        for (int d = part; d < DK; d += 4) {
+            sk = fmaf(ks[t * KP + d], ks[t * KP + d], sk);
+            sq = fmaf(qs[t * KP + d], qs[t * KP + d], sq);
+        }
+        sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+        sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+        const float ik = prologue_inv_norm(sk), iq = prologue_inv_norm(sq);
+        for (int d = part; d < DK; d += 4) {
+            ks[t * KP + d] *= ik;
+            qs[t * KP + d] *= iq;
+        }
+        if (part == 0) {
+            nk[t] = ik;
+            nq[t] = iq;
+        }
+    } else if (tid < C) {
+        nk[tid] = 1.f;
+        nq[tid] = 1.f;
     }
     __syncthreads();
     if (tid < C) {  // row t of Gamma by a running product from the diagonal down; then gamma_t
@@ -313,8 +348,10 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     float *Aout = Aws + cb * C * C;
     for (int idx = tid; idx < C * C; idx += blockDim.x) Aout[idx] = Am[(idx / C) * CP + idx % C];
     if (tid < C) {
-        gws[cb * 2 * C + tid] = gam[tid];
-        gws[cb * 2 * C + C + tid] = Gm[(C - 1) * CP + tid];  // kdec_i = Gamma_{C-1,i}
+        gws[cb * 4 * C + tid] = gam[tid];
+        gws[cb * 4 * C + C + tid] = Gm[(C - 1) * CP + tid];  // kdec_i = Gamma_{C-1,i}
+        gws[cb * 4 * C + 2 * C + tid] = nq[tid];
+        gws[cb * 4 * C + 3 * C + tid] = nk[tid];
     }
 }
 
@@ -326,7 +363,7 @@ template <int DK> struct ChainSmem {
     static constexpr int KP = DK + 1;
     static constexpr int SP = kChainCols + 1;
     static constexpr size_t floats = DK * SP + 3 * kChunk * KP + kChunk * (kChunk + 1) +
-                                     kChunk * SP + 3 * kChunk;
+                                     kChunk * SP + 5 * kChunk;
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
@@ -366,6 +403,7 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     float *Uc = Ac + C * CP;     // [C][SP]  Utilde, then U
     float *gam = Uc + C * SP;    // [C] gamma_t
     float *kdec = gam + C;       // [C] Gamma_{C-1,i}
+    float *nqk = kdec + C;       // [2][C] 1/|q_t|, 1/|k_t| (the prologue; else 1)
 
     const size_t s_base = ((size_t)n * H + h) * DK * dv;
     for (int idx = tid; idx < DK * NC; idx += blockDim.x) {
@@ -378,14 +416,16 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         const size_t cb = (size_t)(c_first + cc) * H + h;
         const int64_t tc0 = t_begin + (int64_t)cc * C;
         const int len = (int)((t_end - tc0) < C ? (t_end - tc0) : C);
+        if (tid < 2 * C) nqk[tid] = gws[cb * 4 * C + 2 * C + tid];
+        __syncthreads();
         for (int idx = tid; idx < C * DK; idx += blockDim.x) {
             const int t = idx / DK, d = idx % DK;
             Wc[t * KP + d] = Wws[cb * C * DK + idx];
             float kv = 0.f, qv = 0.f;
             if (t < len) {
                 const size_t off = ((size_t)(tc0 + t) * H + h) * DK + d;
-                kv = to_f32(k[off]);
-                qv = to_f32(q[off]);
+                kv = to_f32(k[off]) * nqk[C + t];
+                qv = to_f32(q[off]) * nqk[t];
             }
             ks[t * KP + d] = kv;
             qs[t * KP + d] = qv;
@@ -397,8 +437,8 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             Uc[t * SP + j] = Uws[cb * C * dv + (size_t)t * dv + j0 + j];
         }
         if (tid < C) {
-            gam[tid] = gws[cb * 2 * C + tid];
-            kdec[tid] = gws[cb * 2 * C + C + tid];
+            gam[tid] = gws[cb * 4 * C + tid];
+            kdec[tid] = gws[cb * 4 * C + C + tid];
         }
         __syncthreads();
 
@@ -484,7 +524,8 @@ static int launch_exact_t(const PrefillArgs &a, const WsLayout &L) {
         dim3 grid((unsigned)L.max_chunks, (unsigned)a.H);
         exact_prep_kernel<Tin, DK><<<grid, 256, PrepSmem<DK>::bytes, a.stream>>>(
             (const Tin *)a.q, (const Tin *)a.k, (const Tin *)a.v, a.log_alpha, a.beta, a.H, a.dv,
-            (const int4 *)(a.ws + L.plan), ctl, W, U, A, g, a.rule == GDR_RULE_ADDITIVE ? 1 : 0);
+            (const int4 *)(a.ws + L.plan), ctl, W, U, A, g, a.rule == GDR_RULE_ADDITIVE ? 1 : 0,
+            a.prologue, a.gate_A);
         e = cudaGetLastError();
         if (e != cudaSuccess) return GDR_ERR_CUDA;
     }

@@ -263,6 +263,7 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     p.ctl = (int32_t *)(a.ws + L.ctl);
     p.flags = flags;
     p.additive = a.rule == GDR_RULE_ADDITIVE;
+    p.prologue = a.prologue;
     if (a.dv == NV) {  // the output step fused into the chain's epilogue
         p.out_gate = (const __nv_bfloat16 *)a.out_gate;
         p.out_norm_weight = a.out_norm_weight;
@@ -282,6 +283,8 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     sp.flags = flags;
     sp.unit_counter = counters;
     sp.additive = a.rule == GDR_RULE_ADDITIVE;
+    sp.prologue = a.prologue;
+    sp.gate_A = a.gate_A;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
@@ -353,6 +356,7 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
     p.o = (__nv_bfloat16 *)a.o;
     p.ctl = (int32_t *)(a.ws + L.ctl);
     p.additive = a.rule == GDR_RULE_ADDITIVE;
+    p.prologue = a.prologue;
     if (a.dv == NV) {  // the output step fused into the chain's epilogue
         p.out_gate = (const __nv_bfloat16 *)a.out_gate;
         p.out_norm_weight = a.out_norm_weight;

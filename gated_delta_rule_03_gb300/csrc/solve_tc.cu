@@ -32,6 +32,8 @@ int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &
     p.phase = phase;
     p.unit_counter = reinterpret_cast<int32_t *>(a.ws + L.F) + phase;
     p.additive = a.rule == GDR_RULE_ADDITIVE;
+    p.prologue = a.prologue;
+    p.gate_A = a.gate_A;
     if (cudaFuncSetAttribute(tc_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
         return GDR_ERR_CUDA;

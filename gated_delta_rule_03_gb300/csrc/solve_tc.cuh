@@ -15,8 +15,11 @@
 //   A^T_it = exp(g_t - g_i) k_i.q_t                 in the exponential form,
 // both stored as bf16 [64][64] row-major: matrix 2u is T' and 2u + 1 is A^T of unit u,
 // units ordered chunk-major, head-minor. Each unit's decay factors go out with them
-// (fp32 [256]: g[64], gamma[64], kdec[64], then 1 for the ratio form and 0 otherwise),
-// so that the chain kernel uses the same values and the same form. (The two forms are
+// (fp32 [384]: g[64], gamma[64], kdec[64], then 1 for the ratio form and 0 otherwise,
+// then the layer prologue's 1/|k_t| and 1/|q_t|, ones without it), so that the chain
+// kernel uses the same values and the same form. With the prologue, L is formed from
+// unit-length keys (k_t.k_i / (|k_t| |k_i|)); A^T stays the raw products, the chain
+// applying 1/|k_i| through the pseudo-values and 1/|q_t| on the output rows. (The two forms are
 // described in chain_tc.cuh; they differ only in where the decay factors are applied.)
 //
 // Mapping. Each warpgroup of a CTA solves one (chunk, head) unit at a time, on its own:
@@ -79,8 +82,10 @@ constexpr int UNIT_FLOATS = 16 * BS;
 constexpr uint32_t G_K = 0, G_Q = 16384;
 constexpr uint32_t G_BLK = 32768;
 constexpr uint32_t G_GATES = G_BLK + UNIT_FLOATS * 4;
-constexpr int GG_G = 0, GG_GAM = 64, GG_GINV = 128, GG_BETA = 192, GG_KDEC = 256;  // floats
-constexpr uint32_t G_BAR = G_GATES + 5 * 64 * 4;
+constexpr int GG_G = 0, GG_GAM = 64, GG_GINV = 128, GG_BETA = 192, GG_KDEC = 256,
+              GG_NK = 320, GG_NQ = 384;  // floats
+constexpr uint32_t G_BAR = G_GATES + 7 * 64 * 4;
+constexpr int kFactorFloats = 384;  // per unit in the workspace
 constexpr uint32_t G_NEXT = G_BAR + 8;
 constexpr uint32_t GROUP_BYTES = (G_NEXT + 8 + 1023) / 1024 * 1024;
 constexpr uint32_t SMEM_BYTES = kGroups * GROUP_BYTES + 1024;
@@ -179,8 +184,10 @@ struct SolveParams {
     int32_t *flags;
     int32_t *unit_counter;  // units are claimed from it at run time (zeroed by the plan)
     int additive;           // the additive rule: L = 0, so T = diag(beta)
+    int prologue;           // the layer prologue: unit-length q, k; gates from a, b
+    const float *gate_A;    // its per-head rate (null: 1)
     __nv_bfloat16 *Tout;  // [chunks * H][2][64][64]: T' then A^T per unit
-    float *Gout;          // [chunks * H][256]: g, gamma, kdec, form flag per unit
+    float *Gout;          // [chunks * H][kFactorFloats]: g, gamma, kdec, form, 1/|k|, 1/|q|
 };
 
 // One warp's part of the solve: warp W of a group (block row W of every unit), its loop
@@ -227,19 +234,21 @@ struct GroupSolver {
         gv[0] = gv[1] = gv[2] = gv[3] = 0.f;
         if (x < 0) return;
         const int h = unit_at(x) % p.H;
-        if (2 * lane < len) {
-            const size_t off = (size_t)(first + 2 * lane) * p.H + h;
-            gv[0] = p.log_alpha[off];
-            gv[2] = p.beta[off];
-        }
-        if (2 * lane + 1 < len) {
-            const size_t off = (size_t)(first + 2 * lane + 1) * p.H + h;
-            gv[1] = p.log_alpha[off];
-            gv[3] = p.beta[off];
+        const float A = p.prologue && p.gate_A ? p.gate_A[h] : 1.f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            if (2 * lane + e < len) {
+                const size_t off = (size_t)(first + 2 * lane + e) * p.H + h;
+                const float a = p.log_alpha[off], b = p.beta[off];
+                gv[e] = p.prologue ? prologue_log_alpha(a, A) : a;
+                gv[2 + e] = p.prologue ? prologue_beta(b) : b;
+            }
         }
     }
 
-    template <int W>
+    // kPro: the layer prologue (a template parameter, so that the plain path carries none
+    // of its work)
+    template <int W, bool kPro>
     __device__ __forceinline__ void run() const {
         const int gq = lane >> 2, q = lane & 3;  // m16n8 fragment coordinates
         const bool leader = W == 0 && lane == 0;
@@ -279,6 +288,33 @@ struct GroupSolver {
             if (*gfail) break;
             if (leader) ++landed;
             const bool ratio = gt[GG_G + C - 1] > kRatioSafeLogDecay;
+            // 1/|k_r| (threads 0-63 of the group) and 1/|q_r| (64-127): the prologue's unit
+            // lengths, from the staged rows; ones without it
+            if (kPro) {
+                const int i = 32 * W + lane, r = i & 63;
+                float inv = 1.f;
+                {
+                    const uint32_t tile = gbase + (i < 64 ? G_K : G_Q);
+                    float ss = 0.f;
+#pragma unroll
+                    for (int b = 0; b < 2; ++b)
+#pragma unroll
+                        for (int s = 0; s < 8; ++s) {
+                            uint4 u;
+                            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                                         : "r"(sw128_at(tile + b * 8192, r, s)));
+                            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&uw[e]));
+                                ss = fmaf(x.x, x.x, fmaf(x.y, x.y, ss));
+                            }
+                        }
+                    inv = prologue_inv_norm(ss);
+                }
+                gt[(i < 64 ? GG_NK : GG_NQ) + r] = inv;
+            }
 
             // ---- rows 16W .. 16W + 15 of K K^T (keys i < 16W + 16) and of K Q^T (queries
             // t >= 16W): ten 8-column tiles; tile pair j2 <= W holds keys 16 j2 .. 16 j2 + 15,
@@ -304,6 +340,7 @@ struct GroupSolver {
                     mma_bf16_16x8x16(acc[2 * j2 + 1], a, bf[2], bf[3]);
                 }
             }
+            if (kPro) gsync();  // every row's 1/|k| is in place
             // the gates this warp needs: its rows' (t = 16W + gq + 8hh) and the columns' of
             // its tiles (i0 = 8j + 2q, two each)
             float rg[2], rb[2], rgi[2], rkd[2], cg[8][2];
@@ -312,7 +349,8 @@ struct GroupSolver {
                 const int t = 16 * W + gq + 8 * hh;
                 rg[hh] = ratio ? gt[GG_GAM + t] : gt[GG_G + t];
                 rgi[hh] = gt[GG_G + t];
-                rb[hh] = p.additive ? 0.f : gt[GG_BETA + t];  // L = 0 for the additive rule
+                // L = 0 for the additive rule; 1/|k_t| of the prologue folded into beta_t
+                rb[hh] = p.additive ? 0.f : (kPro ? gt[GG_BETA + t] * gt[GG_NK + t] : gt[GG_BETA + t]);
                 rkd[hh] = ratio ? gt[GG_KDEC + t] : 1.f;
             }
 #pragma unroll
@@ -332,8 +370,9 @@ struct GroupSolver {
                     const int t = 16 * W + gq + 8 * hh;
                     const float d0 = ratio ? rg[hh] * cg[j][0] : fast_exp(rg[hh] - cg[j][0]);
                     const float d1 = ratio ? rg[hh] * cg[j][1] : fast_exp(rg[hh] - cg[j][1]);
-                    const float v0 = i0 < t ? rb[hh] * d0 * acc[j][2 * hh] : 0.f;
-                    const float v1 = i0 + 1 < t ? rb[hh] * d1 * acc[j][2 * hh + 1] : 0.f;
+                    const float nk0 = kPro ? gt[GG_NK + i0] : 1.f, nk1 = kPro ? gt[GG_NK + i0 + 1] : 1.f;
+                    const float v0 = i0 < t ? rb[hh] * d0 * nk0 * acc[j][2 * hh] : 0.f;
+                    const float v1 = i0 + 1 < t ? rb[hh] * d1 * nk1 * acc[j][2 * hh + 1] : 0.f;
                     *reinterpret_cast<float2 *>(B + el(gq + 8 * hh, 8 * (j & 1) + 2 * q)) = make_float2(v0, v1);
                 }
             }
@@ -358,14 +397,19 @@ struct GroupSolver {
                 const int idx = lane + 32 * s, r = 16 * W + (idx & 15), seg = idx >> 4;
                 *reinterpret_cast<uint4 *>(arow + r * C + 8 * seg) = make_uint4(0, 0, 0, 0);
             }
-            // the unit's decay factors for the chain: g (warp 0), gamma (1), kdec (2), form (3)
+            // the unit's decay factors for the chain: g (warp 0), gamma (1), kdec (2), form (3);
+            // 1/|k| (warp 0) and 1/|q| (warp 1)
             {
+                float *go = p.Gout + (size_t)u * kFactorFloats;
                 float2 v;
                 if (W == 0) v = *reinterpret_cast<const float2 *>(gt + GG_G + 2 * lane);
                 else if (W == 1) v = *reinterpret_cast<const float2 *>(gt + GG_GAM + 2 * lane);
                 else if (W == 2) v = *reinterpret_cast<const float2 *>(gt + GG_KDEC + 2 * lane);
                 else v = make_float2(lane == 0 ? (ratio ? 1.f : 0.f) : 0.f, 0.f);
-                *reinterpret_cast<float2 *>(p.Gout + (size_t)u * 256 + 64 * W + 2 * lane) = v;
+                *reinterpret_cast<float2 *>(go + 64 * W + 2 * lane) = v;
+                if (kPro && W < 2)  // (the chain reads them only with the prologue)
+                    *reinterpret_cast<float2 *>(go + 256 + 64 * W + 2 * lane) =
+                        *reinterpret_cast<const float2 *>(gt + (W == 0 ? GG_NK : GG_NQ) + 2 * lane);
             }
             if (leader) *next = xn;
             gsync();  // keys and queries are read; L is complete; the next unit is known
@@ -530,10 +574,10 @@ __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUten
                                   reinterpret_cast<float *>(gs + G_BLK), reinterpret_cast<float *>(gs + G_GATES),
                                   next, next + 1, grp, lane, u0, n_units};
     switch (w) {
-        case 0: gsv.template run<0>(); break;
-        case 1: gsv.template run<1>(); break;
-        case 2: gsv.template run<2>(); break;
-        default: gsv.template run<3>(); break;
+        case 0: p.prologue ? gsv.template run<0, true>() : gsv.template run<0, false>(); break;
+        case 1: p.prologue ? gsv.template run<1, true>() : gsv.template run<1, false>(); break;
+        case 2: p.prologue ? gsv.template run<2, true>() : gsv.template run<2, false>(); break;
+        default: p.prologue ? gsv.template run<3, true>() : gsv.template run<3, false>(); break;
     }
 }
 

@@ -23,16 +23,29 @@ class GdrOptions(ctypes.Structure):
     """struct gdr_options of gdr.h."""
     _fields_ = [("rule", ctypes.c_int), ("out_norm_eps", ctypes.c_float),
                 ("out_gate", ctypes.c_void_p), ("out_norm_weight", ctypes.c_void_p),
-                ("reserved", ctypes.c_int * 4)]
+                ("prologue", ctypes.c_int), ("reserved", ctypes.c_int),
+                ("gate_A", ctypes.c_void_p)]
 
 
-def _options(rule, out_gate=None, out_norm_weight=None, out_norm_eps=0.0):
+def _options(rule, out_gate=None, out_norm_weight=None, out_norm_eps=0.0, prologue=False,
+             gate_A=None):
     if rule not in RULES:
         raise ValueError(f"unknown rule {rule!r}; expected one of {sorted(RULES)}")
     opt = GdrOptions(RULES[rule], float(out_norm_eps) if out_gate is not None else 0.0,
                      None if out_gate is None else out_gate.data_ptr(),
-                     None if out_norm_weight is None else out_norm_weight.data_ptr())
+                     None if out_norm_weight is None else out_norm_weight.data_ptr(),
+                     1 if prologue else 0, 0, None if gate_A is None else gate_A.data_ptr())
     return ctypes.byref(opt)
+
+
+def _check_prologue(prologue, gate_A, H, device):
+    if gate_A is None:
+        return
+    if not prologue:
+        raise ValueError("gate_A needs prologue=True")
+    _need(gate_A, "gate_A", torch.float32, device)
+    if gate_A.numel() != H:
+        raise ValueError(f"gate_A must have {H} entries")
 
 
 def _check_out_step(out_gate, out_norm_weight, like, dv):
@@ -139,7 +152,7 @@ def chunk_fwd_workspace_size(num_seqs, total_tokens, H, dk, dv, chunk=64, dtype=
 
 def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None, chunk=64,
               o=None, S_final=None, workspace=None, stream=None, rule="delta", out_gate=None,
-              out_norm_weight=None, out_norm_eps=1e-6):
+              out_norm_weight=None, out_norm_eps=1e-6, prologue=False, gate_A=None):
     """Chunked prefill (gdr_chunk_fwd).
 
     q, k [T, H, dk]; v [T, H, dv] (fp32 or bf16); log_alpha, beta [T, H] fp32;
@@ -148,7 +161,10 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
     S_final and workspace (uint8) tensors are used as given. rule: "delta" (the gated
     delta rule) or "additive" (S <- alpha S + beta k v^T). out_gate [T, H, dv] (o's
     dtype): apply the layer's output step o <- o / rms(o) * out_norm_weight * silu(out_gate)
-    over each head's dv entries (gdr_options in gdr.h). Returns (o, S_final).
+    over each head's dv entries. prologue=True: q and k are raw (scaled to unit length in
+    the kernels) and log_alpha, beta hold the gate pre-activations a, b (log alpha =
+    -gate_A[h] softplus(a), beta = sigmoid(b)); see gdr_options in gdr.h. Returns
+    (o, S_final).
     """
     lib = _load()
     _need(q, "q")
@@ -175,6 +191,7 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
     _need(o, "o", dt, dev)
     _need(S_final, "S_final", torch.float32, dev)
     _check_out_step(out_gate, out_norm_weight, o, dv)
+    _check_prologue(prologue, gate_A, H, dev)
     ws_bytes = chunk_fwd_workspace_size(n, T, H, dk, dv, chunk, dt)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
@@ -183,7 +200,8 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
                               _ptr(cu_seqlens), n, T, H, dk, dv, int(chunk), _DTYPES[dt], _ptr(o),
                               _ptr(S_final), _ptr(workspace),
                               workspace.numel() * workspace.element_size(),
-                              _options(rule, out_gate, out_norm_weight, out_norm_eps),
+                              _options(rule, out_gate, out_norm_weight, out_norm_eps, prologue,
+                                       gate_A),
                               _stream_handle(stream, dev))
     _check(st, "gdr_chunk_fwd_ex")
     return o, S_final
@@ -199,7 +217,7 @@ def read_device_status(workspace, stream=None):
 
 
 def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None, rule="delta", out_gate=None,
-                out_norm_weight=None, out_norm_eps=1e-6):
+                out_norm_weight=None, out_norm_eps=1e-6, prologue=False, gate_A=None):
     """One decode step (gdr_decode_step_ex): q, k [N, H, dk]; v [N, H, dv];
     log_alpha, beta [N, H] fp32; S [N, H, dk, dv] fp32 updated in place; rule "delta"
     (the gated delta rule) or "additive" (S <- alpha S + beta k v^T). Returns o [N, H, dv]."""
@@ -217,9 +235,11 @@ def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None, rule="delta", 
         o = torch.empty((N, H, dv), dtype=dt, device=dev)
     _need(o, "o", dt, dev)
     _check_out_step(out_gate, out_norm_weight, o, dv)
+    _check_prologue(prologue, gate_A, H, dev)
     st = lib.gdr_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S),
                                 _ptr(o), N, H, dk, dv, _DTYPES[dt],
-                                _options(rule, out_gate, out_norm_weight, out_norm_eps),
+                                _options(rule, out_gate, out_norm_weight, out_norm_eps, prologue,
+                                         gate_A),
                                 _stream_handle(stream, dev))
     _check(st, "gdr_decode_step_ex")
     return o

@@ -200,13 +200,27 @@ enum { GDR_RULE_DELTA = 0, GDR_RULE_ADDITIVE = 1 };
  *                    be null and zero). The state is not affected.
  *   out_norm_weight  w: [d_v] fp32, 16-byte aligned; null means all ones.
  *   out_norm_eps     eps >= 0 (finite); 0 means 1e-6.
+ *   prologue         GDR_PROLOGUE_NONE (q, k, log_alpha and beta are used as given)
+ *                    or GDR_PROLOGUE_LAYER: the layer's steps before the recurrence
+ *                    ("Linear attention", "A naive PyTorch implementation") run
+ *                    inside the kernels. q and k are then the raw projections and
+ *                    each token's head vector is scaled to unit length,
+ *                    x / max(|x|, 1e-12); the log_alpha argument holds the forget
+ *                    gate's pre-activation a and beta holds the write gate's b, and
+ *                      log alpha = -A_h softplus(a),   beta = sigmoid(b).
+ *   gate_A           A: [H] fp32 per-head rate (A_h > 0; the layer keeps log A and
+ *                    exponentiates it), 4-byte aligned; null means all ones. Only
+ *                    with GDR_PROLOGUE_LAYER.
  */
+enum { GDR_PROLOGUE_NONE = 0, GDR_PROLOGUE_LAYER = 1 };
 typedef struct gdr_options {
     int rule;
     float out_norm_eps;
     const void *out_gate;
     const float *out_norm_weight;
-    int reserved[4];
+    int prologue;
+    int reserved;
+    const float *gate_A;
 } gdr_options;
 
 /*

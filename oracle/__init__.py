@@ -123,3 +123,21 @@ def out_norm_gate(o, gate, weight=None, eps=1e-6):
     w = np.ones(o.shape[-1]) if weight is None else _f64(weight)
     rms = np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
     return o / rms * w * (g / (1.0 + np.exp(-g)))
+
+
+def layer_prologue(q, k, a, b, A=None):
+    """The layer's steps before the recurrence, in float64 ("Linear attention"
+    (arsalanzafar.ai), "A naive PyTorch implementation"): each token's query and key
+    vector per head scaled to unit length (x / max(|x|, 1e-12), as F.normalize), and the
+    gates from their pre-activations,
+
+        log alpha = -A_h softplus(a),    beta = sigmoid(b),
+
+    q, k [..., H, d_k]; a, b [..., H]; A [H] (None: ones). Returns (q, k, log_alpha, beta)
+    for forward() / decode()."""
+    q, k, a, b = _f64(q), _f64(k), _f64(a), _f64(b)
+    A = np.ones(a.shape[-1]) if A is None else _f64(A)
+    qn = q / np.maximum(np.linalg.norm(q, axis=-1, keepdims=True), 1e-12)
+    kn = k / np.maximum(np.linalg.norm(k, axis=-1, keepdims=True), 1e-12)
+    softplus = np.logaddexp(0.0, a)
+    return qn, kn, -A * softplus, 1.0 / (1.0 + np.exp(-b))

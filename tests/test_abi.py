@@ -128,7 +128,7 @@ def test_options_validated_on_the_host(lib):
 
     bad_rule = GdrOptions(2)
     reserved = GdrOptions(1)
-    reserved.reserved[3] = 1
+    reserved.reserved = 1
     for f in (call, dcall):
         assert f(ctypes.byref(bad_rule)) == -2
         assert f(ctypes.byref(reserved)) == -1
@@ -144,6 +144,14 @@ def test_options_validated_on_the_host(lib):
         assert f(ctypes.byref(o2)) == -1
         assert f(ctypes.byref(o3)) == -1
         assert f(ctypes.byref(o4)) == -3
+    # the prologue: an unknown kind, a rate without it, an unaligned rate
+    p1 = GdrOptions(0, 0.0, None, None, 2, 0, None)
+    p2 = GdrOptions(0, 0.0, None, None, 0, 0, A + 0x8000000)
+    p3 = GdrOptions(0, 0.0, None, None, 1, 0, A + 0x8000002)
+    for f in (call, dcall):
+        assert f(ctypes.byref(p1)) == -2
+        assert f(ctypes.byref(p2)) == -1
+        assert f(ctypes.byref(p3)) == -3
     # a valid options block gets as far as the argument checks of the plain entry points
     ok = GdrOptions(1)
     assert lib.gdr_chunk_fwd_ex(None, p[1], p[2], p[3], p[4], None, None, 1, 128, 2, 64, 64, 64,

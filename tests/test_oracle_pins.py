@@ -427,3 +427,35 @@ def test_out_norm_gate_weight_eps_and_scale():
     np.testing.assert_array_equal(z, 0.0)
     t = oracle.out_norm_gate(np.full((1, 4), 1e-4), np.full((1, 4), 40.0), eps=1e-6)
     np.testing.assert_allclose(t, 1e-4 / np.sqrt(1e-8 + 1e-6) * 40.0, rtol=1e-13)
+
+
+# --------------------------------------------------------------------------- layer prologue
+
+def test_layer_prologue_closed_forms():
+    # q = [3, 4] has length 5; softplus(0) = ln 2, sigmoid(0) = 1/2; A scales log alpha;
+    # softplus(a) -> a for large a and -> e^a for very negative a
+    q = np.array([[[3.0, 4.0]], [[0.0, 0.0]]])
+    k = np.array([[[1.0, 0.0]], [[0.0, 2.0]]])
+    a = np.array([[0.0], [30.0]])
+    b = np.array([[0.0], [np.log(3.0)]])
+    qn, kn, la, beta = oracle.layer_prologue(q, k, a, b, A=np.array([2.0]))
+    np.testing.assert_allclose(qn[0, 0], [0.6, 0.8], rtol=1e-15)
+    np.testing.assert_array_equal(qn[1, 0], [0.0, 0.0])        # zero stays zero (max(|x|, eps))
+    np.testing.assert_allclose(kn[1, 0], [0.0, 1.0], rtol=1e-15)
+    np.testing.assert_allclose(la[:, 0], [-2 * np.log(2.0), -2 * (30.0 + np.log1p(np.exp(-30.0)))],
+                               rtol=1e-15)
+    np.testing.assert_allclose(beta[:, 0], [0.5, 0.75], rtol=1e-15)
+    _, _, la2, _ = oracle.layer_prologue(q, k, np.array([[-40.0], [0.0]]), b)
+    np.testing.assert_allclose(la2[0, 0], -np.exp(-40.0), rtol=1e-12)
+
+
+def test_layer_prologue_makes_unit_vectors_and_gates_in_range():
+    rng = np.random.default_rng(11)
+    q, k = 5 * rng.standard_normal((2, 7, 3, 16))
+    a, b = 3 * rng.standard_normal((2, 7, 3))
+    qn, kn, la, beta = oracle.layer_prologue(q, k, a, b, A=rng.uniform(0.1, 4.0, 3))
+    np.testing.assert_allclose(np.linalg.norm(qn, axis=-1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(np.linalg.norm(kn, axis=-1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(qn * np.linalg.norm(q, axis=-1, keepdims=True), q, rtol=1e-13)
+    assert (la < 0).all() and (np.exp(la) < 1).all()
+    assert (beta > 0).all() and (beta < 1).all()
