@@ -149,6 +149,19 @@ struct TcParams {
     const int32_t *flags;      // fused launch: per solve unit, set once the unit is solved
     int additive;              // the additive rule: W' = 0 (the state does not enter U')
     int prologue;              // the layer prologue: 1/|k|, 1/|q| from the factors apply
+    // Segments of the sequences (the segmented schedule): mode 0 is the plain chain of a
+    // (sequence, head, slice) over this launch's phase. Mode 1 runs, for every segment f
+    // but the last (the phase f of `phases`), the segment's transition P_f (one more
+    // slice: zero values from the identity; d_k = NV) and its local state R_f (the value
+    // slices from zero), without output. Mode 2 runs every segment f from its start
+    // state S_start[f] (a copy of S_in for the first, so that S_out may be S_in), with
+    // output; the last segment's state goes to S_out, the others' to S_discard. Every
+    // per-segment buffer holds [segment][sequence * H + head][d_k][d_v] (P_f in columns
+    // [0, d_k)).
+    int mode;
+    float *S_P, *S_R;
+    const float *S_start;
+    float *S_discard;
     // the layer's output step on o (null out_gate: none; only when d_v = NV, one slice)
     const __nv_bfloat16 *out_gate;
     const float *out_norm_weight;
@@ -225,8 +238,38 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    const int slice = cta % p.n_slices;
-    const int nh = cta / p.n_slices;
+    // this CTA's chain: segment (phase), sequence-head, value slice; state in and out
+    const int NH = (int)p.num_seqs * p.H;
+    const size_t mat_floats = (size_t)DK * p.dv;
+    int phase = p.phase, slice, nh;
+    bool zero_v = false, no_out = false;  // mode 1: the transition slice / no output
+    const int32_t *seq_chunk = p.seq_chunk;
+    const float *S_in_m;  // this chain's [d_k][d_v] start state, or null (zero)
+    float *S_out_m;       // where its end state goes
+    if (p.mode == 0) {
+        slice = cta % p.n_slices;
+        nh = cta / p.n_slices;
+        S_in_m = p.S_in ? p.S_in + nh * mat_floats : nullptr;
+        S_out_m = p.S_out + nh * mat_floats;
+    } else {
+        const int per = p.n_slices + (p.mode == 1 ? 1 : 0);
+        phase = cta / (NH * per);
+        nh = (cta % (NH * per)) / per;
+        const int s1 = cta % per;
+        seq_chunk = p.seq_chunk + (size_t)phase * (p.num_seqs + 1);
+        const size_t mat = ((size_t)phase * NH + nh) * mat_floats;
+        if (p.mode == 1) {
+            zero_v = s1 == 0;
+            no_out = true;
+            slice = zero_v ? 0 : s1 - 1;
+            S_in_m = nullptr;  // (the transition starts from the identity)
+            S_out_m = (zero_v ? p.S_P : p.S_R) + mat;
+        } else {
+            slice = s1;
+            S_in_m = p.S_start + mat;
+            S_out_m = phase == p.phases - 1 ? p.S_out + nh * mat_floats : p.S_discard + mat;
+        }
+    }
     const int n = nh / p.H, h = nh % p.H;
     int64_t seq_begin, seq_end;
     if (p.cu_seqlens) {
@@ -239,8 +282,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
     }
     // this phase's chunks of the sequence: local chunk c is the sequence's chunk cb + c
     const int64_t m = (seq_end - seq_begin + C - 1) / C;
-    const int64_t cb = (int64_t)p.phase * m / p.phases;
-    const int n_chunks = (int)((int64_t)(p.phase + 1) * m / p.phases - cb);
+    const int64_t cb = (int64_t)phase * m / p.phases;
+    const int n_chunks = (int)((int64_t)(phase + 1) * m / p.phases - cb);
     seq_begin += cb * C;
     const int col0 = slice * NV;  // first value column of this CTA
     auto chunk_len = [&](int c) {
@@ -303,16 +346,18 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
     } else if (warp == kProducerWarp) {
         // ============================================================ producer
         if (lane == 0) {
-            const int unit0 = p.seq_chunk[n] * p.H + h;  // chunk c is solve unit unit0 + c * H
+            const int unit0 = seq_chunk[n] * p.H + h;  // chunk c is solve unit unit0 + c * H
             for (int c = 0; c < n_chunks; ++c) {
                 const int tt = (int)(seq_begin + (int64_t)c * C), unit = unit0 + c * p.H;
                 if (kFused && !wait_unit_solved(p.flags + unit, p.ctl)) { note_fail(3); break; }
                 // V, T' (slot free once U'~ and W' of chunk c - 2 are done)
                 if (c >= 2 && !mbar_wait(bar(B_VE0 + (c & 1)), ((c >> 1) - 1) & 1)) { note_fail(3); break; }
                 const uint32_t vs = sbase + vslot(c), vf = bar(B_VF0 + (c & 1));
-                mbar_arrive_expect_tx(vf, 3 * 8192);
-                tma_load_3d(vs, &map_v, vf, col0, h, tt);
-                tma_load_3d(vs + 8192, &map_v, vf, col0 + 64, h, tt);
+                mbar_arrive_expect_tx(vf, zero_v ? 8192 : 3 * 8192);
+                if (!zero_v) {  // (the transition slice has zero values)
+                    tma_load_3d(vs, &map_v, vf, col0, h, tt);
+                    tma_load_3d(vs + 8192, &map_v, vf, col0 + 64, h, tt);
+                }
                 tma_load_3d(vs + RV_T, &map_t, vf, 0, 0, 2 * unit);
                 // K, A^T, factors (slot free once chunk c - 3 is done)
                 if (c >= 3 && !mbar_wait(bar(B_KE0 + c % 3), (c / 3 - 1) & 1)) { note_fail(3); break; }
@@ -413,7 +458,9 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             }
             fence_async_smem();
             named_sync(kBarEpi, kEpiThreads);
-            if (len == C) {
+            if (no_out) {
+                // a segment summary: no output
+            } else if (len == C) {
                 if (etid == 0) {
                     tma_store_3d(&map_o, stg, col0, h, (int)t0);
                     tma_store_3d(&map_o, stg + 8192, col0 + 64, h, (int)t0);
@@ -555,10 +602,12 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                              sw128_desc(sbase + OFF_TG + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0),
                              kk > 0);
                 mma_commit(bar(B_WD0 + (j & 1)));
+                if (!zero_v) {  // U'~ = T'V (zero for the transition slice, never read)
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM_U + 64 * (j & 1), sw128_desc(vs + kk * 2048, 8192, 1024),
-                             sw128_desc(vs + RV_T + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + TM_U + 64 * (j & 1), sw128_desc(vs + kk * 2048, 8192, 1024),
+                                 sw128_desc(vs + RV_T + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
+                }
                 // U'~ needs no barrier of its own: the state reads it after B_WS, which
                 // this thread commits after these MMAs
                 mma_commit(bar(B_VE0 + (j & 1)));  // V and T' are read
@@ -631,16 +680,18 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
         };
         // this thread's 64 entries of S^T: lane col0 + row, d_k columns [64*half, 64*half + 64);
         // they live in the fp32 master in TMEM
-        const size_t s_off = ((size_t)n * p.H + h) * DK * p.dv + col0 + row;
+        const size_t s_off = col0 + row;  // within this chain's [d_k][d_v] matrix
         const uint32_t s_tm = lane_base + TM_S + 64 * half;
-        {  // the incoming state (or zero) into the master; the same thread later writes
-           // the same entries of S_out, so S_out may be S_in
-            const float *src = p.S_in ? p.S_in + s_off + (size_t)(64 * half) * p.dv : nullptr;
+        {  // the incoming state (zero, or the identity for a transition) into the master;
+           // the same thread later writes the same entries of S_out, so S_out may be S_in
+            const float *src = S_in_m ? S_in_m + s_off + (size_t)(64 * half) * p.dv : nullptr;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 float x[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = src ? src[(size_t)(32 * hh + i) * p.dv] : 0.f;
+                for (int i = 0; i < 32; ++i)
+                    x[i] = src ? src[(size_t)(32 * hh + i) * p.dv]
+                               : (zero_v && 64 * half + 32 * hh + i == row ? 1.f : 0.f);
                 tmem_store32(s_tm + 32 * hh, x);
             }
         }
@@ -653,7 +704,12 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 tc_fence_after();
                 {
                     float a[32], b[32];
-                    tmem_load32(lane_base + TM_U + 64 * (cp & 1) + 32 * half, a);
+                    if (zero_v) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) a[i] = 0.f;
+                    } else {
+                        tmem_load32(lane_base + TM_U + 64 * (cp & 1) + 32 * half, a);
+                    }
                     tmem_load32(lane_base + TM_X + 32 * half, b);
                     uint32_t w[16];
                     if (p.prologue) {  // U'_i 1/|k_i|: the unit-length keys of the state update
@@ -673,7 +729,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 tc_fence_after();
             }
             if (c == n_chunks) {  // the outgoing state (no chunks: the incoming one)
-                float *dst = p.S_out + s_off + (size_t)(64 * half) * p.dv;
+                float *dst = S_out_m + s_off + (size_t)(64 * half) * p.dv;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     float x[32];

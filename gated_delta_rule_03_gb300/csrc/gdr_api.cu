@@ -45,8 +45,13 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
         off = align_up(off + (size_t)L.max_chunks * (size_t)H * 384 * sizeof(float), 256);
         L.S = off;  // the state handed from one phase to the next
         off = align_up(off + (size_t)num_seqs * (size_t)H * dk * dv * sizeof(float), 256);
-        L.F = off;  // the solve's pair counters, then one flag per (chunk, head) unit
+        L.F = off;  // the solve's unit counters, then one flag per (chunk, head) unit
         off = align_up(off + ((size_t)kCounters + (size_t)L.max_chunks * (size_t)H) * sizeof(int32_t), 256);
+        L.segmentable = tc_segmentable(num_seqs, total_tokens, H, dv);
+        L.seg = off;  // the segmented schedule's state sets
+        if (L.segmentable)
+            off = align_up(off + (size_t)(4 * kMaxPhases - 3) * (size_t)num_seqs * H * dk * dv *
+                                     sizeof(float), 256);
     }
     L.total = off;
     return L;
@@ -249,8 +254,11 @@ int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H,
     if (st != GDR_OK) return st;
     if (!use_tensor_path(d_k, d_v, dtype)) return 3;  // plan, per-chunk prep, chain
     if (total_tokens == 0) return 1;  // the plan; the state copy is not a kernel of ours
-    const int n = tc_schedule_launches(num_seqs, total_tokens, H, d_v, varlen != 0);
-    return n < 0 ? GDR_ERR_CUDA : n;
+    const int P = tc_schedule_query(num_seqs, total_tokens, H, d_v, varlen != 0);
+    if (P < 0) return GDR_ERR_CUDA;
+    // fused: plan, cooperative kernel; P phases: plan, P solves, P chains; segmented:
+    // plan, solve, summary chain, scan, chain
+    return P == 0 ? 2 : (P > kSegmentedBase ? 5 : 1 + 2 * P);
 }
 
 int gdr_chunk_fwd_schedule(int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v,
@@ -258,10 +266,8 @@ int gdr_chunk_fwd_schedule(int64_t num_seqs, int64_t total_tokens, int H, int d_
     const int st = check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype);
     if (st != GDR_OK) return st;
     if (!use_tensor_path(d_k, d_v, dtype) || total_tokens == 0) return 1;
-    // the fused schedule is two launches (plan, cooperative kernel); P phases are 1 + 2P
-    const int n = tc_schedule_launches(num_seqs, total_tokens, H, d_v, varlen != 0);
-    if (n < 0) return GDR_ERR_CUDA;
-    return n == 2 ? 0 : (n - 1) / 2;
+    const int P = tc_schedule_query(num_seqs, total_tokens, H, d_v, varlen != 0);
+    return P < 0 ? GDR_ERR_CUDA : P;
 }
 
 int gdr_read_device_status(const void *workspace, int *status, gdr_stream_t stream) {

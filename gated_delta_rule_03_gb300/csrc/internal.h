@@ -13,6 +13,18 @@ namespace gdr {
 constexpr int kChunk = 64;  // tokens per chunk (the only chunk size the kernels support)
 constexpr int kMaxPhases = 8;  // most phases a tensor-core prefill is split into
 constexpr int kCounters = 64;  // int32 words before the unit flags in the F region
+// Schedules of the tensor-core path: 0 fused, 1 .. kMaxPhases phased, kSegmentedBase + n
+// segmented into n segments per sequence.
+constexpr int kSegmentedBase = GDR_SCHEDULE_SEGMENTED;
+// phases of the chunk plan a schedule needs (a segment is a phase)
+inline int plan_phases(int schedule) {
+    return schedule == 0 ? 1 : (schedule > kSegmentedBase ? schedule - kSegmentedBase : schedule);
+}
+// Few chains (sequences x heads x 128-column value slices) over long sequences: the
+// workspace then holds the segmented schedule's state sets.
+inline bool tc_segmentable(int64_t num_seqs, int64_t total_tokens, int H, int dv) {
+    return num_seqs > 0 && num_seqs * H * (dv / 128) <= 38 && total_tokens >= num_seqs * 64 * kChunk;
+}
 
 // Everything gdr_chunk_fwd receives, after host validation.
 struct PrefillArgs {
@@ -49,8 +61,13 @@ struct WsLayout {
     size_t T;             // tensor-core path: bf16 [max_chunks * H][2][64][64] T' and A^T per unit
     size_t G;             // tensor-core path: fp32 [max_chunks * H][256] decay factors per unit
     size_t S;             // tensor-core path: fp32 [num_seqs][H][dk][dv] state between phases
-    size_t F;             // tensor-core path: int32 [kCounters] pair counters (one per phase),
-                          // then [max_chunks * H] unit-solved flags (fused schedule)
+    size_t F;             // tensor-core path: int32 [kCounters] unit counters (one per phase,
+                          // then one for a solve of every unit), then [max_chunks * H]
+                          // unit-solved flags (fused schedule)
+    size_t seg;           // tensor-core path, few long chains: the segmented schedule's
+                          // fp32 state sets, [NH][d_k][d_v] each: (kMaxPhases - 1) each
+                          // of P, R and discard, kMaxPhases of start; 0 bytes otherwise
+    bool segmentable;
     size_t total;
     bool tensor_path;     // bf16 tensor-core kernel (true) or exact fp32-arithmetic kernels
 };
@@ -59,21 +76,22 @@ bool use_tensor_path(int dk, int dv, int dtype);
 WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype);
 
 // Launchers (return GDR_OK or GDR_ERR_CUDA).
-// The planning kernel, for `phases` phases (a phase count of 0, the fused schedule, plans
-// one phase and clears the unit flags).
+// The planning kernel for a schedule (the fused schedule, 0, plans one phase and clears
+// the unit flags; the segmented one plans a phase per segment).
 int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases);
 int launch_prefill_exact(const PrefillArgs &a, const WsLayout &L);
 int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases);
 
-// The schedule of a tensor-core prefill: 0 for the fused cooperative launch, else the
-// number of phases (1 .. kMaxPhases) of the two-kernel schedule.
+// The schedule of a tensor-core prefill: 0 for the fused cooperative launch,
+// 1 .. kMaxPhases phases of the two-kernel schedule, or kSegmentedBase + n for n
+// segments per sequence.
 int tc_schedule_for(int64_t num_seqs, int64_t total_tokens, int H, int dv, int sms, bool varlen,
                     bool cooperative);
 // The schedule a call with these arguments runs on the current device (falls back to
 // one phase when the second stream of the phased schedule cannot be had).
 int tc_schedule(const PrefillArgs &a);
-// Kernels one call with these sizes launches on the current device (or -1).
-int tc_schedule_launches(int64_t num_seqs, int64_t total_tokens, int H, int dv, bool varlen);
+// The schedule an uncaptured call with these sizes runs on the current device (or -1).
+int tc_schedule_query(int64_t num_seqs, int64_t total_tokens, int H, int dv, bool varlen);
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
                   int dtype, int rule, const void *out_gate, const float *out_norm_weight,

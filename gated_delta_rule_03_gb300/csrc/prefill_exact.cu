@@ -181,7 +181,7 @@ plan_kernel(const int32_t *__restrict__ cu, int64_t num_seqs, int64_t total_toke
 int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases) {
     const bool fused = phases == 0;
     plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.num_seqs, a.total_tokens, L.max_chunks,
-                                          fused ? 1 : phases, (int4 *)(a.ws + L.plan),
+                                          plan_phases(phases), (int4 *)(a.ws + L.plan),
                                           (int32_t *)(a.ws + L.seq_chunk),
                                           (int32_t *)(a.ws + L.ctl),
                                           L.tensor_path ? (int32_t *)(a.ws + L.F) : nullptr,

@@ -9,6 +9,14 @@
 //    CTAs are resident together, so the waits always end. Used for batches of equal
 //    lengths whose chains leave enough SMs free.
 //  * phased: separate solve and chain kernels over phases of the chunks (below).
+//  * segmented: for a few long chains, which leave most SMs idle under the other two.
+//    The state after a run of chunks is affine in the state before it, S_end = P S + R,
+//    with P (d_k x d_k) the product of the chunks' transitions gamma_C I - Ktilde^T W
+//    and R the end state from zero. Each sequence is cut into n segments; one kernel
+//    runs every segment but the last from the identity with zero values (giving P) and
+//    from zero (giving R), all segments at once; a scan chains the segments' start
+//    states, S_{f+1} = P_f S_f + R_f, in fp32; a second kernel runs every segment from
+//    its start state, with output. Chain steps per call fall from m to about 2 m / n.
 #include <stdlib.h>
 
 #include <mutex>
@@ -40,6 +48,58 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         chain_body<true>(map_q, map_k, map_v, map_t, map_o, p, (int)blockIdx.x);
     else
         solve::solve_body<true>(map_q, map_k, sp);
+}
+
+// The segmented schedule's scan over the segment summaries of one (sequence, head) and
+// 32 value columns: X_0 = S_in (or zero), X_{f+1} = P_f X_f + R_f for f < segs, each X_f
+// stored as start[f]. P_f is read from the first d_k columns of its [d_k][d_v] matrix.
+constexpr int kScanCols = 32, kScanThreads = 256;
+constexpr int kScanPitch = DK + 4;  // row pitch of P in shared memory (floats)
+constexpr uint32_t SCAN_SMEM_BYTES = (DK * kScanPitch + DK * kScanCols) * sizeof(float);
+
+__global__ void __launch_bounds__(kScanThreads)
+seg_scan_kernel(const float *__restrict__ S_in, const float *__restrict__ P,
+                const float *__restrict__ R, float *__restrict__ start, int NH, int dv, int segs) {
+    extern __shared__ float4 scan_smem[];
+    float *sP = reinterpret_cast<float *>(scan_smem);  // [DK][kScanPitch]
+    float *sX = sP + DK * kScanPitch;                   // [DK][kScanCols]
+    griddep_wait();  // the summaries are complete
+    griddep_launch_dependents();
+    const int nh = blockIdx.x, c0 = blockIdx.y * kScanCols, tid = threadIdx.x;
+    const size_t mat = (size_t)DK * dv, set = (size_t)NH * mat;
+    const int i = tid >> 1, j0 = (tid & 1) * 16;  // this thread's row and 16 columns
+    for (int e = tid; e < DK * kScanCols; e += kScanThreads) {
+        const int r = e / kScanCols, c = e % kScanCols;
+        const size_t at = nh * mat + (size_t)r * dv + c0 + c;
+        sX[e] = S_in ? S_in[at] : 0.f;
+        start[at] = sX[e];
+    }
+    for (int f = 0; f < segs; ++f) {
+        const float *Pf = P + f * set + nh * mat;
+        __syncthreads();  // the previous step's reads of sP are done
+        for (int e = tid; e < DK * DK / 4; e += kScanThreads) {
+            const int r = e / (DK / 4), c4 = e % (DK / 4);
+            *reinterpret_cast<float4 *>(sP + r * kScanPitch + 4 * c4) =
+                *reinterpret_cast<const float4 *>(Pf + (size_t)r * dv + 4 * c4);
+        }
+        __syncthreads();
+        const float *Rf = R + f * set + nh * mat + (size_t)i * dv + c0 + j0;
+        float y[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) y[j] = Rf[j];
+        for (int kk = 0; kk < DK; ++kk) {
+            const float pk = sP[i * kScanPitch + kk];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) y[j] = fmaf(pk, sX[kk * kScanCols + j0 + j], y[j]);
+        }
+        __syncthreads();  // every thread has read X_f
+        float *dst = start + (f + 1) * set + nh * mat + (size_t)i * dv + c0 + j0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            sX[i * kScanCols + j0 + j] = y[j];
+            dst[j] = y[j];
+        }
+    }
 }
 
 }  // namespace
@@ -192,6 +252,35 @@ static int forced_phases() {
     return 0;
 }
 
+// Segmented: worth it when the chains leave most SMs idle. Segment count: the summary
+// launch's (sequence, head, slice + 1) CTAs of n - 1 segments, and the second launch's
+// (sequence, head, slice) CTAs of n segments, each fit on the GPU at once. It runs the
+// solve of every unit first (about 2.3 SM-us per unit) and 2 m / n chain steps, against
+// m chain steps of the other schedules (about 1.5 us per chunk step).
+static int segment_count(int64_t num_seqs, int64_t total_tokens, int H, int dv, int sms) {
+    if (!tc_segmentable(num_seqs, total_tokens, H, dv)) return 0;
+    const int64_t nh = num_seqs * H, slices = dv / chain::NV;
+    int64_t n = 1 + sms / (nh * (slices + 1));
+    if (n > kMaxPhases) n = kMaxPhases;
+    while (n > 1 && n * nh * slices > sms) --n;
+    if (n < 3) return 0;
+    const double m = (double)total_tokens / (double)num_seqs / kChunk;
+    const double units = m * (double)nh;
+    const double chained = 1.5 * m;
+    const double segmented = 2.3 * units / sms + 3.0 * m / (double)n + 15.0;
+    return segmented < 0.8 * chained ? (int)n : 0;
+}
+
+// GDR_PREFILL_SEGMENTS=2..8 forces the segmented schedule with that many segments where
+// the workspace holds it (a tuning and testing knob, like GDR_PREFILL_PHASES).
+static int forced_segments() {
+    if (const char *env = getenv("GDR_PREFILL_SEGMENTS")) {
+        const int v = atoi(env);
+        if (v >= 2 && v <= kMaxPhases) return v;
+    }
+    return 0;
+}
+
 static bool cooperative_ok(int dev) {
     static int ok[kMaxDevices] = {};  // 0 unknown, 1 yes, 2 no
     if (dev < 0 || dev >= kMaxDevices) return false;
@@ -212,7 +301,10 @@ static bool cooperative_ok(int dev) {
 int tc_schedule_for(int64_t num_seqs, int64_t total_tokens, int H, int dv, int sms, bool varlen,
                     bool cooperative) {
     if (total_tokens == 0) return 1;
+    if (const int n = forced_segments())
+        if (tc_segmentable(num_seqs, total_tokens, H, dv)) return kSegmentedBase + n;
     if (const int P = forced_phases()) return P;
+    if (const int n = segment_count(num_seqs, total_tokens, H, dv, sms)) return kSegmentedBase + n;
     if (!varlen && cooperative && fused_fits(num_seqs, H, dv, sms)) return 0;
     return phased_count(num_seqs, total_tokens, H, dv, sms);
 }
@@ -222,16 +314,14 @@ int tc_schedule(const PrefillArgs &a) {
     if (a.total_tokens == 0 || cudaGetDevice(&dev) != cudaSuccess) return 1;
     const int P = tc_schedule_for(a.num_seqs, a.total_tokens, a.H, a.dv, device_sms(dev),
                                   a.cu_seqlens != nullptr, cooperative_ok(dev));
-    if (P == 0) return 0;
+    if (P == 0 || P > kSegmentedBase) return P;
     return P > 1 && side_stream(a.stream) ? P : 1;
 }
 
-int tc_schedule_launches(int64_t num_seqs, int64_t total_tokens, int H, int dv, bool varlen) {
+int tc_schedule_query(int64_t num_seqs, int64_t total_tokens, int H, int dv, bool varlen) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-    const int P = tc_schedule_for(num_seqs, total_tokens, H, dv, device_sms(dev), varlen,
-                                  cooperative_ok(dev));
-    return P == 0 ? 2 : 1 + 2 * P;
+    return tc_schedule_for(num_seqs, total_tokens, H, dv, device_sms(dev), varlen, cooperative_ok(dev));
 }
 
 // The fused launch: every chain CTA and, on the remaining SMs, solve CTAs.
@@ -298,6 +388,83 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     return cuda_status(cudaLaunchKernelEx(&cfg, tc_fused_kernel, mq, mk, mv, mt, mo, p, sp, chain_ctas));
 }
 
+// The segmented schedule over `segs` segments per sequence.
+static int launch_segmented(const PrefillArgs &a, const WsLayout &L, int segs, const CUtensorMap &mq,
+                            const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mt,
+                            const CUtensorMap &mo) {
+    using namespace chain;
+    if (!L.segmentable || a.dk != DK) return GDR_ERR_CUDA;  // the schedule asks for neither
+    // the solve of every unit, with the whole GPU
+    int st = tc::launch_solve_tc(a, L, mq, mk, -1, 0, a.stream, true);
+    if (st != GDR_OK) return st;
+    if (cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SCAN_SMEM_BYTES) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    const int n_slices = a.dv / NV;
+    const int64_t NH = a.num_seqs * a.H;
+    const size_t set = (size_t)NH * a.dk * a.dv;  // floats of one state set
+    float *sets = reinterpret_cast<float *>(a.ws + L.seg);
+    float *S_P = sets, *S_R = sets + (kMaxPhases - 1) * set;
+    float *S_discard = sets + 2 * (kMaxPhases - 1) * set, *S_start = sets + 3 * (kMaxPhases - 1) * set;
+    TcParams p = {};
+    p.factors = reinterpret_cast<const float *>(a.ws + L.G);
+    p.cu_seqlens = a.cu_seqlens;
+    p.seq_chunk = reinterpret_cast<const int32_t *>(a.ws + L.seq_chunk);
+    p.num_seqs = a.num_seqs;
+    p.total_tokens = a.total_tokens;
+    p.H = a.H;
+    p.dv = a.dv;
+    p.n_slices = n_slices;
+    p.phases = segs;
+    p.o = (__nv_bfloat16 *)a.o;
+    p.ctl = (int32_t *)(a.ws + L.ctl);
+    p.additive = a.rule == GDR_RULE_ADDITIVE;
+    p.prologue = a.prologue;
+    p.S_P = S_P;
+    p.S_R = S_R;
+    p.S_start = S_start;
+    p.S_discard = S_discard;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = a.stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    // the summaries (P_f, R_f) of every segment but the last, without output
+    p.mode = 1;
+    cfg.gridDim = dim3((unsigned)((segs - 1) * NH * (n_slices + 1)));
+    if (cudaLaunchKernelEx(&cfg, tc_chain_kernel, mq, mk, mv, mt, mo, p) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    // the segments' start states
+    cudaLaunchConfig_t scfg = {};
+    scfg.gridDim = dim3((unsigned)NH, (unsigned)(a.dv / kScanCols));
+    scfg.blockDim = dim3(kScanThreads);
+    scfg.dynamicSmemBytes = SCAN_SMEM_BYTES;
+    scfg.stream = a.stream;
+    scfg.attrs = &attr;
+    scfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&scfg, seg_scan_kernel, (const float *)a.S0, (const float *)S_P,
+                           (const float *)S_R, S_start, (int)NH, a.dv, segs - 1) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    // every segment from its start state, with output
+    p.mode = 2;
+    p.S_out = a.S_final;
+    if (a.dv == NV) {  // the output step fused into the chain's epilogue
+        p.out_gate = (const __nv_bfloat16 *)a.out_gate;
+        p.out_norm_weight = a.out_norm_weight;
+        p.out_norm_eps = a.out_norm_eps;
+    }
+    cfg.gridDim = dim3((unsigned)(segs * NH * n_slices));
+    if (cudaLaunchKernelEx(&cfg, tc_chain_kernel, mq, mk, mv, mt, mo, p) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    return GDR_OK;
+}
+
 int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
     using namespace chain;
     const size_t s_bytes = (size_t)a.num_seqs * a.H * a.dk * a.dv * sizeof(float);
@@ -316,6 +483,8 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
         !tc::make_map_units(&mt, a.ws + L.T, 2 * L.max_chunks * a.H))
         return GDR_ERR_CUDA;
     if (phases == 0) return launch_fused(a, L, mq, mk, mv, mt, mo);
+    if (phases > kSegmentedBase)
+        return launch_segmented(a, L, phases - kSegmentedBase, mq, mk, mv, mt, mo);
     if (cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
         return GDR_ERR_CUDA;

@@ -30,7 +30,7 @@ int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &
     p.Tout = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.T);
     p.Gout = reinterpret_cast<float *>(a.ws + L.G);
     p.phase = phase;
-    p.unit_counter = reinterpret_cast<int32_t *>(a.ws + L.F) + phase;
+    p.unit_counter = reinterpret_cast<int32_t *>(a.ws + L.F) + (phase < 0 ? kMaxPhases : phase);
     p.additive = a.rule == GDR_RULE_ADDITIVE;
     p.prologue = a.prologue;
     p.gate_A = a.gate_A;

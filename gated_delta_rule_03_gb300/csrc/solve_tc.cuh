@@ -177,7 +177,7 @@ struct SolveParams {
     const int4 *plan;  // per chunk: sequence, first token, tokens, index within the sequence
     int32_t *ctl;      // [0] status, [1] number of chunks, [2 + f] first chunk of phase f
     int H;
-    int phase;            // the units of this phase's chunks are solved
+    int phase;            // the units of this phase's chunks are solved (-1: every unit)
     // fused launch (beside the chain): units in chunk-major order over `seqs` sequences of
     // `seq_chunks` chunks each, and a ready flag per unit, set once its results are stored
     int seqs, seq_chunks;
@@ -567,9 +567,11 @@ __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUten
     griddep_wait();
     griddep_launch_dependents();
     // this phase's units are u0 + [0, n_units); local indices, u0 added for addressing
-    const int u0 = kFused ? 0 : p.ctl[2 + p.phase] * p.H;
+    // (phase -1: every unit of the call)
+    const bool all = kFused || p.phase < 0;
+    const int u0 = all ? 0 : p.ctl[2 + p.phase] * p.H;
     const int n_units =
-        p.ctl[0] == GDR_OK ? (kFused ? p.ctl[1] * p.H : p.ctl[3 + p.phase] * p.H - u0) : 0;
+        p.ctl[0] == GDR_OK ? (all ? p.ctl[1] * p.H : p.ctl[3 + p.phase] * p.H - u0) : 0;
     const GroupSolver<kFused> gsv{p, &map_q, &map_k, gbase,
                                   reinterpret_cast<float *>(gs + G_BLK), reinterpret_cast<float *>(gs + G_GATES),
                                   next, next + 1, grp, lane, u0, n_units};

@@ -270,9 +270,13 @@ def chunk_fwd_kernel_launches(num_seqs, total_tokens, H, dk, dv, dtype, varlen=F
     return st
 
 
+SCHEDULE_SEGMENTED = 16  # GDR_SCHEDULE_SEGMENTED
+
+
 def chunk_fwd_schedule(num_seqs, total_tokens, H, dk, dv, dtype, varlen=False):
     """Schedule of a gdr_chunk_fwd call with these sizes on the current device: 0 for the
-    fused tensor-core schedule, else the number of phases."""
+    fused tensor-core schedule, 1 .. 8 phases of the phased one, or SCHEDULE_SEGMENTED + n
+    for the segmented one with n segments per sequence."""
     st = _load().gdr_chunk_fwd_schedule(int(num_seqs), int(total_tokens), int(H), int(dk),
                                         int(dv), 64, _DTYPES[dtype], int(bool(varlen)))
     if st < 0:

@@ -301,11 +301,15 @@ int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H,
  * Schedule of an uncaptured gdr_chunk_fwd call with these sizes on the current
  * device, for diagnostics and benchmarks: 0 for the fused schedule of the
  * tensor-core path (the planning kernel, then one cooperative kernel that runs
- * the chains beside the solve), else the number of phases (1 .. 8) of the
- * phased schedule; the exact path is one phase. varlen as above. Returns a
- * negative status for unsupported or invalid sizes, or GDR_ERR_CUDA if the
- * device cannot be read.
+ * the chains beside the solve); 1 .. 8, the number of phases of the phased
+ * schedule (the exact path is one phase); or GDR_SCHEDULE_SEGMENTED + n for
+ * the segmented schedule of few long chains, each sequence cut into n (2 .. 8)
+ * segments whose state transitions are summarised and chained by a scan
+ * (planning kernel, solve, summary chain, scan, chain). varlen as above.
+ * Returns a negative status for unsupported or invalid sizes, or GDR_ERR_CUDA
+ * if the device cannot be read.
  */
+enum { GDR_SCHEDULE_SEGMENTED = 16 };
 int gdr_chunk_fwd_schedule(int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v,
                            int chunk, int dtype, int varlen);
 
