@@ -156,8 +156,8 @@ struct TcParams {
     // slices from zero), without output. Mode 2 runs every segment f from its start
     // state S_start[f] (a copy of S_in for the first, so that S_out may be S_in), with
     // output; the last segment's state goes to S_out, the others' to S_discard. Every
-    // per-segment buffer holds [segment][sequence * H + head][d_k][d_v] (P_f in columns
-    // [0, d_k)).
+    // per-segment buffer holds [segment][sequence * H + head][d_k][d_v] (P_f transposed,
+    // in columns [0, d_k)).
     int mode;
     float *S_P, *S_R;
     const float *S_start;
@@ -372,9 +372,11 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 // Q (slot free once [QS | WS] of chunk c - 2 is done)
                 if (c >= 2 && !mbar_wait(bar(B_QE0 + (c & 1)), ((c >> 1) - 1) & 1)) { note_fail(3); break; }
                 const uint32_t qs = sbase + qslot(c), qf = bar(B_QF0 + (c & 1));
-                mbar_arrive_expect_tx(qf, 2 * 8192);
-                tma_load_3d(qs, &map_q, qf, 0, h, tt);
-                tma_load_3d(qs + 16384, &map_q, qf, 64, h, tt);
+                mbar_arrive_expect_tx(qf, no_out ? 0 : 2 * 8192);
+                if (!no_out) {  // (a segment summary reads no Q)
+                    tma_load_3d(qs, &map_q, qf, 0, h, tt);
+                    tma_load_3d(qs + 16384, &map_q, qf, 64, h, tt);
+                }
             }
         }
     } else if (warp < kPrepWarp0) {
@@ -390,6 +392,11 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             named_sync(kBarEpi, kEpiThreads);
             if (*fail) break;
             tc_fence_after();
+            if (no_out) {  // a segment summary: no O was computed
+                tc_fence_before();
+                mbar_arrive(bar(B_OFREE));
+                continue;
+            }
             uint32_t r0[32], r1[32];
             tmem_load_16x256b_x8(lane_base + TM_O, r0);
             tmem_load_16x256b_x8(lane_base + (16u << 16) + TM_O, r1);
@@ -458,9 +465,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             }
             fence_async_smem();
             named_sync(kBarEpi, kEpiThreads);
-            if (no_out) {
-                // a segment summary: no output
-            } else if (len == C) {
+            if (len == C) {
                 if (etid == 0) {
                     tma_store_3d(&map_o, stg, col0, h, (int)t0);
                     tma_store_3d(&map_o, stg + 8192, col0 + 64, h, (int)t0);
@@ -625,11 +630,19 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 if (!ok) { note_fail(1); break; }
                 tc_fence_after();
                 const uint32_t qw = sbase + qslot(c);
+                if (no_out) {  // a segment summary: X^T = -S^T W'^T alone (rows -W' of the slot)
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ta(tmem + TM_O, tmem + TM_SA + 8 * kk,
-                                sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                                idesc_bf16(128, 128, 0, 0), kk > 0);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16_ta(tmem + TM_X, tmem + TM_SA + 8 * kk,
+                                    sw128_desc(qw + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32, 16, 1024),
+                                    idesc_bf16(128, 64, 0, 0), kk > 0);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16_ta(tmem + TM_O, tmem + TM_SA + 8 * kk,
+                                    sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                                    idesc_bf16(128, 128, 0, 0), kk > 0);
+                }
                 mma_commit(bar(B_WS));
                 mma_commit(bar(B_QE0 + (c & 1)));  // Q and -W' are read
                 // W', U'~ of the next chunk now, while the state converts U'^T, if prep
@@ -654,7 +667,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // tokens 16kk..16kk+15: columns X + 32(kk/2) + 8(kk%2)
                     mma_bf16_ta(tmem + TM_S, tmem + TM_X + 32 * (kk >> 1) + 8 * (kk & 1),
-                                sw128_desc(ks + kk * 2048, 8192, 1024), idesc_bf16(128, 192, 0, 1), 1);
+                                sw128_desc(ks + kk * 2048, 8192, 1024),
+                                idesc_bf16(128, no_out ? 128 : 192, 0, 1), 1);  // (summary: S only)
                 mma_commit(bar(B_SO));
                 mma_commit(bar(B_KE0 + c % 3));  // the state's last reads of the K slot
                 if (!uw_next) {
@@ -734,8 +748,14 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 for (int hh = 0; hh < 2; ++hh) {
                     float x[32];
                     tmem_load32(s_tm + 32 * hh, x);
+                    if (zero_v) {  // a transition is stored transposed: P^T[row][k]
+                        float4 *t = reinterpret_cast<float4 *>(S_out_m + (size_t)row * p.dv + 64 * half + 32 * hh);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dst[(size_t)(32 * hh + i) * p.dv] = x[i];
+                        for (int i = 0; i < 8; ++i) t[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) dst[(size_t)(32 * hh + i) * p.dv] = x[i];
+                    }
                 }
                 break;
             }

@@ -51,23 +51,38 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 }
 
 // The segmented schedule's scan over the segment summaries of one (sequence, head) and
-// 32 value columns: X_0 = S_in (or zero), X_{f+1} = P_f X_f + R_f for f < segs, each X_f
-// stored as start[f]. P_f is read from the first d_k columns of its [d_k][d_v] matrix.
-constexpr int kScanCols = 32, kScanThreads = 256;
-constexpr int kScanPitch = DK + 4;  // row pitch of P in shared memory (floats)
-constexpr uint32_t SCAN_SMEM_BYTES = (DK * kScanPitch + DK * kScanCols) * sizeof(float);
+// 16 value columns: X_0 = S_in (or zero), X_{f+1} = P_f X_f + R_f for f < segs, each X_f
+// stored as start[f]. P_f is stored transposed in the first d_k columns of its
+// [d_k][d_v] matrix. Thread (rb, cb) owns rows 4rb..4rb+3 and columns 2cb, 2cb+1 of X;
+// P_f^T is staged in shared memory, the next one loading (cp.async) while this one is
+// used.
+constexpr int kScanCols = 16, kScanThreads = 256;
+constexpr uint32_t SCAN_SMEM_BYTES = (2 * DK * DK + DK * kScanCols) * sizeof(float);
+
+__device__ __forceinline__ void scan_stage_p(float *dst, const float *src, int dv, int tid) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(dst);
+#pragma unroll 4
+    for (int e = tid; e < DK * DK / 4; e += kScanThreads) {
+        const int r = e / (DK / 4), c4 = e % (DK / 4);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s + 16u * e),
+                     "l"(src + (size_t)r * dv + 4 * c4)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
 
 __global__ void __launch_bounds__(kScanThreads)
 seg_scan_kernel(const float *__restrict__ S_in, const float *__restrict__ P,
                 const float *__restrict__ R, float *__restrict__ start, int NH, int dv, int segs) {
     extern __shared__ float4 scan_smem[];
-    float *sP = reinterpret_cast<float *>(scan_smem);  // [DK][kScanPitch]
-    float *sX = sP + DK * kScanPitch;                   // [DK][kScanCols]
+    float *sPT = reinterpret_cast<float *>(scan_smem);  // 2 x [DK][DK]: P_f^T[k][i]
+    float *sX = sPT + 2 * DK * DK;                       // [DK][kScanCols]
     griddep_wait();  // the summaries are complete
     griddep_launch_dependents();
     const int nh = blockIdx.x, c0 = blockIdx.y * kScanCols, tid = threadIdx.x;
+    const int cb = tid & 7, rb = tid >> 3;
     const size_t mat = (size_t)DK * dv, set = (size_t)NH * mat;
-    const int i = tid >> 1, j0 = (tid & 1) * 16;  // this thread's row and 16 columns
+    if (segs > 0) scan_stage_p(sPT, P + nh * mat, dv, tid);
     for (int e = tid; e < DK * kScanCols; e += kScanThreads) {
         const int r = e / kScanCols, c = e % kScanCols;
         const size_t at = nh * mat + (size_t)r * dv + c0 + c;
@@ -75,29 +90,31 @@ seg_scan_kernel(const float *__restrict__ S_in, const float *__restrict__ P,
         start[at] = sX[e];
     }
     for (int f = 0; f < segs; ++f) {
-        const float *Pf = P + f * set + nh * mat;
-        __syncthreads();  // the previous step's reads of sP are done
-        for (int e = tid; e < DK * DK / 4; e += kScanThreads) {
-            const int r = e / (DK / 4), c4 = e % (DK / 4);
-            *reinterpret_cast<float4 *>(sP + r * kScanPitch + 4 * c4) =
-                *reinterpret_cast<const float4 *>(Pf + (size_t)r * dv + 4 * c4);
-        }
-        __syncthreads();
-        const float *Rf = R + f * set + nh * mat + (size_t)i * dv + c0 + j0;
-        float y[16];
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();  // P_f^T and X_f are in place; P_{f-1}^T is read no more
+        if (f + 1 < segs) scan_stage_p(sPT + ((f + 1) & 1) * DK * DK, P + (f + 1) * set + nh * mat, dv, tid);
+        const float *pt = sPT + (f & 1) * DK * DK + 4 * rb;
+        const float *Rf = R + f * set + nh * mat + (size_t)(4 * rb) * dv + c0 + 2 * cb;
+        float2 r[4];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) y[j] = Rf[j];
-        for (int kk = 0; kk < DK; ++kk) {
-            const float pk = sP[i * kScanPitch + kk];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y[j] = fmaf(pk, sX[kk * kScanCols + j0 + j], y[j]);
+        for (int i = 0; i < 4; ++i) r[i] = *reinterpret_cast<const float2 *>(Rf + (size_t)i * dv);
+        float y[4][2] = {};
+#pragma unroll 8
+        for (int k = 0; k < DK; ++k) {
+            const float4 a = *reinterpret_cast<const float4 *>(pt + k * DK);
+            const float2 x = *reinterpret_cast<const float2 *>(sX + k * kScanCols + 2 * cb);
+            y[0][0] = fmaf(a.x, x.x, y[0][0]); y[0][1] = fmaf(a.x, x.y, y[0][1]);
+            y[1][0] = fmaf(a.y, x.x, y[1][0]); y[1][1] = fmaf(a.y, x.y, y[1][1]);
+            y[2][0] = fmaf(a.z, x.x, y[2][0]); y[2][1] = fmaf(a.z, x.y, y[2][1]);
+            y[3][0] = fmaf(a.w, x.x, y[3][0]); y[3][1] = fmaf(a.w, x.y, y[3][1]);
         }
         __syncthreads();  // every thread has read X_f
-        float *dst = start + (f + 1) * set + nh * mat + (size_t)i * dv + c0 + j0;
+        float *dst = start + (f + 1) * set + nh * mat + (size_t)(4 * rb) * dv + c0 + 2 * cb;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            sX[i * kScanCols + j0 + j] = y[j];
-            dst[j] = y[j];
+        for (int i = 0; i < 4; ++i) {
+            const float2 v = make_float2(y[i][0] + r[i].x, y[i][1] + r[i].y);
+            *reinterpret_cast<float2 *>(sX + (4 * rb + i) * kScanCols + 2 * cb) = v;
+            *reinterpret_cast<float2 *>(dst + (size_t)i * dv) = v;
         }
     }
 }
