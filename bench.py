@@ -32,7 +32,7 @@ if ROOT not in sys.path:
 from gated_delta_rule_03_gb300 import inputs  # noqa: E402
 
 METRIC = "GDN prefill tokens/s (H=16,d=128,bf16); decode state GB/s vs HBM peak"
-PREFILL_WORKLOAD = "prefill_bf16"
+PREFILL_WORKLOAD = "prefill_bf16"  # the headline workload; --workload picks another
 DECODE_WORKLOAD = "decode_bf16"
 
 
@@ -206,7 +206,7 @@ def oracle_prefill_sample(inp):
                 num_seqs=inp.num_seqs)
 
 
-def cpu_baseline(inp, seconds):
+def cpu_baseline(inp, seconds, name):
     """The oracle, as it stands, on this host's cores: repeat the full workload until
     `seconds` have passed (at least once)."""
     import oracle
@@ -221,7 +221,7 @@ def cpu_baseline(inp, seconds):
             break
     tokens = inp.total_tokens * reps
     return {"value": tokens / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"full {PREFILL_WORKLOAD} workload ({inp.num_seqs}x{inp.seq_lens[0]} "
+            "sample": f"full {name} workload ({inp.num_seqs} sequences, {inp.total_tokens} "
                       f"tokens, H={inp.H}, d_k={inp.dk}, d_v={inp.dv}) x {reps} repetitions, "
                       f"{el:.1f} s, float64 token loop"}
 
@@ -231,7 +231,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    inp = inputs.workload_prefill(PREFILL_WORKLOAD)
+    inp = inputs.workload_prefill(args.workload)
     sample = oracle_prefill_sample(inp)
     threads = oracle.default_threads()
     for _ in range(args.warmup):
@@ -246,9 +246,9 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(inp),
+        "config": workload_config(inp, args.workload),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"each step: the full {PREFILL_WORKLOAD} workload, "
+                         "sample": f"each step: the full {args.workload} workload, "
                                    f"float64 token loop on {threads} host threads"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -258,12 +258,17 @@ def run_reference(args):
     return 0
 
 
-def workload_config(inp):
-    return {"workload": f"{PREFILL_WORKLOAD}: B={inp.num_seqs} H={inp.H} T={inp.seq_lens[0]} "
+def workload_config(inp, name):
+    equal = len(set(inp.seq_lens)) == 1
+    lens = f"T={inp.seq_lens[0]}" if equal else f"T in {min(inp.seq_lens)}..{max(inp.seq_lens)} " \
+                                                 f"packed ({inp.total_tokens} tokens)"
+    s0 = "S0=0" if inp.S0 is None else "S0 ~ N(0, 0.02^2)"
+    return {"workload": f"{name}: B={inp.num_seqs} H={inp.H} {lens} "
                         f"d_k={inp.dk} d_v={inp.dv} chunk={inp.chunk} bf16 q/k/v/o, fp32 "
-                        f"gates and state, S0=0",
-            "global_batch": inp.num_seqs, "seq_len": inp.seq_lens[0], "heads": inp.H,
-            "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"}
+                        f"gates and state, {s0}",
+            "global_batch": inp.num_seqs,
+            "seq_len": inp.seq_lens[0] if equal else inp.total_tokens // inp.num_seqs,
+            "heads": inp.H, "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"}
 
 
 def run_gdr(args):
@@ -276,7 +281,7 @@ def run_gdr(args):
     stream = torch.cuda.Stream(device)
     peaks = load_peaks()
 
-    inp = inputs.workload_prefill(PREFILL_WORKLOAD)
+    inp = inputs.workload_prefill(args.workload)
     d = lambda t: None if t is None else t.to(device)
     q, k, v, la, b = d(inp.q), d(inp.k), d(inp.v), d(inp.log_alpha), d(inp.beta)
     S0, cu = d(inp.S0), d(inp.cu_seqlens)
@@ -307,7 +312,7 @@ def run_gdr(args):
     main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype, schedule=schedule)
     bytes_call = prefill_bytes(inp)
     achieved = bytes_call / (call_ms / 1e3) / 1e9
-    traffic = recorded_traffic(main_kernel, PREFILL_WORKLOAD)
+    traffic = recorded_traffic(main_kernel, args.workload)
 
     # end to end through the public API: pinned host inputs in, results back out
     pin = lambda t: None if t is None else t.pin_memory()
@@ -339,14 +344,14 @@ def run_gdr(args):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, args.cpu_seconds)
+        cpu = cpu_baseline(inp, args.cpu_seconds, args.workload)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ops.chunk_fwd_compute_dtype(inp.dk, inp.dv, q.dtype), "data": "synthetic",
-        "config": workload_config(inp),
+        "config": workload_config(inp, args.workload),
         "roofline": {"kernel": main_kernel, "bound": "hbm", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
@@ -408,6 +413,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gdr", "reference"], default="gdr")
+    ap.add_argument("--workload", choices=["prefill_bf16", "varlen_bf16", "long_bf16"],
+                    default=PREFILL_WORKLOAD,
+                    help="prefill workload of the step (default: the headline prefill_bf16)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
