@@ -31,10 +31,10 @@ def _load():
         lp = ctypes.POINTER(ctypes.c_int64)
         i64 = ctypes.c_int64
         lib.gdr_oracle_forward.argtypes = [dp, dp, dp, dp, dp, dp, lp, i64, i64, i64, i64, i64,
-                                           ctypes.c_int, ctypes.c_int, dp, dp]
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, dp]
         lib.gdr_oracle_forward.restype = ctypes.c_int
         lib.gdr_oracle_decode.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64,
-                                          ctypes.c_int]
+                                          ctypes.c_int, ctypes.c_int]
         lib.gdr_oracle_decode.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -62,7 +62,8 @@ def forward(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
             additive=False, threads=None):
     """Run the recurrence over packed sequences.
 
-    q, k: [total_T, H, dk]; v: [total_T, H, dv]; log_alpha, beta: [total_T, H];
+    q, k: [total_T, H, dk]; v: [total_T, H, dv]; beta: [total_T, H]; log_alpha:
+    [total_T, H] (one rate per head), or [total_T, H, dk] (one rate per key channel);
     S0: [num_seqs, H, dk, dv] or None (zero state); cu_seqlens: [num_seqs+1]
     token offsets or None (then `num_seqs` equal sequences, default 1).
     Returns (o [total_T, H, dv], S_final [num_seqs, H, dk, dv]) in float64.
@@ -72,7 +73,8 @@ def forward(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
     T, H, dk = q.shape
     dv = v.shape[2]
     assert k.shape == (T, H, dk) and v.shape[:2] == (T, H)
-    assert la.shape == (T, H) and b.shape == (T, H)
+    per_channel = la.ndim == 3
+    assert la.shape == ((T, H, dk) if per_channel else (T, H)) and b.shape == (T, H)
     cu = None
     if cu_seqlens is not None:
         cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
@@ -86,7 +88,8 @@ def forward(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
     S = np.zeros((n, H, dk, dv), dtype=np.float64)
     rc = _load().gdr_oracle_forward(
         _ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(s0), _ptr(cu, ctypes.c_int64),
-        n, T, H, dk, dv, int(bool(additive)), int(threads or default_threads()), _ptr(o), _ptr(S))
+        n, T, H, dk, dv, int(bool(additive)), int(per_channel), int(threads or default_threads()),
+        _ptr(o), _ptr(S))
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (status {rc})")
     return o, S
@@ -94,16 +97,19 @@ def forward(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
 
 def decode(q, k, v, log_alpha, beta, S, threads=None):
     """One decode step for N sequences: q, k [N, H, dk]; v [N, H, dv];
-    log_alpha, beta [N, H]; S [N, H, dk, dv]. Returns (o, S_new) in float64;
-    the input S is not modified."""
+    log_alpha [N, H] (or [N, H, dk], one rate per key channel), beta [N, H];
+    S [N, H, dk, dv]. Returns (o, S_new) in float64; the input S is not modified."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     la, b = _f64(log_alpha), _f64(beta)
     S_new = np.array(S, dtype=np.float64, copy=True, order="C")
     N, H, dk = q.shape
     dv = v.shape[2]
     o = np.zeros((N, H, dv), dtype=np.float64)
+    per_channel = la.ndim == 3
+    assert la.shape == ((N, H, dk) if per_channel else (N, H))
     rc = _load().gdr_oracle_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(S_new),
-                                   _ptr(o), N, H, dk, dv, int(threads or default_threads()))
+                                   _ptr(o), N, H, dk, dv, int(per_channel),
+                                   int(threads or default_threads()))
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (status {rc})")
     return o, S_new

@@ -20,6 +20,12 @@
  *   No score scale and no normalisation of q or k: the caller passes the
  *   vectors it wants used.
  *
+ *   With `per_channel` set, alpha_t is a d_k vector: each key channel (row i of
+ *   S) has its own rate, S'_t = diag(alpha_t) S_{t-1} ("Attention as Matrix
+ *   Algebra: From Softmax to the Delta Rule", section 10 "Where this goes next":
+ *   Kimi Delta Attention gives each feature channel its own rate). The other
+ *   steps are unchanged.
+ *
  *   With `additive` set, step (2)-(3) is replaced by the decayed additive write
  *   S_t = alpha_t S_{t-1} + beta_t k_t v_t^T ("From KV Cache to a State Matrix:
  *   Linear Attention and DeltaNet", section "From attention weights to a state
@@ -35,7 +41,7 @@
  * Layouts (all row-major, contiguous):
  *   q, k        [total_tokens, H, dk]
  *   v, o        [total_tokens, H, dv]
- *   log_alpha   [total_tokens, H]
+ *   log_alpha   [total_tokens, H], or [total_tokens, H, dk] with per_channel
  *   beta        [total_tokens, H]
  *   S0, S_final [num_seqs, H, dk, dv]     (S0 may be NULL: zero state)
  *   cu_seqlens  [num_seqs + 1] int64 offsets into the token axis, or NULL
@@ -48,17 +54,20 @@
 #include <stdlib.h>
 #include <string.h>
 
-/* One token of Eqs. (1)-(4) on the state S (dk x dv). `scratch` holds dv doubles. */
+/* One token of Eqs. (1)-(4) on the state S (dk x dv). log_alpha points at the token's
+ * one rate, or at its dk rates with per_channel. `scratch` holds dv doubles. */
 static void oracle_token(double *S, int64_t dk, int64_t dv, const double *q, const double *k,
-                         const double *v, double log_alpha, double beta, int additive,
-                         double *o, double *scratch)
+                         const double *v, const double *log_alpha, int per_channel, double beta,
+                         int additive, double *o, double *scratch)
 {
-    const double alpha = exp(log_alpha);
     int64_t i, j;
 
-    /* (1) decay the whole state */
-    for (i = 0; i < dk * dv; ++i)
-        S[i] *= alpha;
+    /* (1) decay: row i (key channel i) by alpha_t, or by its own alpha_t[i] */
+    for (i = 0; i < dk; ++i) {
+        const double alpha = exp(log_alpha[per_channel ? i : 0]);
+        for (j = 0; j < dv; ++j)
+            S[i * dv + j] *= alpha;
+    }
 
     if (additive) {
         /* decayed additive write: S += beta k v^T */
@@ -91,7 +100,7 @@ typedef struct {
     const double *q, *k, *v, *log_alpha, *beta, *S0;
     const int64_t *cu;      /* may be NULL */
     int64_t num_seqs, total_tokens, H, dk, dv, seq_len;
-    int additive;
+    int additive, per_channel;
     double *o, *S_final;
     int64_t first_item, item_stride;
     int status;
@@ -118,8 +127,8 @@ static void *oracle_worker(void *arg)
         for (int64_t t = t0; t < t1; ++t) {
             const int64_t th = t * H + h;
             oracle_token(S, dk, dv, job->q + th * dk, job->k + th * dk, job->v + th * dv,
-                         job->log_alpha[th], job->beta[th], job->additive, job->o + th * dv,
-                         scratch);
+                         job->log_alpha + th * (job->per_channel ? dk : 1), job->per_channel,
+                         job->beta[th], job->additive, job->o + th * dv, scratch);
         }
     }
     free(scratch);
@@ -176,8 +185,8 @@ static int run_jobs(oracle_job *proto, int nthreads)
 int gdr_oracle_forward(const double *q, const double *k, const double *v,
                        const double *log_alpha, const double *beta, const double *S0,
                        const int64_t *cu_seqlens, int64_t num_seqs, int64_t total_tokens,
-                       int64_t H, int64_t dk, int64_t dv, int additive, int nthreads,
-                       double *o, double *S_final)
+                       int64_t H, int64_t dk, int64_t dv, int additive, int per_channel,
+                       int nthreads, double *o, double *S_final)
 {
     if (num_seqs < 0 || total_tokens < 0 || H <= 0 || dk <= 0 || dv <= 0 || !S_final)
         return -1;
@@ -210,6 +219,7 @@ int gdr_oracle_forward(const double *q, const double *k, const double *v,
     proto.dv = dv;
     proto.seq_len = cu_seqlens ? 0 : total_tokens / num_seqs;
     proto.additive = additive;
+    proto.per_channel = per_channel;
     proto.o = o;
     proto.S_final = S_final;
     return run_jobs(&proto, nthreads);
@@ -217,13 +227,13 @@ int gdr_oracle_forward(const double *q, const double *k, const double *v,
 
 /*
  * One decode step: one token per sequence, the state updated in place.
- * Layouts: q, k [N, H, dk]; v, o [N, H, dv]; log_alpha, beta [N, H];
- * S [N, H, dk, dv]. It is gdr_oracle_forward with one token per sequence and
- * S0 = S_final = S.
+ * Layouts: q, k [N, H, dk]; v, o [N, H, dv]; log_alpha [N, H] (or [N, H, dk] with
+ * per_channel), beta [N, H]; S [N, H, dk, dv]. It is gdr_oracle_forward with one
+ * token per sequence and S0 = S_final = S.
  */
 int gdr_oracle_decode(const double *q, const double *k, const double *v, const double *log_alpha,
                       const double *beta, double *S, double *o, int64_t N, int64_t H, int64_t dk,
-                      int64_t dv, int nthreads)
+                      int64_t dv, int per_channel, int nthreads)
 {
     if (N < 0 || H <= 0 || dk <= 0 || dv <= 0)
         return -1;
@@ -231,6 +241,6 @@ int gdr_oracle_decode(const double *q, const double *k, const double *v, const d
         return 0;
     if (!q || !k || !v || !log_alpha || !beta || !S || !o)
         return -1;
-    return gdr_oracle_forward(q, k, v, log_alpha, beta, S, NULL, N, N, H, dk, dv, 0, nthreads, o,
-                              S);
+    return gdr_oracle_forward(q, k, v, log_alpha, beta, S, NULL, N, N, H, dk, dv, 0, per_channel,
+                              nthreads, o, S);
 }

@@ -18,6 +18,13 @@ substitution gives, per chunk of C tokens entering with state S,
 and the product of the chunk's transitions alpha_t (I - beta_t k_t k_t^T) is
 gamma_C I - Ktilde^T T diag(gamma) K.
 
+With one rate per key channel (log alpha_t a d_k vector, the state's row c decayed
+by alpha_t[c]) the same substitution holds with the decay moved inside the key
+products: g_t is a vector, every Gamma_ti k_t^T k_i becomes
+sum_c k_t[c] k_i[c] exp(g_t[c] - g_i[c]), diag(gamma) K becomes the rows
+gamma_t . k_t, diag(gamma) Q the rows gamma_t . q_t, gamma_C S becomes
+diag(gamma_C) S, and Ktilde_i = exp(g_C - g_i) . k_i (chunk_step_per_channel).
+
 Tests compare this module with the token-by-token oracle; that pins the
 derivation the kernels rely on. Nothing here is used by the CUDA path, and the
 oracle does not use this module either.
@@ -67,3 +74,34 @@ def chunk_transition(k, log_alpha, beta):
     T = solve_triangular(np.eye(C) + L, np.diag(beta), lower=True)
     k_tilde = np.exp(g[-1] - g)[:, None] * k
     return gamma[-1] * np.eye(dk) - k_tilde.T @ T @ (gamma[:, None] * k)
+
+
+def chunk_step_per_channel(S, q, k, v, log_alpha, beta):
+    """One chunk with one rate per key channel: log_alpha [C, dk]; otherwise as chunk_step.
+    Every exponent is g_t - g_i with i <= t (or g_t, g_C - g_i), so every factor is <= 1."""
+    C = len(k)
+    g = np.cumsum(log_alpha, axis=0)                      # [C, dk]
+    lower_incl = np.tril(np.ones((C, C), dtype=bool))
+    diff = g[:, None, :] - g[None, :, :]                  # [t, i, c]
+    dec = np.where(lower_incl[:, :, None], np.exp(np.where(lower_incl[:, :, None], diff, 0.0)), 0.0)
+    KK = np.einsum("tc,ic,tic->ti", k, k, dec)
+    QK = np.einsum("tc,ic,tic->ti", q, k, dec)
+    L = np.tril(beta[:, None] * KK, -1)
+    T = solve_triangular(np.eye(C) + L, np.diag(beta), lower=True)
+    U = T @ v - T @ (np.exp(g) * k) @ S
+    O = (np.exp(g) * q) @ S + QK @ U
+    k_tilde = np.exp(g[-1][None, :] - g) * k
+    S_next = np.exp(g[-1])[:, None] * S + k_tilde.T @ U
+    return O, S_next
+
+
+def chunked_forward_per_channel(q, k, v, log_alpha, beta, C, S0=None):
+    """Whole sequence for one head with per-channel rates, chunk by chunk."""
+    T_len, dk = k.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    out = np.empty((T_len, dv))
+    for c in range(0, T_len, C):
+        sl = slice(c, c + C)
+        out[sl], S = chunk_step_per_channel(S, q[sl], k[sl], v[sl], log_alpha[sl], beta[sl])
+    return out, S

@@ -15,9 +15,13 @@ from oracle.build import SRC, build
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 MUTANTS = {
-    "no decay": ("S[i] *= alpha;", "S[i] *= 1.0;"),
-    "decay squared": ("const double alpha = exp(log_alpha);",
-                      "const double alpha = exp(2.0 * log_alpha);"),
+    "no decay": ("S[i * dv + j] *= alpha;", "S[i * dv + j] *= 1.0;"),
+    "decay squared": ("const double alpha = exp(log_alpha[per_channel ? i : 0]);",
+                      "const double alpha = exp(2.0 * log_alpha[per_channel ? i : 0]);"),
+    "per-channel rate of another channel": ("log_alpha[per_channel ? i : 0]",
+                                            "log_alpha[per_channel ? (i + 1) % dk : 0]"),
+    "per-channel rates ignored": ("log_alpha[per_channel ? i : 0]", "log_alpha[0]"),
+    "per-channel stride of one": ("th * (job->per_channel ? dk : 1)", "th"),
     "sign of the correction": ("beta * k[i] * (v[j] - vhat[j])", "beta * k[i] * (v[j] + vhat[j])"),
     "write strength dropped": ("beta * k[i] * (v[j] - vhat[j])", "k[i] * (v[j] - vhat[j])"),
     "read with the key instead of the query": ("o[j] += S[i * dv + j] * q[i];",

@@ -398,6 +398,115 @@ def test_gated_wy_form_is_the_product_of_transitions():
     np.testing.assert_allclose(S, prod @ S0, rtol=0, atol=1e-13)
 
 
+# --------------------------------------------------------------------------- per-channel decay
+# One rate per key channel ("Attention as Matrix Algebra", section 10 "Where this goes
+# next": Kimi Delta Attention gives each feature channel its own rate). In the keys x
+# values layout channel c is row c of S: S'_t = diag(alpha_t) S_{t-1}.
+
+def run_pc(q, k, v, log_alpha, beta, S0=None, additive=False):
+    """Single head, single sequence, log_alpha [T, dk]."""
+    s0 = None if S0 is None else np.asarray(S0, dtype=np.float64)[None, None]
+    o, S = oracle.forward(q[:, None, :], k[:, None, :], v[:, None, :], log_alpha[:, None, :],
+                          np.asarray(beta)[:, None], S0=s0, additive=additive, threads=1)
+    return o[:, 0, :], S[0, 0]
+
+
+def _pc_case(rng, T, dk, dv):
+    q, k, v, _, b, S0 = _random_case(rng, T, dk, dv)
+    la = -np.logaddexp(0.0, rng.standard_normal((T, dk)))
+    return q, k, v, la, b, S0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_per_channel_brute_force_unrolled_products(seed):
+    # S_t = A_t S_{t-1} + B_t with A_t = (I - beta_t k_t k_t^T) diag(alpha_t) (decay, then
+    # the rank-one correction), B_t = beta_t k_t v_t^T, unrolled as explicit products
+    rng = np.random.default_rng(400 + seed)
+    T = int(rng.integers(2, 9))
+    dk, dv = int(rng.integers(2, 5)), int(rng.integers(1, 5))
+    q, k, v, la, b, S0 = _pc_case(rng, T, dk, dv)
+    A = [(np.eye(dk) - b[t] * np.outer(k[t], k[t])) @ np.diag(np.exp(la[t])) for t in range(T)]
+    states, S_t = [], S0
+    for t in range(T):
+        prod = np.eye(dk)
+        for j in range(t, -1, -1):
+            prod = prod @ A[j]
+        S_t = prod @ S0
+        for i in range(t + 1):
+            P = np.eye(dk)
+            for j in range(t, i, -1):
+                P = P @ A[j]
+            S_t = S_t + P @ (b[i] * np.outer(k[i], v[i]))
+        states.append(S_t)
+    o, S = run_pc(q, k, v, la, b, S0)
+    np.testing.assert_allclose(S, states[-1], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o, np.array([states[t].T @ q[t] for t in range(T)]), rtol=0,
+                               atol=1e-12)
+
+
+def test_per_channel_equal_rates_are_the_head_rate():
+    rng = np.random.default_rng(410)
+    q, k, v, la, b, S0 = _random_case(rng, 40, 6, 5)
+    o, S = run(q, k, v, log_alpha=la, beta=b, S0=S0)
+    op, Sp = run_pc(q, k, v, np.repeat(la[:, None], 6, axis=1), b, S0)
+    np.testing.assert_array_equal(op, o)
+    np.testing.assert_array_equal(Sp, S)
+
+
+def test_per_channel_unwritten_channel_only_decays():
+    # a key channel that no key touches (k[:, c] = 0) is never corrected: row c of S is
+    # S0's row c times the product of its own rates, and its rates reach no other row
+    rng = np.random.default_rng(411)
+    T, dk, dv, c = 30, 5, 4, 2
+    q, k, v, la, b, S0 = _pc_case(rng, T, dk, dv)
+    k[:, c] = 0.0
+    _, S = run_pc(q, k, v, la, b, S0)
+    np.testing.assert_allclose(S[c], np.exp(la[:, c].sum()) * S0[c], rtol=1e-13, atol=0)
+    la2 = la.copy()
+    la2[:, c] -= 0.7
+    _, S2 = run_pc(q, k, v, la2, b, S0)
+    rows = [r for r in range(dk) if r != c]
+    np.testing.assert_array_equal(S2[rows], S[rows])
+
+
+def test_per_channel_beta_zero_is_rowwise_decay():
+    rng = np.random.default_rng(412)
+    q, k, v, la, _, S0 = _pc_case(rng, 12, 4, 3)
+    o, S = run_pc(q, k, v, la, np.zeros(12), S0)
+    g = np.cumsum(la, axis=0)
+    np.testing.assert_allclose(S, np.exp(g[-1])[:, None] * S0, rtol=1e-13, atol=0)
+    np.testing.assert_allclose(o, np.einsum("tc,cj,tc->tj", q, S0, np.exp(g)), rtol=1e-12,
+                               atol=1e-14)
+
+
+def test_per_channel_decode_step_equals_one_token_forward():
+    rng = np.random.default_rng(413)
+    N, H, dk, dv = 3, 2, 4, 6
+    q, k = rng.standard_normal((N, H, dk)), unit(rng.standard_normal((N, H, dk)))
+    v = rng.standard_normal((N, H, dv))
+    la = -np.logaddexp(0.0, rng.standard_normal((N, H, dk)))
+    b = 1 / (1 + np.exp(-rng.standard_normal((N, H))))
+    S = rng.standard_normal((N, H, dk, dv))
+    o, S_new = oracle.decode(q, k, v, la, b, S)
+    of, Sf = oracle.forward(q, k, v, la, b, S0=S, num_seqs=N)
+    np.testing.assert_array_equal(o, of)
+    np.testing.assert_array_equal(S_new, Sf)
+
+
+def test_per_channel_chunk_form_equals_the_recurrence():
+    # the chunk form the exact kernels follow for per-channel rates
+    rng = np.random.default_rng(414)
+    T, dk, dv = 150, 8, 6
+    for shift in (0.0, -6.0):
+        q, k, v, _, b, S0 = _random_case(rng, T, dk, dv)
+        la = -np.logaddexp(0.0, rng.standard_normal((T, dk)) + shift)
+        o, S = run_pc(q, k, v, la, b, S0)
+        for C in (1, 5, 16, 64, 150):
+            oc, Sc = chunk_form.chunked_forward_per_channel(q, k, v, la, b, C, S0=S0)
+            np.testing.assert_allclose(oc, o, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(Sc, S, rtol=0, atol=1e-12)
+
+
 # --------------------------------------------------------------------------- output step
 
 def test_out_norm_gate_worked_values():
