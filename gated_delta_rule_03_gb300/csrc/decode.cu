@@ -9,7 +9,9 @@
 // which is Eqs. (1)-(4) of "Linear attention" (arsalanzafar.ai), "How it works",
 // for a single token. The additive rule (S' = alpha S + beta k v^T) is the same step
 // with u = beta v. With the layer's prologue, k and q are scaled to unit length in
-// shared memory and the gates come from their pre-activations. The layer's output step (o / rms(o) * w * silu(z), over the head's
+// shared memory and the gates come from their pre-activations. With one rate per key
+// channel (PC; log_alpha [N, H, d_k]) alpha becomes diag(alpha): a = S^T (alpha . k),
+// b = S^T (alpha . q), o = b + (k.q) u and row r of S decays by alpha_r. The layer's output step (o / rms(o) * w * silu(z), over the head's
 // value entries) is applied before o is stored when a gate z is given. The kernel is
 // HBM-bound: a generation step reads about
 // d_k d_v numbers ("Attention as Matrix Algebra", section 9).
@@ -53,7 +55,7 @@ template <> struct Vec4<__nv_bfloat16> {
 // z sigmoid(z)
 __device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
 
-template <typename Tin, int DK, int DV>
+template <typename Tin, int DK, int DV, bool PC>
 __global__ void __launch_bounds__(DK * DV / 64)
 decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const Tin *__restrict__ v, const float *__restrict__ log_alpha,
@@ -71,6 +73,7 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     __shared__ float ks[DK], qs[DK], vs[DV], os[DV];
     __shared__ float4 red_k[RG][TPR], red_q[RG][TPR];
     __shared__ float s_kq, s_rstd, s_nk, s_nq;
+    __shared__ float ar[PC ? DK : 1];  // per-channel rates alpha_r
 
     const int64_t nh = blockIdx.x;
     const int tid = threadIdx.x;
@@ -87,13 +90,20 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         qs[i] = to_f32(q[nh * DK + i]);
     }
     for (int j = tid; j < DV; j += NT) vs[j] = to_f32(v[nh * DV + j]);
-    float alpha, b;
+    float alpha = 1.f, b;
     if (prologue) {  // the layer's gate activations from the pre-activations a, b
-        alpha = expf(prologue_log_alpha(log_alpha[nh], gate_A ? gate_A[nh % H] : 1.f));
+        if (!PC) alpha = expf(prologue_log_alpha(log_alpha[nh], gate_A ? gate_A[nh % H] : 1.f));
         b = prologue_beta(beta[nh]);
     } else {
-        alpha = expf(log_alpha[nh]);
+        if (!PC) alpha = expf(log_alpha[nh]);
         b = beta[nh];
+    }
+    if (PC) {  // alpha stays 1; the rates go with the rows
+        const float A = prologue && gate_A ? gate_A[nh % H] : 1.f;
+        for (int i = tid; i < DK; i += NT) {
+            const float x = log_alpha[nh * DK + i];
+            ar[i] = expf(prologue ? prologue_log_alpha(x, A) : x);
+        }
     }
     const float ra = read * alpha;
     __syncthreads();
@@ -125,7 +135,8 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
 #pragma unroll
     for (int m = 0; m < RPT; ++m) {
-        const float kr = ks[rg + m * RG], qr = qs[rg + m * RG];
+        const float rate = PC ? ar[rg + m * RG] : 1.f;
+        const float kr = ks[rg + m * RG] * rate, qr = qs[rg + m * RG] * rate;
         pk.x = fmaf(s[m].x, kr, pk.x); pk.y = fmaf(s[m].y, kr, pk.y);
         pk.z = fmaf(s[m].z, kr, pk.z); pk.w = fmaf(s[m].w, kr, pk.w);
         pq.x = fmaf(s[m].x, qr, pq.x); pq.y = fmaf(s[m].y, qr, pq.y);
@@ -179,11 +190,12 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
     for (int m = 0; m < RPT; ++m) {
         const float kr = ks[rg + m * RG];
+        const float rate = PC ? ar[rg + m * RG] : alpha;
         float4 x;
-        x.x = fmaf(alpha, s[m].x, kr * u.x);
-        x.y = fmaf(alpha, s[m].y, kr * u.y);
-        x.z = fmaf(alpha, s[m].z, kr * u.z);
-        x.w = fmaf(alpha, s[m].w, kr * u.w);
+        x.x = fmaf(rate, s[m].x, kr * u.x);
+        x.y = fmaf(rate, s[m].y, kr * u.y);
+        x.z = fmaf(rate, s[m].z, kr * u.z);
+        x.w = fmaf(rate, s[m].w, kr * u.w);
         __stcs(Sp + (rg + m * RG) * TPR + cg, x);
     }
 }
@@ -192,10 +204,15 @@ template <typename Tin, int DK, int DV>
 static int launch_decode_t(const void *q, const void *k, const void *v, const float *la,
                            const float *beta, float *S, void *o, int64_t NH, float read,
                            const void *z, const float *w, float eps, int prologue,
-                           const float *gate_A, int H, cudaStream_t stream) {
-    decode_step_kernel<Tin, DK, DV><<<(unsigned)NH, DK * DV / 64, 0, stream>>>(
-        (const Tin *)q, (const Tin *)k, (const Tin *)v, la, beta, S, (Tin *)o, read,
-        (const Tin *)z, w, eps, prologue, gate_A, H);
+                           const float *gate_A, int H, bool per_channel, cudaStream_t stream) {
+    if (per_channel)
+        decode_step_kernel<Tin, DK, DV, true><<<(unsigned)NH, DK * DV / 64, 0, stream>>>(
+            (const Tin *)q, (const Tin *)k, (const Tin *)v, la, beta, S, (Tin *)o, read,
+            (const Tin *)z, w, eps, prologue, gate_A, H);
+    else
+        decode_step_kernel<Tin, DK, DV, false><<<(unsigned)NH, DK * DV / 64, 0, stream>>>(
+            (const Tin *)q, (const Tin *)k, (const Tin *)v, la, beta, S, (Tin *)o, read,
+            (const Tin *)z, w, eps, prologue, gate_A, H);
     return cuda_status(cudaGetLastError());
 }
 
@@ -203,11 +220,11 @@ template <typename Tin>
 static int launch_decode_dtype(const void *q, const void *k, const void *v, const float *la,
                                const float *beta, float *S, void *o, int64_t NH, int dk, int dv,
                                float read, const void *z, const float *w, float eps, int prologue,
-                               const float *gate_A, int H, cudaStream_t stream) {
+                               const float *gate_A, int H, bool pc, cudaStream_t stream) {
 #define GDR_DECODE_CASE(DK_, DV_)                                                         \
     if (dk == DK_ && dv == DV_)                                                           \
         return launch_decode_t<Tin, DK_, DV_>(q, k, v, la, beta, S, o, NH, read, z, w, eps, \
-                                              prologue, gate_A, H, stream);
+                                              prologue, gate_A, H, pc, stream);
     GDR_DECODE_CASE(64, 64)
     GDR_DECODE_CASE(64, 128)
     GDR_DECODE_CASE(64, 256)
@@ -221,15 +238,17 @@ static int launch_decode_dtype(const void *q, const void *k, const void *v, cons
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
                   int dtype, int rule, const void *out_gate, const float *out_norm_weight,
-                  float out_norm_eps, int prologue, const float *gate_A, cudaStream_t stream) {
+                  float out_norm_eps, int prologue, const float *gate_A, int decay,
+                  cudaStream_t stream) {
     const int64_t NH = N * H;
     const float read = rule == GDR_RULE_ADDITIVE ? 0.f : 1.f;
+    const bool pc = decay == GDR_DECAY_CHANNEL;
     if (dtype == GDR_BF16)
         return launch_decode_dtype<__nv_bfloat16>(q, k, v, log_alpha, beta, S, o, NH, dk, dv,
                                                   read, out_gate, out_norm_weight, out_norm_eps,
-                                                  prologue, gate_A, H, stream);
+                                                  prologue, gate_A, H, pc, stream);
     return launch_decode_dtype<float>(q, k, v, log_alpha, beta, S, o, NH, dk, dv, read, out_gate,
-                                      out_norm_weight, out_norm_eps, prologue, gate_A, H, stream);
+                                      out_norm_weight, out_norm_eps, prologue, gate_A, H, pc, stream);
 }
 
 }  // namespace gdr

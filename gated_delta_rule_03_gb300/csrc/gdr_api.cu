@@ -16,10 +16,12 @@ bool use_tensor_path(int dk, int dv, int dtype) {
     return dtype == GDR_BF16 && dk == 128 && (dv == 128 || dv == 256);
 }
 
-WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype) {
+WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype,
+                   int decay) {
     WsLayout L;
     memset(&L, 0, sizeof(L));
-    L.tensor_path = use_tensor_path(dk, dv, dtype);
+    // per-channel rates take the exact path
+    L.tensor_path = decay == GDR_DECAY_HEAD && use_tensor_path(dk, dv, dtype);
     L.max_chunks = total_tokens / kChunk + num_seqs;
     size_t off = 0;
     L.ctl = off;
@@ -38,6 +40,8 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
         off = align_up(off + sizeof(float) * per * kChunk, 256);
         L.g = off;  // gamma, kdec, and the prologue's 1/|q|, 1/|k| per chunk token
         off = align_up(off + sizeof(float) * per * 4, 256);
+        L.gc = off;  // per-channel rates: the cumulative log decay per chunk token and channel
+        if (decay == GDR_DECAY_CHANNEL) off = align_up(off + sizeof(float) * per * dk, 256);
     } else {
         L.T = off;  // two 64x64 bf16 matrices per (chunk, head)
         off = align_up(off + (size_t)L.max_chunks * (size_t)H * 2 * kChunk * kChunk * 2, 256);
@@ -82,13 +86,15 @@ struct Opts {
     float out_norm_eps = 0.f;
     int prologue = GDR_PROLOGUE_NONE;
     const float *gate_A = nullptr;
+    int decay = GDR_DECAY_HEAD;
 };
 
-// Reserved words must be zero; the output-step fields need a gate; pointers 16-byte aligned.
+// Known rule, prologue and decay; the output-step fields need a gate; pointers aligned.
 static int check_options(const gdr_options *opt, Opts *o) {
     *o = Opts();
     if (!opt) return GDR_OK;
-    if (opt->reserved != 0) return GDR_ERR_INVALID_ARG;
+    if (opt->decay != GDR_DECAY_HEAD && opt->decay != GDR_DECAY_CHANNEL) return GDR_ERR_INVALID_ARG;
+    o->decay = opt->decay;
     if (opt->rule != GDR_RULE_DELTA && opt->rule != GDR_RULE_ADDITIVE) return GDR_ERR_UNSUPPORTED;
     o->rule = opt->rule;
     if (opt->prologue != GDR_PROLOGUE_NONE && opt->prologue != GDR_PROLOGUE_LAYER)
@@ -142,6 +148,14 @@ size_t gdr_chunk_fwd_workspace_size(int64_t num_seqs, int64_t total_tokens, int 
     return ws_layout(num_seqs, total_tokens, H, d_k, d_v, dtype).total;
 }
 
+size_t gdr_chunk_fwd_workspace_size_ex(int64_t num_seqs, int64_t total_tokens, int H, int d_k,
+                                       int d_v, int chunk, int dtype, const gdr_options *options) {
+    Opts op;
+    if (check_options(options, &op) != GDR_OK) return 0;
+    if (check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype) != GDR_OK) return 0;
+    return ws_layout(num_seqs, total_tokens, H, d_k, d_v, dtype, op.decay).total;
+}
+
 int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
                      const float *beta, const float *S0, const int32_t *cu_seqlens,
                      int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v, int chunk,
@@ -162,7 +176,7 @@ int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     const void *ptrs4[] = {log_alpha, beta, cu_seqlens};
     for (const void *p : ptrs4)
         if (p && !aligned4(p)) return GDR_ERR_ALIGNMENT;
-    const WsLayout L = ws_layout(num_seqs, total_tokens, H, d_k, d_v, dtype);
+    const WsLayout L = ws_layout(num_seqs, total_tokens, H, d_k, d_v, dtype, op.decay);
     if (workspace_bytes < L.total) return GDR_ERR_WORKSPACE;
     const size_t esz = dtype == GDR_F32 ? 4 : 2;
     const size_t o_bytes = (size_t)total_tokens * H * d_v * esz;
@@ -185,6 +199,7 @@ int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     a.out_norm_eps = op.out_norm_eps;
     a.prologue = op.prologue;
     a.gate_A = op.gate_A;
+    a.decay = op.decay;
     a.o = o; a.S_final = S_final;
     a.ws = (char *)workspace;
     a.stream = (cudaStream_t)stream;
@@ -232,7 +247,7 @@ int gdr_decode_step_ex(const void *q, const void *k, const void *v, const float 
     if (op.out_gate && overlaps(op.out_gate, (size_t)N * H * d_v * esz, o, (size_t)N * H * d_v * esz))
         return GDR_ERR_INVALID_ARG;
     return launch_decode(q, k, v, log_alpha, beta, S, o, N, H, d_k, d_v, dtype, op.rule, op.out_gate,
-                         op.out_norm_weight, op.out_norm_eps, op.prologue, op.gate_A,
+                         op.out_norm_weight, op.out_norm_eps, op.prologue, op.gate_A, op.decay,
                          (cudaStream_t)stream);
 }
 

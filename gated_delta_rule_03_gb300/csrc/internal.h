@@ -41,6 +41,7 @@ struct PrefillArgs {
     // the layer's prologue (unit-length q and k, gates from pre-activations)
     int prologue;
     const float *gate_A;
+    int decay;  // GDR_DECAY_HEAD, or GDR_DECAY_CHANNEL: log_alpha [tokens, H, d_k]
     void *o;
     float *S_final;
     char *ws;
@@ -58,6 +59,8 @@ struct WsLayout {
     size_t plan;          // int4[max_chunks]: (sequence, first token, tokens, chunk index)
     size_t seq_chunk;     // int32[kMaxPhases][num_seqs + 1]: first chunk of each sequence per phase
     size_t W, U, A, g;    // fp32 per-chunk intermediates of the exact path (g: gamma, kdec)
+    size_t gc;            // exact path, per-channel rates: fp32 [chunk * H][C][d_k] cumulative
+                          // log decay per key channel
     size_t T;             // tensor-core path: bf16 [max_chunks * H][2][64][64] T' and A^T per unit
     size_t G;             // tensor-core path: fp32 [max_chunks * H][256] decay factors per unit
     size_t S;             // tensor-core path: fp32 [num_seqs][H][dk][dv] state between phases
@@ -73,7 +76,8 @@ struct WsLayout {
 };
 
 bool use_tensor_path(int dk, int dv, int dtype);
-WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype);
+WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype,
+                   int decay = GDR_DECAY_HEAD);
 
 // Launchers (return GDR_OK or GDR_ERR_CUDA).
 // The planning kernel for a schedule (the fused schedule, 0, plans one phase and clears
@@ -95,7 +99,8 @@ int tc_schedule_query(int64_t num_seqs, int64_t total_tokens, int H, int dv, boo
 int launch_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, float *S, void *o, int64_t N, int H, int dk, int dv,
                   int dtype, int rule, const void *out_gate, const float *out_norm_weight,
-                  float out_norm_eps, int prologue, const float *gate_A, cudaStream_t stream);
+                  float out_norm_eps, int prologue, const float *gate_A, int decay,
+                  cudaStream_t stream);
 // The output step over `rows` rows of d_v entries of o, in place (prefill paths that do
 // not fuse it).
 int launch_out_norm_gate(void *o, const void *z, const float *w, float eps, int64_t rows, int dv,

@@ -197,6 +197,8 @@ template <int DK> struct PrepSmem {
     static constexpr int CP = kChunk + 1;
     static constexpr size_t floats = 2 * kChunk * KP + 4 * kChunk * CP + 5 * kChunk;
     static constexpr size_t bytes = floats * sizeof(float);
+    // per-channel rates: the cumulative log decay [C][KP] after the rest
+    static constexpr size_t bytes_per_channel = bytes + kChunk * KP * sizeof(float);
 };
 
 template <typename Tin, int DK>
@@ -206,11 +208,16 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
                   int dv, const int4 *__restrict__ plan, const int32_t *__restrict__ ctl,
                   float *__restrict__ Wws, float *__restrict__ Uws, float *__restrict__ Aws,
                   float *__restrict__ gws, int additive, int prologue,
-                  const float *__restrict__ gate_A) {
+                  const float *__restrict__ gate_A, float *__restrict__ gcws) {
     // gws receives, per chunk, gamma[C], kdec[C], then 1/|q_t| and 1/|k_t| (ones without
     // the prologue). With the additive rule the write does not read the state: L = 0 (so
     // T = diag(beta)) and W = 0. With the layer's prologue the rows of q and k are scaled
     // to unit length here and the gates come from their pre-activations.
+    // With one rate per key channel (gcws non-null; log_alpha [tokens, H, DK]) the decay
+    // moves inside the key products: g_t is a vector, the Gram entries are
+    // sum_d k_t[d] k_i[d] exp(g_t[d] - g_i[d]) (likewise q_t.k_i), W = T (gamma . K) by
+    // rows, and gcws receives g per chunk token and channel for the chain; gamma and kdec
+    // are then ones. Every exponent is g_t - g_i with i <= t, or g_t: all factors <= 1.
     using SM = PrepSmem<DK>;
     constexpr int KP = SM::KP, CP = SM::CP, C = kChunk;
     const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -231,6 +238,8 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     float *gam = bs + C;              // [C] gamma
     float *nq = gam + C;              // [C] 1/|q_t| (prologue), else 1
     float *nk = nq + C;               // [C] 1/|k_t|
+    float *Gs = nk + C;               // [C][KP] per-channel rates: g_t[d] (after the rest)
+    const bool per_channel = gcws != nullptr;
 
     for (int idx = tid; idx < C * DK; idx += blockDim.x) {
         const int t = idx / DK, d = idx % DK;
@@ -249,14 +258,34 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
             const size_t off = (size_t)(t0 + tid) * H + h;
             if (prologue) {
                 b = prologue_beta(beta[off]);
-                a = expf(prologue_log_alpha(log_alpha[off], gate_A ? gate_A[h] : 1.f));
+                if (!per_channel) a = expf(prologue_log_alpha(log_alpha[off], gate_A ? gate_A[h] : 1.f));
             } else {
                 b = beta[off];
-                a = expf(log_alpha[off]);
+                if (!per_channel) a = expf(log_alpha[off]);
             }
         }
         bs[tid] = b;
-        al[tid] = a;
+        al[tid] = a;  // (per-channel rates: 1, so the per-head factors below are ones)
+    }
+    if (per_channel) {  // log alpha per token and channel (0 on padding rows)
+        const float A = prologue && gate_A ? gate_A[h] : 1.f;
+        for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+            const int t = idx / DK, d = idx % DK;
+            float la = 0.f;
+            if (t < len) {
+                const float x = log_alpha[((size_t)(t0 + t) * H + h) * DK + d];
+                la = prologue ? prologue_log_alpha(x, A) : x;
+            }
+            Gs[t * KP + d] = la;
+        }
+        __syncthreads();
+        if (tid < DK) {  // inclusive prefix sum over the chunk's tokens, one channel a thread
+            float acc = 0.f;
+            for (int t = 0; t < C; ++t) {
+                acc += Gs[t * KP + tid];
+                Gs[t * KP + tid] = acc;
+            }
+        }
     }
     __syncthreads();
     if (prologue) {  // unit-length rows: four threads per row of k and of q
@@ -298,7 +327,14 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     for (int idx = tid; idx < C * C; idx += blockDim.x) {
         const int t = idx / C, i = idx % C;
         float kk = 0.f, qk = 0.f, dec = 0.f;
-        if (i <= t) {
+        if (i <= t && per_channel) {
+            for (int d = 0; d < DK; ++d) {
+                const float ki = ks[i * KP + d] * expf(Gs[t * KP + d] - Gs[i * KP + d]);
+                kk = fmaf(ks[t * KP + d], ki, kk);
+                qk = fmaf(qs[t * KP + d], ki, qk);
+            }
+            dec = 1.f;
+        } else if (i <= t) {
             for (int d = 0; d < DK; ++d) {
                 const float ki = ks[i * KP + d];
                 kk = fmaf(ks[t * KP + d], ki, kk);
@@ -333,9 +369,17 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     for (int idx = tid; idx < C * DK; idx += blockDim.x) {
         const int t = idx / DK, d = idx % DK;
         float s = 0.f;
-        for (int i = 0; i <= t; ++i) s = fmaf(Tm[t * CP + i] * gam[i], ks[i * KP + d], s);
+        if (per_channel) {  // rows gamma_i[d] k_i[d]
+            for (int i = 0; i <= t; ++i)
+                s = fmaf(Tm[t * CP + i] * expf(Gs[i * KP + d]), ks[i * KP + d], s);
+        } else {
+            for (int i = 0; i <= t; ++i) s = fmaf(Tm[t * CP + i] * gam[i], ks[i * KP + d], s);
+        }
         Wout[idx] = additive ? 0.f : s;
     }
+    if (per_channel)
+        for (int idx = tid; idx < C * DK; idx += blockDim.x)
+            gcws[cb * C * DK + idx] = Gs[(idx / DK) * KP + idx % DK];
     float *Uout = Uws + cb * C * dv;
     for (int idx = tid; idx < C * dv; idx += blockDim.x) {
         const int t = idx / dv, j = idx % dv;
@@ -375,7 +419,10 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const int32_t *__restrict__ seq_chunk, const int32_t *__restrict__ ctl,
                    const float *__restrict__ Wws, const float *__restrict__ Uws,
                    const float *__restrict__ Aws, const float *__restrict__ gws,
-                   Tin *__restrict__ o, float *__restrict__ S_final) {
+                   const float *__restrict__ gcws, Tin *__restrict__ o, float *__restrict__ S_final) {
+    // gcws (per-channel rates, else null): g_t[d] per chunk token and channel. Then
+    // q_t is scaled by gamma_t[d] = exp(g_t[d]), k_i by exp(g_C[d] - g_i[d]) for the
+    // state update, and row d of S decays by exp(g_C[d]); gamma and kdec are ones.
     using SM = ChainSmem<DK>;
     constexpr int KP = SM::KP, SP = SM::SP, C = kChunk, NC = kChainCols, CP = C + 1;
     if (ctl[0] != GDR_OK) return;
@@ -426,6 +473,11 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 const size_t off = ((size_t)(tc0 + t) * H + h) * DK + d;
                 kv = to_f32(k[off]) * nqk[C + t];
                 qv = to_f32(q[off]) * nqk[t];
+                if (gcws) {
+                    const float *g = gcws + cb * C * DK;
+                    qv *= expf(g[t * DK + d]);
+                    kv *= expf(g[(C - 1) * DK + d] - g[t * DK + d]);
+                }
             }
             ks[t * KP + d] = kv;
             qs[t * KP + d] = qv;
@@ -482,7 +534,7 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             constexpr int TPR = 256 / DK;          // threads per state row
             constexpr int CPT = NC / TPR;          // columns per thread
             const int d = tid / TPR, jb = (tid % TPR) * CPT;
-            const float gC = gam[C - 1];
+            const float gC = gcws ? expf(gcws[cb * C * DK + (C - 1) * DK + d]) : gam[C - 1];
             float acc[CPT];
 #pragma unroll
             for (int x = 0; x < CPT; ++x) acc[x] = gC * Ss[d * SP + jb + x];
@@ -512,9 +564,11 @@ static int launch_exact_t(const PrefillArgs &a, const WsLayout &L) {
     float *W = (float *)(a.ws + L.W), *U = (float *)(a.ws + L.U);
     float *A = (float *)(a.ws + L.A), *g = (float *)(a.ws + L.g);
     cudaError_t e;
+    const bool per_channel = a.decay == GDR_DECAY_CHANNEL;
+    const size_t prep_smem = per_channel ? PrepSmem<DK>::bytes_per_channel : PrepSmem<DK>::bytes;
+    float *gc = per_channel ? (float *)(a.ws + L.gc) : nullptr;
     e = cudaFuncSetAttribute(exact_prep_kernel<Tin, DK>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)PrepSmem<DK>::bytes);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
     if (e != cudaSuccess) return GDR_ERR_CUDA;
     e = cudaFuncSetAttribute(exact_chain_kernel<Tin, DK>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -522,17 +576,17 @@ static int launch_exact_t(const PrefillArgs &a, const WsLayout &L) {
     if (e != cudaSuccess) return GDR_ERR_CUDA;
     if (L.max_chunks > 0) {
         dim3 grid((unsigned)L.max_chunks, (unsigned)a.H);
-        exact_prep_kernel<Tin, DK><<<grid, 256, PrepSmem<DK>::bytes, a.stream>>>(
+        exact_prep_kernel<Tin, DK><<<grid, 256, prep_smem, a.stream>>>(
             (const Tin *)a.q, (const Tin *)a.k, (const Tin *)a.v, a.log_alpha, a.beta, a.H, a.dv,
             (const int4 *)(a.ws + L.plan), ctl, W, U, A, g, a.rule == GDR_RULE_ADDITIVE ? 1 : 0,
-            a.prologue, a.gate_A);
+            a.prologue, a.gate_A, gc);
         e = cudaGetLastError();
         if (e != cudaSuccess) return GDR_ERR_CUDA;
     }
     dim3 grid2((unsigned)(a.num_seqs * a.H), (unsigned)(a.dv / kChainCols));
     exact_chain_kernel<Tin, DK><<<grid2, 256, ChainSmem<DK>::bytes, a.stream>>>(
         (const Tin *)a.q, (const Tin *)a.k, a.S0, a.cu_seqlens, a.num_seqs, a.total_tokens, a.H,
-        a.dv, (const int32_t *)(a.ws + L.seq_chunk), ctl, W, U, A, g, (Tin *)a.o, a.S_final);
+        a.dv, (const int32_t *)(a.ws + L.seq_chunk), ctl, W, U, A, g, gc, (Tin *)a.o, a.S_final);
     return cuda_status(cudaGetLastError());
 }
 

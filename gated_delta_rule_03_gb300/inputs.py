@@ -91,8 +91,9 @@ def _store(x, dtype):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(TORCH_DTYPES[dtype])
 
 
-def _gates(rng, shape, gate):
-    a = rng.standard_normal(shape)
+def _gates(rng, shape, gate, channels=None):
+    # channels: one forget rate per key channel, log alpha of shape shape + (channels,)
+    a = rng.standard_normal(shape if channels is None else tuple(shape) + (channels,))
     b = rng.standard_normal(shape)
     if gate == "default":
         log_alpha = -np.logaddexp(0.0, a)
@@ -110,11 +111,12 @@ def _gates(rng, shape, gate):
 
 
 def prefill_inputs(seq_lens, H, dk, dv, dtype="bf16", seed=0, s0_std=0.0, chunk=64,
-                   gate="default", rng=None, packed=None):
+                   gate="default", rng=None, packed=None, decay="head"):
     """Packed inputs for sequences of the given lengths.
 
     `packed` chooses whether cu_seqlens is produced; by default it is when the
-    lengths differ. Equal-length batches are passed without cu_seqlens.
+    lengths differ. Equal-length batches are passed without cu_seqlens. decay
+    "channel" draws one forget rate per key channel (log_alpha [T, H, dk]).
     """
     rng = np.random.default_rng(seed) if rng is None else rng
     seq_lens = [int(x) for x in seq_lens]
@@ -122,7 +124,7 @@ def prefill_inputs(seq_lens, H, dk, dv, dtype="bf16", seed=0, s0_std=0.0, chunk=
     q = _unit_rows(rng.standard_normal((total, H, dk)))
     k = _unit_rows(rng.standard_normal((total, H, dk)))
     v = rng.standard_normal((total, H, dv))
-    log_alpha, beta = _gates(rng, (total, H), gate)
+    log_alpha, beta = _gates(rng, (total, H), gate, dk if decay == "channel" else None)
     S0 = None
     if s0_std > 0:
         S0 = torch.from_numpy(
@@ -151,7 +153,8 @@ def workload_prefill(name, gate="default"):
                           s0_std=w["s0_std"], chunk=w["chunk"], gate=gate, rng=rng)
 
 
-def decode_inputs(N, H, dk, dv, steps, dtype="bf16", seed=3, s0_std=0.02, gate="default"):
+def decode_inputs(N, H, dk, dv, steps, dtype="bf16", seed=3, s0_std=0.02, gate="default",
+                  decay="head"):
     """State plus per-step inputs for `steps` consecutive decode steps."""
     rng = np.random.default_rng(seed)
     S = torch.from_numpy((s0_std * rng.standard_normal((N, H, dk, dv))).astype(np.float32))
@@ -160,7 +163,7 @@ def decode_inputs(N, H, dk, dv, steps, dtype="bf16", seed=3, s0_std=0.02, gate="
         qs.append(_store(_unit_rows(rng.standard_normal((N, H, dk))), dtype))
         ks.append(_store(_unit_rows(rng.standard_normal((N, H, dk))), dtype))
         vs.append(_store(rng.standard_normal((N, H, dv)), dtype))
-        la, b = _gates(rng, (N, H), gate)
+        la, b = _gates(rng, (N, H), gate, dk if decay == "channel" else None)
         las.append(la)
         bs.append(b)
     return DecodeInputs(S=S, q=torch.stack(qs), k=torch.stack(ks), v=torch.stack(vs),

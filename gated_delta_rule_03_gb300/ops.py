@@ -17,25 +17,39 @@ GDR_F32, GDR_BF16 = 0, 1
 _DTYPES = {torch.float32: GDR_F32, torch.bfloat16: GDR_BF16}
 # the recurrence's write rule (gdr_options.rule)
 RULES = {"delta": 0, "additive": 1}
+# the forget gate's granularity (gdr_options.decay): one rate per head, or per key channel
+DECAYS = {"head": 0, "channel": 1}
 
 
 class GdrOptions(ctypes.Structure):
     """struct gdr_options of gdr.h."""
     _fields_ = [("rule", ctypes.c_int), ("out_norm_eps", ctypes.c_float),
                 ("out_gate", ctypes.c_void_p), ("out_norm_weight", ctypes.c_void_p),
-                ("prologue", ctypes.c_int), ("reserved", ctypes.c_int),
+                ("prologue", ctypes.c_int), ("decay", ctypes.c_int),
                 ("gate_A", ctypes.c_void_p)]
 
 
 def _options(rule, out_gate=None, out_norm_weight=None, out_norm_eps=0.0, prologue=False,
-             gate_A=None):
+             gate_A=None, decay="head"):
     if rule not in RULES:
         raise ValueError(f"unknown rule {rule!r}; expected one of {sorted(RULES)}")
     opt = GdrOptions(RULES[rule], float(out_norm_eps) if out_gate is not None else 0.0,
                      None if out_gate is None else out_gate.data_ptr(),
                      None if out_norm_weight is None else out_norm_weight.data_ptr(),
-                     1 if prologue else 0, 0, None if gate_A is None else gate_A.data_ptr())
+                     1 if prologue else 0, DECAYS[decay],
+                     None if gate_A is None else gate_A.data_ptr())
     return ctypes.byref(opt)
+
+
+def _decay_of(log_alpha, lead, dk):
+    """'head' for log_alpha of shape `lead`, 'channel' for `lead` + (dk,)."""
+    shape = tuple(log_alpha.shape)
+    if shape == tuple(lead):
+        return "head"
+    if shape == tuple(lead) + (dk,):
+        return "channel"
+    raise ValueError(f"log_alpha must have shape {tuple(lead)} (one rate per head) or "
+                     f"{tuple(lead) + (dk,)} (one rate per key channel), got {shape}")
 
 
 def _check_prologue(prologue, gate_A, H, device):
@@ -87,6 +101,9 @@ def _load():
     lib.gdr_status_string.restype = ctypes.c_char_p
     lib.gdr_chunk_fwd_workspace_size.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int]
     lib.gdr_chunk_fwd_workspace_size.restype = ctypes.c_size_t
+    lib.gdr_chunk_fwd_workspace_size_ex.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int,
+                                                    ctypes.c_void_p]
+    lib.gdr_chunk_fwd_workspace_size_ex.restype = ctypes.c_size_t
     lib.gdr_chunk_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, i64, i64, c_int, c_int, c_int,
                                   c_int, c_int, vp, fp, vp, ctypes.c_size_t, vp]
     lib.gdr_chunk_fwd.restype = c_int
@@ -143,11 +160,18 @@ def _need(t, name, dtype=None, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
-def chunk_fwd_workspace_size(num_seqs, total_tokens, H, dk, dv, chunk=64, dtype=torch.bfloat16):
-    """Workspace bytes gdr_chunk_fwd needs (0 if the sizes are unsupported)."""
-    return int(_load().gdr_chunk_fwd_workspace_size(int(num_seqs), int(total_tokens), int(H),
-                                                    int(dk), int(dv), int(chunk),
-                                                    _DTYPES[dtype]))
+def chunk_fwd_workspace_size(num_seqs, total_tokens, H, dk, dv, chunk=64, dtype=torch.bfloat16,
+                             decay="head"):
+    """Workspace bytes gdr_chunk_fwd needs (0 if the sizes are unsupported); decay
+    "channel" (per-channel rates, the exact path) through gdr_chunk_fwd_workspace_size_ex."""
+    lib = _load()
+    if decay == "head":
+        return int(lib.gdr_chunk_fwd_workspace_size(int(num_seqs), int(total_tokens), int(H),
+                                                    int(dk), int(dv), int(chunk), _DTYPES[dtype]))
+    opt = GdrOptions(0, 0.0, None, None, 0, DECAYS[decay], None)
+    return int(lib.gdr_chunk_fwd_workspace_size_ex(int(num_seqs), int(total_tokens), int(H),
+                                                   int(dk), int(dv), int(chunk), _DTYPES[dtype],
+                                                   ctypes.addressof(opt)))
 
 
 def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None, chunk=64,
@@ -155,7 +179,9 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
               out_norm_weight=None, out_norm_eps=1e-6, prologue=False, gate_A=None):
     """Chunked prefill (gdr_chunk_fwd).
 
-    q, k [T, H, dk]; v [T, H, dv] (fp32 or bf16); log_alpha, beta [T, H] fp32;
+    q, k [T, H, dk]; v [T, H, dv] (fp32 or bf16); beta [T, H] fp32; log_alpha [T, H]
+    fp32 (one rate per head), or [T, H, dk] (one rate per key channel, gdr_options.decay
+    GDR_DECAY_CHANNEL: the exact fp32 path);
     S0 [num_seqs, H, dk, dv] fp32 or None; cu_seqlens [num_seqs+1] int32 or None
     (then `num_seqs` equal sequences, default 1). Optional preallocated o,
     S_final and workspace (uint8) tensors are used as given. rule: "delta" (the gated
@@ -177,6 +203,7 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
     _need(v, "v", dt, dev)
     _need(log_alpha, "log_alpha", torch.float32, dev)
     _need(beta, "beta", torch.float32, dev)
+    decay = _decay_of(log_alpha, (T, H), dk)
     if cu_seqlens is not None:
         _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
         n = cu_seqlens.numel() - 1
@@ -192,7 +219,7 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
     _need(S_final, "S_final", torch.float32, dev)
     _check_out_step(out_gate, out_norm_weight, o, dv)
     _check_prologue(prologue, gate_A, H, dev)
-    ws_bytes = chunk_fwd_workspace_size(n, T, H, dk, dv, chunk, dt)
+    ws_bytes = chunk_fwd_workspace_size(n, T, H, dk, dv, chunk, dt, decay)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", device=dev)
@@ -201,7 +228,7 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
                               _ptr(S_final), _ptr(workspace),
                               workspace.numel() * workspace.element_size(),
                               _options(rule, out_gate, out_norm_weight, out_norm_eps, prologue,
-                                       gate_A),
+                                       gate_A, decay),
                               _stream_handle(stream, dev))
     _check(st, "gdr_chunk_fwd_ex")
     return o, S_final
@@ -219,8 +246,9 @@ def read_device_status(workspace, stream=None):
 def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None, rule="delta", out_gate=None,
                 out_norm_weight=None, out_norm_eps=1e-6, prologue=False, gate_A=None):
     """One decode step (gdr_decode_step_ex): q, k [N, H, dk]; v [N, H, dv];
-    log_alpha, beta [N, H] fp32; S [N, H, dk, dv] fp32 updated in place; rule "delta"
-    (the gated delta rule) or "additive" (S <- alpha S + beta k v^T). Returns o [N, H, dv]."""
+    beta [N, H] fp32; log_alpha [N, H] fp32, or [N, H, dk] (one rate per key channel);
+    S [N, H, dk, dv] fp32 updated in place; rule "delta" (the gated delta rule) or
+    "additive" (S <- alpha S + beta k v^T). Returns o [N, H, dv]."""
     lib = _load()
     _need(q, "q")
     dev, dt = q.device, q.dtype
@@ -231,6 +259,7 @@ def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None, rule="delta", 
     _need(log_alpha, "log_alpha", torch.float32, dev)
     _need(beta, "beta", torch.float32, dev)
     _need(S, "S", torch.float32, dev)
+    decay = _decay_of(log_alpha, (N, H), dk)
     if o is None:
         o = torch.empty((N, H, dv), dtype=dt, device=dev)
     _need(o, "o", dt, dev)
@@ -239,7 +268,7 @@ def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None, rule="delta", 
     st = lib.gdr_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S),
                                 _ptr(o), N, H, dk, dv, _DTYPES[dt],
                                 _options(rule, out_gate, out_norm_weight, out_norm_eps, prologue,
-                                         gate_A),
+                                         gate_A, decay),
                                 _stream_handle(stream, dev))
     _check(st, "gdr_decode_step_ex")
     return o

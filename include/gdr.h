@@ -185,8 +185,7 @@ int gdr_decode_step(const void *q, const void *k, const void *v, const float *lo
 enum { GDR_RULE_DELTA = 0, GDR_RULE_ADDITIVE = 1 };
 
 /*
- * Options of the _ex entry points. A null pointer means all defaults; the
- * reserved words must be zero (else GDR_ERR_INVALID_ARG).
+ * Options of the _ex entry points. A null pointer means all defaults.
  *   rule             GDR_RULE_DELTA or GDR_RULE_ADDITIVE (else GDR_ERR_UNSUPPORTED)
  *   out_gate         the layer's output step, applied to o before it is stored
  *                    ("Linear attention" (arsalanzafar.ai), "A naive PyTorch
@@ -211,17 +210,39 @@ enum { GDR_RULE_DELTA = 0, GDR_RULE_ADDITIVE = 1 };
  *   gate_A           A: [H] fp32 per-head rate (A_h > 0; the layer keeps log A and
  *                    exponentiates it), 4-byte aligned; null means all ones. Only
  *                    with GDR_PROLOGUE_LAYER.
+ *   decay            GDR_DECAY_HEAD (default): one forget rate per token and head,
+ *                    log_alpha [tokens, H] ([N, H] for decode). GDR_DECAY_CHANNEL: one
+ *                    rate per token, head and key channel, log_alpha [tokens, H, d_k]
+ *                    ([N, H, d_k] for decode), fp32, 4-byte aligned: row c of the
+ *                    state decays by its own alpha_t[c], S'_t = diag(alpha_t) S_{t-1},
+ *                    the other steps unchanged ("Attention as Matrix Algebra: From
+ *                    Softmax to the Delta Rule", section 10 "Where this goes next":
+ *                    Kimi Delta Attention gives each feature channel its own rate).
+ *                    With GDR_PROLOGUE_LAYER the pre-activation a has that shape too.
+ *                    Prefill with per-channel rates always takes the exact fp32 path
+ *                    (GDR_PATH_EXACT), whose workspace gdr_chunk_fwd_workspace_size_ex
+ *                    sizes. Other values: GDR_ERR_INVALID_ARG.
  */
 enum { GDR_PROLOGUE_NONE = 0, GDR_PROLOGUE_LAYER = 1 };
+enum { GDR_DECAY_HEAD = 0, GDR_DECAY_CHANNEL = 1 };
 typedef struct gdr_options {
     int rule;
     float out_norm_eps;
     const void *out_gate;
     const float *out_norm_weight;
     int prologue;
-    int reserved;
+    int decay;
     const float *gate_A;
 } gdr_options;
+
+/*
+ * Workspace bytes of a gdr_chunk_fwd_ex call with these sizes and options
+ * (the options decide the kernel path: per-channel rates take the exact one);
+ * 0 for unsupported sizes or options. With a null options pointer it equals
+ * gdr_chunk_fwd_workspace_size.
+ */
+size_t gdr_chunk_fwd_workspace_size_ex(int64_t num_seqs, int64_t total_tokens, int H, int d_k,
+                                       int d_v, int chunk, int dtype, const gdr_options *options);
 
 /*
  * gdr_chunk_fwd with options: the same arguments, layouts, ownership and

@@ -139,10 +139,14 @@ def layer_prologue(q, k, a, b, A=None):
 
         log alpha = -A_h softplus(a),    beta = sigmoid(b),
 
-    q, k [..., H, d_k]; a, b [..., H]; A [H] (None: ones). Returns (q, k, log_alpha, beta)
-    for forward() / decode()."""
+    q, k [..., H, d_k]; b [..., H]; a [..., H], or [..., H, d_k] for one rate per key
+    channel; A [H] (None: ones). Returns (q, k, log_alpha, beta) for forward() / decode()."""
     q, k, a, b = _f64(q), _f64(k), _f64(a), _f64(b)
-    A = np.ones(a.shape[-1]) if A is None else _f64(A)
+    per_channel = a.ndim == q.ndim
+    H = a.shape[-2] if per_channel else a.shape[-1]
+    A = np.ones(H) if A is None else _f64(A)
+    if per_channel:
+        A = A[:, None]
     qn = q / np.maximum(np.linalg.norm(q, axis=-1, keepdims=True), 1e-12)
     kn = k / np.maximum(np.linalg.norm(k, axis=-1, keepdims=True), 1e-12)
     softplus = np.logaddexp(0.0, a)

@@ -111,8 +111,8 @@ def test_invalid_arguments_rejected_on_the_host(lib):
 
 
 def test_options_validated_on_the_host(lib):
-    # gdr_options: an unknown rule is unsupported, a nonzero reserved word is invalid; both
-    # are rejected before any other check, so fake pointers are never touched
+    # gdr_options: an unknown rule is unsupported, an unknown decay granularity is invalid;
+    # both are rejected before any other check, so fake pointers are never touched
     from gated_delta_rule_03_gb300.ops import GdrOptions
     A = 0x10000
     p = [_fake(A + i * 0x1000000) for i in range(12)]
@@ -127,11 +127,11 @@ def test_options_validated_on_the_host(lib):
                                       1, opt, None)
 
     bad_rule = GdrOptions(2)
-    reserved = GdrOptions(1)
-    reserved.reserved = 1
+    bad_decay = GdrOptions(1)
+    bad_decay.decay = 2
     for f in (call, dcall):
         assert f(ctypes.byref(bad_rule)) == -2
-        assert f(ctypes.byref(reserved)) == -1
+        assert f(ctypes.byref(bad_decay)) == -1
     # the output-step fields: a weight or an eps without a gate, a negative eps, an
     # unaligned gate
     fake = lambda a: ctypes.c_void_p(a)
@@ -158,3 +158,21 @@ def test_options_validated_on_the_host(lib):
                                 0, p[5], p[6], p[7], ws_bytes, ctypes.byref(ok), None) == -1
     assert lib.gdr_decode_step_ex(p[0], p[1], p[2], p[3], p[4], p[5], p[6], 0, 2, 128, 128, 1,
                                   ctypes.byref(ok), None) == 0
+
+
+def test_per_channel_workspace_takes_the_exact_layout(lib):
+    # per-channel rates run on the exact path: the _ex size query says so, and the plain
+    # query (head rates) is unchanged; bad options size nothing
+    from gated_delta_rule_03_gb300.ops import GdrOptions
+    head = lib.gdr_chunk_fwd_workspace_size(4, 4 * 4096, 16, 128, 128, 64, 1)
+    pc = GdrOptions(0)
+    pc.decay = 1
+    chan = lib.gdr_chunk_fwd_workspace_size_ex(4, 4 * 4096, 16, 128, 128, 64, 1, ctypes.byref(pc))
+    exact_f32 = lib.gdr_chunk_fwd_workspace_size(4, 4 * 4096, 16, 128, 128, 64, 0)
+    assert lib.gdr_chunk_fwd_workspace_size_ex(4, 4 * 4096, 16, 128, 128, 64, 1, None) == head
+    # the exact layout plus one fp32 [C][d_k] block of cumulative log decay per unit
+    units = (4 * 4096 // 64 + 4) * 16
+    assert chan >= exact_f32 + units * 64 * 128 * 4
+    bad = GdrOptions(0)
+    bad.decay = 7
+    assert lib.gdr_chunk_fwd_workspace_size_ex(1, 128, 2, 64, 64, 64, 0, ctypes.byref(bad)) == 0

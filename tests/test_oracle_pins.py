@@ -558,6 +558,16 @@ def test_layer_prologue_closed_forms():
     np.testing.assert_allclose(la2[0, 0], -np.exp(-40.0), rtol=1e-12)
 
 
+def test_layer_prologue_per_channel_rates():
+    # a [T, H, d_k]: each channel's rate from its own pre-activation, A_h per head
+    q = k = np.ones((1, 2, 3))
+    a = np.array([[[0.0, 30.0, -40.0], [0.0, 0.0, 0.0]]])
+    _, _, la, _ = oracle.layer_prologue(q, k, a, np.zeros((1, 2)), A=np.array([1.0, 3.0]))
+    np.testing.assert_allclose(la[0, 0], [-np.log(2.0), -(30.0 + np.log1p(np.exp(-30.0))),
+                                          -np.exp(-40.0)], rtol=1e-12)
+    np.testing.assert_allclose(la[0, 1], [-3 * np.log(2.0)] * 3, rtol=1e-15)
+
+
 def test_layer_prologue_makes_unit_vectors_and_gates_in_range():
     rng = np.random.default_rng(11)
     q, k = 5 * rng.standard_normal((2, 7, 3, 16))
