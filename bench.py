@@ -61,9 +61,11 @@ def prefill_bytes(inp):
     """Algorithmic HBM bytes of one prefill call: read q, k, v and the gates, write o,
     write S_final (and read S0 when given)."""
     esz = 2 if inp.dtype == "bf16" else 4
-    per_token_head = (2 * inp.dk + 2 * inp.dv) * esz + 8
+    per_token_head = (2 * inp.dk + 2 * inp.dv) * esz
+    gates = (inp.log_alpha.numel() + inp.beta.numel()) * 4  # one or d_k forget rates, beta
     state = inp.num_seqs * inp.H * inp.dk * inp.dv * 4
-    return inp.total_tokens * inp.H * per_token_head + state * (2 if inp.S0 is not None else 1)
+    return (inp.total_tokens * inp.H * per_token_head + gates +
+            state * (2 if inp.S0 is not None else 1))
 
 
 def decode_bytes(N, H, dk, dv, esz=2):
@@ -231,7 +233,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    inp = inputs.workload_prefill(args.workload)
+    inp = inputs.workload_prefill(args.workload, decay=args.decay)
     sample = oracle_prefill_sample(inp)
     threads = oracle.default_threads()
     for _ in range(args.warmup):
@@ -260,6 +262,9 @@ def run_reference(args):
 
 def workload_config(inp, name):
     equal = len(set(inp.seq_lens)) == 1
+    if inp.log_alpha.dim() == 3:
+        name += " with one forget rate per key channel"
+
     lens = f"T={inp.seq_lens[0]}" if equal else f"T in {min(inp.seq_lens)}..{max(inp.seq_lens)} " \
                                                  f"packed ({inp.total_tokens} tokens)"
     s0 = "S0=0" if inp.S0 is None else "S0 ~ N(0, 0.02^2)"
@@ -281,14 +286,14 @@ def run_gdr(args):
     stream = torch.cuda.Stream(device)
     peaks = load_peaks()
 
-    inp = inputs.workload_prefill(args.workload)
+    inp = inputs.workload_prefill(args.workload, decay=args.decay)
     d = lambda t: None if t is None else t.to(device)
     q, k, v, la, b = d(inp.q), d(inp.k), d(inp.v), d(inp.log_alpha), d(inp.beta)
     S0, cu = d(inp.S0), d(inp.cu_seqlens)
     o = torch.empty((inp.total_tokens, inp.H, inp.dv), dtype=q.dtype, device=device)
     S = torch.empty((inp.num_seqs, inp.H, inp.dk, inp.dv), dtype=torch.float32, device=device)
     ws = torch.empty(chunk_fwd_workspace_size(inp.num_seqs, inp.total_tokens, inp.H, inp.dk,
-                                              inp.dv, inp.chunk, q.dtype),
+                                              inp.dv, inp.chunk, q.dtype, args.decay),
                      dtype=torch.uint8, device=device)
 
     def step():
@@ -306,13 +311,16 @@ def run_gdr(args):
     tokens = inp.total_tokens
     value = world * tokens * args.steps / (total_ms / 1e3)
     kernel_launches = ops.chunk_fwd_kernel_launches(inp.num_seqs, inp.total_tokens, inp.H, inp.dk,
-                                                    inp.dv, q.dtype, varlen=cu is not None)
+                                                    inp.dv, q.dtype, varlen=cu is not None,
+                                                    decay=args.decay)
     schedule = ops.chunk_fwd_schedule(inp.num_seqs, inp.total_tokens, inp.H, inp.dk, inp.dv,
-                                      q.dtype, varlen=cu is not None)
-    main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype, schedule=schedule)
+                                      q.dtype, varlen=cu is not None, decay=args.decay)
+    main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype, schedule=schedule,
+                                            decay=args.decay)
     bytes_call = prefill_bytes(inp)
     achieved = bytes_call / (call_ms / 1e3) / 1e9
-    traffic = recorded_traffic(main_kernel, args.workload)
+    workload_key = args.workload + ("" if args.decay == "head" else "_channel")
+    traffic = recorded_traffic(main_kernel, workload_key)
 
     # end to end through the public API: pinned host inputs in, results back out
     pin = lambda t: None if t is None else t.pin_memory()
@@ -350,7 +358,8 @@ def run_gdr(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ops.chunk_fwd_compute_dtype(inp.dk, inp.dv, q.dtype), "data": "synthetic",
+        "dtype": ops.chunk_fwd_compute_dtype(inp.dk, inp.dv, q.dtype, args.decay),
+        "data": "synthetic",
         "config": workload_config(inp, args.workload),
         "roofline": {"kernel": main_kernel, "bound": "hbm", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -416,6 +425,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=["prefill_bf16", "varlen_bf16", "long_bf16"],
                     default=PREFILL_WORKLOAD,
                     help="prefill workload of the step (default: the headline prefill_bf16)")
+    ap.add_argument("--decay", choices=["head", "channel"], default="head",
+                    help="forget rates: one per head (default), or one per key channel")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -14,7 +14,8 @@ Recipe (one numpy PCG64 generator per workload, `numpy.random.default_rng(seed)`
     (arsalanzafar.ai), "A naive PyTorch implementation", F.normalize);
   * v ~ N(0, 1);
   * log alpha = -softplus(a), beta = sigmoid(b), a, b ~ N(0, 1), stored fp32
-    (the gate parameterisation of the same section, with A = 1);
+    (the gate parameterisation of the same section, with A = 1); with one rate per
+    key channel a has one more axis of d_k entries, drawn in its place;
   * S0 ~ N(0, std^2) in fp32 when a workload asks for an initial state;
   * storage rounding: float64 -> float32 -> bf16 (round to nearest even, by torch).
 Gate variants used by stress cases: "slow" gives log alpha = -softplus(a - 6)
@@ -100,7 +101,7 @@ def _gates(rng, shape, gate, channels=None):
     elif gate == "slow":
         log_alpha = -np.logaddexp(0.0, a - 6.0)
     elif gate == "none":
-        log_alpha = np.zeros(shape)
+        log_alpha = np.zeros(a.shape)
     elif gate == "strong":
         log_alpha = -np.logaddexp(0.0, a + 1.5)
     else:
@@ -140,8 +141,9 @@ def prefill_inputs(seq_lens, H, dk, dv, dtype="bf16", seed=0, s0_std=0.0, chunk=
                          chunk=chunk, dtype=dtype)
 
 
-def workload_prefill(name, gate="default"):
-    """Inputs of one of the prefill workloads in WORKLOADS."""
+def workload_prefill(name, gate="default", decay="head"):
+    """Inputs of one of the prefill workloads in WORKLOADS (decay "channel": the same
+    shapes with one forget rate per key channel)."""
     w = WORKLOADS[name]
     rng = np.random.default_rng(w["seed"])
     if "len_range" in w:
@@ -150,7 +152,7 @@ def workload_prefill(name, gate="default"):
     else:
         seq_lens = [w["seq_len"]] * w["num_seqs"]
     return prefill_inputs(seq_lens, w["H"], w["dk"], w["dv"], dtype=w["dtype"],
-                          s0_std=w["s0_std"], chunk=w["chunk"], gate=gate, rng=rng)
+                          s0_std=w["s0_std"], chunk=w["chunk"], gate=gate, rng=rng, decay=decay)
 
 
 def decode_inputs(N, H, dk, dv, steps, dtype="bf16", seed=3, s0_std=0.02, gate="default",

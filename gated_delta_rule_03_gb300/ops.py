@@ -282,16 +282,21 @@ _PATHS = {
 }
 
 
-def chunk_fwd_path(dk, dv, dtype):
+def chunk_fwd_path(dk, dv, dtype, decay="head"):
+    """0 (exact fp32 path) or 1 (tensor cores); per-channel rates take the exact path."""
     st = _load().gdr_chunk_fwd_path(int(dk), int(dv), _DTYPES[dtype])
     if st < 0:
         raise GdrError(st, "gdr_chunk_fwd_path")
-    return st
+    return 0 if decay == "channel" else st
 
 
-def chunk_fwd_kernel_launches(num_seqs, total_tokens, H, dk, dv, dtype, varlen=False):
+def chunk_fwd_kernel_launches(num_seqs, total_tokens, H, dk, dv, dtype, varlen=False,
+                              decay="head"):
     """Kernels one gdr_chunk_fwd call launches for these sizes on the current device
     (varlen: the call passes cu_seqlens)."""
+    if decay == "channel":  # the exact path: plan, per-chunk prep, chain
+        chunk_fwd_path(dk, dv, dtype)
+        return 3 if total_tokens > 0 else 1
     st = _load().gdr_chunk_fwd_kernel_launches(int(num_seqs), int(total_tokens), int(H), int(dk),
                                                int(dv), 64, _DTYPES[dtype], int(bool(varlen)))
     if st < 0:
@@ -302,10 +307,12 @@ def chunk_fwd_kernel_launches(num_seqs, total_tokens, H, dk, dv, dtype, varlen=F
 SCHEDULE_SEGMENTED = 16  # GDR_SCHEDULE_SEGMENTED
 
 
-def chunk_fwd_schedule(num_seqs, total_tokens, H, dk, dv, dtype, varlen=False):
+def chunk_fwd_schedule(num_seqs, total_tokens, H, dk, dv, dtype, varlen=False, decay="head"):
     """Schedule of a gdr_chunk_fwd call with these sizes on the current device: 0 for the
     fused tensor-core schedule, 1 .. 8 phases of the phased one, or SCHEDULE_SEGMENTED + n
-    for the segmented one with n segments per sequence."""
+    for the segmented one with n segments per sequence (the exact path: one phase)."""
+    if decay == "channel":
+        return 1
     st = _load().gdr_chunk_fwd_schedule(int(num_seqs), int(total_tokens), int(H), int(dk),
                                         int(dv), 64, _DTYPES[dtype], int(bool(varlen)))
     if st < 0:
@@ -313,15 +320,16 @@ def chunk_fwd_schedule(num_seqs, total_tokens, H, dk, dv, dtype, varlen=False):
     return st
 
 
-def chunk_fwd_main_kernel(dk, dv, dtype, schedule=None):
+def chunk_fwd_main_kernel(dk, dv, dtype, schedule=None, decay="head"):
     """Name of the kernel that dominates a gdr_chunk_fwd call for these sizes. The fused
-    schedule (0) of the tensor-core path runs the solve and the chains in one kernel."""
-    path = chunk_fwd_path(dk, dv, dtype)
+    schedule (0) of the tensor-core path runs the solve and the chains in one kernel; the
+    exact path (and per-channel rates, which take it) is dominated by its chain."""
+    path = chunk_fwd_path(dk, dv, dtype, decay)
     if path == 1 and schedule == 0:
         return "tc_fused_kernel"
     return _PATHS[path]["main_kernel"]
 
 
-def chunk_fwd_compute_dtype(dk, dv, dtype):
+def chunk_fwd_compute_dtype(dk, dv, dtype, decay="head"):
     """Arithmetic type of the products on the path taken (f32 SIMT or bf16 tensor cores)."""
-    return _PATHS[chunk_fwd_path(dk, dv, dtype)]["compute_dtype"]
+    return _PATHS[chunk_fwd_path(dk, dv, dtype, decay)]["compute_dtype"]
