@@ -221,7 +221,9 @@ __device__ __forceinline__ void transpose_store16(const uint32_t (&r)[32], float
 // The chain of CTA `cta`: (sequence, head, d_v slice) = (cta / n_slices / H, ...).
 // kFused: the CTA shares a cooperative launch with the solve and waits for each chunk's
 // unit to be published before loading its results.
-template <bool kFused>
+// kSeg: a launch of the segmented schedule (p.mode 1 or 2); without it p.mode is 0 and
+// the segment branches compile away.
+template <bool kFused, bool kSeg = false>
 __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUtensorMap &map_k,
                                            const CUtensorMap &map_v, const CUtensorMap &map_t,
                                            const CUtensorMap &map_o, const TcParams &p, int cta) {
@@ -246,7 +248,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
     const int32_t *seq_chunk = p.seq_chunk;
     const float *S_in_m;  // this chain's [d_k][d_v] start state, or null (zero)
     float *S_out_m;       // where its end state goes
-    if (p.mode == 0) {
+    if (!kSeg || p.mode == 0) {
         slice = cta % p.n_slices;
         nh = cta / p.n_slices;
         S_in_m = p.S_in ? p.S_in + nh * mat_floats : nullptr;

@@ -28,11 +28,13 @@ namespace gdr {
 namespace chain {
 namespace {
 
+// kSeg: the segmented schedule's launches (summary and chain modes)
+template <bool kSeg>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_t,
                 const __grid_constant__ CUtensorMap map_o, const TcParams p) {
-    chain_body<false>(map_q, map_k, map_v, map_t, map_o, p, (int)blockIdx.x);
+    chain_body<false, kSeg>(map_q, map_k, map_v, map_t, map_o, p, (int)blockIdx.x);
 }
 
 static_assert(solve::kSolveWarps * 32 <= kThreads, "the fused launch runs the solve on the chain's block");
@@ -414,7 +416,7 @@ static int launch_segmented(const PrefillArgs &a, const WsLayout &L, int segs, c
     // the solve of every unit, with the whole GPU
     int st = tc::launch_solve_tc(a, L, mq, mk, -1, 0, a.stream, true);
     if (st != GDR_OK) return st;
-    if (cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess ||
         cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SCAN_SMEM_BYTES) != cudaSuccess)
@@ -455,7 +457,7 @@ static int launch_segmented(const PrefillArgs &a, const WsLayout &L, int segs, c
     // the summaries (P_f, R_f) of every segment but the last, without output
     p.mode = 1;
     cfg.gridDim = dim3((unsigned)((segs - 1) * NH * (n_slices + 1)));
-    if (cudaLaunchKernelEx(&cfg, tc_chain_kernel, mq, mk, mv, mt, mo, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, tc_chain_kernel<true>, mq, mk, mv, mt, mo, p) != cudaSuccess)
         return GDR_ERR_CUDA;
     // the segments' start states
     cudaLaunchConfig_t scfg = {};
@@ -477,7 +479,7 @@ static int launch_segmented(const PrefillArgs &a, const WsLayout &L, int segs, c
         p.out_norm_eps = a.out_norm_eps;
     }
     cfg.gridDim = dim3((unsigned)(segs * NH * n_slices));
-    if (cudaLaunchKernelEx(&cfg, tc_chain_kernel, mq, mk, mv, mt, mo, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, tc_chain_kernel<true>, mq, mk, mv, mt, mo, p) != cudaSuccess)
         return GDR_ERR_CUDA;
     return GDR_OK;
 }
@@ -502,7 +504,7 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
     if (phases == 0) return launch_fused(a, L, mq, mk, mv, mt, mo);
     if (phases > kSegmentedBase)
         return launch_segmented(a, L, phases - kSegmentedBase, mq, mk, mv, mt, mo);
-    if (cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
         return GDR_ERR_CUDA;
     const int n_slices = a.dv / NV;
@@ -567,7 +569,7 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
         attr.val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, tc_chain_kernel, mq, mk, mv, mt, mo, p) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, tc_chain_kernel<false>, mq, mk, mv, mt, mo, p) != cudaSuccess)
             return GDR_ERR_CUDA;
     }
     return GDR_OK;
