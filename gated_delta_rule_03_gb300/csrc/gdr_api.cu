@@ -49,8 +49,8 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
         off = align_up(off + (size_t)L.max_chunks * (size_t)H * 384 * sizeof(float), 256);
         L.S = off;  // the state handed from one phase to the next
         off = align_up(off + (size_t)num_seqs * (size_t)H * dk * dv * sizeof(float), 256);
-        L.F = off;  // the solve's unit counters, then one flag per (chunk, head) unit
-        off = align_up(off + ((size_t)kCounters + (size_t)L.max_chunks * (size_t)H) * sizeof(int32_t), 256);
+        L.F = off;  // one flag per (chunk, head) unit (fused schedule)
+        off = align_up(off + (size_t)L.max_chunks * (size_t)H * sizeof(int32_t), 256);
         L.segmentable = tc_segmentable(num_seqs, total_tokens, H, dv);
         L.seg = off;  // the segmented schedule's state sets
         if (L.segmentable)

@@ -12,7 +12,6 @@ namespace gdr {
 
 constexpr int kChunk = 64;  // tokens per chunk (the only chunk size the kernels support)
 constexpr int kMaxPhases = 8;  // most phases a tensor-core prefill is split into
-constexpr int kCounters = 64;  // int32 words before the unit flags in the F region
 // Schedules of the tensor-core path: 0 fused, 1 .. kMaxPhases phased, kSegmentedBase + n
 // segmented into n segments per sequence.
 constexpr int kSegmentedBase = GDR_SCHEDULE_SEGMENTED;
@@ -64,9 +63,8 @@ struct WsLayout {
     size_t T;             // tensor-core path: bf16 [max_chunks * H][2][64][64] T' and A^T per unit
     size_t G;             // tensor-core path: fp32 [max_chunks * H][256] decay factors per unit
     size_t S;             // tensor-core path: fp32 [num_seqs][H][dk][dv] state between phases
-    size_t F;             // tensor-core path: int32 [kCounters] unit counters (one per phase,
-                          // then one for a solve of every unit), then [max_chunks * H]
-                          // unit-solved flags (fused schedule)
+    size_t F;             // tensor-core path: int32 [max_chunks * H] unit-solved flags
+                          // (fused schedule)
     size_t seg;           // tensor-core path, few long chains: the segmented schedule's
                           // fp32 state sets, [NH][d_k][d_v] each: (kMaxPhases - 1) each
                           // of P, R and discard, kMaxPhases of start; 0 bytes otherwise

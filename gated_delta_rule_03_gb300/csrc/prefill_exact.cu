@@ -70,8 +70,7 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_sums, int *
 //   seq_chunk[f * (num_seqs + 1) + n] first chunk of sequence n in phase f; the entry at
 //                                     n = num_seqs is the end of phase f
 //   ctl[0] status, ctl[1] number of chunks, ctl[2 + f] first chunk of phase f (f <= P)
-//   zero[0 .. n_zero)                 cleared (the solve's pair counters and, for the fused
-//                                     schedule, the unit-solved flags after them)
+//   zero[0 .. n_zero)                 cleared (the fused schedule's unit-solved flags)
 // A single block of 1024 threads: sequences in blocks of 1024 for the prefix sums, then a
 // group of threads per sequence writes its plan entries.
 __global__ void __launch_bounds__(1024)
@@ -186,7 +185,7 @@ int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases) {
                                           (int32_t *)(a.ws + L.ctl),
                                           L.tensor_path ? (int32_t *)(a.ws + L.F) : nullptr,
                                           !L.tensor_path ? 0
-                                          : kCounters + (fused ? L.max_chunks * a.H : 0));
+                                          : (fused ? L.max_chunks * a.H : 0));
     return cuda_status(cudaGetLastError());
 }
 

@@ -49,7 +49,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     if ((int)blockIdx.x < chain_ctas)
         chain_body<true>(map_q, map_k, map_v, map_t, map_o, p, (int)blockIdx.x);
     else
-        solve::solve_body<true>(map_q, map_k, sp);
+        solve::solve_body<true>(map_q, map_k, sp, (int)blockIdx.x - chain_ctas,
+                                (int)gridDim.x - chain_ctas);
 }
 
 // The segmented schedule's scan over the segment summaries of one (sequence, head) and
@@ -353,8 +354,7 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     const int n_slices = a.dv / NV;
     const int chain_ctas = (int)(a.num_seqs * a.H * n_slices);
     const int grid = device_sms(dev);
-    int32_t *counters = reinterpret_cast<int32_t *>(a.ws + L.F);
-    int32_t *flags = counters + kCounters;
+    int32_t *flags = reinterpret_cast<int32_t *>(a.ws + L.F);
     TcParams p = {};
     p.S_in = a.S0;
     p.factors = reinterpret_cast<const float *>(a.ws + L.G);
@@ -390,7 +390,6 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     sp.seqs = (int)a.num_seqs;
     sp.seq_chunks = (int)((a.total_tokens / a.num_seqs + kChunk - 1) / kChunk);
     sp.flags = flags;
-    sp.unit_counter = counters;
     sp.additive = a.rule == GDR_RULE_ADDITIVE;
     sp.prologue = a.prologue;
     sp.gate_A = a.gate_A;

@@ -9,7 +9,7 @@ namespace {
 __global__ void __launch_bounds__(kThreads, 1)
 tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const SolveParams p) {
-    solve_body<false>(map_q, map_k, p);
+    solve_body<false>(map_q, map_k, p, (int)blockIdx.x, (int)gridDim.x);
 }
 
 }  // namespace
@@ -30,7 +30,6 @@ int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &
     p.Tout = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.T);
     p.Gout = reinterpret_cast<float *>(a.ws + L.G);
     p.phase = phase;
-    p.unit_counter = reinterpret_cast<int32_t *>(a.ws + L.F) + (phase < 0 ? kMaxPhases : phase);
     p.additive = a.rule == GDR_RULE_ADDITIVE;
     p.prologue = a.prologue;
     p.gate_A = a.gate_A;

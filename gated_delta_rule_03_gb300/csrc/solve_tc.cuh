@@ -23,8 +23,8 @@
 // described in chain_tc.cuh; they differ only in where the decay factors are applied.)
 //
 // Mapping. Each warpgroup of a CTA solves one (chunk, head) unit at a time, on its own:
-// it claims units from the call's counter, and warp w of the group owns the unit's
-// token rows 16w .. 16w + 15 throughout.
+// group g of the launch's G groups takes units g, g + G, g + 2G, ..., and warp w of the
+// group owns the unit's token rows 16w .. 16w + 15 throughout.
 //   * load: the unit's keys and queries by TMA (128-byte-swizzled 64 x 64 bf16 tiles),
 //     issued for the next unit as soon as this one's have been read;
 //   * gates: warp 0 scans the log-decays of the unit (loaded while the previous unit
@@ -77,8 +77,8 @@ constexpr int UNIT_FLOATS = 16 * BS;
 
 // Shared memory of one group (the CTA holds kGroups of them, 1024-aligned):
 //   keys then queries, each two 64-feature halves of 64 token rows (8 KB, 128-byte
-//   swizzled as TMA writes them); the blocks; the unit's gates; the load barrier, the
-//   next unit's index and the group's failure flag.
+//   swizzled as TMA writes them); the blocks; the unit's gates; the load barrier and the
+//   group's failure flag.
 constexpr uint32_t G_K = 0, G_Q = 16384;
 constexpr uint32_t G_BLK = 32768;
 constexpr uint32_t G_GATES = G_BLK + UNIT_FLOATS * 4;
@@ -86,8 +86,8 @@ constexpr int GG_G = 0, GG_GAM = 64, GG_GINV = 128, GG_BETA = 192, GG_KDEC = 256
               GG_NK = 320, GG_NQ = 384;  // floats
 constexpr uint32_t G_BAR = G_GATES + 7 * 64 * 4;
 constexpr int kFactorFloats = 384;  // per unit in the workspace
-constexpr uint32_t G_NEXT = G_BAR + 8;
-constexpr uint32_t GROUP_BYTES = (G_NEXT + 8 + 1023) / 1024 * 1024;
+constexpr uint32_t G_FAIL = G_BAR + 8;
+constexpr uint32_t GROUP_BYTES = (G_FAIL + 8 + 1023) / 1024 * 1024;
 constexpr uint32_t SMEM_BYTES = kGroups * GROUP_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448 && G_GATES % 16 == 0 && G_BAR % 8 == 0, "shared memory");
 
@@ -182,7 +182,6 @@ struct SolveParams {
     // `seq_chunks` chunks each, and a ready flag per unit, set once its results are stored
     int seqs, seq_chunks;
     int32_t *flags;
-    int32_t *unit_counter;  // units are claimed from it at run time (zeroed by the plan)
     int additive;           // the additive rule: L = 0, so T = diag(beta)
     int prologue;           // the layer prologue: unit-length q, k; gates from a, b
     const float *gate_A;    // its per-head rate (null: 1)
@@ -199,8 +198,9 @@ struct GroupSolver {
     const CUtensorMap *map_q, *map_k;
     uint32_t gbase;            // the group's shared memory
     float *U, *gt;             // its blocks and gates
-    volatile int *next, *gfail;
+    volatile int *gfail;
     int grp, lane, u0, n_units;
+    int gid, gstride;          // units gid, gid + gstride, ... are this group's
 
     // the unit at local index x: the phase's units in order, or (fused) chunk j of
     // sequence n for head h at x = (j * seqs + n) * H + h
@@ -211,12 +211,9 @@ struct GroupSolver {
     }
     __device__ __forceinline__ void gsync() const { named_sync(1 + grp, 128); }
     __device__ __forceinline__ uint32_t bar_ld() const { return gbase + G_BAR; }
-    // the leader claims a unit (-1 after the last) and fetches its plan entry
-    __device__ __forceinline__ int claim(int4 &pl) const {
-        const int x = n_units > 0 ? atomicAdd(p.unit_counter, 1) : 0;
-        if (x >= n_units) return -1;
-        pl = p.plan[unit_at(x) / p.H];
-        return x;
+    // the plan entry of unit x (any x >= n_units: none); every lane of the caller loads it
+    __device__ __forceinline__ int4 plan_of(int x) const {
+        return x < n_units ? p.plan[unit_at(x) / p.H] : make_int4(0, 0, 0, 0);
     }
     __device__ __forceinline__ void issue_load(int x, const int4 &pl) const {  // leader
         const int h = unit_at(x) % p.H;
@@ -227,22 +224,32 @@ struct GroupSolver {
             tma_load_3d(gbase + G_Q + b * 8192, map_q, bar_ld(), 64 * b, h, pl.y);
         }
     }
-    // log-decays and write strengths of unit x, two tokens per lane of warp 0 (zero past
-    // the end of the sequence), from the leader's plan entry of it
-    __device__ __forceinline__ void fetch_gates(int x, const int4 &pl, float (&gv)[4]) const {
-        const int first = __shfl_sync(0xffffffffu, pl.y, 0), len = __shfl_sync(0xffffffffu, pl.z, 0);
-        gv[0] = gv[1] = gv[2] = gv[3] = 0.f;
-        if (x < 0) return;
+    // the stored gates of unit x, two tokens per lane of warp 0 (padding past the end of
+    // the sequence: log alpha = 0, beta = 0). The loads are only issued here; the values
+    // are first used a whole unit later (gates_of), so their latency is hidden.
+    __device__ __forceinline__ void fetch_gates(int x, const int4 &pl, float (&raw)[4]) const {
+        raw[0] = raw[1] = raw[2] = raw[3] = 0.f;
+        if (x >= n_units) return;
         const int h = unit_at(x) % p.H;
-        const float A = p.prologue && p.gate_A ? p.gate_A[h] : 1.f;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            if (2 * lane + e < len) {
-                const size_t off = (size_t)(first + 2 * lane + e) * p.H + h;
-                const float a = p.log_alpha[off], b = p.beta[off];
-                gv[e] = p.prologue ? prologue_log_alpha(a, A) : a;
-                gv[2 + e] = p.prologue ? prologue_beta(b) : b;
+            if (2 * lane + e < pl.z) {
+                const size_t off = (size_t)(pl.y + 2 * lane + e) * p.H + h;
+                raw[e] = p.log_alpha[off];
+                raw[2 + e] = p.beta[off];
             }
+        }
+    }
+    // log alpha and beta from the stored values (the prologue's activations, if any)
+    template <bool kPro>
+    __device__ __forceinline__ void gates_of(int x, const int4 &pl, const float (&raw)[4],
+                                             float (&gv)[4]) const {
+        const float A = kPro && p.gate_A ? p.gate_A[unit_at(x) % p.H] : 1.f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const bool in = 2 * lane + e < pl.z;
+            gv[e] = kPro && in ? prologue_log_alpha(raw[e], A) : raw[e];
+            gv[2 + e] = kPro && in ? prologue_beta(raw[2 + e]) : raw[2 + e];
         }
     }
 
@@ -253,27 +260,29 @@ struct GroupSolver {
         const int gq = lane >> 2, q = lane & 3;  // m16n8 fragment coordinates
         const bool leader = W == 0 && lane == 0;
         int loads = 0, landed = 0;
-        int4 pl_next = make_int4(0, 0, 0, 0);
-        // the first unit
-        if (leader) {
-            const int x = claim(pl_next);
-            *next = x;
-            if (x >= 0) {
-                issue_load(x, pl_next);
+        // This group's units are gid, gid + gstride, ...: fixed in advance, so that warp 0
+        // can fetch a unit's plan entry and gates a whole unit before it needs them (a
+        // claim from a shared counter would put two dependent global round trips on the
+        // group's critical path). The units are equal in work.
+        int x = gid;
+        int4 pl_cur = make_int4(0, 0, 0, 0), pl_next = make_int4(0, 0, 0, 0);
+        float raw[4] = {0.f, 0.f, 0.f, 0.f};  // warp 0: stored gates of unit x
+        if (W == 0) {
+            pl_cur = plan_of(x);
+            if (leader && x < n_units) {
+                issue_load(x, pl_cur);
                 ++loads;
             }
+            fetch_gates(x, pl_cur, raw);
+            pl_next = plan_of(x + gstride);
         }
-        gsync();
-        int x = *next;
-        float gv[4] = {0.f, 0.f, 0.f, 0.f};  // warp 0: log-decays, write strengths of unit x
-        if (W == 0) fetch_gates(x, pl_next, gv);
         uint32_t ld_phase = 0;
-        while (x >= 0) {
+        while (x < n_units) {
             const int u = unit_at(x);
-            int xn = -1;
-            if (leader) xn = claim(pl_next);  // its latency overlaps the work below
             // ---- gates of unit x: the shared scan of warp 0
             if (W == 0) {
+                float gv[4];
+                gates_of<kPro>(x, pl_cur, raw, gv);
                 const ChunkScan sc = chunk_scan(gv[0], gv[1], lane);
                 *reinterpret_cast<float2 *>(gt + GG_G + 2 * lane) = make_float2(sc.g0, sc.g1);
                 *reinterpret_cast<float2 *>(gt + GG_GAM + 2 * lane) = make_float2(fast_exp(sc.g0), fast_exp(sc.g1));
@@ -411,15 +420,20 @@ struct GroupSolver {
                     *reinterpret_cast<float2 *>(go + 256 + 64 * W + 2 * lane) =
                         *reinterpret_cast<const float2 *>(gt + (W == 0 ? GG_NK : GG_NQ) + 2 * lane);
             }
-            if (leader) *next = xn;
-            gsync();  // keys and queries are read; L is complete; the next unit is known
-            x = *next;
-            if (leader && x >= 0) {
-                fence_async_smem();  // the reads above come before the TMA overwrites the tiles
-                issue_load(x, pl_next);
-                ++loads;
+            gsync();  // keys and queries are read; L is complete
+            // the next unit: its keys and queries land while the inverse runs; its gates
+            // and the plan entry of the one after are fetched for later
+            if (W == 0) {
+                const int xn = x + gstride;
+                if (leader && xn < n_units) {
+                    fence_async_smem();  // the reads above come before the TMA overwrites the tiles
+                    issue_load(xn, pl_next);
+                    ++loads;
+                }
+                fetch_gates(xn, pl_next, raw);
+                pl_cur = pl_next;
+                pl_next = plan_of(xn + gstride);
             }
-            if (W == 0) fetch_gates(x, pl_next, gv);
 
             // ---- (I + L)^{-1}: diagonal block W by forward substitution, lane l on column
             // l % 16 (the upper half of the warp repeats the lower and stores nothing)
@@ -528,6 +542,7 @@ struct GroupSolver {
             }
             gsync();  // unit u is stored; the blocks and gates may be reused
             if (kFused && leader) release_flag_gpu(p.flags + u);
+            x += gstride;
         }
         if (leader) {
             if (*gfail) atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
@@ -537,14 +552,15 @@ struct GroupSolver {
     }
 };
 
-// The solve on one CTA. Work is claimed at run time, so the CTA's index does not
-// matter. kFused: the CTA shares a cooperative launch with the chain (whose block has
-// more warps: those past the solve's return at once; no block-wide barrier follows),
-// takes the units in chunk-major order so that the chains find their chunks solved in
-// the order they need them, and publishes each unit with a release of its flag.
+// The solve on one CTA, rank `rank` of the launch's `ranks` solve CTAs. kFused: the
+// CTA shares a cooperative launch with the chain (whose block has more warps: those past
+// the solve's return at once; no block-wide barrier follows), takes the units in
+// chunk-major order so that the chains find their chunks solved in the order they need
+// them (every group runs at the same pace), and publishes each unit with a release of
+// its flag.
 template <bool kFused>
 __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUtensorMap &map_k,
-                                           const SolveParams &p) {
+                                           const SolveParams &p, int rank, int ranks) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -552,11 +568,11 @@ __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUten
     const int grp = warp >> 2, w = warp & 3;  // group, and the warp's block row in it
     unsigned char *gs = sm + grp * GROUP_BYTES;
     const uint32_t gbase = smem_u32(gs);
-    volatile int *next = reinterpret_cast<volatile int *>(gs + G_NEXT);
+    volatile int *fail = reinterpret_cast<volatile int *>(gs + G_FAIL);
     if (w == 0 && lane == 0) {
         mbar_init(gbase + G_BAR, 1);
         fence_mbar_init();
-        next[1] = 0;
+        *fail = 0;
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_q);
     }
@@ -574,7 +590,7 @@ __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUten
         p.ctl[0] == GDR_OK ? (all ? p.ctl[1] * p.H : p.ctl[3 + p.phase] * p.H - u0) : 0;
     const GroupSolver<kFused> gsv{p, &map_q, &map_k, gbase,
                                   reinterpret_cast<float *>(gs + G_BLK), reinterpret_cast<float *>(gs + G_GATES),
-                                  next, next + 1, grp, lane, u0, n_units};
+                                  fail, grp, lane, u0, n_units, rank * kGroups + grp, ranks * kGroups};
     switch (w) {
         case 0: p.prologue ? gsv.template run<0, true>() : gsv.template run<0, false>(); break;
         case 1: p.prologue ? gsv.template run<1, true>() : gsv.template run<1, false>(); break;
