@@ -68,6 +68,13 @@ def prefill_bytes(inp):
             state * (2 if inp.S0 is not None else 1))
 
 
+def prefill_flops(inp):
+    """Algorithmic flops of one prefill call: the chunk count of "Attention as Matrix
+    Algebra", section 8, 4 C d_k + 3 C d_v + 6 d_k d_v per token-head."""
+    C = inp.chunk
+    return inp.total_tokens * inp.H * (4 * C * inp.dk + 3 * C * inp.dv + 6 * inp.dk * inp.dv)
+
+
 def decode_bytes(N, H, dk, dv, esz=2):
     """Algorithmic HBM bytes of one decode step: the fp32 state read and written once,
     plus q, k, v, o and the two gates."""
@@ -366,6 +373,13 @@ def run_gdr(args):
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": bytes_call,
                      "launch_ms": call_ms, "peak_source": peaks["source"],
+                     # the other bound, for the same call: the chunk form's flops against
+                     # the measured bf16 burst peak (the binding one is the HBM fraction)
+                     "tensor": {"achieved": prefill_flops(inp) / (call_ms / 1e3) / 1e12,
+                                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                "frac": prefill_flops(inp) / (call_ms / 1e3) / 1e12 /
+                                        peaks["bf16_tflops"],
+                                "algorithmic_flops_per_launch": prefill_flops(inp)},
                      "timing": "CUDA events around each gdr_chunk_fwd call on its stream"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,

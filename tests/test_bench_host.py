@@ -57,3 +57,9 @@ def test_head_rate_draws_are_unchanged_by_the_option():
     a = inputs.prefill_inputs([50], H=2, dk=8, dv=8, seed=9)
     b = inputs.prefill_inputs([50], H=2, dk=8, dv=8, seed=9, decay="head")
     assert torch.equal(a.log_alpha, b.log_alpha) and torch.equal(a.q, b.q)
+
+
+def test_prefill_flops_is_the_chunk_count():
+    inp = inputs.prefill_inputs([4096] * 4, H=16, dk=128, dv=128, dtype="bf16", seed=1)
+    # 155,648 flops per token-head at d = 128, C = 64
+    assert bench.prefill_flops(inp) == 4 * 4096 * 16 * 155648
