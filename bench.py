@@ -397,7 +397,8 @@ def run_gdr(args):
 
 def run_decode(args, decode_step, device, stream, world, peaks):
     w = inputs.WORKLOADS[DECODE_WORKLOAD]
-    dec = inputs.workload_decode(DECODE_WORKLOAD)
+    decay = getattr(args, "decay", "head")
+    dec = inputs.workload_decode(DECODE_WORKLOAD, decay=decay)
     S = dec.S.to(device)
     qs, ks, vs = dec.q.to(device), dec.k.to(device), dec.v.to(device)
     las, bs = dec.log_alpha.to(device), dec.beta.to(device)
@@ -415,17 +416,21 @@ def run_decode(args, decode_step, device, stream, world, peaks):
     calls = max(dec.steps, args.steps)
     total_ms, call_ms = timed_calls(step, calls, stream, world, device)
     nbytes = decode_bytes(dec.N, dec.H, dec.dk, dec.dv)
+    if decay == "channel":  # d_k fp32 rates per (n, h) instead of one
+        nbytes += dec.N * dec.H * (dec.dk - 1) * 4
     state_bytes = 2 * dec.N * dec.H * dec.dk * dec.dv * 4
     achieved = nbytes / (call_ms / 1e3) / 1e9
+    rates = "" if decay == "head" else ", one forget rate per key channel"
     return {"workload": f"{DECODE_WORKLOAD}: N={w['N']} H={w['H']} d_k={w['dk']} d_v={w['dv']}, "
                         f"{dec.steps} distinct steps cycled, fp32 state "
-                        f"{state_bytes // 2 / 1e6:.0f} MB",
+                        f"{state_bytes // 2 / 1e6:.0f} MB{rates}",
             "calls": calls, "ms_per_step": total_ms / calls,
             "state_gbs": world * state_bytes * calls / (total_ms / 1e3) / 1e9,
             "roofline": {"kernel": "decode_step_kernel", "bound": "hbm", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": recorded_traffic("decode_step_kernel", DECODE_WORKLOAD),
+                         "traffic": recorded_traffic("decode_step_kernel", DECODE_WORKLOAD)
+                         if decay == "head" else None,
                          "algorithmic_bytes_per_launch": nbytes, "launch_ms": call_ms},
             "gpu_launches": calls}
 

@@ -173,7 +173,8 @@ def decode_inputs(N, H, dk, dv, steps, dtype="bf16", seed=3, s0_std=0.02, gate="
                         dv=dv, steps=steps, dtype=dtype)
 
 
-def workload_decode(name="decode_bf16", steps=None, gate="default"):
+def workload_decode(name="decode_bf16", steps=None, gate="default", decay="head"):
     w = WORKLOADS[name]
     return decode_inputs(w["N"], w["H"], w["dk"], w["dv"], steps or w["steps"],
-                         dtype=w["dtype"], seed=w["seed"], s0_std=w["s0_std"], gate=gate)
+                         dtype=w["dtype"], seed=w["seed"], s0_std=w["s0_std"], gate=gate,
+                         decay=decay)
