@@ -190,7 +190,7 @@ struct SolveParams {
 };
 
 // One warp's part of the solve: warp W of a group (block row W of every unit), its loop
-// over the units the group claims. The block row is a template parameter so that every
+// over the group's units. The block row is a template parameter so that every
 // loop bound and mask below is a constant and the loads can be issued early.
 template <bool kFused>
 struct GroupSolver {
