@@ -11,7 +11,8 @@
 // with u = beta v. With the layer's prologue, k and q are scaled to unit length in
 // shared memory and the gates come from their pre-activations. With one rate per key
 // channel (PC; log_alpha [N, H, d_k]) alpha becomes diag(alpha): a = S^T (alpha . k),
-// b = S^T (alpha . q), o = b + (k.q) u and row r of S decays by alpha_r. The layer's output step (o / rms(o) * w * silu(z), over the head's
+// b = S^T (alpha . q), o = b + (k.q) u and row r of S decays by alpha_r; each thread
+// loads the rates of its own rows beside its part of the state. The layer's output step (o / rms(o) * w * silu(z), over the head's
 // value entries) is applied before o is stored when a gate z is given. The kernel is
 // HBM-bound: a generation step reads about
 // d_k d_v numbers ("Attention as Matrix Algebra", section 9).
@@ -73,7 +74,6 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     __shared__ float ks[DK], qs[DK], vs[DV], os[DV];
     __shared__ float4 red_k[RG][TPR], red_q[RG][TPR];
     __shared__ float s_kq, s_rstd, s_nk, s_nq;
-    __shared__ float ar[PC ? DK : 1];  // per-channel rates alpha_r
 
     const int64_t nh = blockIdx.x;
     const int tid = threadIdx.x;
@@ -84,6 +84,12 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     float4 s[RPT];
 #pragma unroll
     for (int m = 0; m < RPT; ++m) s[m] = __ldcs(Sp + (rg + m * RG) * TPR + cg);
+    // per-channel rates of this thread's rows, loaded beside the state (activated below)
+    float rate[PC ? RPT : 1];
+    if (PC) {
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) rate[m] = log_alpha[nh * DK + rg + m * RG];
+    }
 
     for (int i = tid; i < DK; i += NT) {
         ks[i] = to_f32(k[nh * DK + i]);
@@ -100,10 +106,8 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     }
     if (PC) {  // alpha stays 1; the rates go with the rows
         const float A = prologue && gate_A ? gate_A[nh % H] : 1.f;
-        for (int i = tid; i < DK; i += NT) {
-            const float x = log_alpha[nh * DK + i];
-            ar[i] = expf(prologue ? prologue_log_alpha(x, A) : x);
-        }
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) rate[m] = expf(prologue ? prologue_log_alpha(rate[m], A) : rate[m]);
     }
     const float ra = read * alpha;
     __syncthreads();
@@ -135,8 +139,7 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
 #pragma unroll
     for (int m = 0; m < RPT; ++m) {
-        const float rate = PC ? ar[rg + m * RG] : 1.f;
-        const float kr = ks[rg + m * RG] * rate, qr = qs[rg + m * RG] * rate;
+        const float kr = ks[rg + m * RG] * (PC ? rate[m] : 1.f), qr = qs[rg + m * RG] * (PC ? rate[m] : 1.f);
         pk.x = fmaf(s[m].x, kr, pk.x); pk.y = fmaf(s[m].y, kr, pk.y);
         pk.z = fmaf(s[m].z, kr, pk.z); pk.w = fmaf(s[m].w, kr, pk.w);
         pq.x = fmaf(s[m].x, qr, pq.x); pq.y = fmaf(s[m].y, qr, pq.y);
@@ -190,12 +193,12 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
     for (int m = 0; m < RPT; ++m) {
         const float kr = ks[rg + m * RG];
-        const float rate = PC ? ar[rg + m * RG] : alpha;
+        const float rm = PC ? rate[m] : alpha;
         float4 x;
-        x.x = fmaf(rate, s[m].x, kr * u.x);
-        x.y = fmaf(rate, s[m].y, kr * u.y);
-        x.z = fmaf(rate, s[m].z, kr * u.z);
-        x.w = fmaf(rate, s[m].w, kr * u.w);
+        x.x = fmaf(rm, s[m].x, kr * u.x);
+        x.y = fmaf(rm, s[m].y, kr * u.y);
+        x.z = fmaf(rm, s[m].z, kr * u.z);
+        x.w = fmaf(rm, s[m].w, kr * u.w);
         __stcs(Sp + (rg + m * RG) * TPR + cg, x);
     }
 }
