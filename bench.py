@@ -395,6 +395,30 @@ def run_gdr(args):
     return 0
 
 
+def cpu_decode_baseline(dec, seconds, seqs=8):
+    """The oracle's decode step on this host's cores over a bounded sample: the first
+    `seqs` sequences (all heads) of the workload, its steps cycled until `seconds` pass."""
+    import oracle
+    sel = slice(0, seqs)
+    f = lambda t: t.to(torch.float64).numpy()
+    steps = [(f(dec.q[s])[sel], f(dec.k[s])[sel], f(dec.v[s])[sel], f(dec.log_alpha[s])[sel],
+              f(dec.beta[s])[sel]) for s in range(dec.steps)]
+    S = f(dec.S)[sel]
+    threads = oracle.default_threads()
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        _, S = oracle.decode(*steps[calls % dec.steps], S, threads=threads)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or calls >= 10000:
+            break
+    state_bytes = 2 * seqs * dec.H * dec.dk * dec.dv * 4  # fp32 state read + written, as on the GPU
+    return {"value": state_bytes * calls / el / 1e9, "unit": "GB/s (fp32 state read + written)",
+            "cores": threads, "kind": "oracle",
+            "sample": f"{seqs} of {dec.N} sequences x {dec.H} heads, {calls} decode steps, "
+                      f"{el:.1f} s, float64"}
+
+
 def run_decode(args, decode_step, device, stream, world, peaks):
     w = inputs.WORKLOADS[DECODE_WORKLOAD]
     decay = getattr(args, "decay", "head")
@@ -432,7 +456,9 @@ def run_decode(args, decode_step, device, stream, world, peaks):
                          "traffic": recorded_traffic("decode_step_kernel", DECODE_WORKLOAD)
                          if decay == "head" else None,
                          "algorithmic_bytes_per_launch": nbytes, "launch_ms": call_ms},
-            "gpu_launches": calls}
+            "gpu_launches": calls,
+            "cpu_baseline": (cpu_decode_baseline(dec, min(args.cpu_seconds, 5.0))
+                             if world == 1 and not args.no_cpu_baseline else None)}
 
 
 def main(argv=None):

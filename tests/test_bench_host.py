@@ -63,3 +63,10 @@ def test_prefill_flops_is_the_chunk_count():
     inp = inputs.prefill_inputs([4096] * 4, H=16, dk=128, dv=128, dtype="bf16", seed=1)
     # 155,648 flops per token-head at d = 128, C = 64
     assert bench.prefill_flops(inp) == 4 * 4096 * 16 * 155648
+
+
+def test_decode_cpu_baseline_sample():
+    dec = inputs.decode_inputs(N=4, H=2, dk=16, dv=8, steps=3, seed=7)
+    out = bench.cpu_decode_baseline(dec, 0.05, seqs=2)
+    assert out["kind"] == "oracle" and out["value"] > 0 and out["cores"] >= 1
+    assert out["sample"].startswith("2 of 4 sequences x 2 heads")
