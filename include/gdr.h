@@ -131,10 +131,20 @@ size_t gdr_chunk_fwd_workspace_size(int64_t num_seqs, int64_t total_tokens, int 
  *     under stream capture. A call made while `stream` is being captured, before
  *     the calling thread has made an uncaptured call on that device, runs as a
  *     single phase on `stream` alone.
+ *   - segmented (few long chains: at most 38 sequence-head-128-column chains
+ *     over sequences of 64 chunks or more on average, when the estimated time
+ *     beats the others): every sequence is cut into n segments; a first chain
+ *     launch summarises every segment but the last as an affine map of its
+ *     entering state, a scan chains the segments' start states in fp32, and a
+ *     second chain launch runs every segment from its start state. All on
+ *     `stream`, no side stream.
  * The environment variable GDR_PREFILL_PHASES (1 to 8), read at each call,
- * forces the phased schedule with that many phases. The results do not depend
- * on the schedule: the state passes between phases in fp32, exactly as between
- * chunks, and every schedule performs the same arithmetic.
+ * forces the phased schedule with that many phases, and GDR_PREFILL_SEGMENTS
+ * (2 to 8) the segmented schedule with that many segments where the workspace
+ * holds it. The fused and phased schedules give the same bits: the state passes
+ * between phases in fp32, exactly as between chunks, and they perform the same
+ * arithmetic. The segmented schedule rounds differently (the summaries and the
+ * scan), within the same tolerance.
  */
 int gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
                   const float *beta, const float *S0, const int32_t *cu_seqlens,
