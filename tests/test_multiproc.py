@@ -46,7 +46,7 @@ def _worker(rank, world, port, results):
 
 def test_two_gloo_ranks_agree_on_the_max_time():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of this multi-threaded process
     results = mgr.dict()
     mp.spawn(_worker, args=(world, free_port(), results), nprocs=world, join=True)
     assert results[0][0] == results[1][0] == 15.0
