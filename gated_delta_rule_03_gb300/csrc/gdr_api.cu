@@ -285,6 +285,16 @@ int gdr_chunk_fwd_schedule(int64_t num_seqs, int64_t total_tokens, int H, int d_
     return P < 0 ? GDR_ERR_CUDA : P;
 }
 
+int gdr_chunk_fwd_schedule_model(int64_t num_seqs, int64_t total_tokens, int H, int d_k,
+                                 int d_v, int chunk, int dtype, int varlen, int sms,
+                                 int cooperative) {
+    const int st = check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype);
+    if (st != GDR_OK) return st;
+    if (sms < 1) return GDR_ERR_INVALID_ARG;
+    if (!use_tensor_path(d_k, d_v, dtype) || total_tokens == 0) return 1;
+    return tc_schedule_for(num_seqs, total_tokens, H, d_v, sms, varlen != 0, cooperative != 0);
+}
+
 int gdr_read_device_status(const void *workspace, int *status, gdr_stream_t stream) {
     if (!workspace || !status) return GDR_ERR_INVALID_ARG;
     int32_t word = 0;

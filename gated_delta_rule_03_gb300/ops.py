@@ -123,6 +123,9 @@ def _load():
     lib.gdr_chunk_fwd_kernel_launches.restype = c_int
     lib.gdr_chunk_fwd_schedule.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int, c_int]
     lib.gdr_chunk_fwd_schedule.restype = c_int
+    lib.gdr_chunk_fwd_schedule_model.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int, c_int,
+                                                 c_int, c_int]
+    lib.gdr_chunk_fwd_schedule_model.restype = c_int
     lib.gdr_read_device_status.argtypes = [vp, ctypes.POINTER(c_int), vp]
     lib.gdr_read_device_status.restype = c_int
     _lib = lib
@@ -317,6 +320,17 @@ def chunk_fwd_schedule(num_seqs, total_tokens, H, dk, dv, dtype, varlen=False, d
                                         int(dv), 64, _DTYPES[dtype], int(bool(varlen)))
     if st < 0:
         raise GdrError(st, "gdr_chunk_fwd_schedule")
+    return st
+
+
+def chunk_fwd_schedule_model(num_seqs, total_tokens, H, dk, dv, dtype, sms, varlen=False,
+                             cooperative=True):
+    """The schedule a device with `sms` SMs would take for these sizes (no CUDA call)."""
+    st = _load().gdr_chunk_fwd_schedule_model(int(num_seqs), int(total_tokens), int(H), int(dk),
+                                              int(dv), 64, _DTYPES[dtype], int(bool(varlen)),
+                                              int(sms), int(bool(cooperative)))
+    if st < 0:
+        raise GdrError(st, "gdr_chunk_fwd_schedule_model")
     return st
 
 

@@ -118,8 +118,8 @@ size_t gdr_chunk_fwd_workspace_size(int64_t num_seqs, int64_t total_tokens, int 
  * Returns GDR_OK or a negative status from the list above.
  *
  * Schedules. On the bf16 tensor-core path the per-chunk solve and the
- * sequential chain over the chunks run concurrently in one of two ways, chosen
- * from the sizes and the device's SM count:
+ * sequential chain over the chunks run in one of three ways, chosen from the
+ * sizes and the device's SM count:
  *   - fused (sequences of equal length, cu_seqlens NULL, when the chains leave
  *     enough SMs free): one cooperative kernel launch on `stream` whose CTAs
  *     share the work; it needs the whole GPU at one CTA per SM.
@@ -341,6 +341,19 @@ int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H,
  * if the device cannot be read.
  */
 enum { GDR_SCHEDULE_SEGMENTED = 16 };
+
+/*
+ * The schedule gdr_chunk_fwd_schedule would report on a device with `sms` SMs
+ * (cooperative: nonzero if that device can run the fused schedule's cooperative
+ * launch), for tests and capacity planning. It makes no CUDA call. The
+ * environment variables that force a schedule apply here too. Returns a
+ * negative status for unsupported or invalid sizes, or GDR_ERR_INVALID_ARG if
+ * sms < 1. (The phased schedule also needs a side stream, which a real call may
+ * not get under stream capture; see gdr_chunk_fwd.)
+ */
+int gdr_chunk_fwd_schedule_model(int64_t num_seqs, int64_t total_tokens, int H, int d_k,
+                                 int d_v, int chunk, int dtype, int varlen, int sms,
+                                 int cooperative);
 int gdr_chunk_fwd_schedule(int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v,
                            int chunk, int dtype, int varlen);
 

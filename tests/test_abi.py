@@ -9,6 +9,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdr.h")
@@ -176,3 +177,28 @@ def test_per_channel_workspace_takes_the_exact_layout(lib):
     bad = GdrOptions(0)
     bad.decay = 7
     assert lib.gdr_chunk_fwd_workspace_size_ex(1, 128, 2, 64, 64, 64, 0, ctypes.byref(bad)) == 0
+
+
+@pytest.mark.parametrize("env", ["GDR_PREFILL_PHASES", "GDR_PREFILL_SEGMENTS"])
+def test_schedule_model_on_a_152_sm_device(env, monkeypatch):
+    # the schedule selection is host logic: checked here for the workloads' sizes on a
+    # device like the target's, without one
+    from gated_delta_rule_03_gb300 import ops
+    monkeypatch.delenv("GDR_PREFILL_PHASES", raising=False)
+    monkeypatch.delenv("GDR_PREFILL_SEGMENTS", raising=False)
+    bf = torch.bfloat16
+    m = lambda *a, **k: ops.chunk_fwd_schedule_model(*a, **k)
+    seg = ops.SCHEDULE_SEGMENTED
+    assert m(4, 4 * 4096, 16, 128, 128, bf, 152) == 0                     # fused
+    assert m(4, 4 * 4096, 16, 128, 128, bf, 152, cooperative=False) == 2   # phased instead
+    assert m(8, 34816, 16, 128, 128, bf, 152, varlen=True) >= 1            # packed: phased
+    assert m(1, 65536, 8, 128, 256, bf, 152) == seg + 7                    # long: 7 segments
+    assert m(1, 65536, 8, 128, 256, bf, 40) < seg                          # too few SMs
+    assert m(4, 4 * 4096, 16, 128, 128, torch.float32, 152) == 1           # exact path
+    assert m(1, 0, 2, 128, 128, bf, 152) == 1                              # nothing to do
+    with pytest.raises(Exception):
+        m(1, 64, 2, 128, 128, bf, 0)
+    # the forcing knobs
+    monkeypatch.setenv(env, "3")
+    forced = m(1, 65536, 8, 128, 256, bf, 152)
+    assert forced == (3 if env == "GDR_PREFILL_PHASES" else seg + 3)
