@@ -202,3 +202,17 @@ def test_schedule_model_on_a_152_sm_device(env, monkeypatch):
     monkeypatch.setenv(env, "3")
     forced = m(1, 65536, 8, 128, 256, bf, 152)
     assert forced == (3 if env == "GDR_PREFILL_PHASES" else seg + 3)
+
+
+def test_workspace_holds_the_segment_sets_only_when_segmenting_is_possible(lib):
+    # few chains over sequences of 64 chunks or more: 29 fp32 state sets of
+    # num_seqs * H * d_k * d_v floats (7 each of P, R, discard; 8 starts) are added
+    sets = 29 * 1 * 2 * 128 * 128 * 4
+    seg = lib.gdr_chunk_fwd_workspace_size(1, 64 * 64, 2, 128, 128, 64, 1)
+    plain = lib.gdr_chunk_fwd_workspace_size(1, 63 * 64, 2, 128, 128, 64, 1)
+    assert sets <= seg - plain < sets + (1 << 20)
+    # many chains: no sets
+    many = lib.gdr_chunk_fwd_workspace_size(20, 20 * 64 * 64, 2, 128, 128, 64, 1)
+    per_chunk = (lib.gdr_chunk_fwd_workspace_size(20, 20 * 64 * 64 + 20 * 64, 2, 128, 128, 64, 1)
+                 - many)
+    assert per_chunk < 80 * 1024 * 20  # grows by the per-unit buffers, not by state sets
