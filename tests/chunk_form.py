@@ -105,3 +105,14 @@ def chunked_forward_per_channel(q, k, v, log_alpha, beta, C, S0=None):
         sl = slice(c, c + C)
         out[sl], S = chunk_step_per_channel(S, q[sl], k[sl], v[sl], log_alpha[sl], beta[sl])
     return out, S
+
+
+def segment_summary(k, v, log_alpha, beta, C):
+    """The affine map of a run of chunks, S_end = P S + R: P is the end state from the
+    identity with zero values (the product of the run's transitions), R the end state from
+    zero with the values. The segmented GPU schedule computes these per segment."""
+    dk, dv = k.shape[1], v.shape[1]
+    q0 = np.zeros_like(k)
+    _, P = chunked_forward(q0, k, np.zeros((len(k), dk)), log_alpha, beta, C, S0=np.eye(dk))
+    _, R = chunked_forward(q0, k, v, log_alpha, beta, C, S0=np.zeros((dk, dv)))
+    return P, R

@@ -363,6 +363,28 @@ def test_gated_chunk_form_equals_the_recurrence():
             np.testing.assert_allclose(Sc, S, rtol=0, atol=1e-12)
 
 
+def test_segment_summaries_chain_to_the_recurrence():
+    # the state map of a run of chunks is affine, S_end = P S + R (P independent of the
+    # values): chaining the segments' maps from S0 gives every segment's start state, and
+    # each segment run from its start reproduces the recurrence (the segmented schedule)
+    rng = np.random.default_rng(22)
+    T, dk, dv, C = 300, 8, 5, 16
+    for shift in (-6.0, 0.0):
+        q, k, v, _, b, S0 = _random_case(rng, T, dk, dv)
+        la = -np.logaddexp(0.0, rng.standard_normal(T) + shift)
+        o, S = run(q, k, v, log_alpha=la, beta=b, S0=S0)
+        bounds = [0, 64, 128, 192, 300]  # segments of whole chunks, a ragged last one
+        X, outs = S0, []
+        for a, e in zip(bounds[:-1], bounds[1:]):
+            P, R = chunk_form.segment_summary(k[a:e], v[a:e], la[a:e], b[a:e], C)
+            oc, Sc = chunk_form.chunked_forward(q[a:e], k[a:e], v[a:e], la[a:e], b[a:e], C, S0=X)
+            np.testing.assert_allclose(P @ X + R, Sc, rtol=0, atol=1e-11)
+            outs.append(oc)
+            X = P @ X + R
+        np.testing.assert_allclose(np.concatenate(outs), o, rtol=0, atol=1e-11)
+        np.testing.assert_allclose(X, S, rtol=0, atol=1e-11)
+
+
 def test_pages_ungated_chunk_experiment():
     g = golden("p5_chunk_checks.json")
     rng = np.random.default_rng(3)
