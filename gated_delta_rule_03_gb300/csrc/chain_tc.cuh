@@ -625,10 +625,11 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 else note_fail(1);
             }
             for (int c = 0; c < n_chunks && !flags[3]; ++c) {
-                // [O^T | X^T] = S^T [Q; -W']^T once S^T, -W' and (for the O buffer) the
-                // epilogue of chunk c - 1 are ready
-                bool ok = mbar_wait(bar(B_SREADY), c & 1) && mbar_wait(bar(B_WQ0 + (c & 1)), (c >> 1) & 1);
-                if (ok && c > 0) ok = mbar_wait(bar(B_OFREE), (c - 1) & 1);
+                // [O^T | X^T] = S^T [Q; -W']^T once the epilogue has read O of chunk c - 1,
+                // -W' is in place and S^T is written: checked in the order they usually
+                // complete, so that only the last wait is on the chain's critical path
+                bool ok = c == 0 || mbar_wait(bar(B_OFREE), (c - 1) & 1);
+                ok = ok && mbar_wait(bar(B_WQ0 + (c & 1)), (c >> 1) & 1) && mbar_wait(bar(B_SREADY), c & 1);
                 if (!ok) { note_fail(1); break; }
                 tc_fence_after();
                 const uint32_t qw = sbase + qslot(c);
