@@ -4,8 +4,8 @@ import pytest
 import torch
 
 import oracle
-from gated_delta_rule_03_gb300 import decode_step, inputs
-from tests.helpers import TOL, f64, rel_err
+from gated_delta_rule_03_gb300 import inputs
+from tests.helpers import TOL, chunk_fwd, decode_step, f64, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -56,7 +56,6 @@ def test_decode_shapes(dtype, dk, dv):
 
 
 def test_prefill_then_decode_equals_longer_prefill():
-    from gated_delta_rule_03_gb300 import chunk_fwd
     full = inputs.prefill_inputs([150], H=2, dk=128, dv=128, dtype="bf16", seed=13, s0_std=0.2,
                                  gate="slow")
     dev = lambda t: t.cuda()

@@ -13,8 +13,8 @@ import pytest
 import torch
 
 import oracle
-from gated_delta_rule_03_gb300 import chunk_fwd, decode_step, inputs, ops
-from tests.helpers import TOL, f64, gpu_prefill, oracle_prefill, rel_err
+from gated_delta_rule_03_gb300 import inputs, ops
+from tests.helpers import TOL, chunk_fwd, decode_step, f64, gpu_prefill, oracle_prefill, rel_err
 
 pytestmark = pytest.mark.gpu
 

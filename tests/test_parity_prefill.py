@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from gated_delta_rule_03_gb300 import inputs
-from tests.helpers import TOL, gpu_prefill, oracle_prefill, rel_err, f64
+from tests.helpers import TOL, chunk_fwd, gpu_prefill, oracle_prefill, rel_err, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -89,7 +89,6 @@ def test_no_tokens_at_all(dtype):
 @pytest.mark.parametrize("tau", [1, 63, 64, 100, 257])
 def test_split_and_resume(dtype, tau):
     # prefill [0, tau) then [tau, T) passing S equals one call over [0, T), for any tau
-    from gated_delta_rule_03_gb300 import chunk_fwd
     full = inputs.prefill_inputs([300], H=2, dk=128, dv=128, dtype=dtype, seed=7, s0_std=0.3,
                                  gate="slow")
     dev = lambda t: None if t is None else t.cuda()
@@ -109,7 +108,6 @@ def test_split_and_resume(dtype, tau):
 
 
 def test_in_place_state_update():
-    from gated_delta_rule_03_gb300 import chunk_fwd
     inp = inputs.prefill_inputs([150, 90], H=2, dk=128, dv=128, dtype="bf16", seed=8,
                                 s0_std=0.5, gate="slow")
     o_ref, S_ref = oracle_prefill(inp)
@@ -145,7 +143,6 @@ def test_phase_split_matches_single_phase(phases, dv, monkeypatch):
 @pytest.mark.parametrize("phases", [1, 4])
 def test_phase_split_in_place_state(phases, monkeypatch):
     # S_final may be S0: the first phase reads S0 and the last writes S_final
-    from gated_delta_rule_03_gb300 import chunk_fwd
     monkeypatch.setenv("GDR_PREFILL_PHASES", str(phases))
     inp = inputs.prefill_inputs([640, 1000, 3], H=2, dk=128, dv=128, dtype="bf16", seed=12,
                                 s0_std=0.5, gate="none")
@@ -161,7 +158,6 @@ def test_phase_split_in_place_state(phases, monkeypatch):
 def test_phase_split_inside_graph_capture(monkeypatch):
     # the side stream forks from and joins the captured stream; replaying the graph
     # gives the eager result
-    from gated_delta_rule_03_gb300 import chunk_fwd
     monkeypatch.setenv("GDR_PREFILL_PHASES", "4")
     inp = inputs.prefill_inputs([1024, 960], H=4, dk=128, dv=128, dtype="bf16", seed=13,
                                 s0_std=0.2, gate="slow")
@@ -212,7 +208,7 @@ def test_fused_schedule_matches_phased(S, T, H, dv, monkeypatch):
 def test_fused_schedule_repeated_calls_share_a_workspace():
     # the unit flags are cleared by every call's plan: back-to-back calls on one workspace
     # and stream give identical results
-    from gated_delta_rule_03_gb300 import chunk_fwd, ops
+    from gated_delta_rule_03_gb300 import ops
     inp = inputs.prefill_inputs([512] * 2, H=4, dk=128, dv=128, dtype="bf16", seed=31, s0_std=0.2)
     dev = lambda t: t.cuda()
     q, k, v, la, b, S0 = map(dev, (inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0))
@@ -226,7 +222,7 @@ def test_fused_schedule_repeated_calls_share_a_workspace():
 
 
 def test_bad_cu_seqlens_reported_through_the_status_word():
-    from gated_delta_rule_03_gb300 import chunk_fwd, read_device_status
+    from gated_delta_rule_03_gb300 import read_device_status
     inp = inputs.prefill_inputs([100, 50], H=2, dk=128, dv=128, dtype="bf16", seed=9)
     dev = "cuda"
     bad = torch.tensor([0, 120, 100 + 50], dtype=torch.int32)      # fine
