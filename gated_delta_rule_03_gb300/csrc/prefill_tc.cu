@@ -19,6 +19,7 @@
 //    its start state, with output. Chain steps per call fall from m to about 2 m / n.
 #include <stdlib.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "chain_tc.cuh"
@@ -203,15 +204,18 @@ struct SideStream {
 };
 thread_local SideStream t_side[kMaxDevices];
 
+// The SM count of a device, cached on first use. Threads that race on the first use
+// both query and store the same value; the atomics make that race well defined.
+std::atomic<int> g_sms[kMaxDevices];
+
 int device_sms(int dev) {
-    static int sms[kMaxDevices] = {};
     if (dev < 0 || dev >= kMaxDevices) return 0;
-    if (!sms[dev]) {
-        int v = 0;
+    int v = g_sms[dev].load(std::memory_order_relaxed);
+    if (!v) {
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        sms[dev] = v;
+        g_sms[dev].store(v, std::memory_order_relaxed);
     }
-    return sms[dev];
+    return v;
 }
 
 // The current thread's side stream on the current device, or null. Resources are not
@@ -301,10 +305,14 @@ static int forced_segments() {
     return 0;
 }
 
+// Whether the fused schedule's cooperative launch fits on a device, cached on first use
+// (0 unknown, 1 yes, 2 no; racing first uses compute and store the same answer).
+static std::atomic<int> g_cooperative_ok[kMaxDevices];
+
 static bool cooperative_ok(int dev) {
-    static int ok[kMaxDevices] = {};  // 0 unknown, 1 yes, 2 no
     if (dev < 0 || dev >= kMaxDevices) return false;
-    if (!ok[dev]) {
+    int known = g_cooperative_ok[dev].load(std::memory_order_relaxed);
+    if (!known) {
         int coop = 0, blocks = 0;
         const bool yes =
             cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
@@ -313,9 +321,10 @@ static bool cooperative_ok(int dev) {
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, chain::tc_fused_kernel, chain::kThreads,
                                                           chain::FUSED_SMEM_BYTES) == cudaSuccess &&
             blocks >= 1;
-        ok[dev] = yes ? 1 : 2;
+        known = yes ? 1 : 2;
+        g_cooperative_ok[dev].store(known, std::memory_order_relaxed);
     }
-    return ok[dev] == 1;
+    return known == 1;
 }
 
 int tc_schedule_for(int64_t num_seqs, int64_t total_tokens, int H, int dv, int sms, bool varlen,

@@ -14,14 +14,22 @@
  *
  * Conventions shared by every entry point
  *   - Every pointer argument is a DEVICE pointer unless stated otherwise, to
- *     memory owned by the caller. The library never allocates device memory,
- *     never frees caller memory and keeps no state between calls.
+ *     memory owned by the caller. The library never allocates device memory
+ *     at run time and never frees caller memory. What it does keep between
+ *     calls, for the life of the process: per device, the SM count and
+ *     whether the cooperative launch of the fused schedule fits (cached on
+ *     first use, thread-safe); per host thread and device, one side stream
+ *     and 8 events for the phased schedule (created by the first phased call
+ *     on that thread and device, never destroyed); and the static scratch
+ *     array of gdr_chunk_fwd_noalloc, which the module reserves on every
+ *     device it is loaded on. No result depends on any of them.
  *   - Tensors are dense and row-major. q, k, v, o, S0, S, S_final and the
  *     workspace start on a 16-byte boundary; log_alpha, beta and cu_seqlens
  *     on a 4-byte boundary (so per-token slices of the gates are accepted).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
  *     stream) and is asynchronous: outputs are valid once the stream has
- *     reached the call. Only gdr_read_device_status() synchronises.
+ *     reached the call. Only the status readers (gdr_read_device_status,
+ *     gdr_noalloc_read_device_status) synchronise.
  *   - Argument errors are detected on the host before anything is enqueued and
  *     returned as a negative status; nothing is written in that case.
  *   - gdr_dtype selects the storage type of q, k, v and o. Gates and states
@@ -292,20 +300,34 @@ int gdr_decode_step_ex(const void *q, const void *k, const void *v, const float 
  *     GDR_NOALLOC_SCRATCH_BYTES are rejected with GDR_ERR_WORKSPACE before
  *     anything is enqueued; other argument errors are those of gdr_chunk_fwd.
  *   - The device current on the calling thread must be the one the pointers
- *     and the stream belong to. The first call on a device looks up the
- *     array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture.
+ *     and the stream belong to. Every call looks up the array's device
+ *     address there (cudaGetSymbolAddress, which allocates nothing); the
+ *     first call on a device also loads the library's module on it, so make
+ *     that first call before any stream capture.
  *   - All calls share the one array, which keeps the last call's contents
  *     (nothing needs clearing: each call writes all the scratch it reads).
  *     Calls that overlap on the GPU race on it: order them on one stream.
- *   - The status word of the last call sits at the start of the array; it is
- *     not reachable through gdr_read_device_status.
+ *   - The device-side checks (a rejected cu_seqlens: GDR_ERR_BAD_SEQLENS; a
+ *     bounded wait that gave up: GDR_ERR_DEVICE_TIMEOUT) leave their status
+ *     in the first word of the array, and then o and S_final are not
+ *     written. gdr_noalloc_read_device_status reads it.
  */
 #define GDR_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
 int gdr_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_alpha,
                           const float *beta, const float *S0, const int32_t *cu_seqlens,
                           int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v,
                           int chunk, int dtype, void *o, float *S_final, gdr_stream_t stream);
+
+/*
+ * The device status word that the last gdr_chunk_fwd_noalloc call on the
+ * current device left in the library's scratch array (GDR_OK,
+ * GDR_ERR_BAD_SEQLENS or GDR_ERR_DEVICE_TIMEOUT), written to *status (a HOST
+ * pointer). Like gdr_read_device_status it synchronises `stream` first, so it
+ * must not be called inside stream capture; it allocates nothing. Returns
+ * GDR_OK if the status was read, GDR_ERR_INVALID_ARG for a null status
+ * pointer, GDR_ERR_CUDA if the device cannot be read.
+ */
+int gdr_noalloc_read_device_status(int *status, gdr_stream_t stream);
 
 /*
  * Which kernel path gdr_chunk_fwd takes for these sizes, for diagnostics and
