@@ -3,7 +3,10 @@
 One step is one gdr_chunk_fwd call (chunked prefill) over the B=4, H=16,
 T=4096, d_k=d_v=128 bf16 workload, with inputs resident in HBM. The decode row
 of the hot path (gdr_decode_step over 256 sequences x 32 heads, fp32 state of
-537 MB) is timed in the same run and reported under "decode".
+537 MB) is timed in the same run and reported under "decode"; the other prefill
+workloads (packed varying lengths, one long sequence with d_v = 256, the tiny fp32
+case) under "varlen", "long" and "tiny". Every workload also runs a sustained stretch
+of back-to-back calls (about 2 s) with the clocks sampled.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdr|reference]
 
@@ -166,6 +169,28 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo or lscpu), for the baseline records."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    val = line.split(":", 1)[1].strip()
+                    if val:
+                        return val
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
+
+
 def barrier(world):
     if world > 1:
         torch.distributed.barrier()
@@ -204,6 +229,27 @@ def timed_calls(fn, steps, stream, world, device, per_call=True):
     return total, mean_call
 
 
+def sustained_calls(fn, stream, device, local_rank, seconds, est_ms):
+    """Back-to-back calls of fn() for about `seconds` on `stream`, with nvidia-smi sampling
+    the clocks meanwhile: a stretch long enough for an outside sampler to see the GPU
+    busy. Returns the calls, the CUDA-event time and the clock samples."""
+    calls = int(min(max(seconds * 1e3 / max(est_ms, 1e-3), 1), 500_000))
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    torch.cuda.synchronize(device)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(calls):
+            fn()
+        end.record(stream)
+    torch.cuda.synchronize(device)
+    ms = start.elapsed_time(end)
+    return {"calls": calls, "seconds": ms / 1e3, "ms_per_call": ms / calls,
+            "clocks": clocks.stop()}
+
+
 # ----------------------------------------------------------------------------- arms
 
 def oracle_prefill_sample(inp):
@@ -215,11 +261,21 @@ def oracle_prefill_sample(inp):
                 num_seqs=inp.num_seqs)
 
 
-def cpu_baseline(inp, seconds, name):
-    """The oracle, as it stands, on this host's cores: repeat the full workload until
-    `seconds` have passed (at least once)."""
+def cpu_baseline(inp, seconds, name, heads=None):
+    """The oracle, as it stands, on this host's cores: repeat the full workload (or only
+    the given heads of it) until `seconds` have passed (at least once). With a subset of
+    heads the rate is scaled to the workload's H heads (the heads are independent and
+    equal in work) and the per-head rate is reported beside it."""
     import oracle
     args = oracle_prefill_sample(inp)
+    nh = inp.H
+    if heads is not None:
+        sel = list(heads)
+        nh = len(sel)
+        for key in ("q", "k", "v", "log_alpha", "beta"):
+            args[key] = np.ascontiguousarray(args[key][:, sel])
+        if args["S0"] is not None:
+            args["S0"] = np.ascontiguousarray(args["S0"][:, sel])
     threads = oracle.default_threads()
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -228,11 +284,17 @@ def cpu_baseline(inp, seconds, name):
         el = time.perf_counter() - t0
         if el >= seconds or reps >= 1000:
             break
-    tokens = inp.total_tokens * reps
-    return {"value": tokens / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"full {name} workload ({inp.num_seqs} sequences, {inp.total_tokens} "
-                      f"tokens, H={inp.H}, d_k={inp.dk}, d_v={inp.dv}) x {reps} repetitions, "
-                      f"{el:.1f} s, float64 token loop"}
+    token_heads = inp.total_tokens * nh * reps
+    out = {"value": token_heads / inp.H / el, "unit": "tokens/s", "cores": threads,
+           "cpu_model": cpu_model(), "kind": "oracle"}
+    what = f"full {name} workload" if heads is None else \
+        f"{name} workload, heads {sel[0]}-{sel[-1]} of {inp.H} (rate scaled to all heads)"
+    out["sample"] = (f"{what} ({inp.num_seqs} sequences, {inp.total_tokens} tokens, "
+                     f"H={nh}, d_k={inp.dk}, d_v={inp.dv}) x {reps} repetitions, "
+                     f"{el:.1f} s, float64 token loop")
+    if heads is not None:
+        out["per_head_token_rate"] = token_heads / nh / el
+    return out
 
 
 def run_reference(args):
@@ -256,7 +318,8 @@ def run_reference(args):
         "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(inp, args.workload),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                         "cpu_model": cpu_model(), "kind": "oracle",
                          "sample": f"each step: the full {args.workload} workload, "
                                    f"float64 token loop on {threads} host threads"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -276,11 +339,75 @@ def workload_config(inp, name):
                                                  f"packed ({inp.total_tokens} tokens)"
     s0 = "S0=0" if inp.S0 is None else "S0 ~ N(0, 0.02^2)"
     return {"workload": f"{name}: B={inp.num_seqs} H={inp.H} {lens} "
-                        f"d_k={inp.dk} d_v={inp.dv} chunk={inp.chunk} bf16 q/k/v/o, fp32 "
+                        f"d_k={inp.dk} d_v={inp.dv} chunk={inp.chunk} {inp.dtype} q/k/v/o, fp32 "
                         f"gates and state, {s0}",
             "global_batch": inp.num_seqs,
             "seq_len": inp.seq_lens[0] if equal else inp.total_tokens // inp.num_seqs,
             "heads": inp.H, "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"}
+
+
+# the other prefill workloads, timed in the same run as the headline one
+SIDE_WORKLOADS = (("varlen", "varlen_bf16", None), ("long", "long_bf16", (0, 1)),
+                  ("tiny", "tiny_fp32", None))
+
+
+def bench_prefill_workload(name, args, device, stream, world, local, peaks, cpu_heads=None):
+    """One prefill workload: per-call CUDA-event timing over the driver's --steps, a
+    sustained stretch of back-to-back calls with the clocks sampled, the roofline of the
+    call (HBM and tensor fractions), the recorded DRAM traffic and the oracle on the host."""
+    from gated_delta_rule_03_gb300 import chunk_fwd, chunk_fwd_workspace_size, ops
+    inp = inputs.workload_prefill(name)
+    d = lambda t: None if t is None else t.to(device)
+    q, k, v, la, b = d(inp.q), d(inp.k), d(inp.v), d(inp.log_alpha), d(inp.beta)
+    S0, cu = d(inp.S0), d(inp.cu_seqlens)
+    o = torch.empty((inp.total_tokens, inp.H, inp.dv), dtype=q.dtype, device=device)
+    S = torch.empty((inp.num_seqs, inp.H, inp.dk, inp.dv), dtype=torch.float32, device=device)
+    ws = torch.empty(chunk_fwd_workspace_size(inp.num_seqs, inp.total_tokens, inp.H, inp.dk,
+                                              inp.dv, inp.chunk, q.dtype),
+                     dtype=torch.uint8, device=device)
+
+    def step():
+        chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, num_seqs=inp.num_seqs, chunk=inp.chunk,
+                  o=o, S_final=S, workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    total_ms, call_ms = timed_calls(step, args.steps, stream, world, device)
+    sus = sustained_calls(step, stream, device, local, args.sustained_seconds, call_ms)
+    varlen = cu is not None
+    schedule = ops.chunk_fwd_schedule(inp.num_seqs, inp.total_tokens, inp.H, inp.dk, inp.dv,
+                                      q.dtype, varlen=varlen)
+    main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype, schedule=schedule)
+    launches = ops.chunk_fwd_kernel_launches(inp.num_seqs, inp.total_tokens, inp.H, inp.dk,
+                                             inp.dv, q.dtype, varlen=varlen)
+    nbytes, flops = prefill_bytes(inp), prefill_flops(inp)
+    achieved = nbytes / (call_ms / 1e3) / 1e9
+    tflops = flops / (call_ms / 1e3) / 1e12
+    out = {
+        "workload": workload_config(inp, name)["workload"],
+        "tokens_per_s": world * inp.total_tokens * args.steps / (total_ms / 1e3),
+        "ms_per_call": total_ms / args.steps, "steps": args.steps,
+        "schedule": schedule, "dtype": ops.chunk_fwd_compute_dtype(inp.dk, inp.dv, q.dtype),
+        "roofline": {"kernel": main_kernel, "bound": "hbm", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": recorded_traffic(main_kernel, name),
+                     "algorithmic_bytes_per_launch": nbytes, "launch_ms": call_ms,
+                     "tensor": {"achieved": tflops, "peak": peaks["bf16_tflops"],
+                                "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+                                "algorithmic_flops_per_launch": flops}},
+        "sustained": sus,
+        "gpu_launches": launches * (args.steps + sus["calls"]),
+        "cpu_baseline": None,
+    }
+    if inp.dtype == "f32":
+        out["roofline"]["note"] = ("latency-bound: 512 token-heads in 8 chunks; reported, no "
+                                   "roofline target")
+    del q, k, v, la, b, S0, cu, o, S, ws
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(inp, min(args.cpu_seconds, 3.0), name, heads=cpu_heads)
+    return out
 
 
 def run_gdr(args):
@@ -314,6 +441,9 @@ def run_gdr(args):
             step()
     total_ms, call_ms = timed_calls(step, args.steps, stream, world, device)
     clock_info = clocks.stop()
+    # a sustained stretch of the same call (its own clock samples), long enough for an
+    # outside sampler to see the GPU busy; `value` stays the timed --steps above
+    sustained = sustained_calls(step, stream, device, local, args.sustained_seconds, call_ms)
 
     tokens = inp.total_tokens
     value = world * tokens * args.steps / (total_ms / 1e3)
@@ -355,7 +485,14 @@ def run_gdr(args):
 
     decode = None
     if not args.no_decode:
-        decode = run_decode(args, decode_step, device, stream, world, peaks)
+        decode = run_decode(args, decode_step, device, stream, world, peaks, local)
+
+    side = {}
+    if not args.no_side and args.decay == "head":
+        for key, name, heads in SIDE_WORKLOADS:
+            if name != args.workload:
+                side[key] = bench_prefill_workload(name, args, device, stream, world, local,
+                                                   peaks, cpu_heads=heads)
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -386,8 +523,10 @@ def run_gdr(args):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": kernel_launches * args.steps,
         "clocks": clock_info,
+        "sustained": sustained,
         "decode": decode,
     }
+    line.update(side)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -414,12 +553,12 @@ def cpu_decode_baseline(dec, seconds, seqs=8):
             break
     state_bytes = 2 * seqs * dec.H * dec.dk * dec.dv * 4  # fp32 state read + written, as on the GPU
     return {"value": state_bytes * calls / el / 1e9, "unit": "GB/s (fp32 state read + written)",
-            "cores": threads, "kind": "oracle",
+            "cores": threads, "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"{seqs} of {dec.N} sequences x {dec.H} heads, {calls} decode steps, "
                       f"{el:.1f} s, float64"}
 
 
-def run_decode(args, decode_step, device, stream, world, peaks):
+def run_decode(args, decode_step, device, stream, world, peaks, local=0):
     w = inputs.WORKLOADS[DECODE_WORKLOAD]
     decay = getattr(args, "decay", "head")
     dec = inputs.workload_decode(DECODE_WORKLOAD, decay=decay)
@@ -439,6 +578,7 @@ def run_decode(args, decode_step, device, stream, world, peaks):
             step()
     calls = max(dec.steps, args.steps)
     total_ms, call_ms = timed_calls(step, calls, stream, world, device)
+    sus = sustained_calls(step, stream, device, local, args.sustained_seconds, call_ms)
     nbytes = decode_bytes(dec.N, dec.H, dec.dk, dec.dv)
     if decay == "channel":  # d_k fp32 rates per (n, h) instead of one
         nbytes += dec.N * dec.H * (dec.dk - 1) * 4
@@ -456,7 +596,8 @@ def run_decode(args, decode_step, device, stream, world, peaks):
                          "traffic": recorded_traffic("decode_step_kernel", DECODE_WORKLOAD)
                          if decay == "head" else None,
                          "algorithmic_bytes_per_launch": nbytes, "launch_ms": call_ms},
-            "gpu_launches": calls,
+            "sustained": sus,
+            "gpu_launches": calls + sus["calls"],
             "cpu_baseline": (cpu_decode_baseline(dec, min(args.cpu_seconds, 5.0))
                              if world == 1 and not args.no_cpu_baseline else None)}
 
@@ -475,6 +616,10 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sustained-seconds", type=float, default=2.0,
+                    help="length of each workload's stretch of back-to-back calls")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the other prefill workloads (varlen, long, tiny)")
     ap.add_argument("--only", choices=["all", "decode"], default="all",
                     help="'decode' runs only the decode timing (for profiling that kernel)")
     args = ap.parse_args(argv)
@@ -495,7 +640,7 @@ def run_decode_only(args):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
-    out = run_decode(args, decode_step, device, stream, 1, load_peaks())
+    out = run_decode(args, decode_step, device, stream, 1, load_peaks(), local)
     print(json.dumps({"decode": out}), flush=True)
     return 0
 
