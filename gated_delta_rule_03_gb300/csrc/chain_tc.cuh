@@ -125,7 +125,10 @@ enum {
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * B_COUNT;
 constexpr uint32_t OFF_FLAGS = OFF_TMEM_SLOT + 4;  // int: prep, state, epilogue, any failure
-constexpr uint32_t SMEM_USED = OFF_FLAGS + 16;
+// int[7]: the last chunk whose loads the producer issued into each slot (V/T' 0-1,
+// K/A^T/factors 2-4, Q 5-6), -1 for none; the drain after a failure waits for them
+constexpr uint32_t OFF_ISSUED = OFF_FLAGS + 16;
+constexpr uint32_t SMEM_USED = OFF_ISSUED + 32;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for the 1024-byte alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -166,15 +169,21 @@ struct TcParams {
     const __nv_bfloat16 *out_gate;
     const float *out_norm_weight;
     float out_norm_eps;
+    // Bound of every wait in SM cycles (kWaitCycles; twice that for a solved unit), and a
+    // test of the give-up path: the producer of the launch's CTA 0 skips the K-slot load of
+    // chunk fault_chunk (-1: never), so that the roles waiting on it give up, mark the
+    // call GDR_ERR_DEVICE_TIMEOUT and drain.
+    long long wait_cycles;
+    int fault_chunk;
 };
 
 // A chain CTA of a fused launch waits here until the solve has published unit u (its
 // T', A^T and factors stored); false if the call failed meanwhile or the wait ran out.
-constexpr long long kUnitWaitCycles = 1ll << 32;
-__device__ __forceinline__ bool wait_unit_solved(const int32_t *flag, const int32_t *ctl) {
+__device__ __forceinline__ bool wait_unit_solved(const int32_t *flag, const int32_t *ctl,
+                                                 long long limit) {
     const long long t0 = clock64();
     while (acquire_load_gpu(flag) == 0) {
-        if (*reinterpret_cast<const volatile int32_t *>(ctl) != GDR_OK || clock64() - t0 > kUnitWaitCycles)
+        if (*reinterpret_cast<const volatile int32_t *>(ctl) != GDR_OK || clock64() - t0 > limit)
             return false;
         __nanosleep(64);
     }
@@ -237,6 +246,9 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TMEM_SLOT);
     volatile int *flags = reinterpret_cast<volatile int *>(sm + OFF_FLAGS);
     auto note_fail = [&](int role) { flags[role] = 1; flags[3] = 1; };
+    volatile int *issued = reinterpret_cast<volatile int *>(sm + OFF_ISSUED);
+    const long long wait_limit = p.wait_cycles;
+    auto wait = [&](uint32_t b, uint32_t parity) { return mbar_wait_for(b, parity, wait_limit); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -320,6 +332,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
         mbar_init(bar(B_UREADY), kStateWarps);
         fence_mbar_init();
         flags[0] = flags[1] = flags[2] = flags[3] = 0;
+        for (int i = 0; i < 7; ++i) issued[i] = -1;
         prefetch_tensormap(&map_q);
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_v);
@@ -351,9 +364,9 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             const int unit0 = seq_chunk[n] * p.H + h;  // chunk c is solve unit unit0 + c * H
             for (int c = 0; c < n_chunks; ++c) {
                 const int tt = (int)(seq_begin + (int64_t)c * C), unit = unit0 + c * p.H;
-                if (kFused && !wait_unit_solved(p.flags + unit, p.ctl)) { note_fail(3); break; }
+                if (kFused && !wait_unit_solved(p.flags + unit, p.ctl, 2 * wait_limit)) { note_fail(3); break; }
                 // V, T' (slot free once U'~ and W' of chunk c - 2 are done)
-                if (c >= 2 && !mbar_wait(bar(B_VE0 + (c & 1)), ((c >> 1) - 1) & 1)) { note_fail(3); break; }
+                if (c >= 2 && !wait(bar(B_VE0 + (c & 1)), ((c >> 1) - 1) & 1)) { note_fail(3); break; }
                 const uint32_t vs = sbase + vslot(c), vf = bar(B_VF0 + (c & 1));
                 mbar_arrive_expect_tx(vf, zero_v ? 8192 : 3 * 8192);
                 if (!zero_v) {  // (the transition slice has zero values)
@@ -361,24 +374,29 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                     tma_load_3d(vs + 8192, &map_v, vf, col0 + 64, h, tt);
                 }
                 tma_load_3d(vs + RV_T, &map_t, vf, 0, 0, 2 * unit);
+                issued[c & 1] = c;
                 // K, A^T, factors (slot free once chunk c - 3 is done)
-                if (c >= 3 && !mbar_wait(bar(B_KE0 + c % 3), (c / 3 - 1) & 1)) { note_fail(3); break; }
+                if (c >= 3 && !wait(bar(B_KE0 + c % 3), (c / 3 - 1) & 1)) { note_fail(3); break; }
                 const uint32_t ks = sbase + kslot(c), kf = bar(B_KF0 + c % 3);
                 // the factors: the decay's 1 KB, plus 1/|k|, 1/|q| with the prologue
                 const uint32_t fbytes = p.prologue ? kFactorBytes : 1024u;
-                mbar_arrive_expect_tx(kf, 3 * 8192 + fbytes);
-                tma_load_3d(ks, &map_k, kf, 0, h, tt);
-                tma_load_3d(ks + 8192, &map_k, kf, 64, h, tt);
-                tma_load_3d(ks + RK_A, &map_t, kf, 0, 0, 2 * unit + 1);
-                bulk_load(ks + RK_G, p.factors + (size_t)unit * 384, fbytes, kf);
+                if (!(c == p.fault_chunk && cta == 0)) {
+                    mbar_arrive_expect_tx(kf, 3 * 8192 + fbytes);
+                    tma_load_3d(ks, &map_k, kf, 0, h, tt);
+                    tma_load_3d(ks + 8192, &map_k, kf, 64, h, tt);
+                    tma_load_3d(ks + RK_A, &map_t, kf, 0, 0, 2 * unit + 1);
+                    bulk_load(ks + RK_G, p.factors + (size_t)unit * 384, fbytes, kf);
+                    issued[2 + c % 3] = c;
+                }
                 // Q (slot free once [QS | WS] of chunk c - 2 is done)
-                if (c >= 2 && !mbar_wait(bar(B_QE0 + (c & 1)), ((c >> 1) - 1) & 1)) { note_fail(3); break; }
+                if (c >= 2 && !wait(bar(B_QE0 + (c & 1)), ((c >> 1) - 1) & 1)) { note_fail(3); break; }
                 const uint32_t qs = sbase + qslot(c), qf = bar(B_QF0 + (c & 1));
                 mbar_arrive_expect_tx(qf, no_out ? 0 : 2 * 8192);
                 if (!no_out) {  // (a segment summary reads no Q)
                     tma_load_3d(qs, &map_q, qf, 0, h, tt);
                     tma_load_3d(qs + 16384, &map_q, qf, 64, h, tt);
                 }
+                issued[5 + (c & 1)] = c;
             }
         }
     } else if (warp < kPrepWarp0) {
@@ -389,7 +407,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
         for (int c = 0; c < n_chunks; ++c) {
             // Slot c%4 moves on to chunk c + 4 only after this role has read O of chunk
             // c + 1, so the parity below is unambiguous.
-            const bool ok = mbar_wait(bar(B_EG0 + (c & 3)), (c >> 2) & 1) && mbar_wait(bar(B_SO), c & 1);
+            const bool ok = wait(bar(B_EG0 + (c & 3)), (c >> 2) & 1) && wait(bar(B_SO), c & 1);
             if (!ok) note_fail(2);
             named_sync(kBarEpi, kEpiThreads);
             if (*fail) break;
@@ -504,7 +522,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             const uint32_t vs = sbase + vslot(c), ks = sbase + kslot(c), qs = sbase + qslot(c);
             unsigned char *vs_p = sm + vslot(c), *ks_p = sm + kslot(c), *qs_p = sm + qslot(c);
             const float *gate = reinterpret_cast<const float *>(ks_p + RK_G);
-            if (!check(mbar_wait(bar(B_VF0 + (c & 1)), u & 1) && mbar_wait(bar(B_KF0 + c % 3), (c / 3) & 1)))
+            if (!check(wait(bar(B_VF0 + (c & 1)), u & 1) && wait(bar(B_KF0 + c % 3), (c / 3) & 1)))
                 break;
             const bool ratio = gate[G_FORM] != 0.f;
             {
@@ -546,8 +564,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             fence_async_smem();
             mbar_arrive(bar(B_TGR0 + (c & 1)));
             // W' done; the Q slot's -W' half free once [QS | WS] of chunk c - 2 is done
-            bool ok = mbar_wait(bar(B_WD0 + (c & 1)), u & 1);
-            if (ok && c >= 2) ok = mbar_wait(bar(B_QE0 + (c & 1)), (u - 1) & 1);
+            bool ok = wait(bar(B_WD0 + (c & 1)), u & 1);
+            if (ok && c >= 2) ok = wait(bar(B_QE0 + (c & 1)), (u - 1) & 1);
             if (!check(ok)) break;
             tc_fence_after();
 
@@ -566,7 +584,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 transpose_store16(r, wsign, nullptr, lane, 16, row_block);
             }
             // Q has landed ([QS | WS] follows B_WQ, and the exponential form scales it here)
-            if (!check(mbar_wait(bar(B_QF0 + (c & 1)), u & 1))) break;
+            if (!check(wait(bar(B_QF0 + (c & 1)), u & 1))) break;
             if (!ratio) {
                 // exponential form: 16-byte segments of Q (gamma) and K (kdec), in place
 #pragma unroll 4
@@ -621,15 +639,15 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             };
             auto tg_ready = [&](int j) { return bar(B_TGR0 + (j & 1)); };
             if (n_chunks > 0) {
-                if (mbar_wait(tg_ready(0), 0)) issue_uw(0);
+                if (wait(tg_ready(0), 0)) issue_uw(0);
                 else note_fail(1);
             }
             for (int c = 0; c < n_chunks && !flags[3]; ++c) {
                 // [O^T | X^T] = S^T [Q; -W']^T once the epilogue has read O of chunk c - 1,
                 // -W' is in place and S^T is written: checked in the order they usually
                 // complete, so that only the last wait is on the chain's critical path
-                bool ok = c == 0 || mbar_wait(bar(B_OFREE), (c - 1) & 1);
-                ok = ok && mbar_wait(bar(B_WQ0 + (c & 1)), (c >> 1) & 1) && mbar_wait(bar(B_SREADY), c & 1);
+                bool ok = c == 0 || wait(bar(B_OFREE), (c - 1) & 1);
+                ok = ok && wait(bar(B_WQ0 + (c & 1)), (c >> 1) & 1) && wait(bar(B_SREADY), c & 1);
                 if (!ok) { note_fail(1); break; }
                 tc_fence_after();
                 const uint32_t qw = sbase + qslot(c);
@@ -664,7 +682,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                     }
                 }
                 // [S^T | O^T] += U'^T [K | A^T] once U'^T (and the decayed master) is in place
-                if (!mbar_wait(bar(B_UREADY), c & 1)) { note_fail(1); break; }
+                if (!wait(bar(B_UREADY), c & 1)) { note_fail(1); break; }
                 tc_fence_after();
                 const uint32_t ks = sbase + kslot(c);
 #pragma unroll
@@ -675,13 +693,13 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 mma_commit(bar(B_SO));
                 mma_commit(bar(B_KE0 + c % 3));  // the state's last reads of the K slot
                 if (!uw_next) {
-                    if (!mbar_wait(tg_ready(c + 1), ((c + 1) >> 1) & 1)) { note_fail(1); break; }
+                    if (!wait(tg_ready(c + 1), ((c + 1) >> 1) & 1)) { note_fail(1); break; }
                     issue_uw(c + 1);
                 }
             }
             if (flags[3]) {  // let issued MMAs land before TMEM and shared memory go away
                 mma_commit(bar(B_DRAIN));
-                mbar_wait(bar(B_DRAIN), 0);
+                wait(bar(B_DRAIN), 0);
             }
         }
     } else if (warp >= kStateWarp0 && warp < kStateWarp0 + kStateWarps) {
@@ -717,7 +735,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             if (c > 0) {
                 const int cp = c - 1;
                 // ---- U'^T = U'~^T + X^T, as bf16 pairs over this thread's read part of X
-                if (!mbar_wait(bar(B_WS), cp & 1)) { note_fail(1); break; }
+                if (!wait(bar(B_WS), cp & 1)) { note_fail(1); break; }
                 tc_fence_after();
                 {
                     float a[32], b[32];
@@ -742,7 +760,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 }
                 warp_arrive(B_UREADY);
                 // ---- the new state (gamma_C S + U'^T K, accumulated in TMEM)
-                if (!mbar_wait(bar(B_SO), cp & 1)) { note_fail(1); break; }
+                if (!wait(bar(B_SO), cp & 1)) { note_fail(1); break; }
                 tc_fence_after();
             }
             if (c == n_chunks) {  // the outgoing state (no chunks: the incoming one)
@@ -774,7 +792,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 tmem_store16(lane_base + TM_SA + 32 * half + 16 * hh, w);
             }
             warp_arrive(B_SREADY);
-            if (!mbar_wait(bar(B_KF0 + c % 3), (c / 3) & 1)) { note_fail(1); break; }
+            if (!wait(bar(B_KF0 + c % 3), (c / 3) & 1)) { note_fail(1); break; }
             const float gC = reinterpret_cast<const float *>(sm + kslot(c) + RK_G)[G_GAM + C - 1];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -789,14 +807,15 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
     __syncthreads();
     if (flags[3] != 0 && tid == 0) {
         atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
-        // loads still in flight land before the shared memory is released: the last
-        // chunk loaded into each slot (a wait on a phase that never completes gives up)
-        for (int c = n_chunks - 1; c >= 0 && c >= n_chunks - 3; --c) {
-            if (c >= n_chunks - 2) {
-                mbar_wait(bar(B_QF0 + (c & 1)), (c >> 1) & 1);
-                mbar_wait(bar(B_VF0 + (c & 1)), (c >> 1) & 1);
-            }
-            mbar_wait(bar(B_KF0 + c % 3), (c / 3) & 1);
+        // loads still in flight land before the shared memory is released: for each slot,
+        // the last chunk the producer issued into it (earlier ones in the slot completed
+        // before that one was issued)
+        for (int i = 0; i < 7; ++i) {
+            const int c = issued[i];
+            if (c < 0) continue;
+            if (i < 2) wait(bar(B_VF0 + i), (c >> 1) & 1);
+            else if (i < 5) wait(bar(B_KF0 + (i - 2)), (c / 3) & 1);
+            else wait(bar(B_QF0 + (i - 5)), (c >> 1) & 1);
         }
     }
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);

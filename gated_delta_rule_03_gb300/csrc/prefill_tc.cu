@@ -309,6 +309,24 @@ static int forced_segments() {
 // (0 unknown, 1 yes, 2 no; racing first uses compute and store the same answer).
 static std::atomic<int> g_cooperative_ok[kMaxDevices];
 
+// The chain kernels' wait bound, and a test of their give-up path: with
+// GDR_DEBUG_CHAIN_FAULT=<chunk> in the environment, the producer of each chain launch's
+// CTA 0 skips the K-slot load of that chunk, and every wait gives up after 2e7 SM cycles
+// (about 10 ms) instead of 2e9. The roles waiting on the missing load then give up, mark
+// the call GDR_ERR_DEVICE_TIMEOUT in the status word and drain; nothing faults or hangs.
+static void chain_wait_policy(chain::TcParams &p) {
+    p.wait_cycles = sm100::kWaitCycles;
+    p.fault_chunk = -1;
+    if (const char *env = getenv("GDR_DEBUG_CHAIN_FAULT")) {
+        char *end = nullptr;
+        const long c = strtol(env, &end, 10);
+        if (end != env && *end == '\0' && c >= 0 && c < (1l << 30)) {
+            p.fault_chunk = (int)c;
+            p.wait_cycles = 20000000;
+        }
+    }
+}
+
 static bool cooperative_ok(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return false;
     int known = g_cooperative_ok[dev].load(std::memory_order_relaxed);
@@ -365,6 +383,7 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     const int grid = device_sms(dev);
     int32_t *flags = reinterpret_cast<int32_t *>(a.ws + L.F);
     TcParams p = {};
+    chain_wait_policy(p);
     p.S_in = a.S0;
     p.factors = reinterpret_cast<const float *>(a.ws + L.G);
     p.cu_seqlens = nullptr;
@@ -436,6 +455,7 @@ static int launch_segmented(const PrefillArgs &a, const WsLayout &L, int segs, c
     float *S_P = sets, *S_R = sets + (kMaxPhases - 1) * set;
     float *S_discard = sets + 2 * (kMaxPhases - 1) * set, *S_start = sets + 3 * (kMaxPhases - 1) * set;
     TcParams p = {};
+    chain_wait_policy(p);
     p.factors = reinterpret_cast<const float *>(a.ws + L.G);
     p.cu_seqlens = a.cu_seqlens;
     p.seq_chunk = reinterpret_cast<const int32_t *>(a.ws + L.seq_chunk);
@@ -541,6 +561,7 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
         }
     }
     TcParams p = {};
+    chain_wait_policy(p);
     p.factors = reinterpret_cast<const float *>(a.ws + L.G);
     p.cu_seqlens = a.cu_seqlens;
     p.num_seqs = a.num_seqs;

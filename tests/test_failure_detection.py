@@ -1,0 +1,56 @@
+"""The tensor-core chain's bounded device waits give up cleanly.
+
+Every wait in the chain kernel is bounded. A role that gives up marks the call
+GDR_ERR_DEVICE_TIMEOUT in the status word, the other roles give up in turn, the
+loads already issued land, issued MMAs complete, TMEM is freed and the kernel
+returns: nothing faults, traps or hangs, and the context stays usable. The
+failure is made on purpose by the library's test knob GDR_DEBUG_CHAIN_FAULT=<chunk>:
+the producer of one chain CTA skips that chunk's K-slot load (a barrier phase
+that nothing completes), and every wait's bound drops to about 10 ms. The test
+checks that the call returns, that the status word reads the timeout, and that
+the next ordinary call on the same workspace matches the float64 oracle.
+"""
+import time
+
+import pytest
+import torch
+
+from gated_delta_rule_03_gb300 import inputs, ops
+from tests.helpers import TOL, chunk_fwd, f64, oracle_prefill, rel_err
+
+pytestmark = pytest.mark.gpu
+
+GDR_ERR_DEVICE_TIMEOUT = -6
+
+
+@pytest.mark.parametrize("schedule", ["phased", "fused"])
+@pytest.mark.parametrize("fault_chunk", [0, 2, 7])
+def test_chain_gives_up_on_a_missing_load_then_the_next_call_is_clean(schedule, fault_chunk,
+                                                                     monkeypatch):
+    if schedule == "phased":
+        monkeypatch.setenv("GDR_PREFILL_PHASES", "1")
+    inp = inputs.prefill_inputs([512, 512], H=2, dk=128, dv=128, dtype="bf16", seed=41,
+                                s0_std=0.2, gate="slow")
+    n, T = inp.num_seqs, inp.total_tokens
+    assert ops.chunk_fwd_schedule(n, T, inp.H, 128, 128, torch.bfloat16) == \
+        (1 if schedule == "phased" else 0)
+    dev = torch.device("cuda", 0)
+    d = lambda t: None if t is None else t.to(dev)
+    q, k, v, la, b, S0 = d(inp.q), d(inp.k), d(inp.v), d(inp.log_alpha), d(inp.beta), d(inp.S0)
+    ws = torch.empty(ops.chunk_fwd_workspace_size(n, T, inp.H, 128, 128), dtype=torch.uint8,
+                     device=dev)
+
+    monkeypatch.setenv("GDR_DEBUG_CHAIN_FAULT", str(fault_chunk))
+    t0 = time.perf_counter()
+    ops.chunk_fwd(q, k, v, la, b, S0=S0, num_seqs=n, workspace=ws)
+    status = ops.read_device_status(ws)  # synchronises
+    elapsed = time.perf_counter() - t0
+    assert status == GDR_ERR_DEVICE_TIMEOUT, ops.status_string(status)
+    assert elapsed < 10.0
+
+    monkeypatch.delenv("GDR_DEBUG_CHAIN_FAULT")
+    o, S = chunk_fwd(q, k, v, la, b, S0=S0, num_seqs=n, workspace=ws)
+    assert ops.read_device_status(ws) == 0
+    ref_o, ref_S = oracle_prefill(inp)
+    assert rel_err(f64(o), ref_o) <= TOL["bf16"]
+    assert rel_err(f64(S), ref_S) <= TOL["bf16"]
