@@ -29,10 +29,14 @@
 //     issued for the next unit as soon as this one's have been read;
 //   * gates: warp 0 scans the log-decays of the unit (loaded while the previous unit
 //     was worked on) into the decay factors;
-//   * products: warp w forms its 16 rows of K K^T (keys up to its own block, for L) and
-//     of K Q^T (queries from its own block on, for A^T) with warp-level bf16 MMAs,
-//     ten 8-column tiles each, so that the four warps share the work evenly; L goes to
-//     shared memory as fp32 16 x 16 blocks, A^T and the factors to the workspace;
+//   * products: one tcgen05 MMA chain per unit, [K; Q] K^T (M = 128: the 64 keys, then
+//     the 64 queries; N = 64 keys; K = d_k) into the group's 64 TMEM columns, issued
+//     by the group's leader as soon as the unit's tiles have landed -- for the next
+//     unit, during this unit's inverse. TMEM lane quarter w belongs to warp w: warps
+//     0 and 1 read the key rows t of K K^T and write L to shared memory as fp32
+//     16 x 16 blocks; warps 2 and 3 read the query rows t of Q K^T and write A^T to the
+//     workspace (neighbouring queries swap one value each so that every store is a
+//     bf16 pair along t); the factors go to the workspace too;
 //   * inverse: the unit lower-triangular (I + L)^{-1} on the CUDA cores in 16 x 16
 //     blocks: warp w inverts diagonal block w by forward substitution, then the blocks
 //     below the diagonal follow level by level (warp w computes block row w, with
@@ -76,20 +80,28 @@ __host__ __device__ constexpr int nblk(int i, int k) {  // N_ik, i > k
 constexpr int UNIT_FLOATS = 16 * BS;
 
 // Shared memory of one group (the CTA holds kGroups of them, 1024-aligned):
-//   keys then queries, each two 64-feature halves of 64 token rows (8 KB, 128-byte
-//   swizzled as TMA writes them); the blocks; the unit's gates; the load barrier and the
-//   group's failure flag.
-constexpr uint32_t G_K = 0, G_Q = 16384;
+//   the unit's keys and queries: for each 64-feature half b of d_k, the 64 key rows then
+//   the 64 query rows (8 KB each, 128-byte swizzled as TMA writes them), so that half b
+//   is the 128-row A operand [K; Q] of the Gram and its first 64 rows the B operand K;
+//   the blocks; the unit's gates; the load and Gram barriers and the group's failure
+//   flag (group 0 also keeps the CTA's TMEM address after them).
+constexpr uint32_t G_KQ = 0;
 constexpr uint32_t G_BLK = 32768;
 constexpr uint32_t G_GATES = G_BLK + UNIT_FLOATS * 4;
 constexpr int GG_G = 0, GG_GAM = 64, GG_GINV = 128, GG_BETA = 192, GG_KDEC = 256,
               GG_NK = 320, GG_NQ = 384;  // floats
 constexpr uint32_t G_BAR = G_GATES + 7 * 64 * 4;
+constexpr uint32_t G_BAR_MMA = G_BAR + 8;
 constexpr int kFactorFloats = 384;  // per unit in the workspace
-constexpr uint32_t G_FAIL = G_BAR + 8;
-constexpr uint32_t GROUP_BYTES = (G_FAIL + 8 + 1023) / 1024 * 1024;
+constexpr uint32_t G_FAIL = G_BAR_MMA + 8;
+constexpr uint32_t G_TMEM_SLOT = G_FAIL + 8;
+constexpr uint32_t GROUP_BYTES = (G_TMEM_SLOT + 8 + 1023) / 1024 * 1024;
 constexpr uint32_t SMEM_BYTES = kGroups * GROUP_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448 && G_GATES % 16 == 0 && G_BAR % 8 == 0, "shared memory");
+// TMEM: 64 fp32 columns per group for its Gram (rows = the 128 lanes)
+constexpr uint32_t kGramCols = 64, kTmemCols = kGroups * kGramCols;
+static_assert(kTmemCols == 256, "TMEM allocation is a power of two");
+constexpr int kBarSolve = 5;  // named barrier of all the solve warps of a CTA
 
 // ---------------------------------------------------------------- warp-level products
 // The unit lower-triangular solve combines 16x16 blocks. These products are far below
@@ -149,23 +161,6 @@ __device__ __forceinline__ void zero16(Acc16 &a) {
         for (int e = 0; e < 4; ++e) a[nt][e] = 0.f;
 }
 
-// ---------------------------------------------------------------- bf16 products of the Gram
-// ldmatrix of four 8x8 bf16 matrices: lane l supplies a row address of matrix l / 8.
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-// d += A B for a 16x16 bf16 A (row-major) and a 16x8 B (held by column), fp32 accumulators.
-__device__ __forceinline__ void mma_bf16_16x8x16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                                 uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // Shared address of the 16-byte segment (row r, features 8c .. 8c + 7) of a 64-feature
 // half tile as TMA writes it with the 128-byte swizzle (segment c of row r at c ^ r % 8).
 __device__ __forceinline__ uint32_t sw128_at(uint32_t half, int r, int c) {
@@ -201,6 +196,7 @@ struct GroupSolver {
     volatile int *gfail;
     int grp, lane, u0, n_units;
     int gid, gstride;          // units gid, gid + gstride, ... are this group's
+    uint32_t tmem_d;           // the group's TMEM columns (lane field 0)
 
     // the unit at local index x: the phase's units in order, or (fused) chunk j of
     // sequence n for head h at x = (j * seqs + n) * H + h
@@ -211,6 +207,7 @@ struct GroupSolver {
     }
     __device__ __forceinline__ void gsync() const { named_sync(1 + grp, 128); }
     __device__ __forceinline__ uint32_t bar_ld() const { return gbase + G_BAR; }
+    __device__ __forceinline__ uint32_t bar_mma() const { return gbase + G_BAR_MMA; }
     // the plan entry of unit x (any x >= n_units: none); every lane of the caller loads it
     __device__ __forceinline__ int4 plan_of(int x) const {
         return x < n_units ? p.plan[unit_at(x) / p.H] : make_int4(0, 0, 0, 0);
@@ -220,9 +217,22 @@ struct GroupSolver {
         mbar_arrive_expect_tx(bar_ld(), 4 * 8192);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            tma_load_3d(gbase + G_K + b * 8192, map_k, bar_ld(), 64 * b, h, pl.y);
-            tma_load_3d(gbase + G_Q + b * 8192, map_q, bar_ld(), 64 * b, h, pl.y);
+            tma_load_3d(gbase + G_KQ + b * 16384, map_k, bar_ld(), 64 * b, h, pl.y);
+            tma_load_3d(gbase + G_KQ + b * 16384 + 8192, map_q, bar_ld(), 64 * b, h, pl.y);
         }
+    }
+    // [K; Q] K^T of the unit whose keys and queries are in the tiles, into the group's
+    // TMEM columns: D row t < 64 holds k_t . k_i, row 64 + t holds q_t . k_i (i < 64).
+    // Issued by the leader once the tiles have landed; completes on bar_mma.
+    __device__ __forceinline__ void issue_gram() const {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t at = gbase + G_KQ + (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16(tmem_d, sw128_desc(at, 16, 1024), sw128_desc(at, 16, 1024),
+                     idesc_bf16(128, 64, 0, 0), kk > 0);
+        }
+        mma_commit(bar_mma());
     }
     // the stored gates of unit x, two tokens per lane of warp 0 (padding past the end of
     // the sequence: log alpha = 0, beta = 0). The loads are only issued here; the values
@@ -259,7 +269,8 @@ struct GroupSolver {
     __device__ __forceinline__ void run() const {
         const int gq = lane >> 2, q = lane & 3;  // m16n8 fragment coordinates
         const bool leader = W == 0 && lane == 0;
-        int loads = 0, landed = 0;
+        // (leader) loads issued and seen landed, Grams issued and consumed
+        int loads = 0, landed = 0, grams = 0, consumed = 0;
         // This group's units are gid, gid + gstride, ...: fixed in advance, so that warp 0
         // can fetch a unit's plan entry and gates a whole unit before it needs them (a
         // claim from a shared counter would put two dependent global round trips on the
@@ -276,9 +287,21 @@ struct GroupSolver {
             fetch_gates(x, pl_cur, raw);
             pl_next = plan_of(x + gstride);
         }
-        uint32_t ld_phase = 0;
+        // the first unit's Gram, once its keys and queries have landed
+        if (leader && x < n_units) {
+            if (mbar_wait(bar_ld(), 0)) {
+                ++landed;
+                issue_gram();
+                ++grams;
+            } else {
+                *gfail = 1;
+            }
+        }
+        uint32_t ld_phase = 0, mma_phase = 0;
         while (x < n_units) {
             const int u = unit_at(x);
+            const bool has_next = x + gstride < n_units;
+            bool gram_next = false;  // (leader) the next unit's Gram is issued
             // ---- gates of unit x: the shared scan of warp 0
             if (W == 0) {
                 float gv[4];
@@ -291,11 +314,15 @@ struct GroupSolver {
                 *reinterpret_cast<float2 *>(gt + GG_KDEC + 2 * lane) =
                     make_float2(fast_exp(sc.g_last - sc.g0), fast_exp(sc.g_last - sc.g1));
             }
-            if (!mbar_wait(bar_ld(), ld_phase)) *gfail = 1;
+            // the unit's tiles have landed (their bytes visible to this thread) and its
+            // Gram is done
+            if (!(mbar_wait(bar_ld(), ld_phase) && mbar_wait(bar_mma(), mma_phase))) *gfail = 1;
             ld_phase ^= 1;
-            gsync();  // the gates are visible; every thread saw the load land (or gave up)
+            mma_phase ^= 1;
+            if (leader) ++consumed;
+            gsync();  // the gates are visible; every thread saw the Gram done (or gave up)
             if (*gfail) break;
-            if (leader) ++landed;
+            tc_fence_after();
             const bool ratio = gt[GG_G + C - 1] > kRatioSafeLogDecay;
             // 1/|k_r| (threads 0-63 of the group) and 1/|q_r| (64-127): the prologue's unit
             // lengths, from the staged rows; ones without it
@@ -303,7 +330,7 @@ struct GroupSolver {
                 const int i = 32 * W + lane, r = i & 63;
                 float inv = 1.f;
                 {
-                    const uint32_t tile = gbase + (i < 64 ? G_K : G_Q);
+                    const uint32_t tile = gbase + G_KQ + (i < 64 ? 0u : 8192u);
                     float ss = 0.f;
 #pragma unroll
                     for (int b = 0; b < 2; ++b)
@@ -312,7 +339,7 @@ struct GroupSolver {
                             uint4 u;
                             asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                                          : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
-                                         : "r"(sw128_at(tile + b * 8192, r, s)));
+                                         : "r"(sw128_at(tile + b * 16384, r, s)));
                             const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
@@ -323,88 +350,71 @@ struct GroupSolver {
                     inv = prologue_inv_norm(ss);
                 }
                 gt[(i < 64 ? GG_NK : GG_NQ) + r] = inv;
+                gsync();  // every row's 1/|k| is in place
             }
 
-            // ---- rows 16W .. 16W + 15 of K K^T (keys i < 16W + 16) and of K Q^T (queries
-            // t >= 16W): ten 8-column tiles; tile pair j2 <= W holds keys 16 j2 .. 16 j2 + 15,
-            // the others queries 16 (j2 - 1) .. 16 (j2 - 1) + 15
-            float acc[10][4];
-#pragma unroll
-            for (int j = 0; j < 10; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const int b = ks >> 2, c = 2 * (ks & 3);  // d_k half, 8-feature segment
-                uint32_t a[4];
-                ldsm_x4(sw128_at(gbase + G_K + b * 8192, 16 * W + (lane & 15), c + (lane >> 4)), a);
-#pragma unroll
-                for (int j2 = 0; j2 < 5; ++j2) {
-                    const bool keys = j2 <= W;
-                    const int r0 = keys ? 16 * j2 : 16 * (j2 - 1);
-                    const uint32_t half = gbase + (keys ? G_K : G_Q) + b * 8192;
-                    uint32_t bf[4];
-                    ldsm_x4(sw128_at(half, r0 + (lane & 7) + 8 * (lane >> 4), c + ((lane >> 3) & 1)), bf);
-                    mma_bf16_16x8x16(acc[2 * j2], a, bf[0], bf[1]);
-                    mma_bf16_16x8x16(acc[2 * j2 + 1], a, bf[2], bf[3]);
-                }
-            }
-            if (kPro) gsync();  // every row's 1/|k| is in place
-            // the gates this warp needs: its rows' (t = 16W + gq + 8hh) and the columns' of
-            // its tiles (i0 = 8j + 2q, two each)
-            float rg[2], rb[2], rgi[2], rkd[2], cg[8][2];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int t = 16 * W + gq + 8 * hh;
-                rg[hh] = ratio ? gt[GG_GAM + t] : gt[GG_G + t];
-                rgi[hh] = gt[GG_G + t];
+            // ---- read out the Gram: warp W holds TMEM lanes 32W .. 32W + 31, read 16
+            // columns (keys) at a time
+            const uint32_t lanes = tmem_d + ((uint32_t)(32 * W) << 16);
+            if (W < 2) {
+                // key row t of K K^T: L_ti = beta_t Gamma_ti k_t.k_i (i < t) into the blocks
+                // of block row t / 16
+                const int t = 32 * W + lane, br = t >> 4, r = t & 15;
+                const float rg = ratio ? gt[GG_GAM + t] : gt[GG_G + t];
                 // L = 0 for the additive rule; 1/|k_t| of the prologue folded into beta_t
-                rb[hh] = p.additive ? 0.f : (kPro ? gt[GG_BETA + t] * gt[GG_NK + t] : gt[GG_BETA + t]);
-                rkd[hh] = ratio ? gt[GG_KDEC + t] : 1.f;
-            }
+                const float rb = p.additive ? 0.f : (kPro ? gt[GG_BETA + t] * gt[GG_NK + t] : gt[GG_BETA + t]);
+                // the warp-wide TMEM loads run for every block column of the warp's two block
+                // rows (2W and 2W + 1); a row's lanes store only its own blocks
+#pragma unroll 1
+                for (int jb = 0; jb <= 2 * W + 1; ++jb) {  // block column jb: keys 16 jb .. +15
+                    float d[16];
+                    tmem_load16(lanes + 16 * jb, d);
+                    if (jb > br) continue;
+                    float *B = U + blk(br, jb);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float2 f = *reinterpret_cast<const float2 *>(gt + (ratio && j < 2 * (W + 1) ? GG_GINV : GG_G) + 8 * j + 2 * q);
-                cg[j][0] = f.x;
-                cg[j][1] = f.y;
-            }
-            const float ginv_c = gt[GG_GINV + C - 1];
-            // L_ti = beta_t Gamma_ti k_t.k_i (i < t) into block row W
+                    for (int cg = 0; cg < 4; ++cg) {
+                        const int i0 = 16 * jb + 4 * cg;
+                        const float4 cf = *reinterpret_cast<const float4 *>(gt + (ratio ? GG_GINV : GG_G) + i0);
+                        const float4 nk4 = kPro ? *reinterpret_cast<const float4 *>(gt + GG_NK + i0)
+                                                : make_float4(1.f, 1.f, 1.f, 1.f);
+                        const float c[4] = {cf.x, cf.y, cf.z, cf.w}, nk[4] = {nk4.x, nk4.y, nk4.z, nk4.w};
+                        float v[4];
 #pragma unroll
-            for (int j = 0; j < 2 * (W + 1); ++j) {
-                const int i0 = 8 * j + 2 * q;
-                float *B = U + blk(W, j >> 1);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int t = 16 * W + gq + 8 * hh;
-                    const float d0 = ratio ? rg[hh] * cg[j][0] : fast_exp(rg[hh] - cg[j][0]);
-                    const float d1 = ratio ? rg[hh] * cg[j][1] : fast_exp(rg[hh] - cg[j][1]);
-                    const float nk0 = kPro ? gt[GG_NK + i0] : 1.f, nk1 = kPro ? gt[GG_NK + i0 + 1] : 1.f;
-                    const float v0 = i0 < t ? rb[hh] * d0 * nk0 * acc[j][2 * hh] : 0.f;
-                    const float v1 = i0 + 1 < t ? rb[hh] * d1 * nk1 * acc[j][2 * hh + 1] : 0.f;
-                    *reinterpret_cast<float2 *>(B + el(gq + 8 * hh, 8 * (j & 1) + 2 * q)) = make_float2(v0, v1);
+                        for (int e = 0; e < 4; ++e) {
+                            const float dec = ratio ? rg * c[e] : fast_exp(rg - c[e]);
+                            v[e] = i0 + e < t ? rb * dec * nk[e] * d[4 * cg + e] : 0.f;
+                        }
+                        *reinterpret_cast<float4 *>(B + el(r, 4 * cg)) = make_float4(v[0], v[1], v[2], v[3]);
+                    }
                 }
-            }
-            // A^T_it (t >= i) for keys i = 16W + gq + 8hh and queries t from 16W on, bf16 to
-            // the workspace; the queries before 16W are zero
-            __nv_bfloat16 *arow = p.Tout + (size_t)(2 * u + 1) * C * C;
+            } else {
+                // query row t of Q K^T: A^T_it for keys i <= t, else 0, bf16 to the workspace.
+                // Lanes t and t ^ 1 swap one value per key pair, so that the even lane stores
+                // (A^T_{2p, t}, A^T_{2p, t+1}) and the odd lane (A^T_{2p+1, t-1}, A^T_{2p+1, t}).
+                const int t = 32 * (W - 2) + lane;
+                const bool odd = lane & 1;
+                const float g_t = gt[GG_G + t], ginv_c = gt[GG_GINV + C - 1];
+                __nv_bfloat16 *arow = p.Tout + (size_t)(2 * u + 1) * C * C + (t & ~1);
+#pragma unroll 1
+                for (int kb = 0; kb < 4; ++kb) {  // keys 16 kb .. 16 kb + 15
+                    float d[16];
+                    tmem_load16(lanes + 16 * kb, d);
 #pragma unroll
-            for (int j = 2 * (W + 1); j < 10; ++j) {
-                const int t0 = 8 * (j - 2) + 2 * q;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int i = 16 * W + gq + 8 * hh;
-                    const float d0 = ratio ? ginv_c : fast_exp(cg[j - 2][0] - rgi[hh]);
-                    const float d1 = ratio ? ginv_c : fast_exp(cg[j - 2][1] - rgi[hh]);
-                    const float v0 = t0 >= i ? acc[j][2 * hh] * d0 : 0.f;
-                    const float v1 = t0 + 1 >= i ? acc[j][2 * hh + 1] * d1 : 0.f;
-                    *reinterpret_cast<uint32_t *>(arow + i * C + t0) = pack_bf16x2(v0, v1);
+                    for (int pp = 0; pp < 8; ++pp) {
+                        const int i0 = 16 * kb + 2 * pp;
+                        float dec0 = ginv_c, dec1 = ginv_c;
+                        if (!ratio) {
+                            const float2 gi = *reinterpret_cast<const float2 *>(gt + GG_G + i0);
+                            dec0 = fast_exp(g_t - gi.x);
+                            dec1 = fast_exp(g_t - gi.y);
+                        }
+                        const float v0 = i0 <= t ? dec0 * d[2 * pp] : 0.f;
+                        const float v1 = i0 + 1 <= t ? dec1 * d[2 * pp + 1] : 0.f;
+                        const float recv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+                        const uint32_t w = odd ? pack_bf16x2(recv, v1) : pack_bf16x2(v0, recv);
+                        *reinterpret_cast<uint32_t *>(arow + (i0 + (odd ? 1 : 0)) * C) = w;
+                    }
                 }
-            }
-#pragma unroll
-            for (int s = 0; s < W; ++s) {  // rows 16W .. 16W + 15, columns 0 .. 16W - 1
-                const int idx = lane + 32 * s, r = 16 * W + (idx & 15), seg = idx >> 4;
-                *reinterpret_cast<uint4 *>(arow + r * C + 8 * seg) = make_uint4(0, 0, 0, 0);
             }
             // the unit's decay factors for the chain: g (warp 0), gamma (1), kdec (2), form (3);
             // 1/|k| (warp 0) and 1/|q| (warp 1)
@@ -420,19 +430,19 @@ struct GroupSolver {
                     *reinterpret_cast<float2 *>(go + 256 + 64 * W + 2 * lane) =
                         *reinterpret_cast<const float2 *>(gt + (W == 0 ? GG_NK : GG_NQ) + 2 * lane);
             }
-            gsync();  // keys and queries are read; L is complete
-            // the next unit: its keys and queries land while the inverse runs; its gates
-            // and the plan entry of the one after are fetched for later
+            tc_fence_before();
+            gsync();  // L is complete; the tiles and the Gram's TMEM columns are read
+            // the next unit: its keys and queries land while the inverse runs (its Gram is
+            // issued once they have); its gates and the plan entry of the one after are
+            // fetched for later
             if (W == 0) {
                 const int xn = x + gstride;
                 if (leader && xn < n_units) {
-                    fence_async_smem();  // the reads above come before the TMA overwrites the tiles
+                    if (kPro) fence_async_smem();  // the norms' reads come before the TMA writes
                     issue_load(xn, pl_next);
                     ++loads;
                 }
                 fetch_gates(xn, pl_next, raw);
-                pl_cur = pl_next;
-                pl_next = plan_of(xn + gstride);
             }
 
             // ---- (I + L)^{-1}: diagonal block W by forward substitution, lane l on column
@@ -469,6 +479,14 @@ struct GroupSolver {
                 for (int k = 0; k < W; ++k) warp_store16(U + blk(W, k), m[k], lane, 1.f);
             }
             gsync();  // every N_kk is in place
+            // the next unit's Gram, if its tiles have landed (else at the end of this unit);
+            // the Gram's TMEM columns were read before the load was issued
+            if (leader && has_next && mbar_test_wait(bar_ld(), ld_phase)) {
+                ++landed;
+                issue_gram();
+                ++grams;
+                gram_next = true;
+            }
             // level 1: N_{W,W-1} = -M_{W,W-1} N_{W-1,W-1}, and the partial sums that need
             // only the diagonal: P20 = M_20 N_00 (warp 2), P31 = M_31 N_11, P30 = M_30 N_00 (3)
             Acc16 pa, pb;
@@ -509,6 +527,9 @@ struct GroupSolver {
             // blocks right of the diagonal, and the diagonal block's upper part, are zero)
             {
                 __nv_bfloat16 *trow = p.Tout + (size_t)2 * u * C * C;
+                float rkd[2];  // kdec of this thread's rows t = 16W + gq + 8hh (ratio form)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) rkd[hh] = ratio ? gt[GG_KDEC + 16 * W + gq + 8 * hh] : 1.f;
                 float cb[4][2][2];  // beta of columns 16 bi + 8 nt + 2q (+1)
 #pragma unroll
                 for (int bi = 0; bi < 4; ++bi)
@@ -542,12 +563,27 @@ struct GroupSolver {
             }
             gsync();  // unit u is stored; the blocks and gates may be reused
             if (kFused && leader) release_flag_gpu(p.flags + u);
+            if (leader && has_next && !gram_next) {
+                if (mbar_wait(bar_ld(), ld_phase)) {
+                    ++landed;
+                    issue_gram();
+                    ++grams;
+                } else {
+                    *gfail = 1;
+                }
+            }
+            if (W == 0) {
+                pl_cur = pl_next;
+                pl_next = plan_of(x + 2 * gstride);
+            }
             x += gstride;
         }
         if (leader) {
             if (*gfail) atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
-            // a load still in flight lands before the shared memory goes away
+            // a load still in flight lands, and a Gram still in flight completes, before the
+            // shared memory and TMEM go away
             for (int j = landed; j < loads; ++j) mbar_wait(bar_ld(), j & 1);
+            if (grams > consumed) mbar_wait(bar_mma(), (grams - 1) & 1);
         }
     }
 };
@@ -571,12 +607,22 @@ __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUten
     volatile int *fail = reinterpret_cast<volatile int *>(gs + G_FAIL);
     if (w == 0 && lane == 0) {
         mbar_init(gbase + G_BAR, 1);
+        mbar_init(gbase + G_BAR_MMA, 1);
         fence_mbar_init();
         *fail = 0;
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_q);
     }
-    named_sync(1 + grp, 128);
+    // the CTA's TMEM: 64 columns per group (its address kept in group 0's area)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + G_TMEM_SLOT);
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    named_sync(kBarSolve, kSolveWarps * 32);
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
     // Everything above overlaps the tail of the planning kernel (programmatic launch);
     // the plan and the status word are read only after it has completed.
@@ -590,12 +636,21 @@ __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUten
         p.ctl[0] == GDR_OK ? (all ? p.ctl[1] * p.H : p.ctl[3 + p.phase] * p.H - u0) : 0;
     const GroupSolver<kFused> gsv{p, &map_q, &map_k, gbase,
                                   reinterpret_cast<float *>(gs + G_BLK), reinterpret_cast<float *>(gs + G_GATES),
-                                  fail, grp, lane, u0, n_units, rank * kGroups + grp, ranks * kGroups};
+                                  fail, grp, lane, u0, n_units, rank * kGroups + grp, ranks * kGroups,
+                                  tmem + (uint32_t)grp * kGramCols};
     switch (w) {
         case 0: p.prologue ? gsv.template run<0, true>() : gsv.template run<0, false>(); break;
         case 1: p.prologue ? gsv.template run<1, true>() : gsv.template run<1, false>(); break;
         case 2: p.prologue ? gsv.template run<2, true>() : gsv.template run<2, false>(); break;
         default: p.prologue ? gsv.template run<3, true>() : gsv.template run<3, false>(); break;
+    }
+    // every group is done with its TMEM columns (their Grams completed or drained)
+    __syncwarp();
+    tc_fence_before();
+    named_sync(kBarSolve, kSolveWarps * 32);
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
