@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgdr.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["gdr_api.cu", "decode.cu", "prefill_exact.cu", "solve_tc.cu", "prefill_tc.cu", "noalloc.cu",
+SOURCES = ["gdr_api.cu", "decode.cu", "prefill_exact.cu", "solve_tc.cu", "prefill_tc.cu", "channel_tc.cu", "noalloc.cu",
            "epilogue.cu"]
 
 

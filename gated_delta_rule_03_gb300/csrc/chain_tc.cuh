@@ -177,6 +177,9 @@ struct TcParams {
     int fault_chunk;
 };
 
+// Every wait's bound, and the give-up test knob (host side, prefill_tc.cu).
+void chain_wait_policy(TcParams &p);
+
 // A chain CTA of a fused launch waits here until the solve has published unit u (its
 // T', A^T and factors stored); false if the call failed meanwhile or the wait ran out.
 __device__ __forceinline__ bool wait_unit_solved(const int32_t *flag, const int32_t *ctl,
@@ -232,7 +235,13 @@ __device__ __forceinline__ void transpose_store16(const uint32_t (&r)[32], float
 // unit to be published before loading its results.
 // kSeg: a launch of the segmented schedule (p.mode 1 or 2); without it p.mode is 0 and
 // the segment branches compile away.
-template <bool kFused, bool kSeg = false>
+// kPC: one forget rate per key channel (d_k = d_v = 128, one slice): every operand comes
+// precomputed from the per-channel chunk kernel (channel_tc.cuh), in the same slots --
+// e^g . Q and -W in the Q slot, e^{g_C - g} . K, A^T and exp(g_C) per channel in the K
+// slot, Utilde^T in the V slot -- so the chain issues only [QS | WS] and [S_upd | AU],
+// prep has nothing to stage, U' = Utilde + X reads Utilde from shared memory, and the
+// master decays column by column.
+template <bool kFused, bool kSeg = false, bool kPC = false>
 __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUtensorMap &map_k,
                                            const CUtensorMap &map_v, const CUtensorMap &map_t,
                                            const CUtensorMap &map_o, const TcParams &p, int cta) {
@@ -362,7 +371,36 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
         // ============================================================ producer
         if (lane == 0) {
             const int unit0 = seq_chunk[n] * p.H + h;  // chunk c is solve unit unit0 + c * H
-            for (int c = 0; c < n_chunks; ++c) {
+            for (int c = 0; kPC && c < n_chunks; ++c) {
+                // per-channel operands: Utilde^T (V slot), e^{g_C - g} . K, A^T and exp(g_C)
+                // (K slot), e^g . Q and -W (Q slot); units of 64 (or 128) rows
+                const int unit = unit0 + c * p.H;
+                if (c >= 2 && !wait(bar(B_VE0 + (c & 1)), ((c >> 1) - 1) & 1)) { note_fail(3); break; }
+                const uint32_t vs = sbase + vslot(c), vf = bar(B_VF0 + (c & 1));
+                mbar_arrive_expect_tx(vf, 2 * 8192);
+                tma_load_3d(vs, &map_v, vf, 0, 0, 128 * unit);
+                tma_load_3d(vs + 8192, &map_v, vf, 0, 0, 128 * unit + 64);
+                issued[c & 1] = c;
+                if (c >= 3 && !wait(bar(B_KE0 + c % 3), (c / 3 - 1) & 1)) { note_fail(3); break; }
+                const uint32_t ks = sbase + kslot(c), kf = bar(B_KF0 + c % 3);
+                if (!(c == p.fault_chunk && cta == 0)) {
+                    mbar_arrive_expect_tx(kf, 3 * 8192 + 512);
+                    tma_load_3d(ks, &map_k, kf, 0, 0, 64 * unit);
+                    tma_load_3d(ks + 8192, &map_k, kf, 64, 0, 64 * unit);
+                    tma_load_3d(ks + RK_A, &map_t, kf, 0, 0, 2 * unit + 1);
+                    bulk_load(ks + RK_G, p.factors + (size_t)unit * 384, 512, kf);
+                    issued[2 + c % 3] = c;
+                }
+                if (c >= 2 && !wait(bar(B_QE0 + (c & 1)), ((c >> 1) - 1) & 1)) { note_fail(3); break; }
+                const uint32_t qs = sbase + qslot(c), qf = bar(B_QF0 + (c & 1));
+                mbar_arrive_expect_tx(qf, 4 * 8192);
+                tma_load_3d(qs, &map_q, qf, 0, 0, 64 * unit);
+                tma_load_3d(qs + 8192, &map_q, qf, 128, 0, 64 * unit);
+                tma_load_3d(qs + 16384, &map_q, qf, 64, 0, 64 * unit);
+                tma_load_3d(qs + 24576, &map_q, qf, 192, 0, 64 * unit);
+                issued[5 + (c & 1)] = c;
+            }
+            for (int c = 0; !kPC && c < n_chunks; ++c) {
                 const int tt = (int)(seq_begin + (int64_t)c * C), unit = unit0 + c * p.H;
                 if (kFused && !wait_unit_solved(p.flags + unit, p.ctl, 2 * wait_limit)) { note_fail(3); break; }
                 // V, T' (slot free once U'~ and W' of chunk c - 2 are done)
@@ -517,7 +555,15 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             named_sync(kBarPrep, kPrepThreads);
             return *fail == 0;
         };
-        for (int c = 0; c < n_chunks; ++c) {
+        for (int c = 0; kPC && c < n_chunks; ++c) {
+            // nothing to stage: the epilogue's rows need no scale (e^g is in the queries),
+            // and this role's reads of the K slot are done once it has landed
+            if (!check(wait(bar(B_KF0 + c % 3), (c / 3) & 1))) break;
+            if (ptid == 0) eg[256 + (c & 3)] = 0.f;
+            mbar_arrive(bar(B_EG0 + (c & 3)));
+            mbar_arrive(bar(B_KE0 + c % 3));
+        }
+        for (int c = 0; !kPC && c < n_chunks; ++c) {
             const int u = c >> 1;
             const uint32_t vs = sbase + vslot(c), ks = sbase + kslot(c), qs = sbase + qslot(c);
             unsigned char *vs_p = sm + vslot(c), *ks_p = sm + kslot(c), *qs_p = sm + qslot(c);
@@ -638,7 +684,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 mma_commit(bar(B_VE0 + (j & 1)));  // V and T' are read
             };
             auto tg_ready = [&](int j) { return bar(B_TGR0 + (j & 1)); };
-            if (n_chunks > 0) {
+            if (!kPC && n_chunks > 0) {
                 if (wait(tg_ready(0), 0)) issue_uw(0);
                 else note_fail(1);
             }
@@ -647,7 +693,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 // -W' is in place and S^T is written: checked in the order they usually
                 // complete, so that only the last wait is on the chain's critical path
                 bool ok = c == 0 || wait(bar(B_OFREE), (c - 1) & 1);
-                ok = ok && wait(bar(B_WQ0 + (c & 1)), (c >> 1) & 1) && wait(bar(B_SREADY), c & 1);
+                // -W: staged by prep, or (per-channel) loaded with the queries
+                ok = ok && wait(bar((kPC ? B_QF0 : B_WQ0) + (c & 1)), (c >> 1) & 1) && wait(bar(B_SREADY), c & 1);
                 if (!ok) { note_fail(1); break; }
                 tc_fence_after();
                 const uint32_t qw = sbase + qslot(c);
@@ -670,7 +717,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 // stages T' diag(gamma) within a few hundred cycles (TM_U buffer (c+1)%2 was
                 // converted before [S_upd | AU] of chunk c - 1; W' of chunk c was read before
                 // B_WQ); else after [S_upd | AU]
-                bool uw_next = c + 1 >= n_chunks;
+                bool uw_next = kPC || c + 1 >= n_chunks;
                 if (!uw_next) {
                     const uint32_t tb = tg_ready(c + 1), par = ((c + 1) >> 1) & 1;
                     const long long t0 = clock64();
@@ -684,6 +731,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 // [S^T | O^T] += U'^T [K | A^T] once U'^T (and the decayed master) is in place
                 if (!wait(bar(B_UREADY), c & 1)) { note_fail(1); break; }
                 tc_fence_after();
+                if (kPC) mbar_arrive(bar(B_VE0 + (c & 1)));  // the state has read Utilde^T
                 const uint32_t ks = sbase + kslot(c);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // tokens 16kk..16kk+15: columns X + 32(kk/2) + 8(kk%2)
@@ -736,12 +784,33 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
                 const int cp = c - 1;
                 // ---- U'^T = U'~^T + X^T, as bf16 pairs over this thread's read part of X
                 if (!wait(bar(B_WS), cp & 1)) { note_fail(1); break; }
+                // (per-channel: Utilde^T is read from the V slot, which nobody else waits for)
+                if (kPC && !wait(bar(B_VF0 + (cp & 1)), (cp >> 1) & 1)) { note_fail(1); break; }
                 tc_fence_after();
                 {
                     float a[32], b[32];
                     if (zero_v) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) a[i] = 0.f;
+                    } else if (kPC) {
+                        // row `row` of Utilde^T (a 128-byte-swizzled box of 64 rows per half of
+                        // d_v), tokens 32 half .. 32 half + 31: four 16-byte segments
+                        const uint32_t box = sbase + vslot(cp) + (row >> 6) * 8192;
+                        const int rr = row & 63;
+#pragma unroll
+                        for (int s4 = 0; s4 < 4; ++s4) {
+                            uint4 w4;
+                            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(w4.x), "=r"(w4.y), "=r"(w4.z), "=r"(w4.w)
+                                         : "r"(sw128_seg(box, rr, 4 * half + s4)));
+                            const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ww[e]));
+                                a[8 * s4 + 2 * e] = f.x;
+                                a[8 * s4 + 2 * e + 1] = f.y;
+                            }
+                        }
                     } else {
                         tmem_load32(lane_base + TM_U + 64 * (cp & 1) + 32 * half, a);
                     }
@@ -793,12 +862,28 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
             }
             warp_arrive(B_SREADY);
             if (!wait(bar(B_KF0 + c % 3), (c / 3) & 1)) { note_fail(1); break; }
-            const float gC = reinterpret_cast<const float *>(sm + kslot(c) + RK_G)[G_GAM + C - 1];
+            const float *fac = reinterpret_cast<const float *>(sm + kslot(c) + RK_G);
+            if (kPC) {  // exp(g_C) per key channel: column 64 half + 32 hh + i of S^T
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+                for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[hh][i] *= gC;
-                tmem_store32(s_tm + 32 * hh, x[hh]);
+                    for (int i4 = 0; i4 < 8; ++i4) {
+                        const float4 f = *reinterpret_cast<const float4 *>(fac + 64 * half + 32 * hh + 4 * i4);
+                        x[hh][4 * i4] *= f.x;
+                        x[hh][4 * i4 + 1] *= f.y;
+                        x[hh][4 * i4 + 2] *= f.z;
+                        x[hh][4 * i4 + 3] *= f.w;
+                    }
+                    tmem_store32(s_tm + 32 * hh, x[hh]);
+                }
+            } else {
+                const float gC = fac[G_GAM + C - 1];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[hh][i] *= gC;
+                    tmem_store32(s_tm + 32 * hh, x[hh]);
+                }
             }
         }
     }

@@ -1,0 +1,428 @@
+// channel_tc.cuh -- the chunk-parallel half of the tensor-core prefill with one forget
+// rate per key channel (bf16, d_k = d_v = 128): every operand of the chain, per
+// (chunk, head) unit.
+//
+// With one rate per token, head and key channel (Kimi Delta Attention, "Attention as
+// Matrix Algebra: From Softmax to the Delta Rule", section 10) row c of the state decays
+// by alpha_t[c], and the chunk form of section 8 keeps its shape with the decay moved
+// into the key channels. Per chunk of C = 64 tokens, g_t[c] = sum_{i <= t} log alpha_i[c]:
+//   L_ti = beta_t sum_c k_t[c] k_i[c] exp(g_t[c] - g_i[c])   (i < t)
+//   A_ti =        sum_c q_t[c] k_i[c] exp(g_t[c] - g_i[c])   (i <= t)
+//   T = (I + L)^{-1} diag(beta),  W = T (e^g . K),  Utilde = T V
+//   U = Utilde - W S,  O = (e^g . Q) S + A U,  S <- diag(e^{g_C}) S + (e^{g_C - g} . K)^T U
+// (e^g . K: row t scaled by exp(g_t[c]) in channel c). Every factor in the last three
+// lines is at most 1.
+//
+// The Gram entries factor around a reference token r of the chunk (token 31):
+// exp(g_t[c] - g_i[c]) = exp(g_t[c] - g_r[c]) exp(g_r[c] - g_i[c]), so that
+//   [L/beta; A] = [K'; Q'] K''^T,  K' = e^{g - g_r} . K,  Q' = e^{g - g_r} . Q,
+//   K'' = e^{g_r - g} . K,
+// one tcgen05 MMA chain (M = 128, N = 64, K = d_k). The factors can exceed 1 but stay
+// finite while -g_r[c] < 80 and g_r[c] - g_C[c] < 80 in every channel; a chunk that
+// decays further (over about e^-160 in some channel) takes every entry as its own sum
+// with exp(g_t[c] - g_i[c]) <= 1 on the CUDA cores instead. W is formed from K' too,
+// W = T K' with column c scaled by exp(g_r[c]) on the way out (exp(0) without the
+// factored Gram).
+//
+// One CTA of four warps per unit; TMEM lane quarter w belongs to warp w. Outputs (the
+// chain kernel loads them by TMA, 128-byte swizzled 64 x 64 boxes):
+//   QW [units * 64][256] bf16: e^g . Q in columns 0..127, -W in columns 128..255;
+//   KT [units * 64][128] bf16: e^{g_C - g} . K;
+//   UT [units * 128][64] bf16: Utilde^T (row j: value column j over the chunk's tokens);
+//   AT [units][2][64][64] bf16: A^T in matrix 2u + 1 (row i, column t);
+//   G  [units][384] fp32: exp(g_C[c]) in floats 0..127.
+// Padding rows of a partial last chunk get log alpha = 0 and beta = 0: their rows of T,
+// W, Utilde are zero and they change nothing.
+#pragma once
+
+#include "solve_tc.cuh"
+
+namespace gdr {
+namespace channel {
+
+using namespace sm100;
+using namespace tc;
+using solve::Acc16;
+using solve::blk;
+using solve::el;
+using solve::invert_unit;
+using solve::nblk;
+
+constexpr int C = kChunk;
+constexpr int DK = 128, DV = 128;
+constexpr int kThreads = 128;
+// The reference token of the factored Gram, and the bound that keeps its factors finite.
+constexpr int kRefToken = 31;
+constexpr float kFactorLogBound = 80.f;
+
+// Shared memory map (bytes from a 1024-aligned base).
+constexpr uint32_t P_KQ = 0;       // per d_k half b at 16384 b: 64 key rows, then 64 query rows
+constexpr uint32_t P_KC = 32768;   // the Gram's B operand K'': two 64-column halves of 8 KB
+constexpr uint32_t P_V = 49152;    // V: two 64-column halves of 8 KB
+constexpr uint32_t P_G = P_KC;     // (unfactored Gram) g, fp32 [C][DK], over P_KC and P_V
+constexpr uint32_t P_BLK = 65536;  // the unit's 16 x 16 blocks (the solve's layout)
+constexpr uint32_t P_TP = P_BLK + (solve::UNIT_FLOATS * 4 + 1023) / 1024 * 1024;  // T' bf16 [t][i]
+constexpr uint32_t P_MISC = P_TP + 8192;  // floats: beta[64], g_C[128], g_r[128], half sums[128],
+                                          // the "V reload gave up" flag
+constexpr int M_BETA = 0, M_GC = 64, M_GREF = 192, M_HSUM = 320, M_FLAG = 448;
+constexpr uint32_t P_BARS = P_MISC + 456 * 4;  // load, Gram, products, V reload, drain
+constexpr uint32_t P_TMEM = P_BARS + 40;
+constexpr uint32_t P_USED = P_TMEM + 16;
+constexpr uint32_t SMEM_BYTES = P_USED + 1024;
+static_assert(P_TP % 1024 == 0 && P_BARS % 8 == 0 && SMEM_BYTES <= 232448 / 2, "shared memory");
+// TMEM columns: the Gram, W^T, Utilde^T (64 each)
+constexpr uint32_t TM_GRAM = 0, TM_W = 64, TM_UT = 128, TM_COLS = 256;
+
+struct ChannelParams {
+    const float *log_alpha;  // [tokens, H, DK]
+    const float *beta;       // [tokens, H]
+    const int4 *plan;        // per chunk: sequence, first token, tokens, index
+    int32_t *ctl;
+    int H;
+    int additive;            // the additive rule: L = 0, W = 0
+    __nv_bfloat16 *QW, *KT, *UT, *AT;
+    float *G;
+};
+
+// Element (row, col) of a 128-byte-swizzled block of 64-wide bf16 rows at `block`.
+__device__ __forceinline__ float sw_elem(const unsigned char *block, int row, int col) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(block + sw128_offset(row, col)));
+}
+
+// T' = (I + L)^{-1} diag(beta), block row W of warp W, as bf16 into the swizzled [t][i]
+// tile `tp` (the B operand of the products; zeros right of the diagonal).
+template <int W>
+__device__ __forceinline__ void store_t_prime(const float *__restrict__ U, const float *__restrict__ beta,
+                                              unsigned char *tp, int lane) {
+    const int gq = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int bi = 0; bi < 4; ++bi) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int i0 = 16 * bi + 8 * nt + 2 * q;
+            float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+            if (bi <= W) {
+                const float *B = U + (bi == W ? blk(W, W) : nblk(W > bi ? W : 1, W > bi ? bi : 0));
+                lo = *reinterpret_cast<const float2 *>(B + el(gq, 8 * nt + 2 * q));
+                hi = *reinterpret_cast<const float2 *>(B + el(gq + 8, 8 * nt + 2 * q));
+            }
+            const float b0 = beta[i0], b1 = beta[i0 + 1];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int t = 16 * W + gq + 8 * hh;
+                const float2 v = hh ? hi : lo;
+                const float x0 = i0 <= t ? v.x * b0 : 0.f;
+                const float x1 = i0 + 1 <= t ? v.y * b1 : 0.f;
+                *reinterpret_cast<uint32_t *>(tp + sw128_offset(t, i0)) = pack_bf16x2(x0, x1);
+            }
+        }
+    }
+}
+
+// The unit (chunk blockIdx.x, head blockIdx.y). map_q, map_k, map_v: the inputs.
+__global__ void __launch_bounds__(kThreads)
+channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const ChannelParams p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, h = blockIdx.y;
+    float *misc = reinterpret_cast<float *>(sm + P_MISC);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P_TMEM);
+    auto bar = [&](int i) { return sb + P_BARS + 8u * (uint32_t)i; };
+    if (tid == 0) {
+        for (int i = 0; i < 5; ++i) mbar_init(bar(i), 1);
+        misc[M_FLAG] = 0.f;
+        fence_mbar_init();
+        prefetch_tensormap(&map_q);
+        prefetch_tensormap(&map_k);
+        prefetch_tensormap(&map_v);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tslot), TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    // Everything above overlaps the tail of the planning kernel (programmatic launch).
+    griddep_wait();
+    griddep_launch_dependents();
+    const bool live = p.ctl[0] == GDR_OK && c < p.ctl[1];
+    bool fail = false;
+    if (live) {
+        const int4 pl = p.plan[c];
+        const int t0 = pl.y, len = pl.z;
+        const size_t u = (size_t)c * p.H + h;  // chunk-major, head-minor
+        if (tid == 0) {
+            mbar_arrive_expect_tx(bar(0), 6 * 8192);
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                tma_load_3d(sb + P_KQ + 16384 * b, &map_k, bar(0), 64 * b, h, t0);
+                tma_load_3d(sb + P_KQ + 16384 * b + 8192, &map_q, bar(0), 64 * b, h, t0);
+                tma_load_3d(sb + P_V + 8192 * b, &map_v, bar(0), 64 * b, h, t0);
+            }
+        }
+        if (tid < C) misc[M_BETA + tid] = tid < len ? p.beta[(size_t)(t0 + tid) * p.H + h] : 0.f;
+        // g by columns: thread (cp, th) owns channels 2cp, 2cp + 1 over tokens 32th .. 32th + 31
+        const int cp = tid & 63, th = tid >> 6;
+        float g[32][2];
+        {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int t = 32 * th + j;
+                float2 la = make_float2(0.f, 0.f);
+                if (t < len)
+                    la = *reinterpret_cast<const float2 *>(p.log_alpha + ((size_t)(t0 + t) * p.H + h) * DK + 2 * cp);
+                a0 += la.x;
+                a1 += la.y;
+                g[j][0] = a0;
+                g[j][1] = a1;
+            }
+            if (th == 0) {
+                misc[M_HSUM + 2 * cp] = a0;
+                misc[M_HSUM + 2 * cp + 1] = a1;
+                misc[M_GREF + 2 * cp] = g[kRefToken][0];
+                misc[M_GREF + 2 * cp + 1] = g[kRefToken][1];
+            }
+        }
+        __syncthreads();
+        if (th == 1) {
+            const float s0 = misc[M_HSUM + 2 * cp], s1 = misc[M_HSUM + 2 * cp + 1];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                g[j][0] += s0;
+                g[j][1] += s1;
+            }
+            misc[M_GC + 2 * cp] = g[31][0];
+            misc[M_GC + 2 * cp + 1] = g[31][1];
+        }
+        __syncthreads();
+        const float gc0 = misc[M_GC + 2 * cp], gc1 = misc[M_GC + 2 * cp + 1];
+        const float gr0 = misc[M_GREF + 2 * cp], gr1 = misc[M_GREF + 2 * cp + 1];
+        const bool col_ok = -gr0 < kFactorLogBound && gr0 - gc0 < kFactorLogBound &&
+                            -gr1 < kFactorLogBound && gr1 - gc1 < kFactorLogBound;
+        const bool factored = __syncthreads_and(col_ok) != 0;
+        // the shift of the tiles the products read: g_r with the factored Gram, else none
+        const float sh0 = factored ? gr0 : 0.f, sh1 = factored ? gr1 : 0.f;
+        if (!mbar_wait(bar(0), 0)) fail = true;
+        fail = __syncthreads_or(fail) != 0;
+        float *U = reinterpret_cast<float *>(sm + P_BLK);
+        __nv_bfloat16 *arow = p.AT + (u * 2 + 1) * C * C;
+        if (!fail && !factored) {
+            // ---- the unfactored Gram on the CUDA cores: g to shared memory (over K'' and
+            // V; V is loaded again below), every entry as its own sum
+            float *gs = reinterpret_cast<float *>(sm + P_G);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                *reinterpret_cast<float2 *>(gs + (32 * th + j) * DK + 2 * cp) = make_float2(g[j][0], g[j][1]);
+            for (int e = tid; e < 10 * solve::BS; e += kThreads) U[e] = 0.f;  // the ten L blocks
+            __syncthreads();
+            for (int e = tid; e < C * C; e += kThreads) {
+                const int t = e >> 6, i = e & 63;  // A^T row i, column t: this thread's entry
+                float kk = 0.f, qk = 0.f;
+                if (i <= t) {
+                    for (int d = 0; d < DK; ++d) {
+                        const unsigned char *half = sm + P_KQ + 16384 * (d >> 6);
+                        const float f = fast_exp(gs[t * DK + d] - gs[i * DK + d]);
+                        const float ki = sw_elem(half, i, d & 63) * f;
+                        kk = fmaf(sw_elem(half, t, d & 63), ki, kk);
+                        qk = fmaf(sw_elem(half + 8192, t, d & 63), ki, qk);
+                    }
+                    if (i < t && !p.additive) U[blk(t >> 4, i >> 4) + el(t & 15, i & 15)] = misc[M_BETA + t] * kk;
+                }
+                arow[i * C + t] = __float2bfloat16_rn(qk);
+            }
+            fence_async_smem();  // the g table's writes come before the TMA overwrites it
+            __syncthreads();
+            if (tid == 0) {  // V again (the g table used its space)
+                mbar_arrive_expect_tx(bar(3), 2 * 8192);
+                tma_load_3d(sb + P_V, &map_v, bar(3), 0, h, t0);
+                tma_load_3d(sb + P_V + 8192, &map_v, bar(3), 64, h, t0);
+            }
+        }
+        if (!fail) {
+            // ---- element-wise: the chain's e^g . Q and e^{g_C - g} . K to the workspace,
+            // the products' tiles in place: K' = e^{g - sh} . K (and with the factored Gram
+            // Q' = e^{g - sh} . Q, K'' = e^{sh - g} . K). Thread (cp, th): channels 2cp,
+            // 2cp + 1 of its 32 tokens, one bf16 pair each.
+            const int b = cp >> 5, cc = cp & 31;
+            unsigned char *kh = sm + P_KQ + 16384 * b, *qh = kh + 8192, *kc = sm + P_KC + 8192 * b;
+            __nv_bfloat16 *qw = p.QW + (u * C) * 256 + 2 * cp;
+            __nv_bfloat16 *kt = p.KT + (u * C) * DK + 2 * cp;
+#pragma unroll 4
+            for (int j = 0; j < 32; ++j) {
+                const int t = 32 * th + j;
+                const uint32_t off = (uint32_t)(t * 128 + ((((cc >> 2) ^ t) & 7) << 4) + (cc & 3) * 4);
+                const float2 k2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(kh + off));
+                const float2 q2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qh + off));
+                const float e0 = fast_exp(g[j][0]), e1 = fast_exp(g[j][1]);
+                *reinterpret_cast<uint32_t *>(qw + (size_t)t * 256) = pack_bf16x2(q2.x * e0, q2.y * e1);
+                *reinterpret_cast<uint32_t *>(kt + (size_t)t * DK) =
+                    pack_bf16x2(k2.x * fast_exp(gc0 - g[j][0]), k2.y * fast_exp(gc1 - g[j][1]));
+                const float s0 = fast_exp(g[j][0] - sh0), s1 = fast_exp(g[j][1] - sh1);
+                *reinterpret_cast<uint32_t *>(kh + off) = pack_bf16x2(k2.x * s0, k2.y * s1);
+                if (factored) {
+                    *reinterpret_cast<uint32_t *>(qh + off) = pack_bf16x2(q2.x * s0, q2.y * s1);
+                    *reinterpret_cast<uint32_t *>(kc + off) =
+                        pack_bf16x2(k2.x * fast_exp(sh0 - g[j][0]), k2.y * fast_exp(sh1 - g[j][1]));
+                }
+            }
+            fence_async_smem();
+            __syncthreads();
+            if (factored) {
+                if (tid == 0) {  // [K'; Q'] K''^T: row t < 64 of D is L_t. / beta_t, row 64 + t is A_t.
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t at = sb + P_KQ + (kk >> 2) * 16384 + (kk & 3) * 32;
+                        const uint32_t bt = sb + P_KC + (kk >> 2) * 8192 + (kk & 3) * 32;
+                        mma_bf16(tmem + TM_GRAM, sw128_desc(at, 16, 1024), sw128_desc(bt, 16, 1024),
+                                 idesc_bf16(128, 64, 0, 0), kk > 0);
+                    }
+                    mma_commit(bar(1));
+                }
+                if (!mbar_wait(bar(1), 0)) fail = true;
+                tc_fence_after();
+                // the Gram's rows, warp w on TMEM lanes 32w .. 32w + 31, 16 columns at a time
+                const uint32_t lanes = tmem + TM_GRAM + ((uint32_t)(32 * warp) << 16);
+                if (warp < 2) {
+                    const int t = 32 * warp + lane, br = t >> 4, r = t & 15;
+                    const float rb = p.additive ? 0.f : misc[M_BETA + t];
+#pragma unroll 1
+                    for (int jb = 0; jb <= 2 * warp + 1; ++jb) {  // warp-uniform trip count
+                        float d[16];
+                        tmem_load16(lanes + 16 * jb, d);
+                        if (jb > br) continue;
+                        float *B = U + blk(br, jb);
+#pragma unroll
+                        for (int cg = 0; cg < 4; ++cg) {
+                            float v[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) v[e] = 16 * jb + 4 * cg + e < t ? rb * d[4 * cg + e] : 0.f;
+                            *reinterpret_cast<float4 *>(B + el(r, 4 * cg)) = make_float4(v[0], v[1], v[2], v[3]);
+                        }
+                    }
+                } else {
+                    // A^T_it for keys i <= t: neighbouring lanes swap one value per key pair
+                    // so that each store is a bf16 pair along the queries t
+                    const int t = 32 * (warp - 2) + lane;
+                    const bool odd = lane & 1;
+                    __nv_bfloat16 *ar = arow + (t & ~1);
+#pragma unroll 1
+                    for (int kb = 0; kb < 4; ++kb) {
+                        float d[16];
+                        tmem_load16(lanes + 16 * kb, d);
+#pragma unroll
+                        for (int pp = 0; pp < 8; ++pp) {
+                            const int i0 = 16 * kb + 2 * pp;
+                            const float v0 = i0 <= t ? d[2 * pp] : 0.f;
+                            const float v1 = i0 + 1 <= t ? d[2 * pp + 1] : 0.f;
+                            const float recv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+                            *reinterpret_cast<uint32_t *>(ar + (i0 + (odd ? 1 : 0)) * C) =
+                                odd ? pack_bf16x2(recv, v1) : pack_bf16x2(v0, recv);
+                        }
+                    }
+                }
+            }
+            fail = __syncthreads_or(fail) != 0;  // (also: the L blocks are complete)
+        }
+        if (!fail) {
+            // ---- (I + L)^{-1}, then T' = (I + L)^{-1} diag(beta) into the swizzled tile
+            auto sync4 = [] { __syncthreads(); };
+            auto none = [] {};
+            const float *beta_s = misc + M_BETA;
+            unsigned char *tp = sm + P_TP;
+            switch (warp) {
+                case 0: invert_unit<0>(U, lane, sync4, none); store_t_prime<0>(U, beta_s, tp, lane); break;
+                case 1: invert_unit<1>(U, lane, sync4, none); store_t_prime<1>(U, beta_s, tp, lane); break;
+                case 2: invert_unit<2>(U, lane, sync4, none); store_t_prime<2>(U, beta_s, tp, lane); break;
+                default: invert_unit<3>(U, lane, sync4, none); store_t_prime<3>(U, beta_s, tp, lane); break;
+            }
+            fence_async_smem();
+            __syncthreads();
+            // ---- W^T = K'^T T'^T (M = d_k) and Utilde^T = V^T T'^T (M = d_v)
+            if (tid == 0) {
+                bool v_ok = factored || mbar_wait(bar(3), 0);
+                if (v_ok) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + TM_W, sw128_desc(sb + P_KQ + kk * 2048, 16384, 1024),
+                                 sw128_desc(sb + P_TP + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + TM_UT, sw128_desc(sb + P_V + kk * 2048, 8192, 1024),
+                                 sw128_desc(sb + P_TP + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
+                    mma_commit(bar(2));
+                } else {
+                    misc[M_FLAG] = 1.f;  // (the V reload gave up: nothing was issued)
+                }
+            }
+            __syncthreads();
+            const bool issued = misc[M_FLAG] == 0.f;
+            if (!issued) fail = true;
+            if (issued && !mbar_wait(bar(2), 0)) fail = true;
+            tc_fence_after();
+            fail = __syncthreads_or(fail) != 0;
+            if (!fail) {
+                // -W rows: lane j = d_k index of warp w's quarter; column t of W^T scaled by
+                // exp(sh_j); lanes j, j ^ 1 swap one value per token pair so that each store
+                // is a bf16 pair along d_k
+                const int j = 32 * warp + lane;
+                const bool odd = lane & 1;
+                const float sc = p.additive ? 0.f : -fast_exp(factored ? misc[M_GREF + j] : 0.f);
+                __nv_bfloat16 *wq = p.QW + (u * C) * 256 + 128 + (j & ~1);
+                const uint32_t lw = tmem + TM_W + ((uint32_t)(32 * warp) << 16);
+#pragma unroll 1
+                for (int tb = 0; tb < 4; ++tb) {
+                    float d[16];
+                    tmem_load16(lw + 16 * tb, d);
+#pragma unroll
+                    for (int pp = 0; pp < 8; ++pp) {
+                        const int tt = 16 * tb + 2 * pp;
+                        const float v0 = sc * d[2 * pp], v1 = sc * d[2 * pp + 1];
+                        const float recv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+                        *reinterpret_cast<uint32_t *>(wq + (size_t)(tt + (odd ? 1 : 0)) * 256) =
+                            odd ? pack_bf16x2(recv, v1) : pack_bf16x2(v0, recv);
+                    }
+                }
+                // Utilde^T rows: lane j = value column, its 64 tokens as one 128-byte row
+                const uint32_t lu = tmem + TM_UT + ((uint32_t)(32 * warp) << 16);
+                uint4 *ur = reinterpret_cast<uint4 *>(p.UT + (u * DV + j) * C);
+#pragma unroll 1
+                for (int tb = 0; tb < 4; ++tb) {
+                    float d[16];
+                    tmem_load16(lu + 16 * tb, d);
+                    ur[2 * tb] = make_uint4(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]),
+                                            pack_bf16x2(d[4], d[5]), pack_bf16x2(d[6], d[7]));
+                    ur[2 * tb + 1] = make_uint4(pack_bf16x2(d[8], d[9]), pack_bf16x2(d[10], d[11]),
+                                                pack_bf16x2(d[12], d[13]), pack_bf16x2(d[14], d[15]));
+                }
+                // the state's decay over the chunk, per channel
+                p.G[u * 384 + j] = fast_exp(misc[M_GC + j]);
+            }
+        }
+        if (fail && tid == 0) {
+            atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
+            // loads and MMAs still in flight land before the shared memory and TMEM go
+            mbar_wait(bar(0), 0);
+            if (!factored) mbar_wait(bar(3), 0);
+            mma_commit(bar(4));
+            mbar_wait(bar(4), 0);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TM_COLS);
+    }
+}
+
+}  // namespace channel
+}  // namespace gdr

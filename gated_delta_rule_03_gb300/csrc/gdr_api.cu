@@ -16,12 +16,16 @@ bool use_tensor_path(int dk, int dv, int dtype) {
     return dtype == GDR_BF16 && dk == 128 && (dv == 128 || dv == 256);
 }
 
+bool use_channel_tc(int dk, int dv, int dtype, int prologue) {
+    return dtype == GDR_BF16 && dk == 128 && dv == 128 && prologue == GDR_PROLOGUE_NONE;
+}
+
 WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype,
-                   int decay) {
+                   int decay, int prologue) {
     WsLayout L;
     memset(&L, 0, sizeof(L));
-    // per-channel rates take the exact path
     L.tensor_path = decay == GDR_DECAY_HEAD && use_tensor_path(dk, dv, dtype);
+    L.channel_tc = decay == GDR_DECAY_CHANNEL && use_channel_tc(dk, dv, dtype, prologue);
     L.max_chunks = total_tokens / kChunk + num_seqs;
     size_t off = 0;
     L.ctl = off;
@@ -30,7 +34,19 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
     off = align_up(off + sizeof(int4) * (size_t)L.max_chunks, 256);
     L.seq_chunk = off;
     off = align_up(off + sizeof(int32_t) * (size_t)kMaxPhases * (size_t)(num_seqs + 1), 256);
-    if (!L.tensor_path) {
+    if (L.channel_tc) {
+        const size_t units = (size_t)L.max_chunks * (size_t)H;
+        L.T = off;  // A^T in the second of two 64x64 bf16 matrices per unit
+        off = align_up(off + units * 2 * kChunk * kChunk * 2, 256);
+        L.G = off;  // 384 floats per unit: exp(g_C) per channel first
+        off = align_up(off + units * 384 * sizeof(float), 256);
+        L.QW = off;
+        off = align_up(off + units * kChunk * 256 * 2, 256);
+        L.KT = off;
+        off = align_up(off + units * kChunk * 128 * 2, 256);
+        L.UT = off;
+        off = align_up(off + units * 128 * kChunk * 2, 256);
+    } else if (!L.tensor_path) {
         const size_t per = (size_t)L.max_chunks * (size_t)H * kChunk;
         L.W = off;
         off = align_up(off + sizeof(float) * per * dk, 256);
@@ -153,7 +169,7 @@ size_t gdr_chunk_fwd_workspace_size_ex(int64_t num_seqs, int64_t total_tokens, i
     Opts op;
     if (check_options(options, &op) != GDR_OK) return 0;
     if (check_prefill_sizes(num_seqs, total_tokens, H, d_k, d_v, chunk, dtype) != GDR_OK) return 0;
-    return ws_layout(num_seqs, total_tokens, H, d_k, d_v, dtype, op.decay).total;
+    return ws_layout(num_seqs, total_tokens, H, d_k, d_v, dtype, op.decay, op.prologue).total;
 }
 
 int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -176,7 +192,7 @@ int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     const void *ptrs4[] = {log_alpha, beta, cu_seqlens};
     for (const void *p : ptrs4)
         if (p && !aligned4(p)) return GDR_ERR_ALIGNMENT;
-    const WsLayout L = ws_layout(num_seqs, total_tokens, H, d_k, d_v, dtype, op.decay);
+    const WsLayout L = ws_layout(num_seqs, total_tokens, H, d_k, d_v, dtype, op.decay, op.prologue);
     if (workspace_bytes < L.total) return GDR_ERR_WORKSPACE;
     const size_t esz = dtype == GDR_F32 ? 4 : 2;
     const size_t o_bytes = (size_t)total_tokens * H * d_v * esz;
@@ -206,10 +222,11 @@ int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     const int phases = L.tensor_path ? tc_schedule(a) : 1;
     st = launch_plan(a, L, phases);
     if (st != GDR_OK) return st;
-    st = L.tensor_path ? launch_prefill_tc(a, L, phases) : launch_prefill_exact(a, L);
-    // the output step, where the chain did not fuse it (it does on the tensor-core path
+    st = L.channel_tc ? launch_prefill_channel_tc(a, L)
+                      : (L.tensor_path ? launch_prefill_tc(a, L, phases) : launch_prefill_exact(a, L));
+    // the output step, where the chain did not fuse it (it does on the tensor-core paths
     // when one chain CTA holds all d_v = 128 entries of a token)
-    if (st == GDR_OK && a.out_gate && !(L.tensor_path && d_v == 128))
+    if (st == GDR_OK && a.out_gate && !((L.tensor_path || L.channel_tc) && d_v == 128))
         st = launch_out_norm_gate(o, a.out_gate, a.out_norm_weight, a.out_norm_eps,
                                   total_tokens * H, d_v, dtype, a.stream);
     return st;
@@ -260,6 +277,17 @@ int gdr_decode_step(const void *q, const void *k, const void *v, const float *lo
 int gdr_chunk_fwd_path(int d_k, int d_v, int dtype) {
     const int st = check_prefill_sizes(1, 0, 1, d_k, d_v, kChunk, dtype);
     if (st != GDR_OK) return st;
+    return use_tensor_path(d_k, d_v, dtype) ? GDR_PATH_TENSOR : GDR_PATH_EXACT;
+}
+
+int gdr_chunk_fwd_path_ex(int d_k, int d_v, int dtype, const gdr_options *options) {
+    Opts op;
+    int st = check_options(options, &op);
+    if (st != GDR_OK) return st;
+    st = check_prefill_sizes(1, 0, 1, d_k, d_v, kChunk, dtype);
+    if (st != GDR_OK) return st;
+    if (op.decay == GDR_DECAY_CHANNEL)
+        return use_channel_tc(d_k, d_v, dtype, op.prologue) ? GDR_PATH_CHANNEL_TENSOR : GDR_PATH_EXACT;
     return use_tensor_path(d_k, d_v, dtype) ? GDR_PATH_TENSOR : GDR_PATH_EXACT;
 }
 

@@ -69,13 +69,20 @@ struct WsLayout {
                           // fp32 state sets, [NH][d_k][d_v] each: (kMaxPhases - 1) each
                           // of P, R and discard, kMaxPhases of start; 0 bytes otherwise
     bool segmentable;
+    size_t QW, KT, UT;    // tensor-core path with per-channel rates: per unit, bf16
+                          // [64][256] e^g . Q | -W, [64][128] e^{g_C - g} . K, [128][64] Utilde^T
+                          // (T holds A^T, G exp(g_C) per channel)
     size_t total;
-    bool tensor_path;     // bf16 tensor-core kernel (true) or exact fp32-arithmetic kernels
+    bool tensor_path;     // bf16 tensor-core kernels with one rate per head
+    bool channel_tc;      // bf16 tensor-core kernels with one rate per key channel
 };
 
 bool use_tensor_path(int dk, int dv, int dtype);
+// Per-channel rates on the tensor cores: bf16, d_k = d_v = 128, no layer prologue (the other
+// cases take the exact path).
+bool use_channel_tc(int dk, int dv, int dtype, int prologue);
 WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype,
-                   int decay = GDR_DECAY_HEAD);
+                   int decay = GDR_DECAY_HEAD, int prologue = GDR_PROLOGUE_NONE);
 
 // Launchers (return GDR_OK or GDR_ERR_CUDA).
 // The planning kernel for a schedule (the fused schedule, 0, plans one phase and clears
@@ -83,6 +90,9 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
 int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases);
 int launch_prefill_exact(const PrefillArgs &a, const WsLayout &L);
 int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases);
+// The tensor-core path with one forget rate per key channel: the per-channel chunk kernel
+// over every unit, then the chains (one phase).
+int launch_prefill_channel_tc(const PrefillArgs &a, const WsLayout &L);
 
 // The schedule of a tensor-core prefill: 0 for the fused cooperative launch,
 // 1 .. kMaxPhases phases of the two-kernel schedule, or kSegmentedBase + n for n

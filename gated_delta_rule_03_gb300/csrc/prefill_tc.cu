@@ -314,7 +314,8 @@ static std::atomic<int> g_cooperative_ok[kMaxDevices];
 // CTA 0 skips the K-slot load of that chunk, and every wait gives up after 2e7 SM cycles
 // (about 10 ms) instead of 2e9. The roles waiting on the missing load then give up, mark
 // the call GDR_ERR_DEVICE_TIMEOUT in the status word and drain; nothing faults or hangs.
-static void chain_wait_policy(chain::TcParams &p) {
+namespace chain {
+void chain_wait_policy(TcParams &p) {
     p.wait_cycles = sm100::kWaitCycles;
     p.fault_chunk = -1;
     if (const char *env = getenv("GDR_DEBUG_CHAIN_FAULT")) {
@@ -326,6 +327,7 @@ static void chain_wait_policy(chain::TcParams &p) {
         }
     }
 }
+}  // namespace chain
 
 static bool cooperative_ok(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return false;

@@ -167,6 +167,87 @@ __device__ __forceinline__ uint32_t sw128_at(uint32_t half, int r, int c) {
     return half + (uint32_t)(r * 128 + (((c ^ r) & 7) << 4));
 }
 
+// (I + L)^{-1} of one unit, in place in its 16 x 16 blocks (the layout above). On entry
+// the ten lower blocks hold L: strictly lower triangular, the diagonal blocks zero on and
+// above their diagonal. On return blk(i, i) holds N_ii and nblk(i, k) holds N_ik (i > k)
+// of N = (I + L)^{-1} (blk(i, k), i > k, then holds M_ik = N_ii L_ik). Warp W of four
+// computes block row W: the diagonal block by forward substitution (lane l on column
+// l % 16; the upper half of the warp repeats the lower and stores nothing), then the
+// blocks below the diagonal level by level with warp-level TF32 products. sync() is a
+// barrier of the four warps; after_diag() runs on every thread once the diagonal blocks'
+// inverses are in place (before the levels).
+template <int W, typename Sync, typename Hook>
+__device__ __forceinline__ void invert_unit(float *__restrict__ U, int lane, Sync sync, Hook after_diag) {
+    {
+        float *D = U + blk(W, W);
+        const int c0 = lane & 15;
+        float xv[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) xv[r] = (r == c0) ? 1.f : 0.f;
+#pragma unroll
+        for (int k = 0; k < 15; ++k) {
+            const float ak = xv[k];
+#pragma unroll
+            for (int r = k + 1; r < 16; ++r) xv[r] = fmaf(-D[el(r, k)], ak, xv[r]);
+        }
+        __syncwarp();
+        if (lane < 16) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) D[el(r, c0)] = xv[r];
+        }
+        __syncwarp();
+    }
+    // M_Wk = N_WW L_Wk over L_Wk (k < W): the warp's own blocks
+    if (W >= 1) {
+        Acc16 m[W > 0 ? W : 1];
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            zero16(m[k]);
+            warp_gemm16(U + blk(W, W), U + blk(W, k), m[k], lane);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < W; ++k) warp_store16(U + blk(W, k), m[k], lane, 1.f);
+    }
+    sync();  // every N_kk is in place
+    after_diag();
+    // level 1: N_{W,W-1} = -M_{W,W-1} N_{W-1,W-1}, and the partial sums that need
+    // only the diagonal: P20 = M_20 N_00 (warp 2), P31 = M_31 N_11, P30 = M_30 N_00 (3)
+    Acc16 pa, pb;
+    zero16(pa);
+    zero16(pb);
+    if (W >= 1) {
+        constexpr int Wm = W > 0 ? W - 1 : 0;
+        Acc16 n1;
+        zero16(n1);
+        warp_gemm16(U + blk(W, Wm), U + blk(Wm, Wm), n1, lane);
+        if (W == 2) warp_gemm16(U + blk(2, 0), U + blk(0, 0), pa, lane);
+        if (W == 3) {
+            warp_gemm16(U + blk(3, 1), U + blk(1, 1), pa, lane);
+            warp_gemm16(U + blk(3, 0), U + blk(0, 0), pb, lane);
+        }
+        warp_store16(U + nblk(W > 0 ? W : 1, Wm), n1, lane, -1.f);
+    }
+    sync();  // N_10, N_21, N_32 are in place
+    // level 2: N_20 = -(P20 + M_21 N_10) (warp 2); N_31 = -(P31 + M_32 N_21) and
+    // P30 += M_31 N_10 (warp 3)
+    if (W == 2) {
+        warp_gemm16(U + blk(2, 1), U + nblk(1, 0), pa, lane);
+        warp_store16(U + nblk(2, 0), pa, lane, -1.f);
+    } else if (W == 3) {
+        warp_gemm16(U + blk(3, 2), U + nblk(2, 1), pa, lane);
+        warp_gemm16(U + blk(3, 1), U + nblk(1, 0), pb, lane);
+        warp_store16(U + nblk(3, 1), pa, lane, -1.f);
+    }
+    sync();  // N_20 is in place
+    // level 3: N_30 = -(P30 + M_32 N_20) (warp 3)
+    if (W == 3) {
+        warp_gemm16(U + blk(3, 2), U + nblk(2, 0), pb, lane);
+        warp_store16(U + nblk(3, 0), pb, lane, -1.f);
+    }
+    __syncwarp();
+}
+
 struct SolveParams {
     const float *log_alpha, *beta;
     const int4 *plan;  // per chunk: sequence, first token, tokens, index within the sequence
@@ -445,83 +526,17 @@ struct GroupSolver {
                 fetch_gates(xn, pl_next, raw);
             }
 
-            // ---- (I + L)^{-1}: diagonal block W by forward substitution, lane l on column
-            // l % 16 (the upper half of the warp repeats the lower and stores nothing)
-            {
-                float *D = U + blk(W, W);
-                const int c0 = lane & 15;
-                float xv[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) xv[r] = (r == c0) ? 1.f : 0.f;
-#pragma unroll
-                for (int k = 0; k < 15; ++k) {
-                    const float ak = xv[k];
-#pragma unroll
-                    for (int r = k + 1; r < 16; ++r) xv[r] = fmaf(-D[el(r, k)], ak, xv[r]);
+            // ---- (I + L)^{-1} in the blocks
+            invert_unit<W>(U, lane, [&] { gsync(); }, [&] {
+                // the next unit's Gram, if its tiles have landed (else at the end of this
+                // unit); the Gram's TMEM columns were read before the load was issued
+                if (leader && has_next && mbar_test_wait(bar_ld(), ld_phase)) {
+                    ++landed;
+                    issue_gram();
+                    ++grams;
+                    gram_next = true;
                 }
-                __syncwarp();
-                if (lane < 16) {
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) D[el(r, c0)] = xv[r];
-                }
-                __syncwarp();
-            }
-            // M_Wk = N_WW L_Wk over L_Wk (k < W): the warp's own blocks
-            if (W >= 1) {
-                Acc16 m[W > 0 ? W : 1];
-#pragma unroll
-                for (int k = 0; k < W; ++k) {
-                    zero16(m[k]);
-                    warp_gemm16(U + blk(W, W), U + blk(W, k), m[k], lane);
-                }
-                __syncwarp();
-#pragma unroll
-                for (int k = 0; k < W; ++k) warp_store16(U + blk(W, k), m[k], lane, 1.f);
-            }
-            gsync();  // every N_kk is in place
-            // the next unit's Gram, if its tiles have landed (else at the end of this unit);
-            // the Gram's TMEM columns were read before the load was issued
-            if (leader && has_next && mbar_test_wait(bar_ld(), ld_phase)) {
-                ++landed;
-                issue_gram();
-                ++grams;
-                gram_next = true;
-            }
-            // level 1: N_{W,W-1} = -M_{W,W-1} N_{W-1,W-1}, and the partial sums that need
-            // only the diagonal: P20 = M_20 N_00 (warp 2), P31 = M_31 N_11, P30 = M_30 N_00 (3)
-            Acc16 pa, pb;
-            zero16(pa);
-            zero16(pb);
-            if (W >= 1) {
-                constexpr int Wm = W > 0 ? W - 1 : 0;
-                Acc16 n1;
-                zero16(n1);
-                warp_gemm16(U + blk(W, Wm), U + blk(Wm, Wm), n1, lane);
-                if (W == 2) warp_gemm16(U + blk(2, 0), U + blk(0, 0), pa, lane);
-                if (W == 3) {
-                    warp_gemm16(U + blk(3, 1), U + blk(1, 1), pa, lane);
-                    warp_gemm16(U + blk(3, 0), U + blk(0, 0), pb, lane);
-                }
-                warp_store16(U + nblk(W > 0 ? W : 1, Wm), n1, lane, -1.f);
-            }
-            gsync();  // N_10, N_21, N_32 are in place
-            // level 2: N_20 = -(P20 + M_21 N_10) (warp 2); N_31 = -(P31 + M_32 N_21) and
-            // P30 += M_31 N_10 (warp 3)
-            if (W == 2) {
-                warp_gemm16(U + blk(2, 1), U + nblk(1, 0), pa, lane);
-                warp_store16(U + nblk(2, 0), pa, lane, -1.f);
-            } else if (W == 3) {
-                warp_gemm16(U + blk(3, 2), U + nblk(2, 1), pa, lane);
-                warp_gemm16(U + blk(3, 1), U + nblk(1, 0), pb, lane);
-                warp_store16(U + nblk(3, 1), pa, lane, -1.f);
-            }
-            gsync();  // N_20 is in place
-            // level 3: N_30 = -(P30 + M_32 N_20) (warp 3)
-            if (W == 3) {
-                warp_gemm16(U + blk(3, 2), U + nblk(2, 0), pb, lane);
-                warp_store16(U + nblk(3, 0), pb, lane, -1.f);
-            }
-            __syncwarp();
+            });
 
             // ---- T' block row W: diag(kd) N diag(beta), bf16 pairs to the workspace (the
             // blocks right of the diagonal, and the diagonal block's upper part, are zero)

@@ -118,6 +118,8 @@ def _load():
     lib.gdr_decode_step_ex.restype = c_int
     lib.gdr_chunk_fwd_path.argtypes = [c_int, c_int, c_int]
     lib.gdr_chunk_fwd_path.restype = c_int
+    lib.gdr_chunk_fwd_path_ex.argtypes = [c_int, c_int, c_int, vp]
+    lib.gdr_chunk_fwd_path_ex.restype = c_int
     lib.gdr_chunk_fwd_kernel_launches.argtypes = [i64, i64, c_int, c_int, c_int, c_int, c_int,
                                                   c_int]
     lib.gdr_chunk_fwd_kernel_launches.restype = c_int
@@ -164,14 +166,15 @@ def _need(t, name, dtype=None, device=None):
 
 
 def chunk_fwd_workspace_size(num_seqs, total_tokens, H, dk, dv, chunk=64, dtype=torch.bfloat16,
-                             decay="head"):
+                             decay="head", prologue=False):
     """Workspace bytes gdr_chunk_fwd needs (0 if the sizes are unsupported); decay
-    "channel" (per-channel rates, the exact path) through gdr_chunk_fwd_workspace_size_ex."""
+    "channel" (per-channel rates, whose path also depends on the prologue) through
+    gdr_chunk_fwd_workspace_size_ex."""
     lib = _load()
     if decay == "head":
         return int(lib.gdr_chunk_fwd_workspace_size(int(num_seqs), int(total_tokens), int(H),
                                                     int(dk), int(dv), int(chunk), _DTYPES[dtype]))
-    opt = GdrOptions(0, 0.0, None, None, 0, DECAYS[decay], None)
+    opt = GdrOptions(0, 0.0, None, None, int(bool(prologue)), DECAYS[decay], None)
     return int(lib.gdr_chunk_fwd_workspace_size_ex(int(num_seqs), int(total_tokens), int(H),
                                                    int(dk), int(dv), int(chunk), _DTYPES[dtype],
                                                    ctypes.addressof(opt)))
@@ -184,7 +187,8 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
 
     q, k [T, H, dk]; v [T, H, dv] (fp32 or bf16); beta [T, H] fp32; log_alpha [T, H]
     fp32 (one rate per head), or [T, H, dk] (one rate per key channel, gdr_options.decay
-    GDR_DECAY_CHANNEL: the exact fp32 path);
+    GDR_DECAY_CHANNEL: tensor cores for bf16 with dk = dv = 128 and no prologue, else
+    the exact fp32 path);
     S0 [num_seqs, H, dk, dv] fp32 or None; cu_seqlens [num_seqs+1] int32 or None
     (then `num_seqs` equal sequences, default 1). Optional preallocated o,
     S_final and workspace (uint8) tensors are used as given. rule: "delta" (the gated
@@ -222,7 +226,7 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
     _need(S_final, "S_final", torch.float32, dev)
     _check_out_step(out_gate, out_norm_weight, o, dv)
     _check_prologue(prologue, gate_A, H, dev)
-    ws_bytes = chunk_fwd_workspace_size(n, T, H, dk, dv, chunk, dt, decay)
+    ws_bytes = chunk_fwd_workspace_size(n, T, H, dk, dv, chunk, dt, decay, prologue)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", device=dev)
@@ -282,23 +286,27 @@ def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None, rule="delta", 
 _PATHS = {
     0: dict(main_kernel="exact_chain_kernel", compute_dtype="f32"),
     1: dict(main_kernel="tc_chain_kernel", compute_dtype="bf16"),
+    2: dict(main_kernel="tc_chain_channel_kernel", compute_dtype="bf16"),
 }
+PATH_CHANNEL_TENSOR = 2  # GDR_PATH_CHANNEL_TENSOR
 
 
-def chunk_fwd_path(dk, dv, dtype, decay="head"):
-    """0 (exact fp32 path) or 1 (tensor cores); per-channel rates take the exact path."""
-    st = _load().gdr_chunk_fwd_path(int(dk), int(dv), _DTYPES[dtype])
+def chunk_fwd_path(dk, dv, dtype, decay="head", prologue=False):
+    """0 (exact fp32 path), 1 (tensor cores, one rate per head) or 2 (tensor cores,
+    one rate per key channel), from gdr_chunk_fwd_path_ex."""
+    opt = GdrOptions(0, 0.0, None, None, int(bool(prologue)), DECAYS[decay], None)
+    st = _load().gdr_chunk_fwd_path_ex(int(dk), int(dv), _DTYPES[dtype], ctypes.addressof(opt))
     if st < 0:
-        raise GdrError(st, "gdr_chunk_fwd_path")
-    return 0 if decay == "channel" else st
+        raise GdrError(st, "gdr_chunk_fwd_path_ex")
+    return st
 
 
 def chunk_fwd_kernel_launches(num_seqs, total_tokens, H, dk, dv, dtype, varlen=False,
                               decay="head"):
     """Kernels one gdr_chunk_fwd call launches for these sizes on the current device
     (varlen: the call passes cu_seqlens)."""
-    if decay == "channel":  # the exact path: plan, per-chunk prep, chain
-        chunk_fwd_path(dk, dv, dtype)
+    if decay == "channel":  # either per-channel path: plan, per-chunk operands, chain
+        chunk_fwd_path(dk, dv, dtype, decay)
         return 3 if total_tokens > 0 else 1
     st = _load().gdr_chunk_fwd_kernel_launches(int(num_seqs), int(total_tokens), int(H), int(dk),
                                                int(dv), 64, _DTYPES[dtype], int(bool(varlen)))
@@ -337,7 +345,7 @@ def chunk_fwd_schedule_model(num_seqs, total_tokens, H, dk, dv, dtype, sms, varl
 def chunk_fwd_main_kernel(dk, dv, dtype, schedule=None, decay="head"):
     """Name of the kernel that dominates a gdr_chunk_fwd call for these sizes. The fused
     schedule (0) of the tensor-core path runs the solve and the chains in one kernel; the
-    exact path (and per-channel rates, which take it) is dominated by its chain."""
+    other paths are dominated by their chain."""
     path = chunk_fwd_path(dk, dv, dtype, decay)
     if path == 1 and schedule == 0:
         return "tc_fused_kernel"

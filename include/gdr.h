@@ -237,9 +237,12 @@ enum { GDR_RULE_DELTA = 0, GDR_RULE_ADDITIVE = 1 };
  *                    Softmax to the Delta Rule", section 10 "Where this goes next":
  *                    Kimi Delta Attention gives each feature channel its own rate).
  *                    With GDR_PROLOGUE_LAYER the pre-activation a has that shape too.
- *                    Prefill with per-channel rates always takes the exact fp32 path
- *                    (GDR_PATH_EXACT), whose workspace gdr_chunk_fwd_workspace_size_ex
- *                    sizes. Other values: GDR_ERR_INVALID_ARG.
+ *                    Prefill with per-channel rates takes the per-channel tensor-core
+ *                    path (GDR_PATH_CHANNEL_TENSOR) for bf16 with d_k = d_v = 128 and
+ *                    no prologue, else the exact fp32 path (GDR_PATH_EXACT);
+ *                    gdr_chunk_fwd_workspace_size_ex sizes the workspace of either,
+ *                    and gdr_chunk_fwd_path_ex says which one a call takes. Other
+ *                    values: GDR_ERR_INVALID_ARG.
  */
 enum { GDR_PROLOGUE_NONE = 0, GDR_PROLOGUE_LAYER = 1 };
 enum { GDR_DECAY_HEAD = 0, GDR_DECAY_CHANNEL = 1 };
@@ -337,8 +340,20 @@ int gdr_noalloc_read_device_status(int *status, gdr_stream_t stream);
  * chunk-parallel solve kernel and a per-sequence chain kernel).
  * Returns a negative status for unsupported sizes.
  */
-enum { GDR_PATH_EXACT = 0, GDR_PATH_TENSOR = 1 };
+enum { GDR_PATH_EXACT = 0, GDR_PATH_TENSOR = 1, GDR_PATH_CHANNEL_TENSOR = 2 };
 int gdr_chunk_fwd_path(int d_k, int d_v, int dtype);
+
+/*
+ * The kernel path of a gdr_chunk_fwd_ex call with these sizes and options (null:
+ * the defaults, the same answer as gdr_chunk_fwd_path). With per-channel rates
+ * (decay = GDR_DECAY_CHANNEL) it is GDR_PATH_CHANNEL_TENSOR (bf16 tensor cores:
+ * a planning kernel, a chunk-parallel kernel that builds every chunk's operands
+ * with per-channel decay folded in, and a per-sequence chain kernel) for bf16
+ * with d_k = d_v = 128 and no prologue, else GDR_PATH_EXACT. Host-only, no
+ * CUDA call. Returns a negative status for unsupported sizes or options, as
+ * gdr_chunk_fwd_ex would.
+ */
+int gdr_chunk_fwd_path_ex(int d_k, int d_v, int dtype, const gdr_options *options);
 
 /*
  * Number of kernels one uncaptured gdr_chunk_fwd call with these sizes

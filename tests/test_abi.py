@@ -161,22 +161,51 @@ def test_options_validated_on_the_host(lib):
                                   ctypes.byref(ok), None) == 0
 
 
-def test_per_channel_workspace_takes_the_exact_layout(lib):
-    # per-channel rates run on the exact path: the _ex size query says so, and the plain
-    # query (head rates) is unchanged; bad options size nothing
+def test_per_channel_workspace_follows_the_path(lib):
+    # per-channel rates: bf16 with d_k = d_v = 128 takes the per-channel tensor-core path,
+    # whose workspace holds every unit's operands; other sizes (and the prologue) take the
+    # exact path, whose layout adds one fp32 [C][d_k] block of cumulative log decay per
+    # unit. The plain query (head rates) is unchanged; bad options size nothing.
     from gated_delta_rule_03_gb300.ops import GdrOptions
     head = lib.gdr_chunk_fwd_workspace_size(4, 4 * 4096, 16, 128, 128, 64, 1)
     pc = GdrOptions(0)
     pc.decay = 1
     chan = lib.gdr_chunk_fwd_workspace_size_ex(4, 4 * 4096, 16, 128, 128, 64, 1, ctypes.byref(pc))
-    exact_f32 = lib.gdr_chunk_fwd_workspace_size(4, 4 * 4096, 16, 128, 128, 64, 0)
     assert lib.gdr_chunk_fwd_workspace_size_ex(4, 4 * 4096, 16, 128, 128, 64, 1, None) == head
-    # the exact layout plus one fp32 [C][d_k] block of cumulative log decay per unit
     units = (4 * 4096 // 64 + 4) * 16
-    assert chan >= exact_f32 + units * 64 * 128 * 4
+    # per unit: A^T and T' (2 x 64 x 64 bf16), 384 decay factors, [e^g Q | -W] (64 x 256
+    # bf16), decayed K (64 x 128 bf16), U~^T (128 x 64 bf16)
+    per_unit = 2 * 64 * 64 * 2 + 384 * 4 + 64 * 256 * 2 + 64 * 128 * 2 + 128 * 64 * 2
+    assert units * per_unit <= chan <= units * per_unit + (1 << 20)
+    pc.prologue = 1
+    exact_pro = lib.gdr_chunk_fwd_workspace_size_ex(4, 4 * 4096, 16, 128, 128, 64, 1,
+                                                    ctypes.byref(pc))
+    exact_f32 = lib.gdr_chunk_fwd_workspace_size(4, 4 * 4096, 16, 128, 128, 64, 0)
+    assert exact_pro >= exact_f32 + units * 64 * 128 * 4
     bad = GdrOptions(0)
     bad.decay = 7
     assert lib.gdr_chunk_fwd_workspace_size_ex(1, 128, 2, 64, 64, 64, 0, ctypes.byref(bad)) == 0
+
+
+def test_path_query_with_options(lib):
+    from gated_delta_rule_03_gb300.ops import GdrOptions
+    fn = lib.gdr_chunk_fwd_path_ex
+    fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    EXACT, TENSOR, CHANNEL = 0, 1, 2
+    opt = lambda decay=0, prologue=0: ctypes.byref(GdrOptions(0, 0.0, None, None, prologue,
+                                                              decay, None))
+    for dk, dv, dt in [(128, 128, 1), (128, 256, 1), (64, 64, 1), (128, 128, 0)]:
+        assert fn(dk, dv, dt, None) == lib.gdr_chunk_fwd_path(dk, dv, dt)
+        assert fn(dk, dv, dt, opt()) == lib.gdr_chunk_fwd_path(dk, dv, dt)
+    assert fn(128, 128, 1, None) == TENSOR
+    assert fn(128, 128, 1, opt(decay=1)) == CHANNEL
+    assert fn(128, 128, 1, opt(decay=1, prologue=1)) == EXACT
+    assert fn(128, 256, 1, opt(decay=1)) == EXACT
+    assert fn(128, 128, 0, opt(decay=1)) == EXACT
+    assert fn(64, 64, 1, opt(decay=1)) == EXACT
+    assert fn(128, 128, 1, opt(decay=7)) == -1  # GDR_ERR_INVALID_ARG
+    assert fn(100, 128, 1, opt(decay=1)) < 0
 
 
 @pytest.mark.parametrize("env", ["GDR_PREFILL_PHASES", "GDR_PREFILL_SEGMENTS"])

@@ -3,10 +3,12 @@
 One forget rate per token, head and key channel: row c of the state decays by
 alpha_t[c] ("Attention as Matrix Algebra: From Softmax to the Delta Rule", section 10:
 Kimi Delta Attention gives each feature channel its own rate). The oracle takes
-log_alpha [T, H, d_k] and runs the same token loop. Prefill runs on the exact fp32 path
-(per-channel chunk form: the decay inside the Gram products); decode streams the state
-once with the rates applied per row. Tolerances as for every path: max |gpu - oracle| /
-max |oracle| <= 1e-4 for fp32 inputs and <= 2e-2 for bf16 inputs.
+log_alpha [T, H, d_k] and runs the same token loop. Prefill with bf16 inputs and
+d_k = d_v = 128 runs on the per-channel tensor-core path (a chunk-parallel kernel folds
+each channel's decay into the operands, the chain applies it per state row); other
+sizes run on the exact fp32 path (the decay inside the Gram products). Decode streams the
+state once with the rates applied per row. Tolerances as for every path: max |gpu -
+oracle| / max |oracle| <= 1e-4 for fp32 inputs and <= 2e-2 for bf16 inputs.
 """
 import numpy as np
 import pytest
@@ -138,6 +140,79 @@ def test_prologue_and_output_step(dv):
                                   cu_seqlens=cu.numpy().astype(np.int64))
     o_ref = oracle.out_norm_gate(o_ref, f64(z), f64(w), eps=1e-5)
     assert rel_err(f64(o), o_ref) <= TOL["bf16"] and rel_err(f64(S), S_ref) <= TOL["bf16"]
+
+
+# ------------------------------------------------- prefill on the per-channel tensor-core path
+
+def test_bf16_128_takes_the_channel_tensor_path():
+    assert ops.chunk_fwd_path(128, 128, torch.bfloat16, "channel") == ops.PATH_CHANNEL_TENSOR
+    assert ops.chunk_fwd_main_kernel(128, 128, torch.bfloat16, decay="channel") == \
+        "tc_chain_channel_kernel"
+    assert ops.chunk_fwd_compute_dtype(128, 128, torch.bfloat16, "channel") == "bf16"
+
+
+@pytest.mark.parametrize("lens", [[64], [63], [1], [65, 64], [2048], [130, 1, 64, 700, 0, 65]])
+def test_tensor_path_lengths(lens):
+    # one chunk, a short one, a single token, two chunks, a long chain, and a packed mix
+    # with an empty sequence: ragged tails fall inside the chunk-parallel tiles
+    inp = inputs.prefill_inputs(lens, H=3, dk=128, dv=128, dtype="bf16", seed=650 + len(lens),
+                                s0_std=0.5, gate="default", decay="channel", packed=True)
+    check(inp, per_sequence=True)
+
+
+def test_tensor_path_mixes_factored_and_exact_chunks():
+    # channels that lose e^-160 over half a chunk cannot be split into two bounded
+    # factors around the chunk's middle token; those chunks build their Gram products
+    # one element at a time, the others from factored operands, in the same call
+    rng = np.random.default_rng(651)
+    inp = inputs.prefill_inputs([300, 200], H=2, dk=128, dv=128, dtype="bf16", seed=651,
+                                s0_std=0.5, gate="slow", decay="channel")
+    la = inp.log_alpha.clone()
+    steep = rng.choice(128, 5, replace=False)
+    la[64:128, 0, steep] = -5.0  # chunk 1 of sequence 0, head 0
+    la[300 + 130:300 + 200, 1, steep[:2]] = -6.0  # the tail of sequence 1, head 1
+    la[200:230, :, :] = -0.02  # slow everywhere in between
+    inp.log_alpha = la
+    check(inp, per_sequence=True)
+
+
+def test_tensor_path_output_step():
+    inp = inputs.prefill_inputs([150, 64, 33], H=2, dk=128, dv=128, dtype="bf16", seed=652,
+                                s0_std=0.3, gate="default", decay="channel")
+    rng = np.random.default_rng(652)
+    z = torch.from_numpy((2.0 * rng.standard_normal((inp.total_tokens, 2, 128))).astype(
+        np.float32)).to(torch.bfloat16)
+    w = torch.from_numpy(rng.uniform(0.5, 1.5, 128).astype(np.float32))
+    d = lambda t: None if t is None else t.cuda()
+    o, S = chunk_fwd(d(inp.q), d(inp.k), d(inp.v), d(inp.log_alpha), d(inp.beta), S0=d(inp.S0),
+                     cu_seqlens=d(inp.cu_seqlens), out_gate=d(z), out_norm_weight=d(w),
+                     out_norm_eps=1e-5)
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle_prefill(inp)
+    o_ref = oracle.out_norm_gate(o_ref, f64(z), f64(w), eps=1e-5)
+    assert rel_err(f64(o), o_ref) <= TOL["bf16"] and rel_err(f64(S), S_ref) <= TOL["bf16"]
+
+
+def test_tensor_path_equal_rates_match_the_head_rate_path():
+    # the same rate in every channel: the per-channel and the one-rate-per-head tensor-core
+    # paths compute the same recurrence with different operand scalings
+    inp = inputs.prefill_inputs([300, 77], H=2, dk=128, dv=128, dtype="bf16", seed=653,
+                                s0_std=0.3, gate="default")
+    d = lambda t: None if t is None else t.cuda()
+    o_h, S_h = chunk_fwd(d(inp.q), d(inp.k), d(inp.v), d(inp.log_alpha), d(inp.beta),
+                         S0=d(inp.S0), cu_seqlens=d(inp.cu_seqlens))
+    la_c = inp.log_alpha[:, :, None].expand(-1, -1, 128).contiguous()
+    o_c, S_c = chunk_fwd(d(inp.q), d(inp.k), d(inp.v), d(la_c), d(inp.beta), S0=d(inp.S0),
+                         cu_seqlens=d(inp.cu_seqlens))
+    torch.cuda.synchronize()
+    assert rel_err(f64(o_c), f64(o_h)) <= TOL["bf16"] and rel_err(f64(S_c), f64(S_h)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("lens", [[0, 70, 0, 5], [0, 0]])
+def test_tensor_path_empty_sequences_keep_their_state(lens):
+    inp = inputs.prefill_inputs(lens, H=2, dk=128, dv=128, dtype="bf16", seed=654,
+                                s0_std=0.5, gate="slow", decay="channel", packed=True)
+    check(inp, per_sequence=True)
 
 
 def test_log_alpha_shape_is_checked():
