@@ -46,7 +46,9 @@ int launch_prefill_channel_tc(const PrefillArgs &a, const WsLayout &L) {
 
     // every unit's operands, a programmatic dependent of the planning kernel
     if (cudaFuncSetAttribute(channel::channel_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)channel::SMEM_BYTES) != cudaSuccess)
+                             (int)channel::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(channel::channel_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return GDR_ERR_CUDA;
     channel::ChannelParams cp = {};
     cp.log_alpha = a.log_alpha;

@@ -24,8 +24,9 @@
 // W = T K' with column c scaled by exp(g_r[c]) on the way out (exp(0) without the
 // factored Gram).
 //
-// One CTA of four warps per unit; TMEM lane quarter w belongs to warp w. Outputs (the
-// chain kernel loads them by TMA, 128-byte swizzled 64 x 64 boxes):
+// One CTA of four warps per unit, four CTAs per SM (52 KB of shared memory and 128 TMEM
+// columns each); TMEM lane quarter w belongs to warp w. Outputs (the chain kernel loads
+// them by TMA, 128-byte swizzled 64 x 64 boxes):
 //   QW [units * 64][256] bf16: e^g . Q in columns 0..127, -W in columns 128..255;
 //   KT [units * 64][128] bf16: e^{g_C - g} . K;
 //   UT [units * 128][64] bf16: Utilde^T (row j: value column j over the chunk's tokens);
@@ -55,23 +56,28 @@ constexpr int kThreads = 128;
 constexpr int kRefToken = 31;
 constexpr float kFactorLogBound = 80.f;
 
-// Shared memory map (bytes from a 1024-aligned base).
+// Shared memory map (bytes from a 1024-aligned base). Regions are reused as the unit
+// moves on: V is loaded over the query rows once Q is spent (after the Gram MMA, or after
+// the element-wise pass without the factored Gram); the blocks of the inverse go over
+// K'' once the Gram has completed, and T' over the blocks once every warp holds its
+// block row in registers.
 constexpr uint32_t P_KQ = 0;       // per d_k half b at 16384 b: 64 key rows, then 64 query rows
+constexpr uint32_t P_V = 8192;     // V's 64-column halves at P_V and P_V + 16384
 constexpr uint32_t P_KC = 32768;   // the Gram's B operand K'': two 64-column halves of 8 KB
-constexpr uint32_t P_V = 49152;    // V: two 64-column halves of 8 KB
-constexpr uint32_t P_G = P_KC;     // (unfactored Gram) g, fp32 [C][DK], over P_KC and P_V
-constexpr uint32_t P_BLK = 65536;  // the unit's 16 x 16 blocks (the solve's layout)
-constexpr uint32_t P_TP = P_BLK + (solve::UNIT_FLOATS * 4 + 1023) / 1024 * 1024;  // T' bf16 [t][i]
-constexpr uint32_t P_MISC = P_TP + 8192;  // floats: beta[64], g_C[128], g_r[128], half sums[128],
-                                          // the "V reload gave up" flag
+constexpr uint32_t P_BLK = P_KC;   // the unit's 16 x 16 blocks (the solve's layout)
+constexpr uint32_t P_TP = P_KC;    // T' bf16 [t][i], 128-byte swizzled
+constexpr uint32_t P_MISC = P_KC + (solve::UNIT_FLOATS * 4 + 1023) / 1024 * 1024;
+                                   // floats: beta[64], g_C[128], g_r[128], half sums[128],
+                                   // the "V load gave up" flag
 constexpr int M_BETA = 0, M_GC = 64, M_GREF = 192, M_HSUM = 320, M_FLAG = 448;
 constexpr uint32_t P_BARS = P_MISC + 456 * 4;  // load, Gram, products, V reload, drain
 constexpr uint32_t P_TMEM = P_BARS + 40;
 constexpr uint32_t P_USED = P_TMEM + 16;
 constexpr uint32_t SMEM_BYTES = P_USED + 1024;
-static_assert(P_TP % 1024 == 0 && P_BARS % 8 == 0 && SMEM_BYTES <= 232448 / 2, "shared memory");
-// TMEM columns: the Gram, W^T, Utilde^T (64 each)
-constexpr uint32_t TM_GRAM = 0, TM_W = 64, TM_UT = 128, TM_COLS = 256;
+static_assert(P_TP % 1024 == 0 && P_BARS % 8 == 0 && SMEM_BYTES + 1024 <= 233472 / 4,
+              "shared memory: four CTAs per SM");
+// TMEM columns: the Gram, then W^T in the same columns once the Gram is read; Utilde^T
+constexpr uint32_t TM_GRAM = 0, TM_W = 0, TM_UT = 64, TM_COLS = 128;
 
 struct ChannelParams {
     const float *log_alpha;  // [tokens, H, DK]
@@ -90,27 +96,37 @@ __device__ __forceinline__ float sw_elem(const unsigned char *block, int row, in
 }
 
 // T' = (I + L)^{-1} diag(beta), block row W of warp W, as bf16 into the swizzled [t][i]
-// tile `tp` (the B operand of the products; zeros right of the diagonal).
-template <int W>
+// tile `tp` (the B operand of the products; zeros right of the diagonal). The tile lies
+// over the blocks: every warp reads its row into registers, then `sync` (the whole CTA),
+// then the stores.
+template <int W, typename Sync>
 __device__ __forceinline__ void store_t_prime(const float *__restrict__ U, const float *__restrict__ beta,
-                                              unsigned char *tp, int lane) {
+                                              unsigned char *tp, int lane, Sync sync) {
     const int gq = lane >> 2, q = lane & 3;
+    float2 lo[4][2], hi[4][2];
+#pragma unroll
+    for (int bi = 0; bi < 4; ++bi) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            lo[bi][nt] = hi[bi][nt] = make_float2(0.f, 0.f);
+            if (bi <= W) {
+                const float *B = U + (bi == W ? blk(W, W) : nblk(W > bi ? W : 1, W > bi ? bi : 0));
+                lo[bi][nt] = *reinterpret_cast<const float2 *>(B + el(gq, 8 * nt + 2 * q));
+                hi[bi][nt] = *reinterpret_cast<const float2 *>(B + el(gq + 8, 8 * nt + 2 * q));
+            }
+        }
+    }
+    sync();
 #pragma unroll
     for (int bi = 0; bi < 4; ++bi) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const int i0 = 16 * bi + 8 * nt + 2 * q;
-            float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
-            if (bi <= W) {
-                const float *B = U + (bi == W ? blk(W, W) : nblk(W > bi ? W : 1, W > bi ? bi : 0));
-                lo = *reinterpret_cast<const float2 *>(B + el(gq, 8 * nt + 2 * q));
-                hi = *reinterpret_cast<const float2 *>(B + el(gq + 8, 8 * nt + 2 * q));
-            }
             const float b0 = beta[i0], b1 = beta[i0 + 1];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int t = 16 * W + gq + 8 * hh;
-                const float2 v = hh ? hi : lo;
+                const float2 v = hh ? hi[bi][nt] : lo[bi][nt];
                 const float x0 = i0 <= t ? v.x * b0 : 0.f;
                 const float x1 = i0 + 1 <= t ? v.y * b1 : 0.f;
                 *reinterpret_cast<uint32_t *>(tp + sw128_offset(t, i0)) = pack_bf16x2(x0, x1);
@@ -120,7 +136,7 @@ __device__ __forceinline__ void store_t_prime(const float *__restrict__ U, const
 }
 
 // The unit (chunk blockIdx.x, head blockIdx.y). map_q, map_k, map_v: the inputs.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const ChannelParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -158,14 +174,21 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         const int t0 = pl.y, len = pl.z;
         const size_t u = (size_t)c * p.H + h;  // chunk-major, head-minor
         if (tid == 0) {
-            mbar_arrive_expect_tx(bar(0), 6 * 8192);
+            mbar_arrive_expect_tx(bar(0), 4 * 8192);
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
                 tma_load_3d(sb + P_KQ + 16384 * b, &map_k, bar(0), 64 * b, h, t0);
                 tma_load_3d(sb + P_KQ + 16384 * b + 8192, &map_q, bar(0), 64 * b, h, t0);
-                tma_load_3d(sb + P_V + 8192 * b, &map_v, bar(0), 64 * b, h, t0);
             }
         }
+        // V over the query rows, once they are spent (thread 0 issues it and drains it)
+        bool v_issued = false;
+        auto load_v = [&] {
+            mbar_arrive_expect_tx(bar(3), 2 * 8192);
+            tma_load_3d(sb + P_V, &map_v, bar(3), 0, h, t0);
+            tma_load_3d(sb + P_V + 16384, &map_v, bar(3), 64, h, t0);
+            v_issued = true;
+        };
         if (tid < C) misc[M_BETA + tid] = tid < len ? p.beta[(size_t)(t0 + tid) * p.H + h] : 0.f;
         // g by columns: thread (cp, th) owns channels 2cp, 2cp + 1 over tokens 32th .. 32th + 31
         const int cp = tid & 63, th = tid >> 6;
@@ -214,9 +237,10 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         float *U = reinterpret_cast<float *>(sm + P_BLK);
         __nv_bfloat16 *arow = p.AT + (u * 2 + 1) * C * C;
         if (!fail && !factored) {
-            // ---- the unfactored Gram on the CUDA cores: g to shared memory (over K'' and
-            // V; V is loaded again below), every entry as its own sum
-            float *gs = reinterpret_cast<float *>(sm + P_G);
+            // ---- the unfactored Gram on the CUDA cores, every entry as its own sum. g goes
+            // to the unit's slot of QW in the workspace (fp32 [C][DK], 32 KB), which the
+            // element-wise pass below fills only after this loop has read it.
+            float *gs = reinterpret_cast<float *>(p.QW + (u * C) * 256);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
                 *reinterpret_cast<float2 *>(gs + (32 * th + j) * DK + 2 * cp) = make_float2(g[j][0], g[j][1]);
@@ -237,13 +261,7 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 }
                 arow[i * C + t] = __float2bfloat16_rn(qk);
             }
-            fence_async_smem();  // the g table's writes come before the TMA overwrites it
-            __syncthreads();
-            if (tid == 0) {  // V again (the g table used its space)
-                mbar_arrive_expect_tx(bar(3), 2 * 8192);
-                tma_load_3d(sb + P_V, &map_v, bar(3), 0, h, t0);
-                tma_load_3d(sb + P_V + 8192, &map_v, bar(3), 64, h, t0);
-            }
+            __syncthreads();  // every read of the g table before the QW stores below
         }
         if (!fail) {
             // ---- element-wise: the chain's e^g . Q and e^{g_C - g} . K to the workspace,
@@ -254,7 +272,7 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             unsigned char *kh = sm + P_KQ + 16384 * b, *qh = kh + 8192, *kc = sm + P_KC + 8192 * b;
             __nv_bfloat16 *qw = p.QW + (u * C) * 256 + 2 * cp;
             __nv_bfloat16 *kt = p.KT + (u * C) * DK + 2 * cp;
-#pragma unroll 4
+#pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int t = 32 * th + j;
                 const uint32_t off = (uint32_t)(t * 128 + ((((cc >> 2) ^ t) & 7) << 4) + (cc & 3) * 4);
@@ -274,6 +292,7 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             }
             fence_async_smem();
             __syncthreads();
+            if (!factored && tid == 0) load_v();  // the query rows are spent
             if (factored) {
                 if (tid == 0) {  // [K'; Q'] K''^T: row t < 64 of D is L_t. / beta_t, row 64 + t is A_t.
                     tc_fence_after();
@@ -287,6 +306,11 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     mma_commit(bar(1));
                 }
                 if (!mbar_wait(bar(1), 0)) fail = true;
+                // a Gram that did not complete is neither read nor written over
+                fail = __syncthreads_or(fail) != 0;
+            }
+            if (factored && !fail) {
+                if (tid == 0) load_v();  // the query rows are spent
                 tc_fence_after();
                 // the Gram's rows, warp w on TMEM lanes 32w .. 32w + 31, 16 columns at a time
                 const uint32_t lanes = tmem + TM_GRAM + ((uint32_t)(32 * warp) << 16);
@@ -328,6 +352,7 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                         }
                     }
                 }
+                tc_fence_before();  // the reads come before W^T's MMA into the same columns
             }
             fail = __syncthreads_or(fail) != 0;  // (also: the L blocks are complete)
         }
@@ -338,16 +363,16 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             const float *beta_s = misc + M_BETA;
             unsigned char *tp = sm + P_TP;
             switch (warp) {
-                case 0: invert_unit<0>(U, lane, sync4, none); store_t_prime<0>(U, beta_s, tp, lane); break;
-                case 1: invert_unit<1>(U, lane, sync4, none); store_t_prime<1>(U, beta_s, tp, lane); break;
-                case 2: invert_unit<2>(U, lane, sync4, none); store_t_prime<2>(U, beta_s, tp, lane); break;
-                default: invert_unit<3>(U, lane, sync4, none); store_t_prime<3>(U, beta_s, tp, lane); break;
+                case 0: invert_unit<0>(U, lane, sync4, none); store_t_prime<0>(U, beta_s, tp, lane, sync4); break;
+                case 1: invert_unit<1>(U, lane, sync4, none); store_t_prime<1>(U, beta_s, tp, lane, sync4); break;
+                case 2: invert_unit<2>(U, lane, sync4, none); store_t_prime<2>(U, beta_s, tp, lane, sync4); break;
+                default: invert_unit<3>(U, lane, sync4, none); store_t_prime<3>(U, beta_s, tp, lane, sync4); break;
             }
             fence_async_smem();
             __syncthreads();
             // ---- W^T = K'^T T'^T (M = d_k) and Utilde^T = V^T T'^T (M = d_v)
             if (tid == 0) {
-                bool v_ok = factored || mbar_wait(bar(3), 0);
+                const bool v_ok = mbar_wait(bar(3), 0);
                 if (v_ok) {
                     tc_fence_after();
 #pragma unroll
@@ -356,11 +381,11 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                                  sw128_desc(sb + P_TP + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + TM_UT, sw128_desc(sb + P_V + kk * 2048, 8192, 1024),
+                        mma_bf16(tmem + TM_UT, sw128_desc(sb + P_V + kk * 2048, 16384, 1024),
                                  sw128_desc(sb + P_TP + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
                     mma_commit(bar(2));
                 } else {
-                    misc[M_FLAG] = 1.f;  // (the V reload gave up: nothing was issued)
+                    misc[M_FLAG] = 1.f;  // (the V load gave up: nothing was issued)
                 }
             }
             __syncthreads();
@@ -411,7 +436,7 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
             // loads and MMAs still in flight land before the shared memory and TMEM go
             mbar_wait(bar(0), 0);
-            if (!factored) mbar_wait(bar(3), 0);
+            if (v_issued) mbar_wait(bar(3), 0);
             mma_commit(bar(4));
             mbar_wait(bar(4), 0);
         }
