@@ -52,6 +52,7 @@ using solve::nblk;
 constexpr int C = kChunk;
 constexpr int DK = 128, DV = 128;
 constexpr int kThreads = 128;
+constexpr int kCtasPerSm = 4;  // resident CTAs per SM (shared memory and TMEM are sized for it)
 // The reference token of the factored Gram, and the bound that keeps its factors finite.
 constexpr int kRefToken = 31;
 constexpr float kFactorLogBound = 80.f;
@@ -67,14 +68,14 @@ constexpr uint32_t P_KC = 32768;   // the Gram's B operand K'': two 64-column ha
 constexpr uint32_t P_BLK = P_KC;   // the unit's 16 x 16 blocks (the solve's layout)
 constexpr uint32_t P_TP = P_KC;    // T' bf16 [t][i], 128-byte swizzled
 constexpr uint32_t P_MISC = P_KC + (solve::UNIT_FLOATS * 4 + 1023) / 1024 * 1024;
-                                   // floats: beta[64], g_C[128], g_r[128], half sums[128],
+                                   // floats: beta[64], g_C[128], g_r[128], (128 spare),
                                    // the "V load gave up" flag
 constexpr int M_BETA = 0, M_GC = 64, M_GREF = 192, M_HSUM = 320, M_FLAG = 448;
 constexpr uint32_t P_BARS = P_MISC + 456 * 4;  // load, Gram, products, V reload, drain
 constexpr uint32_t P_TMEM = P_BARS + 40;
 constexpr uint32_t P_USED = P_TMEM + 16;
 constexpr uint32_t SMEM_BYTES = P_USED + 1024;
-static_assert(P_TP % 1024 == 0 && P_BARS % 8 == 0 && SMEM_BYTES + 1024 <= 233472 / 4,
+static_assert(P_TP % 1024 == 0 && P_BARS % 8 == 0 && SMEM_BYTES + 1024 <= 233472 / kCtasPerSm,
               "shared memory: four CTAs per SM");
 // TMEM columns: the Gram, then W^T in the same columns once the Gram is read; Utilde^T
 constexpr uint32_t TM_GRAM = 0, TM_W = 0, TM_UT = 64, TM_COLS = 128;
@@ -93,6 +94,23 @@ struct ChannelParams {
 // Element (row, col) of a 128-byte-swizzled block of 64-wide bf16 rows at `block`.
 __device__ __forceinline__ float sw_elem(const unsigned char *block, int row, int col) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(block + sw128_offset(row, col)));
+}
+
+// The two bf16 halves of a packed pair, as fp32 (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// 2^x and 1/x from the hardware approximations (about 2 ulp; subnormal results flush to
+// zero). Every value they see here is within e^{+-80}.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float fast_rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // T' = (I + L)^{-1} diag(beta), block row W of warp W, as bf16 into the swizzled [t][i]
@@ -136,7 +154,7 @@ __device__ __forceinline__ void store_t_prime(const float *__restrict__ U, const
 }
 
 // The unit (chunk blockIdx.x, head blockIdx.y). map_q, map_k, map_v: the inputs.
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const ChannelParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -167,7 +185,8 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     // Everything above overlaps the tail of the planning kernel (programmatic launch).
     griddep_wait();
     griddep_launch_dependents();
-    const bool live = p.ctl[0] == GDR_OK && c < p.ctl[1];
+    const int n_chunks = p.ctl[0] == GDR_OK ? p.ctl[1] : 0;
+    const bool live = c < n_chunks;
     bool fail = false;
     if (live) {
         const int4 pl = p.plan[c];
@@ -190,48 +209,70 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             v_issued = true;
         };
         if (tid < C) misc[M_BETA + tid] = tid < len ? p.beta[(size_t)(t0 + tid) * p.H + h] : 0.f;
-        // g by columns: thread (cp, th) owns channels 2cp, 2cp + 1 over tokens 32th .. 32th + 31
-        const int cp = tid & 63, th = tid >> 6;
-        float g[32][2];
+        // g by tiles: thread (o, grp) owns channels 8o .. 8o + 7 over tokens 8grp .. 8grp + 7
+        const int o = tid & 15, grp = tid >> 4;
+        float g[8][8];
         {
-            float a0 = 0.f, a1 = 0.f;
+            float acc[8];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int t = 32 * th + j;
-                float2 la = make_float2(0.f, 0.f);
-                if (t < len)
-                    la = *reinterpret_cast<const float2 *>(p.log_alpha + ((size_t)(t0 + t) * p.H + h) * DK + 2 * cp);
-                a0 += la.x;
-                a1 += la.y;
-                g[j][0] = a0;
-                g[j][1] = a1;
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int t = 8 * grp + j;
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+                if (t < len) {
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        p.log_alpha + ((size_t)(t0 + t) * p.H + h) * DK + 8 * o);
+                    a = src[0];
+                    b = src[1];
+                }
+                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) g[j][e] = acc[e];
             }
-            if (th == 0) {
-                misc[M_HSUM + 2 * cp] = a0;
-                misc[M_HSUM + 2 * cp + 1] = a1;
-                misc[M_GREF + 2 * cp] = g[kRefToken][0];
-                misc[M_GREF + 2 * cp + 1] = g[kRefToken][1];
+            // each group's sums, over K'' (written only after the scan)
+            float4 *sums = reinterpret_cast<float4 *>(sm + P_KC) + (grp * DK + 8 * o) / 4;
+            sums[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            sums[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        __syncthreads();
+        {
+            float base[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) base[e] = 0.f;
+            const float4 *sums = reinterpret_cast<const float4 *>(sm + P_KC) + 2 * o;
+            for (int gg = 0; gg < grp; ++gg) {
+                const float4 a = sums[gg * (DK / 4)], b = sums[gg * (DK / 4) + 1];
+                base[0] += a.x; base[1] += a.y; base[2] += a.z; base[3] += a.w;
+                base[4] += b.x; base[5] += b.y; base[6] += b.z; base[7] += b.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) g[j][e] += base[e];
+            float4 *gref = reinterpret_cast<float4 *>(misc + M_GREF + 8 * o);
+            float4 *gcs = reinterpret_cast<float4 *>(misc + M_GC + 8 * o);
+            constexpr int jr = kRefToken % 8;
+            if (grp == kRefToken / 8) {
+                gref[0] = make_float4(g[jr][0], g[jr][1], g[jr][2], g[jr][3]);
+                gref[1] = make_float4(g[jr][4], g[jr][5], g[jr][6], g[jr][7]);
+            }
+            if (grp == 7) {
+                gcs[0] = make_float4(g[7][0], g[7][1], g[7][2], g[7][3]);
+                gcs[1] = make_float4(g[7][4], g[7][5], g[7][6], g[7][7]);
             }
         }
         __syncthreads();
-        if (th == 1) {
-            const float s0 = misc[M_HSUM + 2 * cp], s1 = misc[M_HSUM + 2 * cp + 1];
+        float gc[8], gr[8];
+        bool col_ok = true;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                g[j][0] += s0;
-                g[j][1] += s1;
-            }
-            misc[M_GC + 2 * cp] = g[31][0];
-            misc[M_GC + 2 * cp + 1] = g[31][1];
+        for (int e = 0; e < 8; ++e) {
+            gc[e] = misc[M_GC + 8 * o + e];
+            gr[e] = misc[M_GREF + 8 * o + e];
+            col_ok = col_ok && -gr[e] < kFactorLogBound && gr[e] - gc[e] < kFactorLogBound;
         }
-        __syncthreads();
-        const float gc0 = misc[M_GC + 2 * cp], gc1 = misc[M_GC + 2 * cp + 1];
-        const float gr0 = misc[M_GREF + 2 * cp], gr1 = misc[M_GREF + 2 * cp + 1];
-        const bool col_ok = -gr0 < kFactorLogBound && gr0 - gc0 < kFactorLogBound &&
-                            -gr1 < kFactorLogBound && gr1 - gc1 < kFactorLogBound;
         const bool factored = __syncthreads_and(col_ok) != 0;
-        // the shift of the tiles the products read: g_r with the factored Gram, else none
-        const float sh0 = factored ? gr0 : 0.f, sh1 = factored ? gr1 : 0.f;
         if (!mbar_wait(bar(0), 0)) fail = true;
         fail = __syncthreads_or(fail) != 0;
         float *U = reinterpret_cast<float *>(sm + P_BLK);
@@ -242,8 +283,11 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             // element-wise pass below fills only after this loop has read it.
             float *gs = reinterpret_cast<float *>(p.QW + (u * C) * 256);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                *reinterpret_cast<float2 *>(gs + (32 * th + j) * DK + 2 * cp) = make_float2(g[j][0], g[j][1]);
+            for (int j = 0; j < 8; ++j) {
+                float4 *row = reinterpret_cast<float4 *>(gs + (8 * grp + j) * DK + 8 * o);
+                row[0] = make_float4(g[j][0], g[j][1], g[j][2], g[j][3]);
+                row[1] = make_float4(g[j][4], g[j][5], g[j][6], g[j][7]);
+            }
             for (int e = tid; e < 10 * solve::BS; e += kThreads) U[e] = 0.f;  // the ten L blocks
             __syncthreads();
             for (int e = tid; e < C * C; e += kThreads) {
@@ -266,28 +310,74 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         if (!fail) {
             // ---- element-wise: the chain's e^g . Q and e^{g_C - g} . K to the workspace,
             // the products' tiles in place: K' = e^{g - sh} . K (and with the factored Gram
-            // Q' = e^{g - sh} . Q, K'' = e^{sh - g} . K). Thread (cp, th): channels 2cp,
-            // 2cp + 1 of its 32 tokens, one bf16 pair each.
-            const int b = cp >> 5, cc = cp & 31;
+            // Q' = e^{g - sh} . Q, K'' = e^{sh - g} . K), sh = g_r with the factored Gram,
+            // else 0. Thread (o, grp): one 16-byte row segment of 8 channels per token.
+            // With the factored Gram every factor comes from s = e^{g - g_r} (within e^{+-80}):
+            // e^{g - g_r} = s, e^{g_r - g} = 1 / s, e^g = e^{g_r} s, e^{g_C - g} = e^{g_C - g_r} / s.
+            const int b = o >> 3, cc = o & 7;
             unsigned char *kh = sm + P_KQ + 16384 * b, *qh = kh + 8192, *kc = sm + P_KC + 8192 * b;
-            __nv_bfloat16 *qw = p.QW + (u * C) * 256 + 2 * cp;
-            __nv_bfloat16 *kt = p.KT + (u * C) * DK + 2 * cp;
+            __nv_bfloat16 *qw = p.QW + (u * C) * 256 + 8 * o;
+            __nv_bfloat16 *kt = p.KT + (u * C) * DK + 8 * o;
+            constexpr float kLog2e = 1.4426950408889634f;
+            if (factored) {
+                float shl[8], eq[8], ek[8];  // -g_r log2(e), e^{g_r}, e^{g_C - g_r}
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int t = 32 * th + j;
-                const uint32_t off = (uint32_t)(t * 128 + ((((cc >> 2) ^ t) & 7) << 4) + (cc & 3) * 4);
-                const float2 k2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(kh + off));
-                const float2 q2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qh + off));
-                const float e0 = fast_exp(g[j][0]), e1 = fast_exp(g[j][1]);
-                *reinterpret_cast<uint32_t *>(qw + (size_t)t * 256) = pack_bf16x2(q2.x * e0, q2.y * e1);
-                *reinterpret_cast<uint32_t *>(kt + (size_t)t * DK) =
-                    pack_bf16x2(k2.x * fast_exp(gc0 - g[j][0]), k2.y * fast_exp(gc1 - g[j][1]));
-                const float s0 = fast_exp(g[j][0] - sh0), s1 = fast_exp(g[j][1] - sh1);
-                *reinterpret_cast<uint32_t *>(kh + off) = pack_bf16x2(k2.x * s0, k2.y * s1);
-                if (factored) {
-                    *reinterpret_cast<uint32_t *>(qh + off) = pack_bf16x2(q2.x * s0, q2.y * s1);
-                    *reinterpret_cast<uint32_t *>(kc + off) =
-                        pack_bf16x2(k2.x * fast_exp(sh0 - g[j][0]), k2.y * fast_exp(sh1 - g[j][1]));
+                for (int e = 0; e < 8; ++e) {
+                    shl[e] = -gr[e] * kLog2e;
+                    eq[e] = fast_exp(gr[e]);
+                    ek[e] = fast_exp(gc[e] - gr[e]);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int t = 8 * grp + j;
+                    const uint32_t off = (uint32_t)(t * 128 + ((cc ^ (t & 7)) << 4));
+                    const uint4 kr = *reinterpret_cast<const uint4 *>(kh + off);
+                    const uint4 qr = *reinterpret_cast<const uint4 *>(qh + off);
+                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, qv[4] = {qr.x, qr.y, qr.z, qr.w};
+                    uint32_t o_qw[4], o_kt[4], o_k1[4], o_q1[4], o_k2[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float k0 = bf16_lo(kw[w]), k1 = bf16_hi(kw[w]);
+                        const float q0 = bf16_lo(qv[w]), q1 = bf16_hi(qv[w]);
+                        const int e0 = 2 * w, e1 = 2 * w + 1;
+                        const float s0 = fast_exp2(fmaf(g[j][e0], kLog2e, shl[e0]));
+                        const float s1 = fast_exp2(fmaf(g[j][e1], kLog2e, shl[e1]));
+                        const float r0 = fast_rcp(s0), r1 = fast_rcp(s1);
+                        o_qw[w] = pack_bf16x2(q0 * s0 * eq[e0], q1 * s1 * eq[e1]);
+                        o_kt[w] = pack_bf16x2(k0 * r0 * ek[e0], k1 * r1 * ek[e1]);
+                        o_k1[w] = pack_bf16x2(k0 * s0, k1 * s1);
+                        o_q1[w] = pack_bf16x2(q0 * s0, q1 * s1);
+                        o_k2[w] = pack_bf16x2(k0 * r0, k1 * r1);
+                    }
+                    *reinterpret_cast<uint4 *>(qw + (size_t)t * 256) = make_uint4(o_qw[0], o_qw[1], o_qw[2], o_qw[3]);
+                    *reinterpret_cast<uint4 *>(kt + (size_t)t * DK) = make_uint4(o_kt[0], o_kt[1], o_kt[2], o_kt[3]);
+                    *reinterpret_cast<uint4 *>(kh + off) = make_uint4(o_k1[0], o_k1[1], o_k1[2], o_k1[3]);
+                    *reinterpret_cast<uint4 *>(qh + off) = make_uint4(o_q1[0], o_q1[1], o_q1[2], o_q1[3]);
+                    *reinterpret_cast<uint4 *>(kc + off) = make_uint4(o_k2[0], o_k2[1], o_k2[2], o_k2[3]);
+                }
+            } else {
+                // each factor as its own exponential (no factor above 1 to divide by)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int t = 8 * grp + j;
+                    const uint32_t off = (uint32_t)(t * 128 + ((cc ^ (t & 7)) << 4));
+                    const uint4 kr = *reinterpret_cast<const uint4 *>(kh + off);
+                    const uint4 qr = *reinterpret_cast<const uint4 *>(qh + off);
+                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, qv[4] = {qr.x, qr.y, qr.z, qr.w};
+                    uint32_t o_qw[4], o_kt[4], o_k1[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float k0 = bf16_lo(kw[w]), k1 = bf16_hi(kw[w]);
+                        const float q0 = bf16_lo(qv[w]), q1 = bf16_hi(qv[w]);
+                        const int e0 = 2 * w, e1 = 2 * w + 1;
+                        const float x0 = fast_exp(g[j][e0]), x1 = fast_exp(g[j][e1]);
+                        o_qw[w] = pack_bf16x2(q0 * x0, q1 * x1);
+                        o_kt[w] = pack_bf16x2(k0 * fast_exp(gc[e0] - g[j][e0]), k1 * fast_exp(gc[e1] - g[j][e1]));
+                        o_k1[w] = pack_bf16x2(k0 * x0, k1 * x1);
+                    }
+                    *reinterpret_cast<uint4 *>(qw + (size_t)t * 256) = make_uint4(o_qw[0], o_qw[1], o_qw[2], o_qw[3]);
+                    *reinterpret_cast<uint4 *>(kt + (size_t)t * DK) = make_uint4(o_kt[0], o_kt[1], o_kt[2], o_kt[3]);
+                    *reinterpret_cast<uint4 *>(kh + off) = make_uint4(o_k1[0], o_k1[1], o_k1[2], o_k1[3]);
                 }
             }
             fence_async_smem();

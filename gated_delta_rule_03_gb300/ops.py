@@ -79,9 +79,13 @@ def _check_out_step(out_gate, out_norm_weight, like, dv):
 class GdrError(RuntimeError):
     """A libgdr call returned a negative status."""
 
-    def __init__(self, status, what):
+    def __init__(self, status, what, detail=None):
+        # detail: the status text; read from the library unless given (it is given when
+        # the library itself cannot be loaded)
         self.status = status
-        super().__init__(f"{what}: {status_string(status)} ({status})")
+        if detail is None:
+            detail = status_string(status)
+        super().__init__(f"{what}: {detail} ({status})")
 
 
 def library_path():
@@ -94,7 +98,8 @@ def _load():
         return _lib
     if not os.path.exists(_LIB_PATH):
         raise GdrError(-5, f"libgdr.so not found at {_LIB_PATH}; build it with "
-                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+                           "`python -c 'import __graft_entry__ as g; g.build()'`",
+                       detail="the CUDA library is not built")
     lib = ctypes.CDLL(_LIB_PATH)
     vp, fp, i64, c_int = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.gdr_status_string.argtypes = [c_int]

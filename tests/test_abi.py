@@ -245,3 +245,16 @@ def test_workspace_holds_the_segment_sets_only_when_segmenting_is_possible(lib):
     per_chunk = (lib.gdr_chunk_fwd_workspace_size(20, 20 * 64 * 64 + 20 * 64, 2, 128, 128, 64, 1)
                  - many)
     assert per_chunk < 80 * 1024 * 20  # grows by the per-unit buffers, not by state sets
+
+
+def test_a_missing_library_fails_loudly(monkeypatch):
+    # without the built library every call raises GdrError naming the missing file (no
+    # fallback path, and no recursion through the status-text lookup)
+    from gated_delta_rule_03_gb300 import ops
+    monkeypatch.setattr(ops, "_lib", None)
+    monkeypatch.setattr(ops, "_LIB_PATH", "/nonexistent/libgdr.so")
+    with pytest.raises(ops.GdrError, match="not found") as e:
+        ops.chunk_fwd_workspace_size(1, 64, 2, 64, 64)
+    assert e.value.status == -5
+    with pytest.raises(ops.GdrError, match="not built"):
+        ops.status_string(0)
