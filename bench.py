@@ -261,11 +261,13 @@ def oracle_prefill_sample(inp):
                 num_seqs=inp.num_seqs)
 
 
-def cpu_baseline(inp, seconds, name, heads=None):
+def cpu_baseline(inp, seconds, name, heads=None, gpu_out=None):
     """The oracle, as it stands, on this host's cores: repeat the full workload (or only
     the given heads of it) until `seconds` have passed (at least once). With a subset of
     heads the rate is scaled to the workload's H heads (the heads are independent and
-    equal in work) and the per-head rate is reported beside it."""
+    equal in work) and the per-head rate is reported beside it. gpu_out: the timed call's
+    (o, S_final) for the same heads, as float64 arrays; the oracle's result is compared
+    with them (max |gpu - oracle| / max |oracle|, the tests' measure) under "parity"."""
     import oracle
     args = oracle_prefill_sample(inp)
     nh = inp.H
@@ -279,7 +281,7 @@ def cpu_baseline(inp, seconds, name, heads=None):
     threads = oracle.default_threads()
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.forward(**args, threads=threads)
+        ref = oracle.forward(**args, threads=threads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds or reps >= 1000:
@@ -294,7 +296,19 @@ def cpu_baseline(inp, seconds, name, heads=None):
                      f"{el:.1f} s, float64 token loop")
     if heads is not None:
         out["per_head_token_rate"] = token_heads / nh / el
+    if gpu_out is not None:
+        err = lambda g, r: float(np.abs(g - r).max() / max(np.abs(r).max(), 1e-300))
+        out["parity"] = {"o_rel_err": err(gpu_out[0], ref[0]), "S_rel_err": err(gpu_out[1], ref[1]),
+                         "tolerance": 1e-4 if inp.dtype == "f32" else 2e-2,
+                         "heads": "all" if heads is None else list(heads)}
     return out
+
+
+def host_outputs(o, S, heads=None):
+    """The call's o and S_final (the given heads only) as float64 host arrays."""
+    if heads is not None:
+        o, S = o[:, list(heads)], S[:, list(heads)]
+    return (o.to(torch.float64).cpu().numpy(), S.to(torch.float64).cpu().numpy())
 
 
 def run_reference(args):
@@ -347,23 +361,26 @@ def workload_config(inp, name):
 
 
 # the other prefill workloads, timed in the same run as the headline one
-SIDE_WORKLOADS = (("varlen", "varlen_bf16", None), ("long", "long_bf16", (0, 1)),
-                  ("tiny", "tiny_fp32", None))
+# (key, workload, heads the CPU baseline runs (None: all), forget-rate granularity)
+SIDE_WORKLOADS = (("varlen", "varlen_bf16", None, "head"), ("long", "long_bf16", (0, 1), "head"),
+                  ("tiny", "tiny_fp32", None, "head"),
+                  ("channel", "prefill_bf16", (0, 1), "channel"))
 
 
-def bench_prefill_workload(name, args, device, stream, world, local, peaks, cpu_heads=None):
+def bench_prefill_workload(name, args, device, stream, world, local, peaks, cpu_heads=None,
+                           decay="head"):
     """One prefill workload: per-call CUDA-event timing over the driver's --steps, a
     sustained stretch of back-to-back calls with the clocks sampled, the roofline of the
     call (HBM and tensor fractions), the recorded DRAM traffic and the oracle on the host."""
     from gated_delta_rule_03_gb300 import chunk_fwd, chunk_fwd_workspace_size, ops
-    inp = inputs.workload_prefill(name)
+    inp = inputs.workload_prefill(name, decay=decay)
     d = lambda t: None if t is None else t.to(device)
     q, k, v, la, b = d(inp.q), d(inp.k), d(inp.v), d(inp.log_alpha), d(inp.beta)
     S0, cu = d(inp.S0), d(inp.cu_seqlens)
     o = torch.empty((inp.total_tokens, inp.H, inp.dv), dtype=q.dtype, device=device)
     S = torch.empty((inp.num_seqs, inp.H, inp.dk, inp.dv), dtype=torch.float32, device=device)
     ws = torch.empty(chunk_fwd_workspace_size(inp.num_seqs, inp.total_tokens, inp.H, inp.dk,
-                                              inp.dv, inp.chunk, q.dtype),
+                                              inp.dv, inp.chunk, q.dtype, decay),
                      dtype=torch.uint8, device=device)
 
     def step():
@@ -377,10 +394,12 @@ def bench_prefill_workload(name, args, device, stream, world, local, peaks, cpu_
     sus = sustained_calls(step, stream, device, local, args.sustained_seconds, call_ms)
     varlen = cu is not None
     schedule = ops.chunk_fwd_schedule(inp.num_seqs, inp.total_tokens, inp.H, inp.dk, inp.dv,
-                                      q.dtype, varlen=varlen)
-    main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype, schedule=schedule)
+                                      q.dtype, varlen=varlen, decay=decay)
+    main_kernel = ops.chunk_fwd_main_kernel(inp.dk, inp.dv, q.dtype, schedule=schedule,
+                                            decay=decay)
     launches = ops.chunk_fwd_kernel_launches(inp.num_seqs, inp.total_tokens, inp.H, inp.dk,
-                                             inp.dv, q.dtype, varlen=varlen)
+                                             inp.dv, q.dtype, varlen=varlen, decay=decay)
+    traffic_key = name + ("" if decay == "head" else "_channel")
     nbytes, flops = prefill_bytes(inp), prefill_flops(inp)
     achieved = nbytes / (call_ms / 1e3) / 1e9
     tflops = flops / (call_ms / 1e3) / 1e12
@@ -388,10 +407,10 @@ def bench_prefill_workload(name, args, device, stream, world, local, peaks, cpu_
         "workload": workload_config(inp, name)["workload"],
         "tokens_per_s": world * inp.total_tokens * args.steps / (total_ms / 1e3),
         "ms_per_call": total_ms / args.steps, "steps": args.steps,
-        "schedule": schedule, "dtype": ops.chunk_fwd_compute_dtype(inp.dk, inp.dv, q.dtype),
+        "schedule": schedule, "dtype": ops.chunk_fwd_compute_dtype(inp.dk, inp.dv, q.dtype, decay),
         "roofline": {"kernel": main_kernel, "bound": "hbm", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": recorded_traffic(main_kernel, name),
+                     "traffic": recorded_traffic(main_kernel, traffic_key),
                      "algorithmic_bytes_per_launch": nbytes, "launch_ms": call_ms,
                      "tensor": {"achieved": tflops, "peak": peaks["bf16_tflops"],
                                 "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
@@ -403,10 +422,12 @@ def bench_prefill_workload(name, args, device, stream, world, local, peaks, cpu_
     if inp.dtype == "f32":
         out["roofline"]["note"] = ("latency-bound: 512 token-heads in 8 chunks; reported, no "
                                    "roofline target")
+    gpu_out = host_outputs(o, S, cpu_heads)
     del q, k, v, la, b, S0, cu, o, S, ws
     torch.cuda.empty_cache()
     if world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(inp, min(args.cpu_seconds, 3.0), name, heads=cpu_heads)
+        out["cpu_baseline"] = cpu_baseline(inp, min(args.cpu_seconds, 3.0), traffic_key,
+                                           heads=cpu_heads, gpu_out=gpu_out)
     return out
 
 
@@ -489,14 +510,14 @@ def run_gdr(args):
 
     side = {}
     if not args.no_side and args.decay == "head":
-        for key, name, heads in SIDE_WORKLOADS:
-            if name != args.workload:
+        for key, name, heads, decay in SIDE_WORKLOADS:
+            if (name, decay) != (args.workload, args.decay):
                 side[key] = bench_prefill_workload(name, args, device, stream, world, local,
-                                                   peaks, cpu_heads=heads)
+                                                   peaks, cpu_heads=heads, decay=decay)
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, args.cpu_seconds, args.workload)
+        cpu = cpu_baseline(inp, args.cpu_seconds, workload_key, gpu_out=host_outputs(o, S))
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,

@@ -291,7 +291,7 @@ def decode_step(q, k, v, log_alpha, beta, S, o=None, stream=None, rule="delta", 
 _PATHS = {
     0: dict(main_kernel="exact_chain_kernel", compute_dtype="f32"),
     1: dict(main_kernel="tc_chain_kernel", compute_dtype="bf16"),
-    2: dict(main_kernel="tc_chain_channel_kernel", compute_dtype="bf16"),
+    2: dict(main_kernel="channel_prep_kernel", compute_dtype="bf16"),
 }
 PATH_CHANNEL_TENSOR = 2  # GDR_PATH_CHANNEL_TENSOR
 

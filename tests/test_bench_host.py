@@ -70,3 +70,19 @@ def test_decode_cpu_baseline_sample():
     out = bench.cpu_decode_baseline(dec, 0.05, seqs=2)
     assert out["kind"] == "oracle" and out["value"] > 0 and out["cores"] >= 1
     assert out["sample"].startswith("2 of 4 sequences x 2 heads")
+
+
+def test_cpu_baseline_compares_the_given_outputs_with_the_oracle():
+    import numpy as np
+    import oracle
+    inp = inputs.prefill_inputs([70, 30], H=3, dk=16, dv=8, dtype="f32", seed=5, s0_std=0.1)
+    full = oracle.forward(**bench.oracle_prefill_sample(inp))
+    sel = [0, 2]
+    o, S = full[0][:, sel], full[1][:, sel]
+    out = bench.cpu_baseline(inp, 0.0, "small", heads=sel, gpu_out=(o, S))
+    assert out["parity"]["o_rel_err"] < 1e-12 and out["parity"]["S_rel_err"] < 1e-12
+    assert out["parity"]["tolerance"] == 1e-4 and out["parity"]["heads"] == sel
+    bad = o.copy()
+    bad[5, 1, 3] += 0.5 * np.abs(o).max()  # one wrong element of head 2
+    out = bench.cpu_baseline(inp, 0.0, "small", heads=sel, gpu_out=(bad, S))
+    assert out["parity"]["o_rel_err"] == pytest.approx(0.5, rel=1e-9)

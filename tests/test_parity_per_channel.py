@@ -147,7 +147,7 @@ def test_prologue_and_output_step(dv):
 def test_bf16_128_takes_the_channel_tensor_path():
     assert ops.chunk_fwd_path(128, 128, torch.bfloat16, "channel") == ops.PATH_CHANNEL_TENSOR
     assert ops.chunk_fwd_main_kernel(128, 128, torch.bfloat16, decay="channel") == \
-        "tc_chain_channel_kernel"
+        "channel_prep_kernel"
     assert ops.chunk_fwd_compute_dtype(128, 128, torch.bfloat16, "channel") == "bf16"
 
 
