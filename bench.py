@@ -422,10 +422,11 @@ def bench_prefill_workload(name, args, device, stream, world, local, peaks, cpu_
     if inp.dtype == "f32":
         out["roofline"]["note"] = ("latency-bound: 512 token-heads in 8 chunks; reported, no "
                                    "roofline target")
-    gpu_out = host_outputs(o, S, cpu_heads)
+    cpu = world == 1 and not args.no_cpu_baseline
+    gpu_out = host_outputs(o, S, cpu_heads) if cpu else None
     del q, k, v, la, b, S0, cu, o, S, ws
     torch.cuda.empty_cache()
-    if world == 1 and not args.no_cpu_baseline:
+    if cpu:
         out["cpu_baseline"] = cpu_baseline(inp, min(args.cpu_seconds, 3.0), traffic_key,
                                            heads=cpu_heads, gpu_out=gpu_out)
     return out
