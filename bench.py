@@ -481,28 +481,62 @@ def run_gdr(args):
     workload_key = args.workload + ("" if args.decay == "head" else "_channel")
     traffic = recorded_traffic(main_kernel, workload_key)
 
-    # end to end through the public API: pinned host inputs in, results back out
+    # end to end through the public API: every step copies its inputs in from pinned host
+    # memory and its results (o and the final state) back out. Steps are pipelined over
+    # three streams with two device copies of the inputs and outputs: the copy-in of step
+    # i + 1 and the copy-out of step i - 1 run while step i computes.
     pin = lambda t: None if t is None else t.pin_memory()
-    qh, kh, vh, lah, bh = pin(inp.q), pin(inp.k), pin(inp.v), pin(inp.log_alpha), pin(inp.beta)
-    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    Sh = torch.empty(S.shape, dtype=S.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, lah, bh))
-    d2h = oh.numel() * oh.element_size() + Sh.numel() * Sh.element_size()
+    host_in = [pin(t) for t in (inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0)
+               if t is not None]
+    dev_in = [[torch.empty(t.shape, dtype=t.dtype, device=device) for t in host_in]
+              for _ in range(2)]
+    dev_out = [(torch.empty_like(o), torch.empty_like(S)) for _ in range(2)]
+    host_out = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                 torch.empty(S.shape, dtype=S.dtype).pin_memory()) for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer set b landed
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # the call on set b finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # the outputs of set b copied out
 
-    def e2e_step():
-        q.copy_(qh, non_blocking=True)
-        k.copy_(kh, non_blocking=True)
-        v.copy_(vh, non_blocking=True)
-        la.copy_(lah, non_blocking=True)
-        b.copy_(bh, non_blocking=True)
-        step()
-        oh.copy_(o, non_blocking=True)
-        Sh.copy_(S, non_blocking=True)
+    def e2e_steps(n):
+        for i in range(n):
+            bset = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:  # the call two steps back has read this set's inputs
+                    s_in.wait_event(ev_done[bset])
+                for h, dv in zip(host_in, dev_in[bset]):
+                    dv.copy_(h, non_blocking=True)
+                ev_in[bset].record(s_in)
+            stream.wait_event(ev_in[bset])
+            if i >= 2:  # this set's outputs of two steps back are out
+                stream.wait_event(ev_out[bset])
+            qd, kd, vd, lad, bd = dev_in[bset][:5]
+            s0d = dev_in[bset][5] if inp.S0 is not None else None
+            chunk_fwd(qd, kd, vd, lad, bd, S0=s0d, cu_seqlens=cu, num_seqs=inp.num_seqs,
+                      chunk=inp.chunk, o=dev_out[bset][0], S_final=dev_out[bset][1],
+                      workspace=ws, stream=stream)
+            ev_done[bset].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[bset])
+                host_out[bset][0].copy_(dev_out[bset][0], non_blocking=True)
+                host_out[bset][1].copy_(dev_out[bset][1], non_blocking=True)
+                ev_out[bset].record(s_out)
 
-    with torch.cuda.stream(stream):
-        for _ in range(min(args.warmup, 3)):
-            e2e_step()
-    e2e_ms, _ = timed_calls(e2e_step, args.steps, stream, world, device, per_call=False)
+    e2e_steps(min(args.warmup, 3))
+    torch.cuda.synchronize(device)
+    barrier(world)
+    e2e_start, e2e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_start.record(s_in)
+    stream.wait_event(e2e_start)
+    s_out.wait_event(e2e_start)
+    e2e_steps(args.steps)
+    s_out.wait_event(ev_done[(args.steps - 1) % 2])
+    e2e_end.record(s_out)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    e2e_ms = max_over_ranks(e2e_start.elapsed_time(e2e_end), world, device)
     e2e_value = world * tokens * args.steps / (e2e_ms / 1e3)
 
     decode = None
@@ -542,7 +576,9 @@ def run_gdr(args):
                      "timing": "CUDA events around each gdr_chunk_fwd call on its stream"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
+                "pipeline": "two device sets of inputs and outputs on three streams: the "
+                            "copy-in of step i+1 and the copy-out of step i-1 overlap step i"},
         "gpu_launches": kernel_launches * args.steps,
         "clocks": clock_info,
         "sustained": sustained,
