@@ -1,6 +1,8 @@
 // channel_tc.cu -- the tensor-core prefill with one forget rate per key channel: the
 // per-channel chunk kernel (channel_tc.cuh), the chain in its per-channel mode
 // (chain_tc.cuh), and their host launcher.
+#include <cstdlib>
+
 #include "chain_tc.cuh"
 #include "channel_tc.cuh"
 
@@ -17,6 +19,24 @@ tc_chain_channel_kernel(const __grid_constant__ CUtensorMap map_qw, const __grid
 
 }  // namespace
 }  // namespace chain
+
+// The operands kernel's wait bound, and a test of its give-up path: with
+// GDR_DEBUG_PREP_FAULT=<chunk> in the environment, head 0's CTA of that chunk skips its key
+// and query loads and every wait gives up after 2e7 SM cycles (about 10 ms) instead of
+// 2e9. That CTA then marks the call GDR_ERR_DEVICE_TIMEOUT in the status word and drains;
+// the chain kernel, seeing the status, writes nothing. Nothing faults or hangs.
+static void channel_wait_policy(channel::ChannelParams &p) {
+    p.wait_cycles = sm100::kWaitCycles;
+    p.fault_chunk = -1;
+    if (const char *env = getenv("GDR_DEBUG_PREP_FAULT")) {
+        char *end = nullptr;
+        const long c = strtol(env, &end, 10);
+        if (end != env && *end == '\0' && c >= 0 && c < (1l << 30)) {
+            p.fault_chunk = (int)c;
+            p.wait_cycles = 20000000;
+        }
+    }
+}
 
 int launch_prefill_channel_tc(const PrefillArgs &a, const WsLayout &L) {
     using namespace chain;
@@ -62,6 +82,7 @@ int launch_prefill_channel_tc(const PrefillArgs &a, const WsLayout &L) {
     cp.UT = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.UT);
     cp.AT = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.T);
     cp.G = reinterpret_cast<float *>(a.ws + L.G);
+    channel_wait_policy(cp);
     cudaLaunchConfig_t pcfg = {};
     pcfg.gridDim = dim3((unsigned)L.max_chunks, (unsigned)a.H);
     pcfg.blockDim = dim3(channel::kThreads);

@@ -89,6 +89,9 @@ struct ChannelParams {
     int additive;            // the additive rule: L = 0, W = 0
     __nv_bfloat16 *QW, *KT, *UT, *AT;
     float *G;
+    long long wait_cycles;   // bound of every wait (SM cycles)
+    int fault_chunk;         // test knob: head 0's CTA of this chunk skips its key and query
+                             // loads, so that its wait gives up (-1: never)
 };
 
 // Element (row, col) of a 128-byte-swizzled block of 64-wide bf16 rows at `block`.
@@ -165,6 +168,7 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     float *misc = reinterpret_cast<float *>(sm + P_MISC);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P_TMEM);
     auto bar = [&](int i) { return sb + P_BARS + 8u * (uint32_t)i; };
+    auto wait = [&](int i, uint32_t parity) { return mbar_wait_for(bar(i), parity, p.wait_cycles); };
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(bar(i), 1);
         misc[M_FLAG] = 0.f;
@@ -192,7 +196,9 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         const int4 pl = p.plan[c];
         const int t0 = pl.y, len = pl.z;
         const size_t u = (size_t)c * p.H + h;  // chunk-major, head-minor
-        if (tid == 0) {
+        // (thread 0 issues every copy and drains them after a failure)
+        const bool kq_issued = !(c == p.fault_chunk && h == 0);
+        if (tid == 0 && kq_issued) {
             mbar_arrive_expect_tx(bar(0), 4 * 8192);
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
@@ -273,7 +279,7 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             col_ok = col_ok && -gr[e] < kFactorLogBound && gr[e] - gc[e] < kFactorLogBound;
         }
         const bool factored = __syncthreads_and(col_ok) != 0;
-        if (!mbar_wait(bar(0), 0)) fail = true;
+        if (!wait(0, 0)) fail = true;
         fail = __syncthreads_or(fail) != 0;
         float *U = reinterpret_cast<float *>(sm + P_BLK);
         __nv_bfloat16 *arow = p.AT + (u * 2 + 1) * C * C;
@@ -395,7 +401,7 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     }
                     mma_commit(bar(1));
                 }
-                if (!mbar_wait(bar(1), 0)) fail = true;
+                if (!wait(1, 0)) fail = true;
                 // a Gram that did not complete is neither read nor written over
                 fail = __syncthreads_or(fail) != 0;
             }
@@ -462,7 +468,7 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             __syncthreads();
             // ---- W^T = K'^T T'^T (M = d_k) and Utilde^T = V^T T'^T (M = d_v)
             if (tid == 0) {
-                const bool v_ok = mbar_wait(bar(3), 0);
+                const bool v_ok = wait(3, 0);
                 if (v_ok) {
                     tc_fence_after();
 #pragma unroll
@@ -481,7 +487,7 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             __syncthreads();
             const bool issued = misc[M_FLAG] == 0.f;
             if (!issued) fail = true;
-            if (issued && !mbar_wait(bar(2), 0)) fail = true;
+            if (issued && !wait(2, 0)) fail = true;
             tc_fence_after();
             fail = __syncthreads_or(fail) != 0;
             if (!fail) {
@@ -525,10 +531,10 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         if (fail && tid == 0) {
             atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
             // loads and MMAs still in flight land before the shared memory and TMEM go
-            mbar_wait(bar(0), 0);
-            if (v_issued) mbar_wait(bar(3), 0);
+            if (kq_issued) wait(0, 0);
+            if (v_issued) wait(3, 0);
             mma_commit(bar(4));
-            mbar_wait(bar(4), 0);
+            wait(4, 0);
         }
     }
     tc_fence_before();

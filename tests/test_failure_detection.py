@@ -86,3 +86,38 @@ def test_per_channel_chain_gives_up_on_a_missing_load_then_the_next_call_is_clea
     ref_o, ref_S = oracle_prefill(inp)
     assert rel_err(f64(o), ref_o) <= TOL["bf16"]
     assert rel_err(f64(S), ref_S) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("fault_chunk", [0, 6])
+def test_per_channel_operands_kernel_gives_up_then_the_next_call_is_clean(fault_chunk,
+                                                                         monkeypatch):
+    # GDR_DEBUG_PREP_FAULT=<chunk>: head 0's CTA of that chunk in the kernel that builds the
+    # per-channel operands skips its key and query loads; its wait runs out, it marks the
+    # status word and drains, and the chain after it writes nothing
+    inp = inputs.prefill_inputs([300, 200], H=2, dk=128, dv=128, dtype="bf16", seed=43,
+                                s0_std=0.2, gate="slow", decay="channel")
+    n, T = inp.num_seqs, inp.total_tokens
+    dev = torch.device("cuda", 0)
+    d = lambda t: None if t is None else t.to(dev)
+    q, k, v, la, b, S0 = d(inp.q), d(inp.k), d(inp.v), d(inp.log_alpha), d(inp.beta), d(inp.S0)
+    cu = d(inp.cu_seqlens)
+    ws = torch.empty(ops.chunk_fwd_workspace_size(n, T, inp.H, 128, 128, decay="channel"),
+                     dtype=torch.uint8, device=dev)
+    o = torch.full((T, inp.H, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    S = torch.full((n, inp.H, 128, 128), float("nan"), device=dev)
+
+    monkeypatch.setenv("GDR_DEBUG_PREP_FAULT", str(fault_chunk))
+    t0 = time.perf_counter()
+    ops.chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, num_seqs=n, o=o, S_final=S, workspace=ws)
+    status = ops.read_device_status(ws)  # synchronises
+    elapsed = time.perf_counter() - t0
+    assert status == GDR_ERR_DEVICE_TIMEOUT, ops.status_string(status)
+    assert elapsed < 10.0
+    assert bool(torch.isnan(o).all()) and bool(torch.isnan(S).all())  # the chain wrote nothing
+
+    monkeypatch.delenv("GDR_DEBUG_PREP_FAULT")
+    o, S = chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, num_seqs=n, workspace=ws)
+    assert ops.read_device_status(ws) == 0
+    ref_o, ref_S = oracle_prefill(inp)
+    assert rel_err(f64(o), ref_o) <= TOL["bf16"]
+    assert rel_err(f64(S), ref_S) <= TOL["bf16"]
