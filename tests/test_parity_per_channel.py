@@ -215,6 +215,39 @@ def test_tensor_path_empty_sequences_keep_their_state(lens):
     check(inp, per_sequence=True)
 
 
+def test_tensor_path_in_place_state_graph_capture_and_repeated_calls():
+    # S_final may be S0 (each chain thread reads its entries of S0 before it writes the same
+    # entries of S_final); calls on one workspace give identical bits; the call captures
+    # into a CUDA graph on one stream and its replay gives the same bits again
+    inp = inputs.prefill_inputs([300, 77, 64], H=2, dk=128, dv=128, dtype="bf16", seed=655,
+                                s0_std=0.3, gate="default", decay="channel")
+    d = lambda t: None if t is None else t.cuda()
+    q, k, v, la, b, S0, cu = map(d, (inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0,
+                                     inp.cu_seqlens))
+    n, T = inp.num_seqs, inp.total_tokens
+    ws = torch.empty(ops.chunk_fwd_workspace_size(n, T, 2, 128, 128, decay="channel"),
+                     dtype=torch.uint8, device="cuda")
+    o_e, S_e = chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, workspace=ws)
+    o_e2, S_e2 = chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, workspace=ws)
+    S_io = S0.clone()
+    o_io, _ = chunk_fwd(q, k, v, la, b, S0=S_io, cu_seqlens=cu, S_final=S_io, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o_e, o_e2) and torch.equal(S_e, S_e2)
+    assert torch.equal(o_io, o_e) and torch.equal(S_io, S_e)
+    o, S = torch.empty_like(o_e), torch.empty_like(S_e)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ops.chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, o=o, S_final=S, workspace=ws,
+                      stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_e) and torch.equal(S, S_e)
+    assert ops.read_device_status(ws) == 0
+    o_ref, S_ref = oracle_prefill(inp)
+    assert rel_err(f64(o_e), o_ref) <= TOL["bf16"] and rel_err(f64(S_e), S_ref) <= TOL["bf16"]
+
+
 def test_log_alpha_shape_is_checked():
     inp = inputs.prefill_inputs([64], H=2, dk=64, dv=64, dtype="f32", seed=615)
     c = lambda t: t.cuda()
