@@ -83,8 +83,14 @@ int launch_prefill_channel_tc(const PrefillArgs &a, const WsLayout &L) {
     cp.AT = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.T);
     cp.G = reinterpret_cast<float *>(a.ws + L.G);
     channel_wait_policy(cp);
+    // persistent CTAs, as many as are resident at once
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    const int64_t resident = (int64_t)channel::kCtasPerSm * sms;
     cudaLaunchConfig_t pcfg = {};
-    pcfg.gridDim = dim3((unsigned)L.max_chunks, (unsigned)a.H);
+    pcfg.gridDim = dim3((unsigned)(units < resident ? units : resident));
     pcfg.blockDim = dim3(channel::kThreads);
     pcfg.dynamicSmemBytes = channel::SMEM_BYTES;
     pcfg.stream = a.stream;

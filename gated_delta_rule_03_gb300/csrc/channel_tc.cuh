@@ -24,8 +24,9 @@
 // W = T K' with column c scaled by exp(g_r[c]) on the way out (exp(0) without the
 // factored Gram).
 //
-// One CTA of four warps per unit, four CTAs per SM (52 KB of shared memory and 128 TMEM
-// columns each); TMEM lane quarter w belongs to warp w. Outputs (the chain kernel loads
+// Four warps per CTA, four CTAs per SM (52 KB of shared memory and 128 TMEM columns each),
+// each CTA taking units blockIdx.x, blockIdx.x + gridDim.x, ... in turn; TMEM lane quarter
+// w belongs to warp w. Outputs (the chain kernel loads
 // them by TMA, 128-byte swizzled 64 x 64 boxes):
 //   QW [units * 64][256] bf16: e^g . Q in columns 0..127, -W in columns 128..255;
 //   KT [units * 64][128] bf16: e^{g_C - g} . K;
@@ -99,6 +100,14 @@ __device__ __forceinline__ float sw_elem(const unsigned char *block, int row, in
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(block + sw128_offset(row, col)));
 }
 
+// Brings `bytes` (a multiple of 16) at the 16-byte-aligned global address `ptr` into L2;
+// a hint with no completion to wait for.
+__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // The two bf16 halves of a packed pair, as fp32 (exact).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -156,7 +165,7 @@ __device__ __forceinline__ void store_t_prime(const float *__restrict__ U, const
     }
 }
 
-// The unit (chunk blockIdx.x, head blockIdx.y). map_q, map_k, map_v: the inputs.
+// A persistent CTA over units (chunk-major, head-minor). map_q, map_k, map_v: the inputs.
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const ChannelParams p) {
@@ -164,7 +173,6 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, h = blockIdx.y;
     float *misc = reinterpret_cast<float *>(sm + P_MISC);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P_TMEM);
     auto bar = [&](int i) { return sb + P_BARS + 8u * (uint32_t)i; };
@@ -190,29 +198,47 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     griddep_wait();
     griddep_launch_dependents();
     const int n_chunks = p.ctl[0] == GDR_OK ? p.ctl[1] : 0;
-    const bool live = c < n_chunks;
+    const int64_t n_units = (int64_t)n_chunks * p.H;
     bool fail = false;
-    if (live) {
+    // Barrier phases (a barrier completes once for each unit that uses it), and (thread 0,
+    // which issues every copy) the copies issued and not yet seen landed: a failure drains
+    // those before the shared memory goes.
+    uint32_t ph_kq = 0, ph_gram = 0, ph_mma = 0, ph_v = 0;
+    bool kq_pending = false, v_pending = false;
+    // the keys and queries of unit x (chunk-major, head-minor), whose first token is t0x,
+    // unless the test knob drops them; thread 0
+    auto issue_kq = [&](int64_t x, int t0x) {
+        const int cx = (int)(x / p.H), hx = (int)(x % p.H);
+        if (cx == p.fault_chunk && hx == 0) return;
+        mbar_arrive_expect_tx(bar(0), 4 * 8192);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(sb + P_KQ + 16384 * b, &map_k, bar(0), 64 * b, hx, t0x);
+            tma_load_3d(sb + P_KQ + 16384 * b + 8192, &map_q, bar(0), 64 * b, hx, t0x);
+        }
+        kq_pending = true;
+    };
+    if (tid == 0 && (int64_t)blockIdx.x < n_units) issue_kq(blockIdx.x, p.plan[blockIdx.x / p.H].y);
+    // Units blockIdx.x, blockIdx.x + gridDim.x, ...: the next unit's keys and queries are
+    // copied in while this one's outputs are stored.
+    for (int64_t x = blockIdx.x; x < n_units; x += gridDim.x) {
+        const int c = (int)(x / p.H), h = (int)(x % p.H);
         const int4 pl = p.plan[c];
         const int t0 = pl.y, len = pl.z;
-        const size_t u = (size_t)c * p.H + h;  // chunk-major, head-minor
-        // (thread 0 issues every copy and drains them after a failure)
-        const bool kq_issued = !(c == p.fault_chunk && h == 0);
-        if (tid == 0 && kq_issued) {
-            mbar_arrive_expect_tx(bar(0), 4 * 8192);
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                tma_load_3d(sb + P_KQ + 16384 * b, &map_k, bar(0), 64 * b, h, t0);
-                tma_load_3d(sb + P_KQ + 16384 * b + 8192, &map_q, bar(0), 64 * b, h, t0);
-            }
-        }
-        // V over the query rows, once they are spent (thread 0 issues it and drains it)
-        bool v_issued = false;
+        const size_t u = (size_t)x;
+        const int64_t x_next = x + gridDim.x;
+        // the next unit's first token and length: thread 0 copies its keys and queries in,
+        // threads 0..63 bring its rates into L2, while this unit's outputs are stored
+        int4 pl_next = make_int4(0, 0, 0, 0);
+        if (tid < C && x_next < n_units) pl_next = p.plan[x_next / p.H];
+        const int t0_next = pl_next.y;
+        if (tid == 0) misc[M_FLAG] = 0.f;
+        // V over the query rows, once they are spent
         auto load_v = [&] {
             mbar_arrive_expect_tx(bar(3), 2 * 8192);
             tma_load_3d(sb + P_V, &map_v, bar(3), 0, h, t0);
             tma_load_3d(sb + P_V + 16384, &map_v, bar(3), 64, h, t0);
-            v_issued = true;
+            v_pending = true;
         };
         if (tid < C) misc[M_BETA + tid] = tid < len ? p.beta[(size_t)(t0 + tid) * p.H + h] : 0.f;
         // g by tiles: thread (o, grp) owns channels 8o .. 8o + 7 over tokens 8grp .. 8grp + 7
@@ -279,7 +305,12 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             col_ok = col_ok && -gr[e] < kFactorLogBound && gr[e] - gc[e] < kFactorLogBound;
         }
         const bool factored = __syncthreads_and(col_ok) != 0;
-        if (!wait(0, 0)) fail = true;
+        if (!wait(0, ph_kq)) {
+            fail = true;
+        } else {
+            ph_kq ^= 1;
+            kq_pending = false;
+        }
         fail = __syncthreads_or(fail) != 0;
         float *U = reinterpret_cast<float *>(sm + P_BLK);
         __nv_bfloat16 *arow = p.AT + (u * 2 + 1) * C * C;
@@ -401,7 +432,8 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     }
                     mma_commit(bar(1));
                 }
-                if (!wait(1, 0)) fail = true;
+                if (!wait(1, ph_gram)) fail = true;
+                ph_gram ^= 1;
                 // a Gram that did not complete is neither read nor written over
                 fail = __syncthreads_or(fail) != 0;
             }
@@ -468,7 +500,11 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             __syncthreads();
             // ---- W^T = K'^T T'^T (M = d_k) and Utilde^T = V^T T'^T (M = d_v)
             if (tid == 0) {
-                const bool v_ok = wait(3, 0);
+                const bool v_ok = wait(3, ph_v);
+                if (v_ok) {
+                    ph_v ^= 1;
+                    v_pending = false;
+                }
                 if (v_ok) {
                     tc_fence_after();
 #pragma unroll
@@ -487,10 +523,18 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             __syncthreads();
             const bool issued = misc[M_FLAG] == 0.f;
             if (!issued) fail = true;
-            if (issued && !wait(2, 0)) fail = true;
+            if (issued) {
+                if (!wait(2, ph_mma)) fail = true;
+                ph_mma ^= 1;
+            }
             tc_fence_after();
             fail = __syncthreads_or(fail) != 0;
             if (!fail) {
+                // the products have read K' and V: the next unit's keys and queries may land
+                if (tid == 0 && x_next < n_units) issue_kq(x_next, t0_next);
+                if (tid < pl_next.z)
+                    prefetch_l2(p.log_alpha + ((size_t)(t0_next + tid) * p.H + x_next % p.H) * DK,
+                                DK * sizeof(float));
                 // -W rows: lane j = d_k index of warp w's quarter; column t of W^T scaled by
                 // exp(sh_j); lanes j, j ^ 1 swap one value per token pair so that each store
                 // is a bf16 pair along d_k
@@ -528,14 +572,21 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 p.G[u * 384 + j] = fast_exp(misc[M_GC + j]);
             }
         }
-        if (fail && tid == 0) {
-            atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
-            // loads and MMAs still in flight land before the shared memory and TMEM go
-            if (kq_issued) wait(0, 0);
-            if (v_issued) wait(3, 0);
-            mma_commit(bar(4));
-            wait(4, 0);
+        if (fail) {
+            if (tid == 0) {
+                atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
+                // loads and MMAs still in flight land before the shared memory and TMEM go
+                if (kq_pending) wait(0, ph_kq);
+                if (v_pending) wait(3, ph_v);
+                mma_commit(bar(4));
+                wait(4, 0);
+            }
+            break;
         }
+        // the unit's TMEM columns, blocks and gates are free for the next one
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
     }
     tc_fence_before();
     __syncthreads();
