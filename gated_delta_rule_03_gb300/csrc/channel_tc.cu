@@ -50,16 +50,23 @@ int launch_prefill_channel_tc(const PrefillArgs &a, const WsLayout &L) {
     }
     if (a.dk != channel::DK || a.dv != channel::DV) return GDR_ERR_UNSUPPORTED;
     const int64_t units = L.max_chunks * a.H;
-    CUtensorMap mq, mk, mv, mo, mqw, mkt, mut, mt;
+    CUtensorMap mq, mk, mv, mla, mo, mqw, mkt, mut, mt;
     if (!tc::make_map_thd(&mq, a.q, a.dk, a.H, a.total_tokens) ||
         !tc::make_map_thd(&mk, a.k, a.dk, a.H, a.total_tokens) ||
         !tc::make_map_thd(&mv, a.v, a.dv, a.H, a.total_tokens) ||
+
         !tc::make_map_thd(&mo, a.o, a.dv, a.H, a.total_tokens) ||
         !tc::make_map_thd(&mqw, a.ws + L.QW, 256, 1, units * kChunk) ||
         !tc::make_map_thd(&mkt, a.ws + L.KT, 128, 1, units * kChunk) ||
         !tc::make_map_thd(&mut, a.ws + L.UT, kChunk, 1, units * 128) ||
         !tc::make_map_units(&mt, a.ws + L.T, 2 * units))
         return GDR_ERR_CUDA;
+    // log_alpha need only be 4-byte aligned: 16-byte loads of it, and its tensor map for
+    // the L2 prefetch, where its base is 16-byte aligned
+    const bool rates_vec = ((uintptr_t)a.log_alpha & 15u) == 0;
+    const bool rates_map = rates_vec &&
+                           tc::make_map_rows_f32(&mla, a.log_alpha, a.dk, a.H, a.total_tokens);
+    if (!rates_map) mla = mq;  // (not read)
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
@@ -82,6 +89,8 @@ int launch_prefill_channel_tc(const PrefillArgs &a, const WsLayout &L) {
     cp.UT = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.UT);
     cp.AT = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.T);
     cp.G = reinterpret_cast<float *>(a.ws + L.G);
+    cp.rates_vec = rates_vec;
+    cp.prefetch_rates = rates_map;
     channel_wait_policy(cp);
     // persistent CTAs, as many as are resident at once
     int dev = 0, sms = 0;
@@ -96,7 +105,7 @@ int launch_prefill_channel_tc(const PrefillArgs &a, const WsLayout &L) {
     pcfg.stream = a.stream;
     pcfg.attrs = &attr;
     pcfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&pcfg, channel::channel_prep_kernel, mq, mk, mv, cp) != cudaSuccess)
+    if (cudaLaunchKernelEx(&pcfg, channel::channel_prep_kernel, mq, mk, mv, mla, cp) != cudaSuccess)
         return GDR_ERR_CUDA;
 
     // the chains, one CTA per (sequence, head), a programmatic dependent of the above

@@ -91,6 +91,9 @@ struct ChannelParams {
     __nv_bfloat16 *QW, *KT, *UT, *AT;
     float *G;
     long long wait_cycles;   // bound of every wait (SM cycles)
+    int rates_vec;           // log_alpha starts on a 16-byte boundary (every row then does):
+                             // its rows are read 16 bytes at a time, else 4
+    int prefetch_rates;      // map_la is a tensor map of log_alpha (needs a 16-byte base)
     int fault_chunk;         // test knob: head 0's CTA of this chunk skips its key and query
                              // loads, so that its wait gives up (-1: never)
 };
@@ -100,11 +103,10 @@ __device__ __forceinline__ float sw_elem(const unsigned char *block, int row, in
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(block + sw128_offset(row, col)));
 }
 
-// Brings `bytes` (a multiple of 16) at the 16-byte-aligned global address `ptr` into L2;
-// a hint with no completion to wait for.
-__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)),
-                 "r"(bytes)
+// Brings the box of `map` at (c0, c1, c2) into L2: a hint with no completion to wait for.
+__device__ __forceinline__ void prefetch_box_l2(const CUtensorMap *map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
 }
 
@@ -165,10 +167,12 @@ __device__ __forceinline__ void store_t_prime(const float *__restrict__ U, const
     }
 }
 
-// A persistent CTA over units (chunk-major, head-minor). map_q, map_k, map_v: the inputs.
+// A persistent CTA over units (chunk-major, head-minor). map_q, map_k, map_v: the inputs;
+// map_la: the rates, when p.prefetch_rates (used only to bring the next unit's into L2).
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                    const __grid_constant__ CUtensorMap map_v, const ChannelParams p) {
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_la,
+                    const ChannelParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
@@ -184,6 +188,7 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         prefetch_tensormap(&map_q);
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_v);
+        if (p.prefetch_rates) prefetch_tensormap(&map_la);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tslot), TM_COLS);
@@ -227,11 +232,9 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         const int t0 = pl.y, len = pl.z;
         const size_t u = (size_t)x;
         const int64_t x_next = x + gridDim.x;
-        // the next unit's first token and length: thread 0 copies its keys and queries in,
-        // threads 0..63 bring its rates into L2, while this unit's outputs are stored
-        int4 pl_next = make_int4(0, 0, 0, 0);
-        if (tid < C && x_next < n_units) pl_next = p.plan[x_next / p.H];
-        const int t0_next = pl_next.y;
+        // the next unit's first token: thread 0 copies its keys and queries in and brings
+        // its rates into L2 while this unit's outputs are stored
+        const int t0_next = (tid == 0 && x_next < n_units) ? p.plan[x_next / p.H].y : 0;
         if (tid == 0) misc[M_FLAG] = 0.f;
         // V over the query rows, once they are spent
         auto load_v = [&] {
@@ -253,10 +256,14 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 const int t = 8 * grp + j;
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
                 if (t < len) {
-                    const float4 *src = reinterpret_cast<const float4 *>(
-                        p.log_alpha + ((size_t)(t0 + t) * p.H + h) * DK + 8 * o);
-                    a = src[0];
-                    b = src[1];
+                    const float *src = p.log_alpha + ((size_t)(t0 + t) * p.H + h) * DK + 8 * o;
+                    if (p.rates_vec) {
+                        a = reinterpret_cast<const float4 *>(src)[0];
+                        b = reinterpret_cast<const float4 *>(src)[1];
+                    } else {
+                        a = make_float4(src[0], src[1], src[2], src[3]);
+                        b = make_float4(src[4], src[5], src[6], src[7]);
+                    }
                 }
                 acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
                 acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
@@ -531,10 +538,10 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             fail = __syncthreads_or(fail) != 0;
             if (!fail) {
                 // the products have read K' and V: the next unit's keys and queries may land
-                if (tid == 0 && x_next < n_units) issue_kq(x_next, t0_next);
-                if (tid < pl_next.z)
-                    prefetch_l2(p.log_alpha + ((size_t)(t0_next + tid) * p.H + x_next % p.H) * DK,
-                                DK * sizeof(float));
+                if (tid == 0 && x_next < n_units) {
+                    issue_kq(x_next, t0_next);
+                    if (p.prefetch_rates) prefetch_box_l2(&map_la, 0, (int)(x_next % p.H), t0_next);
+                }
                 // -W rows: lane j = d_k index of warp w's quarter; column t of W^T scaled by
                 // exp(sh_j); lanes j, j ^ 1 swap one value per token pair so that each store
                 // is a bf16 pair along d_k

@@ -150,13 +150,15 @@ EncodeTiledFn encode_fn() {
 }
 
 bool encode_3d(CUtensorMap *map, const void *base, const cuuint64_t (&dims)[3],
-               const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3]) {
+               const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3],
+               CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint32_t elem[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-              elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(map, type, 3, const_cast<void *>(base), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -168,6 +170,14 @@ bool make_map_thd(CUtensorMap *map, const void *base, int d, int H, int64_t T) {
     const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * H * 2};
     const cuuint32_t box[3] = {64, 1, 64};
     return encode_3d(map, base, dims, strides, box);
+}
+
+bool make_map_rows_f32(CUtensorMap *map, const float *base, int d, int H, int64_t T) {
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)d * H * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)d, 1, 64};
+    return encode_3d(map, base, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 bool make_map_units(CUtensorMap *map, const void *base, int64_t units) {

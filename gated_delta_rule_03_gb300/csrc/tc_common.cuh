@@ -80,6 +80,9 @@ __device__ __forceinline__ ChunkScan chunk_scan(float a0, float a1, int lane) {
 bool make_map_thd(CUtensorMap *map, const void *base, int d, int H, int64_t T);
 // Tensor map over [units][64][64] bf16 matrices, one whole matrix per box, 128-byte swizzle.
 bool make_map_units(CUtensorMap *map, const void *base, int64_t units);
+// Tensor map over a packed [T, H, d] fp32 tensor with d (features) x 1 (head) x 64 (tokens)
+// boxes, no swizzle (d * 4 a multiple of 16, d at most 256).
+bool make_map_rows_f32(CUtensorMap *map, const float *base, int d, int H, int64_t T);
 
 // The chunk-parallel solve: T' and A^T for every (chunk, head) of one phase into the
 // workspace, on `stream`, with at most max_ctas CTAs (all SMs when max_ctas <= 0);

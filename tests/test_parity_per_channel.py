@@ -248,6 +248,26 @@ def test_tensor_path_in_place_state_graph_capture_and_repeated_calls():
     assert rel_err(f64(o_e), o_ref) <= TOL["bf16"] and rel_err(f64(S_e), S_ref) <= TOL["bf16"]
 
 
+def test_tensor_path_rates_at_a_4_byte_offset():
+    # log_alpha needs only 4-byte alignment; at an offset that is not a multiple of 16
+    # bytes the operands kernel has no tensor map of it (no L2 prefetch), same results
+    inp = inputs.prefill_inputs([300, 77], H=2, dk=128, dv=128, dtype="bf16", seed=656,
+                                s0_std=0.3, gate="default", decay="channel")
+    d = lambda t: None if t is None else t.cuda()
+    flat = torch.empty(inp.log_alpha.numel() + 1, dtype=torch.float32, device="cuda")
+    la_off = flat[1:].view(inp.log_alpha.shape)
+    la_off.copy_(inp.log_alpha)
+    assert la_off.data_ptr() % 16 == 4
+    o, S = chunk_fwd(d(inp.q), d(inp.k), d(inp.v), la_off, d(inp.beta), S0=d(inp.S0),
+                     cu_seqlens=d(inp.cu_seqlens))
+    o_a, S_a = chunk_fwd(d(inp.q), d(inp.k), d(inp.v), d(inp.log_alpha), d(inp.beta),
+                         S0=d(inp.S0), cu_seqlens=d(inp.cu_seqlens))
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_a) and torch.equal(S, S_a)
+    o_ref, S_ref = oracle_prefill(inp)
+    assert rel_err(f64(o), o_ref) <= TOL["bf16"] and rel_err(f64(S), S_ref) <= TOL["bf16"]
+
+
 def test_log_alpha_shape_is_checked():
     inp = inputs.prefill_inputs([64], H=2, dk=64, dv=64, dtype="f32", seed=615)
     c = lambda t: t.cuda()
