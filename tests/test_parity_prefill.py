@@ -279,3 +279,29 @@ def test_near_zero_decay_tokens(dtype):
     la[idx, :] = -1.0e4
     inp.log_alpha.copy_(la)
     check(inp, per_sequence=True)
+
+
+@pytest.mark.parametrize("dtype,dk,lens", [("bf16", 128, [512, 512]), ("bf16", 128, [300, 77]),
+                                           ("f32", 64, [300, 77])])
+def test_gates_at_a_4_byte_offset(dtype, dk, lens):
+    # log_alpha and beta need only 4-byte alignment (per-token slices of a larger buffer):
+    # the fused, phased and exact paths read them at any such offset, same bits
+    inp = inputs.prefill_inputs(lens, H=2, dk=dk, dv=dk, dtype=dtype, seed=57, s0_std=0.2,
+                                gate="slow")
+    d = lambda t: None if t is None else t.cuda()
+
+    def shifted(t):
+        flat = torch.empty(t.numel() + 1, dtype=torch.float32, device="cuda")
+        out = flat[1:].view(t.shape)
+        out.copy_(t)
+        assert out.data_ptr() % 16 == 4
+        return out
+
+    args = (d(inp.q), d(inp.k), d(inp.v))
+    kw = dict(S0=d(inp.S0), cu_seqlens=d(inp.cu_seqlens), num_seqs=inp.num_seqs)
+    o, S = chunk_fwd(*args, shifted(inp.log_alpha), shifted(inp.beta), **kw)
+    o_a, S_a = chunk_fwd(*args, d(inp.log_alpha), d(inp.beta), **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_a) and torch.equal(S, S_a)
+    ref_o, ref_S = oracle_prefill(inp)
+    assert rel_err(f64(o), ref_o) <= TOL[dtype] and rel_err(f64(S), ref_S) <= TOL[dtype]
