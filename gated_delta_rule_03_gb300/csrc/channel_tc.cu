@@ -72,9 +72,11 @@ int launch_prefill_channel_tc(const PrefillArgs &a, const WsLayout &L) {
     attr.val.programmaticStreamSerializationAllowed = 1;
 
     // every unit's operands, a programmatic dependent of the planning kernel
-    if (cudaFuncSetAttribute(channel::channel_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // the plain kernel or the one with the layer prologue folded in
+    auto prep = a.prologue ? channel::channel_prep_kernel<true> : channel::channel_prep_kernel<false>;
+    if (cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)channel::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(channel::channel_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+        cudaFuncSetAttribute(prep, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return GDR_ERR_CUDA;
     channel::ChannelParams cp = {};
@@ -84,6 +86,7 @@ int launch_prefill_channel_tc(const PrefillArgs &a, const WsLayout &L) {
     cp.ctl = reinterpret_cast<int32_t *>(a.ws + L.ctl);
     cp.H = a.H;
     cp.additive = a.rule == GDR_RULE_ADDITIVE;
+    cp.gate_A = a.gate_A;
     cp.QW = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.QW);
     cp.KT = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.KT);
     cp.UT = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.UT);
@@ -105,7 +108,7 @@ int launch_prefill_channel_tc(const PrefillArgs &a, const WsLayout &L) {
     pcfg.stream = a.stream;
     pcfg.attrs = &attr;
     pcfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&pcfg, channel::channel_prep_kernel, mq, mk, mv, mla, cp) != cudaSuccess)
+    if (cudaLaunchKernelEx(&pcfg, prep, mq, mk, mv, mla, cp) != cudaSuccess)
         return GDR_ERR_CUDA;
 
     // the chains, one CTA per (sequence, head), a programmatic dependent of the above

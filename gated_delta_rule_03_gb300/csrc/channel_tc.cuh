@@ -24,10 +24,16 @@
 // W = T K' with column c scaled by exp(g_r[c]) on the way out (exp(0) without the
 // factored Gram).
 //
+// With the layer prologue ("Linear attention", "A naive PyTorch implementation") the rates
+// and beta arrive as pre-activations, log alpha = -A_h softplus(a) per channel and
+// beta = sigmoid(b), and q, k are scaled to unit length per token: the kernel takes the
+// norms from the staged bf16 rows and scales every row it writes, so that the chain
+// needs no change.
+//
 // Four warps per CTA, four CTAs per SM (52 KB of shared memory and 128 TMEM columns each),
 // each CTA taking units blockIdx.x, blockIdx.x + gridDim.x, ... in turn; TMEM lane quarter
-// w belongs to warp w. Outputs (the chain kernel loads
-// them by TMA, 128-byte swizzled 64 x 64 boxes):
+// w belongs to warp w. Outputs (the chain kernel loads them by TMA, 128-byte swizzled
+// 64 x 64 boxes):
 //   QW [units * 64][256] bf16: e^g . Q in columns 0..127, -W in columns 128..255;
 //   KT [units * 64][128] bf16: e^{g_C - g} . K;
 //   UT [units * 128][64] bf16: Utilde^T (row j: value column j over the chunk's tokens);
@@ -69,9 +75,10 @@ constexpr uint32_t P_KC = 32768;   // the Gram's B operand K'': two 64-column ha
 constexpr uint32_t P_BLK = P_KC;   // the unit's 16 x 16 blocks (the solve's layout)
 constexpr uint32_t P_TP = P_KC;    // T' bf16 [t][i], 128-byte swizzled
 constexpr uint32_t P_MISC = P_KC + (solve::UNIT_FLOATS * 4 + 1023) / 1024 * 1024;
-                                   // floats: beta[64], g_C[128], g_r[128], (128 spare),
+                                   // floats: beta[64], g_C[128], g_r[128], the prologue's
+                                   // 1/|k_t|[64] and 1/|q_t|[64],
                                    // the "V load gave up" flag
-constexpr int M_BETA = 0, M_GC = 64, M_GREF = 192, M_HSUM = 320, M_FLAG = 448;
+constexpr int M_BETA = 0, M_GC = 64, M_GREF = 192, M_RK = 320, M_RQ = 384, M_FLAG = 448;
 constexpr uint32_t P_BARS = P_MISC + 456 * 4;  // load, Gram, products, V reload, drain
 constexpr uint32_t P_TMEM = P_BARS + 40;
 constexpr uint32_t P_USED = P_TMEM + 16;
@@ -88,6 +95,7 @@ struct ChannelParams {
     int32_t *ctl;
     int H;
     int additive;            // the additive rule: L = 0, W = 0
+    const float *gate_A;     // the layer prologue's per-head rate A_h (null: 1)
     __nv_bfloat16 *QW, *KT, *UT, *AT;
     float *G;
     long long wait_cycles;   // bound of every wait (SM cycles)
@@ -169,6 +177,9 @@ __device__ __forceinline__ void store_t_prime(const float *__restrict__ U, const
 
 // A persistent CTA over units (chunk-major, head-minor). map_q, map_k, map_v: the inputs;
 // map_la: the rates, when p.prefetch_rates (used only to bring the next unit's into L2).
+// kPro: the layer prologue (a compile-time variant, so that the plain path carries none
+// of its work).
+template <bool kPro>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_la,
@@ -243,7 +254,15 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             tma_load_3d(sb + P_V + 16384, &map_v, bar(3), 64, h, t0);
             v_pending = true;
         };
-        if (tid < C) misc[M_BETA + tid] = tid < len ? p.beta[(size_t)(t0 + tid) * p.H + h] : 0.f;
+        if (tid < C) {
+            float bt = 0.f;
+            if (tid < len) {
+                bt = p.beta[(size_t)(t0 + tid) * p.H + h];
+                if (kPro) bt = prologue_beta(bt);
+            }
+            misc[M_BETA + tid] = bt;
+        }
+        const float gate_a = kPro && p.gate_A ? p.gate_A[h] : 1.f;
         // g by tiles: thread (o, grp) owns channels 8o .. 8o + 7 over tokens 8grp .. 8grp + 7
         const int o = tid & 15, grp = tid >> 4;
         float g[8][8];
@@ -263,6 +282,12 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     } else {
                         a = make_float4(src[0], src[1], src[2], src[3]);
                         b = make_float4(src[4], src[5], src[6], src[7]);
+                    }
+                    if (kPro) {  // log alpha = -A_h softplus(a), per channel
+                        a = make_float4(prologue_log_alpha(a.x, gate_a), prologue_log_alpha(a.y, gate_a),
+                                        prologue_log_alpha(a.z, gate_a), prologue_log_alpha(a.w, gate_a));
+                        b = make_float4(prologue_log_alpha(b.x, gate_a), prologue_log_alpha(b.y, gate_a),
+                                        prologue_log_alpha(b.z, gate_a), prologue_log_alpha(b.w, gate_a));
                     }
                 }
                 acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
@@ -319,6 +344,38 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             kq_pending = false;
         }
         fail = __syncthreads_or(fail) != 0;
+        if (!fail && kPro) {
+            // 1/|k_t| and 1/|q_t| from the staged bf16 rows: the 16 threads of a token group
+            // (one half-warp) each sum 8 channels, then combine
+            const int b = o >> 3, cc = o & 7;
+            const unsigned char *kh = sm + P_KQ + 16384 * b, *qh = kh + 8192;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int t = 8 * grp + j;
+                const uint32_t off = (uint32_t)(t * 128 + ((cc ^ (t & 7)) << 4));
+                const uint4 kr = *reinterpret_cast<const uint4 *>(kh + off);
+                const uint4 qr = *reinterpret_cast<const uint4 *>(qh + off);
+                const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, qv[4] = {qr.x, qr.y, qr.z, qr.w};
+                float sk = 0.f, sq = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float k0 = bf16_lo(kw[w]), k1 = bf16_hi(kw[w]);
+                    const float q0 = bf16_lo(qv[w]), q1 = bf16_hi(qv[w]);
+                    sk = fmaf(k0, k0, fmaf(k1, k1, sk));
+                    sq = fmaf(q0, q0, fmaf(q1, q1, sq));
+                }
+#pragma unroll
+                for (int off2 = 1; off2 < 16; off2 <<= 1) {
+                    sk += __shfl_xor_sync(0xffffffffu, sk, off2);
+                    sq += __shfl_xor_sync(0xffffffffu, sq, off2);
+                }
+                if (o == 0) {
+                    misc[M_RK + t] = prologue_inv_norm(sk);
+                    misc[M_RQ + t] = prologue_inv_norm(sq);
+                }
+            }
+            __syncthreads();
+        }
         float *U = reinterpret_cast<float *>(sm + P_BLK);
         __nv_bfloat16 *arow = p.AT + (u * 2 + 1) * C * C;
         if (!fail && !factored) {
@@ -344,6 +401,11 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                         const float ki = sw_elem(half, i, d & 63) * f;
                         kk = fmaf(sw_elem(half, t, d & 63), ki, kk);
                         qk = fmaf(sw_elem(half + 8192, t, d & 63), ki, qk);
+                    }
+                    if (kPro) {
+                        const float rki = misc[M_RK + i];
+                        kk *= misc[M_RK + t] * rki;
+                        qk *= misc[M_RQ + t] * rki;
                     }
                     if (i < t && !p.additive) U[blk(t >> 4, i >> 4) + el(t & 15, i & 15)] = misc[M_BETA + t] * kk;
                 }
@@ -378,11 +440,12 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     const uint4 kr = *reinterpret_cast<const uint4 *>(kh + off);
                     const uint4 qr = *reinterpret_cast<const uint4 *>(qh + off);
                     const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, qv[4] = {qr.x, qr.y, qr.z, qr.w};
+                    const float rk = kPro ? misc[M_RK + t] : 1.f, rq = kPro ? misc[M_RQ + t] : 1.f;
                     uint32_t o_qw[4], o_kt[4], o_k1[4], o_q1[4], o_k2[4];
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
-                        const float k0 = bf16_lo(kw[w]), k1 = bf16_hi(kw[w]);
-                        const float q0 = bf16_lo(qv[w]), q1 = bf16_hi(qv[w]);
+                        const float k0 = bf16_lo(kw[w]) * rk, k1 = bf16_hi(kw[w]) * rk;
+                        const float q0 = bf16_lo(qv[w]) * rq, q1 = bf16_hi(qv[w]) * rq;
                         const int e0 = 2 * w, e1 = 2 * w + 1;
                         const float s0 = fast_exp2(fmaf(g[j][e0], kLog2e, shl[e0]));
                         const float s1 = fast_exp2(fmaf(g[j][e1], kLog2e, shl[e1]));
@@ -408,11 +471,12 @@ channel_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     const uint4 kr = *reinterpret_cast<const uint4 *>(kh + off);
                     const uint4 qr = *reinterpret_cast<const uint4 *>(qh + off);
                     const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, qv[4] = {qr.x, qr.y, qr.z, qr.w};
+                    const float rk = kPro ? misc[M_RK + t] : 1.f, rq = kPro ? misc[M_RQ + t] : 1.f;
                     uint32_t o_qw[4], o_kt[4], o_k1[4];
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
-                        const float k0 = bf16_lo(kw[w]), k1 = bf16_hi(kw[w]);
-                        const float q0 = bf16_lo(qv[w]), q1 = bf16_hi(qv[w]);
+                        const float k0 = bf16_lo(kw[w]) * rk, k1 = bf16_hi(kw[w]) * rk;
+                        const float q0 = bf16_lo(qv[w]) * rq, q1 = bf16_hi(qv[w]) * rq;
                         const int e0 = 2 * w, e1 = 2 * w + 1;
                         const float x0 = fast_exp(g[j][e0]), x1 = fast_exp(g[j][e1]);
                         o_qw[w] = pack_bf16x2(q0 * x0, q1 * x1);

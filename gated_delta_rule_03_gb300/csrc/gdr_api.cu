@@ -17,7 +17,8 @@ bool use_tensor_path(int dk, int dv, int dtype) {
 }
 
 bool use_channel_tc(int dk, int dv, int dtype, int prologue) {
-    return dtype == GDR_BF16 && dk == 128 && dv == 128 && prologue == GDR_PROLOGUE_NONE;
+    (void)prologue;  // the operands kernel folds the prologue in
+    return dtype == GDR_BF16 && dk == 128 && dv == 128;
 }
 
 WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv, int dtype,

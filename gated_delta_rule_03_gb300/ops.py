@@ -192,8 +192,8 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, num_seqs=None,
 
     q, k [T, H, dk]; v [T, H, dv] (fp32 or bf16); beta [T, H] fp32; log_alpha [T, H]
     fp32 (one rate per head), or [T, H, dk] (one rate per key channel, gdr_options.decay
-    GDR_DECAY_CHANNEL: tensor cores for bf16 with dk = dv = 128 and no prologue, else
-    the exact fp32 path);
+    GDR_DECAY_CHANNEL: tensor cores for bf16 with dk = dv = 128, else the exact fp32
+    path);
     S0 [num_seqs, H, dk, dv] fp32 or None; cu_seqlens [num_seqs+1] int32 or None
     (then `num_seqs` equal sequences, default 1). Optional preallocated o,
     S_final and workspace (uint8) tensors are used as given. rule: "delta" (the gated

@@ -238,8 +238,8 @@ enum { GDR_RULE_DELTA = 0, GDR_RULE_ADDITIVE = 1 };
  *                    Kimi Delta Attention gives each feature channel its own rate).
  *                    With GDR_PROLOGUE_LAYER the pre-activation a has that shape too.
  *                    Prefill with per-channel rates takes the per-channel tensor-core
- *                    path (GDR_PATH_CHANNEL_TENSOR) for bf16 with d_k = d_v = 128 and
- *                    no prologue, else the exact fp32 path (GDR_PATH_EXACT);
+ *                    path (GDR_PATH_CHANNEL_TENSOR) for bf16 with d_k = d_v = 128,
+ *                    else the exact fp32 path (GDR_PATH_EXACT);
  *                    gdr_chunk_fwd_workspace_size_ex sizes the workspace of either,
  *                    and gdr_chunk_fwd_path_ex says which one a call takes. Other
  *                    values: GDR_ERR_INVALID_ARG.
@@ -349,7 +349,7 @@ int gdr_chunk_fwd_path(int d_k, int d_v, int dtype);
  * (decay = GDR_DECAY_CHANNEL) it is GDR_PATH_CHANNEL_TENSOR (bf16 tensor cores:
  * a planning kernel, a chunk-parallel kernel that builds every chunk's operands
  * with per-channel decay folded in, and a per-sequence chain kernel) for bf16
- * with d_k = d_v = 128 and no prologue, else GDR_PATH_EXACT. Host-only, no
+ * with d_k = d_v = 128, else GDR_PATH_EXACT. Host-only, no
  * CUDA call. Returns a negative status for unsupported sizes or options, as
  * gdr_chunk_fwd_ex would.
  */

@@ -163,9 +163,9 @@ def test_options_validated_on_the_host(lib):
 
 def test_per_channel_workspace_follows_the_path(lib):
     # per-channel rates: bf16 with d_k = d_v = 128 takes the per-channel tensor-core path,
-    # whose workspace holds every unit's operands; other sizes (and the prologue) take the
-    # exact path, whose layout adds one fp32 [C][d_k] block of cumulative log decay per
-    # unit. The plain query (head rates) is unchanged; bad options size nothing.
+    # whose workspace holds every unit's operands; other sizes take the exact path, whose
+    # layout adds one fp32 [C][d_k] block of cumulative log decay per unit. The plain query
+    # (head rates) is unchanged; bad options size nothing.
     from gated_delta_rule_03_gb300.ops import GdrOptions
     head = lib.gdr_chunk_fwd_workspace_size(4, 4 * 4096, 16, 128, 128, 64, 1)
     pc = GdrOptions(0)
@@ -177,11 +177,14 @@ def test_per_channel_workspace_follows_the_path(lib):
     # bf16), decayed K (64 x 128 bf16), U~^T (128 x 64 bf16)
     per_unit = 2 * 64 * 64 * 2 + 384 * 4 + 64 * 256 * 2 + 64 * 128 * 2 + 128 * 64 * 2
     assert units * per_unit <= chan <= units * per_unit + (1 << 20)
-    pc.prologue = 1
-    exact_pro = lib.gdr_chunk_fwd_workspace_size_ex(4, 4 * 4096, 16, 128, 128, 64, 1,
-                                                    ctypes.byref(pc))
+    pc.prologue = 1  # (the prologue keeps the tensor-core layout)
+    assert lib.gdr_chunk_fwd_workspace_size_ex(4, 4 * 4096, 16, 128, 128, 64, 1,
+                                               ctypes.byref(pc)) == chan
+    pc.prologue = 0
+    exact_chan = lib.gdr_chunk_fwd_workspace_size_ex(4, 4 * 4096, 16, 128, 128, 64, 0,
+                                                     ctypes.byref(pc))
     exact_f32 = lib.gdr_chunk_fwd_workspace_size(4, 4 * 4096, 16, 128, 128, 64, 0)
-    assert exact_pro >= exact_f32 + units * 64 * 128 * 4
+    assert exact_chan >= exact_f32 + units * 64 * 128 * 4
     bad = GdrOptions(0)
     bad.decay = 7
     assert lib.gdr_chunk_fwd_workspace_size_ex(1, 128, 2, 64, 64, 64, 0, ctypes.byref(bad)) == 0
@@ -200,7 +203,7 @@ def test_path_query_with_options(lib):
         assert fn(dk, dv, dt, opt()) == lib.gdr_chunk_fwd_path(dk, dv, dt)
     assert fn(128, 128, 1, None) == TENSOR
     assert fn(128, 128, 1, opt(decay=1)) == CHANNEL
-    assert fn(128, 128, 1, opt(decay=1, prologue=1)) == EXACT
+    assert fn(128, 128, 1, opt(decay=1, prologue=1)) == CHANNEL
     assert fn(128, 256, 1, opt(decay=1)) == EXACT
     assert fn(128, 128, 0, opt(decay=1)) == EXACT
     assert fn(64, 64, 1, opt(decay=1)) == EXACT

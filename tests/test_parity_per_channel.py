@@ -268,6 +268,33 @@ def test_tensor_path_rates_at_a_4_byte_offset():
     assert rel_err(f64(o), o_ref) <= TOL["bf16"] and rel_err(f64(S), S_ref) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("steep", [False, True])
+def test_tensor_path_prologue(steep):
+    # raw q, k and per-channel gate pre-activations on the tensor-core path; steep: rates
+    # large enough that chunks take the exact element-wise Gram
+    rng = np.random.default_rng(657 + steep)
+    lens, H, dk = [300, 64, 33], 2, 128
+    T = sum(lens)
+    assert ops.chunk_fwd_path(dk, dk, torch.bfloat16, "channel", prologue=True) == \
+        ops.PATH_CHANNEL_TENSOR
+    st = lambda x: torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    q, k = st(rng.standard_normal((T, H, dk))), st(3.0 * rng.standard_normal((T, H, dk)))
+    v = st(rng.standard_normal((T, H, dk)))
+    a = torch.from_numpy((rng.standard_normal((T, H, dk)) + (3.0 if steep else -4.0)).astype(np.float32))
+    b = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32))
+    A = torch.from_numpy(rng.uniform(0.2, 2.0, H).astype(np.float32))
+    S0 = torch.from_numpy((0.3 * rng.standard_normal((3, H, dk, dk))).astype(np.float32))
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    c = lambda t: t.cuda()
+    o, S = chunk_fwd(c(q), c(k), c(v), c(a), c(b), S0=c(S0), cu_seqlens=c(cu), prologue=True,
+                     gate_A=c(A))
+    torch.cuda.synchronize()
+    qn, kn, la, beta = oracle.layer_prologue(f64(q), f64(k), f64(a), f64(b), f64(A))
+    o_ref, S_ref = oracle.forward(qn, kn, f64(v), la, beta, S0=f64(S0),
+                                  cu_seqlens=cu.numpy().astype(np.int64))
+    assert rel_err(f64(o), o_ref) <= TOL["bf16"] and rel_err(f64(S), S_ref) <= TOL["bf16"]
+
+
 def test_log_alpha_shape_is_checked():
     inp = inputs.prefill_inputs([64], H=2, dk=64, dv=64, dtype="f32", seed=615)
     c = lambda t: t.cuda()
