@@ -88,13 +88,16 @@ def test_per_channel_chain_gives_up_on_a_missing_load_then_the_next_call_is_clea
     assert rel_err(f64(S), ref_S) <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("fault_chunk", [0, 6])
-def test_per_channel_operands_kernel_gives_up_then_the_next_call_is_clean(fault_chunk,
+@pytest.mark.parametrize("fault_chunk,lens,H", [(0, [300, 200], 2), (6, [300, 200], 2),
+                                                (70, [4096, 4096], 16)])
+def test_per_channel_operands_kernel_gives_up_then_the_next_call_is_clean(fault_chunk, lens, H,
                                                                          monkeypatch):
-    # GDR_DEBUG_PREP_FAULT=<chunk>: head 0's CTA of that chunk in the kernel that builds the
-    # per-channel operands skips its key and query loads; its wait runs out, it marks the
-    # status word and drains, and the chain after it writes nothing
-    inp = inputs.prefill_inputs([300, 200], H=2, dk=128, dv=128, dtype="bf16", seed=43,
+    # GDR_DEBUG_PREP_FAULT=<chunk>: head 0's unit of that chunk in the kernel that builds the
+    # per-channel operands gets no key and query loads; its wait runs out, its CTA marks
+    # the status word and drains, and the chain after it writes nothing. With 2,048 units
+    # (more than the kernel's resident CTAs) the dropped unit, 70 * 16 = 1,120, is its
+    # CTA's second: the copies were to be issued while the first unit's outputs were stored.
+    inp = inputs.prefill_inputs(lens, H=H, dk=128, dv=128, dtype="bf16", seed=43,
                                 s0_std=0.2, gate="slow", decay="channel")
     n, T = inp.num_seqs, inp.total_tokens
     dev = torch.device("cuda", 0)
@@ -105,6 +108,9 @@ def test_per_channel_operands_kernel_gives_up_then_the_next_call_is_clean(fault_
                      dtype=torch.uint8, device=dev)
     o = torch.full((T, inp.H, 128), float("nan"), dtype=torch.bfloat16, device=dev)
     S = torch.full((n, inp.H, 128, 128), float("nan"), device=dev)
+    if H == 16:  # the dropped unit is the second of its CTA on a 152-SM device
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        assert fault_chunk * H >= 4 * sms
 
     monkeypatch.setenv("GDR_DEBUG_PREP_FAULT", str(fault_chunk))
     t0 = time.perf_counter()
