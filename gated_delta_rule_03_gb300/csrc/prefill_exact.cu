@@ -379,14 +379,26 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     if (per_channel)
         for (int idx = tid; idx < C * DK; idx += blockDim.x)
             gcws[cb * C * DK + idx] = Gs[(idx / DK) * KP + idx % DK];
+    // Utilde = T V, 64 value columns at a time staged in shared memory over the queries
+    // (spent once the Gram is formed); padding rows of V are zero
     float *Uout = Uws + cb * C * dv;
-    for (int idx = tid; idx < C * dv; idx += blockDim.x) {
-        const int t = idx / dv, j = idx % dv;
-        float s = 0.f;
-        const int last = t < len ? t : len - 1;
-        for (int i = 0; i <= last; ++i)
-            s = fmaf(Tm[t * CP + i], to_f32(v[((size_t)(t0 + i) * H + h) * dv + j]), s);
-        Uout[idx] = s;
+    float *Vs = qs;  // [C][64 + 1]
+    constexpr int VB = 64, VP = VB + 1;
+    static_assert(VP <= KP, "a value block fits in the query tile");
+    for (int jb = 0; jb < dv; jb += VB) {
+        const int nb = dv - jb < VB ? dv - jb : VB;
+        __syncthreads();  // (the queries, or the previous block, are read)
+        for (int idx = tid; idx < C * VB; idx += blockDim.x) {
+            const int i = idx / VB, j = idx % VB;
+            Vs[i * VP + j] = (i < len && j < nb) ? to_f32(v[((size_t)(t0 + i) * H + h) * dv + jb + j]) : 0.f;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < C * nb; idx += blockDim.x) {
+            const int t = idx / nb, j = idx % nb;
+            float s = 0.f;
+            for (int i = 0; i <= t; ++i) s = fmaf(Tm[t * CP + i], Vs[i * VP + j], s);
+            Uout[t * dv + jb + j] = s;
+        }
     }
     float *Aout = Aws + cb * C * C;
     for (int idx = tid; idx < C * C; idx += blockDim.x) Aout[idx] = Am[(idx / C) * CP + idx % C];
