@@ -413,6 +413,16 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
 // ----------------------------------------------------------------------------- chain
 
 constexpr int kChainCols = 32;  // value columns per chain CTA
+constexpr int kChainThreads = 256;
+
+// Four consecutive elements at p (16-byte aligned for fp32, 8-byte for bf16) as fp32.
+__device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
 
 template <int DK> struct ChainSmem {
     static constexpr int KP = DK + 1;
@@ -423,7 +433,7 @@ template <int DK> struct ChainSmem {
 };
 
 template <typename Tin, int DK>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kChainThreads)
 exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const float *__restrict__ S0, const int32_t *__restrict__ cu,
                    int64_t num_seqs, int64_t total_tokens, int H, int dv,
@@ -475,29 +485,70 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         const int64_t tc0 = t_begin + (int64_t)cc * C;
         const int len = (int)((t_end - tc0) < C ? (t_end - tc0) : C);
         if (tid < 2 * C) nqk[tid] = gws[cb * 4 * C + 2 * C + tid];
-        __syncthreads();
-        for (int idx = tid; idx < C * DK; idx += blockDim.x) {
-            const int t = idx / DK, d = idx % DK;
-            Wc[t * KP + d] = Wws[cb * C * DK + idx];
-            float kv = 0.f, qv = 0.f;
+        // W, q and k, A and Utilde of the chunk: every load of a thread is issued before
+        // any is used, four elements at a time
+        constexpr int NK = C * DK / 4 / kChainThreads, NA = C * C / 4 / kChainThreads,
+                      NU = C * NC / 4 / kChainThreads;
+        float4 wv[NK], kv4[NK], qv4[NK], gv4[NK], gl4[NK], av[NA], uv[NU];
+#pragma unroll
+        for (int r = 0; r < NK; ++r) {
+            const int e = 4 * (tid + r * kChainThreads), t = e / DK, d = e % DK;
+            wv[r] = load4(Wws + cb * C * DK + e);
+            kv4[r] = qv4[r] = gv4[r] = gl4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (t < len) {
                 const size_t off = ((size_t)(tc0 + t) * H + h) * DK + d;
-                kv = to_f32(k[off]) * nqk[C + t];
-                qv = to_f32(q[off]) * nqk[t];
+                kv4[r] = load4(k + off);
+                qv4[r] = load4(q + off);
                 if (gcws) {
-                    const float *g = gcws + cb * C * DK;
-                    qv *= expf(g[t * DK + d]);
-                    kv *= expf(g[(C - 1) * DK + d] - g[t * DK + d]);
+                    gv4[r] = load4(gcws + cb * C * DK + t * DK + d);
+                    gl4[r] = load4(gcws + cb * C * DK + (C - 1) * DK + d);
                 }
             }
-            ks[t * KP + d] = kv;
-            qs[t * KP + d] = qv;
         }
-        for (int idx = tid; idx < C * C; idx += blockDim.x)
-            Ac[(idx / C) * CP + idx % C] = Aws[cb * C * C + idx];
-        for (int idx = tid; idx < C * NC; idx += blockDim.x) {
-            const int t = idx / NC, j = idx % NC;
-            Uc[t * SP + j] = Uws[cb * C * dv + (size_t)t * dv + j0 + j];
+#pragma unroll
+        for (int r = 0; r < NA; ++r) av[r] = load4(Aws + cb * C * C + 4 * (tid + r * kChainThreads));
+#pragma unroll
+        for (int r = 0; r < NU; ++r) {
+            const int e = 4 * (tid + r * kChainThreads), t = e / NC, j = e % NC;
+            uv[r] = load4(Uws + cb * C * dv + (size_t)t * dv + j0 + j);
+        }
+        __syncthreads();  // (nqk)
+#pragma unroll
+        for (int r = 0; r < NK; ++r) {
+            const int e = 4 * (tid + r * kChainThreads), t = e / DK, d = e % DK;
+            const float w4[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+            const float k4[4] = {kv4[r].x, kv4[r].y, kv4[r].z, kv4[r].w};
+            const float q4[4] = {qv4[r].x, qv4[r].y, qv4[r].z, qv4[r].w};
+            const float g4[4] = {gv4[r].x, gv4[r].y, gv4[r].z, gv4[r].w};
+            const float c4[4] = {gl4[r].x, gl4[r].y, gl4[r].z, gl4[r].w};
+            const float nk = t < len ? nqk[C + t] : 0.f, nq = t < len ? nqk[t] : 0.f;
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                float kv = k4[x] * nk, qv = q4[x] * nq;
+                if (gcws) {
+                    qv *= expf(g4[x]);
+                    kv *= expf(c4[x] - g4[x]);
+                }
+                Wc[t * KP + d + x] = w4[x];
+                ks[t * KP + d + x] = kv;
+                qs[t * KP + d + x] = qv;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < NA; ++r) {
+            const int e = 4 * (tid + r * kChainThreads), t = e / C, i = e % C;
+            Ac[t * CP + i] = av[r].x;
+            Ac[t * CP + i + 1] = av[r].y;
+            Ac[t * CP + i + 2] = av[r].z;
+            Ac[t * CP + i + 3] = av[r].w;
+        }
+#pragma unroll
+        for (int r = 0; r < NU; ++r) {
+            const int e = 4 * (tid + r * kChainThreads), t = e / NC, j = e % NC;
+            Uc[t * SP + j] = uv[r].x;
+            Uc[t * SP + j + 1] = uv[r].y;
+            Uc[t * SP + j + 2] = uv[r].z;
+            Uc[t * SP + j + 3] = uv[r].w;
         }
         if (tid < C) {
             gam[tid] = gws[cb * 4 * C + tid];
@@ -595,7 +646,7 @@ static int launch_exact_t(const PrefillArgs &a, const WsLayout &L) {
         if (e != cudaSuccess) return GDR_ERR_CUDA;
     }
     dim3 grid2((unsigned)(a.num_seqs * a.H), (unsigned)(a.dv / kChainCols));
-    exact_chain_kernel<Tin, DK><<<grid2, 256, ChainSmem<DK>::bytes, a.stream>>>(
+    exact_chain_kernel<Tin, DK><<<grid2, kChainThreads, ChainSmem<DK>::bytes, a.stream>>>(
         (const Tin *)a.q, (const Tin *)a.k, a.S0, a.cu_seqlens, a.num_seqs, a.total_tokens, a.H,
         a.dv, (const int32_t *)(a.ws + L.seq_chunk), ctl, W, U, A, g, gc, (Tin *)a.o, a.S_final);
     return cuda_status(cudaGetLastError());
