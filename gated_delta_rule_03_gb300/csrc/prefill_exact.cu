@@ -191,6 +191,17 @@ int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases) {
 
 // ----------------------------------------------------------------------------- prep
 
+// Four consecutive elements at p (16-byte aligned for fp32, 8-byte for bf16) as fp32.
+__device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+constexpr int kPrepThreads = 256;
+
 template <int DK> struct PrepSmem {
     static constexpr int KP = DK + 1;  // padded row pitch (floats)
     static constexpr int CP = kChunk + 1;
@@ -201,7 +212,7 @@ template <int DK> struct PrepSmem {
 };
 
 template <typename Tin, int DK>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kPrepThreads)
 exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                   const float *__restrict__ log_alpha, const float *__restrict__ beta, int H,
                   int dv, const int4 *__restrict__ plan, const int32_t *__restrict__ ctl,
@@ -240,16 +251,26 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     float *Gs = nk + C;               // [C][KP] per-channel rates: g_t[d] (after the rest)
     const bool per_channel = gcws != nullptr;
 
-    for (int idx = tid; idx < C * DK; idx += blockDim.x) {
-        const int t = idx / DK, d = idx % DK;
-        float kv = 0.f, qv = 0.f;
-        if (t < len) {
-            const size_t off = ((size_t)(t0 + t) * H + h) * DK + d;
-            kv = to_f32(k[off]);
-            qv = to_f32(q[off]);
+    {  // keys and queries, four elements a load, every load issued before any is used
+        constexpr int NK = C * DK / 4 / kPrepThreads;
+        float4 kv4[NK], qv4[NK];
+#pragma unroll
+        for (int r = 0; r < NK; ++r) {
+            const int e = 4 * (tid + r * kPrepThreads), t = e / DK, d = e % DK;
+            kv4[r] = qv4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < len) {
+                const size_t off = ((size_t)(t0 + t) * H + h) * DK + d;
+                kv4[r] = load4(k + off);
+                qv4[r] = load4(q + off);
+            }
         }
-        ks[t * KP + d] = kv;
-        qs[t * KP + d] = qv;
+#pragma unroll
+        for (int r = 0; r < NK; ++r) {
+            const int e = 4 * (tid + r * kPrepThreads), t = e / DK, d = e % DK;
+            float *kr = ks + t * KP + d, *qr = qs + t * KP + d;
+            kr[0] = kv4[r].x; kr[1] = kv4[r].y; kr[2] = kv4[r].z; kr[3] = kv4[r].w;
+            qr[0] = qv4[r].x; qr[1] = qv4[r].y; qr[2] = qv4[r].z; qr[3] = qv4[r].w;
+        }
     }
     if (tid < C) {
         float b = 0.f, a = 1.f;
@@ -388,9 +409,13 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     for (int jb = 0; jb < dv; jb += VB) {
         const int nb = dv - jb < VB ? dv - jb : VB;
         __syncthreads();  // (the queries, or the previous block, are read)
-        for (int idx = tid; idx < C * VB; idx += blockDim.x) {
-            const int i = idx / VB, j = idx % VB;
-            Vs[i * VP + j] = (i < len && j < nb) ? to_f32(v[((size_t)(t0 + i) * H + h) * dv + jb + j]) : 0.f;
+#pragma unroll
+        for (int r = 0; r < C * VB / 4 / kPrepThreads; ++r) {  // four elements a load
+            const int e = 4 * (tid + r * kPrepThreads), i = e / VB, j = e % VB;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < len && j < nb) x = load4(v + ((size_t)(t0 + i) * H + h) * dv + jb + j);
+            float *vr = Vs + i * VP + j;
+            vr[0] = x.x; vr[1] = x.y; vr[2] = x.z; vr[3] = x.w;
         }
         __syncthreads();
         for (int idx = tid; idx < C * nb; idx += blockDim.x) {
@@ -415,14 +440,6 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
 constexpr int kChainCols = 32;  // value columns per chain CTA
 constexpr int kChainThreads = 256;
 
-// Four consecutive elements at p (16-byte aligned for fp32, 8-byte for bf16) as fp32.
-__device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
-__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
-    const uint2 u = *reinterpret_cast<const uint2 *>(p);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-    return make_float4(a.x, a.y, b.x, b.y);
-}
 
 template <int DK> struct ChainSmem {
     static constexpr int KP = DK + 1;
@@ -638,7 +655,7 @@ static int launch_exact_t(const PrefillArgs &a, const WsLayout &L) {
     if (e != cudaSuccess) return GDR_ERR_CUDA;
     if (L.max_chunks > 0) {
         dim3 grid((unsigned)L.max_chunks, (unsigned)a.H);
-        exact_prep_kernel<Tin, DK><<<grid, 256, prep_smem, a.stream>>>(
+        exact_prep_kernel<Tin, DK><<<grid, kPrepThreads, prep_smem, a.stream>>>(
             (const Tin *)a.q, (const Tin *)a.k, (const Tin *)a.v, a.log_alpha, a.beta, a.H, a.dv,
             (const int4 *)(a.ws + L.plan), ctl, W, U, A, g, a.rule == GDR_RULE_ADDITIVE ? 1 : 0,
             a.prologue, a.gate_A, gc);
