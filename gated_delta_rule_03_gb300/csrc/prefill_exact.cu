@@ -443,7 +443,7 @@ constexpr int kChainThreads = 256;
 
 template <int DK> struct ChainSmem {
     static constexpr int KP = DK + 1;
-    static constexpr int SP = kChainCols + 1;
+    static constexpr int SP = kChainCols + 4;  // (rows of S and U on 16-byte boundaries)
     static constexpr size_t floats = DK * SP + 3 * kChunk * KP + kChunk * (kChunk + 1) +
                                      kChunk * SP + 5 * kChunk;
     static constexpr size_t bytes = floats * sizeof(float);
@@ -486,6 +486,7 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     float *ks = qs + C * KP;     // [C][KP]
     float *Ac = ks + C * KP;     // [C][CP]
     float *Uc = Ac + C * CP;     // [C][SP]  Utilde, then U
+    static_assert((DK * SP + 3 * C * KP + C * CP) % 4 == 0, "U rows on 16-byte boundaries");
     float *gam = Uc + C * SP;    // [C] gamma_t
     float *kdec = gam + C;       // [C] Gamma_{C-1,i}
     float *nqk = kdec + C;       // [2][C] 1/|q_t|, 1/|k_t| (the prologue; else 1)
@@ -581,13 +582,16 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             u[x] = 0.f;
             qsv[x] = 0.f;
         }
+#pragma unroll 4
         for (int d = 0; d < DK; ++d) {
             const float w = Wc[t * KP + d], qq = qs[t * KP + d];
+            const float4 sa = *reinterpret_cast<const float4 *>(Ss + d * SP + jg);
+            const float4 sb = *reinterpret_cast<const float4 *>(Ss + d * SP + jg + 4);
+            const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
             for (int x = 0; x < 8; ++x) {
-                const float sv = Ss[d * SP + jg + x];
-                u[x] = fmaf(w, sv, u[x]);
-                qsv[x] = fmaf(qq, sv, qsv[x]);
+                u[x] = fmaf(w, sv[x], u[x]);
+                qsv[x] = fmaf(qq, sv[x], qsv[x]);
             }
         }
         __syncthreads();  // every thread has read S and Utilde is still intact
@@ -601,8 +605,11 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             for (int x = 0; x < 8; ++x) outv[x] = gam[t] * qsv[x];
             for (int i = 0; i <= t; ++i) {
                 const float aw = Ac[t * CP + i];
+                const float4 ua = *reinterpret_cast<const float4 *>(Uc + i * SP + jg);
+                const float4 ub = *reinterpret_cast<const float4 *>(Uc + i * SP + jg + 4);
+                const float uv8[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-                for (int x = 0; x < 8; ++x) outv[x] = fmaf(aw, Uc[i * SP + jg + x], outv[x]);
+                for (int x = 0; x < 8; ++x) outv[x] = fmaf(aw, uv8[x], outv[x]);
             }
             Tin *op = o + ((size_t)(tc0 + t) * H + h) * dv + j0 + jg;
 #pragma unroll
@@ -614,17 +621,33 @@ exact_chain_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             constexpr int CPT = NC / TPR;          // columns per thread
             const int d = tid / TPR, jb = (tid % TPR) * CPT;
             const float gC = gcws ? expf(gcws[cb * C * DK + (C - 1) * DK + d]) : gam[C - 1];
+            static_assert(CPT % 4 == 0, "state columns in 16-byte groups");
             float acc[CPT];
 #pragma unroll
-            for (int x = 0; x < CPT; ++x) acc[x] = gC * Ss[d * SP + jb + x];
+            for (int x4 = 0; x4 < CPT / 4; ++x4) {
+                const float4 s4 = *reinterpret_cast<const float4 *>(Ss + d * SP + jb + 4 * x4);
+                acc[4 * x4] = gC * s4.x;
+                acc[4 * x4 + 1] = gC * s4.y;
+                acc[4 * x4 + 2] = gC * s4.z;
+                acc[4 * x4 + 3] = gC * s4.w;
+            }
+#pragma unroll 4
             for (int i = 0; i < C; ++i) {
                 const float kt = kdec[i] * ks[i * KP + d];
 #pragma unroll
-                for (int x = 0; x < CPT; ++x) acc[x] = fmaf(kt, Uc[i * SP + jb + x], acc[x]);
+                for (int x4 = 0; x4 < CPT / 4; ++x4) {
+                    const float4 u4 = *reinterpret_cast<const float4 *>(Uc + i * SP + jb + 4 * x4);
+                    acc[4 * x4] = fmaf(kt, u4.x, acc[4 * x4]);
+                    acc[4 * x4 + 1] = fmaf(kt, u4.y, acc[4 * x4 + 1]);
+                    acc[4 * x4 + 2] = fmaf(kt, u4.z, acc[4 * x4 + 2]);
+                    acc[4 * x4 + 3] = fmaf(kt, u4.w, acc[4 * x4 + 3]);
+                }
             }
             __syncthreads();  // all reads of the old S (QS above) are done
 #pragma unroll
-            for (int x = 0; x < CPT; ++x) Ss[d * SP + jb + x] = acc[x];
+            for (int x4 = 0; x4 < CPT / 4; ++x4)
+                *reinterpret_cast<float4 *>(Ss + d * SP + jb + 4 * x4) =
+                    make_float4(acc[4 * x4], acc[4 * x4 + 1], acc[4 * x4 + 2], acc[4 * x4 + 3]);
         }
         __syncthreads();
     }
