@@ -367,20 +367,28 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     }
     __syncthreads();
 
-    // Forward substitution, one column of T per thread: (I + L) x = beta_j e_j.
+    // Forward substitution, one column of T per thread: (I + L) x = beta_j e_j. The column
+    // stays in registers (both loops unrolled, so every index is a constant; x_i = 0 for
+    // i < j), each row's sum in four partial sums.
     if (tid < C) {
         const int j = tid;
+        float x[C];
+#pragma unroll
         for (int t = 0; t < C; ++t) {
-            float x = 0.f;
-            if (t == j) {
-                x = bs[j];
-            } else if (t > j) {
-                float s = 0.f;
-                for (int i = j; i < t; ++i) s = fmaf(Lm[t * CP + i], Tm[i * CP + j], s);
-                x = -s;
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+            for (int i = 0; i + 3 < t; i += 4) {
+                s0 = fmaf(Lm[t * CP + i], x[i], s0);
+                s1 = fmaf(Lm[t * CP + i + 1], x[i + 1], s1);
+                s2 = fmaf(Lm[t * CP + i + 2], x[i + 2], s2);
+                s3 = fmaf(Lm[t * CP + i + 3], x[i + 3], s3);
             }
-            Tm[t * CP + j] = x;
+#pragma unroll
+            for (int i = t & ~3; i < t; ++i) s0 = fmaf(Lm[t * CP + i], x[i], s0);
+            x[t] = t == j ? bs[j] : (t > j ? -((s0 + s1) + (s2 + s3)) : 0.f);
         }
+#pragma unroll
+        for (int t = 0; t < C; ++t) Tm[t * CP + j] = x[t];
     }
     __syncthreads();
 
