@@ -344,26 +344,58 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
     }
     __syncthreads();
 
-    for (int idx = tid; idx < C * C; idx += blockDim.x) {
-        const int t = idx / C, i = idx % C;
-        float kk = 0.f, qk = 0.f, dec = 0.f;
-        if (i <= t && per_channel) {
-            for (int d = 0; d < DK; ++d) {
-                const float ki = ks[i * KP + d] * expf(Gs[t * KP + d] - Gs[i * KP + d]);
-                kk = fmaf(ks[t * KP + d], ki, kk);
-                qk = fmaf(qs[t * KP + d], ki, qk);
+    if (per_channel) {
+        for (int idx = tid; idx < C * C; idx += blockDim.x) {
+            const int t = idx / C, i = idx % C;
+            float kk = 0.f, qk = 0.f;
+            if (i <= t) {
+                for (int d = 0; d < DK; ++d) {
+                    const float ki = ks[i * KP + d] * expf(Gs[t * KP + d] - Gs[i * KP + d]);
+                    kk = fmaf(ks[t * KP + d], ki, kk);
+                    qk = fmaf(qs[t * KP + d], ki, qk);
+                }
             }
-            dec = 1.f;
-        } else if (i <= t) {
-            for (int d = 0; d < DK; ++d) {
-                const float ki = ks[i * KP + d];
-                kk = fmaf(ks[t * KP + d], ki, kk);
-                qk = fmaf(qs[t * KP + d], ki, qk);
-            }
-            dec = Gm[t * CP + i];
+            Lm[t * CP + i] = (i < t && !additive) ? bs[t] * kk : 0.f;
+            Am[t * CP + i] = qk;
         }
-        Lm[t * CP + i] = (i < t && !additive) ? bs[t] * dec * kk : 0.f;
-        Am[t * CP + i] = dec * qk;
+    } else {
+        // 4 x 4 blocks of (t, i) per thread: per feature, 4 keys and 4 queries of rows t and 4
+        // keys of rows i serve 32 products; blocks right of the diagonal are zero
+        static_assert(C * C / 16 == kPrepThreads, "one 4 x 4 block per thread");
+        const int t0 = 4 * (tid / (C / 4)), i0 = 4 * (tid % (C / 4));
+        float kk[4][4], qk[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) kk[a][b] = qk[a][b] = 0.f;
+        if (i0 <= t0 + 3) {
+#pragma unroll 4
+            for (int d = 0; d < DK; ++d) {
+                float kt[4], qt[4], ki[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    kt[a] = ks[(t0 + a) * KP + d];
+                    qt[a] = qs[(t0 + a) * KP + d];
+                    ki[a] = ks[(i0 + a) * KP + d];
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        kk[a][b] = fmaf(kt[a], ki[b], kk[a][b]);
+                        qk[a][b] = fmaf(qt[a], ki[b], qk[a][b]);
+                    }
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int t = t0 + a, i = i0 + b;
+                const float dec = i <= t ? Gm[t * CP + i] : 0.f;
+                Lm[t * CP + i] = (i < t && !additive) ? bs[t] * dec * kk[a][b] : 0.f;
+                Am[t * CP + i] = dec * qk[a][b];
+            }
     }
     __syncthreads();
 
