@@ -426,16 +426,45 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
 
     const size_t cb = (size_t)c * H + h;
     float *Wout = Wws + cb * C * DK;
-    for (int idx = tid; idx < C * DK; idx += blockDim.x) {
-        const int t = idx / DK, d = idx % DK;
-        float s = 0.f;
-        if (per_channel) {  // rows gamma_i[d] k_i[d]
-            for (int i = 0; i <= t; ++i)
+    if (per_channel) {
+        for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+            const int t = idx / DK, d = idx % DK;
+            float s = 0.f;
+            for (int i = 0; i <= t; ++i)  // rows gamma_i[d] k_i[d]
                 s = fmaf(Tm[t * CP + i] * expf(Gs[i * KP + d]), ks[i * KP + d], s);
-        } else {
-            for (int i = 0; i <= t; ++i) s = fmaf(Tm[t * CP + i] * gam[i], ks[i * KP + d], s);
+            Wout[idx] = additive ? 0.f : s;
         }
-        Wout[idx] = additive ? 0.f : s;
+    } else {
+        // 4 x 4 blocks of (t, d) per thread; T is zero right of its diagonal, so a block's
+        // sums run to its last row, each in the order of the unblocked loop
+        constexpr int NBD = DK / 4;
+        for (int blk = tid; blk < (C / 4) * NBD; blk += kPrepThreads) {
+            const int tb = 4 * (blk / NBD), d0 = 4 * (blk % NBD);
+            float acc[4][4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 4
+            for (int i = 0; i <= tb + 3; ++i) {
+                const float gi = gam[i];
+                float tv[4], kv[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    tv[a] = Tm[(tb + a) * CP + i] * gi;
+                    kv[a] = ks[i * KP + d0 + a];
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(tv[a], kv[b], acc[a][b]);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                *reinterpret_cast<float4 *>(Wout + (tb + a) * DK + d0) =
+                    additive ? make_float4(0.f, 0.f, 0.f, 0.f)
+                             : make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        }
     }
     if (per_channel)
         for (int idx = tid; idx < C * DK; idx += blockDim.x)
@@ -458,11 +487,32 @@ exact_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Ti
             vr[0] = x.x; vr[1] = x.y; vr[2] = x.z; vr[3] = x.w;
         }
         __syncthreads();
-        for (int idx = tid; idx < C * nb; idx += blockDim.x) {
-            const int t = idx / nb, j = idx % nb;
-            float s = 0.f;
-            for (int i = 0; i <= t; ++i) s = fmaf(Tm[t * CP + i], Vs[i * VP + j], s);
-            Uout[t * dv + jb + j] = s;
+        // 4 x 4 blocks of (t, j) per thread, as for W
+        const int nbj = nb / 4;
+        for (int blk = tid; blk < (C / 4) * nbj; blk += kPrepThreads) {
+            const int tb = 4 * (blk / nbj), j4 = 4 * (blk % nbj);
+            float acc[4][4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 4
+            for (int i = 0; i <= tb + 3; ++i) {
+                float tv[4], vv[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    tv[a] = Tm[(tb + a) * CP + i];
+                    vv[a] = Vs[i * VP + j4 + a];
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(tv[a], vv[b], acc[a][b]);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                *reinterpret_cast<float4 *>(Uout + (size_t)(tb + a) * dv + jb + j4) =
+                    make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
         }
     }
     float *Aout = Aws + cb * C * C;
