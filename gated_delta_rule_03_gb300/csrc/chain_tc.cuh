@@ -175,6 +175,7 @@ struct TcParams {
     // call GDR_ERR_DEVICE_TIMEOUT and drain.
     long long wait_cycles;
     int fault_chunk;
+    int only_pair;  // run nothing unless ctl[kPairWord] hands the call to this launch
 };
 
 // Every wait's bound, and the give-up test knob (host side, prefill_tc.cu).
@@ -363,7 +364,8 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
     // previous phase) is read only after it has completed.
     griddep_wait();
     griddep_launch_dependents();
-    const bool live = p.ctl[0] == GDR_OK;  // cu_seqlens rejected, or a solve gave up
+    // (not live: cu_seqlens rejected, a solve gave up, or the call is another launch's)
+    const bool live = p.ctl[0] == GDR_OK && (!p.only_pair || p.ctl[kPairWord] == 1);
 
     if (!live) {
         // nothing is read or written

@@ -68,6 +68,10 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
         off = align_up(off + (size_t)num_seqs * (size_t)H * dk * dv * sizeof(float), 256);
         L.F = off;  // one flag per (chunk, head) unit (fused schedule)
         off = align_up(off + (size_t)L.max_chunks * (size_t)H * sizeof(int32_t), 256);
+        L.order = off;  // the claim order of the fused schedule over packed sequences
+        off = align_up(off + (size_t)L.max_chunks * sizeof(int4), 256);
+        L.trig = off;
+        off = align_up(off + (size_t)num_seqs * sizeof(int32_t), 256);
         L.segmentable = tc_segmentable(num_seqs, total_tokens, H, dv);
         L.seg = off;  // the segmented schedule's state sets
         if (L.segmentable)
@@ -300,9 +304,10 @@ int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H,
     if (total_tokens == 0) return 1;  // the plan; the state copy is not a kernel of ours
     const int P = tc_schedule_query(num_seqs, total_tokens, H, d_v, varlen != 0);
     if (P < 0) return GDR_ERR_CUDA;
-    // fused: plan, cooperative kernel; P phases: plan, P solves, P chains; segmented:
-    // plan, solve, summary chain, scan, chain
-    return P == 0 ? 2 : (P > kSegmentedBase ? 5 : 1 + 2 * P);
+    // fused: plan, cooperative kernel (packed sequences: then the solve and chain of one
+    // phase, which the plan may hand the call to); P phases: plan, P solves, P chains;
+    // segmented: plan, solve, summary chain, scan, chain
+    return P == 0 ? (varlen ? 4 : 2) : (P > kSegmentedBase ? 5 : 1 + 2 * P);
 }
 
 int gdr_chunk_fwd_schedule(int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v,

@@ -15,6 +15,16 @@ constexpr int kMaxPhases = 8;  // most phases a tensor-core prefill is split int
 // Schedules of the tensor-core path: 0 fused, 1 .. kMaxPhases phased, kSegmentedBase + n
 // segmented into n segments per sequence.
 constexpr int kSegmentedBase = GDR_SCHEDULE_SEGMENTED;
+// The fused schedule over packed sequences: at most this many sequences (the planning
+// kernel keeps their chunk counts in shared memory), and the control word that counts
+// the solve's claims.
+constexpr int kMaxClaimSeqs = 128;
+constexpr int kClaimWord = 32;
+// For packed sequences the host launches the fused kernel and, after it, the phased
+// schedule's two kernels (one phase); the planning kernel sets ctl[kPairWord] to 1 when
+// the pair is to do the work (the fused kernel then returns at once), else to 0 (the
+// pair then returns at once).
+constexpr int kPairWord = 33;
 // phases of the chunk plan a schedule needs (a segment is a phase)
 inline int plan_phases(int schedule) {
     return schedule == 0 ? 1 : (schedule > kSegmentedBase ? schedule - kSegmentedBase : schedule);
@@ -65,6 +75,11 @@ struct WsLayout {
     size_t S;             // tensor-core path: fp32 [num_seqs][H][dk][dv] state between phases
     size_t F;             // tensor-core path: int32 [max_chunks * H] unit-solved flags
                           // (fused schedule)
+    size_t order;         // tensor-core path: int4 [max_chunks] the claim order of the fused
+                          // schedule over packed sequences: (chunk, first token, tokens,
+                          // sequence) per claim row
+    size_t trig;          // tensor-core path: int32 [num_seqs] the claim count at which the
+                          // chain CTAs of each sequence stop solving and start their chains
     size_t seg;           // tensor-core path, few long chains: the segmented schedule's
                           // fp32 state sets, [NH][d_k][d_v] each: (kMaxPhases - 1) each
                           // of P, R and discard, kMaxPhases of start; 0 bytes otherwise
@@ -88,6 +103,8 @@ WsLayout ws_layout(int64_t num_seqs, int64_t total_tokens, int H, int dk, int dv
 // The planning kernel for a schedule (the fused schedule, 0, plans one phase and clears
 // the unit flags; the segmented one plans a phase per segment).
 int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases);
+// The SM count of the current device (0 if it cannot be read), cached.
+int current_device_sms();
 int launch_prefill_exact(const PrefillArgs &a, const WsLayout &L);
 int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases);
 // The tensor-core path with one forget rate per key channel: the per-channel chunk kernel

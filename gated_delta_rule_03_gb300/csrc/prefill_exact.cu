@@ -73,14 +73,34 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_sums, int *
 //   zero[0 .. n_zero)                 cleared (the fused schedule's unit-solved flags)
 // A single block of 1024 threads: sequences in blocks of 1024 for the prefix sums, then a
 // group of threads per sequence writes its plan entries.
+//
+// With `order` (the fused schedule over packed sequences, one phase, at most
+// kMaxClaimSeqs sequences) it also lists the claim order of the solve and the chains'
+// triggers. Sequence n of m_n chunks starts its chains s_n = m_max - m_n chain steps
+// after the longest, so that all end together; its chunk j is due at step s_n + j, and
+// the rows (n, j) are claimed in order of that step (ties by sequence). A sequence's
+// chain CTAs solve until the claims reach trig[n], then run their chains. The trigger
+// is no earlier than the sequence's first row (H x that row's place in the order), and
+// late enough that the units still unclaimed can be solved in the m_n steps left: in
+// those steps every chain k runs min(m_k, m_n) of its steps, and each SM that runs no
+// chain solves about one unit per chain step (a unit takes about 2 us of an SM when
+// four are in flight on it, a chain step beside the solve about 1.8 us), so
+// trig[n] >= U - (sms m_n - chains_per_seq sum_k min(m_k, m_n)) for U units in all.
+// The claim counter ctl[kClaimWord] starts at zero. When the SMs the chains leave free
+// over the longest chain's steps could solve less than half of the units (equal or
+// nearly equal lengths over many chains), little of the solve would overlap the chains
+// and the two-kernel pair that follows the fused launch is faster: ctl[kPairWord] = 1
+// hands the call to it (else 0).
 __global__ void __launch_bounds__(1024)
 plan_kernel(const int32_t *__restrict__ cu, int64_t num_seqs, int64_t total_tokens,
             int64_t max_chunks, int phases, int4 *__restrict__ plan,
             int32_t *__restrict__ seq_chunk, int32_t *__restrict__ ctl,
-            int32_t *__restrict__ zero, int64_t n_zero) {
+            int32_t *__restrict__ zero, int64_t n_zero, int4 *__restrict__ order,
+            int32_t *__restrict__ trig, int H, int chains_per_seq, int sms) {
     __shared__ int s_warp[32];
     __shared__ int s_off[kMaxPhases + 1];
     __shared__ int s_bad;
+    __shared__ int s_m[kMaxClaimSeqs], s_mmax;  // (claim order) chunks per sequence, and most
     const int tid = threadIdx.x;
     const int64_t row = num_seqs + 1;  // seq_chunk entries per phase
     // the solve kernel after this one may be launched now (programmatic launch): it sets
@@ -169,23 +189,74 @@ plan_kernel(const int32_t *__restrict__ cu, int64_t num_seqs, int64_t total_toke
                 }
             }
         }
+        // pass 4: the claim order and the triggers
+        if (order && num_seqs <= kMaxClaimSeqs) {
+            if (tid == 0) s_mmax = 0;
+            __syncthreads();
+            for (int n = tid; n < num_seqs; n += blockDim.x) {
+                s_m[n] = seq_chunk[n + 1] - seq_chunk[n];
+                atomicMax(&s_mmax, s_m[n]);
+            }
+            __syncthreads();
+            const int mmax = s_mmax, rows = s_off[1];
+            const int64_t units = (int64_t)rows * H;
+            if (tid == 0) {
+                const int64_t free_all = (int64_t)sms * mmax - (int64_t)chains_per_seq * rows;
+                ctl[kPairWord] = 2 * free_all < units ? 1 : 0;
+            }
+            for (int n = g; n < num_seqs; n += G) {
+                const int m = s_m[n], sn = mmax - m;
+                int64_t t0, len;
+                seq_range(n, t0, len);
+                for (int j = gt; j < m; j += gsize) {
+                    // rows of sequence k due before row (n, j), or at the same step if k < n
+                    const int due = sn + j;
+                    int pos = 0;
+                    for (int k = 0; k < num_seqs; ++k) {
+                        int c = due - (mmax - s_m[k]) + (k < n ? 1 : 0);
+                        pos += c < 0 ? 0 : (c > s_m[k] ? s_m[k] : c);
+                    }
+                    const int64_t rem = len - (int64_t)j * kChunk;
+                    order[pos] = make_int4(seq_chunk[n] + j, (int)(t0 + (int64_t)j * kChunk),
+                                           (int)(rem < kChunk ? rem : kChunk), n);
+                    if (j == 0) {
+                        int64_t steps = 0;  // chain steps of all sequences in the last m steps
+                        for (int k = 0; k < num_seqs; ++k) steps += s_m[k] < m ? s_m[k] : m;
+                        const int64_t free_steps = (int64_t)sms * m - (int64_t)chains_per_seq * steps;
+                        const int64_t late = units - (free_steps > 0 ? free_steps : 0);
+                        const int64_t first = (int64_t)pos * H;
+                        trig[n] = (int)(late > first ? late : first);
+                    }
+                }
+                // a sequence without chunks solves to the end; its chain only copies S0
+                if (m == 0 && gt == 0) trig[n] = (int)units;
+            }
+        }
     }
+    if (order && bad)  // no chain runs; no CTA solves first
+        for (int64_t n = tid; n < num_seqs && n < kMaxClaimSeqs; n += blockDim.x) trig[n] = 0;
     if (tid == 0) {
         ctl[0] = bad ? GDR_ERR_BAD_SEQLENS : GDR_OK;
         ctl[1] = bad ? 0 : s_off[phases];
         for (int f = 0; f <= phases; ++f) ctl[2 + f] = bad ? 0 : s_off[f];
+        ctl[kClaimWord] = 0;
     }
 }
 
 int launch_plan(const PrefillArgs &a, const WsLayout &L, int phases) {
     const bool fused = phases == 0;
+    // the fused schedule over packed sequences claims its units in a planned order
+    const bool claim = fused && L.tensor_path && a.cu_seqlens;
     plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.num_seqs, a.total_tokens, L.max_chunks,
                                           plan_phases(phases), (int4 *)(a.ws + L.plan),
                                           (int32_t *)(a.ws + L.seq_chunk),
                                           (int32_t *)(a.ws + L.ctl),
                                           L.tensor_path ? (int32_t *)(a.ws + L.F) : nullptr,
                                           !L.tensor_path ? 0
-                                          : (fused ? L.max_chunks * a.H : 0));
+                                          : (fused ? L.max_chunks * a.H : 0),
+                                          claim ? (int4 *)(a.ws + L.order) : nullptr,
+                                          claim ? (int32_t *)(a.ws + L.trig) : nullptr, a.H,
+                                          a.H * (a.dv / 128), current_device_sms());
     return cuda_status(cudaGetLastError());
 }
 

@@ -35,23 +35,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_chain_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_t,
                 const __grid_constant__ CUtensorMap map_o, const TcParams p) {
+    // The plan's choice between the fused kernel and this pair: the plan completed before
+    // the fused kernel ahead of this launch began, so the word is read at once. A launch
+    // left out lets the next one start, and ends only after the kernel ahead of it.
+    if (p.only_pair && p.ctl[kPairWord] != 1) {
+        griddep_launch_dependents();
+        griddep_wait();
+        return;
+    }
     chain_body<false, kSeg>(map_q, map_k, map_v, map_t, map_o, p, (int)blockIdx.x);
 }
 
 static_assert(solve::kSolveWarps * 32 <= kThreads, "the fused launch runs the solve on the chain's block");
 constexpr uint32_t FUSED_SMEM_BYTES = SMEM_BYTES > solve::SMEM_BYTES ? SMEM_BYTES : solve::SMEM_BYTES;
 
-// CTAs [0, chain_ctas) run chains, the others the solve.
+// CTAs [0, chain_ctas) run chains, the others the solve. kClaim (packed sequences): the
+// solve CTAs claim units from the grid's counter in the plan's claim order, and a chain
+// CTA first solves too, until the claims reach the trigger trig[n] of its sequence n
+// (the plan puts it where the chain is due to start), then runs its chain.
+template <bool kClaim>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_fused_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_t,
                 const __grid_constant__ CUtensorMap map_o, const TcParams p,
-                const solve::SolveParams sp, int chain_ctas) {
-    if ((int)blockIdx.x < chain_ctas)
+                const solve::SolveParams sp, int chain_ctas, const int32_t *trig) {
+    if (kClaim && p.ctl[kPairWord] == 1) return;  // the two-kernel pair after it runs the call
+    if ((int)blockIdx.x < chain_ctas) {
+        if (kClaim) {
+            const int stop = trig[(int)blockIdx.x / p.n_slices / p.H];
+            if (stop > 0) solve::solve_body<true, true>(map_q, map_k, sp, 0, 1, stop, true);
+        }
         chain_body<true>(map_q, map_k, map_v, map_t, map_o, p, (int)blockIdx.x);
-    else
-        solve::solve_body<true>(map_q, map_k, sp, (int)blockIdx.x - chain_ctas,
-                                (int)gridDim.x - chain_ctas);
+    } else {
+        solve::solve_body<true, kClaim>(map_q, map_k, sp, (int)blockIdx.x - chain_ctas,
+                                        (int)gridDim.x - chain_ctas);
+    }
 }
 
 // The segmented schedule's scan over the segment summaries of one (sequence, head) and
@@ -252,6 +270,21 @@ SideStream *side_stream(cudaStream_t caller) {
 
 }  // namespace
 
+int current_device_sms() {
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess ? device_sms(dev) : 0;
+}
+
+// Fused over packed sequences (solve units claimed in the plan's order, chain CTAs
+// solving until their chains are due): every chain CTA and at least 16 solve-only CTAs
+// fit on the GPU at once, over at most kMaxClaimSeqs sequences (the plan's limit), of
+// 32 chunks or more on average (shorter work does not pay for the cooperative launch and
+// the ramp of the solve ahead of the chains).
+static bool claim_fits(int64_t num_seqs, int64_t total_tokens, int H, int dv, int sms) {
+    return num_seqs <= kMaxClaimSeqs && num_seqs * H * (dv / chain::NV) + 16 <= sms &&
+           total_tokens >= num_seqs * 32 * kChunk;
+}
+
 // Fused: the chain CTAs plus at least 1.2 solve CTAs per (sequence, head) must fit on
 // the GPU at one CTA per SM. A solve CTA finishes a unit about every 2 us and a chain
 // step takes about 1.5 us, so with that many solve CTAs the solve about keeps pace with
@@ -339,18 +372,25 @@ void chain_wait_policy(TcParams &p) {
 }
 }  // namespace chain
 
+template <typename K>
+static bool one_block_fits(K kernel) {
+    int blocks = 0;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)chain::FUSED_SMEM_BYTES) == cudaSuccess &&
+           cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, chain::kThreads,
+                                                         chain::FUSED_SMEM_BYTES) == cudaSuccess &&
+           blocks >= 1;
+}
+
+// (both forms of the fused kernel)
 static bool cooperative_ok(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return false;
     int known = g_cooperative_ok[dev].load(std::memory_order_relaxed);
     if (!known) {
-        int coop = 0, blocks = 0;
+        int coop = 0;
         const bool yes =
             cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
-            cudaFuncSetAttribute(chain::tc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)chain::FUSED_SMEM_BYTES) == cudaSuccess &&
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, chain::tc_fused_kernel, chain::kThreads,
-                                                          chain::FUSED_SMEM_BYTES) == cudaSuccess &&
-            blocks >= 1;
+            one_block_fits(chain::tc_fused_kernel<false>) && one_block_fits(chain::tc_fused_kernel<true>);
         known = yes ? 1 : 2;
         g_cooperative_ok[dev].store(known, std::memory_order_relaxed);
     }
@@ -364,6 +404,7 @@ int tc_schedule_for(int64_t num_seqs, int64_t total_tokens, int H, int dv, int s
         if (tc_segmentable(num_seqs, total_tokens, H, dv)) return kSegmentedBase + n;
     if (const int P = forced_phases()) return P;
     if (const int n = segment_count(num_seqs, total_tokens, H, dv, sms)) return kSegmentedBase + n;
+    if (varlen && cooperative && claim_fits(num_seqs, total_tokens, H, dv, sms)) return 0;
     if (!varlen && cooperative && fused_fits(num_seqs, H, dv, sms)) return 0;
     return phased_count(num_seqs, total_tokens, H, dv, sms);
 }
@@ -383,7 +424,8 @@ int tc_schedule_query(int64_t num_seqs, int64_t total_tokens, int H, int dv, boo
     return tc_schedule_for(num_seqs, total_tokens, H, dv, device_sms(dev), varlen, cooperative_ok(dev));
 }
 
-// The fused launch: every chain CTA and, on the remaining SMs, solve CTAs.
+// The fused launch: every chain CTA and, on the remaining SMs, solve CTAs (claiming
+// their units, and with chain CTAs solving first, for packed sequences).
 static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &mq,
                         const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mt,
                         const CUtensorMap &mo) {
@@ -396,9 +438,10 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     int32_t *flags = reinterpret_cast<int32_t *>(a.ws + L.F);
     TcParams p = {};
     chain_wait_policy(p);
+    const bool claim = a.cu_seqlens != nullptr;
     p.S_in = a.S0;
     p.factors = reinterpret_cast<const float *>(a.ws + L.G);
-    p.cu_seqlens = nullptr;
+    p.cu_seqlens = a.cu_seqlens;
     p.seq_chunk = reinterpret_cast<const int32_t *>(a.ws + L.seq_chunk);
     p.num_seqs = a.num_seqs;
     p.total_tokens = a.total_tokens;
@@ -430,9 +473,12 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     sp.seqs = (int)a.num_seqs;
     sp.seq_chunks = (int)((a.total_tokens / a.num_seqs + kChunk - 1) / kChunk);
     sp.flags = flags;
+    sp.order = reinterpret_cast<const int4 *>(a.ws + L.order);
+    sp.claim = p.ctl + kClaimWord;
     sp.additive = a.rule == GDR_RULE_ADDITIVE;
     sp.prologue = a.prologue;
     sp.gate_A = a.gate_A;
+    const int32_t *trig = reinterpret_cast<const int32_t *>(a.ws + L.trig);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
@@ -443,7 +489,10 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     attr.val.cooperative = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, tc_fused_kernel, mq, mk, mv, mt, mo, p, sp, chain_ctas));
+    return cuda_status(claim ? cudaLaunchKernelEx(&cfg, tc_fused_kernel<true>, mq, mk, mv, mt, mo, p,
+                                                  sp, chain_ctas, trig)
+                             : cudaLaunchKernelEx(&cfg, tc_fused_kernel<false>, mq, mk, mv, mt, mo, p,
+                                                  sp, chain_ctas, trig));
 }
 
 // The segmented schedule over `segs` segments per sequence.
@@ -541,7 +590,14 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
         !tc::make_map_thd(&mo, a.o, a.dv, a.H, a.total_tokens) ||
         !tc::make_map_units(&mt, a.ws + L.T, 2 * L.max_chunks * a.H))
         return GDR_ERR_CUDA;
-    if (phases == 0) return launch_fused(a, L, mq, mk, mv, mt, mo);
+    // Packed sequences on the fused schedule: the fused launch, then the two-kernel pair
+    // of one phase; the plan has chosen on the device which of the two does the work.
+    const bool only_pair = phases == 0 && a.cu_seqlens;
+    if (phases == 0) {
+        const int st = launch_fused(a, L, mq, mk, mv, mt, mo);
+        if (st != GDR_OK || !only_pair) return st;
+        phases = 1;
+    }
     if (phases > kSegmentedBase)
         return launch_segmented(a, L, phases - kSegmentedBase, mq, mk, mv, mt, mo);
     if (cudaFuncSetAttribute(tc_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -559,7 +615,7 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
     const int free_sms = (int)(device_sms(dev) - chain_ctas);
 
     // solve of phase 0 on the caller's stream, with the whole GPU
-    int st = tc::launch_solve_tc(a, L, mq, mk, 0, 0, a.stream, true);
+    int st = tc::launch_solve_tc(a, L, mq, mk, 0, 0, a.stream, true, only_pair);
     if (st != GDR_OK) return st;
     if (phases > 1) {  // solves of phases 1 .. P-1 on the side stream, after the solve of
                        // phase 0 (which has had every SM) and beside the chains
@@ -586,6 +642,7 @@ int launch_prefill_tc(const PrefillArgs &a, const WsLayout &L, int phases) {
     p.ctl = (int32_t *)(a.ws + L.ctl);
     p.additive = a.rule == GDR_RULE_ADDITIVE;
     p.prologue = a.prologue;
+    p.only_pair = only_pair;
     if (a.dv == NV) {  // the output step fused into the chain's epilogue
         p.out_gate = (const __nv_bfloat16 *)a.out_gate;
         p.out_norm_weight = a.out_norm_weight;

@@ -25,6 +25,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Ends the life of an initialised mbarrier, so that its shared memory may be used for
+// something else (a CTA that changes role reuses its shared memory).
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -364,6 +370,18 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 __device__ __forceinline__ void release_flag_gpu(int32_t *flag) {
     asm volatile("fence.acq_rel.gpu;\n\tst.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1)
                  : "memory");
+}
+// Takes the next index of a work counter shared by the grid (relaxed: the index only
+// orders the work; what the work reads is published by other flags).
+__device__ __forceinline__ int32_t claim_next(int32_t *counter) {
+    int32_t v;
+    asm volatile("atom.relaxed.gpu.global.add.s32 %0, [%1], 1;" : "=r"(v) : "l"(counter) : "memory");
+    return v;
+}
+__device__ __forceinline__ int32_t relaxed_load_gpu(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 __device__ __forceinline__ int32_t acquire_load_gpu(const int32_t *flag) {
     int32_t v;

@@ -9,6 +9,14 @@ namespace {
 __global__ void __launch_bounds__(kThreads, 1)
 tc_solve_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const SolveParams p) {
+    // The plan's choice between the fused kernel and this pair: the plan completed before
+    // the fused kernel ahead of this launch began, so the word is read at once. A launch
+    // left out lets the next one start, and ends only after the kernel ahead of it.
+    if (p.only_pair && p.ctl[kPairWord] != 1) {
+        griddep_launch_dependents();
+        griddep_wait();
+        return;
+    }
     solve_body<false>(map_q, map_k, p, (int)blockIdx.x, (int)gridDim.x);
 }
 
@@ -19,7 +27,7 @@ namespace tc {
 
 int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &map_q,
                     const CUtensorMap &map_k, int phase, int max_ctas,
-                    cudaStream_t stream, bool programmatic) {
+                    cudaStream_t stream, bool programmatic, bool only_pair) {
     using namespace solve;
     SolveParams p = {};
     p.log_alpha = a.log_alpha;
@@ -33,6 +41,7 @@ int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &
     p.additive = a.rule == GDR_RULE_ADDITIVE;
     p.prologue = a.prologue;
     p.gate_A = a.gate_A;
+    p.only_pair = only_pair;
     if (cudaFuncSetAttribute(tc_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
         return GDR_ERR_CUDA;

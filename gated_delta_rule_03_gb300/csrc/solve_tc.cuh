@@ -95,7 +95,8 @@ constexpr uint32_t G_BAR_MMA = G_BAR + 8;
 constexpr int kFactorFloats = 384;  // per unit in the workspace
 constexpr uint32_t G_FAIL = G_BAR_MMA + 8;
 constexpr uint32_t G_TMEM_SLOT = G_FAIL + 8;
-constexpr uint32_t GROUP_BYTES = (G_TMEM_SLOT + 8 + 1023) / 1024 * 1024;
+constexpr uint32_t G_XSLOT = G_TMEM_SLOT + 8;  // claimed units: the group's next unit
+constexpr uint32_t GROUP_BYTES = (G_XSLOT + 8 + 1023) / 1024 * 1024;
 constexpr uint32_t SMEM_BYTES = kGroups * GROUP_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448 && G_GATES % 16 == 0 && G_BAR % 8 == 0, "shared memory");
 // TMEM: 64 fp32 columns per group for its Gram (rows = the 128 lanes)
@@ -258,6 +259,12 @@ struct SolveParams {
     // `seq_chunks` chunks each, and a ready flag per unit, set once its results are stored
     int seqs, seq_chunks;
     int32_t *flags;
+    // fused launch over packed sequences: the units are claimed one at a time from a
+    // counter shared by the grid, in the order of the plan's claim rows (row r: chunk
+    // order[r].x, first token .y, tokens .z; its H units are heads 0 .. H - 1)
+    const int4 *order;
+    int32_t *claim;
+    int only_pair;  // solve nothing unless ctl[kPairWord] hands the call to this launch
     int additive;           // the additive rule: L = 0, so T = diag(beta)
     int prologue;           // the layer prologue: unit-length q, k; gates from a, b
     const float *gate_A;    // its per-head rate (null: 1)
@@ -268,7 +275,7 @@ struct SolveParams {
 // One warp's part of the solve: warp W of a group (block row W of every unit), its loop
 // over the group's units. The block row is a template parameter so that every
 // loop bound and mask below is a constant and the loads can be issued early.
-template <bool kFused>
+template <bool kFused, bool kClaim = false>
 struct GroupSolver {
     const SolveParams &p;
     const CUtensorMap *map_q, *map_k;
@@ -278,10 +285,12 @@ struct GroupSolver {
     int grp, lane, u0, n_units;
     int gid, gstride;          // units gid, gid + gstride, ... are this group's
     uint32_t tmem_d;           // the group's TMEM columns (lane field 0)
+    int stop;                  // kClaim: no claim once the group holds a unit >= stop
 
     // the unit at local index x: the phase's units in order, or (fused) chunk j of
     // sequence n for head h at x = (j * seqs + n) * H + h
     __device__ __forceinline__ int unit_at(int x) const {
+        if (kClaim) return p.order[x / p.H].x * p.H + x % p.H;
         if (!kFused) return u0 + x;
         const int h = x % p.H, r = x / p.H;
         return ((r % p.seqs) * p.seq_chunks + r / p.seqs) * p.H + h;
@@ -291,7 +300,21 @@ struct GroupSolver {
     __device__ __forceinline__ uint32_t bar_mma() const { return gbase + G_BAR_MMA; }
     // the plan entry of unit x (any x >= n_units: none); every lane of the caller loads it
     __device__ __forceinline__ int4 plan_of(int x) const {
+        if (kClaim) return x < n_units ? p.order[x / p.H] : make_int4(0, 0, 0, 0);
         return x < n_units ? p.plan[unit_at(x) / p.H] : make_int4(0, 0, 0, 0);
+    }
+    // kClaim: warp 0 claims the next unit (lane 0's atomic; the index is read later, so
+    // that its latency is not waited for); n_units when the group claims no more
+    __device__ __forceinline__ int claim_issue(int held) const {
+        return lane == 0 && held < n_units && held < stop ? claim_next(p.claim) : n_units;
+    }
+    __device__ __forceinline__ int claim_read(int c) const {
+        const int x = __shfl_sync(0xffffffffu, c, 0);
+        return x < n_units ? x : n_units;
+    }
+    __device__ __forceinline__ volatile int *xslot() const {
+        return reinterpret_cast<volatile int *>(reinterpret_cast<volatile unsigned char *>(gfail) - G_FAIL +
+                                                G_XSLOT);
     }
     __device__ __forceinline__ void issue_load(int x, const int4 &pl) const {  // leader
         const int h = unit_at(x) % p.H;
@@ -356,9 +379,21 @@ struct GroupSolver {
         // can fetch a unit's plan entry and gates a whole unit before it needs them (a
         // claim from a shared counter would put two dependent global round trips on the
         // group's critical path). The units are equal in work.
+        // (kClaim: the group's units come from the grid's claim counter instead; warp 0
+        // claims them a unit ahead and passes each to the group through shared memory.)
         int x = gid;
+        int x_next = 0, claimed = 0;  // kClaim, warp 0: the next unit; the pending claim
         int4 pl_cur = make_int4(0, 0, 0, 0), pl_next = make_int4(0, 0, 0, 0);
         float raw[4] = {0.f, 0.f, 0.f, 0.f};  // warp 0: stored gates of unit x
+        if (kClaim) {
+            if (W == 0) {
+                x = claim_read(claim_issue(-1));
+                if (lane == 0) *xslot() = x;
+                claimed = claim_issue(x);
+            }
+            gsync();
+            x = *xslot();
+        }
         if (W == 0) {
             pl_cur = plan_of(x);
             if (leader && x < n_units) {
@@ -366,7 +401,7 @@ struct GroupSolver {
                 ++loads;
             }
             fetch_gates(x, pl_cur, raw);
-            pl_next = plan_of(x + gstride);
+            if (!kClaim) pl_next = plan_of(x + gstride);
         }
         // the first unit's Gram, once its keys and queries have landed
         if (leader && x < n_units) {
@@ -381,7 +416,8 @@ struct GroupSolver {
         uint32_t ld_phase = 0, mma_phase = 0;
         while (x < n_units) {
             const int u = unit_at(x);
-            const bool has_next = x + gstride < n_units;
+            // (kClaim: known to warp 0 only, after the first barrier below)
+            bool has_next = x + gstride < n_units;
             bool gram_next = false;  // (leader) the next unit's Gram is issued
             // ---- gates of unit x: the shared scan of warp 0
             if (W == 0) {
@@ -404,6 +440,11 @@ struct GroupSolver {
             gsync();  // the gates are visible; every thread saw the Gram done (or gave up)
             if (*gfail) break;
             tc_fence_after();
+            if (kClaim && W == 0) {  // the unit after this one, claimed during the last
+                x_next = claim_read(claimed);
+                has_next = x_next < n_units;
+                pl_next = plan_of(x_next);
+            }
             const bool ratio = gt[GG_G + C - 1] > kRatioSafeLogDecay;
             // 1/|k_r| (threads 0-63 of the group) and 1/|q_r| (64-127): the prologue's unit
             // lengths, from the staged rows; ones without it
@@ -517,7 +558,7 @@ struct GroupSolver {
             // issued once they have); its gates and the plan entry of the one after are
             // fetched for later
             if (W == 0) {
-                const int xn = x + gstride;
+                const int xn = kClaim ? x_next : x + gstride;
                 if (leader && xn < n_units) {
                     if (kPro) fence_async_smem();  // the norms' reads come before the TMA writes
                     issue_load(xn, pl_next);
@@ -576,6 +617,7 @@ struct GroupSolver {
                     }
                 }
             }
+            if (kClaim && W == 0 && lane == 0) *xslot() = x_next;
             gsync();  // unit u is stored; the blocks and gates may be reused
             if (kFused && leader) release_flag_gpu(p.flags + u);
             if (leader && has_next && !gram_next) {
@@ -587,11 +629,19 @@ struct GroupSolver {
                     *gfail = 1;
                 }
             }
-            if (W == 0) {
-                pl_cur = pl_next;
-                pl_next = plan_of(x + 2 * gstride);
+            if (kClaim) {
+                x = *xslot();
+                if (W == 0) {
+                    pl_cur = pl_next;
+                    claimed = claim_issue(x);
+                }
+            } else {
+                if (W == 0) {
+                    pl_cur = pl_next;
+                    pl_next = plan_of(x + 2 * gstride);
+                }
+                x += gstride;
             }
-            x += gstride;
         }
         if (leader) {
             if (*gfail) atomicExch(p.ctl, GDR_ERR_DEVICE_TIMEOUT);
@@ -608,10 +658,14 @@ struct GroupSolver {
 // the solve's return at once; no block-wide barrier follows), takes the units in
 // chunk-major order so that the chains find their chunks solved in the order they need
 // them (every group runs at the same pace), and publishes each unit with a release of
-// its flag.
-template <bool kFused>
+// its flag. kClaim (with kFused): the units are claimed from the grid's counter in the
+// plan's claim order instead, each group stopping after the first unit it holds at or
+// past `stop`; with then_chain the CTA goes on to run a chain, so its TMEM allocation
+// right is kept and its barriers are ended for the chain to reuse the shared memory.
+template <bool kFused, bool kClaim = false>
 __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUtensorMap &map_k,
-                                           const SolveParams &p, int rank, int ranks) {
+                                           const SolveParams &p, int rank, int ranks,
+                                           int stop = 0x7fffffff, bool then_chain = false) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -632,7 +686,7 @@ __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUten
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + G_TMEM_SLOT);
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
+        if (!then_chain) tmem_relinquish();
     }
     tc_fence_before();
     named_sync(kBarSolve, kSolveWarps * 32);
@@ -647,12 +701,12 @@ __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUten
     // (phase -1: every unit of the call)
     const bool all = kFused || p.phase < 0;
     const int u0 = all ? 0 : p.ctl[2 + p.phase] * p.H;
-    const int n_units =
-        p.ctl[0] == GDR_OK ? (all ? p.ctl[1] * p.H : p.ctl[3 + p.phase] * p.H - u0) : 0;
-    const GroupSolver<kFused> gsv{p, &map_q, &map_k, gbase,
-                                  reinterpret_cast<float *>(gs + G_BLK), reinterpret_cast<float *>(gs + G_GATES),
-                                  fail, grp, lane, u0, n_units, rank * kGroups + grp, ranks * kGroups,
-                                  tmem + (uint32_t)grp * kGramCols};
+    const bool runs = p.ctl[0] == GDR_OK && (!p.only_pair || p.ctl[kPairWord] == 1);
+    const int n_units = runs ? (all ? p.ctl[1] * p.H : p.ctl[3 + p.phase] * p.H - u0) : 0;
+    const GroupSolver<kFused, kClaim> gsv{p, &map_q, &map_k, gbase,
+                                          reinterpret_cast<float *>(gs + G_BLK), reinterpret_cast<float *>(gs + G_GATES),
+                                          fail, grp, lane, u0, n_units, rank * kGroups + grp, ranks * kGroups,
+                                          tmem + (uint32_t)grp * kGramCols, stop};
     switch (w) {
         case 0: p.prologue ? gsv.template run<0, true>() : gsv.template run<0, false>(); break;
         case 1: p.prologue ? gsv.template run<1, true>() : gsv.template run<1, false>(); break;
@@ -666,6 +720,13 @@ __device__ __forceinline__ void solve_body(const CUtensorMap &map_q, const CUten
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    if (then_chain) {  // nothing waits on the group's barriers any more
+        if (w == 0 && lane == 0) {
+            mbar_inval(gbase + G_BAR);
+            mbar_inval(gbase + G_BAR_MMA);
+        }
+        named_sync(kBarSolve, kSolveWarps * 32);
     }
 }
 

@@ -86,10 +86,11 @@ bool make_map_rows_f32(CUtensorMap *map, const float *base, int d, int H, int64_
 
 // The chunk-parallel solve: T' and A^T for every (chunk, head) of one phase into the
 // workspace, on `stream`, with at most max_ctas CTAs (all SMs when max_ctas <= 0);
-// `programmatic` launches it as a programmatic dependent of the kernel ahead of it.
+// `programmatic` launches it as a programmatic dependent of the kernel ahead of it;
+// `only_pair`: it solves nothing unless the plan handed the call to the two-kernel pair.
 int launch_solve_tc(const PrefillArgs &a, const WsLayout &L, const CUtensorMap &map_q,
                     const CUtensorMap &map_k, int phase, int max_ctas,
-                    cudaStream_t stream, bool programmatic);
+                    cudaStream_t stream, bool programmatic, bool only_pair = false);
 
 }  // namespace tc
 }  // namespace gdr

@@ -223,7 +223,14 @@ def test_schedule_model_on_a_152_sm_device(env, monkeypatch):
     seg = ops.SCHEDULE_SEGMENTED
     assert m(4, 4 * 4096, 16, 128, 128, bf, 152) == 0                     # fused
     assert m(4, 4 * 4096, 16, 128, 128, bf, 152, cooperative=False) == 2   # phased instead
-    assert m(8, 34816, 16, 128, 128, bf, 152, varlen=True) >= 1            # packed: phased
+    assert m(8, 34816, 16, 128, 128, bf, 152, varlen=True) == 0            # packed: fused,
+    # its solve claiming units (the chains leave at least 16 SMs)
+    assert m(8, 34816, 16, 128, 128, bf, 152, varlen=True, cooperative=False) == 1
+    assert m(9, 34816, 16, 128, 128, bf, 152, varlen=True) == 1            # 144 chains: phased
+    assert m(128, 128 * 2048, 1, 128, 128, bf, 152, varlen=True) == 0      # most sequences
+    assert m(129, 129 * 2048, 1, 128, 128, bf, 152, varlen=True) == 1
+    assert m(8, 8 * 2047, 16, 128, 128, bf, 152, varlen=True) == 1         # short: phased
+    assert m(2, 70000, 16, 128, 256, bf, 152, varlen=True) == 0            # 64 two-slice chains
     assert m(1, 65536, 8, 128, 256, bf, 152) == seg + 7                    # long: 7 segments
     assert m(1, 65536, 8, 128, 256, bf, 40) < seg                          # too few SMs
     assert m(4, 4 * 4096, 16, 128, 128, torch.float32, 152) == 1           # exact path

@@ -23,33 +23,39 @@ pytestmark = pytest.mark.gpu
 GDR_ERR_DEVICE_TIMEOUT = -6
 
 
-@pytest.mark.parametrize("schedule", ["phased", "fused"])
+@pytest.mark.parametrize("schedule", ["phased", "fused", "fused_packed"])
 @pytest.mark.parametrize("fault_chunk", [0, 2, 7])
 def test_chain_gives_up_on_a_missing_load_then_the_next_call_is_clean(schedule, fault_chunk,
                                                                      monkeypatch):
+    # (fused_packed: packed sequences, the solve claiming units and the chain CTAs of the
+    # shorter sequence solving before their chains start)
     if schedule == "phased":
         monkeypatch.setenv("GDR_PREFILL_PHASES", "1")
-    inp = inputs.prefill_inputs([512, 512], H=2, dk=128, dv=128, dtype="bf16", seed=41,
+    lens = [4000, 300] if schedule == "fused_packed" else [512, 512]
+    inp = inputs.prefill_inputs(lens, H=2, dk=128, dv=128, dtype="bf16", seed=41,
                                 s0_std=0.2, gate="slow")
     n, T = inp.num_seqs, inp.total_tokens
-    assert ops.chunk_fwd_schedule(n, T, inp.H, 128, 128, torch.bfloat16) == \
+    varlen = inp.cu_seqlens is not None
+    assert varlen == (schedule == "fused_packed")
+    assert ops.chunk_fwd_schedule(n, T, inp.H, 128, 128, torch.bfloat16, varlen=varlen) == \
         (1 if schedule == "phased" else 0)
     dev = torch.device("cuda", 0)
     d = lambda t: None if t is None else t.to(dev)
     q, k, v, la, b, S0 = d(inp.q), d(inp.k), d(inp.v), d(inp.log_alpha), d(inp.beta), d(inp.S0)
+    cu = d(inp.cu_seqlens)
     ws = torch.empty(ops.chunk_fwd_workspace_size(n, T, inp.H, 128, 128), dtype=torch.uint8,
                      device=dev)
 
     monkeypatch.setenv("GDR_DEBUG_CHAIN_FAULT", str(fault_chunk))
     t0 = time.perf_counter()
-    ops.chunk_fwd(q, k, v, la, b, S0=S0, num_seqs=n, workspace=ws)
+    ops.chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, num_seqs=n, workspace=ws)
     status = ops.read_device_status(ws)  # synchronises
     elapsed = time.perf_counter() - t0
     assert status == GDR_ERR_DEVICE_TIMEOUT, ops.status_string(status)
     assert elapsed < 10.0
 
     monkeypatch.delenv("GDR_DEBUG_CHAIN_FAULT")
-    o, S = chunk_fwd(q, k, v, la, b, S0=S0, num_seqs=n, workspace=ws)
+    o, S = chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, num_seqs=n, workspace=ws)
     assert ops.read_device_status(ws) == 0
     ref_o, ref_S = oracle_prefill(inp)
     assert rel_err(f64(o), ref_o) <= TOL["bf16"]

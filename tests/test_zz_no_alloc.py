@@ -7,9 +7,11 @@ inside the library instead. These tests call it through the C ABI and check it
 against gdr_chunk_fwd (with a torch-allocated workspace) and against the float64
 oracle, each case twice in a row: the second call finds the first call's
 contents in the shared array and must still be right. The cases cover the
-schedules that keep per-call state in the array: the phased one (packed
-sequences), the fused one (equal lengths: per-unit ready flags) and the
-segmented one (few long chains: segment state sets). The device status word
+schedules that keep per-call state in the array: the fused one over packed
+sequences (a claim counter, the claim order and per-unit ready flags), the
+phased one (forced, packed sequences), the fused one over equal lengths
+(per-unit ready flags) and the segmented one (few long chains: segment state
+sets). The device status word
 is read back through gdr_noalloc_read_device_status. The file is collected
 last, so that a run stopping at the first failure has run every other test.
 """
@@ -63,9 +65,13 @@ def run_noalloc(fn, dev, q, k, v, la, b, S0, cu, num_seqs, inp):
 
 
 CASES = {
-    # packed sequences: the phased schedule (bf16) and the exact path (fp32)
-    "packed_bf16": lambda: inputs.prefill_inputs([150, 77], H=2, dk=128, dv=128, dtype="bf16",
+    # packed sequences: the fused schedule with the solve claiming units (bf16), the
+    # phased schedule (bf16, forced below) and the exact path (fp32)
+    "packed_bf16": lambda: inputs.prefill_inputs([150, 4000], H=2, dk=128, dv=128, dtype="bf16",
                                                  seed=31, s0_std=0.2, gate="slow"),
+    "packed_bf16_phased": lambda: inputs.prefill_inputs([150, 77], H=2, dk=128, dv=128,
+                                                        dtype="bf16", seed=35, s0_std=0.2,
+                                                        gate="slow"),
     "packed_f32": lambda: inputs.prefill_inputs([64, 3, 200], H=3, dk=64, dv=96, dtype="f32",
                                                 seed=32, s0_std=0.5, gate="slow"),
     # equal lengths, no cu_seqlens: the fused cooperative schedule
@@ -81,6 +87,8 @@ CASES = {
 def test_noalloc_matches_chunk_fwd_and_the_oracle_on_two_calls_in_a_row(case, monkeypatch):
     if case == "segmented_bf16":
         monkeypatch.setenv("GDR_PREFILL_SEGMENTS", "4")
+    if case == "packed_bf16_phased":
+        monkeypatch.setenv("GDR_PREFILL_PHASES", "2")
     dev = torch.device("cuda", 0)
     fn = noalloc_fn()
     inp = CASES[case]()
@@ -92,8 +100,10 @@ def test_noalloc_matches_chunk_fwd_and_the_oracle_on_two_calls_in_a_row(case, mo
     if inp.dtype == "bf16":
         sched = ops.chunk_fwd_schedule(n, inp.total_tokens, inp.H, inp.dk, inp.dv,
                                        torch.bfloat16, varlen=varlen)
-        if case == "fused_bf16":
+        if case in ("fused_bf16", "packed_bf16"):
             assert sched == 0
+        elif case == "packed_bf16_phased":
+            assert sched == 2
         elif case == "segmented_bf16":
             assert sched == ops.SCHEDULE_SEGMENTED + 4
     d = lambda t: None if t is None else t.to(dev)
