@@ -7,7 +7,13 @@
 //    CTAs that take the units in chunk-major order; a chain CTA waits (bounded) on each
 //    unit's flag before loading its results. Cooperative launch guarantees that all the
 //    CTAs are resident together, so the waits always end. Used for batches of equal
-//    lengths whose chains leave enough SMs free.
+//    lengths whose chains leave enough SMs free. For packed sequences of different
+//    lengths the solve CTAs claim units from a counter in the order the planning kernel
+//    lists (each chain's chunks by the step at which it needs them, when all chains end
+//    together), and a chain CTA solves too until the claims reach its sequence's
+//    trigger; only then does it start its chain. No solving CTA waits on a chain, so
+//    every claimed unit is published. The phased pair follows that launch, and the plan
+//    hands the call to one of the two.
 //  * phased: separate solve and chain kernels over phases of the chunks (below).
 //  * segmented: for a few long chains, which leave most SMs idle under the other two.
 //    The state after a run of chunks is affine in the state before it, S_end = P S + R,

@@ -369,7 +369,10 @@ int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H,
  * Schedule of an uncaptured gdr_chunk_fwd call with these sizes on the current
  * device, for diagnostics and benchmarks: 0 for the fused schedule of the
  * tensor-core path (the planning kernel, then one cooperative kernel that runs
- * the chains beside the solve); 1 .. 8, the number of phases of the phased
+ * the chains beside the solve; with varlen, the solve kernel and the chain kernel
+ * of one phase follow it, and the planning kernel, which sees the lengths, hands
+ * the call to either the cooperative kernel or that pair, the other returning at
+ * once); 1 .. 8, the number of phases of the phased
  * schedule (the exact path is one phase); or GDR_SCHEDULE_SEGMENTED + n for
  * the segmented schedule of few long chains, each sequence cut into n (2 .. 8)
  * segments whose state transitions are summarised and chained by a scan
