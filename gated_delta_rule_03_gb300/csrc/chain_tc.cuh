@@ -372,7 +372,9 @@ __device__ __forceinline__ void chain_body(const CUtensorMap &map_q, const CUten
     } else if (warp == kProducerWarp) {
         // ============================================================ producer
         if (lane == 0) {
-            const int unit0 = seq_chunk[n] * p.H + h;  // chunk c is solve unit unit0 + c * H
+            // chunk c is solve unit unit0 + c * H (equal lengths in a fused launch: closed form)
+            const int first = kFused && !p.cu_seqlens ? n * (int)m : seq_chunk[n];
+            const int unit0 = first * p.H + h;
             for (int c = 0; kPC && c < n_chunks; ++c) {
                 // per-channel operands: Utilde^T (V slot), e^{g_C - g} . K, A^T and exp(g_C)
                 // (K slot), e^g . Q and -W (Q slot); units of 64 (or 128) rows

@@ -225,8 +225,11 @@ int gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *l
     a.ws = (char *)workspace;
     a.stream = (cudaStream_t)stream;
     const int phases = L.tensor_path ? tc_schedule(a) : 1;
-    st = launch_plan(a, L, phases);
-    if (st != GDR_OK) return st;
+    // (the fused schedule over equal lengths plans itself: its plan is closed form)
+    if (!(L.tensor_path && phases == 0 && !cu_seqlens)) {
+        st = launch_plan(a, L, phases);
+        if (st != GDR_OK) return st;
+    }
     st = L.channel_tc ? launch_prefill_channel_tc(a, L)
                       : (L.tensor_path ? launch_prefill_tc(a, L, phases) : launch_prefill_exact(a, L));
     // the output step, where the chain did not fuse it (it does on the tensor-core paths
@@ -304,10 +307,11 @@ int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H,
     if (total_tokens == 0) return 1;  // the plan; the state copy is not a kernel of ours
     const int P = tc_schedule_query(num_seqs, total_tokens, H, d_v, varlen != 0);
     if (P < 0) return GDR_ERR_CUDA;
-    // fused: plan, cooperative kernel (packed sequences: then the solve and chain of one
-    // phase, which the plan may hand the call to); P phases: plan, P solves, P chains;
+    // fused: the cooperative kernel alone (equal lengths: it plans itself), or for packed
+    // sequences the plan, the cooperative kernel, then the solve and chain of one phase,
+    // which the plan may hand the call to; P phases: plan, P solves, P chains;
     // segmented: plan, solve, summary chain, scan, chain
-    return P == 0 ? (varlen ? 4 : 2) : (P > kSegmentedBase ? 5 : 1 + 2 * P);
+    return P == 0 ? (varlen ? 4 : 1) : (P > kSegmentedBase ? 5 : 1 + 2 * P);
 }
 
 int gdr_chunk_fwd_schedule(int64_t num_seqs, int64_t total_tokens, int H, int d_k, int d_v,

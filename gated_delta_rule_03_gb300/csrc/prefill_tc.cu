@@ -28,6 +28,8 @@
 #include <atomic>
 #include <mutex>
 
+#include <cooperative_groups.h>
+
 #include "chain_tc.cuh"
 #include "solve_tc.cuh"
 
@@ -65,6 +67,23 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_t,
                 const __grid_constant__ CUtensorMap map_o, const TcParams p,
                 const solve::SolveParams sp, int chain_ctas, const int32_t *trig) {
+    if (!kClaim) {
+        // Equal lengths: no planning kernel runs ahead of this launch (its plan is closed
+        // form). Every CTA clears its share of the unit flags and CTA 0 resets the control
+        // words; the grid barrier of the cooperative launch then makes them visible to all
+        // before any unit is published or waited on.
+        const int n_flags = sp.seqs * sp.seq_chunks * p.H;
+        for (int i = (int)(blockIdx.x * blockDim.x + threadIdx.x); i < n_flags; i += (int)(gridDim.x * blockDim.x))
+            sp.flags[i] = 0;
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            const int chunks = sp.seqs * sp.seq_chunks;
+            p.ctl[0] = GDR_OK;
+            p.ctl[1] = chunks;
+            p.ctl[2] = 0;
+            p.ctl[3] = chunks;
+        }
+        cooperative_groups::this_grid().sync();
+    }
     if (kClaim && p.ctl[kPairWord] == 1) return;  // the two-kernel pair after it runs the call
     if ((int)blockIdx.x < chain_ctas) {
         if (kClaim) {
@@ -478,6 +497,7 @@ static int launch_fused(const PrefillArgs &a, const WsLayout &L, const CUtensorM
     sp.phase = 0;
     sp.seqs = (int)a.num_seqs;
     sp.seq_chunks = (int)((a.total_tokens / a.num_seqs + kChunk - 1) / kChunk);
+    sp.seq_len = (int)(a.total_tokens / a.num_seqs);
     sp.flags = flags;
     sp.order = reinterpret_cast<const int4 *>(a.ws + L.order);
     sp.claim = p.ctl + kClaimWord;

@@ -256,8 +256,9 @@ struct SolveParams {
     int H;
     int phase;            // the units of this phase's chunks are solved (-1: every unit)
     // fused launch (beside the chain): units in chunk-major order over `seqs` sequences of
-    // `seq_chunks` chunks each, and a ready flag per unit, set once its results are stored
-    int seqs, seq_chunks;
+    // `seq_chunks` chunks (seq_len tokens) each, and a ready flag per unit, set once its
+    // results are stored; the plan of such a call is closed-form and not read
+    int seqs, seq_chunks, seq_len;
     int32_t *flags;
     // fused launch over packed sequences: the units are claimed one at a time from a
     // counter shared by the grid, in the order of the plan's claim rows (row r: chunk
@@ -301,6 +302,12 @@ struct GroupSolver {
     // the plan entry of unit x (any x >= n_units: none); every lane of the caller loads it
     __device__ __forceinline__ int4 plan_of(int x) const {
         if (kClaim) return x < n_units ? p.order[x / p.H] : make_int4(0, 0, 0, 0);
+        if (kFused) {  // chunk c of the call is chunk c % seq_chunks of sequence c / seq_chunks
+            if (x >= n_units) return make_int4(0, 0, 0, 0);
+            const int c = unit_at(x) / p.H, n = c / p.seq_chunks, j = c % p.seq_chunks;
+            const int rem = p.seq_len - j * C;
+            return make_int4(n, n * p.seq_len + j * C, rem < C ? rem : C, j);
+        }
         return x < n_units ? p.plan[unit_at(x) / p.H] : make_int4(0, 0, 0, 0);
     }
     // kClaim: warp 0 claims the next unit (lane 0's atomic; the index is read later, so

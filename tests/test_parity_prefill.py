@@ -196,7 +196,7 @@ def test_fused_schedule_matches_phased(S, T, H, dv, monkeypatch):
     assert inp.cu_seqlens is None
     monkeypatch.delenv("GDR_PREFILL_PHASES", raising=False)
     assert ops.chunk_fwd_schedule(S, S * T, H, 128, dv, torch.bfloat16) == 0
-    assert ops.chunk_fwd_kernel_launches(S, S * T, H, 128, dv, torch.bfloat16) == 2
+    assert ops.chunk_fwd_kernel_launches(S, S * T, H, 128, dv, torch.bfloat16) == 1
     o_f, S_f = gpu_prefill(inp)
     monkeypatch.setenv("GDR_PREFILL_PHASES", "1")
     o_p, S_p = gpu_prefill(inp)
