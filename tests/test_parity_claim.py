@@ -172,3 +172,37 @@ def test_bad_cu_seqlens_under_the_claimed_solve():
     assert ops.read_device_status(ws) == 0
     o_ref, S_ref = oracle_prefill(inp)
     assert rel_err(f64(o), o_ref) <= TOL["bf16"] and rel_err(f64(S), S_ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_fused_schedules_inside_graph_capture(packed, monkeypatch):
+    # both forms of the fused schedule are stream-ordered launches on the caller's stream
+    # (the equal-length one a single cooperative kernel that plans itself): a captured call
+    # replays to the eager bits, twice in a row on one workspace
+    monkeypatch.delenv("GDR_PREFILL_PHASES", raising=False)
+    lens = [900, 77, 6000] if packed else [2048, 2048]
+    inp = inputs.prefill_inputs(lens, H=4, dk=128, dv=128, dtype="bf16", seed=410 + packed,
+                                s0_std=0.2, gate="slow")
+    assert (inp.cu_seqlens is not None) == packed
+    n, T = inp.num_seqs, inp.total_tokens
+    assert ops.chunk_fwd_schedule(n, T, 4, 128, 128, torch.bfloat16, varlen=packed) == 0
+    d = lambda t: None if t is None else t.cuda()
+    q, k, v, la, b, S0, cu = map(d, (inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0,
+                                     inp.cu_seqlens))
+    ws = torch.empty(ops.chunk_fwd_workspace_size(n, T, 4, 128, 128), dtype=torch.uint8,
+                     device="cuda")
+    o_e, S_e = chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, num_seqs=n, workspace=ws)
+    torch.cuda.synchronize()
+    o, S = torch.full_like(o_e, float("nan")), torch.full_like(S_e, float("nan"))
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ops.chunk_fwd(q, k, v, la, b, S0=S0, cu_seqlens=cu, num_seqs=n, o=o, S_final=S,
+                      workspace=ws, stream=s)
+    for _ in range(2):
+        o.fill_(float("nan"))
+        S.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_e) and torch.equal(S, S_e)
+    assert ops.read_device_status(ws) == 0
