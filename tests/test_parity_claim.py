@@ -206,3 +206,42 @@ def test_fused_schedules_inside_graph_capture(packed, monkeypatch):
         torch.cuda.synchronize()
         assert torch.equal(o, o_e) and torch.equal(S, S_e)
     assert ops.read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_claimed_solve_seeded_sweep(seed, monkeypatch):
+    # seeded packed batches the claiming form takes (32 chunks or more per sequence on
+    # average, 40 to 136 chains: fewer long chains take the segmented schedule): lengths
+    # from 0 to 9000 tokens, 3-8 sequences, one or two value slices, an initial state or
+    # none, the additive rule at random; bit-equal to the phased schedule and within 2e-2
+    # of the oracle (head 0)
+    rng = np.random.default_rng(900 + seed)
+    n = int(rng.integers(3, 9))
+    lens = [int(x) for x in rng.integers(0, 9001, size=n)]
+    lens[int(rng.integers(0, n))] = max(lens) + 2048  # at least one long sequence
+    dv = 256 if rng.random() < 0.3 else 128
+    per = n * (dv // 128)
+    H = int(rng.integers(-(-40 // per), 136 // per + 1))
+    inp = inputs.prefill_inputs(lens, H=H, dk=128, dv=dv, dtype="bf16", seed=1000 + seed,
+                                s0_std=0.3 if rng.random() < 0.6 else 0.0,
+                                gate="slow" if rng.random() < 0.5 else "default", packed=True)
+    if sum(lens) < 32 * 64 * n:
+        pytest.skip("too short on average for the claiming form")
+    kw = dict(rule="additive") if rng.random() < 0.25 else {}
+    monkeypatch.delenv("GDR_PREFILL_PHASES", raising=False)
+    assert ops.chunk_fwd_schedule(n, inp.total_tokens, H, 128, dv, torch.bfloat16,
+                                  varlen=True) == 0
+    o_c, S_c = call(inp, **kw)
+    monkeypatch.setenv("GDR_PREFILL_PHASES", "1")
+    o_p, S_p = call(inp, **kw)
+    assert torch.equal(o_c, o_p) and torch.equal(S_c, S_p)
+    import oracle
+    h0 = lambda t: f64(t[:, :1])  # head 0 only
+    cu = inp.cu_seqlens.numpy().astype(np.int64)
+    o_ref, S_ref = oracle.forward(h0(inp.q), h0(inp.k), h0(inp.v), h0(inp.log_alpha),
+                                  h0(inp.beta), S0=None if inp.S0 is None else h0(inp.S0),
+                                  cu_seqlens=cu, additive=bool(kw))
+    o_g, S_g = h0(o_c), h0(S_c)
+    assert np.isfinite(o_g).all() and np.isfinite(S_g).all()
+    assert rel_err(o_g, o_ref) <= TOL["bf16"], rel_err(o_g, o_ref)
+    assert rel_err(S_g, S_ref) <= TOL["bf16"], rel_err(S_g, S_ref)
