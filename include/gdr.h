@@ -336,8 +336,9 @@ int gdr_noalloc_read_device_status(int *status, gdr_stream_t stream);
  * Which kernel path gdr_chunk_fwd takes for these sizes, for diagnostics and
  * benchmarks (host-only, no CUDA call): GDR_PATH_EXACT (plain fp32 arithmetic:
  * a planning kernel, a per-chunk kernel and a per-sequence chain kernel) or
- * GDR_PATH_TENSOR (bf16 tensor cores: a planning kernel, then per phase a
- * chunk-parallel solve kernel and a per-sequence chain kernel).
+ * GDR_PATH_TENSOR (bf16 tensor cores: a chunk-parallel solve and per-sequence
+ * chains, as one cooperative kernel or as separate kernels after a planning
+ * kernel; see gdr_chunk_fwd_schedule).
  * Returns a negative status for unsupported sizes.
  */
 enum { GDR_PATH_EXACT = 0, GDR_PATH_TENSOR = 1, GDR_PATH_CHANNEL_TENSOR = 2 };
@@ -368,10 +369,11 @@ int gdr_chunk_fwd_kernel_launches(int64_t num_seqs, int64_t total_tokens, int H,
 /*
  * Schedule of an uncaptured gdr_chunk_fwd call with these sizes on the current
  * device, for diagnostics and benchmarks: 0 for the fused schedule of the
- * tensor-core path (the planning kernel, then one cooperative kernel that runs
- * the chains beside the solve; with varlen, the solve kernel and the chain kernel
- * of one phase follow it, and the planning kernel, which sees the lengths, hands
- * the call to either the cooperative kernel or that pair, the other returning at
+ * tensor-core path (one cooperative kernel that runs the chains beside the solve;
+ * over equal lengths it is the call's only kernel, its plan being closed form;
+ * with varlen a planning kernel runs first, the solve kernel and the chain kernel
+ * of one phase follow, and the planning kernel, which sees the lengths, hands the
+ * call to either the cooperative kernel or that pair, the other returning at
  * once); 1 .. 8, the number of phases of the phased
  * schedule (the exact path is one phase); or GDR_SCHEDULE_SEGMENTED + n for
  * the segmented schedule of few long chains, each sequence cut into n (2 .. 8)
